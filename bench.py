@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the copy-on-write tree KV cache hot path on GB300.
+
+Workload (default): Llama-3-8B-shaped attention layer (32 Q heads, 8 KV heads,
+head_dim 128, bf16, block_size 16); 8 independent requests with a 4096-token
+shared prefix, forked 4 ways, each branch 256 divergent tokens, one decode
+query per branch.  The prefixes are prefilled once before timing (resident in
+HBM).  One step is one pass of the whole path over that batch:
+
+    fork (8 parents x 4 children, batched)  ->  copy-on-write append of the
+    256 divergent tokens of all 32 branches  ->  tree decode attention (plan,
+    shared-prefix + leaf partials, log-sum-exp merge)  ->  free of the 32 branches
+
+`value` is branch-queries per second of step time (32 queries per step per
+GPU; all ranks summed).  The roofline entry covers the dominant kernel, the
+attention partial kernel: unique KV bytes (each shared block counted once)
+plus Q read and partial/out bytes excluded, over its CUDA-event duration.
+
+`--impl reference` times the fp64 CPU oracle (single thread) on a bounded
+sample of the same workload: the tree attention of the 4 branches of one
+request per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (a timing reduction, not a data-path
+    collective)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workload
+def beam_workload(seed: int):
+    from copy_write_forked_gb300 import workloads as W
+    return W.beam(requests=8, prefix=4096, width=4, divergent=256, seed=seed)
+
+
+def config_of(w):
+    m = w.meta
+    return {"workload": "beam-like 4-way fork, Llama-3-8B attention layer", "name": w.name,
+            "requests": m["requests"], "prefix_tokens": m["prefix"], "fork_width": m["width"],
+            "divergent_tokens": m["divergent"], "branch_queries_per_step": len(w.query),
+            "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "l2": "flushed between steps (256 MiB write)",
+            "step": "fork + CoW append + tree decode attention + free"}
+
+
+# ---------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__ as g
+    g.build()
+    from copy_write_forked_gb300.dendrite import Pool
+    from copy_write_forked_gb300 import workloads as W
+
+    w = beam_workload(seed=rank)
+    R, P, Wd, Dv = (w.meta[k] for k in ("requests", "prefix", "width", "divergent"))
+    nq, nkv, d = w.n_q_heads, w.n_kv_heads, w.head_dim
+    bs = w.block_size
+    nblocks = R * (P // bs + 1) + R * Wd * (Dv // bs + 2) + 64
+    pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R * (Wd + 1) + 8,
+                max_blocks_per_branch=(P + Dv) // bs + 8)
+    # prefill (untimed): the 8 prefixes, resident in HBM
+    roots = [pool.new_branch() for _ in range(R)]
+    prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
+    Kp, Vp = w.kv(prefill_idx, dev)
+    pool.append_kv(roots, Kp, Vp)
+    del Kp, Vp
+    div_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == Dv)
+    Kd, Vd = w.kv(div_idx, dev)            # divergent tokens of the 32 branches, resident
+    Q = w.q(dev)
+    out = torch.empty_like(Q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    pool.set_profiling(True)
+    pool.sync()
+
+    def step():
+        kids = pool.fork_batch(roots, [Wd] * R)
+        br = [c for ks in kids for c in ks]
+        pool.append_kv(br, Kd, Vd)
+        pool.tree_attn_decode(Q, br, out=out)
+        pool.free(br)
+        return br
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    pool.sync()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
+                            "attn_total")}
+    plan_us = []
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(1)
+            ev[i][0].record(stream)
+            br = step()
+            ev[i][1].record(stream)
+            st = pool.last_plan_stats()
+            plan_us.append(st["plan_us"])
+            tm = pool.last_timings()
+            for k in kern:
+                if tm.get(k) is not None:
+                    kern[k].append(tm[k])
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    pool.sync()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    ms = max_over_ranks(ms, world, dev)
+    n_queries = len(w.query)
+    value = world * n_queries / (ms / 1e3)
+
+    # roofline of the attention partial kernel
+    unique_kv = w.unique_kv_bytes()
+    q_bytes = Q.numel() * Q.element_size()
+    attn_ms = statistics.mean(kern["attn_partial"])
+    achieved = (unique_kv + q_bytes) / (attn_ms / 1e3) / 1e9
+    peak, peak_src = read_peaks()
+    plan = pool.last_plan_stats()
+
+    # ----- e2e through the public API with host buffers (pinned), H2D + D2H inside
+    Kh, Vh, Qh = Kd.cpu().pin_memory(), Vd.cpu().pin_memory(), Q.cpu().pin_memory()
+    outh = torch.empty(Q.shape, dtype=Q.dtype).pin_memory()
+    Kd2, Vd2, Q2 = torch.empty_like(Kd), torch.empty_like(Vd), torch.empty_like(Q)
+
+    def e2e_step():
+        Kd2.copy_(Kh, non_blocking=True)
+        Vd2.copy_(Vh, non_blocking=True)
+        Q2.copy_(Qh, non_blocking=True)
+        kids = pool.fork_batch(roots, [Wd] * R)
+        br = [c for ks in kids for c in ks]
+        pool.append_kv(br, Kd2, Vd2)
+        pool.tree_attn_decode(Q2, br, out=out)
+        outh.copy_(out, non_blocking=True)
+        pool.free(br)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(statistics.mean(e2e_ms), world, dev)
+    h2d = (Kh.numel() + Vh.numel() + Qh.numel()) * 2
+    d2h = outh.numel() * 2
+
+    # ----- fork latency at depth 500 blocks (tail half full), 1 and 4 children
+    fork = fork_latency(dev) if rank == 0 else {}
+    pool.sync()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    gpu_launches = 7 * args.steps   # fork 1 + append 2 + attention 2 + free 2 per step
+    line = {
+        "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
+        "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
+        "config": dict(config_of(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes": unique_kv + q_bytes, "kernel_ms": attn_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * n_queries / (e2e / 1e3), "unit": "branch-queries/s", "ms_per_step": e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "kernels_ms": {k: (statistics.mean(v) if v else None) for k, v in kern.items()},
+        "attn_branch_queries_per_s": n_queries / (statistics.mean(kern["attn_total"]) / 1e3),
+        "plan": {"segments": plan["n_segments"], "units": plan["n_units"], "ctas": plan["n_ctas"],
+                 "partials": plan["n_partials"], "tiles": plan["tiles"], "unique_tiles": plan["unique_tiles"],
+                 "host_plan_us_mean": statistics.mean(plan_us)},
+        "fork_us": fork,
+        "wall_s": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    pool.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def fork_latency(dev, reps=200):
+    """Batched fork of a chain of `depth` blocks with a half-full tail:
+    device time of the fork kernel and host time of the API call."""
+    import torch
+    from copy_write_forked_gb300.dendrite import Pool
+    res = {}
+    for depth in (1, 10, 50, 100, 500):
+        L = depth * 16 - 8
+        pool = Pool(depth + 64, 16, 8, 128, torch.bfloat16, max_branches=16, max_blocks_per_branch=depth + 4)
+        r = pool.new_branch()
+        K = torch.zeros(1, L, 8, 128, dtype=torch.bfloat16, device=dev)
+        pool.append_kv([r], K, K)
+        pool.set_profiling(True)
+        pool.sync()
+        for nc in (1, 4):
+            gpu, host = [], []
+            for i in range(reps):
+                t0 = time.perf_counter()
+                kids = pool.fork(r, nc)
+                host.append((time.perf_counter() - t0) * 1e6)
+                gpu.append(pool.last_timings()["fork"] * 1e3)
+                pool.free(kids)
+            res[f"depth{depth}_children{nc}"] = {"gpu_us_median": statistics.median(gpu[10:]),
+                                                  "host_call_us_median": statistics.median(host[10:])}
+        pool.close()
+    return res
+
+
+# ------------------------------------------------------------ oracle arm
+def _oracle_sample(seconds: float):
+    """Runs in a fresh single-threaded process: the oracle's tree attention on
+    branches of the beam workload until `seconds` of CPU work are spent."""
+    import torch
+    torch.set_num_threads(1)
+    from copy_write_forked_gb300 import workloads as W
+    from oracle import KVTree
+    w = beam_workload(seed=0)
+    ids = list(w.query[:4])                 # the 4 branches of request 0
+    tree = _oracle_request_tree(w, 0)
+    Q = [w.q_one(i) for i in range(4)]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        tree.attend(ids[n % 4], Q[n % 4])
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return n, dt
+
+
+def _oracle_request_tree(w, req):
+    from oracle import KVTree
+    pre = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == w.meta["prefix"])
+    div = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == w.meta["divergent"])
+    width = w.meta["width"]
+    tree = KVTree(w.n_kv_heads, w.head_dim)
+    tree.new_root(req)
+    k, v = w.kv_one(pre, req)
+    tree.append(req, k, v)
+    kids = [w.query[req * width + j] for j in range(width)]
+    tree.fork(req, kids)
+    for j, c in enumerate(kids):
+        k, v = w.kv_one(div, req * width + j)
+        tree.append(c, k, v)
+    return tree
+
+
+def cpu_baseline(seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; n, dt = bench._oracle_sample(%f); "
+            "print(json.dumps([n, dt]))" % (ROOT, seconds))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr[-300:]}
+    n, dt = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": n / dt, "unit": "branch-queries/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} branch queries (fp64 tree attention, 4352-token branches of request 0 of the "
+                      f"beam workload) in {dt:.1f} s, single thread"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    torch.set_num_threads(1)
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    from copy_write_forked_gb300 import workloads as W
+    w = beam_workload(seed=0)
+    tree = _oracle_request_tree(w, 0)
+    ids = list(w.query[:4])
+    Q = [w.q_one(i) for i in range(4)]
+
+    def step():
+        for j in range(4):
+            tree.attend(ids[j], Q[j])
+
+    for _ in range(args.warmup):
+        step()
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        t.append(time.perf_counter() - t0)
+    ms = statistics.mean(t) * 1e3
+    value = 4 / (ms / 1e3)
+    line = {"impl": "reference",
+            "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
+            "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
+            "config": dict(config_of(w), parallelism="single thread"),
+            "cpu_baseline": {"value": value, "unit": "branch-queries/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step: fp64 tree attention of the 4 branches of request 0"},
+            "e2e": {"value": value, "unit": "branch-queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # the oracle runs single-threaded: pin BLAS/OpenMP pools before numpy loads
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,945 @@
+// Tree-aware split-KV decode attention over the copy-on-write block pool.
+//
+// Method (Dendrite article, ainews.cool, section 技术深度解析): attention walks
+// the cache tree and gathers keys and values from the shared ancestor path and
+// from the branch's own leaf path; the shared prefix is stored once.  Here the
+// tree is cut into segments (block ranges read by a fixed set of queried
+// branches, see planner.cpp).  Every segment is streamed from HBM once for all
+// of its query rows (branches x q_len x GQA group), producing partial
+// (max, sum, acc) triples per row; a log-sum-exp merge combines the partials
+// of each output row:
+//     M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  out = sum_i acc_i 2^(m_i - M) / L
+// (scores are kept in base-2 units: s * log2(e) / sqrt(head_dim)).
+//
+// Work decomposition: a unit is (segment, kv head, group of <= 64 rows); its
+// tiles are (block, kv head) pairs of 16 tokens x head_dim.  All tiles of all
+// units form one list that is split evenly (by tiles x row tiles) over a
+// persistent grid; a CTA that crosses a unit boundary writes one partial per
+// unit it touched.
+//
+// bf16 kernel (head_dim 128): 4 consumer warps + 1 producer warp.  The
+// producer streams K and V tiles with TMA (cp.async.bulk.tensor, 128-byte
+// swizzle) into a 3-stage mbarrier ring; a stage holds up to 4 tiles of one
+// unit.  Each consumer warp owns one 16-row query tile and one tile position
+// within the stage: for units with 1, 2 or 4 row tiles a stage carries 4, 2 or
+// 1 tiles.  S = Q K^T and O += P V run on tensor cores (mma.sync m16n8k16,
+// bf16 in, fp32 accumulate) with an online softmax in registers.  Warps that
+// worked on the same rows combine their states through shared memory at the
+// end of a unit.
+//
+// Every mbarrier wait is bounded (about 2 s of %globaltimer): on expiry the
+// kernel records DENDRITE_ETIMEOUT in the pool status, skips the rest of its
+// work (keeping the same barrier sequence) and waits, again bounded, for its
+// own copies still in flight before it exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "dendrite_internal.h"
+
+using namespace dendrite;
+
+namespace {
+
+constexpr int D = 128;
+constexpr int BS = 16;
+constexpr int NSTAGE = 3;
+constexpr int HALF_BYTES = BS * 64 * 2;          // one 64-column half of a K or V tile
+constexpr int SLOT_BYTES = 4 * HALF_BYTES;       // K (2 halves) + V (2 halves) of one tile
+constexpr int STAGE_BYTES = 4 * SLOT_BYTES;
+constexpr int NCONS = 4;
+constexpr int THREADS = (NCONS + 1) * 32;
+constexpr int ML_BYTES = NCONS * 16 * 2 * 4;
+constexpr size_t SMEM_BF16 = 1024 + (size_t)NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8 + ML_BYTES;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+struct AttnArgs {
+    AttnPlanDev plan;
+    const void* Q;
+    const int32_t* table;
+    const float* pool_k;   // fp32 kernel only
+    const float* pool_v;
+    float* part_acc;       // [partial rows][head_dim]
+    float2* part_ml;       // [partial rows] (m, l)
+    DevMeta* meta;
+    int32_t bpb;
+    int32_t n_kv;
+    int32_t head_dim;
+    int32_t n_blocks;
+    float scale_log2;      // log2(e) / sqrt(head_dim)
+};
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: true when the phase with `parity` completed; false on
+// timeout or when another role of the CTA already gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+        }
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Byte offset of element (token t, column d) inside one swizzled K or V tile:
+// two 64-column halves of 16 rows x 128 bytes, 16-byte chunks XOR-ed with
+// (row & 7) as TMA's 128-byte swizzle lays them out.
+__device__ __forceinline__ uint32_t swz(int t, int d) {
+    return (uint32_t)((d >> 6) * HALF_BYTES + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4) + (d & 7) * 2);
+}
+
+// Walks a CTA's share of the tile list: calls f(unit, unit_index, first
+// tile, tile count, P, is_last_stage_of_chunk) for every stage.
+struct Sched {
+    int32_t t, tend, u;
+};
+
+// ============================================================ bf16 kernel
+__global__ void __launch_bounds__(THREADS, 2)
+k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const AttnArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* sm = smem_raw + (base - raw);
+    const uint32_t bar_full = base + NSTAGE * STAGE_BYTES;
+    const uint32_t bar_empty = bar_full + NSTAGE * 8;
+    float* ml = reinterpret_cast<float*>(sm + NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, NCONS);
+        }
+        abort_flag = a.meta->status != 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (abort_flag) return;
+
+    const AttnPlanDev& pl = a.plan;
+    const int c = blockIdx.x;
+    const int32_t t_begin = pl.cta_begin[c], t_end = pl.cta_begin[c + 1];
+    int32_t u0 = pl.cta_unit[c];
+    volatile int* abortp = &abort_flag;
+
+    if (warp == NCONS) {
+        // ------------------------------------------------------ producer
+        uint32_t issued = 0, parity_bits = 0;
+        int32_t stage = 0;
+        int32_t t = t_begin, u = u0;
+        while (t < t_end) {
+            const AttnUnit U = pl.units[u];
+            const int32_t uend = U.tile_off + U.n_blk;
+            if (t >= uend) { ++u; continue; }
+            const int32_t cend = min(t_end, uend);
+            const int P = 4 / U.rt;
+            const int32_t* trow = a.table + (int64_t)U.table_row * a.bpb + U.blk_start - U.tile_off;
+            for (int32_t st = t; st < cend; st += P, ++stage) {
+                const int slot = stage % NSTAGE;
+                const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
+                const int ntiles = min(P, cend - st);
+                bool ok = true;
+                if (lane == 0 && !*abortp) {
+                    ok = mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abortp);
+                    if (!ok) {
+                        *abortp = 1;
+                        atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && !*abortp;
+                if (!ok) continue;
+                if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
+                __syncwarp();
+                if (lane < ntiles) {
+                    int32_t blk = trow[st + lane];
+                    if ((uint32_t)blk >= (uint32_t)a.n_blocks) {   // broken table: poison, read zeros
+                        atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
+                        blk = -1;
+                    }
+                    const int32_t row0 = (blk * a.n_kv + U.kv_head) * BS;
+                    const uint32_t dst = base + slot * STAGE_BYTES + lane * SLOT_BYTES;
+                    const uint32_t fb = bar_full + 8 * slot;
+                    tma_load_3d(dst, &tmK, 0, 0, row0, fb);
+                    tma_load_3d(dst + HALF_BYTES, &tmK, 0, 1, row0, fb);
+                    tma_load_3d(dst + 2 * HALF_BYTES, &tmV, 0, 0, row0, fb);
+                    tma_load_3d(dst + 3 * HALF_BYTES, &tmV, 0, 1, row0, fb);
+                }
+                issued |= 1u << slot;
+                parity_bits = (parity_bits & ~(1u << slot)) | (ph << slot);
+            }
+            t = cend;
+            ++u;
+        }
+        // after a timeout, wait (bounded) for this CTA's copies still in flight
+        if (lane == 0 && *abortp) {
+            for (int s = 0; s < NSTAGE; ++s) {
+                if (!(issued >> s & 1u)) continue;
+                const uint32_t fb = bar_full + 8 * s, ph = parity_bits >> s & 1u;
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(fb, ph) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const float NEG_INF = -INFINITY;
+    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
+    int32_t stage = 0;
+    int32_t t = t_begin, u = u0;
+    while (t < t_end) {
+        const AttnUnit U = pl.units[u];
+        const int32_t uend = U.tile_off + U.n_blk;
+        if (t >= uend) { ++u; continue; }
+        const int32_t cend = min(t_end, uend);
+        const int P = 4 / U.rt;
+        const int r = warp / P, pidx = warp % P;
+        const bool has_rows = r < U.rt;
+
+        // query fragments of rows r*16 + lane/4 (+8), and their visibility limits
+        uint32_t qa[8][4];
+        int32_t lim0 = 0, lim1 = 0;
+        {
+            const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
+            const bool v0 = has_rows && row0 < U.n_rows, v1 = has_rows && row1 < U.n_rows;
+            const AttnRow R0 = v0 ? pl.rows[U.row_off + row0] : AttnRow{0, 0};
+            const AttnRow R1 = v1 ? pl.rows[U.row_off + row1] : AttnRow{0, 0};
+            lim0 = R0.limit;
+            lim1 = R1.limit;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R0.q_row * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R1.q_row * D);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int w = ks * 8 + (lane & 3);   // 32-bit word index of column ks*16 + 2*(lane&3)
+                qa[ks][0] = v0 ? q0[w] : 0u;
+                qa[ks][1] = v1 ? q1[w] : 0u;
+                qa[ks][2] = v0 ? q0[w + 4] : 0u;
+                qa[ks][3] = v1 ? q1[w + 4] : 0u;
+            }
+        }
+        float o[16][4];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+        for (int32_t st = t; st < cend; st += P, ++stage) {
+            const int slot = stage % NSTAGE;
+            const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
+            const int ntiles = min(P, cend - st);
+            const bool last = st + P >= cend;
+            bool ok = !*abortp;
+            if (ok) {
+                ok = mbar_wait(bar_full + 8 * slot, ph, abortp);
+                if (!ok) {
+                    *abortp = 1;
+                    atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok) && !*abortp;
+            if (ok && has_rows && pidx < ntiles) {
+                const uint32_t kt = base + slot * STAGE_BYTES + pidx * SLOT_BYTES;
+                const uint32_t vt = kt + 2 * HALF_BYTES;
+                // S = Q K^T (16 rows x 16 tokens)
+                float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    const int mi = lane >> 3;
+                    const int tok = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kt + swz(tok, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+                        mma16816(s[0], qa[ks], b0, b1);
+                        mma16816(s[1], qa[ks], b2, b3);
+                    }
+                }
+                // scale, mask by per-row visibility, online softmax
+                const int32_t pos0 = (U.blk_start + (st - U.tile_off) + pidx) * BS + (lane & 3) * 2;
+                float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int32_t pos = pos0 + nt * 8 + e;
+                        s[nt][e] = pos < lim0 ? s[nt][e] * a.scale_log2 : NEG_INF;
+                        s[nt][2 + e] = pos < lim1 ? s[nt][2 + e] * a.scale_log2 : NEG_INF;
+                        mx0 = fmaxf(mx0, s[nt][e]);
+                        mx1 = fmaxf(mx1, s[nt][2 + e]);
+                    }
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                const float u0s = n0 == NEG_INF ? 0.f : n0, u1s = n1 == NEG_INF ? 0.f : n1;
+                const float al0 = exp2f(m0 - u0s), al1 = exp2f(m1 - u1s);
+                m0 = n0;
+                m1 = n1;
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        s[nt][e] = exp2f(s[nt][e] - u0s);
+                        s[nt][2 + e] = exp2f(s[nt][2 + e] - u1s);
+                        ps0 += s[nt][e];
+                        ps1 += s[nt][2 + e];
+                    }
+                }
+                l0 = l0 * al0 + ps0;
+                l1 = l1 * al1 + ps1;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= al0;
+                    o[n][1] *= al0;
+                    o[n][2] *= al1;
+                    o[n][3] *= al1;
+                }
+                // O += P V
+                uint32_t pa[4];
+                pa[0] = pack_bf16(s[0][0], s[0][1]);
+                pa[1] = pack_bf16(s[0][2], s[0][3]);
+                pa[2] = pack_bf16(s[1][0], s[1][1]);
+                pa[3] = pack_bf16(s[1][2], s[1][3]);
+                {
+                    const int mi = lane >> 3;
+                    const int tok = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                    for (int np = 0; np < 8; ++np) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vt + swz(tok, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
+                        mma16816(o[2 * np], pa, b0, b1);
+                        mma16816(o[2 * np + 1], pa, b2, b3);
+                    }
+                }
+            }
+
+            if (last) {
+                // ---------------------------------------- end of this unit's chunk
+                l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+                l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+                const int32_t prow0 = U.prow_base + (c - U.cfirst) * U.n_rows;
+                if (P == 1) {
+                    if (ok && has_rows) {
+                        const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
+                        if (row0 < U.n_rows) {
+                            float* dst = a.part_acc + (int64_t)(prow0 + row0) * D + (lane & 3) * 2;
+#pragma unroll
+                            for (int n = 0; n < 16; ++n)
+                                *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][0], o[n][1]);
+                            if ((lane & 3) == 0) a.part_ml[prow0 + row0] = make_float2(m0, l0);
+                        }
+                        if (row1 < U.n_rows) {
+                            float* dst = a.part_acc + (int64_t)(prow0 + row1) * D + (lane & 3) * 2;
+#pragma unroll
+                            for (int n = 0; n < 16; ++n)
+                                *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2], o[n][3]);
+                            if ((lane & 3) == 0) a.part_ml[prow0 + row1] = make_float2(m1, l1);
+                        }
+                    }
+                } else {
+                    // combine the P warps of each row tile through this stage's buffer
+                    consumer_sync();   // every warp is done reading the stage's K/V
+                    float* ob = reinterpret_cast<float*>(sm + slot * STAGE_BYTES) + warp * 16 * D;
+                    {
+                        const int ra = lane >> 2, rb = ra + 8;
+#pragma unroll
+                        for (int n = 0; n < 16; ++n) {
+                            const int col = n * 8 + (lane & 3) * 2;
+                            *reinterpret_cast<float2*>(ob + ra * D + (col ^ ((ra & 7) << 3))) =
+                                make_float2(o[n][0], o[n][1]);
+                            *reinterpret_cast<float2*>(ob + rb * D + (col ^ ((rb & 7) << 3))) =
+                                make_float2(o[n][2], o[n][3]);
+                        }
+                        if ((lane & 3) == 0) {
+                            ml[(warp * 16 + ra) * 2] = m0;
+                            ml[(warp * 16 + ra) * 2 + 1] = l0;
+                            ml[(warp * 16 + rb) * 2] = m1;
+                            ml[(warp * 16 + rb) * 2 + 1] = l1;
+                        }
+                    }
+                    consumer_sync();
+                    if (ok) {
+                        const float* obase = reinterpret_cast<const float*>(sm + slot * STAGE_BYTES);
+                        const int items = U.rt * 16 * (D / 4);
+                        for (int idx = threadIdx.x; idx < items; idx += NCONS * 32) {
+                            const int rr = idx / (16 * (D / 4));
+                            const int row = (idx / (D / 4)) % 16;
+                            const int d = (idx % (D / 4)) * 4;
+                            const int grow = rr * 16 + row;
+                            if (grow >= U.n_rows) continue;
+                            float M = NEG_INF;
+                            for (int p2 = 0; p2 < P; ++p2) M = fmaxf(M, ml[((rr * P + p2) * 16 + row) * 2]);
+                            const float Mu = M == NEG_INF ? 0.f : M;
+                            float L = 0.f;
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int p2 = 0; p2 < P; ++p2) {
+                                const int w2 = rr * P + p2;
+                                const float wgt = exp2f(ml[(w2 * 16 + row) * 2] - Mu);
+                                L += ml[(w2 * 16 + row) * 2 + 1] * wgt;
+                                const float4 v = *reinterpret_cast<const float4*>(
+                                    obase + (w2 * 16 + row) * D + (d ^ ((row & 7) << 3)));
+                                acc.x += v.x * wgt;
+                                acc.y += v.y * wgt;
+                                acc.z += v.z * wgt;
+                                acc.w += v.w * wgt;
+                            }
+                            *reinterpret_cast<float4*>(a.part_acc + (int64_t)(prow0 + grow) * D + d) = acc;
+                            if (d == 0) a.part_ml[prow0 + grow] = make_float2(M, L);
+                        }
+                    }
+                    fence_async_smem();
+                    consumer_sync();   // buffer free again before it is handed back to TMA
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+        t = cend;
+        ++u;
+    }
+}
+
+// ============================================================ fp32 kernel
+// CUDA-core path for fp32 pools (FFMA only, no TF32).  One warp per query
+// row (up to 4 rows per warp), one 16-token tile at a time in shared memory.
+__global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
+    extern __shared__ float fsm[];
+    const int d = a.head_dim, nj = d / 32;
+    float* Ks = fsm;
+    float* Vs = fsm + BS * d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int st0;
+    if (threadIdx.x == 0) st0 = a.meta->status;
+    __syncthreads();
+    if (st0) return;
+    const AttnPlanDev& pl = a.plan;
+    const int c = blockIdx.x;
+    int32_t t = pl.cta_begin[c];
+    const int32_t t_end = pl.cta_begin[c + 1];
+    int32_t u = pl.cta_unit[c];
+    const float* Q = static_cast<const float*>(a.Q);
+    while (t < t_end) {
+        const AttnUnit U = pl.units[u];
+        const int32_t uend = U.tile_off + U.n_blk;
+        if (t >= uend) { ++u; continue; }
+        const int32_t cend = min(t_end, uend);
+        float q[4][8], acc[4][8], m[4], l[4];
+        int32_t lim[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int row = warp + 4 * rr;
+            const bool v = row < U.n_rows;
+            const AttnRow R = v ? pl.rows[U.row_off + row] : AttnRow{0, 0};
+            lim[rr] = R.limit;
+            m[rr] = -INFINITY;
+            l[rr] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                q[rr][j] = (v && j < nj) ? Q[(int64_t)R.q_row * d + lane + 32 * j] : 0.f;
+                acc[rr][j] = 0.f;
+            }
+        }
+        for (int32_t tt = t; tt < cend; ++tt) {
+            const int32_t lb = U.blk_start + (tt - U.tile_off);
+            int32_t blk = a.table[(int64_t)U.table_row * a.bpb + lb];
+            if ((uint32_t)blk >= (uint32_t)a.n_blocks) {
+                if (threadIdx.x == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
+                blk = 0;   // read a valid block; the pool is poisoned anyway
+            }
+            const float* kg = a.pool_k + ((int64_t)blk * a.n_kv + U.kv_head) * BS * d;
+            const float* vg = a.pool_v + ((int64_t)blk * a.n_kv + U.kv_head) * BS * d;
+            __syncthreads();
+            for (int e = threadIdx.x; e < BS * d; e += blockDim.x) {
+                Ks[e] = kg[e];
+                Vs[e] = vg[e];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                if (warp + 4 * rr >= U.n_rows) continue;
+                for (int tok = 0; tok < BS; ++tok) {
+                    if (lb * BS + tok >= lim[rr]) break;
+                    float dot = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < nj) dot = fmaf(q[rr][j], Ks[tok * d + lane + 32 * j], dot);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                    const float sc = dot * a.scale_log2;
+                    const float mn = fmaxf(m[rr], sc);
+                    const float al = exp2f(m[rr] - mn);
+                    const float p = exp2f(sc - mn);
+                    l[rr] = l[rr] * al + p;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < nj) acc[rr][j] = fmaf(p, Vs[tok * d + lane + 32 * j], acc[rr][j] * al);
+                    m[rr] = mn;
+                }
+            }
+        }
+        const int32_t prow0 = U.prow_base + (c - U.cfirst) * U.n_rows;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int row = warp + 4 * rr;
+            if (row >= U.n_rows) continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < nj) a.part_acc[(int64_t)(prow0 + row) * d + lane + 32 * j] = acc[rr][j];
+            if (lane == 0) a.part_ml[prow0 + row] = make_float2(m[rr], l[rr]);
+        }
+        t = cend;
+        ++u;
+    }
+}
+
+// ============================================================ LSE merge
+// One warp per output row: M = max m_i, L = sum l_i 2^(m_i - M),
+// out = sum acc_i 2^(m_i - M) / L, written in the pool dtype.
+template <typename T>
+__global__ void k_attn_merge(const AttnArgs a, T* __restrict__ out) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (a.meta->status) return;
+    if (warp >= a.plan.n_out_rows) return;
+    const int d = a.head_dim, nj = d / 32;
+    const int32_t b = a.plan.csr_ptr[warp], e = a.plan.csr_ptr[warp + 1];
+    float M = -INFINITY;
+    for (int32_t k = b; k < e; ++k) M = fmaxf(M, a.part_ml[a.plan.csr_idx[k]].x);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float L = 0.f, acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int32_t k = b; k < e; ++k) {
+        const int32_t pr = a.plan.csr_idx[k];
+        const float2 mlv = a.part_ml[pr];
+        const float w = exp2f(mlv.x - Mu);
+        L += mlv.y * w;
+        const float* src = a.part_acc + (int64_t)pr * d;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < nj) acc[j] = fmaf(src[lane + 32 * j], w, acc[j]);
+    }
+    const float inv = 1.f / L;
+    T* dst = out + (int64_t)warp * d;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j < nj) {
+            if constexpr (sizeof(T) == 2) dst[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
+            else dst[lane + 32 * j] = acc[j] * inv;
+        }
+}
+
+// ============================================================ host planning
+struct HostPlan {
+    std::vector<AttnUnit> units;
+    std::vector<AttnRow> rows;
+    std::vector<int32_t> cta_begin, cta_unit, csr_ptr, csr_idx;
+    int64_t tiles = 0, unique_tiles = 0;
+    int32_t n_segments = 0;
+    size_t partial_rows = 0;
+};
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
+               HostPlan& hp) {
+    const int32_t G = nq / p->n_kv;
+    const int max_rows = p->dtype == DENDRITE_BF16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    const int32_t n_nodes = (int32_t)p->nodes.size();
+    std::vector<int32_t> parent(n_nodes), fork_len(n_nodes), len(n_nodes), queried(n);
+    for (int32_t i = 0; i < n_nodes; ++i) {
+        parent[i] = p->nodes[i].parent;
+        fork_len[i] = p->nodes[i].fork_len;
+        len[i] = p->nodes[i].len;
+    }
+    for (int32_t i = 0; i < n; ++i) queried[i] = p->br[branches[i]].node;
+    std::vector<Segment> segs;
+    std::vector<int32_t> members;
+    plan_segments(n_nodes, parent.data(), fork_len.data(), len.data(), p->block_size, queried.data(), n, segs,
+                  members);
+    hp.n_segments = (int32_t)segs.size();
+    int64_t tile_off = 0, weight = 0;
+    for (const Segment& sg : segs) {
+        const int32_t rows_per_head = sg.n_members * q_len * G;
+        const int32_t rep = p->nodes[sg.rep_node].handle;
+        hp.unique_tiles += (int64_t)sg.block_count * p->n_kv;
+        for (int32_t h = 0; h < p->n_kv; ++h) {
+            for (int32_t g0 = 0; g0 < rows_per_head; g0 += max_rows) {
+                const int32_t nr = std::min(max_rows, rows_per_head - g0);
+                AttnUnit U{};
+                U.table_row = rep;
+                U.blk_start = sg.block_start;
+                U.n_blk = sg.block_count;
+                U.kv_head = h;
+                U.row_off = (int32_t)hp.rows.size();
+                U.n_rows = nr;
+                U.rt = nr <= 16 ? 1 : nr <= 32 ? 2 : 4;
+                U.tile_off = (int32_t)tile_off;
+                for (int32_t r = g0; r < g0 + nr; ++r) {
+                    const int32_t mi = r / (q_len * G), j = (r / G) % q_len, g = r % G;
+                    const int32_t qi = members[sg.member_offset + mi];
+                    const int32_t L = p->br[branches[qi]].len;
+                    hp.rows.push_back({(qi * q_len + j) * nq + h * G + g, L - q_len + j + 1});
+                }
+                tile_off += U.n_blk;
+                weight += (int64_t)U.n_blk * U.rt;
+                hp.units.push_back(U);
+            }
+        }
+    }
+    if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
+    hp.tiles = tile_off;
+    // even split of the weighted tile list (weight of a tile = row tiles of its unit)
+    const int64_t T = tile_off;
+    int C = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + 3) / 4));
+    hp.cta_begin.assign(C + 1, 0);
+    {
+        int c = 1;
+        int64_t cw = 0;
+        for (const AttnUnit& U : hp.units) {
+            const int64_t uw = (int64_t)U.n_blk * U.rt;
+            while (c < C) {
+                const int64_t target = (weight * c + C - 1) / C;   // first weight index of CTA c
+                if (target >= cw + uw) break;
+                const int64_t k = (target - cw + U.rt - 1) / U.rt;    // tile within unit
+                hp.cta_begin[c] = (int32_t)(U.tile_off + std::min<int64_t>(k, U.n_blk));
+                ++c;
+            }
+            cw += uw;
+        }
+        for (; c < C; ++c) hp.cta_begin[c] = (int32_t)T;
+        hp.cta_begin[C] = (int32_t)T;
+        for (int i = 1; i <= C; ++i) hp.cta_begin[i] = std::max(hp.cta_begin[i], hp.cta_begin[i - 1]);
+    }
+    // CTA holding a tile: the largest c with cta_begin[c] <= t
+    auto cta_of = [&](int32_t t) {
+        return (int32_t)(std::upper_bound(hp.cta_begin.begin(), hp.cta_begin.end() - 1, t) - hp.cta_begin.begin()) - 1;
+    };
+    hp.cta_unit.assign(C, 0);
+    {
+        size_t u = 0;
+        for (int c = 0; c < C; ++c) {
+            while (u + 1 < hp.units.size() && hp.units[u].tile_off + hp.units[u].n_blk <= hp.cta_begin[c]) ++u;
+            hp.cta_unit[c] = (int32_t)u;
+        }
+    }
+    // partial rows per unit chunk, and the merge lists
+    const int32_t n_out = n * q_len * nq;
+    std::vector<int32_t> count(n_out, 0);
+    size_t prow = 0;
+    for (AttnUnit& U : hp.units) {
+        const int32_t cf = cta_of(U.tile_off), cl = cta_of(U.tile_off + U.n_blk - 1);
+        U.cfirst = cf;
+        U.prow_base = (int32_t)prow;
+        prow += (size_t)(cl - cf + 1) * U.n_rows;
+        for (int32_t c = cf; c <= cl; ++c) {
+            if (hp.cta_begin[c] == hp.cta_begin[c + 1]) continue;
+            for (int32_t r = 0; r < U.n_rows; ++r) count[hp.rows[U.row_off + r].q_row]++;
+        }
+    }
+    if (prow >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
+    hp.partial_rows = prow;
+    hp.csr_ptr.assign(n_out + 1, 0);
+    for (int32_t o = 0; o < n_out; ++o) hp.csr_ptr[o + 1] = hp.csr_ptr[o] + count[o];
+    hp.csr_idx.assign(hp.csr_ptr[n_out], 0);
+    std::vector<int32_t> fill(hp.csr_ptr.begin(), hp.csr_ptr.end() - 1);
+    for (const AttnUnit& U : hp.units) {
+        const int32_t cl = cta_of(U.tile_off + U.n_blk - 1);
+        for (int32_t c = U.cfirst; c <= cl; ++c) {
+            if (hp.cta_begin[c] == hp.cta_begin[c + 1]) continue;
+            for (int32_t r = 0; r < U.n_rows; ++r)
+                hp.csr_idx[fill[hp.rows[U.row_off + r].q_row]++] = U.prow_base + (c - U.cfirst) * U.n_rows + r;
+        }
+    }
+    for (int32_t o = 0; o < n_out; ++o)
+        if (count[o] == 0) return DENDRITE_EINVAL;   // a row with no visible key
+    return DENDRITE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
+    auto enc = get_encode();
+    if (!enc) return DENDRITE_ECUDA;
+    CUtensorMap m;
+    // [rows = blocks * kv heads * 16][2 halves][64 columns] of bf16, one box = 16 rows x 64 columns
+    cuuint64_t dims[3] = {64, 2, (cuuint64_t)p->num_blocks * p->n_kv * BS};
+    cuuint64_t strides[2] = {128, 256};
+    cuuint32_t box[3] = {64, 1, BS};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return DENDRITE_ECUDA;
+    static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+    std::memcpy(out, &m, sizeof(m));
+    return DENDRITE_OK;
+}
+
+int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows) {
+    if (plan_bytes > p->plan_cap) {
+        size_t cap = std::max<size_t>(plan_bytes * 2, 1 << 20);
+        DENDRITE_CUDA(cudaDeviceSynchronize());
+        if (p->d_plan) cudaFree(p->d_plan);
+        p->d_plan = nullptr;
+        p->plan_cap = 0;
+        DENDRITE_CUDA(cudaMalloc(&p->d_plan, cap));
+        p->plan_cap = cap;
+        p->plan.valid = false;
+    }
+    if (plan_bytes > p->h_plan_cap) {
+        size_t cap = std::max<size_t>(plan_bytes * 2, 1 << 20);
+        DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));
+        if (p->h_plan) cudaFreeHost(p->h_plan);
+        p->h_plan = nullptr;
+        p->h_plan_cap = 0;
+        DENDRITE_CUDA(cudaMallocHost(&p->h_plan, cap));
+        p->h_plan_cap = cap;
+    }
+    if (partial_rows > p->partial_rows_cap) {
+        size_t cap = std::max<size_t>(partial_rows * 3 / 2, 4096);
+        DENDRITE_CUDA(cudaDeviceSynchronize());
+        if (p->d_partial) cudaFree(p->d_partial);
+        p->d_partial = nullptr;
+        p->partial_rows_cap = 0;
+        DENDRITE_CUDA(cudaMalloc(&p->d_partial, cap * (p->head_dim + 2) * sizeof(float)));
+        p->partial_rows_cap = cap;
+    }
+    return DENDRITE_OK;
+}
+
+}  // namespace
+
+namespace dendrite {
+
+int attn_setup(dendrite_pool* p) {
+    if (p->dtype == DENDRITE_BF16) {
+        DENDRITE_TRY(encode_pool_map(p, p->d_k, p->tmap_k));
+        DENDRITE_TRY(encode_pool_map(p, p->d_v, p->tmap_v));
+        p->tmaps_ok = true;
+        DENDRITE_CUDA(cudaFuncSetAttribute(k_attn_partial_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BF16));
+        int occ = 0;
+        DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_bf16, THREADS, SMEM_BF16));
+        p->attn_ctas_per_sm = std::max(1, occ);
+    } else {
+        const size_t sm = 2 * BS * p->head_dim * sizeof(float);
+        int occ = 0;
+        DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_f32, 128, sm));
+        p->attn_ctas_per_sm = std::max(1, occ);
+    }
+    return DENDRITE_OK;
+}
+
+void attn_teardown(dendrite_pool* p) {
+    if (p->d_plan) cudaFree(p->d_plan);
+    if (p->h_plan) cudaFreeHost(p->h_plan);
+    if (p->d_partial) cudaFree(p->d_partial);
+    p->d_plan = nullptr;
+    p->h_plan = nullptr;
+    p->d_partial = nullptr;
+}
+
+}  // namespace dendrite
+
+extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_t n_q_heads, int32_t q_len,
+                                         const int32_t* branches, int32_t n, void* out, void* stream) {
+    if (!p) return DENDRITE_EINVAL;
+    if (p->poisoned) return p->poisoned;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    if (!Q || !out || !branches || n <= 0 || q_len <= 0 || n_q_heads <= 0) return DENDRITE_EINVAL;
+    if (n_q_heads % p->n_kv) return DENDRITE_EINVAL;
+    if (((uintptr_t)Q | (uintptr_t)out) & 15) return DENDRITE_EINVAL;
+    if ((int64_t)n * q_len * n_q_heads >= INT32_MAX / 2) return DENDRITE_ELIMIT;
+    for (int32_t i = 0; i < n; ++i) {
+        DENDRITE_TRY(check_live(p, branches[i]));
+        if (p->br[branches[i]].len < q_len) return DENDRITE_EINVAL;
+    }
+    {
+        std::vector<int32_t> s(branches, branches + n);
+        std::sort(s.begin(), s.end());
+        if (std::adjacent_find(s.begin(), s.end()) != s.end()) return DENDRITE_EINVAL;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf16 = p->dtype == DENDRITE_BF16;
+    const int max_ctas = p->sm_count * p->attn_ctas_per_sm;
+    PlanCache& pc = p->plan;
+    const bool hit = pc.valid && pc.version == p->version && pc.q_len == q_len && pc.n_q_heads == n_q_heads &&
+                     (int32_t)pc.branches.size() == n && std::equal(branches, branches + n, pc.branches.begin());
+    if (!hit) {
+        const auto t0 = std::chrono::steady_clock::now();
+        HostPlan hp;
+        DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, hp));
+        const int32_t C = (int32_t)hp.cta_unit.size();
+        const int32_t n_out = n * q_len * n_q_heads;
+        size_t off[7];
+        size_t b = 0;
+        off[0] = b; b = align16(b + hp.units.size() * sizeof(AttnUnit));
+        off[1] = b; b = align16(b + hp.rows.size() * sizeof(AttnRow));
+        off[2] = b; b = align16(b + hp.cta_begin.size() * 4);
+        off[3] = b; b = align16(b + hp.cta_unit.size() * 4);
+        off[4] = b; b = align16(b + hp.csr_ptr.size() * 4);
+        off[5] = b; b = align16(b + hp.csr_idx.size() * 4);
+        off[6] = b;
+        DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
+        DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
+        char* h = p->h_plan;
+        std::memcpy(h + off[0], hp.units.data(), hp.units.size() * sizeof(AttnUnit));
+        std::memcpy(h + off[1], hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
+        std::memcpy(h + off[2], hp.cta_begin.data(), hp.cta_begin.size() * 4);
+        std::memcpy(h + off[3], hp.cta_unit.data(), hp.cta_unit.size() * 4);
+        std::memcpy(h + off[4], hp.csr_ptr.data(), hp.csr_ptr.size() * 4);
+        std::memcpy(h + off[5], hp.csr_idx.data(), hp.csr_idx.size() * 4);
+        DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, h, b, cudaMemcpyHostToDevice, s));
+        DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
+        char* d = p->d_plan;
+        pc.dev.units = reinterpret_cast<const AttnUnit*>(d + off[0]);
+        pc.dev.rows = reinterpret_cast<const AttnRow*>(d + off[1]);
+        pc.dev.cta_begin = reinterpret_cast<const int32_t*>(d + off[2]);
+        pc.dev.cta_unit = reinterpret_cast<const int32_t*>(d + off[3]);
+        pc.dev.csr_ptr = reinterpret_cast<const int32_t*>(d + off[4]);
+        pc.dev.csr_idx = reinterpret_cast<const int32_t*>(d + off[5]);
+        pc.dev.n_units = (int32_t)hp.units.size();
+        pc.dev.n_ctas = C;
+        pc.dev.n_out_rows = n_out;
+        pc.n_partial_rows = hp.partial_rows;
+        pc.valid = true;
+        pc.version = p->version;
+        pc.q_len = q_len;
+        pc.n_q_heads = n_q_heads;
+        pc.branches.assign(branches, branches + n);
+        pc.stats.n_segments = hp.n_segments;
+        pc.stats.n_units = (int32_t)hp.units.size();
+        pc.stats.n_ctas = C;
+        pc.stats.n_partials = (int32_t)hp.csr_idx.size();
+        pc.stats.tiles = hp.tiles;
+        pc.stats.unique_tiles = hp.unique_tiles;
+        pc.stats.plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    } else {
+        pc.stats.plan_us = 0.0;
+    }
+    AttnArgs a;
+    a.plan = pc.dev;
+    a.Q = Q;
+    a.table = p->d_table;
+    a.pool_k = static_cast<const float*>(p->d_k);
+    a.pool_v = static_cast<const float*>(p->d_v);
+    a.part_acc = p->d_partial;
+    a.part_ml = reinterpret_cast<float2*>(p->d_partial + p->partial_rows_cap * p->head_dim);
+    a.meta = p->d_meta;
+    a.bpb = p->bpb;
+    a.n_kv = p->n_kv;
+    a.head_dim = p->head_dim;
+    a.n_blocks = (int32_t)p->num_blocks;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
+    prof_begin(p, T_ATTN_TOTAL, s);
+    prof_begin(p, T_ATTN_PARTIAL, s);
+    if (bf16) {
+        CUtensorMap mk, mv;
+        std::memcpy(&mk, p->tmap_k, sizeof(mk));
+        std::memcpy(&mv, p->tmap_v, sizeof(mv));
+        k_attn_partial_bf16<<<pc.dev.n_ctas, THREADS, SMEM_BF16, s>>>(mk, mv, a);
+    } else {
+        k_attn_partial_f32<<<pc.dev.n_ctas, 128, 2 * BS * p->head_dim * sizeof(float), s>>>(a);
+    }
+    prof_end(p, T_ATTN_PARTIAL, s);
+    DENDRITE_CUDA(cudaGetLastError());
+    prof_begin(p, T_ATTN_MERGE, s);
+    const int warps_per_cta = 4;
+    const unsigned grid = (unsigned)((pc.dev.n_out_rows + warps_per_cta - 1) / warps_per_cta);
+    if (bf16) k_attn_merge<__nv_bfloat16><<<grid, 32 * warps_per_cta, 0, s>>>(a, static_cast<__nv_bfloat16*>(out));
+    else k_attn_merge<float><<<grid, 32 * warps_per_cta, 0, s>>>(a, static_cast<float*>(out));
+    prof_end(p, T_ATTN_MERGE, s);
+    prof_end(p, T_ATTN_TOTAL, s);
+    DENDRITE_CUDA(cudaGetLastError());
+    return DENDRITE_OK;
+}
+
+extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* out) {
+    if (!p || !out) return DENDRITE_EINVAL;
+    if (!p->plan.valid) return DENDRITE_EINVAL;
+    *out = p->plan.stats;
+    return DENDRITE_OK;
+}

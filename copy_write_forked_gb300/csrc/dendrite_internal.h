@@ -1,0 +1,216 @@
+// Internal declarations of the dendrite library (host + device).
+// Not part of the public ABI; see include/dendrite.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <chrono>
+#include <deque>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "dendrite.h"
+
+namespace dendrite {
+
+// ------------------------------------------------------------------ limits
+constexpr int kBlockSize = 16;        // tokens per block (= attention tile height)
+constexpr int kMaxUnitRowsBf16 = 64;  // rows per attention work unit (4 row tiles of 16)
+constexpr int kMaxUnitRowsF32 = 16;
+constexpr int kAppendMetaThreads = 1024;
+constexpr int kFreeCollectThreads = 1024;
+
+// Device-resident pool metadata words.
+struct DevMeta {
+    int32_t top;        // free stack size
+    int32_t status;     // sticky error code (0 = ok)
+    int32_t rel_lo;     // smallest block id released by the current free call
+    int32_t rel_hi;     // largest block id released by the current free call
+    int32_t rel_count;  // blocks released by the current free call
+    int32_t pad[3];
+};
+
+// One attention work unit: a (segment, kv head, row group).
+struct AttnUnit {
+    int32_t table_row;  // branch handle whose table row holds the segment's block ids
+    int32_t blk_start;  // first logical block index
+    int32_t n_blk;      // tiles (blocks) in the unit
+    int32_t kv_head;
+    int32_t row_off;    // first row in the row list
+    int32_t n_rows;     // 1..64 query rows
+    int32_t rt;         // row tiles of 16 (1, 2 or 4)
+    int32_t cfirst;     // CTA holding the unit's first tile
+    int32_t tile_off;   // global index of the unit's first tile
+    int32_t prow_base;  // first partial row of the unit's first chunk
+    int32_t pad[2];
+};
+static_assert(sizeof(AttnUnit) == 48, "AttnUnit layout");
+
+// One query row of a unit.
+struct AttnRow {
+    int32_t q_row;   // row of Q/out viewed as [n_rows_total][head_dim]
+    int32_t limit;   // number of visible positions (query sees positions < limit)
+};
+
+// Device view of an uploaded attention plan.
+struct AttnPlanDev {
+    const AttnUnit* units;
+    const AttnRow* rows;
+    const int32_t* cta_begin;   // [n_ctas + 1] global tile boundaries
+    const int32_t* cta_unit;    // [n_ctas] unit holding cta_begin[c]
+    const int32_t* csr_ptr;     // [n_out_rows + 1]
+    const int32_t* csr_idx;     // partial row indices per output row
+    int32_t n_units;
+    int32_t n_ctas;
+    int32_t n_out_rows;
+};
+
+// ------------------------------------------------------- host bookkeeping
+struct Branch {
+    int32_t live = 0;
+    int32_t len = 0;
+    int32_t node = -1;
+};
+
+struct Node {
+    int32_t parent = -1;
+    int32_t fork_len = 0;
+    int32_t len = 0;
+    int32_t handle = -1;
+    int32_t refs = 0;   // (live handle ? 1 : 0) + number of child nodes
+};
+
+// Pinned host -> device staging ring for per-call argument arrays.
+class Staging {
+public:
+    int init(size_t cap);
+    void destroy();
+    // Reserve `bytes` (256-aligned); returns host and device pointers.
+    int reserve(size_t bytes, char** h, char** d);
+    // Copy the reserved region to the device on `stream`.
+    int upload(cudaStream_t stream, char* h, size_t bytes);
+    // Mark every region reserved since the last release as reusable once
+    // the work queued on `stream` so far has completed.
+    int release(cudaStream_t stream);
+
+private:
+    int grow(size_t need);
+    int wait_overlap(size_t off, size_t n);
+    char* h_ = nullptr;
+    char* d_ = nullptr;
+    size_t cap_ = 0;
+    size_t head_ = 0;
+    size_t pending_begin_ = 0, pending_end_ = 0;
+    bool pending_ = false;
+    bool pending_wrapped_ = false;
+    struct Region { size_t off, end; cudaEvent_t ev; };
+    std::deque<Region> inflight_;
+    std::vector<cudaEvent_t> spare_;
+};
+
+enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_ATTN_MERGE, T_FREE,
+                  T_ATTN_TOTAL, T_COUNT };
+
+struct PlanCache {
+    bool valid = false;
+    uint64_t version = 0;
+    int32_t q_len = 0, n_q_heads = 0;
+    std::vector<int32_t> branches;
+    AttnPlanDev dev{};
+    size_t n_partial_rows = 0;
+    dendrite_plan_stats stats{};
+};
+
+}  // namespace dendrite
+
+struct dendrite_pool {
+    // geometry
+    int64_t num_blocks = 0;
+    int32_t block_size = 0, n_kv = 0, head_dim = 0, dtype = 0, elt = 0;
+    int32_t max_branches = 0, bpb = 0;
+    int device = 0;
+    int sm_count = 0;
+    int attn_ctas_per_sm = 1;
+
+    // device state
+    void* d_k = nullptr;
+    void* d_v = nullptr;
+    int32_t* d_refcount = nullptr;
+    int32_t* d_stack = nullptr;
+    int32_t* d_table = nullptr;
+    dendrite::DevMeta* d_meta = nullptr;
+    int32_t* d_holders = nullptr;    // [num_blocks] holders of a shared tail within one append
+    int32_t* d_last = nullptr;       // [num_blocks] last holder index within one append
+    int32_t* d_released = nullptr;   // [num_blocks] flags set by free phase A
+    int32_t* d_call_i32 = nullptr;   // [4 * max_branches] per-call scratch (offsets, cow src/dst)
+
+    // tensor maps for the bf16 attention kernel (opaque 128-byte blobs)
+    alignas(64) unsigned char tmap_k[128];
+    alignas(64) unsigned char tmap_v[128];
+    bool tmaps_ok = false;
+
+    // attention workspace (grow-only)
+    char* d_plan = nullptr;
+    size_t plan_cap = 0;
+    char* h_plan = nullptr;          // pinned
+    size_t h_plan_cap = 0;
+    cudaEvent_t plan_copied = nullptr;
+    float* d_partial = nullptr;      // partial rows: [rows][head_dim] acc then [rows][2] (m, l)
+    size_t partial_rows_cap = 0;
+    dendrite::PlanCache plan;
+
+    // host mirror
+    std::vector<dendrite::Branch> br;
+    std::vector<int32_t> free_handles;
+    std::vector<dendrite::Node> nodes;
+    std::vector<int32_t> free_nodes;
+    uint64_t version = 1;
+    int32_t poisoned = 0;
+
+    dendrite::Staging staging;
+
+    // profiling
+    bool profiling = false;
+    cudaEvent_t ev[dendrite::T_COUNT][2] = {};
+    bool ev_recorded[dendrite::T_COUNT] = {};
+};
+
+namespace dendrite {
+
+// -------------------------------------------------------------- helpers
+int cuda_err(cudaError_t e);     // maps a CUDA error to DENDRITE_ECUDA (and clears it)
+void prof_begin(dendrite_pool* p, TimingKind k, cudaStream_t s);
+void prof_end(dendrite_pool* p, TimingKind k, cudaStream_t s);
+int check_live(const dendrite_pool* p, int32_t h);
+
+// Planner (planner.cpp): segments over the node forest.
+struct Segment {
+    int32_t rep_node;
+    int32_t block_start;
+    int32_t block_count;
+    int32_t member_offset;
+    int32_t n_members;
+};
+void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                   const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
+                   std::vector<Segment>& segs, std::vector<int32_t>& members);
+
+// Attention (attn.cu)
+int attn_setup(dendrite_pool* p);      // tensor maps, occupancy
+void attn_teardown(dendrite_pool* p);
+
+}  // namespace dendrite
+
+#define DENDRITE_TRY(x)                   \
+    do {                                  \
+        int _rc = (x);                    \
+        if (_rc != DENDRITE_OK) return _rc; \
+    } while (0)
+
+#define DENDRITE_CUDA(x)                                  \
+    do {                                                  \
+        cudaError_t _e = (x);                             \
+        if (_e != cudaSuccess) return dendrite::cuda_err(_e); \
+    } while (0)

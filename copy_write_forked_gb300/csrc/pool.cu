@@ -1,0 +1,955 @@
+// Block pool, fork, copy-on-write append and free.
+//
+// Method: Dendrite article (ainews.cool, "Dendrite: O(1) KV cache forking",
+// section 技术深度解析) and dendrite demo.tape (section "The problem":
+// copy-on-write block table).  A fork copies block-table entries and raises
+// refcounts; it never copies KV.  An append copies a partially filled tail
+// block only when it is still shared (refcount > 1).  Freed blocks go back to
+// a free stack.
+//
+// Device state (all owned by the pool):
+//   K, V pools   [num_blocks][n_kv][block_size][head_dim]
+//   refcount     int32[num_blocks]
+//   free stack   int32[num_blocks], size in DevMeta::top; pop = stack[--top]
+//   tables       int32[max_branches][bpb], -1 = empty
+//   DevMeta      top, sticky status, scratch words of the free call
+//
+// Determinism: block ids handed out by one append follow argument order
+// (copy of the tail first, then new blocks in position order), and the blocks
+// released by one free are pushed in descending id order, so tables, refcounts
+// and the free stack are bit-for-bit reproducible.
+#include <algorithm>
+#include <climits>
+#include <cstdio>
+#include <cstring>
+#include <unordered_set>
+
+#include "dendrite_internal.h"
+
+using namespace dendrite;
+
+// =================================================================== kernels
+namespace {
+
+__device__ __forceinline__ void set_status(DevMeta* m, int32_t code) {
+    atomicCAS(&m->status, 0, code);
+}
+
+__global__ void k_init(int32_t* stack, int32_t* refcount, int32_t* holders, int32_t* last,
+                       int32_t* released, int64_t n, int32_t* table, int64_t n_table, DevMeta* meta) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        stack[i] = (int32_t)(n - 1 - i);
+        refcount[i] = 0;
+        holders[i] = 0;
+        last[i] = -1;
+        released[i] = 0;
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_table; i += stride) table[i] = -1;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        meta->top = (int32_t)n;
+        meta->status = 0;
+        meta->rel_lo = INT_MAX;
+        meta->rel_hi = -1;
+        meta->rel_count = 0;
+    }
+}
+
+// ---------------------------------------------------------------- fork
+// One warp per (parent, child) pair: the child's table row becomes a copy of
+// the parent's first nb entries.  The pair flagged with add > 0 also raises
+// the refcount of each of those blocks by `add` (the parent's child count),
+// so each parent's blocks see exactly one atomic add per fork call.
+template <int CAP>
+struct ForkParams {
+    int32_t n_pairs;
+    int32_t child[CAP];
+    int32_t parent[CAP];
+    int32_t nb[CAP];
+    int32_t add[CAP];
+};
+
+__device__ __forceinline__ void fork_pair(int32_t* __restrict__ table, int32_t* __restrict__ refcount,
+                                          int32_t bpb, int32_t child, int32_t parent, int32_t nb,
+                                          int32_t add, int lane, int32_t n_blocks, DevMeta* meta) {
+    const int32_t* src = table + (int64_t)parent * bpb;
+    int32_t* dst = table + (int64_t)child * bpb;
+    for (int32_t k = lane; k < nb; k += 32) {
+        const int32_t blk = src[k];
+        dst[k] = blk;
+        if ((uint32_t)blk >= (uint32_t)n_blocks) {
+            set_status(meta, DENDRITE_ECORRUPT);
+            continue;
+        }
+        if (add) atomicAdd(refcount + blk, add);
+    }
+}
+
+template <int CAP>
+__global__ void k_fork_param(const __grid_constant__ ForkParams<CAP> a, int32_t* table,
+                             int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
+    if (meta->status) return;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (warp >= a.n_pairs) return;
+    fork_pair(table, refcount, bpb, a.child[warp], a.parent[warp], a.nb[warp], a.add[warp],
+              threadIdx.x & 31, n_blocks, meta);
+}
+
+// Same for batches too large for kernel parameters: the four arrays
+// (child, parent, nb, add) are read from device memory.
+__global__ void k_fork_global(const int32_t* __restrict__ args, int32_t n_pairs, int32_t* table,
+                              int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
+    if (meta->status) return;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (warp >= n_pairs) return;
+    fork_pair(table, refcount, bpb, args[warp], args[n_pairs + warp], args[2 * n_pairs + warp],
+              args[3 * n_pairs + warp], threadIdx.x & 31, n_blocks, meta);
+}
+
+// ------------------------------------------------------------ block scan
+template <int NT>
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_sums, int32_t* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t s = lane < NT / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < NT / 32) warp_sums[lane] = s;   // inclusive warp prefix
+        if (lane == NT / 32 - 1) *total = s;
+    }
+    __syncthreads();
+    const int32_t res = x - v + (wid ? warp_sums[wid - 1] : 0);
+    __syncthreads();
+    return res;
+}
+
+// ------------------------------------------------------- append, phase 1
+// One CTA.  Decides, for every branch of the call in argument order, whether
+// its partially filled tail must be copied, reserves its blocks from the free
+// stack with one exclusive scan, checks capacity (all-or-nothing) and writes
+// the table/refcount updates.
+//
+// Copy-on-write decision as if the branches were served one after the other:
+// a branch copies iff the tail's refcount is above 1 at its turn.  Earlier
+// holders of the same tail in this call all copy (each leaves one reference),
+// so with r = refcount[tail] and k holders in the call, holder number j
+// (0-based, argument order) copies iff r - j > 1.  Since r >= k, only the last
+// holder can write in place, and only when r == k.
+__global__ void __launch_bounds__(kAppendMetaThreads)
+k_append_meta(const int32_t* __restrict__ args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb,
+              int32_t n_blocks, int32_t* table, int32_t* refcount, const int32_t* stack, int32_t* holders,
+              int32_t* last, int32_t* call, DevMeta* meta) {
+    __shared__ int32_t warp_sums[kAppendMetaThreads / 32];
+    __shared__ int32_t chunk_total;
+    __shared__ int32_t status0, top0;
+    const int32_t* branch = args;
+    const int32_t* lens = args + n;
+    int32_t* offs = call;              // [n] first stack offset of each branch
+    int32_t* cow_src = call + n;       // [n] copied tail (-1 = none)
+    int32_t* cow_dst = call + 2 * n;   // [n] its copy
+    if (threadIdx.x == 0) {
+        status0 = meta->status;
+        top0 = meta->top;
+    }
+    __syncthreads();
+    if (status0) return;
+    // every tail id must be a block id (a broken table poisons the pool instead
+    // of being dereferenced)
+    __shared__ int32_t bad;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t L = lens[i];
+        if (L % bs && (uint32_t)table[(int64_t)branch[i] * bpb + L / bs] >= (uint32_t)n_blocks) bad = 1;
+    }
+    __syncthreads();
+    if (bad) {
+        if (threadIdx.x == 0) set_status(meta, DENDRITE_ECORRUPT);
+        return;
+    }
+    // holders of each shared tail within the call
+    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t L = lens[i];
+        if (L % bs) {
+            const int32_t tail = table[(int64_t)branch[i] * bpb + L / bs];
+            atomicAdd(holders + tail, 1);
+            atomicMax(last + tail, i);
+        }
+    }
+    __syncthreads();
+    int32_t carry = 0;
+    for (int32_t base = 0; base < n; base += blockDim.x) {
+        const int32_t i = base + threadIdx.x;
+        int32_t demand = 0;
+        if (i < n) {
+            const int32_t L = lens[i];
+            int32_t cow = 0, tail = -1;
+            if (L % bs) {
+                tail = table[(int64_t)branch[i] * bpb + L / bs];
+                cow = !(refcount[tail] == holders[tail] && last[tail] == i);
+            }
+            demand = cow + (L + n_new + bs - 1) / bs - (L + bs - 1) / bs;
+            cow_src[i] = cow ? tail : -1;
+        }
+        const int32_t ex = block_exclusive_scan<kAppendMetaThreads>(demand, warp_sums, &chunk_total);
+        if (i < n) offs[i] = carry + ex;
+        carry += chunk_total;
+        __syncthreads();
+    }
+    const bool fits = carry <= top0;
+    if (fits) {
+        for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+            const int32_t b = branch[i], L = lens[i];
+            int32_t o = offs[i];
+            int32_t* row = table + (int64_t)b * bpb;
+            const int32_t src = cow_src[i];
+            if (src >= 0) {
+                const int32_t blk = stack[top0 - 1 - o];
+                ++o;
+                atomicSub(refcount + src, 1);
+                refcount[blk] = 1;
+                row[L / bs] = blk;
+                cow_dst[i] = blk;
+            } else {
+                cow_dst[i] = -1;
+            }
+            const int32_t nb0 = (L + bs - 1) / bs, nb1 = (L + n_new + bs - 1) / bs;
+            for (int32_t k = nb0; k < nb1; ++k, ++o) {
+                const int32_t blk = stack[top0 - 1 - o];
+                refcount[blk] = 1;
+                row[k] = blk;
+            }
+        }
+    }
+    __syncthreads();
+    // reset the holder scratch for the next call
+    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int32_t L = lens[i];
+        if (L % bs) {
+            // the tail id may have been replaced in the table; the original is in cow_src
+            // when copied, else still in the table
+            const int32_t tail = cow_src[i] >= 0 ? cow_src[i] : table[(int64_t)branch[i] * bpb + L / bs];
+            holders[tail] = 0;
+            last[tail] = -1;
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (fits) meta->top = top0 - carry;
+        else set_status(meta, DENDRITE_ENOMEM);
+    }
+}
+
+// ------------------------------------------------------- append, phase 2
+// One CTA per (branch, touched block, kv head) tile: copies the valid slots
+// of a copied-on-write tail (if any) and scatters the new rows into their
+// slots with 16-byte vector moves.  tile_pre[i] is the exclusive prefix of
+// touched blocks per branch (host computed; depends only on lengths).
+__global__ void k_append_copy(const int32_t* __restrict__ args, const int32_t* __restrict__ tile_pre,
+                              int32_t n, int32_t n_new, int32_t bs, int32_t bpb, int32_t n_kv,
+                              int32_t row_vec, int32_t n_blocks, const int32_t* __restrict__ table,
+                              const int32_t* __restrict__ call, const uint4* __restrict__ Kin,
+                              const uint4* __restrict__ Vin, uint4* __restrict__ Kp, uint4* __restrict__ Vp,
+                              const DevMeta* meta) {
+    if (meta->status) return;
+    const int32_t* branch = args;
+    const int32_t* lens = args + n;
+    const int32_t* cow_src = call + n;
+    const int64_t tile = blockIdx.x;
+    const int32_t h = (int32_t)(tile % n_kv);
+    const int32_t t = (int32_t)(tile / n_kv);   // touched-block index over the call
+    // branch i with tile_pre[i] <= t < tile_pre[i+1]
+    int32_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (tile_pre[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int32_t i = lo;
+    const int32_t L = lens[i];
+    const int32_t lblk = L / bs + (t - tile_pre[i]);
+    const int32_t dst = table[(int64_t)branch[i] * bpb + lblk];
+    if ((uint32_t)dst >= (uint32_t)n_blocks || cow_src[i] >= n_blocks) {
+        if (threadIdx.x == 0) atomicCAS(const_cast<int32_t*>(&meta->status), 0, DENDRITE_ECORRUPT);
+        return;
+    }
+    const int32_t s0 = lblk == L / bs ? L % bs : 0;
+    const int32_t s1 = min(bs, L + n_new - lblk * bs);
+    const int64_t tile_vec = (int64_t)bs * row_vec;
+    uint4* kd = Kp + ((int64_t)dst * n_kv + h) * tile_vec;
+    uint4* vd = Vp + ((int64_t)dst * n_kv + h) * tile_vec;
+    // copy of the shared tail's valid slots
+    if (lblk == L / bs && cow_src[i] >= 0) {
+        const uint4* ks = Kp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec;
+        const uint4* vs = Vp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec;
+        for (int32_t e = threadIdx.x; e < s0 * row_vec; e += blockDim.x) {
+            kd[e] = ks[e];
+            vd[e] = vs[e];
+        }
+    }
+    // new rows: token (lblk*bs + s - L) of branch i
+    const int32_t cnt = (s1 - s0) * row_vec;
+    for (int32_t e = threadIdx.x; e < cnt; e += blockDim.x) {
+        const int32_t s = s0 + e / row_vec, v = e % row_vec;
+        const int64_t tok = (int64_t)lblk * bs + s - L;
+        const int64_t src = (((int64_t)i * n_new + tok) * n_kv + h) * row_vec + v;
+        kd[(int64_t)s * row_vec + v] = Kin[src];
+        vd[(int64_t)s * row_vec + v] = Vin[src];
+    }
+}
+
+// ----------------------------------------------------------------- free
+// Phase A: one thread per table entry of the freed branches.  Drops one
+// reference; an entry whose refcount reaches zero marks its block released.
+__global__ void k_free_release(const int32_t* __restrict__ args, const int32_t* __restrict__ ent_pre,
+                               int32_t n, int32_t total, int32_t bpb, int32_t n_blocks, int32_t* table,
+                               int32_t* refcount, int32_t* released, DevMeta* meta) {
+    if (meta->status) return;
+    const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= total) return;
+    int32_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (ent_pre[mid] <= e) lo = mid; else hi = mid - 1;
+    }
+    int32_t* slot = table + (int64_t)args[lo] * bpb + (e - ent_pre[lo]);
+    const int32_t blk = *slot;
+    *slot = -1;
+    if ((uint32_t)blk >= (uint32_t)n_blocks) {
+        set_status(meta, DENDRITE_ECORRUPT);
+        return;
+    }
+    const int32_t old = atomicSub(refcount + blk, 1);
+    if (old == 1) {
+        released[blk] = 1;
+        atomicMin(&meta->rel_lo, blk);
+        atomicMax(&meta->rel_hi, blk);
+        atomicAdd(&meta->rel_count, 1);
+    } else if (old < 1) {
+        set_status(meta, DENDRITE_ECORRUPT);
+    }
+}
+
+// Phase B: one CTA pushes the released blocks onto the free stack in
+// descending id order (scan over [rel_lo, rel_hi] from the top down).
+__global__ void __launch_bounds__(kFreeCollectThreads)
+k_free_push(int32_t* stack, int32_t* released, DevMeta* meta) {
+    __shared__ int32_t warp_sums[kFreeCollectThreads / 32];
+    __shared__ int32_t chunk_total;
+    __shared__ int32_t lo, hi, top0, cnt, st;
+    if (threadIdx.x == 0) {
+        lo = meta->rel_lo;
+        hi = meta->rel_hi;
+        top0 = meta->top;
+        cnt = meta->rel_count;
+        st = meta->status;
+    }
+    __syncthreads();
+    if (st || cnt == 0) return;
+    int32_t carry = 0;
+    for (int32_t base = 0; base <= hi - lo; base += blockDim.x) {
+        const int32_t j = hi - (base + (int32_t)threadIdx.x);
+        const int32_t f = (j >= lo) ? released[j] : 0;
+        const int32_t ex = block_exclusive_scan<kFreeCollectThreads>(f, warp_sums, &chunk_total);
+        if (f) {
+            stack[top0 + carry + ex] = j;
+            released[j] = 0;
+        }
+        carry += chunk_total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        meta->top = top0 + carry;
+        meta->rel_lo = INT_MAX;
+        meta->rel_hi = -1;
+        meta->rel_count = 0;
+    }
+}
+
+}  // namespace
+
+// ============================================================ host helpers
+namespace dendrite {
+
+int cuda_err(cudaError_t e) {
+    (void)e;
+    cudaGetLastError();
+    return DENDRITE_ECUDA;
+}
+
+void prof_begin(dendrite_pool* p, TimingKind k, cudaStream_t s) {
+    if (p->profiling) cudaEventRecord(p->ev[k][0], s);
+}
+void prof_end(dendrite_pool* p, TimingKind k, cudaStream_t s) {
+    if (p->profiling) {
+        cudaEventRecord(p->ev[k][1], s);
+        p->ev_recorded[k] = true;
+    }
+}
+
+int check_live(const dendrite_pool* p, int32_t h) {
+    if (h < 0 || h >= p->max_branches || !p->br[h].live) return DENDRITE_EBADHANDLE;
+    return DENDRITE_OK;
+}
+
+// ----------------------------------------------------------------- staging
+int Staging::init(size_t cap) {
+    cap_ = cap;
+    if (cudaMallocHost(&h_, cap) != cudaSuccess) return cuda_err(cudaErrorMemoryAllocation);
+    if (cudaMalloc(&d_, cap) != cudaSuccess) return cuda_err(cudaErrorMemoryAllocation);
+    return DENDRITE_OK;
+}
+
+void Staging::destroy() {
+    for (auto& r : inflight_) cudaEventDestroy(r.ev);
+    for (auto e : spare_) cudaEventDestroy(e);
+    inflight_.clear();
+    spare_.clear();
+    if (h_) cudaFreeHost(h_);
+    if (d_) cudaFree(d_);
+    h_ = d_ = nullptr;
+}
+
+int Staging::wait_overlap(size_t off, size_t n) {
+    while (!inflight_.empty()) {
+        const Region& r = inflight_.front();
+        const bool overlap = r.off < off + n && off < r.end;
+        if (!overlap) {
+            // regions are handed out in ring order; stop at the first one that
+            // does not overlap unless it lies behind the new range
+            bool later = false;
+            for (const Region& q : inflight_)
+                if (q.off < off + n && off < q.end) later = true;
+            if (!later) break;
+        }
+        DENDRITE_CUDA(cudaEventSynchronize(r.ev));
+        spare_.push_back(r.ev);
+        inflight_.pop_front();
+    }
+    return DENDRITE_OK;
+}
+
+int Staging::grow(size_t need) {
+    // wait for everything in flight, then reallocate
+    for (auto& r : inflight_) {
+        cudaEventSynchronize(r.ev);
+        spare_.push_back(r.ev);
+    }
+    inflight_.clear();
+    size_t cap = cap_;
+    while (cap < need) cap *= 2;
+    cudaFreeHost(h_);
+    cudaFree(d_);
+    h_ = d_ = nullptr;
+    cap_ = 0;
+    head_ = 0;
+    pending_ = false;
+    return init(cap);
+}
+
+int Staging::reserve(size_t bytes, char** h, char** d) {
+    bytes = (bytes + 255) & ~size_t(255);
+    if (bytes == 0) bytes = 256;
+    if (bytes > cap_ / 2) {
+        if (pending_) return DENDRITE_EINVAL;   // one oversized region per call only
+        DENDRITE_TRY(grow(bytes * 2));
+    }
+    size_t off = head_;
+    if (off + bytes > cap_) {
+        off = 0;
+        if (pending_) pending_wrapped_ = true;
+    }
+    DENDRITE_TRY(wait_overlap(off, bytes));
+    if (!pending_) {
+        pending_ = true;
+        pending_wrapped_ = false;
+        pending_begin_ = off;
+    }
+    pending_end_ = off + bytes;
+    head_ = off + bytes;
+    *h = h_ + off;
+    *d = d_ + off;
+    return DENDRITE_OK;
+}
+
+int Staging::upload(cudaStream_t stream, char* h, size_t bytes) {
+    DENDRITE_CUDA(cudaMemcpyAsync(d_ + (h - h_), h, bytes, cudaMemcpyHostToDevice, stream));
+    return DENDRITE_OK;
+}
+
+int Staging::release(cudaStream_t stream) {
+    if (!pending_) return DENDRITE_OK;
+    cudaEvent_t ev;
+    if (!spare_.empty()) {
+        ev = spare_.back();
+        spare_.pop_back();
+    } else {
+        DENDRITE_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    }
+    DENDRITE_CUDA(cudaEventRecord(ev, stream));
+    if (pending_wrapped_) {
+        inflight_.push_back({pending_begin_, cap_, ev});
+        cudaEvent_t ev2;
+        DENDRITE_CUDA(cudaEventCreateWithFlags(&ev2, cudaEventDisableTiming));
+        DENDRITE_CUDA(cudaEventRecord(ev2, stream));
+        inflight_.push_back({0, pending_end_, ev2});
+    } else {
+        inflight_.push_back({pending_begin_, pending_end_, ev});
+    }
+    pending_ = false;
+    return DENDRITE_OK;
+}
+
+}  // namespace dendrite
+
+// ================================================================ host API
+namespace {
+
+int32_t new_node(dendrite_pool* p, int32_t parent, int32_t fork_len, int32_t handle) {
+    int32_t id;
+    if (!p->free_nodes.empty()) {
+        id = p->free_nodes.back();
+        p->free_nodes.pop_back();
+    } else {
+        id = (int32_t)p->nodes.size();
+        p->nodes.emplace_back();
+    }
+    Node& n = p->nodes[id];
+    n.parent = parent;
+    n.fork_len = fork_len;
+    n.len = fork_len;
+    n.handle = handle;
+    n.refs = 1;
+    if (parent >= 0) p->nodes[parent].refs++;
+    return id;
+}
+
+void drop_node_ref(dendrite_pool* p, int32_t id) {
+    while (id >= 0) {
+        Node& n = p->nodes[id];
+        if (--n.refs > 0) return;
+        const int32_t up = n.parent;
+        n = Node();
+        p->free_nodes.push_back(id);
+        id = up;
+    }
+}
+
+int32_t alloc_handle(dendrite_pool* p) {
+    const int32_t h = p->free_handles.back();
+    p->free_handles.pop_back();
+    return h;
+}
+
+int prelude(dendrite_pool* p) {
+    if (!p) return DENDRITE_EINVAL;
+    if (p->poisoned) return p->poisoned;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    return DENDRITE_OK;
+}
+
+int check_unique_live(dendrite_pool* p, const int32_t* b, int32_t n) {
+    for (int32_t i = 0; i < n; ++i) DENDRITE_TRY(check_live(p, b[i]));
+    if (n > 1) {
+        std::vector<int32_t> s(b, b + n);
+        std::sort(s.begin(), s.end());
+        if (std::adjacent_find(s.begin(), s.end()) != s.end()) return DENDRITE_EINVAL;
+    }
+    return DENDRITE_OK;
+}
+
+template <int CAP>
+int launch_fork_param(dendrite_pool* p, const std::vector<int32_t>& child, const std::vector<int32_t>& par,
+                      const std::vector<int32_t>& nb, const std::vector<int32_t>& add, cudaStream_t s) {
+    ForkParams<CAP> a;
+    a.n_pairs = (int32_t)child.size();
+    for (size_t i = 0; i < child.size(); ++i) {
+        a.child[i] = child[i];
+        a.parent[i] = par[i];
+        a.nb[i] = nb[i];
+        a.add[i] = add[i];
+    }
+    const int threads = 128;
+    const int blocks = (int)((child.size() * 32 + threads - 1) / threads);
+    k_fork_param<CAP><<<blocks, threads, 0, s>>>(a, p->d_table, p->d_refcount, p->bpb, (int32_t)p->num_blocks,
+                                                  p->d_meta);
+    DENDRITE_CUDA(cudaGetLastError());
+    return DENDRITE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dendrite_version(void) { return "dendrite-gb300 0.1.0 (sm_103a)"; }
+
+int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int32_t head_dim,
+                         int32_t dtype, const dendrite_pool_opts* opts, dendrite_pool** out) {
+    if (!out) return DENDRITE_EINVAL;
+    *out = nullptr;
+    if (num_blocks <= 0 || num_blocks >= INT32_MAX || n_kv_heads < 1 || n_kv_heads > 64) return DENDRITE_EINVAL;
+    if (block_size != kBlockSize) return DENDRITE_EDTYPE;
+    if (dtype == DENDRITE_BF16) {
+        if (head_dim != 128) return DENDRITE_EDTYPE;
+    } else if (dtype == DENDRITE_FP32) {
+        if (head_dim <= 0 || head_dim > 256 || head_dim % 32) return DENDRITE_EDTYPE;
+    } else {
+        return DENDRITE_EDTYPE;
+    }
+    int32_t max_branches = 4096, bpb = 4096;
+    if (opts) {
+        for (int i = 0; i < 6; ++i)
+            if (opts->reserved[i]) return DENDRITE_EINVAL;
+        if (opts->max_branches) max_branches = opts->max_branches;
+        if (opts->max_blocks_per_branch) bpb = opts->max_blocks_per_branch;
+    }
+    if (max_branches < 1 || bpb < 1 || (int64_t)max_branches * bpb > (int64_t)1 << 34) return DENDRITE_EINVAL;
+
+    dendrite_pool* p = new dendrite_pool();
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->n_kv = n_kv_heads;
+    p->head_dim = head_dim;
+    p->dtype = dtype;
+    p->elt = dtype == DENDRITE_BF16 ? 2 : 4;
+    p->max_branches = max_branches;
+    p->bpb = bpb;
+    int rc = DENDRITE_OK;
+    auto fail = [&](int code) {
+        dendrite_pool_destroy(p);
+        return code;
+    };
+    if (cudaGetDevice(&p->device) != cudaSuccess) return fail(cuda_err(cudaErrorNoDevice));
+    cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device);
+    const size_t pool_bytes = (size_t)num_blocks * n_kv_heads * block_size * head_dim * p->elt;
+    if (cudaMalloc(&p->d_k, pool_bytes) != cudaSuccess || cudaMalloc(&p->d_v, pool_bytes) != cudaSuccess)
+        return fail(cuda_err(cudaErrorMemoryAllocation));
+    const size_t nb4 = (size_t)num_blocks * 4;
+    if (cudaMalloc(&p->d_refcount, nb4) != cudaSuccess || cudaMalloc(&p->d_stack, nb4) != cudaSuccess ||
+        cudaMalloc(&p->d_holders, nb4) != cudaSuccess || cudaMalloc(&p->d_last, nb4) != cudaSuccess ||
+        cudaMalloc(&p->d_released, nb4) != cudaSuccess ||
+        cudaMalloc(&p->d_table, (size_t)max_branches * bpb * 4) != cudaSuccess ||
+        cudaMalloc(&p->d_call_i32, (size_t)max_branches * 4 * 4) != cudaSuccess ||
+        cudaMalloc(&p->d_meta, sizeof(DevMeta)) != cudaSuccess)
+        return fail(cuda_err(cudaErrorMemoryAllocation));
+    if ((rc = p->staging.init(4u << 20)) != DENDRITE_OK) return fail(rc);
+    for (int k = 0; k < T_COUNT; ++k)
+        if (cudaEventCreate(&p->ev[k][0]) != cudaSuccess || cudaEventCreate(&p->ev[k][1]) != cudaSuccess)
+            return fail(cuda_err(cudaErrorUnknown));
+    if (cudaEventCreateWithFlags(&p->plan_copied, cudaEventDisableTiming) != cudaSuccess)
+        return fail(cuda_err(cudaErrorUnknown));
+    k_init<<<std::max(1, std::min(4 * p->sm_count, (int)((num_blocks + 255) / 256))), 256>>>(
+        p->d_stack, p->d_refcount, p->d_holders, p->d_last, p->d_released, num_blocks, p->d_table,
+        (int64_t)max_branches * bpb, p->d_meta);
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return fail(cuda_err(cudaErrorUnknown));
+    if ((rc = attn_setup(p)) != DENDRITE_OK) return fail(rc);
+    p->br.assign(max_branches, Branch());
+    p->free_handles.reserve(max_branches);
+    for (int32_t h = max_branches - 1; h >= 0; --h) p->free_handles.push_back(h);
+    *out = p;
+    return DENDRITE_OK;
+}
+
+int dendrite_pool_destroy(dendrite_pool* p) {
+    if (!p) return DENDRITE_EINVAL;
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    attn_teardown(p);
+    p->staging.destroy();
+    void* bufs[] = {p->d_k, p->d_v, p->d_refcount, p->d_stack, p->d_holders, p->d_last,
+                    p->d_released, p->d_table, p->d_call_i32, p->d_meta};
+    for (void* b : bufs)
+        if (b) cudaFree(b);
+    for (int k = 0; k < T_COUNT; ++k)
+        for (int j = 0; j < 2; ++j)
+            if (p->ev[k][j]) cudaEventDestroy(p->ev[k][j]);
+    if (p->plan_copied) cudaEventDestroy(p->plan_copied);
+    cudaGetLastError();
+    delete p;
+    return DENDRITE_OK;
+}
+
+int dendrite_branch_new(dendrite_pool* p, int32_t* out) {
+    DENDRITE_TRY(prelude(p));
+    if (!out) return DENDRITE_EINVAL;
+    if (p->free_handles.empty()) return DENDRITE_ELIMIT;
+    const int32_t h = alloc_handle(p);
+    p->br[h].live = 1;
+    p->br[h].len = 0;
+    p->br[h].node = new_node(p, -1, 0, h);
+    p->version++;
+    *out = h;
+    return DENDRITE_OK;
+}
+
+int dendrite_fork_batch(dendrite_pool* p, const int32_t* parents, const int32_t* n_children, int32_t n_parents,
+                        int32_t* out_children, void* stream) {
+    DENDRITE_TRY(prelude(p));
+    if (n_parents < 0 || (n_parents > 0 && (!parents || !n_children || !out_children))) return DENDRITE_EINVAL;
+    int64_t total = 0;
+    for (int32_t i = 0; i < n_parents; ++i) {
+        DENDRITE_TRY(check_live(p, parents[i]));
+        if (n_children[i] <= 0) return DENDRITE_EINVAL;
+        total += n_children[i];
+    }
+    if (total > (int64_t)p->free_handles.size()) return DENDRITE_ELIMIT;
+    if (total == 0) return DENDRITE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    std::vector<int32_t> child, par, nb, add;
+    child.reserve(total);
+    par.reserve(total);
+    nb.reserve(total);
+    add.reserve(total);
+    int64_t k = 0;
+    for (int32_t i = 0; i < n_parents; ++i) {
+        const int32_t pa = parents[i];
+        const int32_t L = p->br[pa].len;
+        const int32_t nblk = (L + p->block_size - 1) / p->block_size;
+        for (int32_t c = 0; c < n_children[i]; ++c) {
+            const int32_t h = alloc_handle(p);
+            p->br[h].live = 1;
+            p->br[h].len = L;
+            p->br[h].node = new_node(p, p->br[pa].node, L, h);
+            out_children[k++] = h;
+            child.push_back(h);
+            par.push_back(pa);
+            nb.push_back(nblk);
+            add.push_back(c == 0 ? n_children[i] : 0);
+        }
+    }
+    p->version++;
+    prof_begin(p, T_FORK, s);
+    int rc;
+    const size_t n = child.size();
+    if (n <= 4) rc = launch_fork_param<4>(p, child, par, nb, add, s);
+    else if (n <= 32) rc = launch_fork_param<32>(p, child, par, nb, add, s);
+    else if (n <= 256) rc = launch_fork_param<256>(p, child, par, nb, add, s);
+    else {
+        char *h, *d;
+        DENDRITE_TRY(p->staging.reserve(n * 16, &h, &d));
+        int32_t* a = (int32_t*)h;
+        std::memcpy(a, child.data(), n * 4);
+        std::memcpy(a + n, par.data(), n * 4);
+        std::memcpy(a + 2 * n, nb.data(), n * 4);
+        std::memcpy(a + 3 * n, add.data(), n * 4);
+        DENDRITE_TRY(p->staging.upload(s, h, n * 16));
+        const int threads = 128;
+        const int blocks = (int)((n * 32 + threads - 1) / threads);
+        k_fork_global<<<blocks, threads, 0, s>>>((const int32_t*)d, (int32_t)n, p->d_table, p->d_refcount,
+                                                  p->bpb, (int32_t)p->num_blocks, p->d_meta);
+        rc = cudaGetLastError() == cudaSuccess ? DENDRITE_OK : DENDRITE_ECUDA;
+        DENDRITE_TRY(p->staging.release(s));
+    }
+    prof_end(p, T_FORK, s);
+    return rc;
+}
+
+int dendrite_fork(dendrite_pool* p, int32_t parent, int32_t n_children, int32_t* out_children, void* stream) {
+    return dendrite_fork_batch(p, &parent, &n_children, 1, out_children, stream);
+}
+
+int dendrite_append_kv(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t n_new, const void* K,
+                       const void* V, void* stream) {
+    DENDRITE_TRY(prelude(p));
+    if (n < 0 || n_new < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
+    if (n == 0 || n_new == 0) return DENDRITE_OK;
+    if (!K || !V) return DENDRITE_EINVAL;
+    if (((uintptr_t)K | (uintptr_t)V) & 15) return DENDRITE_EINVAL;
+    DENDRITE_TRY(check_unique_live(p, branches, n));
+    const int32_t bs = p->block_size;
+    int64_t touched = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t L = p->br[branches[i]].len;
+        if (L + n_new > INT32_MAX / 2) return DENDRITE_ELIMIT;
+        if ((L + n_new + bs - 1) / bs > p->bpb) return DENDRITE_ELIMIT;
+        touched += (L + n_new - 1) / bs - L / bs + 1;
+    }
+    if (touched * p->n_kv > INT32_MAX) return DENDRITE_ELIMIT;
+    cudaStream_t s = (cudaStream_t)stream;
+    // args: branch[n], len[n] | tile prefix[n]
+    char *h, *d;
+    const size_t bytes = (size_t)n * 12;
+    DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
+    int32_t* a = (int32_t*)h;
+    int32_t acc = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t L = p->br[branches[i]].len;
+        a[i] = branches[i];
+        a[n + i] = L;
+        a[2 * n + i] = acc;
+        acc += (L + n_new - 1) / bs - L / bs + 1;
+    }
+    DENDRITE_TRY(p->staging.upload(s, h, bytes));
+    const int32_t* dargs = (const int32_t*)d;
+    prof_begin(p, T_APPEND_META, s);
+    k_append_meta<<<1, kAppendMetaThreads, 0, s>>>(dargs, n, n_new, bs, p->bpb, (int32_t)p->num_blocks,
+                                                   p->d_table, p->d_refcount,
+                                                   p->d_stack, p->d_holders, p->d_last, p->d_call_i32, p->d_meta);
+    prof_end(p, T_APPEND_META, s);
+    DENDRITE_CUDA(cudaGetLastError());
+    const int32_t row_vec = p->head_dim * p->elt / 16;
+    prof_begin(p, T_APPEND_COPY, s);
+    k_append_copy<<<(unsigned)(touched * p->n_kv), 128, 0, s>>>(
+        dargs, dargs + 2 * n, n, n_new, bs, p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks, p->d_table,
+        p->d_call_i32,
+        (const uint4*)K, (const uint4*)V, (uint4*)p->d_k, (uint4*)p->d_v, p->d_meta);
+    prof_end(p, T_APPEND_COPY, s);
+    DENDRITE_CUDA(cudaGetLastError());
+    DENDRITE_TRY(p->staging.release(s));
+    for (int32_t i = 0; i < n; ++i) {
+        Branch& b = p->br[branches[i]];
+        b.len += n_new;
+        p->nodes[b.node].len = b.len;
+    }
+    p->version++;
+    return DENDRITE_OK;
+}
+
+int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* stream) {
+    DENDRITE_TRY(prelude(p));
+    if (n < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
+    if (n == 0) return DENDRITE_OK;
+    DENDRITE_TRY(check_unique_live(p, branches, n));
+    cudaStream_t s = (cudaStream_t)stream;
+    const int32_t bs = p->block_size;
+    char *h, *d;
+    const size_t bytes = (size_t)n * 8;
+    DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
+    int32_t* a = (int32_t*)h;
+    int64_t total = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        a[i] = branches[i];
+        a[n + i] = (int32_t)total;
+        total += (p->br[branches[i]].len + bs - 1) / bs;
+    }
+    if (total > INT32_MAX) return DENDRITE_ELIMIT;
+    DENDRITE_TRY(p->staging.upload(s, h, bytes));
+    prof_begin(p, T_FREE, s);
+    if (total > 0) {
+        k_free_release<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            (const int32_t*)d, (const int32_t*)d + n, n, (int32_t)total, p->bpb, (int32_t)p->num_blocks,
+            p->d_table, p->d_refcount, p->d_released, p->d_meta);
+        DENDRITE_CUDA(cudaGetLastError());
+        k_free_push<<<1, kFreeCollectThreads, 0, s>>>(p->d_stack, p->d_released, p->d_meta);
+        DENDRITE_CUDA(cudaGetLastError());
+    }
+    prof_end(p, T_FREE, s);
+    DENDRITE_TRY(p->staging.release(s));
+    for (int32_t i = 0; i < n; ++i) {
+        Branch& b = p->br[branches[i]];
+        const int32_t node = b.node;
+        p->nodes[node].handle = -1;
+        b = Branch();
+        p->free_handles.push_back(branches[i]);
+        drop_node_ref(p, node);
+    }
+    p->version++;
+    return DENDRITE_OK;
+}
+
+int dendrite_sync(dendrite_pool* p, void* stream) {
+    if (!p) return DENDRITE_EINVAL;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    int32_t st = 0;
+    DENDRITE_CUDA(cudaMemcpy(&st, &p->d_meta->status, 4, cudaMemcpyDeviceToHost));
+    if (st && !p->poisoned) p->poisoned = st;
+    return p->poisoned;
+}
+
+int dendrite_branch_len(dendrite_pool* p, int32_t branch, int32_t* out_len) {
+    if (!p || !out_len) return DENDRITE_EINVAL;
+    DENDRITE_TRY(check_live(p, branch));
+    *out_len = p->br[branch].len;
+    return DENDRITE_OK;
+}
+
+int dendrite_read_table(dendrite_pool* p, int32_t branch, int32_t* out, int32_t cap, int32_t* n_out,
+                        void* stream) {
+    if (!p || !n_out) return DENDRITE_EINVAL;
+    DENDRITE_TRY(check_live(p, branch));
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    const int32_t nb = (p->br[branch].len + p->block_size - 1) / p->block_size;
+    *n_out = nb;
+    if (nb > cap) return DENDRITE_ELIMIT;
+    if (nb == 0) return DENDRITE_OK;
+    if (!out) return DENDRITE_EINVAL;
+    DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    DENDRITE_CUDA(cudaMemcpy(out, p->d_table + (int64_t)branch * p->bpb, (size_t)nb * 4, cudaMemcpyDeviceToHost));
+    return DENDRITE_OK;
+}
+
+int dendrite_read_refcounts(dendrite_pool* p, int32_t* out, void* stream) {
+    if (!p || !out) return DENDRITE_EINVAL;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    DENDRITE_CUDA(cudaMemcpy(out, p->d_refcount, (size_t)p->num_blocks * 4, cudaMemcpyDeviceToHost));
+    return DENDRITE_OK;
+}
+
+int dendrite_read_free_stack(dendrite_pool* p, int32_t* out, int32_t* top_out, void* stream) {
+    if (!p || !out || !top_out) return DENDRITE_EINVAL;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    DevMeta m;
+    DENDRITE_CUDA(cudaMemcpy(&m, p->d_meta, sizeof(m), cudaMemcpyDeviceToHost));
+    *top_out = m.top;
+    if (m.top < 0 || m.top > p->num_blocks) return DENDRITE_ECORRUPT;
+    if (m.top) DENDRITE_CUDA(cudaMemcpy(out, p->d_stack, (size_t)m.top * 4, cudaMemcpyDeviceToHost));
+    return DENDRITE_OK;
+}
+
+int dendrite_read_block(dendrite_pool* p, int32_t block, void* k_out, void* v_out, void* stream) {
+    if (!p || !k_out || !v_out || block < 0 || block >= p->num_blocks) return DENDRITE_EINVAL;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    const size_t bytes = (size_t)p->n_kv * p->block_size * p->head_dim * p->elt;
+    DENDRITE_CUDA(cudaMemcpy(k_out, (char*)p->d_k + bytes * block, bytes, cudaMemcpyDeviceToHost));
+    DENDRITE_CUDA(cudaMemcpy(v_out, (char*)p->d_v + bytes * block, bytes, cudaMemcpyDeviceToHost));
+    return DENDRITE_OK;
+}
+
+int dendrite_pool_info(dendrite_pool* p, int64_t* num_blocks, int32_t* block_size, int32_t* n_kv_heads,
+                       int32_t* head_dim, int32_t* dtype) {
+    if (!p) return DENDRITE_EINVAL;
+    if (num_blocks) *num_blocks = p->num_blocks;
+    if (block_size) *block_size = p->block_size;
+    if (n_kv_heads) *n_kv_heads = p->n_kv;
+    if (head_dim) *head_dim = p->head_dim;
+    if (dtype) *dtype = p->dtype;
+    return DENDRITE_OK;
+}
+
+int dendrite_set_profiling(dendrite_pool* p, int32_t enable) {
+    if (!p) return DENDRITE_EINVAL;
+    p->profiling = enable != 0;
+    for (int k = 0; k < T_COUNT; ++k) p->ev_recorded[k] = false;
+    return DENDRITE_OK;
+}
+
+int dendrite_last_timings(dendrite_pool* p, float* ms, int32_t n) {
+    if (!p || !ms || n < 0) return DENDRITE_EINVAL;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    for (int32_t k = 0; k < n; ++k) {
+        ms[k] = -1.f;
+        if (k < T_COUNT && p->ev_recorded[k]) {
+            DENDRITE_CUDA(cudaEventSynchronize(p->ev[k][1]));
+            float t = 0;
+            DENDRITE_CUDA(cudaEventElapsedTime(&t, p->ev[k][0], p->ev[k][1]));
+            ms[k] = t;
+        }
+    }
+    return DENDRITE_OK;
+}
+
+}  // extern "C"

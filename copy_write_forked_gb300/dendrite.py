@@ -1,0 +1,285 @@
+"""Thin Python binding of libdendrite.so (argument marshalling only).
+
+Every step of the path (fork, copy-on-write append, planning, attention,
+merge, free) runs inside the C-ABI library and its CUDA kernels; this module
+only turns torch tensors into device pointers and the current torch stream
+into a ``cudaStream_t``.  If the library is missing it raises at import of
+:func:`lib` -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _build
+
+__all__ = ["lib", "Pool", "DendriteError", "ERRORS", "plan_segments", "TIMING_NAMES"]
+
+ERRORS = {
+    -1: "EINVAL", -2: "ENOMEM", -3: "EBADHANDLE", -4: "ELIMIT", -5: "EDTYPE",
+    -6: "ECUDA", -7: "ETIMEOUT", -8: "ECORRUPT",
+}
+TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total")
+FP32, BF16 = 0, 1
+
+_LIB = None
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+_pi32 = ctypes.POINTER(ctypes.c_int32)
+
+
+class DendriteError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        self.name = ERRORS.get(code, str(code))
+        super().__init__(f"dendrite error {self.name} ({code}){': ' + what if what else ''}")
+
+
+class _Opts(ctypes.Structure):
+    _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("reserved", _i32 * 6)]
+
+
+class _PlanStats(ctypes.Structure):
+    _fields_ = [("n_segments", _i32), ("n_units", _i32), ("n_ctas", _i32), ("n_partials", _i32),
+                ("tiles", _i64), ("unique_tiles", _i64), ("plan_us", ctypes.c_double)]
+
+
+class _Segment(ctypes.Structure):
+    _fields_ = [("rep", _i32), ("block_start", _i32), ("block_count", _i32),
+                ("member_offset", _i32), ("n_members", _i32)]
+
+
+_SIGS = {
+    "dendrite_pool_create": [_i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_Opts), ctypes.POINTER(_p)],
+    "dendrite_pool_destroy": [_p],
+    "dendrite_branch_new": [_p, _pi32],
+    "dendrite_fork": [_p, _i32, _i32, _pi32, _p],
+    "dendrite_fork_batch": [_p, _pi32, _pi32, _i32, _pi32, _p],
+    "dendrite_append_kv": [_p, _pi32, _i32, _i32, _p, _p, _p],
+    "dendrite_tree_attn_decode": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
+    "dendrite_free": [_p, _pi32, _i32, _p],
+    "dendrite_sync": [_p, _p],
+    "dendrite_branch_len": [_p, _i32, _pi32],
+    "dendrite_read_table": [_p, _i32, _pi32, _i32, _pi32, _p],
+    "dendrite_read_refcounts": [_p, _pi32, _p],
+    "dendrite_read_free_stack": [_p, _pi32, _pi32, _p],
+    "dendrite_read_block": [_p, _i32, _p, _p, _p],
+    "dendrite_pool_info": [_p, ctypes.POINTER(_i64), _pi32, _pi32, _pi32, _pi32],
+    "dendrite_set_profiling": [_p, _i32],
+    "dendrite_last_timings": [_p, ctypes.POINTER(ctypes.c_float), _i32],
+    "dendrite_last_plan_stats": [_p, ctypes.POINTER(_PlanStats)],
+    "dendrite_plan_segments": [_i32, _pi32, _pi32, _pi32, _i32, _pi32, _i32, ctypes.POINTER(_Segment), _i32,
+                               _pi32, _pi32, _i32, _pi32],
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdendrite.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.dendrite_version.restype = ctypes.c_char_p
+        L.dendrite_version.argtypes = []
+        _LIB = L
+    return _LIB
+
+
+def _check(rc: int, what: str = "") -> None:
+    if rc != 0:
+        raise DendriteError(rc, what)
+
+
+def _arr(xs: Sequence[int]):
+    a = (ctypes.c_int32 * max(1, len(xs)))(*[int(x) for x in xs])
+    return a
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+_DT = {torch.float32: FP32, torch.bfloat16: BF16}
+
+
+class Pool:
+    """A device block pool with copy-on-write branch forking and tree decode attention."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
+                 dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
+                 max_blocks_per_branch: int = 4096, device=None):
+        if dtype not in _DT:
+            raise DendriteError(-5, f"dtype {dtype}")
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
+        opts = _Opts(int(max_branches), int(max_blocks_per_branch))
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(lib().dendrite_pool_create(self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim,
+                                              _DT[dtype], ctypes.byref(opts), ctypes.byref(h)), "pool_create")
+        self._h = h
+
+    # ------------------------------------------------------------ lifetime
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().dendrite_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # --------------------------------------------------------------- ops
+    def new_branch(self) -> int:
+        out = ctypes.c_int32()
+        _check(lib().dendrite_branch_new(self._h, ctypes.byref(out)), "branch_new")
+        return out.value
+
+    def fork(self, parent: int, n_children: int, stream=None) -> List[int]:
+        out = (ctypes.c_int32 * n_children)()
+        _check(lib().dendrite_fork(self._h, int(parent), int(n_children), out, _stream_ptr(stream)), "fork")
+        return list(out)
+
+    def fork_batch(self, parents: Sequence[int], n_children: Sequence[int], stream=None) -> List[List[int]]:
+        total = sum(int(n) for n in n_children)
+        out = (ctypes.c_int32 * max(1, total))()
+        _check(lib().dendrite_fork_batch(self._h, _arr(parents), _arr(n_children), len(parents), out,
+                                         _stream_ptr(stream)), "fork_batch")
+        res, k = [], 0
+        for n in n_children:
+            res.append(list(out[k:k + n]))
+            k += n
+        return res
+
+    def _check_tensor(self, t: torch.Tensor, name: str) -> None:
+        if not t.is_cuda or t.dtype != self.dtype or not t.is_contiguous():
+            raise DendriteError(-1, f"{name} must be a contiguous {self.dtype} CUDA tensor")
+
+    def append_kv(self, branches: Sequence[int], K: torch.Tensor, V: torch.Tensor, stream=None) -> None:
+        """K, V: ``[n_branches][n_new][n_kv_heads][head_dim]``."""
+        self._check_tensor(K, "K")
+        self._check_tensor(V, "V")
+        nb = len(branches)
+        if K.shape != V.shape or K.dim() != 4 or K.shape[0] != nb or K.shape[2] != self.n_kv_heads \
+                or K.shape[3] != self.head_dim:
+            raise DendriteError(-1, f"K/V shape {tuple(K.shape)}")
+        _check(lib().dendrite_append_kv(self._h, _arr(branches), nb, int(K.shape[1]), ctypes.c_void_p(K.data_ptr()),
+                                        ctypes.c_void_p(V.data_ptr()), _stream_ptr(stream)), "append_kv")
+
+    def tree_attn_decode(self, Q: torch.Tensor, branches: Sequence[int], out: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+        """Q: ``[n_branches][q_len][n_q_heads][head_dim]``; returns out of the same shape."""
+        self._check_tensor(Q, "Q")
+        if Q.dim() != 4 or Q.shape[0] != len(branches) or Q.shape[3] != self.head_dim:
+            raise DendriteError(-1, f"Q shape {tuple(Q.shape)}")
+        if out is None:
+            out = torch.empty_like(Q)
+        self._check_tensor(out, "out")
+        if out.shape != Q.shape:
+            raise DendriteError(-1, "out shape")
+        _check(lib().dendrite_tree_attn_decode(self._h, ctypes.c_void_p(Q.data_ptr()), int(Q.shape[2]),
+                                               int(Q.shape[1]), _arr(branches), len(branches),
+                                               ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)),
+               "tree_attn_decode")
+        return out
+
+    def free(self, branches: Sequence[int], stream=None) -> None:
+        _check(lib().dendrite_free(self._h, _arr(branches), len(branches), _stream_ptr(stream)), "free")
+
+    def sync(self, stream=None) -> None:
+        _check(lib().dendrite_sync(self._h, _stream_ptr(stream)), "sync")
+
+    def sync_status(self, stream=None) -> int:
+        """Like :meth:`sync` but returns the status code instead of raising."""
+        return lib().dendrite_sync(self._h, _stream_ptr(stream))
+
+    # -------------------------------------------------------- inspection
+    def branch_len(self, b: int) -> int:
+        out = ctypes.c_int32()
+        _check(lib().dendrite_branch_len(self._h, int(b), ctypes.byref(out)), "branch_len")
+        return out.value
+
+    def read_table(self, b: int, stream=None) -> List[int]:
+        n = ctypes.c_int32()
+        cap = (self.branch_len(b) + self.block_size - 1) // self.block_size
+        buf = (ctypes.c_int32 * max(1, cap))()
+        _check(lib().dendrite_read_table(self._h, int(b), buf, cap, ctypes.byref(n), _stream_ptr(stream)),
+               "read_table")
+        return list(buf[:n.value])
+
+    def read_refcounts(self, stream=None) -> List[int]:
+        buf = (ctypes.c_int32 * self.num_blocks)()
+        _check(lib().dendrite_read_refcounts(self._h, buf, _stream_ptr(stream)), "read_refcounts")
+        return list(buf)
+
+    def read_free_stack(self, stream=None) -> List[int]:
+        buf = (ctypes.c_int32 * self.num_blocks)()
+        top = ctypes.c_int32()
+        _check(lib().dendrite_read_free_stack(self._h, buf, ctypes.byref(top), _stream_ptr(stream)),
+               "read_free_stack")
+        return list(buf[:top.value])
+
+    def read_block(self, blk: int, stream=None):
+        shape = (self.n_kv_heads, self.block_size, self.head_dim)
+        k = torch.empty(shape, dtype=self.dtype)
+        v = torch.empty(shape, dtype=self.dtype)
+        _check(lib().dendrite_read_block(self._h, int(blk), ctypes.c_void_p(k.data_ptr()),
+                                         ctypes.c_void_p(v.data_ptr()), _stream_ptr(stream)), "read_block")
+        return k, v
+
+    # --------------------------------------------------------- profiling
+    def set_profiling(self, enable: bool) -> None:
+        _check(lib().dendrite_set_profiling(self._h, 1 if enable else 0), "set_profiling")
+
+    def last_timings(self) -> dict:
+        buf = (ctypes.c_float * len(TIMING_NAMES))()
+        _check(lib().dendrite_last_timings(self._h, buf, len(TIMING_NAMES)), "last_timings")
+        return {k: (v if v >= 0 else None) for k, v in zip(TIMING_NAMES, buf)}
+
+    def last_plan_stats(self) -> dict:
+        st = _PlanStats()
+        _check(lib().dendrite_last_plan_stats(self._h, ctypes.byref(st)), "last_plan_stats")
+        return {f: getattr(st, f) for f, _ in _PlanStats._fields_}
+
+
+def plan_segments(parent: Sequence[int], fork_len: Sequence[int], length: Sequence[int], block_size: int,
+                  queried: Sequence[int]):
+    """Host planner (no GPU): returns a list of (rep, block_start, block_count, members)."""
+    n = len(parent)
+    ns, nm = ctypes.c_int32(), ctypes.c_int32()
+    L = lib()
+    rc = L.dendrite_plan_segments(n, _arr(parent), _arr(fork_len), _arr(length), block_size, _arr(queried),
+                                  len(queried), None, 0, ctypes.byref(ns), None, 0, ctypes.byref(nm))
+    if rc not in (0, -4):
+        _check(rc, "plan_segments")
+    segs = (_Segment * max(1, ns.value))()
+    mem = (ctypes.c_int32 * max(1, nm.value))()
+    _check(L.dendrite_plan_segments(n, _arr(parent), _arr(fork_len), _arr(length), block_size, _arr(queried),
+                                    len(queried), segs, ns.value, ctypes.byref(ns), mem, nm.value,
+                                    ctypes.byref(nm)), "plan_segments")
+    out = []
+    for s in segs[:ns.value]:
+        out.append((s.rep, s.block_start, s.block_count, list(mem[s.member_offset:s.member_offset + s.n_members])))
+    return out

@@ -1,0 +1,42 @@
+"""Replays a workload script (see :mod:`.workloads`) through the C-ABI library.
+
+Only marshalling: every operation is one library call (fork, append, free),
+and the library returns the handles that logical ids map to."""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from .dendrite import Pool
+
+
+def run_script(pool: Pool, w, device="cuda", stop: Optional[int] = None, stream=None) -> Dict[int, int]:
+    h: Dict[int, int] = {}
+    for idx, op in enumerate(w.ops[:stop]):
+        if op.kind == "new":
+            h[op.branches[0]] = pool.new_branch()
+        elif op.kind == "fork":
+            got = pool.fork_batch([h[p] for p in op.branches], [len(c) for c in op.children], stream=stream)
+            for ch, handles in zip(op.children, got):
+                for logical, handle in zip(ch, handles):
+                    h[logical] = handle
+        elif op.kind == "append":
+            if op.n_new == 0:
+                continue
+            K, V = w.kv(idx, device)
+            pool.append_kv([h[b] for b in op.branches], K, V, stream=stream)
+        elif op.kind == "free":
+            pool.free([h[b] for b in op.branches], stream=stream)
+            for b in op.branches:
+                del h[b]
+    return h
+
+
+def pool_for(w, extra_blocks: int = 16, max_branches: Optional[int] = None, **kw) -> Pool:
+    """A pool sized for workload ``w``."""
+    nb = max(1, w.blocks_upper_bound() + extra_blocks)
+    mb = max_branches or max(16, w.n_branch_ids() + 8)
+    bpb = max(16, max(-(-L // w.block_size) for L in w.lengths().values()) + 4) if w.lengths() else 16
+    return Pool(nb, w.block_size, w.n_kv_heads, w.head_dim, w.dtype, max_branches=mb,
+                max_blocks_per_branch=bpb, **kw)

@@ -1,0 +1,249 @@
+/*
+ * dendrite.h -- C ABI of a copy-on-write, tree-structured paged KV cache with
+ * tree-aware decode attention, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (Dendrite article, ainews.cool "Dendrite: O(1) KV cache forking",
+ * section 技术深度解析; dendrite demo.tape, section "The problem"):
+ *   - KV rows live in fixed-size blocks; each branch has a block table.
+ *   - A fork at token t shares every block of positions 0..t-1 with the
+ *     parent (table copy + refcount increment, no KV copied); the child then
+ *     owns only the leaf blocks it appends.
+ *   - An append into a partially filled tail block that is still shared
+ *     (refcount > 1) first copies that block (copy-on-write).
+ *   - Decode attention walks the tree: keys/values of the shared ancestor path
+ *     and of the branch's own leaf path.  Shared-prefix blocks are streamed
+ *     from HBM once for all descendant queries; partial (max, sum, acc)
+ *     triples are merged with a log-sum-exp step.
+ *
+ * Conventions (all calls):
+ *   - Every call returns an int: DENDRITE_OK (0) or a negative error code.
+ *   - Host-checkable errors (bad argument, bad handle, capacity, dtype) are
+ *     returned immediately and the call changes nothing.
+ *   - Device work is stream-ordered on the caller's stream (a cudaStream_t
+ *     passed as void*; NULL = the legacy default stream).  Calls return before
+ *     the GPU work finishes.
+ *   - Errors found on the device (an exhausted block pool, a wait that timed
+ *     out) are sticky: the offending call's device effects are not applied,
+ *     every later kernel of the pool becomes a no-op, and the error is
+ *     returned by dendrite_sync() and by every call after the host has seen
+ *     it.  A pool in this state can only be inspected and destroyed.
+ *   - A pool is not thread-safe; calls on different streams must be ordered
+ *     by the caller.
+ *
+ * Ownership:
+ *   - The pool owns the KV block storage, refcounts, free stack, block tables
+ *     and its scratch (cudaMalloc'd at create time, plus a grow-only
+ *     attention workspace).
+ *   - The caller owns Q, K, V and out (device pointers).  They must stay valid
+ *     until the stream work of the call has completed.  The library keeps no
+ *     caller pointer after a call returns.
+ *   - Host arrays (branch lists, counts) are read during the call only.
+ *   - Branch handles (int32) are owned by the caller until dendrite_free.
+ */
+#ifndef DENDRITE_H
+#define DENDRITE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------- error codes */
+#define DENDRITE_OK           0
+#define DENDRITE_EINVAL      -1  /* bad argument (size, layout, duplicate branch, ...) */
+#define DENDRITE_ENOMEM      -2  /* block pool exhausted (found on the device; sticky) */
+#define DENDRITE_EBADHANDLE  -3  /* handle not live */
+#define DENDRITE_ELIMIT      -4  /* branch count or per-branch table capacity exceeded */
+#define DENDRITE_EDTYPE      -5  /* unsupported dtype / head_dim / block_size combination */
+#define DENDRITE_ECUDA       -6  /* a CUDA runtime call failed */
+#define DENDRITE_ETIMEOUT    -7  /* a bounded device wait gave up (sticky) */
+#define DENDRITE_ECORRUPT    -8  /* device metadata inconsistent (refcount underflow; sticky) */
+
+/* ------------------------------------------------------------------ dtypes */
+#define DENDRITE_FP32  0   /* fp32 K/V/Q/out; attention in fp32 FMA (no TF32)          */
+#define DENDRITE_BF16  1   /* bf16 K/V/Q/out; attention on tensor cores, fp32 accumulate */
+
+typedef struct dendrite_pool dendrite_pool;
+
+/* Optional pool settings; pass NULL for defaults. */
+typedef struct dendrite_pool_opts {
+    int32_t max_branches;          /* live handles at once (default 4096)                 */
+    int32_t max_blocks_per_branch; /* block-table row length (default 4096 = 64K tokens)  */
+    int32_t reserved[6];           /* must be zero                                         */
+} dendrite_pool_opts;
+
+/*
+ * Create a block pool.
+ *   num_blocks  > 0: number of KV blocks.
+ *   block_size  tokens per block; 16 (the attention kernels' tile height).
+ *   n_kv_heads  KV heads per token (1..64).
+ *   head_dim    bf16: 128.  fp32: a multiple of 32, at most 256.
+ *   dtype       DENDRITE_FP32 or DENDRITE_BF16.
+ * Device layout: K and V pools are [num_blocks][n_kv_heads][block_size][head_dim]
+ * (one (block, head) tile is contiguous); refcount int32[num_blocks]; the free
+ * stack int32[num_blocks] starts as [num_blocks-1, ..., 0] so block 0 is handed
+ * out first; block tables int32[max_branches][max_blocks_per_branch] (-1 = empty).
+ * Synchronous.  Uses the current CUDA device.
+ */
+int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads,
+                         int32_t head_dim, int32_t dtype, const dendrite_pool_opts* opts,
+                         dendrite_pool** out);
+
+/* Synchronises the device, then releases everything the pool owns. */
+int dendrite_pool_destroy(dendrite_pool* pool);
+
+/* New empty root branch (length 0).  Host only: no device work. */
+int dendrite_branch_new(dendrite_pool* pool, int32_t* out_branch);
+
+/*
+ * Fork: n_children new branches that share every block of `parent`
+ * (Dendrite article, section 技术深度解析: a fork at t keeps positions 0..t-1
+ * shared and gives each branch an empty leaf for positions >= t).
+ * On the device: each child's table row is a copy of the parent's
+ * ceil(len/block_size) entries and each of those blocks gains n_children
+ * references.  No KV is copied.  The parent stays live and unchanged.
+ * out_children: host int32[n_children], written before the call returns.
+ */
+int dendrite_fork(dendrite_pool* pool, int32_t parent, int32_t n_children,
+                  int32_t* out_children, void* stream);
+
+/*
+ * Batched fork: parent i gets n_children[i] children, written in order to
+ * out_children (host int32[sum n_children]).  One kernel launch for the whole
+ * batch.  A parent may appear more than once.
+ */
+int dendrite_fork_batch(dendrite_pool* pool, const int32_t* parents, const int32_t* n_children,
+                        int32_t n_parents, int32_t* out_children, void* stream);
+
+/*
+ * Append n_new tokens to every branch in `branches` (host int32[n_branches],
+ * no duplicates).  K, V: device, [n_branches][n_new][n_kv_heads][head_dim] in
+ * the pool dtype, contiguous.
+ * Copy-on-write (dendrite demo.tape, section "The problem"): a branch whose
+ * tail block is partially filled copies the tail's valid slots into a fresh
+ * block first iff the tail's refcount is above 1 at its turn; the branches of
+ * one call are served as if one after the other in argument order.  New blocks
+ * come off the free stack in argument order, copy first, then in position
+ * order.  All-or-nothing: if the pool has too few free blocks the call
+ * applies nothing and the pool reports DENDRITE_ENOMEM (sticky).
+ * n_new == 0 is a no-op.
+ */
+int dendrite_append_kv(dendrite_pool* pool, const int32_t* branches, int32_t n_branches,
+                       int32_t n_new, const void* K, const void* V, void* stream);
+
+/*
+ * Tree decode attention (Dendrite article, section 技术深度解析: attention
+ * gathers keys and values from the shared ancestor path and the branch's own
+ * leaf path).
+ *   Q:   device, [n_branches][q_len][n_q_heads][head_dim], pool dtype.
+ *   out: device, same shape and dtype (written).
+ *   n_q_heads: a multiple of n_kv_heads; query head h reads KV head h / (n_q_heads / n_kv_heads).
+ *   q_len >= 1: the queries are the branch's last q_len positions; query j sees
+ *        positions <= len - q_len + j.  Every branch needs len >= q_len.
+ * out = softmax(q K^T / sqrt(head_dim)) V per query row.  Blocks shared by
+ * several queried branches are read from HBM once for all of them (split-KV
+ * partials, then a log-sum-exp merge).  The plan built from the branch tree is
+ * cached until the tree changes.  `branches` may not hold duplicates.
+ */
+int dendrite_tree_attn_decode(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,
+                              const int32_t* branches, int32_t n_branches, void* out, void* stream);
+
+/*
+ * Free branches (host int32[n_branches], no duplicates): every block of each
+ * table loses one reference; blocks that reach zero are pushed on the free
+ * stack in descending id order (so one call that frees everything restores
+ * the initial stack).  Handles become invalid at once.
+ */
+int dendrite_free(dendrite_pool* pool, const int32_t* branches, int32_t n_branches, void* stream);
+
+/* Wait for the pool's work on `stream`, then return its sticky device status. */
+int dendrite_sync(dendrite_pool* pool, void* stream);
+
+/* ------------------------------------------------------------ inspection
+ * Synchronous helpers for tests and tools (they synchronise `stream`).     */
+
+/* Current length (tokens) of a live branch (host mirror; no device work). */
+int dendrite_branch_len(dendrite_pool* pool, int32_t branch, int32_t* out_len);
+
+/* Copy the first ceil(len/block_size) table entries of `branch` to host
+ * int32 out[cap]; *n_out receives the count. */
+int dendrite_read_table(dendrite_pool* pool, int32_t branch, int32_t* out, int32_t cap,
+                        int32_t* n_out, void* stream);
+
+/* Copy refcount[0..num_blocks) to host int32 out[num_blocks]. */
+int dendrite_read_refcounts(dendrite_pool* pool, int32_t* out, void* stream);
+
+/* Copy the live part of the free stack (bottom to top) to host int32
+ * out[num_blocks]; *top_out receives its size. */
+int dendrite_read_free_stack(dendrite_pool* pool, int32_t* out, int32_t* top_out, void* stream);
+
+/* Copy one block's K and V ([n_kv_heads][block_size][head_dim], pool dtype)
+ * to host buffers k_out / v_out. */
+int dendrite_read_block(dendrite_pool* pool, int32_t block, void* k_out, void* v_out, void* stream);
+
+/* Pool geometry: num_blocks, block_size, n_kv_heads, head_dim, dtype. */
+int dendrite_pool_info(dendrite_pool* pool, int64_t* num_blocks, int32_t* block_size,
+                       int32_t* n_kv_heads, int32_t* head_dim, int32_t* dtype);
+
+/* ------------------------------------------------------------ profiling
+ * When enabled, each call records CUDA events around each of its kernels on
+ * the caller's stream.  dendrite_last_timings() synchronises on them and
+ * returns the device milliseconds of the most recent call of each kind:
+ *   ms[0] fork, ms[1] append metadata, ms[2] append copy/scatter,
+ *   ms[3] attention partials, ms[4] attention merge, ms[5] free (both phases),
+ *   ms[6] whole attention call (partials + merge).
+ * Entries with no recorded call are set to -1.                                */
+#define DENDRITE_N_TIMINGS 7
+int dendrite_set_profiling(dendrite_pool* pool, int32_t enable);
+int dendrite_last_timings(dendrite_pool* pool, float* ms, int32_t n);
+
+/* Attention plan statistics of the most recent dendrite_tree_attn_decode call. */
+typedef struct dendrite_plan_stats {
+    int32_t n_segments;     /* shared + private block ranges planned               */
+    int32_t n_units;        /* (segment, kv head, row group) work units            */
+    int32_t n_ctas;         /* CTAs of the partial kernel                           */
+    int32_t n_partials;     /* partial triples written                              */
+    int64_t tiles;          /* (block, kv head) tiles streamed by the partial kernel */
+    int64_t unique_tiles;   /* distinct (block, kv head) tiles among them            */
+    double  plan_us;        /* host time spent building the plan (0 if cached)      */
+} dendrite_plan_stats;
+int dendrite_last_plan_stats(dendrite_pool* pool, dendrite_plan_stats* out);
+
+/* ------------------------------------------------------------ planner
+ * The sharing planner as a pure host function (no pool, no GPU), used by the
+ * attention call and exposed for tests.
+ * Tree: node i has parent[i] (-1 for a root) and fork_len[i] (the parent's
+ * length when i was forked; 0 for a root); len[i] is its current length.
+ * For the queried nodes it returns the segments: maximal ranges of logical
+ * blocks that a fixed set of queried branches reads from the same physical
+ * blocks.  Only blocks that were full at every fork on the way are shared; a
+ * partial block at a fork point counts as the child's own.
+ * segs[k] = {rep, block_start, block_count, member_offset, n_members}:
+ * members[member_offset .. +n_members) are indices into `queried`, and rep is
+ * a member whose table holds the segment.  Segment order: by owner node in
+ * first-visit order, then by block_start.
+ * Returns DENDRITE_ELIMIT if seg_cap or member_cap is too small (the needed
+ * sizes are still written to *n_segs / *n_members).
+ */
+typedef struct dendrite_segment {
+    int32_t rep;
+    int32_t block_start;
+    int32_t block_count;
+    int32_t member_offset;
+    int32_t n_members;
+} dendrite_segment;
+
+int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                           const int32_t* len, int32_t block_size,
+                           const int32_t* queried, int32_t n_queried,
+                           dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
+                           int32_t* members, int32_t member_cap, int32_t* n_members);
+
+/* Library version string. */
+const char* dendrite_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DENDRITE_H */

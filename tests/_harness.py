@@ -1,0 +1,84 @@
+"""Helpers shared by the GPU parity tests: run a workload through the C-ABI
+library and build the oracle's view of the same seeded inputs."""
+from __future__ import annotations
+
+from typing import Dict, Iterable, List, Set
+
+import numpy as np
+import torch
+
+from copy_write_forked_gb300 import workloads as W
+from copy_write_forked_gb300.runner import pool_for, run_script
+from oracle import KVTree
+from oracle.block_pool import bits_of
+
+
+def ancestors(w, ids: Iterable[int]) -> Set[int]:
+    par = {}
+    for op in w.ops:
+        if op.kind == "fork":
+            for p, ch in zip(op.branches, op.children):
+                for c in ch:
+                    par[c] = p
+    out = set()
+    for b in ids:
+        while b is not None and b not in out:
+            out.add(b)
+            b = par.get(b)
+    return out
+
+
+def oracle_tree(w, ids: Iterable[int], device="cpu") -> KVTree:
+    """O1 tree holding only the ancestor chains of ``ids``; each append slice
+    is regenerated from its own seed on ``device`` (the values the GPU got)."""
+    keep = ancestors(w, ids)
+    tree = KVTree(w.n_kv_heads, w.head_dim)
+    for idx, op in enumerate(w.ops):
+        if op.kind == "new" and op.branches[0] in keep:
+            tree.new_root(op.branches[0])
+        elif op.kind == "fork":
+            for p, ch in zip(op.branches, op.children):
+                if p in keep:
+                    tree.fork(p, [c for c in ch if c in keep])
+        elif op.kind == "append" and op.n_new:
+            for pos, b in enumerate(op.branches):
+                if b in keep:
+                    k, v = w.kv_one(idx, pos, device)
+                    tree.append(b, k.cpu(), v.cpu())
+    return tree
+
+
+def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device="cuda") -> float:
+    """Max |GPU - oracle| over the sampled query positions (indices into w.query)."""
+    ids = [w.query[i] for i in sample]
+    tree = oracle_tree(w, ids, device)
+    worst = 0.0
+    for i in sample:
+        q = w.q_one(i, device).cpu()
+        ref = tree.attend(w.query[i], q)
+        got = out[i].double().cpu().numpy()
+        assert np.isfinite(got).all()
+        err = float(np.abs(got - ref).max())
+        worst = max(worst, err)
+        assert err <= tol, (w.name, i, err)
+    return worst
+
+
+def pool_state_matches(pool, h: Dict[int, int], ref, check_bytes=True) -> None:
+    """Bit-exact comparison of the device pool against the O2 model."""
+    for b, tab in ref.table.items():
+        assert pool.read_table(h[b]) == tab, ("table", b)
+    assert pool.read_refcounts() == ref.refcount.tolist()
+    assert pool.read_free_stack() == ref.free_stack()
+    if not check_bytes:
+        return
+    valid = {}
+    for b, tab in ref.table.items():
+        for pos in range(ref.len[b]):
+            valid.setdefault(tab[pos // ref.bs], set()).add(pos % ref.bs)
+    for blk, slots in valid.items():
+        k, v = pool.read_block(blk)
+        kb, vb = bits_of(k), bits_of(v)
+        sl = sorted(slots)
+        assert np.array_equal(kb[:, sl], ref.K[blk][:, sl]), ("K bytes", blk)
+        assert np.array_equal(vb[:, sl], ref.V[blk][:, sl]), ("V bytes", blk)

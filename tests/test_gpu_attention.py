@@ -1,0 +1,114 @@
+"""Tree decode attention through the C-ABI library against the fp64 oracle,
+element by element: fp32 pools within 1e-5, bf16 pools within 5e-3 (max abs
+error; inputs ~ N(0, 1), fp32 accumulation, output rounded to bf16)."""
+import numpy as np
+import pytest
+import torch
+
+from copy_write_forked_gb300 import workloads as W
+from copy_write_forked_gb300.dendrite import Pool
+from copy_write_forked_gb300.runner import pool_for, run_script
+
+from _harness import check_attention
+
+pytestmark = pytest.mark.gpu
+TOL_BF16 = 5e-3
+TOL_F32 = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+    torch.cuda.set_device(0)
+
+
+def run_and_check(w, tol, sample=None):
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    Q = w.q("cuda")
+    out = pool.tree_attn_decode(Q, [h[b] for b in w.query])
+    pool.sync()
+    idx = list(range(len(w.query))) if sample is None else sample
+    err = check_attention(w, out, idx, tol)
+    stats = pool.last_plan_stats()
+    pool.close()
+    return err, stats
+
+
+@pytest.mark.parametrize("variant", ["a", "b", "c"])
+def test_tiny_fp32(variant):
+    run_and_check(W.tiny_cow(variant), TOL_F32)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_trees_fp32(seed):
+    q_len = 1 + seed % 3
+    w = W.random_script(seed, n_ops=30, max_live=8, max_append=70, n_kv=2, n_q=4, d=64, bs=16,
+                        q_len=q_len, seed=seed)
+    run_and_check(w, TOL_F32)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_trees_bf16(seed):
+    q_len = 1 + seed % 4
+    w = W.random_script(seed, n_ops=30, max_live=8, max_append=90, n_kv=2, n_q=8, d=128, bs=16,
+                        dtype=torch.bfloat16, q_len=q_len, seed=seed)
+    run_and_check(w, TOL_BF16)
+
+
+def test_beam_small_ragged():
+    # ragged prefix and leaves: partial blocks at the fork point and at every tail
+    w = W.beam(requests=3, prefix=211, width=4, divergent=37)
+    err, st = run_and_check(w, TOL_BF16)
+    assert st["n_segments"] == 3 + 12
+
+
+def test_wide_fork_spans_row_groups():
+    # 20 branches x G=4 = 80 rows per KV head: row groups of 64 and 16
+    w = W.beam(requests=2, prefix=300, width=20, divergent=5)
+    run_and_check(w, TOL_BF16)
+
+
+def test_gqa_group_8_and_group_1():
+    for n_kv, n_q in ((2, 16), (8, 8)):
+        w = W.beam(requests=2, prefix=150, width=3, divergent=20, n_kv=n_kv, n_q=n_q)
+        run_and_check(w, TOL_BF16)
+
+
+def test_mcts_small():
+    w = W.mcts(root=256, iters=60, width=4, per_node=32, max_depth=6)
+    run_and_check(w, TOL_BF16)
+
+
+def test_spec_verify_small_causal():
+    w = W.spec_verify(requests=3, prefix=500, paths=3, draft=8)
+    run_and_check(w, TOL_BF16)
+
+
+def test_child_with_no_new_tokens_and_single_token_branch():
+    ops = [W.Op("new", (0,)), W.Op("append", (0,), 1), W.Op("new", (1,)), W.Op("append", (1,), 45),
+           W.Op("fork", (1,), children=((2, 3),)), W.Op("append", (3,), 2)]
+    w = W.Workload("edge", 2, 4, 128, 16, torch.bfloat16, ops, (0, 1, 2, 3))
+    run_and_check(w, TOL_BF16)
+
+
+def test_repeated_calls_reuse_the_plan_and_agree():
+    w = W.beam(requests=2, prefix=333, width=4, divergent=21)
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    Q = w.q("cuda")
+    br = [h[b] for b in w.query]
+    o1 = pool.tree_attn_decode(Q, br).clone()
+    assert pool.last_plan_stats()["plan_us"] > 0
+    o2 = pool.tree_attn_decode(Q, br)
+    assert pool.last_plan_stats()["plan_us"] == 0
+    assert torch.equal(o1, o2)
+    pool.close()
+
+
+def test_attention_after_free_of_shared_parent():
+    ops = [W.Op("new", (0,)), W.Op("append", (0,), 100), W.Op("fork", (0,), children=((1, 2),)),
+           W.Op("free", (0,)), W.Op("append", (1, 2), 30)]
+    w = W.Workload("orphans", 2, 4, 128, 16, torch.bfloat16, ops, (1, 2))
+    run_and_check(w, TOL_BF16)
