@@ -71,7 +71,11 @@ def read_peaks():
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi (every 50 ms)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -81,21 +85,21 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu),
-                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc:
@@ -104,26 +108,31 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+            self.proc = None
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    def summary(self, t0: float, t1: float):
+        """Samples received in [t0, t1 + 0.1 s]; if none, the two nearest."""
+        time.sleep(0.12)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for ts, ln in list(self.lines):
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 7:
+            if len(f) < 8:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
+                rows.append((ts, float(f[1]), float(f[2]), f[4:8]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.1]
+        window = "timed region"
+        if not inside and rows:
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
 
 
 # ------------------------------------------------------------ workload
@@ -173,10 +182,15 @@ def run_ours(args):
     Kd, Vd = w.kv(div_idx, dev)            # divergent tokens of the 32 branches, resident
     Q = w.q(dev)
     out = torch.empty_like(Q)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    pool.set_profiling(True)
     pool.sync()
+
+    flush_r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        # read-only pass over 256 MiB (2x L2): evicts the cache and leaves it
+        # holding clean lines, so no write-back lands inside the next step
+        flush_r.max()
 
     def step():
         kids = pool.fork_batch(roots, [Wd] * R)
@@ -186,39 +200,54 @@ def run_ours(args):
         pool.free(br)
         return br
 
+    clk = ClockSampler(local).__enter__()
+    pool.set_profiling(False)
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2()
         step()
     pool.sync()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
+    # ---- timed region: K steps enqueued back to back, one event pair per step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
-                            "attn_total")}
-    plan_us = []
+    t_clk0 = time.time()
     wall0 = time.perf_counter()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(1)
-            ev[i][0].record(stream)
-            br = step()
-            ev[i][1].record(stream)
-            st = pool.last_plan_stats()
-            plan_us.append(st["plan_us"])
-            tm = pool.last_timings()
-            for k in kern:
-                if tm.get(k) is not None:
-                    kern[k].append(tm[k])
-        torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    t_clk1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.summary(t_clk0, t_clk1)
+    clk.__exit__(None, None, None)
     pool.sync()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
     ms = max_over_ranks(ms, world, dev)
     n_queries = len(w.query)
     value = world * n_queries / (ms / 1e3)
+
+    # ---- per-kernel device times (profiling events inside the library; one
+    # synchronised step at a time so the events of each call can be read)
+    pool.set_profiling(True)
+    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
+                            "attn_total")}
+    plan_us = []
+    for i in range(min(args.steps, 100)):
+        flush_l2()
+        step()
+        tm = pool.last_timings()
+        plan_us.append(pool.last_plan_stats()["plan_us"])
+        for k in kern:
+            if tm.get(k) is not None:
+                kern[k].append(tm[k])
+    pool.set_profiling(False)
 
     # roofline of the attention partial kernel
     unique_kv = w.unique_kv_bytes()
@@ -245,19 +274,18 @@ def run_ours(args):
         pool.free(br)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2()
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        flush_l2()
+        e2e_ev[i][0].record(stream)
         e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e = max_over_ranks(statistics.mean(e2e_ms), world, dev)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
     h2d = (Kh.numel() + Vh.numel() + Qh.numel()) * 2
     d2h = outh.numel() * 2
 
@@ -269,7 +297,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
 
-    gpu_launches = 7 * args.steps   # fork 1 + append 2 + attention 2 + free 2 per step
+    gpu_launches = 7 * args.steps   # fork 1 + append 2 + attention 2 + free 2 per timed step
     line = {
         "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
         "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
@@ -283,7 +311,7 @@ def run_ours(args):
         "e2e": {"value": world * n_queries / (e2e / 1e3), "unit": "branch-queries/s", "ms_per_step": e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "kernels_ms": {k: (statistics.mean(v) if v else None) for k, v in kern.items()},
         "attn_branch_queries_per_s": n_queries / (statistics.mean(kern["attn_total"]) / 1e3),
         "plan": {"segments": plan["n_segments"], "units": plan["n_units"], "ctas": plan["n_ctas"],
@@ -300,29 +328,46 @@ def run_ours(args):
 
 
 def fork_latency(dev, reps=200):
-    """Batched fork of a chain of `depth` blocks with a half-full tail:
-    device time of the fork kernel and host time of the API call."""
+    """Fork of a chain of `depth` blocks whose tail block is half full, with 1
+    and 4 children (then freed).  Three views per call: the host time of the C
+    call, the device time between events recorded around the launch, and the
+    round trip (call + stream synchronisation)."""
+    import ctypes
     import torch
-    from copy_write_forked_gb300.dendrite import Pool
+    from copy_write_forked_gb300.dendrite import Pool, lib
+    L = lib()
     res = {}
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
     for depth in (1, 10, 50, 100, 500):
-        L = depth * 16 - 8
+        n = depth * 16 - 8
         pool = Pool(depth + 64, 16, 8, 128, torch.bfloat16, max_branches=16, max_blocks_per_branch=depth + 4)
         r = pool.new_branch()
-        K = torch.zeros(1, L, 8, 128, dtype=torch.bfloat16, device=dev)
+        K = torch.zeros(1, n, 8, 128, dtype=torch.bfloat16, device=dev)
         pool.append_kv([r], K, K)
-        pool.set_profiling(True)
         pool.sync()
         for nc in (1, 4):
-            gpu, host = [], []
+            out = (ctypes.c_int32 * nc)()
+            host, gpu, rt = [], [], []
             for i in range(reps):
+                pool.set_profiling(i % 2 == 1)
+                stream.synchronize()
                 t0 = time.perf_counter()
-                kids = pool.fork(r, nc)
-                host.append((time.perf_counter() - t0) * 1e6)
-                gpu.append(pool.last_timings()["fork"] * 1e3)
-                pool.free(kids)
-            res[f"depth{depth}_children{nc}"] = {"gpu_us_median": statistics.median(gpu[10:]),
-                                                  "host_call_us_median": statistics.median(host[10:])}
+                rc = L.dendrite_fork(pool._h, r, nc, out, sp)
+                t1 = time.perf_counter()
+                stream.synchronize()
+                t2 = time.perf_counter()
+                assert rc == 0
+                if i % 2 == 1:
+                    gpu.append(pool.last_timings()["fork"] * 1e3)
+                else:
+                    host.append((t1 - t0) * 1e6)
+                    rt.append((t2 - t0) * 1e6)
+                pool.free(list(out))
+            res[f"depth{depth}_children{nc}"] = {
+                "host_call_us": statistics.median(host[5:]),
+                "gpu_event_us": statistics.median(gpu[5:]),
+                "round_trip_us": statistics.median(rt[5:])}
         pool.close()
     return res
 
@@ -393,9 +438,13 @@ def run_reference(args):
     ids = list(w.query[:4])
     Q = [w.q_one(i) for i in range(4)]
 
+    k = [0]
+
     def step():
-        for j in range(4):
-            tree.attend(ids[j], Q[j])
+        # one branch query (round robin over the 4 branches of request 0)
+        j = k[0] % 4
+        tree.attend(ids[j], Q[j])
+        k[0] += 1
 
     for _ in range(args.warmup):
         step()
@@ -405,7 +454,7 @@ def run_reference(args):
         step()
         t.append(time.perf_counter() - t0)
     ms = statistics.mean(t) * 1e3
-    value = 4 / (ms / 1e3)
+    value = 1 / (ms / 1e3)
     line = {"impl": "reference",
             "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
             "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
@@ -413,7 +462,8 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
             "config": dict(config_of(w), parallelism="single thread"),
             "cpu_baseline": {"value": value, "unit": "branch-queries/s", "cores": 1, "kind": "oracle",
-                             "sample": "per step: fp64 tree attention of the 4 branches of request 0"},
+                             "sample": "per step: fp64 tree attention (materialise + softmax(qK^T/sqrt(d))V, "
+                                       "32 heads) of one 4352-token branch of request 0, single thread"},
             "e2e": {"value": value, "unit": "branch-queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -421,8 +471,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -143,6 +143,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ float bf16_pair_sum(uint32_t v) {
+    return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
+}
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -344,17 +347,23 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 const float al0 = exp2f(m0 - u0s), al1 = exp2f(m1 - u1s);
                 m0 = n0;
                 m1 = n1;
-                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         s[nt][e] = exp2f(s[nt][e] - u0s);
                         s[nt][2 + e] = exp2f(s[nt][2 + e] - u1s);
-                        ps0 += s[nt][e];
-                        ps1 += s[nt][2 + e];
                     }
                 }
+                // P goes to the tensor cores in bf16; the row sums use the same
+                // rounded weights so numerator and denominator stay consistent
+                uint32_t pa[4];
+                pa[0] = pack_bf16(s[0][0], s[0][1]);
+                pa[1] = pack_bf16(s[0][2], s[0][3]);
+                pa[2] = pack_bf16(s[1][0], s[1][1]);
+                pa[3] = pack_bf16(s[1][2], s[1][3]);
+                const float ps0 = bf16_pair_sum(pa[0]) + bf16_pair_sum(pa[2]);
+                const float ps1 = bf16_pair_sum(pa[1]) + bf16_pair_sum(pa[3]);
                 l0 = l0 * al0 + ps0;
                 l1 = l1 * al1 + ps1;
 #pragma unroll
@@ -365,11 +374,6 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     o[n][3] *= al1;
                 }
                 // O += P V
-                uint32_t pa[4];
-                pa[0] = pack_bf16(s[0][0], s[0][1]);
-                pa[1] = pack_bf16(s[0][2], s[0][3]);
-                pa[2] = pack_bf16(s[1][0], s[1][1]);
-                pa[3] = pack_bf16(s[1][2], s[1][3]);
                 {
                     const int mi = lane >> 3;
                     const int tok = (mi & 1) * 8 + (lane & 7);
@@ -608,6 +612,14 @@ struct HostPlan {
     int64_t tiles = 0, unique_tiles = 0;
     int32_t n_segments = 0;
     size_t partial_rows = 0;
+    std::vector<int32_t> parent, fork_len, len, queried, members, count, fill;
+    std::vector<Segment> segs;
+    void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
+        units.clear(); rows.clear(); cta_begin.clear(); cta_unit.clear(); csr_ptr.clear(); csr_idx.clear();
+        tiles = unique_tiles = 0;
+        n_segments = 0;
+        partial_rows = 0;
+    }
 };
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -617,15 +629,19 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     const int32_t G = nq / p->n_kv;
     const int max_rows = p->dtype == DENDRITE_BF16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
     const int32_t n_nodes = (int32_t)p->nodes.size();
-    std::vector<int32_t> parent(n_nodes), fork_len(n_nodes), len(n_nodes), queried(n);
+    std::vector<int32_t>&parent = hp.parent, &fork_len = hp.fork_len, &len = hp.len, &queried = hp.queried;
+    parent.resize(n_nodes);
+    fork_len.resize(n_nodes);
+    len.resize(n_nodes);
+    queried.resize(n);
     for (int32_t i = 0; i < n_nodes; ++i) {
         parent[i] = p->nodes[i].parent;
         fork_len[i] = p->nodes[i].fork_len;
         len[i] = p->nodes[i].len;
     }
     for (int32_t i = 0; i < n; ++i) queried[i] = p->br[branches[i]].node;
-    std::vector<Segment> segs;
-    std::vector<int32_t> members;
+    std::vector<Segment>& segs = hp.segs;
+    std::vector<int32_t>& members = hp.members;
     plan_segments(n_nodes, parent.data(), fork_len.data(), len.data(), p->block_size, queried.data(), n, segs,
                   members);
     hp.n_segments = (int32_t)segs.size();
@@ -696,7 +712,8 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     }
     // partial rows per unit chunk, and the merge lists
     const int32_t n_out = n * q_len * nq;
-    std::vector<int32_t> count(n_out, 0);
+    std::vector<int32_t>& count = hp.count;
+    count.assign(n_out, 0);
     size_t prow = 0;
     for (AttnUnit& U : hp.units) {
         const int32_t cf = cta_of(U.tile_off), cl = cta_of(U.tile_off + U.n_blk - 1);
@@ -713,7 +730,8 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     hp.csr_ptr.assign(n_out + 1, 0);
     for (int32_t o = 0; o < n_out; ++o) hp.csr_ptr[o + 1] = hp.csr_ptr[o] + count[o];
     hp.csr_idx.assign(hp.csr_ptr[n_out], 0);
-    std::vector<int32_t> fill(hp.csr_ptr.begin(), hp.csr_ptr.end() - 1);
+    std::vector<int32_t>& fill = hp.fill;
+    fill.assign(hp.csr_ptr.begin(), hp.csr_ptr.end() - 1);
     for (const AttnUnit& U : hp.units) {
         const int32_t cl = cta_of(U.tile_off + U.n_blk - 1);
         for (int32_t c = U.cfirst; c <= cl; ++c) {
@@ -850,7 +868,8 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
                      (int32_t)pc.branches.size() == n && std::equal(branches, branches + n, pc.branches.begin());
     if (!hit) {
         const auto t0 = std::chrono::steady_clock::now();
-        HostPlan hp;
+        static thread_local HostPlan hp;
+        hp.clear();
         DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, hp));
         const int32_t C = (int32_t)hp.cta_unit.size();
         const int32_t n_out = n * q_len * n_q_heads;

@@ -31,10 +31,13 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
                    std::vector<Segment>& segs, std::vector<int32_t>& members) {
     segs.clear();
     members.clear();
-    struct Rec { int32_t member; int32_t cap; };
-    std::vector<int32_t> order;                 // owner nodes in first-visit order
-    std::vector<int32_t> slot(n_nodes, -1);     // owner node -> index into recs
-    std::vector<std::vector<Rec>> recs;
+    struct Rec { int32_t grp, cap, member; };
+    static thread_local std::vector<int32_t> slot, order, mem;
+    static thread_local std::vector<Rec> recs;
+    slot.assign(n_nodes, -1);
+    order.clear();
+    recs.clear();
+    // walk every queried branch up to its root: owner node -> [start, cap)
     for (int32_t qi = 0; qi < n_queried; ++qi) {
         int32_t node = queried[qi];
         int32_t cap = (len[node] + bs - 1) / bs;
@@ -42,44 +45,50 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
             const int32_t start = parent[node] >= 0 ? fork_len[node] / bs : 0;
             if (start < cap) {
                 if (slot[node] < 0) {
-                    slot[node] = (int32_t)recs.size();
-                    recs.emplace_back();
+                    slot[node] = (int32_t)order.size();
                     order.push_back(node);
                 }
-                recs[slot[node]].push_back({qi, cap});
+                recs.push_back({slot[node], cap, qi});
             }
             if (parent[node] < 0) break;
             cap = std::min(cap, start);
             node = parent[node];
         }
     }
-    for (int32_t node : order) {
-        std::vector<Rec>& r = recs[slot[node]];
+    // group by owner (first-visit order), caps descending
+    std::sort(recs.begin(), recs.end(), [](const Rec& a, const Rec& b) {
+        if (a.grp != b.grp) return a.grp < b.grp;
+        if (a.cap != b.cap) return a.cap > b.cap;
+        return a.member < b.member;
+    });
+    for (size_t g0 = 0; g0 < recs.size();) {
+        size_t g1 = g0;
+        while (g1 < recs.size() && recs[g1].grp == recs[g0].grp) ++g1;
+        const int32_t node = order[recs[g0].grp];
         const int32_t start = parent[node] >= 0 ? fork_len[node] / bs : 0;
-        // caps ascending; members of [c_k, c_{k+1}) are those with cap >= c_{k+1}
-        std::stable_sort(r.begin(), r.end(), [](const Rec& a, const Rec& b) { return a.cap > b.cap; });
-        std::vector<int32_t> caps;
-        for (const Rec& x : r)
-            if (caps.empty() || caps.back() != x.cap) caps.push_back(x.cap);
-        std::reverse(caps.begin(), caps.end());   // ascending
+        // ascending cuts: the smallest cap first; members of [lo, cut) are the
+        // records with cap >= cut, i.e. a prefix of the group
         int32_t lo = start;
-        for (int32_t cut : caps) {
-            if (cut <= lo) continue;
-            Segment s;
-            s.block_start = lo;
-            s.block_count = cut - lo;
-            s.member_offset = (int32_t)members.size();
-            // members: every record whose cap reaches `cut`, in query order
-            std::vector<int32_t> mem;
-            for (const Rec& x : r)
-                if (x.cap >= cut) mem.push_back(x.member);
-            std::sort(mem.begin(), mem.end());
-            members.insert(members.end(), mem.begin(), mem.end());
-            s.n_members = (int32_t)mem.size();
-            s.rep_node = queried[mem.front()];
-            segs.push_back(s);
-            lo = cut;
+        size_t end = g1;
+        while (end > g0) {
+            const int32_t cut = recs[end - 1].cap;
+            if (cut > lo) {
+                Segment sg;
+                sg.block_start = lo;
+                sg.block_count = cut - lo;
+                sg.member_offset = (int32_t)members.size();
+                mem.clear();
+                for (size_t k = g0; k < end; ++k) mem.push_back(recs[k].member);
+                std::sort(mem.begin(), mem.end());
+                members.insert(members.end(), mem.begin(), mem.end());
+                sg.n_members = (int32_t)mem.size();
+                sg.rep_node = queried[mem.front()];
+                segs.push_back(sg);
+                lo = cut;
+            }
+            while (end > g0 && recs[end - 1].cap == cut) --end;
         }
+        g0 = g1;
     }
 }
 

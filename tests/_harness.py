@@ -48,8 +48,21 @@ def oracle_tree(w, ids: Iterable[int], device="cpu") -> KVTree:
     return tree
 
 
-def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device="cuda") -> float:
-    """Max |GPU - oracle| over the sampled query positions (indices into w.query)."""
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers (8 significant bits) around |x|."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device="cuda",
+                    strict: bool = False) -> float:
+    """Max |GPU - oracle| over the sampled query positions (indices into w.query).
+
+    ``tol`` bounds the arithmetic.  A bf16 output is also rounded to bf16 when
+    stored, which alone can move it by half a bf16 ulp (up to 2^-8 |out|, so
+    more than 5e-3 once |out| >= 1.28, as happens when a query sees one or two
+    keys); unless ``strict``, that half ulp of the exact result is added to
+    the bound element by element."""
     ids = [w.query[i] for i in sample]
     tree = oracle_tree(w, ids, device)
     worst = 0.0
@@ -58,9 +71,10 @@ def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device=
         ref = tree.attend(w.query[i], q)
         got = out[i].double().cpu().numpy()
         assert np.isfinite(got).all()
-        err = float(np.abs(got - ref).max())
-        worst = max(worst, err)
-        assert err <= tol, (w.name, i, err)
+        err = np.abs(got - ref)
+        bound = tol if (strict or out.dtype != torch.bfloat16) else tol + half_ulp_bf16(ref)
+        worst = max(worst, float(err.max()))
+        assert (err <= bound).all(), (w.name, i, float(err.max()), float((err - bound).max()))
     return worst
 
 
