@@ -236,8 +236,7 @@ def run_ours(args):
     # ---- per-kernel device times (profiling events inside the library; one
     # synchronised step at a time so the events of each call can be read)
     pool.set_profiling(True)
-    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
-                            "attn_total")}
+    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "free", "attn_total")}
     plan_us = []
     for i in range(min(args.steps, 100)):
         flush_l2()

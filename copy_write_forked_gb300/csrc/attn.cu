@@ -60,6 +60,8 @@ constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 struct AttnArgs {
     AttnPlanDev plan;
     const void* Q;
+    void* out;
+    int32_t* arrivals;     // [n_queried * n_kv], zero between calls
     const int32_t* table;
     const float* pool_k;   // fp32 kernel only
     const float* pool_v;
@@ -156,11 +158,108 @@ __device__ __forceinline__ uint32_t swz(int t, int d) {
     return (uint32_t)((d >> 6) * HALF_BYTES + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4) + (d & 7) * 2);
 }
 
-// Walks a CTA's share of the tile list: calls f(unit, unit_index, first
-// tile, tile count, P, is_last_stage_of_chunk) for every stage.
-struct Sched {
-    int32_t t, tend, u;
-};
+
+// Query row r of unit U: the Q/out row it reads/writes and its visibility limit.
+__device__ __forceinline__ void unit_row(const AttnPlanDev& pl, const AttnSeg& S, const AttnUnit& U, int r,
+                                         int32_t& q_row, int32_t& limit) {
+    const int RM = pl.q_len * pl.group;
+    const int sr = U.row_lo + r;
+    const int mi = sr / RM;
+    const int rem = sr - mi * RM;
+    const int j = rem / pl.group;
+    const int g = rem - j * pl.group;
+    const AttnMember M = pl.members[S.mem_off + mi];
+    q_row = (M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * pl.group + g;
+    limit = M.len - pl.q_len + j + 1;
+}
+
+// Log-sum-exp merge of one output row (warp-wide): walks the segments on the
+// branch's path and every chunk of the unit holding the row, keeping a running
+// (M, L, acc): M = max m_i, L = sum l_i 2^(m_i - M), acc = sum acc_i 2^(m_i - M),
+// then writes out = acc / L in the output dtype.
+template <typename T>
+__device__ void merge_row(const AttnArgs& a, int32_t qi, int32_t h, int32_t j, int32_t g, int lane) {
+    const AttnPlanDev& pl = a.plan;
+    const int d = a.head_dim, nj = d / 32;
+    const int RM = pl.q_len * pl.group;
+    const float2* ml = a.part_ml;
+    float M = -INFINITY, L = 0.f, acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    for (int32_t e = pl.path_off[qi]; e < pl.path_off[qi + 1]; ++e) {
+        const int32_t seg = pl.path[2 * e], mi = pl.path[2 * e + 1];
+        const AttnSeg S = pl.segs[seg];
+        const int32_t sr = mi * RM + j * pl.group + g;
+        const int32_t grp = sr / pl.max_rows;
+        const int32_t r = sr - grp * pl.max_rows;
+        const AttnUnit U = pl.units[S.unit_base + h * S.ngroups + grp];
+        for (int32_t k = 0; k < U.nchunks; ++k) {
+            const int32_t prow = U.prow_base + k * U.n_rows + r;
+            const float2 v = __ldcg(ml + prow);
+            if (v.x == -INFINITY) continue;
+            const float* src = a.part_acc + (int64_t)prow * d;
+            float wa, wb;   // weights of the running state and of this partial
+            if (v.x > M) {
+                wa = exp2f(M - v.x);
+                wb = 1.f;
+                M = v.x;
+            } else {
+                wa = 1.f;
+                wb = exp2f(v.x - M);
+            }
+            L = L * wa + v.y * wb;
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2)
+                if (k2 < nj) acc[k2] = acc[k2] * wa + __ldcg(src + lane + 32 * k2) * wb;
+        }
+    }
+    const float inv = 1.f / L;
+    T* dst = static_cast<T*>(a.out) + ((int64_t)(qi * pl.q_len + j) * pl.n_q_heads + h * pl.group + g) * d;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nj) {
+            if constexpr (sizeof(T) == 2) dst[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+            else dst[lane + 32 * k] = acc[k] * inv;
+        }
+}
+
+// End of a unit chunk, run by the NT consumer threads of a CTA after they
+// wrote the chunk's partial rows: count one arrival for every (branch, kv
+// head) group whose rows the unit holds; the CTA that brings a group to its
+// expected count merges that group's rows (the last writer, so every partial
+// of the group is complete) and resets its counter for the next call.
+template <typename T, typename Sync>
+__device__ void arrive_and_merge(const AttnArgs& a, const AttnSeg& S, const AttnUnit& U, int32_t* list,
+                                 int32_t* n_list, int tid, int NT, Sync sync) {
+    const AttnPlanDev& pl = a.plan;
+    sync();
+    if (tid == 0) {
+        __threadfence();
+        const int RM = pl.q_len * pl.group;
+        const int m0 = U.row_lo / RM, m1 = (U.row_lo + U.n_rows - 1) / RM;
+        int n = 0;
+        for (int mi = m0; mi <= m1; ++mi) {
+            const int32_t gq = pl.members[S.mem_off + mi].qi * a.n_kv + U.kv_head;
+            const int32_t old = atomicAdd(a.arrivals + gq, 1);
+            if (old + 1 == pl.expected[gq]) {
+                a.arrivals[gq] = 0;
+                list[n++] = gq;
+            }
+        }
+        if (n) __threadfence();
+        *n_list = n;
+    }
+    sync();
+    const int n = *n_list;
+    const int rows = pl.q_len * pl.group;
+    const int warp = tid >> 5, lane = tid & 31, nw = NT >> 5;
+    for (int idx = warp; idx < n * rows; idx += nw) {
+        const int32_t gq = list[idx / rows];
+        const int rr = idx % rows;
+        merge_row<T>(a, gq / a.n_kv, gq % a.n_kv, rr / pl.group, rr % pl.group, lane);
+    }
+    sync();
+}
 
 // ============================================================ bf16 kernel
 __global__ void __launch_bounds__(THREADS, 2)
@@ -168,6 +267,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const AttnArgs a) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ int abort_flag;
+    __shared__ int32_t merge_list[64];
+    __shared__ int32_t merge_n;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* sm = smem_raw + (base - raw);
@@ -200,11 +301,12 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         int32_t t = t_begin, u = u0;
         while (t < t_end) {
             const AttnUnit U = pl.units[u];
-            const int32_t uend = U.tile_off + U.n_blk;
+            const AttnSeg S = pl.segs[U.seg];
+            const int32_t uend = U.tile_off + S.n_blk;
             if (t >= uend) { ++u; continue; }
             const int32_t cend = min(t_end, uend);
             const int P = 4 / U.rt;
-            const int32_t* trow = a.table + (int64_t)U.table_row * a.bpb + U.blk_start - U.tile_off;
+            const int32_t* trow = a.table + (int64_t)S.table_row * a.bpb + S.blk_start - U.tile_off;
             for (int32_t st = t; st < cend; st += P, ++stage) {
                 const int slot = stage % NSTAGE;
                 const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
@@ -261,7 +363,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     int32_t t = t_begin, u = u0;
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
-        const int32_t uend = U.tile_off + U.n_blk;
+        const AttnSeg S = pl.segs[U.seg];
+        const int32_t uend = U.tile_off + S.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
         const int P = 4 / U.rt;
@@ -274,12 +377,11 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         {
             const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
             const bool v0 = has_rows && row0 < U.n_rows, v1 = has_rows && row1 < U.n_rows;
-            const AttnRow R0 = v0 ? pl.rows[U.row_off + row0] : AttnRow{0, 0};
-            const AttnRow R1 = v1 ? pl.rows[U.row_off + row1] : AttnRow{0, 0};
-            lim0 = R0.limit;
-            lim1 = R1.limit;
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R0.q_row * D);
-            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R1.q_row * D);
+            int32_t qr0 = 0, qr1 = 0;
+            if (v0) unit_row(pl, S, U, row0, qr0, lim0);
+            if (v1) unit_row(pl, S, U, row1, qr1, lim1);
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)qr0 * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Q + (int64_t)qr1 * D);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int w = ks * 8 + (lane & 3);   // 32-bit word index of column ks*16 + 2*(lane&3)
@@ -325,7 +427,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     }
                 }
                 // scale, mask by per-row visibility, online softmax
-                const int32_t pos0 = (U.blk_start + (st - U.tile_off) + pidx) * BS + (lane & 3) * 2;
+                const int32_t pos0 = (S.blk_start + (st - U.tile_off) + pidx) * BS + (lane & 3) * 2;
                 float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -466,6 +568,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     fence_async_smem();
                     consumer_sync();   // buffer free again before it is handed back to TMA
                 }
+                arrive_and_merge<__nv_bfloat16>(a, S, U, merge_list, &merge_n, threadIdx.x, NCONS * 32,
+                                                consumer_sync);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -485,6 +589,8 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
     float* Vs = fsm + BS * d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int st0;
+    __shared__ int32_t merge_list[64];
+    __shared__ int32_t merge_n;
     if (threadIdx.x == 0) st0 = a.meta->status;
     __syncthreads();
     if (st0) return;
@@ -496,7 +602,8 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
     const float* Q = static_cast<const float*>(a.Q);
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
-        const int32_t uend = U.tile_off + U.n_blk;
+        const AttnSeg S = pl.segs[U.seg];
+        const int32_t uend = U.tile_off + S.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
         float q[4][8], acc[4][8], m[4], l[4];
@@ -505,7 +612,8 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
         for (int rr = 0; rr < 4; ++rr) {
             const int row = warp + 4 * rr;
             const bool v = row < U.n_rows;
-            const AttnRow R = v ? pl.rows[U.row_off + row] : AttnRow{0, 0};
+            struct { int32_t q_row, limit; } R = {0, 0};
+            if (v) unit_row(pl, S, U, row, R.q_row, R.limit);
             lim[rr] = R.limit;
             m[rr] = -INFINITY;
             l[rr] = 0.f;
@@ -516,8 +624,8 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
             }
         }
         for (int32_t tt = t; tt < cend; ++tt) {
-            const int32_t lb = U.blk_start + (tt - U.tile_off);
-            int32_t blk = a.table[(int64_t)U.table_row * a.bpb + lb];
+            const int32_t lb = S.blk_start + (tt - U.tile_off);
+            int32_t blk = a.table[(int64_t)S.table_row * a.bpb + lb];
             if ((uint32_t)blk >= (uint32_t)a.n_blocks) {
                 if (threadIdx.x == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                 blk = 0;   // read a valid block; the pool is poisoned anyway
@@ -563,61 +671,27 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
                 if (j < nj) a.part_acc[(int64_t)(prow0 + row) * d + lane + 32 * j] = acc[rr][j];
             if (lane == 0) a.part_ml[prow0 + row] = make_float2(m[rr], l[rr]);
         }
+        arrive_and_merge<float>(a, S, U, merge_list, &merge_n, threadIdx.x, 128, [] { __syncthreads(); });
         t = cend;
         ++u;
     }
 }
 
-// ============================================================ LSE merge
-// One warp per output row: M = max m_i, L = sum l_i 2^(m_i - M),
-// out = sum acc_i 2^(m_i - M) / L, written in the pool dtype.
-template <typename T>
-__global__ void k_attn_merge(const AttnArgs a, T* __restrict__ out) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (a.meta->status) return;
-    if (warp >= a.plan.n_out_rows) return;
-    const int d = a.head_dim, nj = d / 32;
-    const int32_t b = a.plan.csr_ptr[warp], e = a.plan.csr_ptr[warp + 1];
-    float M = -INFINITY;
-    for (int32_t k = b; k < e; ++k) M = fmaxf(M, a.part_ml[a.plan.csr_idx[k]].x);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f, acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    for (int32_t k = b; k < e; ++k) {
-        const int32_t pr = a.plan.csr_idx[k];
-        const float2 mlv = a.part_ml[pr];
-        const float w = exp2f(mlv.x - Mu);
-        L += mlv.y * w;
-        const float* src = a.part_acc + (int64_t)pr * d;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < nj) acc[j] = fmaf(src[lane + 32 * j], w, acc[j]);
-    }
-    const float inv = 1.f / L;
-    T* dst = out + (int64_t)warp * d;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        if (j < nj) {
-            if constexpr (sizeof(T) == 2) dst[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
-            else dst[lane + 32 * j] = acc[j] * inv;
-        }
-}
-
 // ============================================================ host planning
 struct HostPlan {
+    std::vector<AttnSeg> segs;
+    std::vector<AttnMember> members;
     std::vector<AttnUnit> units;
-    std::vector<AttnRow> rows;
-    std::vector<int32_t> cta_begin, cta_unit, csr_ptr, csr_idx;
+    std::vector<int32_t> cta_begin, cta_unit, path_off, path, expected;
+    std::vector<int64_t> cuts;
     int64_t tiles = 0, unique_tiles = 0;
-    int32_t n_segments = 0;
     size_t partial_rows = 0;
-    std::vector<int32_t> parent, fork_len, len, queried, members, count, fill;
-    std::vector<Segment> segs;
+    std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
+    std::vector<Segment> psegs;
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
-        units.clear(); rows.clear(); cta_begin.clear(); cta_unit.clear(); csr_ptr.clear(); csr_idx.clear();
+        segs.clear(); members.clear(); units.clear(); cta_begin.clear(); cta_unit.clear();
+        path_off.clear(); path.clear(); expected.clear(); cuts.clear();
         tiles = unique_tiles = 0;
-        n_segments = 0;
         partial_rows = 0;
     }
 };
@@ -626,122 +700,134 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
                HostPlan& hp) {
-    const int32_t G = nq / p->n_kv;
+    const int32_t G = nq / p->n_kv, nkv = p->n_kv;
+    const int32_t RM = q_len * G;
     const int max_rows = p->dtype == DENDRITE_BF16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
     const int32_t n_nodes = (int32_t)p->nodes.size();
-    std::vector<int32_t>&parent = hp.parent, &fork_len = hp.fork_len, &len = hp.len, &queried = hp.queried;
-    parent.resize(n_nodes);
-    fork_len.resize(n_nodes);
-    len.resize(n_nodes);
-    queried.resize(n);
+    hp.parent.resize(n_nodes);
+    hp.fork_len.resize(n_nodes);
+    hp.len.resize(n_nodes);
+    hp.queried.resize(n);
     for (int32_t i = 0; i < n_nodes; ++i) {
-        parent[i] = p->nodes[i].parent;
-        fork_len[i] = p->nodes[i].fork_len;
-        len[i] = p->nodes[i].len;
+        hp.parent[i] = p->nodes[i].parent;
+        hp.fork_len[i] = p->nodes[i].fork_len;
+        hp.len[i] = p->nodes[i].len;
     }
-    for (int32_t i = 0; i < n; ++i) queried[i] = p->br[branches[i]].node;
-    std::vector<Segment>& segs = hp.segs;
-    std::vector<int32_t>& members = hp.members;
-    plan_segments(n_nodes, parent.data(), fork_len.data(), len.data(), p->block_size, queried.data(), n, segs,
-                  members);
-    hp.n_segments = (int32_t)segs.size();
+    for (int32_t i = 0; i < n; ++i) hp.queried[i] = p->br[branches[i]].node;
+    plan_segments(n_nodes, hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
+                  hp.psegs, hp.seg_members);
+    // segments, their members and their units (kv head major, then row group)
     int64_t tile_off = 0, weight = 0;
-    for (const Segment& sg : segs) {
-        const int32_t rows_per_head = sg.n_members * q_len * G;
-        const int32_t rep = p->nodes[sg.rep_node].handle;
-        hp.unique_tiles += (int64_t)sg.block_count * p->n_kv;
-        for (int32_t h = 0; h < p->n_kv; ++h) {
-            for (int32_t g0 = 0; g0 < rows_per_head; g0 += max_rows) {
-                const int32_t nr = std::min(max_rows, rows_per_head - g0);
+    for (const Segment& sg : hp.psegs) {
+        const int32_t rows_per_head = sg.n_members * RM;
+        AttnSeg S;
+        S.table_row = p->nodes[sg.rep_node].handle;
+        S.blk_start = sg.block_start;
+        S.n_blk = sg.block_count;
+        S.mem_off = (int32_t)hp.members.size();
+        S.n_mem = sg.n_members;
+        S.unit_base = (int32_t)hp.units.size();
+        S.ngroups = (rows_per_head + max_rows - 1) / max_rows;
+        S.pad = 0;
+        for (int32_t k = 0; k < sg.n_members; ++k) {
+            const int32_t qi = hp.seg_members[sg.member_offset + k];
+            hp.members.push_back({qi, p->br[branches[qi]].len});
+        }
+        hp.unique_tiles += (int64_t)sg.block_count * nkv;
+        const int32_t seg_index = (int32_t)hp.segs.size();
+        for (int32_t h = 0; h < nkv; ++h) {
+            for (int32_t grp = 0; grp < S.ngroups; ++grp) {
                 AttnUnit U{};
-                U.table_row = rep;
-                U.blk_start = sg.block_start;
-                U.n_blk = sg.block_count;
+                U.seg = seg_index;
                 U.kv_head = h;
-                U.row_off = (int32_t)hp.rows.size();
-                U.n_rows = nr;
-                U.rt = nr <= 16 ? 1 : nr <= 32 ? 2 : 4;
+                U.row_lo = grp * max_rows;
+                U.n_rows = std::min(max_rows, rows_per_head - U.row_lo);
+                U.rt = U.n_rows <= 16 ? 1 : U.n_rows <= 32 ? 2 : 4;
                 U.tile_off = (int32_t)tile_off;
-                for (int32_t r = g0; r < g0 + nr; ++r) {
-                    const int32_t mi = r / (q_len * G), j = (r / G) % q_len, g = r % G;
-                    const int32_t qi = members[sg.member_offset + mi];
-                    const int32_t L = p->br[branches[qi]].len;
-                    hp.rows.push_back({(qi * q_len + j) * nq + h * G + g, L - q_len + j + 1});
-                }
-                tile_off += U.n_blk;
-                weight += (int64_t)U.n_blk * U.rt;
+                tile_off += S.n_blk;
+                weight += (int64_t)S.n_blk * U.rt;
                 hp.units.push_back(U);
             }
         }
+        hp.segs.push_back(S);
     }
     if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
     hp.tiles = tile_off;
-    // even split of the weighted tile list (weight of a tile = row tiles of its unit)
+    // even split of the weighted tile list (weight of a tile = row tiles of its
+    // unit); cuts are made strictly increasing so that no CTA is empty
     const int64_t T = tile_off;
-    int C = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + 3) / 4));
-    hp.cta_begin.assign(C + 1, 0);
+    const int C0 = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + 3) / 4));
+    hp.cuts.push_back(0);
     {
         int c = 1;
         int64_t cw = 0;
         for (const AttnUnit& U : hp.units) {
-            const int64_t uw = (int64_t)U.n_blk * U.rt;
-            while (c < C) {
-                const int64_t target = (weight * c + C - 1) / C;   // first weight index of CTA c
+            const int64_t nb = hp.segs[U.seg].n_blk;
+            const int64_t uw = nb * U.rt;
+            while (c < C0) {
+                const int64_t target = (weight * c + C0 - 1) / C0;
                 if (target >= cw + uw) break;
-                const int64_t k = (target - cw + U.rt - 1) / U.rt;    // tile within unit
-                hp.cta_begin[c] = (int32_t)(U.tile_off + std::min<int64_t>(k, U.n_blk));
+                const int64_t k = (target - cw + U.rt - 1) / U.rt;
+                const int64_t cut = U.tile_off + std::min<int64_t>(k, nb);
+                if (cut > hp.cuts.back() && cut < T) hp.cuts.push_back(cut);
                 ++c;
             }
             cw += uw;
         }
-        for (; c < C; ++c) hp.cta_begin[c] = (int32_t)T;
-        hp.cta_begin[C] = (int32_t)T;
-        for (int i = 1; i <= C; ++i) hp.cta_begin[i] = std::max(hp.cta_begin[i], hp.cta_begin[i - 1]);
     }
-    // CTA holding a tile: the largest c with cta_begin[c] <= t
-    auto cta_of = [&](int32_t t) {
-        return (int32_t)(std::upper_bound(hp.cta_begin.begin(), hp.cta_begin.end() - 1, t) - hp.cta_begin.begin()) - 1;
-    };
-    hp.cta_unit.assign(C, 0);
+    hp.cuts.push_back(T);
+    const int C = (int)hp.cuts.size() - 1;
+    hp.cta_begin.resize(C + 1);
+    for (int i = 0; i <= C; ++i) hp.cta_begin[i] = (int32_t)hp.cuts[i];
+    hp.cta_unit.resize(C);
     {
         size_t u = 0;
         for (int c = 0; c < C; ++c) {
-            while (u + 1 < hp.units.size() && hp.units[u].tile_off + hp.units[u].n_blk <= hp.cta_begin[c]) ++u;
+            while (u + 1 < hp.units.size() &&
+                   hp.units[u].tile_off + hp.segs[hp.units[u].seg].n_blk <= hp.cta_begin[c])
+                ++u;
             hp.cta_unit[c] = (int32_t)u;
         }
     }
-    // partial rows per unit chunk, and the merge lists
-    const int32_t n_out = n * q_len * nq;
-    std::vector<int32_t>& count = hp.count;
-    count.assign(n_out, 0);
+    // chunks and partial rows per unit; arrivals expected per (branch, kv head)
+    hp.expected.assign((size_t)n * nkv, 0);
     size_t prow = 0;
-    for (AttnUnit& U : hp.units) {
-        const int32_t cf = cta_of(U.tile_off), cl = cta_of(U.tile_off + U.n_blk - 1);
-        U.cfirst = cf;
-        U.prow_base = (int32_t)prow;
-        prow += (size_t)(cl - cf + 1) * U.n_rows;
-        for (int32_t c = cf; c <= cl; ++c) {
-            if (hp.cta_begin[c] == hp.cta_begin[c + 1]) continue;
-            for (int32_t r = 0; r < U.n_rows; ++r) count[hp.rows[U.row_off + r].q_row]++;
+    {
+        int c = 0;
+        for (AttnUnit& U : hp.units) {
+            const int32_t last = U.tile_off + hp.segs[U.seg].n_blk - 1;
+            while (hp.cta_begin[c + 1] <= U.tile_off) ++c;
+            int cl = c;
+            while (hp.cta_begin[cl + 1] <= last) ++cl;
+            U.cfirst = c;
+            U.nchunks = cl - c + 1;
+            U.prow_base = (int32_t)prow;
+            prow += (size_t)U.nchunks * U.n_rows;
+            const AttnSeg& S = hp.segs[U.seg];
+            const int m0 = U.row_lo / RM, m1 = (U.row_lo + U.n_rows - 1) / RM;
+            for (int mi = m0; mi <= m1; ++mi)
+                hp.expected[(size_t)hp.members[S.mem_off + mi].qi * nkv + U.kv_head] += U.nchunks;
         }
     }
     if (prow >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
     hp.partial_rows = prow;
-    hp.csr_ptr.assign(n_out + 1, 0);
-    for (int32_t o = 0; o < n_out; ++o) hp.csr_ptr[o + 1] = hp.csr_ptr[o] + count[o];
-    hp.csr_idx.assign(hp.csr_ptr[n_out], 0);
-    std::vector<int32_t>& fill = hp.fill;
-    fill.assign(hp.csr_ptr.begin(), hp.csr_ptr.end() - 1);
-    for (const AttnUnit& U : hp.units) {
-        const int32_t cl = cta_of(U.tile_off + U.n_blk - 1);
-        for (int32_t c = U.cfirst; c <= cl; ++c) {
-            if (hp.cta_begin[c] == hp.cta_begin[c + 1]) continue;
-            for (int32_t r = 0; r < U.n_rows; ++r)
-                hp.csr_idx[fill[hp.rows[U.row_off + r].q_row]++] = U.prow_base + (c - U.cfirst) * U.n_rows + r;
+    // path of every queried branch: (segment, member index) pairs
+    hp.path_off.assign(n + 1, 0);
+    for (const AttnSeg& S : hp.segs)
+        for (int32_t k = 0; k < S.n_mem; ++k) hp.path_off[hp.members[S.mem_off + k].qi + 1]++;
+    for (int32_t i = 0; i < n; ++i) hp.path_off[i + 1] += hp.path_off[i];
+    hp.path.resize(2 * (size_t)hp.path_off[n]);
+    hp.cursor.assign(hp.path_off.begin(), hp.path_off.end() - 1);
+    for (int32_t si = 0; si < (int32_t)hp.segs.size(); ++si) {
+        const AttnSeg& S = hp.segs[si];
+        for (int32_t k = 0; k < S.n_mem; ++k) {
+            const int32_t e = hp.cursor[hp.members[S.mem_off + k].qi]++;
+            hp.path[2 * e] = si;
+            hp.path[2 * e + 1] = k;
         }
     }
-    for (int32_t o = 0; o < n_out; ++o)
-        if (count[o] == 0) return DENDRITE_EINVAL;   // a row with no visible key
+    for (int32_t i = 0; i < n; ++i)
+        if (hp.path_off[i + 1] == hp.path_off[i]) return DENDRITE_EINVAL;   // a branch with no visible key
     return DENDRITE_OK;
 }
 
@@ -776,7 +862,17 @@ int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
     return DENDRITE_OK;
 }
 
-int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows) {
+int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows, size_t groups) {
+    if (groups > p->arrivals_cap) {
+        size_t cap = std::max<size_t>(groups * 2, 4096);
+        DENDRITE_CUDA(cudaDeviceSynchronize());
+        if (p->d_arrivals) cudaFree(p->d_arrivals);
+        p->d_arrivals = nullptr;
+        p->arrivals_cap = 0;
+        DENDRITE_CUDA(cudaMalloc(&p->d_arrivals, cap * sizeof(int32_t)));
+        DENDRITE_CUDA(cudaMemset(p->d_arrivals, 0, cap * sizeof(int32_t)));
+        p->arrivals_cap = cap;
+    }
     if (plan_bytes > p->plan_cap) {
         size_t cap = std::max<size_t>(plan_bytes * 2, 1 << 20);
         DENDRITE_CUDA(cudaDeviceSynchronize());
@@ -835,9 +931,11 @@ void attn_teardown(dendrite_pool* p) {
     if (p->d_plan) cudaFree(p->d_plan);
     if (p->h_plan) cudaFreeHost(p->h_plan);
     if (p->d_partial) cudaFree(p->d_partial);
+    if (p->d_arrivals) cudaFree(p->d_arrivals);
     p->d_plan = nullptr;
     p->h_plan = nullptr;
     p->d_partial = nullptr;
+    p->d_arrivals = nullptr;
 }
 
 }  // namespace dendrite
@@ -872,47 +970,56 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         hp.clear();
         DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, hp));
         const int32_t C = (int32_t)hp.cta_unit.size();
-        const int32_t n_out = n * q_len * n_q_heads;
-        size_t off[7];
+        size_t off[9];
         size_t b = 0;
-        off[0] = b; b = align16(b + hp.units.size() * sizeof(AttnUnit));
-        off[1] = b; b = align16(b + hp.rows.size() * sizeof(AttnRow));
-        off[2] = b; b = align16(b + hp.cta_begin.size() * 4);
-        off[3] = b; b = align16(b + hp.cta_unit.size() * 4);
-        off[4] = b; b = align16(b + hp.csr_ptr.size() * 4);
-        off[5] = b; b = align16(b + hp.csr_idx.size() * 4);
-        off[6] = b;
-        DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
+        off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
+        off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
+        off[2] = b; b = align16(b + hp.units.size() * sizeof(AttnUnit));
+        off[3] = b; b = align16(b + hp.cta_begin.size() * 4);
+        off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
+        off[5] = b; b = align16(b + hp.path_off.size() * 4);
+        off[6] = b; b = align16(b + hp.path.size() * 4);
+        off[7] = b; b = align16(b + hp.expected.size() * 4);
+        off[8] = b;
+        DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows, hp.expected.size()));
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
         char* h = p->h_plan;
-        std::memcpy(h + off[0], hp.units.data(), hp.units.size() * sizeof(AttnUnit));
-        std::memcpy(h + off[1], hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
-        std::memcpy(h + off[2], hp.cta_begin.data(), hp.cta_begin.size() * 4);
-        std::memcpy(h + off[3], hp.cta_unit.data(), hp.cta_unit.size() * 4);
-        std::memcpy(h + off[4], hp.csr_ptr.data(), hp.csr_ptr.size() * 4);
-        std::memcpy(h + off[5], hp.csr_idx.data(), hp.csr_idx.size() * 4);
+        std::memcpy(h + off[0], hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
+        std::memcpy(h + off[1], hp.members.data(), hp.members.size() * sizeof(AttnMember));
+        std::memcpy(h + off[2], hp.units.data(), hp.units.size() * sizeof(AttnUnit));
+        std::memcpy(h + off[3], hp.cta_begin.data(), hp.cta_begin.size() * 4);
+        std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
+        std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
+        std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
+        std::memcpy(h + off[7], hp.expected.data(), hp.expected.size() * 4);
         DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, h, b, cudaMemcpyHostToDevice, s));
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
         char* d = p->d_plan;
-        pc.dev.units = reinterpret_cast<const AttnUnit*>(d + off[0]);
-        pc.dev.rows = reinterpret_cast<const AttnRow*>(d + off[1]);
-        pc.dev.cta_begin = reinterpret_cast<const int32_t*>(d + off[2]);
-        pc.dev.cta_unit = reinterpret_cast<const int32_t*>(d + off[3]);
-        pc.dev.csr_ptr = reinterpret_cast<const int32_t*>(d + off[4]);
-        pc.dev.csr_idx = reinterpret_cast<const int32_t*>(d + off[5]);
+        pc.dev.segs = reinterpret_cast<const AttnSeg*>(d + off[0]);
+        pc.dev.members = reinterpret_cast<const AttnMember*>(d + off[1]);
+        pc.dev.units = reinterpret_cast<const AttnUnit*>(d + off[2]);
+        pc.dev.cta_begin = reinterpret_cast<const int32_t*>(d + off[3]);
+        pc.dev.cta_unit = reinterpret_cast<const int32_t*>(d + off[4]);
+        pc.dev.path_off = reinterpret_cast<const int32_t*>(d + off[5]);
+        pc.dev.path = reinterpret_cast<const int32_t*>(d + off[6]);
+        pc.dev.expected = reinterpret_cast<const int32_t*>(d + off[7]);
         pc.dev.n_units = (int32_t)hp.units.size();
         pc.dev.n_ctas = C;
-        pc.dev.n_out_rows = n_out;
+        pc.dev.n_queried = n;
+        pc.dev.q_len = q_len;
+        pc.dev.n_q_heads = n_q_heads;
+        pc.dev.group = n_q_heads / p->n_kv;
+        pc.dev.max_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
         pc.version = p->version;
         pc.q_len = q_len;
         pc.n_q_heads = n_q_heads;
         pc.branches.assign(branches, branches + n);
-        pc.stats.n_segments = hp.n_segments;
+        pc.stats.n_segments = (int32_t)hp.segs.size();
         pc.stats.n_units = (int32_t)hp.units.size();
         pc.stats.n_ctas = C;
-        pc.stats.n_partials = (int32_t)hp.csr_idx.size();
+        pc.stats.n_partials = (int32_t)hp.partial_rows;
         pc.stats.tiles = hp.tiles;
         pc.stats.unique_tiles = hp.unique_tiles;
         pc.stats.plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
@@ -922,6 +1029,8 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
     AttnArgs a;
     a.plan = pc.dev;
     a.Q = Q;
+    a.out = out;
+    a.arrivals = p->d_arrivals;
     a.table = p->d_table;
     a.pool_k = static_cast<const float*>(p->d_k);
     a.pool_v = static_cast<const float*>(p->d_v);
@@ -944,14 +1053,8 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         k_attn_partial_f32<<<pc.dev.n_ctas, 128, 2 * BS * p->head_dim * sizeof(float), s>>>(a);
     }
     prof_end(p, T_ATTN_PARTIAL, s);
-    DENDRITE_CUDA(cudaGetLastError());
-    prof_begin(p, T_ATTN_MERGE, s);
-    const int warps_per_cta = 4;
-    const unsigned grid = (unsigned)((pc.dev.n_out_rows + warps_per_cta - 1) / warps_per_cta);
-    if (bf16) k_attn_merge<__nv_bfloat16><<<grid, 32 * warps_per_cta, 0, s>>>(a, static_cast<__nv_bfloat16*>(out));
-    else k_attn_merge<float><<<grid, 32 * warps_per_cta, 0, s>>>(a, static_cast<float*>(out));
-    prof_end(p, T_ATTN_MERGE, s);
     prof_end(p, T_ATTN_TOTAL, s);
+    DENDRITE_CUDA(cudaGetLastError());
     DENDRITE_CUDA(cudaGetLastError());
     return DENDRITE_OK;
 }

@@ -32,39 +32,61 @@ struct DevMeta {
     int32_t pad[3];
 };
 
-// One attention work unit: a (segment, kv head, row group).
+// One sharing segment: blocks [blk_start, blk_start + n_blk) of the table row
+// `table_row`, read by the queried branches listed in members[mem_off ..).
+// Its units are unit_base + kv_head * ngroups + row_group.
+struct AttnSeg {
+    int32_t table_row;
+    int32_t blk_start;
+    int32_t n_blk;
+    int32_t mem_off;
+    int32_t n_mem;
+    int32_t unit_base;
+    int32_t ngroups;
+    int32_t pad;
+};
+
+// A queried branch as a segment member: its index in the query list and length.
+struct AttnMember {
+    int32_t qi;
+    int32_t len;
+};
+
+// One attention work unit: a (segment, kv head, row group).  Its rows are
+// segment rows [row_lo, row_lo + n_rows); segment row sr belongs to member
+// sr / (q_len * G), query token (sr % (q_len * G)) / G and head group g = sr % G.
 struct AttnUnit {
-    int32_t table_row;  // branch handle whose table row holds the segment's block ids
-    int32_t blk_start;  // first logical block index
-    int32_t n_blk;      // tiles (blocks) in the unit
+    int32_t seg;
     int32_t kv_head;
-    int32_t row_off;    // first row in the row list
-    int32_t n_rows;     // 1..64 query rows
+    int32_t row_lo;
+    int32_t n_rows;     // 1..max rows per unit
     int32_t rt;         // row tiles of 16 (1, 2 or 4)
-    int32_t cfirst;     // CTA holding the unit's first tile
     int32_t tile_off;   // global index of the unit's first tile
-    int32_t prow_base;  // first partial row of the unit's first chunk
-    int32_t pad[2];
+    int32_t cfirst;     // CTA holding the unit's first tile
+    int32_t nchunks;    // CTAs its tiles are split over (all non-empty)
+    int32_t prow_base;  // first partial row; chunk k uses rows prow_base + k * n_rows ..
+    int32_t pad[3];
 };
 static_assert(sizeof(AttnUnit) == 48, "AttnUnit layout");
 
-// One query row of a unit.
-struct AttnRow {
-    int32_t q_row;   // row of Q/out viewed as [n_rows_total][head_dim]
-    int32_t limit;   // number of visible positions (query sees positions < limit)
-};
-
 // Device view of an uploaded attention plan.
 struct AttnPlanDev {
+    const AttnSeg* segs;
+    const AttnMember* members;
     const AttnUnit* units;
-    const AttnRow* rows;
-    const int32_t* cta_begin;   // [n_ctas + 1] global tile boundaries
+    const int32_t* cta_begin;   // [n_ctas + 1] strictly increasing tile boundaries
     const int32_t* cta_unit;    // [n_ctas] unit holding cta_begin[c]
-    const int32_t* csr_ptr;     // [n_out_rows + 1]
-    const int32_t* csr_idx;     // partial row indices per output row
+    const int32_t* path_off;    // [n_queried + 1] into path
+    const int32_t* path;        // pairs (segment, member index) along each queried branch
+    const int32_t* expected;    // [n_queried * n_kv] chunk arrivals per (branch, kv head) group
     int32_t n_units;
     int32_t n_ctas;
-    int32_t n_out_rows;
+    int32_t n_queried;
+    int32_t q_len;
+    int32_t n_q_heads;
+    int32_t group;              // G = n_q_heads / n_kv
+    int32_t max_rows;           // rows per unit (row-group size)
+    int32_t pad;
 };
 
 // ------------------------------------------------------- host bookkeeping
@@ -110,7 +132,7 @@ private:
     std::vector<cudaEvent_t> spare_;
 };
 
-enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_ATTN_MERGE, T_FREE,
+enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_RESERVED4, T_FREE,
                   T_ATTN_TOTAL, T_COUNT };
 
 struct PlanCache {
@@ -159,6 +181,8 @@ struct dendrite_pool {
     cudaEvent_t plan_copied = nullptr;
     float* d_partial = nullptr;      // partial rows: [rows][head_dim] acc then [rows][2] (m, l)
     size_t partial_rows_cap = 0;
+    int32_t* d_arrivals = nullptr;   // per (branch, kv head) arrival counters, zero between calls
+    size_t arrivals_cap = 0;
     dendrite::PlanCache plan;
 
     // host mirror

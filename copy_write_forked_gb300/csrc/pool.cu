@@ -72,16 +72,29 @@ struct ForkParams {
 __device__ __forceinline__ void fork_pair(int32_t* __restrict__ table, int32_t* __restrict__ refcount,
                                           int32_t bpb, int32_t child, int32_t parent, int32_t nb,
                                           int32_t add, int lane, int32_t n_blocks, DevMeta* meta) {
+    // the parent's row is not written by this launch (children are new handles),
+    // so its entries are read through the read-only path, 8 per lane at once
     const int32_t* src = table + (int64_t)parent * bpb;
     int32_t* dst = table + (int64_t)child * bpb;
-    for (int32_t k = lane; k < nb; k += 32) {
-        const int32_t blk = src[k];
-        dst[k] = blk;
-        if ((uint32_t)blk >= (uint32_t)n_blocks) {
-            set_status(meta, DENDRITE_ECORRUPT);
-            continue;
+    constexpr int U = 8;
+    for (int32_t base = 0; base < nb; base += 32 * U) {
+        int32_t v[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int32_t k = base + i * 32 + lane;
+            v[i] = k < nb ? __ldg(src + k) : -1;
         }
-        if (add) atomicAdd(refcount + blk, add);
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int32_t k = base + i * 32 + lane;
+            if (k >= nb) continue;
+            dst[k] = v[i];
+            if ((uint32_t)v[i] >= (uint32_t)n_blocks) {
+                set_status(meta, DENDRITE_ECORRUPT);
+                continue;
+            }
+            if (add) atomicAdd(refcount + v[i], add);
+        }
     }
 }
 

@@ -8,6 +8,7 @@ into a ``cudaStream_t``.  If the library is missing it raises at import of
 """
 from __future__ import annotations
 
+import array
 import ctypes
 import os
 from typing import List, Optional, Sequence
@@ -22,14 +23,14 @@ ERRORS = {
     -1: "EINVAL", -2: "ENOMEM", -3: "EBADHANDLE", -4: "ELIMIT", -5: "EDTYPE",
     -6: "ECUDA", -7: "ETIMEOUT", -8: "ECORRUPT",
 }
-TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total")
+TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "reserved", "free", "attn_total")
 FP32, BF16 = 0, 1
 
 _LIB = None
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
-_pi32 = ctypes.POINTER(ctypes.c_int32)
+_pi32 = ctypes.c_void_p
 
 
 class DendriteError(RuntimeError):
@@ -100,15 +101,30 @@ def _check(rc: int, what: str = "") -> None:
         raise DendriteError(rc, what)
 
 
-def _arr(xs: Sequence[int]):
-    a = (ctypes.c_int32 * max(1, len(xs)))(*[int(x) for x in xs])
+def _arr(xs: Sequence[int]) -> array.array:
+    """int32 host buffer (kept alive by the caller for the duration of the call)."""
+    a = array.array("i", xs)
+    if not a:
+        a.append(0)
     return a
 
 
-def _stream_ptr(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+def _ptr(a: array.array) -> int:
+    return a.buffer_info()[0]
+
+
+try:
+    _raw_stream = torch._C._cuda_getCurrentRawStream
+except AttributeError:  # pragma: no cover
+    _raw_stream = None
+
+
+def _stream_ptr(stream, device_index: int = 0) -> int:
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(device_index)
+    return torch.cuda.current_stream().cuda_stream
 
 
 _DT = {torch.float32: FP32, torch.bfloat16: BF16}
@@ -132,6 +148,7 @@ class Pool:
             _check(lib().dendrite_pool_create(self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim,
                                               _DT[dtype], ctypes.byref(opts), ctypes.byref(h)), "pool_create")
         self._h = h
+        self._dev = self.device.index
 
     # ------------------------------------------------------------ lifetime
     def close(self) -> None:
@@ -154,22 +171,25 @@ class Pool:
     # --------------------------------------------------------------- ops
     def new_branch(self) -> int:
         out = ctypes.c_int32()
-        _check(lib().dendrite_branch_new(self._h, ctypes.byref(out)), "branch_new")
+        _check(lib().dendrite_branch_new(self._h, ctypes.addressof(out)), "branch_new")
         return out.value
 
     def fork(self, parent: int, n_children: int, stream=None) -> List[int]:
         out = (ctypes.c_int32 * n_children)()
-        _check(lib().dendrite_fork(self._h, int(parent), int(n_children), out, _stream_ptr(stream)), "fork")
+        _check(lib().dendrite_fork(self._h, int(parent), int(n_children), ctypes.addressof(out),
+                                   _stream_ptr(stream, self._dev)),
+               "fork")
         return list(out)
 
     def fork_batch(self, parents: Sequence[int], n_children: Sequence[int], stream=None) -> List[List[int]]:
         total = sum(int(n) for n in n_children)
-        out = (ctypes.c_int32 * max(1, total))()
-        _check(lib().dendrite_fork_batch(self._h, _arr(parents), _arr(n_children), len(parents), out,
-                                         _stream_ptr(stream)), "fork_batch")
+        out = array.array("i", bytes(4 * max(1, total)))
+        pa, na = _arr(parents), _arr(n_children)
+        _check(lib().dendrite_fork_batch(self._h, _ptr(pa), _ptr(na), len(parents), _ptr(out),
+                                         _stream_ptr(stream, self._dev)), "fork_batch")
         res, k = [], 0
         for n in n_children:
-            res.append(list(out[k:k + n]))
+            res.append(out[k:k + n].tolist())
             k += n
         return res
 
@@ -185,8 +205,9 @@ class Pool:
         if K.shape != V.shape or K.dim() != 4 or K.shape[0] != nb or K.shape[2] != self.n_kv_heads \
                 or K.shape[3] != self.head_dim:
             raise DendriteError(-1, f"K/V shape {tuple(K.shape)}")
-        _check(lib().dendrite_append_kv(self._h, _arr(branches), nb, int(K.shape[1]), ctypes.c_void_p(K.data_ptr()),
-                                        ctypes.c_void_p(V.data_ptr()), _stream_ptr(stream)), "append_kv")
+        ba = _arr(branches)
+        _check(lib().dendrite_append_kv(self._h, _ptr(ba), nb, K.shape[1], K.data_ptr(), V.data_ptr(),
+                                        _stream_ptr(stream, self._dev)), "append_kv")
 
     def tree_attn_decode(self, Q: torch.Tensor, branches: Sequence[int], out: Optional[torch.Tensor] = None,
                          stream=None) -> torch.Tensor:
@@ -199,45 +220,49 @@ class Pool:
         self._check_tensor(out, "out")
         if out.shape != Q.shape:
             raise DendriteError(-1, "out shape")
-        _check(lib().dendrite_tree_attn_decode(self._h, ctypes.c_void_p(Q.data_ptr()), int(Q.shape[2]),
-                                               int(Q.shape[1]), _arr(branches), len(branches),
-                                               ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)),
+        ba = _arr(branches)
+        _check(lib().dendrite_tree_attn_decode(self._h, Q.data_ptr(), Q.shape[2], Q.shape[1], _ptr(ba),
+                                               len(branches), out.data_ptr(), _stream_ptr(stream, self._dev)),
                "tree_attn_decode")
         return out
 
     def free(self, branches: Sequence[int], stream=None) -> None:
-        _check(lib().dendrite_free(self._h, _arr(branches), len(branches), _stream_ptr(stream)), "free")
+        ba = _arr(branches)
+        _check(lib().dendrite_free(self._h, _ptr(ba), len(branches), _stream_ptr(stream, self._dev)), "free")
 
     def sync(self, stream=None) -> None:
-        _check(lib().dendrite_sync(self._h, _stream_ptr(stream)), "sync")
+        _check(lib().dendrite_sync(self._h, _stream_ptr(stream, self._dev)), "sync")
 
     def sync_status(self, stream=None) -> int:
         """Like :meth:`sync` but returns the status code instead of raising."""
-        return lib().dendrite_sync(self._h, _stream_ptr(stream))
+        return lib().dendrite_sync(self._h, _stream_ptr(stream, self._dev))
 
     # -------------------------------------------------------- inspection
     def branch_len(self, b: int) -> int:
         out = ctypes.c_int32()
-        _check(lib().dendrite_branch_len(self._h, int(b), ctypes.byref(out)), "branch_len")
+        _check(lib().dendrite_branch_len(self._h, int(b), ctypes.addressof(out)), "branch_len")
         return out.value
 
     def read_table(self, b: int, stream=None) -> List[int]:
         n = ctypes.c_int32()
         cap = (self.branch_len(b) + self.block_size - 1) // self.block_size
         buf = (ctypes.c_int32 * max(1, cap))()
-        _check(lib().dendrite_read_table(self._h, int(b), buf, cap, ctypes.byref(n), _stream_ptr(stream)),
+        _check(lib().dendrite_read_table(self._h, int(b), ctypes.addressof(buf), cap, ctypes.addressof(n),
+                                         _stream_ptr(stream, self._dev)),
                "read_table")
         return list(buf[:n.value])
 
     def read_refcounts(self, stream=None) -> List[int]:
         buf = (ctypes.c_int32 * self.num_blocks)()
-        _check(lib().dendrite_read_refcounts(self._h, buf, _stream_ptr(stream)), "read_refcounts")
+        _check(lib().dendrite_read_refcounts(self._h, ctypes.addressof(buf), _stream_ptr(stream, self._dev)),
+               "read_refcounts")
         return list(buf)
 
     def read_free_stack(self, stream=None) -> List[int]:
         buf = (ctypes.c_int32 * self.num_blocks)()
         top = ctypes.c_int32()
-        _check(lib().dendrite_read_free_stack(self._h, buf, ctypes.byref(top), _stream_ptr(stream)),
+        _check(lib().dendrite_read_free_stack(self._h, ctypes.addressof(buf), ctypes.addressof(top),
+                                              _stream_ptr(stream, self._dev)),
                "read_free_stack")
         return list(buf[:top.value])
 
@@ -245,8 +270,8 @@ class Pool:
         shape = (self.n_kv_heads, self.block_size, self.head_dim)
         k = torch.empty(shape, dtype=self.dtype)
         v = torch.empty(shape, dtype=self.dtype)
-        _check(lib().dendrite_read_block(self._h, int(blk), ctypes.c_void_p(k.data_ptr()),
-                                         ctypes.c_void_p(v.data_ptr()), _stream_ptr(stream)), "read_block")
+        _check(lib().dendrite_read_block(self._h, int(blk), k.data_ptr(), v.data_ptr(),
+                                         _stream_ptr(stream, self._dev)), "read_block")
         return k, v
 
     # --------------------------------------------------------- profiling
@@ -270,15 +295,16 @@ def plan_segments(parent: Sequence[int], fork_len: Sequence[int], length: Sequen
     n = len(parent)
     ns, nm = ctypes.c_int32(), ctypes.c_int32()
     L = lib()
-    rc = L.dendrite_plan_segments(n, _arr(parent), _arr(fork_len), _arr(length), block_size, _arr(queried),
-                                  len(queried), None, 0, ctypes.byref(ns), None, 0, ctypes.byref(nm))
+    pa, fa, la, qa = _arr(parent), _arr(fork_len), _arr(length), _arr(queried)
+    rc = L.dendrite_plan_segments(n, _ptr(pa), _ptr(fa), _ptr(la), block_size, _ptr(qa),
+                                  len(queried), None, 0, ctypes.addressof(ns), None, 0, ctypes.addressof(nm))
     if rc not in (0, -4):
         _check(rc, "plan_segments")
     segs = (_Segment * max(1, ns.value))()
     mem = (ctypes.c_int32 * max(1, nm.value))()
-    _check(L.dendrite_plan_segments(n, _arr(parent), _arr(fork_len), _arr(length), block_size, _arr(queried),
-                                    len(queried), segs, ns.value, ctypes.byref(ns), mem, nm.value,
-                                    ctypes.byref(nm)), "plan_segments")
+    _check(L.dendrite_plan_segments(n, _ptr(pa), _ptr(fa), _ptr(la), block_size, _ptr(qa),
+                                    len(queried), segs, ns.value, ctypes.addressof(ns), ctypes.addressof(mem),
+                                    nm.value, ctypes.addressof(nm)), "plan_segments")
     out = []
     for s in segs[:ns.value]:
         out.append((s.rep, s.block_start, s.block_count, list(mem[s.member_offset:s.member_offset + s.n_members])))
