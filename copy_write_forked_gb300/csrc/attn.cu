@@ -48,6 +48,7 @@ namespace {
 constexpr int D = 128;
 constexpr int BS = 16;
 constexpr int NSTAGE = 3;
+constexpr int LEAD = 4;                          // L2 prefetch lead, in stages
 constexpr int HALF_BYTES = BS * 64 * 2;          // one 64-column half of a K or V tile
 constexpr int SLOT_BYTES = 4 * HALF_BYTES;       // K (2 halves) + V (2 halves) of one tile
 constexpr int STAGE_BYTES = 4 * SLOT_BYTES;
@@ -61,10 +62,10 @@ struct AttnArgs {
     AttnPlanDev plan;
     const void* Q;
     void* out;
-    int32_t* arrivals;     // [n_queried * n_kv], zero between calls
     const int32_t* table;
-    const float* pool_k;   // fp32 kernel only
+    const float* pool_k;   // fp32 kernel
     const float* pool_v;
+    const void* pool_kv[2];   // K and V pool bases (bf16 kernel's L2 prefetches)
     float* part_acc;       // [partial rows][head_dim]
     float2* part_ml;       // [partial rows] (m, l)
     DevMeta* meta;
@@ -173,92 +174,48 @@ __device__ __forceinline__ void unit_row(const AttnPlanDev& pl, const AttnSeg& S
     limit = M.len - pl.q_len + j + 1;
 }
 
-// Log-sum-exp merge of one output row (warp-wide): walks the segments on the
-// branch's path and every chunk of the unit holding the row, keeping a running
-// (M, L, acc): M = max m_i, L = sum l_i 2^(m_i - M), acc = sum acc_i 2^(m_i - M),
-// then writes out = acc / L in the output dtype.
-template <typename T>
-__device__ void merge_row(const AttnArgs& a, int32_t qi, int32_t h, int32_t j, int32_t g, int lane) {
-    const AttnPlanDev& pl = a.plan;
-    const int d = a.head_dim, nj = d / 32;
-    const int RM = pl.q_len * pl.group;
-    const float2* ml = a.part_ml;
-    float M = -INFINITY, L = 0.f, acc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-    for (int32_t e = pl.path_off[qi]; e < pl.path_off[qi + 1]; ++e) {
-        const int32_t seg = pl.path[2 * e], mi = pl.path[2 * e + 1];
-        const AttnSeg S = pl.segs[seg];
-        const int32_t sr = mi * RM + j * pl.group + g;
-        const int32_t grp = sr / pl.max_rows;
-        const int32_t r = sr - grp * pl.max_rows;
-        const AttnUnit U = pl.units[S.unit_base + h * S.ngroups + grp];
-        for (int32_t k = 0; k < U.nchunks; ++k) {
-            const int32_t prow = U.prow_base + k * U.n_rows + r;
-            const float2 v = __ldcg(ml + prow);
-            if (v.x == -INFINITY) continue;
-            const float* src = a.part_acc + (int64_t)prow * d;
-            float wa, wb;   // weights of the running state and of this partial
-            if (v.x > M) {
-                wa = exp2f(M - v.x);
-                wb = 1.f;
-                M = v.x;
-            } else {
-                wa = 1.f;
-                wb = exp2f(v.x - M);
+// Schedule walker over a CTA's share of the tile list, one stage at a time.
+// A stage is up to P = 4 / rt consecutive tiles of one unit.
+struct Walker {
+    const AttnPlanDev* pl;
+    int32_t t, t_end, u, cend;
+    int P;
+    AttnUnit U;
+    AttnSeg S;
+    __device__ void init(const AttnPlanDev& p, int c) {
+        pl = &p;
+        t = p.cta_begin[c];
+        t_end = p.cta_begin[c + 1];
+        u = p.cta_unit[c];
+        settle();
+    }
+    __device__ bool valid() const { return t < t_end; }
+    __device__ void settle() {
+        while (t < t_end) {
+            U = pl->units[u];
+            S = pl->segs[U.seg];
+            const int32_t uend = U.tile_off + S.n_blk;
+            if (t < uend) {
+                cend = min(t_end, uend);
+                P = 4 / U.rt;
+                return;
             }
-            L = L * wa + v.y * wb;
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2)
-                if (k2 < nj) acc[k2] = acc[k2] * wa + __ldcg(src + lane + 32 * k2) * wb;
+            ++u;
         }
     }
-    const float inv = 1.f / L;
-    T* dst = static_cast<T*>(a.out) + ((int64_t)(qi * pl.q_len + j) * pl.n_q_heads + h * pl.group + g) * d;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (k < nj) {
-            if constexpr (sizeof(T) == 2) dst[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
-            else dst[lane + 32 * k] = acc[k] * inv;
+    __device__ int ntiles() const { return min(P, cend - t); }
+    __device__ void next() {
+        t += P;
+        if (t >= cend) {
+            t = cend;
+            ++u;
+            settle();
         }
-}
+    }
+};
 
-// End of a unit chunk, run by the NT consumer threads of a CTA after they
-// wrote the chunk's partial rows: count one arrival for every (branch, kv
-// head) group whose rows the unit holds; the CTA that brings a group to its
-// expected count merges that group's rows (the last writer, so every partial
-// of the group is complete) and resets its counter for the next call.
-template <typename T, typename Sync>
-__device__ void arrive_and_merge(const AttnArgs& a, const AttnSeg& S, const AttnUnit& U, int32_t* list,
-                                 int32_t* n_list, int tid, int NT, Sync sync) {
-    const AttnPlanDev& pl = a.plan;
-    sync();
-    if (tid == 0) {
-        __threadfence();
-        const int RM = pl.q_len * pl.group;
-        const int m0 = U.row_lo / RM, m1 = (U.row_lo + U.n_rows - 1) / RM;
-        int n = 0;
-        for (int mi = m0; mi <= m1; ++mi) {
-            const int32_t gq = pl.members[S.mem_off + mi].qi * a.n_kv + U.kv_head;
-            const int32_t old = atomicAdd(a.arrivals + gq, 1);
-            if (old + 1 == pl.expected[gq]) {
-                a.arrivals[gq] = 0;
-                list[n++] = gq;
-            }
-        }
-        if (n) __threadfence();
-        *n_list = n;
-    }
-    sync();
-    const int n = *n_list;
-    const int rows = pl.q_len * pl.group;
-    const int warp = tid >> 5, lane = tid & 31, nw = NT >> 5;
-    for (int idx = warp; idx < n * rows; idx += nw) {
-        const int32_t gq = list[idx / rows];
-        const int rr = idx % rows;
-        merge_row<T>(a, gq / a.n_kv, gq % a.n_kv, rr / pl.group, rr % pl.group, lane);
-    }
-    sync();
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ============================================================ bf16 kernel
@@ -267,8 +224,6 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const AttnArgs a) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ int abort_flag;
-    __shared__ int32_t merge_list[64];
-    __shared__ int32_t merge_n;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* sm = smem_raw + (base - raw);
@@ -282,6 +237,9 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, NCONS);
         }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs of the previous kernel are ready
+    if (threadIdx.x == 0) {
         abort_flag = a.meta->status != 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -296,40 +254,53 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
     if (warp == NCONS) {
         // ------------------------------------------------------ producer
+        // TMA loads fill the NSTAGE-deep ring; bulk L2 prefetches run LEAD
+        // stages ahead of them so that DRAM sees more requests in flight than
+        // shared memory can hold.
         uint32_t issued = 0, parity_bits = 0;
         int32_t stage = 0;
-        int32_t t = t_begin, u = u0;
-        while (t < t_end) {
-            const AttnUnit U = pl.units[u];
-            const AttnSeg S = pl.segs[U.seg];
-            const int32_t uend = U.tile_off + S.n_blk;
-            if (t >= uend) { ++u; continue; }
-            const int32_t cend = min(t_end, uend);
-            const int P = 4 / U.rt;
-            const int32_t* trow = a.table + (int64_t)S.table_row * a.bpb + S.blk_start - U.tile_off;
-            for (int32_t st = t; st < cend; st += P, ++stage) {
-                const int slot = stage % NSTAGE;
-                const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
-                const int ntiles = min(P, cend - st);
-                bool ok = true;
-                if (lane == 0 && !*abortp) {
-                    ok = mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abortp);
-                    if (!ok) {
-                        *abortp = 1;
-                        atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
-                    }
+        Walker w, pf;
+        w.init(pl, c);
+        pf = w;
+        const char* kbase = static_cast<const char*>(a.pool_kv[0]);
+        const char* vbase = static_cast<const char*>(a.pool_kv[1]);
+        auto prefetch_stage = [&](const Walker& x) {
+            if (lane < x.ntiles()) {
+                const int32_t blk = a.table[(int64_t)x.S.table_row * a.bpb + x.S.blk_start + (x.t - x.U.tile_off) + lane];
+                if ((uint32_t)blk < (uint32_t)a.n_blocks) {
+                    const int64_t off = ((int64_t)blk * a.n_kv + x.U.kv_head) * (2 * HALF_BYTES);
+                    l2_prefetch(kbase + off, 2 * HALF_BYTES);
+                    l2_prefetch(vbase + off, 2 * HALF_BYTES);
                 }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && !*abortp;
-                if (!ok) continue;
+            }
+        };
+        for (int k = 0; k < LEAD && pf.valid(); ++k) {
+            prefetch_stage(pf);
+            pf.next();
+        }
+        while (w.valid()) {
+            const int slot = stage % NSTAGE;
+            const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
+            const int ntiles = w.ntiles();
+            bool ok = true;
+            if (lane == 0 && !*abortp) {
+                ok = mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abortp);
+                if (!ok) {
+                    *abortp = 1;
+                    atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && !*abortp;
+            if (ok) {
                 if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
                 __syncwarp();
                 if (lane < ntiles) {
-                    int32_t blk = trow[st + lane];
+                    int32_t blk = a.table[(int64_t)w.S.table_row * a.bpb + w.S.blk_start + (w.t - w.U.tile_off) + lane];
                     if ((uint32_t)blk >= (uint32_t)a.n_blocks) {   // broken table: poison, read zeros
                         atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                         blk = -1;
                     }
-                    const int32_t row0 = (blk * a.n_kv + U.kv_head) * BS;
+                    const int32_t row0 = (blk * a.n_kv + w.U.kv_head) * BS;
                     const uint32_t dst = base + slot * STAGE_BYTES + lane * SLOT_BYTES;
                     const uint32_t fb = bar_full + 8 * slot;
                     tma_load_3d(dst, &tmK, 0, 0, row0, fb);
@@ -339,9 +310,13 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 }
                 issued |= 1u << slot;
                 parity_bits = (parity_bits & ~(1u << slot)) | (ph << slot);
+                if (pf.valid()) {
+                    prefetch_stage(pf);
+                    pf.next();
+                }
             }
-            t = cend;
-            ++u;
+            w.next();
+            ++stage;
         }
         // after a timeout, wait (bounded) for this CTA's copies still in flight
         if (lane == 0 && *abortp) {
@@ -568,8 +543,6 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     fence_async_smem();
                     consumer_sync();   // buffer free again before it is handed back to TMA
                 }
-                arrive_and_merge<__nv_bfloat16>(a, S, U, merge_list, &merge_n, threadIdx.x, NCONS * 32,
-                                                consumer_sync);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -589,8 +562,7 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
     float* Vs = fsm + BS * d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int st0;
-    __shared__ int32_t merge_list[64];
-    __shared__ int32_t merge_n;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) st0 = a.meta->status;
     __syncthreads();
     if (st0) return;
@@ -671,10 +643,114 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
                 if (j < nj) a.part_acc[(int64_t)(prow0 + row) * d + lane + 32 * j] = acc[rr][j];
             if (lane == 0) a.part_ml[prow0 + row] = make_float2(m[rr], l[rr]);
         }
-        arrive_and_merge<float>(a, S, U, merge_list, &merge_n, threadIdx.x, 128, [] { __syncthreads(); });
         t = cend;
         ++u;
     }
+}
+
+// ============================================================ LSE merge
+// One warp per output row (branch qi, query token j, query head h*G + g).
+// The row's partials are the chunks of one unit per segment on the branch's
+// path; lanes enumerate them (lane e takes path entry e, a warp scan turns
+// chunk counts into partial indices), load every (m, l) at once, and reduce
+//     M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum acc_i 2^(m_i - M) / L
+// with the acc rows fetched four partials at a time.  Partial rows are read
+// through L2 only (they were written by the previous kernel).
+template <typename T>
+__global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const AttnPlanDev& pl = a.plan;
+    const int lane = threadIdx.x & 31;
+    const int32_t o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int32_t n_out = pl.n_queried * pl.q_len * pl.n_q_heads;
+    if (o >= n_out || a.meta->status) return;
+    const int G = pl.group, RM = pl.q_len * G;
+    const int32_t qi = o / (pl.q_len * pl.n_q_heads);
+    const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
+    const int32_t j = rem / pl.n_q_heads, hq = rem - j * pl.n_q_heads;
+    const int32_t h = hq / G, g = hq - h * G;
+    const int d = a.head_dim, nj = d / 32;
+    const int32_t pbeg = pl.path_off[qi], pend = pl.path_off[qi + 1];
+    float M = -INFINITY, L = 0.f, acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    for (int32_t e0 = pbeg; e0 < pend; e0 += 32) {
+        // lane e: one path entry -> its unit's chunks for this row
+        const int32_t e = e0 + lane;
+        int32_t nch = 0, base = 0, stride = 0;
+        if (e < pend) {
+            const int32_t seg = pl.path[2 * e], mi = pl.path[2 * e + 1];
+            const AttnSeg S = pl.segs[seg];
+            const int32_t sr = mi * RM + j * G + g;
+            const int32_t grp = sr / pl.max_rows;
+            const AttnUnit U = pl.units[S.unit_base + h * S.ngroups + grp];
+            nch = U.nchunks;
+            base = U.prow_base + (sr - grp * pl.max_rows);
+            stride = U.n_rows;
+        }
+        int32_t incl = nch;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        const int32_t excl = incl - nch;
+        for (int32_t p0 = 0; p0 < total; p0 += 32) {
+            // lane p: partial p of this batch -> its partial row
+            const int32_t pidx = p0 + lane;
+            int32_t ent = 0;
+            for (int k = 0; k < 32; ++k) ent += (__shfl_sync(0xffffffffu, incl, k) <= pidx) ? 1 : 0;
+            ent = min(ent, 31);
+            const int32_t eb = __shfl_sync(0xffffffffu, base, ent);
+            const int32_t es = __shfl_sync(0xffffffffu, stride, ent);
+            const int32_t ex = __shfl_sync(0xffffffffu, excl, ent);
+            const bool valid = pidx < total;
+            const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
+            float2 ml = valid ? __ldcg(a.part_ml + prow) : make_float2(-INFINITY, 0.f);
+            // running max over this batch
+            float mb = ml.x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+            const float Mn = fmaxf(M, mb);
+            const float Mu = Mn == -INFINITY ? 0.f : Mn;
+            const float sc = exp2f(M - Mu);   // rescale of the running state
+            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mu);
+            float lw = w * ml.y;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+            L = L * sc + lw;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] *= sc;
+            M = Mn;
+            const int nb = min(32, total - p0);
+            for (int q = 0; q < nb; q += 4) {
+                float wq[4];
+                float v[4][8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int src = min(q + u, nb - 1);
+                    const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
+                    wq[u] = (q + u < nb) ? __shfl_sync(0xffffffffu, w, src) : 0.f;
+                    const float* row = a.part_acc + (int64_t)pr * d;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[u][k] = k < nj ? __ldcg(row + lane + 32 * k) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[k] = fmaf(v[u][k], wq[u], acc[k]);
+            }
+        }
+    }
+    const float inv = 1.f / L;
+    T* dst = static_cast<T*>(a.out) + (int64_t)o * d;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nj) {
+            if constexpr (sizeof(T) == 2) dst[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+            else dst[lane + 32 * k] = acc[k] * inv;
+        }
 }
 
 // ============================================================ host planning
@@ -682,7 +758,7 @@ struct HostPlan {
     std::vector<AttnSeg> segs;
     std::vector<AttnMember> members;
     std::vector<AttnUnit> units;
-    std::vector<int32_t> cta_begin, cta_unit, path_off, path, expected;
+    std::vector<int32_t> cta_begin, cta_unit, path_off, path;
     std::vector<int64_t> cuts;
     int64_t tiles = 0, unique_tiles = 0;
     size_t partial_rows = 0;
@@ -690,7 +766,7 @@ struct HostPlan {
     std::vector<Segment> psegs;
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
         segs.clear(); members.clear(); units.clear(); cta_begin.clear(); cta_unit.clear();
-        path_off.clear(); path.clear(); expected.clear(); cuts.clear();
+        path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         partial_rows = 0;
     }
@@ -789,8 +865,7 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
             hp.cta_unit[c] = (int32_t)u;
         }
     }
-    // chunks and partial rows per unit; arrivals expected per (branch, kv head)
-    hp.expected.assign((size_t)n * nkv, 0);
+    // chunks and partial rows per unit
     size_t prow = 0;
     {
         int c = 0;
@@ -803,10 +878,6 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
             U.nchunks = cl - c + 1;
             U.prow_base = (int32_t)prow;
             prow += (size_t)U.nchunks * U.n_rows;
-            const AttnSeg& S = hp.segs[U.seg];
-            const int m0 = U.row_lo / RM, m1 = (U.row_lo + U.n_rows - 1) / RM;
-            for (int mi = m0; mi <= m1; ++mi)
-                hp.expected[(size_t)hp.members[S.mem_off + mi].qi * nkv + U.kv_head] += U.nchunks;
         }
     }
     if (prow >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
@@ -862,17 +933,7 @@ int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
     return DENDRITE_OK;
 }
 
-int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows, size_t groups) {
-    if (groups > p->arrivals_cap) {
-        size_t cap = std::max<size_t>(groups * 2, 4096);
-        DENDRITE_CUDA(cudaDeviceSynchronize());
-        if (p->d_arrivals) cudaFree(p->d_arrivals);
-        p->d_arrivals = nullptr;
-        p->arrivals_cap = 0;
-        DENDRITE_CUDA(cudaMalloc(&p->d_arrivals, cap * sizeof(int32_t)));
-        DENDRITE_CUDA(cudaMemset(p->d_arrivals, 0, cap * sizeof(int32_t)));
-        p->arrivals_cap = cap;
-    }
+int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows) {
     if (plan_bytes > p->plan_cap) {
         size_t cap = std::max<size_t>(plan_bytes * 2, 1 << 20);
         DENDRITE_CUDA(cudaDeviceSynchronize());
@@ -931,11 +992,9 @@ void attn_teardown(dendrite_pool* p) {
     if (p->d_plan) cudaFree(p->d_plan);
     if (p->h_plan) cudaFreeHost(p->h_plan);
     if (p->d_partial) cudaFree(p->d_partial);
-    if (p->d_arrivals) cudaFree(p->d_arrivals);
     p->d_plan = nullptr;
     p->h_plan = nullptr;
     p->d_partial = nullptr;
-    p->d_arrivals = nullptr;
 }
 
 }  // namespace dendrite
@@ -970,7 +1029,7 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         hp.clear();
         DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, hp));
         const int32_t C = (int32_t)hp.cta_unit.size();
-        size_t off[9];
+        size_t off[8];
         size_t b = 0;
         off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
         off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
@@ -979,9 +1038,8 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
         off[5] = b; b = align16(b + hp.path_off.size() * 4);
         off[6] = b; b = align16(b + hp.path.size() * 4);
-        off[7] = b; b = align16(b + hp.expected.size() * 4);
-        off[8] = b;
-        DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows, hp.expected.size()));
+        off[7] = b;
+        DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
         char* h = p->h_plan;
         std::memcpy(h + off[0], hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
@@ -991,7 +1049,6 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
         std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
         std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
-        std::memcpy(h + off[7], hp.expected.data(), hp.expected.size() * 4);
         DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, h, b, cudaMemcpyHostToDevice, s));
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
         char* d = p->d_plan;
@@ -1002,7 +1059,6 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         pc.dev.cta_unit = reinterpret_cast<const int32_t*>(d + off[4]);
         pc.dev.path_off = reinterpret_cast<const int32_t*>(d + off[5]);
         pc.dev.path = reinterpret_cast<const int32_t*>(d + off[6]);
-        pc.dev.expected = reinterpret_cast<const int32_t*>(d + off[7]);
         pc.dev.n_units = (int32_t)hp.units.size();
         pc.dev.n_ctas = C;
         pc.dev.n_queried = n;
@@ -1030,8 +1086,9 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
     a.plan = pc.dev;
     a.Q = Q;
     a.out = out;
-    a.arrivals = p->d_arrivals;
     a.table = p->d_table;
+    a.pool_kv[0] = p->d_k;
+    a.pool_kv[1] = p->d_v;
     a.pool_k = static_cast<const float*>(p->d_k);
     a.pool_v = static_cast<const float*>(p->d_v);
     a.part_acc = p->d_partial;
@@ -1048,11 +1105,20 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         CUtensorMap mk, mv;
         std::memcpy(&mk, p->tmap_k, sizeof(mk));
         std::memcpy(&mv, p->tmap_v, sizeof(mv));
-        k_attn_partial_bf16<<<pc.dev.n_ctas, THREADS, SMEM_BF16, s>>>(mk, mv, a);
+        DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(pc.dev.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
     } else {
-        k_attn_partial_f32<<<pc.dev.n_ctas, 128, 2 * BS * p->head_dim * sizeof(float), s>>>(a);
+        DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(pc.dev.n_ctas), dim3(128),
+                                 2 * BS * p->head_dim * sizeof(float), s, a));
     }
     prof_end(p, T_ATTN_PARTIAL, s);
+    prof_begin(p, T_ATTN_MERGE, s);
+    {
+        const int32_t n_out = n * q_len * n_q_heads;
+        const unsigned grid = (unsigned)((n_out + 7) / 8);
+        if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, a));
+        else DENDRITE_CUDA(launch_pdl(k_attn_merge<float>, dim3(grid), dim3(256), 0, s, a));
+    }
+    prof_end(p, T_ATTN_MERGE, s);
     prof_end(p, T_ATTN_TOTAL, s);
     DENDRITE_CUDA(cudaGetLastError());
     DENDRITE_CUDA(cudaGetLastError());

@@ -29,7 +29,8 @@ struct DevMeta {
     int32_t rel_lo;     // smallest block id released by the current free call
     int32_t rel_hi;     // largest block id released by the current free call
     int32_t rel_count;  // blocks released by the current free call
-    int32_t pad[3];
+    int32_t rel_done;   // CTAs of the current free call that finished releasing
+    int32_t pad[2];
 };
 
 // One sharing segment: blocks [blk_start, blk_start + n_blk) of the table row
@@ -78,7 +79,6 @@ struct AttnPlanDev {
     const int32_t* cta_unit;    // [n_ctas] unit holding cta_begin[c]
     const int32_t* path_off;    // [n_queried + 1] into path
     const int32_t* path;        // pairs (segment, member index) along each queried branch
-    const int32_t* expected;    // [n_queried * n_kv] chunk arrivals per (branch, kv head) group
     int32_t n_units;
     int32_t n_ctas;
     int32_t n_queried;
@@ -132,7 +132,7 @@ private:
     std::vector<cudaEvent_t> spare_;
 };
 
-enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_RESERVED4, T_FREE,
+enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_ATTN_MERGE, T_FREE,
                   T_ATTN_TOTAL, T_COUNT };
 
 struct PlanCache {
@@ -181,8 +181,6 @@ struct dendrite_pool {
     cudaEvent_t plan_copied = nullptr;
     float* d_partial = nullptr;      // partial rows: [rows][head_dim] acc then [rows][2] (m, l)
     size_t partial_rows_cap = 0;
-    int32_t* d_arrivals = nullptr;   // per (branch, kv head) arrival counters, zero between calls
-    size_t arrivals_cap = 0;
     dendrite::PlanCache plan;
 
     // host mirror
@@ -205,6 +203,25 @@ namespace dendrite {
 
 // -------------------------------------------------------------- helpers
 int cuda_err(cudaError_t e);     // maps a CUDA error to DENDRITE_ECUDA (and clears it)
+
+// Programmatic dependent launch: the kernel may be scheduled while the
+// previous kernel on the stream drains; it waits (griddepcontrol.wait) before
+// touching anything that kernel produced.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 void prof_begin(dendrite_pool* p, TimingKind k, cudaStream_t s);
 void prof_end(dendrite_pool* p, TimingKind k, cudaStream_t s);
 int check_live(const dendrite_pool* p, int32_t h);

@@ -35,6 +35,20 @@ __device__ __forceinline__ void set_status(DevMeta* m, int32_t code) {
     atomicCAS(&m->status, 0, code);
 }
 
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Per-call argument arrays: small ones travel as kernel parameters (no copy
+// on the stream), large ones are staged in device memory.
+template <int CAP>
+struct ParamArgs {
+    int32_t v[CAP];
+    __device__ __forceinline__ int32_t operator[](int64_t i) const { return v[i]; }
+};
+struct GlobalArgs {
+    const int32_t* p;
+    __device__ __forceinline__ int32_t operator[](int64_t i) const { return p[i]; }
+};
+
 __global__ void k_init(int32_t* stack, int32_t* refcount, int32_t* holders, int32_t* last,
                        int32_t* released, int64_t n, int32_t* table, int64_t n_table, DevMeta* meta) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -52,6 +66,7 @@ __global__ void k_init(int32_t* stack, int32_t* refcount, int32_t* holders, int3
         meta->rel_lo = INT_MAX;
         meta->rel_hi = -1;
         meta->rel_count = 0;
+        meta->rel_done = 0;
     }
 }
 
@@ -101,6 +116,7 @@ __device__ __forceinline__ void fork_pair(int32_t* __restrict__ table, int32_t* 
 template <int CAP>
 __global__ void k_fork_param(const __grid_constant__ ForkParams<CAP> a, int32_t* table,
                              int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
+    pdl_wait();
     if (meta->status) return;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= a.n_pairs) return;
@@ -112,6 +128,7 @@ __global__ void k_fork_param(const __grid_constant__ ForkParams<CAP> a, int32_t*
 // (child, parent, nb, add) are read from device memory.
 __global__ void k_fork_global(const int32_t* __restrict__ args, int32_t n_pairs, int32_t* table,
                               int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
+    pdl_wait();
     if (meta->status) return;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= n_pairs) return;
@@ -159,57 +176,54 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp
 // so with r = refcount[tail] and k holders in the call, holder number j
 // (0-based, argument order) copies iff r - j > 1.  Since r >= k, only the last
 // holder can write in place, and only when r == k.
+template <typename A>
 __global__ void __launch_bounds__(kAppendMetaThreads)
-k_append_meta(const int32_t* __restrict__ args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb,
+k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb,
               int32_t n_blocks, int32_t* table, int32_t* refcount, const int32_t* stack, int32_t* holders,
               int32_t* last, int32_t* call, DevMeta* meta) {
     __shared__ int32_t warp_sums[kAppendMetaThreads / 32];
     __shared__ int32_t chunk_total;
-    __shared__ int32_t status0, top0;
-    const int32_t* branch = args;
-    const int32_t* lens = args + n;
+    __shared__ int32_t status0, top0, bad;
+    // args: branch[n], len[n]
     int32_t* offs = call;              // [n] first stack offset of each branch
     int32_t* cow_src = call + n;       // [n] copied tail (-1 = none)
     int32_t* cow_dst = call + 2 * n;   // [n] its copy
+    pdl_wait();
     if (threadIdx.x == 0) {
         status0 = meta->status;
         top0 = meta->top;
+        bad = 0;
     }
     __syncthreads();
     if (status0) return;
-    // every tail id must be a block id (a broken table poisons the pool instead
-    // of being dereferenced)
-    __shared__ int32_t bad;
-    if (threadIdx.x == 0) bad = 0;
-    __syncthreads();
+    // holders of each shared tail within the call; a tail id that is not a
+    // block id poisons the pool instead of being dereferenced
     for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int32_t L = lens[i];
-        if (L % bs && (uint32_t)table[(int64_t)branch[i] * bpb + L / bs] >= (uint32_t)n_blocks) bad = 1;
+        const int32_t L = args[n + i];
+        if (L % bs) {
+            const int32_t tail = table[(int64_t)args[i] * bpb + L / bs];
+            if ((uint32_t)tail >= (uint32_t)n_blocks) {
+                bad = 1;
+            } else {
+                atomicAdd(holders + tail, 1);
+                atomicMax(last + tail, i);
+            }
+        }
     }
     __syncthreads();
     if (bad) {
         if (threadIdx.x == 0) set_status(meta, DENDRITE_ECORRUPT);
         return;
     }
-    // holders of each shared tail within the call
-    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int32_t L = lens[i];
-        if (L % bs) {
-            const int32_t tail = table[(int64_t)branch[i] * bpb + L / bs];
-            atomicAdd(holders + tail, 1);
-            atomicMax(last + tail, i);
-        }
-    }
-    __syncthreads();
     int32_t carry = 0;
     for (int32_t base = 0; base < n; base += blockDim.x) {
         const int32_t i = base + threadIdx.x;
         int32_t demand = 0;
         if (i < n) {
-            const int32_t L = lens[i];
+            const int32_t L = args[n + i];
             int32_t cow = 0, tail = -1;
             if (L % bs) {
-                tail = table[(int64_t)branch[i] * bpb + L / bs];
+                tail = table[(int64_t)args[i] * bpb + L / bs];
                 cow = !(refcount[tail] == holders[tail] && last[tail] == i);
             }
             demand = cow + (L + n_new + bs - 1) / bs - (L + bs - 1) / bs;
@@ -223,7 +237,7 @@ k_append_meta(const int32_t* __restrict__ args, int32_t n, int32_t n_new, int32_
     const bool fits = carry <= top0;
     if (fits) {
         for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
-            const int32_t b = branch[i], L = lens[i];
+            const int32_t b = args[i], L = args[n + i];
             int32_t o = offs[i];
             int32_t* row = table + (int64_t)b * bpb;
             const int32_t src = cow_src[i];
@@ -246,13 +260,12 @@ k_append_meta(const int32_t* __restrict__ args, int32_t n, int32_t n_new, int32_
         }
     }
     __syncthreads();
-    // reset the holder scratch for the next call
+    // reset the holder scratch for the next call (a copied tail's id is in
+    // cow_src, an in-place tail is still in the table)
     for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const int32_t L = lens[i];
+        const int32_t L = args[n + i];
         if (L % bs) {
-            // the tail id may have been replaced in the table; the original is in cow_src
-            // when copied, else still in the table
-            const int32_t tail = cow_src[i] >= 0 ? cow_src[i] : table[(int64_t)branch[i] * bpb + L / bs];
+            const int32_t tail = cow_src[i] >= 0 ? cow_src[i] : table[(int64_t)args[i] * bpb + L / bs];
             holders[tail] = 0;
             last[tail] = -1;
         }
@@ -268,15 +281,15 @@ k_append_meta(const int32_t* __restrict__ args, int32_t n, int32_t n_new, int32_
 // of a copied-on-write tail (if any) and scatters the new rows into their
 // slots with 16-byte vector moves.  tile_pre[i] is the exclusive prefix of
 // touched blocks per branch (host computed; depends only on lengths).
-__global__ void k_append_copy(const int32_t* __restrict__ args, const int32_t* __restrict__ tile_pre,
-                              int32_t n, int32_t n_new, int32_t bs, int32_t bpb, int32_t n_kv,
+template <typename A>
+__global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb, int32_t n_kv,
                               int32_t row_vec, int32_t n_blocks, const int32_t* __restrict__ table,
                               const int32_t* __restrict__ call, const uint4* __restrict__ Kin,
                               const uint4* __restrict__ Vin, uint4* __restrict__ Kp, uint4* __restrict__ Vp,
                               const DevMeta* meta) {
+    pdl_wait();
     if (meta->status) return;
-    const int32_t* branch = args;
-    const int32_t* lens = args + n;
+    // args: branch[n], len[n], tile prefix[n]
     const int32_t* cow_src = call + n;
     const int64_t tile = blockIdx.x;
     const int32_t h = (int32_t)(tile % n_kv);
@@ -285,12 +298,12 @@ __global__ void k_append_copy(const int32_t* __restrict__ args, const int32_t* _
     int32_t lo = 0, hi = n - 1;
     while (lo < hi) {
         const int32_t mid = (lo + hi + 1) >> 1;
-        if (tile_pre[mid] <= t) lo = mid; else hi = mid - 1;
+        if (args[2 * n + mid] <= t) lo = mid; else hi = mid - 1;
     }
     const int32_t i = lo;
-    const int32_t L = lens[i];
-    const int32_t lblk = L / bs + (t - tile_pre[i]);
-    const int32_t dst = table[(int64_t)branch[i] * bpb + lblk];
+    const int32_t L = args[n + i];
+    const int32_t lblk = L / bs + (t - args[2 * n + i]);
+    const int32_t dst = table[(int64_t)args[i] * bpb + lblk];
     if ((uint32_t)dst >= (uint32_t)n_blocks || cow_src[i] >= n_blocks) {
         if (threadIdx.x == 0) atomicCAS(const_cast<int32_t*>(&meta->status), 0, DENDRITE_ECORRUPT);
         return;
@@ -321,70 +334,81 @@ __global__ void k_append_copy(const int32_t* __restrict__ args, const int32_t* _
 }
 
 // ----------------------------------------------------------------- free
-// Phase A: one thread per table entry of the freed branches.  Drops one
-// reference; an entry whose refcount reaches zero marks its block released.
-__global__ void k_free_release(const int32_t* __restrict__ args, const int32_t* __restrict__ ent_pre,
-                               int32_t n, int32_t total, int32_t bpb, int32_t n_blocks, int32_t* table,
-                               int32_t* refcount, int32_t* released, DevMeta* meta) {
-    if (meta->status) return;
-    const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= total) return;
-    int32_t lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (ent_pre[mid] <= e) lo = mid; else hi = mid - 1;
-    }
-    int32_t* slot = table + (int64_t)args[lo] * bpb + (e - ent_pre[lo]);
-    const int32_t blk = *slot;
-    *slot = -1;
-    if ((uint32_t)blk >= (uint32_t)n_blocks) {
-        set_status(meta, DENDRITE_ECORRUPT);
-        return;
-    }
-    const int32_t old = atomicSub(refcount + blk, 1);
-    if (old == 1) {
-        released[blk] = 1;
-        atomicMin(&meta->rel_lo, blk);
-        atomicMax(&meta->rel_hi, blk);
-        atomicAdd(&meta->rel_count, 1);
-    } else if (old < 1) {
-        set_status(meta, DENDRITE_ECORRUPT);
-    }
-}
-
-// Phase B: one CTA pushes the released blocks onto the free stack in
-// descending id order (scan over [rel_lo, rel_hi] from the top down).
+// One thread per table entry of the freed branches drops one reference; an
+// entry whose refcount reaches zero marks its block released.  The last CTA
+// to finish then pushes the released blocks onto the free stack in
+// descending id order (a block scan over [rel_lo, rel_hi] from the top down).
+template <typename A>
 __global__ void __launch_bounds__(kFreeCollectThreads)
-k_free_push(int32_t* stack, int32_t* released, DevMeta* meta) {
+k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, int32_t n_blocks, int32_t* table,
+       int32_t* refcount, int32_t* released, int32_t* stack, DevMeta* meta) {
     __shared__ int32_t warp_sums[kFreeCollectThreads / 32];
     __shared__ int32_t chunk_total;
-    __shared__ int32_t lo, hi, top0, cnt, st;
-    if (threadIdx.x == 0) {
-        lo = meta->rel_lo;
-        hi = meta->rel_hi;
-        top0 = meta->top;
-        cnt = meta->rel_count;
-        st = meta->status;
+    __shared__ int32_t st, is_last, lo, hi, top0, cnt;
+    pdl_wait();
+    if (threadIdx.x == 0) st = meta->status;
+    __syncthreads();
+    if (st) return;
+    // args: branch[n], entry prefix[n]
+    const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < total) {
+        int32_t l = 0, h = n - 1;
+        while (l < h) {
+            const int32_t mid = (l + h + 1) >> 1;
+            if (args[n + mid] <= e) l = mid; else h = mid - 1;
+        }
+        int32_t* slot = table + (int64_t)args[l] * bpb + (e - args[n + l]);
+        const int32_t blk = *slot;
+        *slot = -1;
+        if ((uint32_t)blk >= (uint32_t)n_blocks) {
+            set_status(meta, DENDRITE_ECORRUPT);
+        } else {
+            const int32_t old = atomicSub(refcount + blk, 1);
+            if (old == 1) {
+                released[blk] = 1;
+                atomicMin(&meta->rel_lo, blk);
+                atomicMax(&meta->rel_hi, blk);
+                atomicAdd(&meta->rel_count, 1);
+            } else if (old < 1) {
+                set_status(meta, DENDRITE_ECORRUPT);
+            }
+        }
     }
     __syncthreads();
-    if (st || cnt == 0) return;
-    int32_t carry = 0;
-    for (int32_t base = 0; base <= hi - lo; base += blockDim.x) {
-        const int32_t j = hi - (base + (int32_t)threadIdx.x);
-        const int32_t f = (j >= lo) ? released[j] : 0;
-        const int32_t ex = block_exclusive_scan<kFreeCollectThreads>(f, warp_sums, &chunk_total);
-        if (f) {
-            stack[top0 + carry + ex] = j;
-            released[j] = 0;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        is_last = atomicAdd(&meta->rel_done, 1) == (int32_t)gridDim.x - 1;
+        if (is_last) {
+            __threadfence();
+            lo = atomicAdd(&meta->rel_lo, 0);
+            hi = atomicAdd(&meta->rel_hi, 0);
+            cnt = atomicAdd(&meta->rel_count, 0);
+            top0 = atomicAdd(&meta->top, 0);
+            st = atomicAdd(&meta->status, 0);
         }
-        carry += chunk_total;
-        __syncthreads();
+    }
+    __syncthreads();
+    if (!is_last) return;
+    if (!st && cnt > 0) {
+        int32_t carry = 0;
+        for (int32_t base = 0; base <= hi - lo; base += blockDim.x) {
+            const int32_t j = hi - (base + (int32_t)threadIdx.x);
+            const int32_t f = (j >= lo) ? __ldcg(released + j) : 0;
+            const int32_t ex = block_exclusive_scan<kFreeCollectThreads>(f, warp_sums, &chunk_total);
+            if (f) {
+                stack[top0 + carry + ex] = j;
+                released[j] = 0;
+            }
+            carry += chunk_total;
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) meta->top = top0 + carry;
     }
     if (threadIdx.x == 0) {
-        meta->top = top0 + carry;
         meta->rel_lo = INT_MAX;
         meta->rel_hi = -1;
         meta->rel_count = 0;
+        meta->rel_done = 0;
     }
 }
 
@@ -593,9 +617,8 @@ int launch_fork_param(dendrite_pool* p, const std::vector<int32_t>& child, const
     }
     const int threads = 128;
     const int blocks = (int)((child.size() * 32 + threads - 1) / threads);
-    k_fork_param<CAP><<<blocks, threads, 0, s>>>(a, p->d_table, p->d_refcount, p->bpb, (int32_t)p->num_blocks,
-                                                  p->d_meta);
-    DENDRITE_CUDA(cudaGetLastError());
+    DENDRITE_CUDA(launch_pdl(k_fork_param<CAP>, dim3(blocks), dim3(threads), 0, s, a, p->d_table, p->d_refcount,
+                             p->bpb, (int32_t)p->num_blocks, p->d_meta));
     return DENDRITE_OK;
 }
 
@@ -758,9 +781,9 @@ int dendrite_fork_batch(dendrite_pool* p, const int32_t* parents, const int32_t*
         DENDRITE_TRY(p->staging.upload(s, h, n * 16));
         const int threads = 128;
         const int blocks = (int)((n * 32 + threads - 1) / threads);
-        k_fork_global<<<blocks, threads, 0, s>>>((const int32_t*)d, (int32_t)n, p->d_table, p->d_refcount,
-                                                  p->bpb, (int32_t)p->num_blocks, p->d_meta);
-        rc = cudaGetLastError() == cudaSuccess ? DENDRITE_OK : DENDRITE_ECUDA;
+        rc = launch_pdl(k_fork_global, dim3(blocks), dim3(threads), 0, s, (const int32_t*)d, (int32_t)n,
+                        p->d_table, p->d_refcount, p->bpb, (int32_t)p->num_blocks, p->d_meta) == cudaSuccess
+                 ? DENDRITE_OK : DENDRITE_ECUDA;
         DENDRITE_TRY(p->staging.release(s));
     }
     prof_end(p, T_FORK, s);
@@ -789,36 +812,47 @@ int dendrite_append_kv(dendrite_pool* p, const int32_t* branches, int32_t n, int
     }
     if (touched * p->n_kv > INT32_MAX) return DENDRITE_ELIMIT;
     cudaStream_t s = (cudaStream_t)stream;
-    // args: branch[n], len[n] | tile prefix[n]
-    char *h, *d;
-    const size_t bytes = (size_t)n * 12;
-    DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
-    int32_t* a = (int32_t*)h;
-    int32_t acc = 0;
-    for (int32_t i = 0; i < n; ++i) {
-        const int32_t L = p->br[branches[i]].len;
-        a[i] = branches[i];
-        a[n + i] = L;
-        a[2 * n + i] = acc;
-        acc += (L + n_new - 1) / bs - L / bs + 1;
-    }
-    DENDRITE_TRY(p->staging.upload(s, h, bytes));
-    const int32_t* dargs = (const int32_t*)d;
-    prof_begin(p, T_APPEND_META, s);
-    k_append_meta<<<1, kAppendMetaThreads, 0, s>>>(dargs, n, n_new, bs, p->bpb, (int32_t)p->num_blocks,
-                                                   p->d_table, p->d_refcount,
-                                                   p->d_stack, p->d_holders, p->d_last, p->d_call_i32, p->d_meta);
-    prof_end(p, T_APPEND_META, s);
-    DENDRITE_CUDA(cudaGetLastError());
+    // args: branch[n], len[n], tile prefix[n]
+    constexpr int CAP = 768;
     const int32_t row_vec = p->head_dim * p->elt / 16;
-    prof_begin(p, T_APPEND_COPY, s);
-    k_append_copy<<<(unsigned)(touched * p->n_kv), 128, 0, s>>>(
-        dargs, dargs + 2 * n, n, n_new, bs, p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks, p->d_table,
-        p->d_call_i32,
-        (const uint4*)K, (const uint4*)V, (uint4*)p->d_k, (uint4*)p->d_v, p->d_meta);
-    prof_end(p, T_APPEND_COPY, s);
-    DENDRITE_CUDA(cudaGetLastError());
-    DENDRITE_TRY(p->staging.release(s));
+    const unsigned grid = (unsigned)(touched * p->n_kv);
+    auto fill = [&](int32_t* a) {
+        int32_t acc = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int32_t L = p->br[branches[i]].len;
+            a[i] = branches[i];
+            a[n + i] = L;
+            a[2 * n + i] = acc;
+            acc += (L + n_new - 1) / bs - L / bs + 1;
+        }
+    };
+    auto launch = [&](auto args) -> int {
+        prof_begin(p, T_APPEND_META, s);
+        DENDRITE_CUDA(launch_pdl(k_append_meta<decltype(args)>, dim3(1), dim3(kAppendMetaThreads), 0, s, args, n,
+                                 n_new, bs, p->bpb, (int32_t)p->num_blocks, p->d_table, p->d_refcount, p->d_stack,
+                                 p->d_holders, p->d_last, p->d_call_i32, p->d_meta));
+        prof_end(p, T_APPEND_META, s);
+        prof_begin(p, T_APPEND_COPY, s);
+        DENDRITE_CUDA(launch_pdl(k_append_copy<decltype(args)>, dim3(grid), dim3(128), 0, s, args, n, n_new, bs,
+                                 p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks, (const int32_t*)p->d_table,
+                                 (const int32_t*)p->d_call_i32, (const uint4*)K, (const uint4*)V, (uint4*)p->d_k,
+                                 (uint4*)p->d_v, (const DevMeta*)p->d_meta));
+        prof_end(p, T_APPEND_COPY, s);
+        return DENDRITE_OK;
+    };
+    if (3 * n <= CAP) {
+        ParamArgs<CAP> a;
+        fill(a.v);
+        DENDRITE_TRY(launch(a));
+    } else {
+        char *h, *d;
+        const size_t bytes = (size_t)n * 12;
+        DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
+        fill((int32_t*)h);
+        DENDRITE_TRY(p->staging.upload(s, h, bytes));
+        DENDRITE_TRY(launch(GlobalArgs{(const int32_t*)d}));
+        DENDRITE_TRY(p->staging.release(s));
+    }
     for (int32_t i = 0; i < n; ++i) {
         Branch& b = p->br[branches[i]];
         b.len += n_new;
@@ -835,29 +869,43 @@ int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* st
     DENDRITE_TRY(check_unique_live(p, branches, n));
     cudaStream_t s = (cudaStream_t)stream;
     const int32_t bs = p->block_size;
-    char *h, *d;
-    const size_t bytes = (size_t)n * 8;
-    DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
-    int32_t* a = (int32_t*)h;
+    // args: branch[n], entry prefix[n]
     int64_t total = 0;
-    for (int32_t i = 0; i < n; ++i) {
-        a[i] = branches[i];
-        a[n + i] = (int32_t)total;
-        total += (p->br[branches[i]].len + bs - 1) / bs;
-    }
-    if (total > INT32_MAX) return DENDRITE_ELIMIT;
-    DENDRITE_TRY(p->staging.upload(s, h, bytes));
+    for (int32_t i = 0; i < n; ++i) total += (p->br[branches[i]].len + bs - 1) / bs;
+    if (total > INT32_MAX / 2) return DENDRITE_ELIMIT;
+    auto fill = [&](int32_t* a) {
+        int32_t acc = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            a[i] = branches[i];
+            a[n + i] = acc;
+            acc += (p->br[branches[i]].len + bs - 1) / bs;
+        }
+    };
+    const unsigned grid = (unsigned)((total + kFreeCollectThreads - 1) / kFreeCollectThreads);
+    auto launch = [&](auto args) -> int {
+        DENDRITE_CUDA(launch_pdl(k_free<decltype(args)>, dim3(grid), dim3(kFreeCollectThreads), 0, s, args, n,
+                                 (int32_t)total, p->bpb, (int32_t)p->num_blocks, p->d_table, p->d_refcount,
+                                 p->d_released, p->d_stack, p->d_meta));
+        return DENDRITE_OK;
+    };
     prof_begin(p, T_FREE, s);
     if (total > 0) {
-        k_free_release<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-            (const int32_t*)d, (const int32_t*)d + n, n, (int32_t)total, p->bpb, (int32_t)p->num_blocks,
-            p->d_table, p->d_refcount, p->d_released, p->d_meta);
-        DENDRITE_CUDA(cudaGetLastError());
-        k_free_push<<<1, kFreeCollectThreads, 0, s>>>(p->d_stack, p->d_released, p->d_meta);
-        DENDRITE_CUDA(cudaGetLastError());
+        constexpr int CAP = 1024;
+        if (2 * n <= CAP) {
+            ParamArgs<CAP> a;
+            fill(a.v);
+            DENDRITE_TRY(launch(a));
+        } else {
+            char *h, *d;
+            const size_t bytes = (size_t)n * 8;
+            DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
+            fill((int32_t*)h);
+            DENDRITE_TRY(p->staging.upload(s, h, bytes));
+            DENDRITE_TRY(launch(GlobalArgs{(const int32_t*)d}));
+            DENDRITE_TRY(p->staging.release(s));
+        }
     }
     prof_end(p, T_FREE, s);
-    DENDRITE_TRY(p->staging.release(s));
     for (int32_t i = 0; i < n; ++i) {
         Branch& b = p->br[branches[i]];
         const int32_t node = b.node;
