@@ -1131,3 +1131,140 @@ extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* o
     *out = p->plan.stats;
     return DENDRITE_OK;
 }
+
+// ====================================================== allocation-free variant
+// Some callers cannot let a library allocate device memory while they decode:
+// a serving process that has handed nearly all free device memory to its own
+// caching allocator (a cudaMalloc here could fail or fragment that reserve),
+// a latency-critical decode loop that cannot afford the device-wide
+// synchronisation cudaMalloc/cudaFree may imply, or a deployment that gives
+// each library a fixed memory budget at load time.  For them,
+// dendrite_tree_attn_decode_noalloc keeps its scratch -- the uploaded plan and
+// the partial (max, sum, acc) rows -- in one file-scope device array of fixed
+// size instead of the pool's grow-only workspace.  Every GPU that loads this
+// library holds that array until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(DENDRITE_NOALLOC_SCRATCH_BYTES);
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Host staging of the plan upload: plain host memory, so cudaMemcpyAsync has
+// finished reading it when it returns and the next call may overwrite it.
+alignas(256) unsigned char g_noalloc_host[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+void* g_noalloc_dev[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on `device` (the current device).  In
+// host code the array's name is only a host-side stand-in, so the address is
+// looked up once per device, on that device's first call.
+int noalloc_scratch(int device, unsigned char** out) {
+    if (device < 0 || device >= kNoAllocMaxDevices) return DENDRITE_EINVAL;
+    if (!g_noalloc_dev[device]) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_err(e);
+        if (!ptr) return DENDRITE_ECUDA;
+        g_noalloc_dev[device] = ptr;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_dev[device]);
+    return DENDRITE_OK;
+}
+
+}  // namespace
+
+extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q, int32_t n_q_heads,
+                                                 int32_t q_len, const int32_t* branches, int32_t n, void* out,
+                                                 void* stream) {
+    if (!p) return DENDRITE_EINVAL;
+    if (p->poisoned) return p->poisoned;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    if (!Q || !out || !branches || n <= 0 || q_len <= 0 || n_q_heads <= 0) return DENDRITE_EINVAL;
+    if (n_q_heads % p->n_kv) return DENDRITE_EINVAL;
+    if (((uintptr_t)Q | (uintptr_t)out) & 15) return DENDRITE_EINVAL;
+    if ((int64_t)n * q_len * n_q_heads >= INT32_MAX / 2) return DENDRITE_ELIMIT;
+    static thread_local std::vector<uint8_t> seen;
+    seen.assign(p->max_branches, 0);
+    for (int32_t i = 0; i < n; ++i) {
+        DENDRITE_TRY(check_live(p, branches[i]));
+        if (p->br[branches[i]].len < q_len) return DENDRITE_EINVAL;
+        if (seen[branches[i]]) return DENDRITE_EINVAL;
+        seen[branches[i]] = 1;
+    }
+    unsigned char* scratch = nullptr;
+    DENDRITE_TRY(noalloc_scratch(p->device, &scratch));
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf16 = p->dtype == DENDRITE_BF16;
+    static thread_local HostPlan hp;
+    hp.clear();
+    DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, hp));
+    // scratch layout: plan sections, then partial acc rows, then partial (m, l)
+    size_t off[8];
+    size_t b = 0;
+    off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
+    off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
+    off[2] = b; b = align16(b + hp.units.size() * sizeof(AttnUnit));
+    off[3] = b; b = align16(b + hp.cta_begin.size() * 4);
+    off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
+    off[5] = b; b = align16(b + hp.path_off.size() * 4);
+    off[6] = b; b = align16(b + hp.path.size() * 4);
+    off[7] = b;
+    const size_t plan_bytes = (b + 255) & ~size_t(255);
+    const size_t acc_bytes = hp.partial_rows * p->head_dim * sizeof(float);
+    const size_t ml_bytes = hp.partial_rows * sizeof(float2);
+    if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
+    unsigned char* h = g_noalloc_host;
+    std::memcpy(h + off[0], hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
+    std::memcpy(h + off[1], hp.members.data(), hp.members.size() * sizeof(AttnMember));
+    std::memcpy(h + off[2], hp.units.data(), hp.units.size() * sizeof(AttnUnit));
+    std::memcpy(h + off[3], hp.cta_begin.data(), hp.cta_begin.size() * 4);
+    std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
+    std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
+    std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
+    DENDRITE_CUDA(cudaMemcpyAsync(scratch, h, b, cudaMemcpyHostToDevice, s));
+    AttnArgs a;
+    a.plan.segs = reinterpret_cast<const AttnSeg*>(scratch + off[0]);
+    a.plan.members = reinterpret_cast<const AttnMember*>(scratch + off[1]);
+    a.plan.units = reinterpret_cast<const AttnUnit*>(scratch + off[2]);
+    a.plan.cta_begin = reinterpret_cast<const int32_t*>(scratch + off[3]);
+    a.plan.cta_unit = reinterpret_cast<const int32_t*>(scratch + off[4]);
+    a.plan.path_off = reinterpret_cast<const int32_t*>(scratch + off[5]);
+    a.plan.path = reinterpret_cast<const int32_t*>(scratch + off[6]);
+    a.plan.n_units = (int32_t)hp.units.size();
+    a.plan.n_ctas = (int32_t)hp.cta_unit.size();
+    a.plan.n_queried = n;
+    a.plan.q_len = q_len;
+    a.plan.n_q_heads = n_q_heads;
+    a.plan.group = n_q_heads / p->n_kv;
+    a.plan.max_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    a.plan.pad = 0;
+    a.Q = Q;
+    a.out = out;
+    a.table = p->d_table;
+    a.pool_kv[0] = p->d_k;
+    a.pool_kv[1] = p->d_v;
+    a.pool_k = static_cast<const float*>(p->d_k);
+    a.pool_v = static_cast<const float*>(p->d_v);
+    a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);
+    a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
+    a.meta = p->d_meta;
+    a.bpb = p->bpb;
+    a.n_kv = p->n_kv;
+    a.head_dim = p->head_dim;
+    a.n_blocks = (int32_t)p->num_blocks;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
+    if (bf16) {
+        CUtensorMap mk, mv;
+        std::memcpy(&mk, p->tmap_k, sizeof(mk));
+        std::memcpy(&mv, p->tmap_v, sizeof(mv));
+        DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
+    } else {
+        DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(a.plan.n_ctas), dim3(128),
+                                 2 * BS * p->head_dim * sizeof(float), s, a));
+    }
+    const int32_t n_out = n * q_len * n_q_heads;
+    const unsigned grid = (unsigned)((n_out + 7) / 8);
+    if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, a));
+    else DENDRITE_CUDA(launch_pdl(k_attn_merge<float>, dim3(grid), dim3(256), 0, s, a));
+    return DENDRITE_OK;
+}

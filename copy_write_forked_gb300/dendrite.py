@@ -62,6 +62,7 @@ _SIGS = {
     "dendrite_fork_batch": [_p, _pi32, _pi32, _i32, _pi32, _p],
     "dendrite_append_kv": [_p, _pi32, _i32, _i32, _p, _p, _p],
     "dendrite_tree_attn_decode": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
+    "dendrite_tree_attn_decode_noalloc": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_free": [_p, _pi32, _i32, _p],
     "dendrite_sync": [_p, _p],
     "dendrite_branch_len": [_p, _i32, _pi32],
@@ -224,6 +225,22 @@ class Pool:
         _check(lib().dendrite_tree_attn_decode(self._h, Q.data_ptr(), Q.shape[2], Q.shape[1], _ptr(ba),
                                                len(branches), out.data_ptr(), _stream_ptr(stream, self._dev)),
                "tree_attn_decode")
+        return out
+
+    def tree_attn_decode_noalloc(self, Q: torch.Tensor, branches: Sequence[int], out: torch.Tensor,
+                                 stream=None) -> torch.Tensor:
+        """Same as :meth:`tree_attn_decode` but with scratch in the library's fixed
+        16 MiB per-device array (no device allocation during the call); ``out``
+        must be given.  Raises ELIMIT when the plan and partials do not fit."""
+        self._check_tensor(Q, "Q")
+        self._check_tensor(out, "out")
+        if Q.dim() != 4 or Q.shape[0] != len(branches) or Q.shape[3] != self.head_dim or out.shape != Q.shape:
+            raise DendriteError(-1, f"Q/out shape {tuple(Q.shape)}")
+        ba = _arr(branches)
+        _check(lib().dendrite_tree_attn_decode_noalloc(self._h, Q.data_ptr(), Q.shape[2], Q.shape[1], _ptr(ba),
+                                                       len(branches), out.data_ptr(),
+                                                       _stream_ptr(stream, self._dev)),
+               "tree_attn_decode_noalloc (scratch limit 16 MiB)")
         return out
 
     def free(self, branches: Sequence[int], stream=None) -> None:

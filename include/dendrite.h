@@ -240,6 +240,38 @@ int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t
                            dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
                            int32_t* members, int32_t member_cap, int32_t* n_members);
 
+/* ------------------------------------------------- allocation-free variant
+ * No counterpart on the pages: this entry point exists for callers that must
+ * not have the library allocate device memory during decoding -- a serving
+ * process whose device memory already belongs to its own caching allocator,
+ * a latency-critical loop that cannot absorb the device synchronisation that
+ * cudaMalloc / cudaFree may trigger, or a deployment that fixes each
+ * library's memory at load time.
+ *
+ * Same arguments, layouts, results and errors as dendrite_tree_attn_decode,
+ * but its scratch (the uploaded plan and the partial (max, sum, acc) rows)
+ * lives in one file-scope device array of DENDRITE_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU loading the library holds until the process exits.
+ * The call itself calls no cudaMalloc, cudaFree, cudaMallocHost or other
+ * allocating CUDA or torch routine; its host-side planning reuses per-thread
+ * host buffers.  It does not use or grow the pool's attention workspace.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) once for that device; make that first call before
+ *     any stream capture.
+ *   - A call whose plan plus partial rows exceed the array returns
+ *     DENDRITE_ELIMIT and launches nothing (roughly: more than ~30,000 partial
+ *     rows of head_dim 128).
+ *   - Nothing in the array needs to start at zero: each call writes the plan
+ *     and every partial row before reading them.
+ *   - All calls share the one array per device and it keeps the last call's
+ *     contents: calls whose GPU work overlaps (other streams, other pools on
+ *     the same device, other threads) race on it and must be ordered by the
+ *     caller.
+ */
+#define DENDRITE_NOALLOC_SCRATCH_BYTES (16u << 20)
+int dendrite_tree_attn_decode_noalloc(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,
+                                      const int32_t* branches, int32_t n_branches, void* out, void* stream);
+
 /* Library version string. */
 const char* dendrite_version(void);
 

@@ -1,0 +1,86 @@
+"""The allocation-free attention entry point, through the C-ABI, against the
+regular entry point.
+
+Callers such as a serving process whose device memory is already owned by its
+own caching allocator, or a latency-critical decode loop that cannot absorb a
+cudaMalloc's device synchronisation, use dendrite_tree_attn_decode_noalloc: it
+keeps its plan and partial rows in the library's fixed per-device array
+instead of allocating.  Its output must match the regular call within the
+bf16 tolerance the other tests use, on two calls in a row (the array keeps the
+previous call's contents)."""
+import ctypes
+
+import pytest
+import torch
+
+from copy_write_forked_gb300 import workloads as W
+from copy_write_forked_gb300.dendrite import lib
+from copy_write_forked_gb300.runner import pool_for, run_script
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+    torch.cuda.set_device(0)
+
+
+def _call(fn, pool, Q, branches, out):
+    arr = (ctypes.c_int32 * len(branches))(*branches)
+    stream = torch.cuda.current_stream().cuda_stream
+    return fn(pool._h, Q.data_ptr(), Q.shape[2], Q.shape[1], ctypes.addressof(arr), len(branches),
+              out.data_ptr(), stream)
+
+
+def test_noalloc_matches_regular_entry_point_on_two_calls():
+    w = W.beam(requests=3, prefix=333, width=4, divergent=29)
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    br = [h[b] for b in w.query]
+    Q = w.q("cuda")
+    ref = torch.empty_like(Q)
+    assert _call(lib().dendrite_tree_attn_decode, pool, Q, br, ref) == 0
+    for _ in range(2):
+        got = torch.full_like(Q, float("nan"))
+        assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, got) == 0
+        torch.cuda.synchronize()
+        assert torch.isfinite(got.float()).all()
+        assert (got.float() - ref.float()).abs().max().item() <= TOL
+    pool.sync()
+    pool.close()
+
+
+def test_noalloc_fp32_pool_matches_on_two_calls():
+    w = W.tiny_cow("b")
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    br = [h[b] for b in w.query]
+    Q = w.q("cuda")
+    ref = torch.empty_like(Q)
+    assert _call(lib().dendrite_tree_attn_decode, pool, Q, br, ref) == 0
+    for _ in range(2):
+        got = torch.full_like(Q, float("nan"))
+        assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, got) == 0
+        torch.cuda.synchronize()
+        assert (got - ref).abs().max().item() <= 1e-5
+    pool.close()
+
+
+def test_noalloc_rejects_work_beyond_its_scratch():
+    # 1024 branches forked from one 16-token root: 32768 output rows, each with
+    # at least one partial row of 130 floats -- more than the 16 MiB array
+    pool = __import__("copy_write_forked_gb300").Pool(8, 16, 8, 128, torch.bfloat16, max_branches=1100,
+                                                       max_blocks_per_branch=4)
+    r = pool.new_branch()
+    K = torch.randn(1, 16, 8, 128, device="cuda").bfloat16()
+    pool.append_kv([r], K, K)
+    kids = pool.fork(r, 1024)
+    Q = torch.randn(1024, 1, 32, 128, device="cuda").bfloat16()
+    out = torch.empty_like(Q)
+    assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, kids, out) == -4   # DENDRITE_ELIMIT
+    assert _call(lib().dendrite_tree_attn_decode, pool, Q, kids, out) == 0
+    pool.sync()
+    pool.close()
