@@ -326,6 +326,66 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def other_workload(name):
+    from copy_write_forked_gb300 import workloads as W
+    if name == "mcts":
+        return W.mcts(), "MCTS tree: root 2048, 500 iterations of fork 4 x 32 tokens, one query per live leaf"
+    if name == "specverify":
+        return W.spec_verify(), "speculative verification: 32 x prefix 8192, 3 draft paths x 8 tokens, q_len 8"
+    if name == "stress":
+        return W.fork_stress_attention(), "stress: 16 x prefix 32768, fork 64 x 1024 tokens"
+    raise ValueError(name)
+
+
+def run_attention_only(args):
+    """Tree decode attention on a prebuilt tree (plan cached); K timed calls."""
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__ as g
+    g.build()
+    from copy_write_forked_gb300.runner import pool_for, run_script
+    w, desc = other_workload(args.workload)
+    pool = pool_for(w)
+    h = run_script(pool, w, device=dev)
+    br = [h[b] for b in w.query]
+    Q = w.q(dev)
+    out = torch.empty_like(Q)
+    flush_r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    pool.sync()
+    for _ in range(args.warmup):
+        flush_r.max()
+        pool.tree_attn_decode(Q, br, out=out)
+    pool.set_profiling(True)
+    part, tot = [], []
+    for _ in range(args.steps):
+        flush_r.max()
+        pool.tree_attn_decode(Q, br, out=out)
+        tm = pool.last_timings()
+        part.append(tm["attn_partial"])
+        tot.append(tm["attn_total"])
+    pool.sync()
+    st = pool.last_plan_stats()
+    unique = w.unique_kv_bytes() + Q.numel() * Q.element_size()
+    pk_ms, tot_ms = statistics.median(part), statistics.median(tot)
+    peak, src = read_peaks()
+    ach = unique / (pk_ms / 1e3) / 1e9
+    nq = len(w.query) * w.q_len
+    line = {"metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
+            "workload": args.workload, "value": nq / (tot_ms / 1e3), "unit": "branch-queries/s",
+            "ms_per_call": tot_ms, "partial_kernel_ms": pk_ms, "steps": args.steps, "warmup": args.warmup,
+            "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
+            "config": {"workload": desc, "step": "tree decode attention on a prebuilt tree (plan cached)",
+                       "l2": "flushed between calls (256 MiB read)"},
+            "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": ach, "peak": peak,
+                         "peak_source": src, "unit": "GB/s", "frac": ach / peak, "algorithmic_bytes": unique},
+            "plan": st}
+    print(json.dumps(line), flush=True)
+    pool.close()
+
+
 def fork_latency(dev, reps=200):
     """Fork of a chain of `depth` blocks whose tail block is half full, with 1
     and 4 children (then freed).  Three views per call: the host time of the C
@@ -475,9 +535,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="beam", choices=["beam", "mcts", "specverify", "stress"],
+                    help="beam = the full-path step (default JSON line); others time tree attention only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.impl == "ours" and args.workload != "beam":
+        run_attention_only(args)
+        return
     if args.impl == "reference":
         # the oracle runs single-threaded: pin BLAS/OpenMP pools before numpy loads
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):

@@ -48,7 +48,6 @@ namespace {
 constexpr int D = 128;
 constexpr int BS = 16;
 constexpr int NSTAGE = 3;
-constexpr int LEAD = 4;                          // L2 prefetch lead, in stages
 constexpr int HALF_BYTES = BS * 64 * 2;          // one 64-column half of a K or V tile
 constexpr int SLOT_BYTES = 4 * HALF_BYTES;       // K (2 halves) + V (2 halves) of one tile
 constexpr int STAGE_BYTES = 4 * SLOT_BYTES;
@@ -214,10 +213,6 @@ struct Walker {
     }
 };
 
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // ============================================================ bf16 kernel
 __global__ void __launch_bounds__(THREADS, 2)
 k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -254,31 +249,27 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
     if (warp == NCONS) {
         // ------------------------------------------------------ producer
-        // TMA loads fill the NSTAGE-deep ring; bulk L2 prefetches run LEAD
-        // stages ahead of them so that DRAM sees more requests in flight than
-        // shared memory can hold.
+        // The block ids of a stage are read from the table three stages before
+        // its TMA loads are issued, so table reads overlap the ring's waits
+        // instead of sitting between a free slot and its copies.
         uint32_t issued = 0, parity_bits = 0;
         int32_t stage = 0;
-        Walker w, pf;
+        Walker w, ah;
         w.init(pl, c);
-        pf = w;
-        const char* kbase = static_cast<const char*>(a.pool_kv[0]);
-        const char* vbase = static_cast<const char*>(a.pool_kv[1]);
-        auto prefetch_stage = [&](const Walker& x) {
-            if (lane < x.ntiles()) {
-                const int32_t blk = a.table[(int64_t)x.S.table_row * a.bpb + x.S.blk_start + (x.t - x.U.tile_off) + lane];
-                if ((uint32_t)blk < (uint32_t)a.n_blocks) {
-                    const int64_t off = ((int64_t)blk * a.n_kv + x.U.kv_head) * (2 * HALF_BYTES);
-                    l2_prefetch(kbase + off, 2 * HALF_BYTES);
-                    l2_prefetch(vbase + off, 2 * HALF_BYTES);
-                }
-            }
+        ah = w;
+        auto load_ids = [&](const Walker& x) -> int32_t {
+            if (!x.valid() || lane >= x.ntiles()) return -1;
+            return a.table[(int64_t)x.S.table_row * a.bpb + x.S.blk_start + (x.t - x.U.tile_off) + lane];
         };
-        for (int k = 0; k < LEAD && pf.valid(); ++k) {
-            prefetch_stage(pf);
-            pf.next();
-        }
+        int32_t id0 = load_ids(ah);
+        if (ah.valid()) ah.next();
+        int32_t id1 = load_ids(ah);
+        if (ah.valid()) ah.next();
+        int32_t id2 = load_ids(ah);
+        if (ah.valid()) ah.next();
         while (w.valid()) {
+            const int32_t id3 = load_ids(ah);
+            if (ah.valid()) ah.next();
             const int slot = stage % NSTAGE;
             const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
             const int ntiles = w.ntiles();
@@ -295,7 +286,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
                 __syncwarp();
                 if (lane < ntiles) {
-                    int32_t blk = a.table[(int64_t)w.S.table_row * a.bpb + w.S.blk_start + (w.t - w.U.tile_off) + lane];
+                    int32_t blk = id0;
                     if ((uint32_t)blk >= (uint32_t)a.n_blocks) {   // broken table: poison, read zeros
                         atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                         blk = -1;
@@ -310,11 +301,10 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 }
                 issued |= 1u << slot;
                 parity_bits = (parity_bits & ~(1u << slot)) | (ph << slot);
-                if (pf.valid()) {
-                    prefetch_stage(pf);
-                    pf.next();
-                }
             }
+            id0 = id1;
+            id1 = id2;
+            id2 = id3;
             w.next();
             ++stage;
         }
@@ -679,11 +669,10 @@ __global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
         const int32_t e = e0 + lane;
         int32_t nch = 0, base = 0, stride = 0;
         if (e < pend) {
-            const int32_t seg = pl.path[2 * e], mi = pl.path[2 * e + 1];
-            const AttnSeg S = pl.segs[seg];
-            const int32_t sr = mi * RM + j * G + g;
+            const int4 pe = __ldg(reinterpret_cast<const int4*>(pl.path) + e);   // unit_base, ngroups, sr0
+            const int32_t sr = pe.z + j * G + g;
             const int32_t grp = sr / pl.max_rows;
-            const AttnUnit U = pl.units[S.unit_base + h * S.ngroups + grp];
+            const AttnUnit U = pl.units[pe.x + h * pe.y + grp];
             nch = U.nchunks;
             base = U.prow_base + (sr - grp * pl.max_rows);
             stride = U.n_rows;
@@ -887,14 +876,16 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     for (const AttnSeg& S : hp.segs)
         for (int32_t k = 0; k < S.n_mem; ++k) hp.path_off[hp.members[S.mem_off + k].qi + 1]++;
     for (int32_t i = 0; i < n; ++i) hp.path_off[i + 1] += hp.path_off[i];
-    hp.path.resize(2 * (size_t)hp.path_off[n]);
+    hp.path.resize(4 * (size_t)hp.path_off[n]);
     hp.cursor.assign(hp.path_off.begin(), hp.path_off.end() - 1);
     for (int32_t si = 0; si < (int32_t)hp.segs.size(); ++si) {
         const AttnSeg& S = hp.segs[si];
         for (int32_t k = 0; k < S.n_mem; ++k) {
             const int32_t e = hp.cursor[hp.members[S.mem_off + k].qi]++;
-            hp.path[2 * e] = si;
-            hp.path[2 * e + 1] = k;
+            hp.path[4 * e] = S.unit_base;
+            hp.path[4 * e + 1] = S.ngroups;
+            hp.path[4 * e + 2] = k * RM;
+            hp.path[4 * e + 3] = si;
         }
     }
     for (int32_t i = 0; i < n; ++i)

@@ -78,7 +78,8 @@ struct AttnPlanDev {
     const int32_t* cta_begin;   // [n_ctas + 1] strictly increasing tile boundaries
     const int32_t* cta_unit;    // [n_ctas] unit holding cta_begin[c]
     const int32_t* path_off;    // [n_queried + 1] into path
-    const int32_t* path;        // pairs (segment, member index) along each queried branch
+    const int32_t* path;        // per path entry: (first unit of the segment, row groups per kv head,
+                                //  first segment row of the member, segment index)
     int32_t n_units;
     int32_t n_ctas;
     int32_t n_queried;

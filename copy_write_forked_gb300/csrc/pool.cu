@@ -313,23 +313,41 @@ __global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t
     const int64_t tile_vec = (int64_t)bs * row_vec;
     uint4* kd = Kp + ((int64_t)dst * n_kv + h) * tile_vec;
     uint4* vd = Vp + ((int64_t)dst * n_kv + h) * tile_vec;
-    // copy of the shared tail's valid slots
-    if (lblk == L / bs && cow_src[i] >= 0) {
-        const uint4* ks = Kp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec;
-        const uint4* vs = Vp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec;
-        for (int32_t e = threadIdx.x; e < s0 * row_vec; e += blockDim.x) {
-            kd[e] = ks[e];
-            vd[e] = vs[e];
+    // copy of the shared tail's valid slots, then the new rows (token
+    // lblk*bs + s - L of branch i); each thread issues its loads before its
+    // stores so the moves of a tile are in flight together
+    const bool cow = lblk == L / bs && cow_src[i] >= 0;
+    const uint4* ks = cow ? Kp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec : nullptr;
+    const uint4* vs = cow ? Vp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec : nullptr;
+    const int32_t total = s1 * row_vec;   // slots [0, s1) of the destination tile
+    constexpr int U = 4;
+    for (int32_t e0 = threadIdx.x; e0 < total; e0 += U * blockDim.x) {
+        uint4 kv[U], vv[U];
+        int32_t idx[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int32_t e = e0 + u * blockDim.x;
+            idx[u] = -1;
+            if (e >= total) continue;
+            const int32_t s = e / row_vec, v = e % row_vec;
+            if (s < s0) {
+                if (!cow) continue;
+                kv[u] = ks[e];
+                vv[u] = vs[e];
+            } else {
+                const int64_t tok = (int64_t)lblk * bs + s - L;
+                const int64_t src = (((int64_t)i * n_new + tok) * n_kv + h) * row_vec + v;
+                kv[u] = __ldg(Kin + src);
+                vv[u] = __ldg(Vin + src);
+            }
+            idx[u] = e;
         }
-    }
-    // new rows: token (lblk*bs + s - L) of branch i
-    const int32_t cnt = (s1 - s0) * row_vec;
-    for (int32_t e = threadIdx.x; e < cnt; e += blockDim.x) {
-        const int32_t s = s0 + e / row_vec, v = e % row_vec;
-        const int64_t tok = (int64_t)lblk * bs + s - L;
-        const int64_t src = (((int64_t)i * n_new + tok) * n_kv + h) * row_vec + v;
-        kd[(int64_t)s * row_vec + v] = Kin[src];
-        vd[(int64_t)s * row_vec + v] = Vin[src];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (idx[u] < 0) continue;
+            kd[idx[u]] = kv[u];
+            vd[idx[u]] = vv[u];
+        }
     }
 }
 
