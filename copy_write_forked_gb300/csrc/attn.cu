@@ -159,60 +159,6 @@ __device__ __forceinline__ uint32_t swz(int t, int d) {
 }
 
 
-// Query row r of unit U: the Q/out row it reads/writes and its visibility limit.
-__device__ __forceinline__ void unit_row(const AttnPlanDev& pl, const AttnSeg& S, const AttnUnit& U, int r,
-                                         int32_t& q_row, int32_t& limit) {
-    const int RM = pl.q_len * pl.group;
-    const int sr = U.row_lo + r;
-    const int mi = sr / RM;
-    const int rem = sr - mi * RM;
-    const int j = rem / pl.group;
-    const int g = rem - j * pl.group;
-    const AttnMember M = pl.members[S.mem_off + mi];
-    q_row = (M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * pl.group + g;
-    limit = M.len - pl.q_len + j + 1;
-}
-
-// Schedule walker over a CTA's share of the tile list, one stage at a time.
-// A stage is up to P = 4 / rt consecutive tiles of one unit.
-struct Walker {
-    const AttnPlanDev* pl;
-    int32_t t, t_end, u, cend;
-    int P;
-    AttnUnit U;
-    AttnSeg S;
-    __device__ void init(const AttnPlanDev& p, int c) {
-        pl = &p;
-        t = p.cta_begin[c];
-        t_end = p.cta_begin[c + 1];
-        u = p.cta_unit[c];
-        settle();
-    }
-    __device__ bool valid() const { return t < t_end; }
-    __device__ void settle() {
-        while (t < t_end) {
-            U = pl->units[u];
-            S = pl->segs[U.seg];
-            const int32_t uend = U.tile_off + S.n_blk;
-            if (t < uend) {
-                cend = min(t_end, uend);
-                P = 4 / U.rt;
-                return;
-            }
-            ++u;
-        }
-    }
-    __device__ int ntiles() const { return min(P, cend - t); }
-    __device__ void next() {
-        t += P;
-        if (t >= cend) {
-            t = cend;
-            ++u;
-            settle();
-        }
-    }
-};
-
 // ============================================================ bf16 kernel
 __global__ void __launch_bounds__(THREADS, 2)
 k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -244,54 +190,46 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const AttnPlanDev& pl = a.plan;
     const int c = blockIdx.x;
     const int32_t t_begin = pl.cta_begin[c], t_end = pl.cta_begin[c + 1];
-    int32_t u0 = pl.cta_unit[c];
+    const int32_t u0 = pl.cta_unit[c];
     volatile int* abortp = &abort_flag;
 
     if (warp == NCONS) {
         // ------------------------------------------------------ producer
-        // The block ids of a stage are read from the table three stages before
-        // its TMA loads are issued, so table reads overlap the ring's waits
-        // instead of sitting between a free slot and its copies.
+        // Each stage is up to 4 consecutive tiles (blocks x one kv head) of
+        // one unit; lane i reads tile i's block id and issues its four TMA
+        // boxes (K and V, two 64-column halves each).
         uint32_t issued = 0, parity_bits = 0;
         int32_t stage = 0;
-        Walker w, ah;
-        w.init(pl, c);
-        ah = w;
-        auto load_ids = [&](const Walker& x) -> int32_t {
-            if (!x.valid() || lane >= x.ntiles()) return -1;
-            return a.table[(int64_t)x.S.table_row * a.bpb + x.S.blk_start + (x.t - x.U.tile_off) + lane];
-        };
-        int32_t id0 = load_ids(ah);
-        if (ah.valid()) ah.next();
-        int32_t id1 = load_ids(ah);
-        if (ah.valid()) ah.next();
-        int32_t id2 = load_ids(ah);
-        if (ah.valid()) ah.next();
-        while (w.valid()) {
-            const int32_t id3 = load_ids(ah);
-            if (ah.valid()) ah.next();
-            const int slot = stage % NSTAGE;
-            const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
-            const int ntiles = w.ntiles();
-            bool ok = true;
-            if (lane == 0 && !*abortp) {
-                ok = mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abortp);
-                if (!ok) {
-                    *abortp = 1;
-                    atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
+        int32_t t = t_begin, u = u0;
+        while (t < t_end) {
+            const AttnUnit U = pl.units[u];
+            const int32_t uend = U.tile_off + U.n_blk;
+            if (t >= uend) { ++u; continue; }
+            const int32_t cend = min(t_end, uend);
+            const int32_t* trow = a.table + (int64_t)U.table_row * a.bpb + U.blk_start - U.tile_off;
+            for (int32_t st = t; st < cend; st += 4, ++stage) {
+                const int slot = stage % NSTAGE;
+                const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
+                const int ntiles = min(4, cend - st);
+                bool ok = true;
+                if (lane == 0 && !*abortp) {
+                    ok = mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abortp);
+                    if (!ok) {
+                        *abortp = 1;
+                        atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
+                    }
                 }
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && !*abortp;
-            if (ok) {
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && !*abortp;
+                if (!ok) continue;
                 if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
                 __syncwarp();
                 if (lane < ntiles) {
-                    int32_t blk = id0;
+                    int32_t blk = trow[st + lane];
                     if ((uint32_t)blk >= (uint32_t)a.n_blocks) {   // broken table: poison, read zeros
                         atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                         blk = -1;
                     }
-                    const int32_t row0 = (blk * a.n_kv + w.U.kv_head) * BS;
+                    const int32_t row0 = (blk * a.n_kv + U.kv_head) * BS;
                     const uint32_t dst = base + slot * STAGE_BYTES + lane * SLOT_BYTES;
                     const uint32_t fb = bar_full + 8 * slot;
                     tma_load_3d(dst, &tmK, 0, 0, row0, fb);
@@ -302,11 +240,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 issued |= 1u << slot;
                 parity_bits = (parity_bits & ~(1u << slot)) | (ph << slot);
             }
-            id0 = id1;
-            id1 = id2;
-            id2 = id3;
-            w.next();
-            ++stage;
+            t = cend;
+            ++u;
         }
         // after a timeout, wait (bounded) for this CTA's copies still in flight
         if (lane == 0 && *abortp) {
@@ -322,31 +257,32 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
 
     // ---------------------------------------------------------- consumers
+    // Warp w owns row tile r = w / P of the unit (P = 4 / rt) and, within
+    // each stage, the tiles p, p + P, ... where p = w % P.
     const float NEG_INF = -INFINITY;
     const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
     int32_t stage = 0;
     int32_t t = t_begin, u = u0;
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
-        const AttnSeg S = pl.segs[U.seg];
-        const int32_t uend = U.tile_off + S.n_blk;
+        const int32_t uend = U.tile_off + U.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
         const int P = 4 / U.rt;
         const int r = warp / P, pidx = warp % P;
-        const bool has_rows = r < U.rt;
 
         // query fragments of rows r*16 + lane/4 (+8), and their visibility limits
         uint32_t qa[8][4];
         int32_t lim0 = 0, lim1 = 0;
         {
             const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
-            const bool v0 = has_rows && row0 < U.n_rows, v1 = has_rows && row1 < U.n_rows;
-            int32_t qr0 = 0, qr1 = 0;
-            if (v0) unit_row(pl, S, U, row0, qr0, lim0);
-            if (v1) unit_row(pl, S, U, row1, qr1, lim1);
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)qr0 * D);
-            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Q + (int64_t)qr1 * D);
+            const bool v0 = row0 < U.n_rows, v1 = row1 < U.n_rows;
+            const AttnRow R0 = v0 ? pl.rows[U.row_off + row0] : AttnRow{0, 0};
+            const AttnRow R1 = v1 ? pl.rows[U.row_off + row1] : AttnRow{0, 0};
+            lim0 = R0.limit;
+            lim1 = R1.limit;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R0.q_row * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R1.q_row * D);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int w = ks * 8 + (lane & 3);   // 32-bit word index of column ks*16 + 2*(lane&3)
@@ -361,11 +297,11 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
 
-        for (int32_t st = t; st < cend; st += P, ++stage) {
+        for (int32_t st = t; st < cend; st += 4, ++stage) {
             const int slot = stage % NSTAGE;
             const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
-            const int ntiles = min(P, cend - st);
-            const bool last = st + P >= cend;
+            const int ntiles = min(4, cend - st);
+            const bool last = st + 4 >= cend;
             bool ok = !*abortp;
             if (ok) {
                 ok = mbar_wait(bar_full + 8 * slot, ph, abortp);
@@ -375,8 +311,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 }
             }
             ok = __all_sync(0xffffffffu, ok) && !*abortp;
-            if (ok && has_rows && pidx < ntiles) {
-                const uint32_t kt = base + slot * STAGE_BYTES + pidx * SLOT_BYTES;
+            for (int ti = pidx; ok && ti < ntiles; ti += P) {
+                const uint32_t kt = base + slot * STAGE_BYTES + ti * SLOT_BYTES;
                 const uint32_t vt = kt + 2 * HALF_BYTES;
                 // S = Q K^T (16 rows x 16 tokens)
                 float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -392,7 +328,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     }
                 }
                 // scale, mask by per-row visibility, online softmax
-                const int32_t pos0 = (S.blk_start + (st - U.tile_off) + pidx) * BS + (lane & 3) * 2;
+                const int32_t pos0 = (U.blk_start + (st - U.tile_off) + ti) * BS + (lane & 3) * 2;
                 float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -462,7 +398,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
                 const int32_t prow0 = U.prow_base + (c - U.cfirst) * U.n_rows;
                 if (P == 1) {
-                    if (ok && has_rows) {
+                    if (ok) {
                         const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
                         if (row0 < U.n_rows) {
                             float* dst = a.part_acc + (int64_t)(prow0 + row0) * D + (lane & 3) * 2;
@@ -564,8 +500,7 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
     const float* Q = static_cast<const float*>(a.Q);
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
-        const AttnSeg S = pl.segs[U.seg];
-        const int32_t uend = U.tile_off + S.n_blk;
+        const int32_t uend = U.tile_off + U.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
         float q[4][8], acc[4][8], m[4], l[4];
@@ -574,8 +509,7 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
         for (int rr = 0; rr < 4; ++rr) {
             const int row = warp + 4 * rr;
             const bool v = row < U.n_rows;
-            struct { int32_t q_row, limit; } R = {0, 0};
-            if (v) unit_row(pl, S, U, row, R.q_row, R.limit);
+            const AttnRow R = v ? pl.rows[U.row_off + row] : AttnRow{0, 0};
             lim[rr] = R.limit;
             m[rr] = -INFINITY;
             l[rr] = 0.f;
@@ -586,8 +520,8 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
             }
         }
         for (int32_t tt = t; tt < cend; ++tt) {
-            const int32_t lb = S.blk_start + (tt - U.tile_off);
-            int32_t blk = a.table[(int64_t)S.table_row * a.bpb + lb];
+            const int32_t lb = U.blk_start + (tt - U.tile_off);
+            int32_t blk = a.table[(int64_t)U.table_row * a.bpb + lb];
             if ((uint32_t)blk >= (uint32_t)a.n_blocks) {
                 if (threadIdx.x == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                 blk = 0;   // read a valid block; the pool is poisoned anyway
@@ -747,6 +681,7 @@ struct HostPlan {
     std::vector<AttnSeg> segs;
     std::vector<AttnMember> members;
     std::vector<AttnUnit> units;
+    std::vector<AttnRow> rows;
     std::vector<int32_t> cta_begin, cta_unit, path_off, path;
     std::vector<int64_t> cuts;
     int64_t tiles = 0, unique_tiles = 0;
@@ -754,7 +689,7 @@ struct HostPlan {
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
-        segs.clear(); members.clear(); units.clear(); cta_begin.clear(); cta_unit.clear();
+        segs.clear(); members.clear(); units.clear(); rows.clear(); cta_begin.clear(); cta_unit.clear();
         path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         partial_rows = 0;
@@ -762,6 +697,13 @@ struct HostPlan {
 };
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// Partition weights, fitted to per-CTA timelines on GB300: a tile of a unit
+// with rt row tiles costs about (1 + rt) units (HBM time plus mma time: 0.25 us
+// for rt = 1 vs 0.61 us for rt = 4 per CTA), and every chunk boundary (partial
+// store, combine, next unit's Q) about as much as 8 one-row-tile tiles.
+constexpr int64_t kUnitStartWeight = 16;
+inline int64_t tile_weight(int rt) { return 1 + rt; }
 
 int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
                HostPlan& hp) {
@@ -809,8 +751,28 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
                 U.n_rows = std::min(max_rows, rows_per_head - U.row_lo);
                 U.rt = U.n_rows <= 16 ? 1 : U.n_rows <= 32 ? 2 : 4;
                 U.tile_off = (int32_t)tile_off;
+                U.table_row = S.table_row;
+                U.blk_start = S.blk_start;
+                U.n_blk = S.n_blk;
+                U.row_off = (int32_t)hp.rows.size();
+                // rows: segment row sr -> member sr / RM, token (sr % RM) / G, group sr % G
+                {
+                    int32_t mi = U.row_lo / RM, rem = U.row_lo % RM;
+                    int32_t j = rem / G, g = rem % G;
+                    for (int32_t r = 0; r < U.n_rows; ++r) {
+                        const AttnMember& M = hp.members[S.mem_off + mi];
+                        hp.rows.push_back({(M.qi * q_len + j) * nq + h * G + g, M.len - q_len + j + 1});
+                        if (++g == G) {
+                            g = 0;
+                            if (++j == q_len) {
+                                j = 0;
+                                ++mi;
+                            }
+                        }
+                    }
+                }
                 tile_off += S.n_blk;
-                weight += (int64_t)S.n_blk * U.rt;
+                weight += kUnitStartWeight + (int64_t)S.n_blk * tile_weight(U.rt);
                 hp.units.push_back(U);
             }
         }
@@ -818,21 +780,23 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     }
     if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
     hp.tiles = tile_off;
-    // even split of the weighted tile list (weight of a tile = row tiles of its
-    // unit); cuts are made strictly increasing so that no CTA is empty
+    // even split of the weighted tile list (tile_weight per tile plus
+    // kUnitStartWeight per unit start); cuts are made strictly increasing so
+    // that no CTA is empty.
     const int64_t T = tile_off;
-    const int C0 = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + 3) / 4));
+    const int C0 = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + 7) / 8));
     hp.cuts.push_back(0);
     {
         int c = 1;
         int64_t cw = 0;
         for (const AttnUnit& U : hp.units) {
             const int64_t nb = hp.segs[U.seg].n_blk;
-            const int64_t uw = nb * U.rt;
+            const int64_t tw = tile_weight(U.rt);
+            const int64_t uw = kUnitStartWeight + nb * tw;
             while (c < C0) {
                 const int64_t target = (weight * c + C0 - 1) / C0;
                 if (target >= cw + uw) break;
-                const int64_t k = (target - cw + U.rt - 1) / U.rt;
+                const int64_t k = std::max<int64_t>(0, (target - cw - kUnitStartWeight + tw - 1) / tw);
                 const int64_t cut = U.tile_off + std::min<int64_t>(k, nb);
                 if (cut > hp.cuts.back() && cut < T) hp.cuts.push_back(cut);
                 ++c;
@@ -1020,7 +984,7 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         hp.clear();
         DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, hp));
         const int32_t C = (int32_t)hp.cta_unit.size();
-        size_t off[8];
+        size_t off[9];
         size_t b = 0;
         off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
         off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
@@ -1029,7 +993,8 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
         off[5] = b; b = align16(b + hp.path_off.size() * 4);
         off[6] = b; b = align16(b + hp.path.size() * 4);
-        off[7] = b;
+        off[7] = b; b = align16(b + hp.rows.size() * sizeof(AttnRow));
+        off[8] = b;
         DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
         char* h = p->h_plan;
@@ -1040,6 +1005,7 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
         std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
         std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
+        std::memcpy(h + off[7], hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
         DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, h, b, cudaMemcpyHostToDevice, s));
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
         char* d = p->d_plan;
@@ -1050,6 +1016,7 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         pc.dev.cta_unit = reinterpret_cast<const int32_t*>(d + off[4]);
         pc.dev.path_off = reinterpret_cast<const int32_t*>(d + off[5]);
         pc.dev.path = reinterpret_cast<const int32_t*>(d + off[6]);
+        pc.dev.rows = reinterpret_cast<const AttnRow*>(d + off[7]);
         pc.dev.n_units = (int32_t)hp.units.size();
         pc.dev.n_ctas = C;
         pc.dev.n_queried = n;
@@ -1096,7 +1063,7 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         CUtensorMap mk, mv;
         std::memcpy(&mk, p->tmap_k, sizeof(mk));
         std::memcpy(&mv, p->tmap_v, sizeof(mv));
-        DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(pc.dev.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
+        k_attn_partial_bf16<<<pc.dev.n_ctas, THREADS, SMEM_BF16, s>>>(mk, mv, a);
     } else {
         DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(pc.dev.n_ctas), dim3(128),
                                  2 * BS * p->head_dim * sizeof(float), s, a));
@@ -1190,7 +1157,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     hp.clear();
     DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, hp));
     // scratch layout: plan sections, then partial acc rows, then partial (m, l)
-    size_t off[8];
+    size_t off[9];
     size_t b = 0;
     off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
     off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
@@ -1199,7 +1166,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
     off[5] = b; b = align16(b + hp.path_off.size() * 4);
     off[6] = b; b = align16(b + hp.path.size() * 4);
-    off[7] = b;
+    off[7] = b; b = align16(b + hp.rows.size() * sizeof(AttnRow));
     const size_t plan_bytes = (b + 255) & ~size_t(255);
     const size_t acc_bytes = hp.partial_rows * p->head_dim * sizeof(float);
     const size_t ml_bytes = hp.partial_rows * sizeof(float2);
@@ -1212,6 +1179,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
     std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
     std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
+    std::memcpy(h + off[7], hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
     DENDRITE_CUDA(cudaMemcpyAsync(scratch, h, b, cudaMemcpyHostToDevice, s));
     AttnArgs a;
     a.plan.segs = reinterpret_cast<const AttnSeg*>(scratch + off[0]);
@@ -1221,6 +1189,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     a.plan.cta_unit = reinterpret_cast<const int32_t*>(scratch + off[4]);
     a.plan.path_off = reinterpret_cast<const int32_t*>(scratch + off[5]);
     a.plan.path = reinterpret_cast<const int32_t*>(scratch + off[6]);
+    a.plan.rows = reinterpret_cast<const AttnRow*>(scratch + off[7]);
     a.plan.n_units = (int32_t)hp.units.size();
     a.plan.n_ctas = (int32_t)hp.cta_unit.size();
     a.plan.n_queried = n;

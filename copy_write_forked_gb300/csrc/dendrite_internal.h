@@ -56,6 +56,9 @@ struct AttnMember {
 // One attention work unit: a (segment, kv head, row group).  Its rows are
 // segment rows [row_lo, row_lo + n_rows); segment row sr belongs to member
 // sr / (q_len * G), query token (sr % (q_len * G)) / G and head group g = sr % G.
+// The segment's table row and block range are repeated here so the partial
+// kernel needs no second lookup, and rows[row_off ..) hold each row's Q/out
+// row and visibility limit.
 struct AttnUnit {
     int32_t seg;
     int32_t kv_head;
@@ -66,15 +69,26 @@ struct AttnUnit {
     int32_t cfirst;     // CTA holding the unit's first tile
     int32_t nchunks;    // CTAs its tiles are split over (all non-empty)
     int32_t prow_base;  // first partial row; chunk k uses rows prow_base + k * n_rows ..
+    int32_t table_row;  // branch handle whose table row holds the segment's block ids
+    int32_t blk_start;  // first logical block of the segment
+    int32_t n_blk;      // blocks (tiles) of the segment
+    int32_t row_off;    // first entry of the unit's rows in the row list
     int32_t pad[3];
 };
-static_assert(sizeof(AttnUnit) == 48, "AttnUnit layout");
+static_assert(sizeof(AttnUnit) == 64, "AttnUnit layout");
+
+// One query row of a unit.
+struct AttnRow {
+    int32_t q_row;   // row of Q/out viewed as [rows][head_dim]
+    int32_t limit;   // visible positions: the row sees positions < limit
+};
 
 // Device view of an uploaded attention plan.
 struct AttnPlanDev {
     const AttnSeg* segs;
     const AttnMember* members;
     const AttnUnit* units;
+    const AttnRow* rows;
     const int32_t* cta_begin;   // [n_ctas + 1] strictly increasing tile boundaries
     const int32_t* cta_unit;    // [n_ctas] unit holding cta_begin[c]
     const int32_t* path_off;    // [n_queried + 1] into path

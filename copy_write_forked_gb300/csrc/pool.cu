@@ -351,8 +351,9 @@ __global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t
     }
 }
 
-// ----------------------------------------------------------------- free
-// One thread per table entry of the freed branches drops one reference; an
+// ------------------------------------------------------- free / truncate
+// One thread per released table entry (branch i releases its entries
+// [start_i, start_i + count_i)) drops one reference and clears the entry; an
 // entry whose refcount reaches zero marks its block released.  The last CTA
 // to finish then pushes the released blocks onto the free stack in
 // descending id order (a block scan over [rel_lo, rel_hi] from the top down).
@@ -367,7 +368,7 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
     if (threadIdx.x == 0) st = meta->status;
     __syncthreads();
     if (st) return;
-    // args: branch[n], entry prefix[n]
+    // args: branch[n], entry prefix[n], first released entry[n]
     const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e < total) {
         int32_t l = 0, h = n - 1;
@@ -375,7 +376,7 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
             const int32_t mid = (l + h + 1) >> 1;
             if (args[n + mid] <= e) l = mid; else h = mid - 1;
         }
-        int32_t* slot = table + (int64_t)args[l] * bpb + (e - args[n + l]);
+        int32_t* slot = table + (int64_t)args[l] * bpb + args[2 * n + l] + (e - args[n + l]);
         const int32_t blk = *slot;
         *slot = -1;
         if ((uint32_t)blk >= (uint32_t)n_blocks) {
@@ -880,23 +881,24 @@ int dendrite_append_kv(dendrite_pool* p, const int32_t* branches, int32_t n, int
     return DENDRITE_OK;
 }
 
-int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* stream) {
-    DENDRITE_TRY(prelude(p));
-    if (n < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
-    if (n == 0) return DENDRITE_OK;
-    DENDRITE_TRY(check_unique_live(p, branches, n));
-    cudaStream_t s = (cudaStream_t)stream;
-    const int32_t bs = p->block_size;
-    // args: branch[n], entry prefix[n]
+}  // extern "C"
+
+namespace {
+
+// Releases table entries [start_i, end_i) of each branch on the device.
+int release_entries(dendrite_pool* p, const int32_t* branches, const int32_t* start, const int32_t* end,
+                    int32_t n, cudaStream_t s) {
     int64_t total = 0;
-    for (int32_t i = 0; i < n; ++i) total += (p->br[branches[i]].len + bs - 1) / bs;
+    for (int32_t i = 0; i < n; ++i) total += end[i] - start[i];
     if (total > INT32_MAX / 2) return DENDRITE_ELIMIT;
+    if (total == 0) return DENDRITE_OK;
     auto fill = [&](int32_t* a) {
         int32_t acc = 0;
         for (int32_t i = 0; i < n; ++i) {
             a[i] = branches[i];
             a[n + i] = acc;
-            acc += (p->br[branches[i]].len + bs - 1) / bs;
+            a[2 * n + i] = start[i];
+            acc += end[i] - start[i];
         }
     };
     const unsigned grid = (unsigned)((total + kFreeCollectThreads - 1) / kFreeCollectThreads);
@@ -906,23 +908,38 @@ int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* st
                                  p->d_released, p->d_stack, p->d_meta));
         return DENDRITE_OK;
     };
-    prof_begin(p, T_FREE, s);
-    if (total > 0) {
-        constexpr int CAP = 1024;
-        if (2 * n <= CAP) {
-            ParamArgs<CAP> a;
-            fill(a.v);
-            DENDRITE_TRY(launch(a));
-        } else {
-            char *h, *d;
-            const size_t bytes = (size_t)n * 8;
-            DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
-            fill((int32_t*)h);
-            DENDRITE_TRY(p->staging.upload(s, h, bytes));
-            DENDRITE_TRY(launch(GlobalArgs{(const int32_t*)d}));
-            DENDRITE_TRY(p->staging.release(s));
-        }
+    constexpr int CAP = 1536;
+    if (3 * n <= CAP) {
+        ParamArgs<CAP> a;
+        fill(a.v);
+        return launch(a);
     }
+    char *h, *d;
+    const size_t bytes = (size_t)n * 12;
+    DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
+    fill((int32_t*)h);
+    DENDRITE_TRY(p->staging.upload(s, h, bytes));
+    DENDRITE_TRY(launch(GlobalArgs{(const int32_t*)d}));
+    return p->staging.release(s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* stream) {
+    DENDRITE_TRY(prelude(p));
+    if (n < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
+    if (n == 0) return DENDRITE_OK;
+    DENDRITE_TRY(check_unique_live(p, branches, n));
+    cudaStream_t s = (cudaStream_t)stream;
+    const int32_t bs = p->block_size;
+    static thread_local std::vector<int32_t> start, end;
+    start.assign(n, 0);
+    end.resize(n);
+    for (int32_t i = 0; i < n; ++i) end[i] = (p->br[branches[i]].len + bs - 1) / bs;
+    prof_begin(p, T_FREE, s);
+    DENDRITE_TRY(release_entries(p, branches, start.data(), end.data(), n, s));
     prof_end(p, T_FREE, s);
     for (int32_t i = 0; i < n; ++i) {
         Branch& b = p->br[branches[i]];
@@ -931,6 +948,41 @@ int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* st
         b = Branch();
         p->free_handles.push_back(branches[i]);
         drop_node_ref(p, node);
+    }
+    p->version++;
+    return DENDRITE_OK;
+}
+
+int dendrite_truncate(dendrite_pool* p, const int32_t* branches, const int32_t* new_lens, int32_t n,
+                      void* stream) {
+    DENDRITE_TRY(prelude(p));
+    if (n < 0 || (n > 0 && (!branches || !new_lens))) return DENDRITE_EINVAL;
+    if (n == 0) return DENDRITE_OK;
+    DENDRITE_TRY(check_unique_live(p, branches, n));
+    for (int32_t i = 0; i < n; ++i)
+        if (new_lens[i] < 0 || new_lens[i] > p->br[branches[i]].len) return DENDRITE_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int32_t bs = p->block_size;
+    static thread_local std::vector<int32_t> start, end;
+    start.resize(n);
+    end.resize(n);
+    for (int32_t i = 0; i < n; ++i) {
+        start[i] = (new_lens[i] + bs - 1) / bs;
+        end[i] = (p->br[branches[i]].len + bs - 1) / bs;
+    }
+    prof_begin(p, T_FREE, s);
+    DENDRITE_TRY(release_entries(p, branches, start.data(), end.data(), n, s));
+    prof_end(p, T_FREE, s);
+    // the branch continues as a new node cut from its old one at new_len, so
+    // children forked from the old node keep the blocks they share with it
+    for (int32_t i = 0; i < n; ++i) {
+        Branch& b = p->br[branches[i]];
+        if (new_lens[i] == b.len) continue;
+        const int32_t old = b.node;
+        b.node = new_node(p, old, new_lens[i], branches[i]);
+        b.len = new_lens[i];
+        p->nodes[old].handle = -1;
+        drop_node_ref(p, old);
     }
     p->version++;
     return DENDRITE_OK;

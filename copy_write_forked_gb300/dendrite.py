@@ -64,6 +64,7 @@ _SIGS = {
     "dendrite_tree_attn_decode": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_tree_attn_decode_noalloc": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_free": [_p, _pi32, _i32, _p],
+    "dendrite_truncate": [_p, _pi32, _pi32, _i32, _p],
     "dendrite_sync": [_p, _p],
     "dendrite_branch_len": [_p, _i32, _pi32],
     "dendrite_read_table": [_p, _i32, _pi32, _i32, _pi32, _p],
@@ -246,6 +247,14 @@ class Pool:
     def free(self, branches: Sequence[int], stream=None) -> None:
         ba = _arr(branches)
         _check(lib().dendrite_free(self._h, _ptr(ba), len(branches), _stream_ptr(stream, self._dev)), "free")
+
+    def truncate(self, branches: Sequence[int], new_lens: Sequence[int], stream=None) -> None:
+        """Roll branch i back to its first ``new_lens[i]`` tokens."""
+        ba, la = _arr(branches), _arr(new_lens)
+        if len(branches) != len(new_lens):
+            raise DendriteError(-1, "branches / new_lens length")
+        _check(lib().dendrite_truncate(self._h, _ptr(ba), _ptr(la), len(branches), _stream_ptr(stream, self._dev)),
+               "truncate")
 
     def sync(self, stream=None) -> None:
         _check(lib().dendrite_sync(self._h, _stream_ptr(stream, self._dev)), "sync")

@@ -30,13 +30,35 @@ def run_script(pool: Pool, w, device="cuda", stop: Optional[int] = None, stream=
             pool.free([h[b] for b in op.branches], stream=stream)
             for b in op.branches:
                 del h[b]
+        elif op.kind == "truncate":
+            pool.truncate([h[b] for b in op.branches], op.new_lens, stream=stream)
     return h
+
+
+def _max_len(w) -> int:
+    """Longest any branch gets during the script (rollbacks make it exceed the final lengths)."""
+    ln, top = {}, 0
+    for op in w.ops:
+        if op.kind == "new":
+            ln[op.branches[0]] = 0
+        elif op.kind == "append":
+            for b in op.branches:
+                ln[b] += op.n_new
+                top = max(top, ln[b])
+        elif op.kind == "fork":
+            for p, ch in zip(op.branches, op.children):
+                for c in ch:
+                    ln[c] = ln[p]
+        elif op.kind == "truncate":
+            for b, n in zip(op.branches, op.new_lens):
+                ln[b] = n
+    return top
 
 
 def pool_for(w, extra_blocks: int = 16, max_branches: Optional[int] = None, **kw) -> Pool:
     """A pool sized for workload ``w``."""
     nb = max(1, w.blocks_upper_bound() + extra_blocks)
     mb = max_branches or max(16, w.n_branch_ids() + 8)
-    bpb = max(16, max(-(-L // w.block_size) for L in w.lengths().values()) + 4) if w.lengths() else 16
+    bpb = max(16, -(-_max_len(w) // w.block_size) + 4)
     return Pool(nb, w.block_size, w.n_kv_heads, w.head_dim, w.dtype, max_branches=mb,
                 max_blocks_per_branch=bpb, **kw)

@@ -49,11 +49,13 @@ class Op:
       'fork'   -- fork each parent in ``branches``; parent i gets the children
                   ``children[i]`` (a tuple of new logical ids)
       'free'   -- release every branch in ``branches`` (one call)
+      'truncate' -- roll branch i of ``branches`` back to ``new_lens[i]`` tokens (one call)
     """
     kind: str
     branches: Tuple[int, ...]
     n_new: int = 0
     children: Tuple[Tuple[int, ...], ...] = ()
+    new_lens: Tuple[int, ...] = ()
 
 
 @dataclass
@@ -129,6 +131,9 @@ class Workload:
             elif op.kind == "free":
                 for b in op.branches:
                     del ln[b]
+            elif op.kind == "truncate":
+                for b, n in zip(op.branches, op.new_lens):
+                    ln[b] = n
         return ln
 
     def n_branch_ids(self) -> int:
@@ -159,6 +164,9 @@ class Workload:
                 for p, ch in zip(op.branches, op.children):
                     for c in ch:
                         ln[c] = ln[p]
+            elif op.kind == "truncate":
+                for b, n in zip(op.branches, op.new_lens):
+                    ln[b] = n
         return total
 
     def unique_kv_tokens(self) -> int:
@@ -167,25 +175,36 @@ class Workload:
         A token is identified by the branch that appended it and its position;
         forks share everything before the fork point (Dendrite article, section
         "技术深度解析": the shared prefix is stored once)."""
-        parent: Dict[int, Tuple[int, int]] = {}
-        ln: Dict[int, int] = {}
+        # nodes are (branch id, version); a truncate starts a new version of
+        # the branch cut from the old one at the new length
+        parent: Dict[Tuple[int, int], Tuple[Tuple[int, int], int]] = {}
+        ln: Dict[Tuple[int, int], int] = {}
+        cur: Dict[int, Tuple[int, int]] = {}
         for op in self.ops:
             if op.kind == "new":
-                ln[op.branches[0]] = 0
+                cur[op.branches[0]] = (op.branches[0], 0)
+                ln[cur[op.branches[0]]] = 0
             elif op.kind == "append":
                 for b in op.branches:
-                    ln[b] += op.n_new
+                    ln[cur[b]] += op.n_new
             elif op.kind == "fork":
                 for p, ch in zip(op.branches, op.children):
                     for c in ch:
-                        parent[c] = (p, ln[p])
-                        ln[c] = ln[p]
+                        cur[c] = (c, 0)
+                        parent[cur[c]] = (cur[p], ln[cur[p]])
+                        ln[cur[c]] = ln[cur[p]]
+            elif op.kind == "truncate":
+                for b, n in zip(op.branches, op.new_lens):
+                    old = cur[b]
+                    cur[b] = (b, old[1] + 1)
+                    parent[cur[b]] = (old, n)
+                    ln[cur[b]] = n
         # Owner intervals: token position pos of branch b belongs to b when it
         # is at or beyond b's fork point, else to the parent (recursively).
         seen = set()
         for b in self.query:
-            cap = ln[b]
-            node = b
+            node = cur[b]
+            cap = ln[node]
             while True:
                 start = parent[node][1] if node in parent else 0
                 if start < cap:
@@ -322,7 +341,8 @@ def fork_chain_script(depth_blocks: int, block_size: int = 16) -> int:
 
 
 def random_script(rng_seed: int, n_ops: int = 40, max_live: int = 8, max_append: int = 40,
-                  n_kv=2, n_q=4, d=16, bs=4, dtype=torch.float32, q_len=1, seed=0) -> Workload:
+                  n_kv=2, n_q=4, d=16, bs=4, dtype=torch.float32, q_len=1, seed=0,
+                  truncates: bool = False) -> Workload:
     """A random op sequence (fork / append / free) over a small pool, for
     property tests.  Appends pick several distinct live branches at once."""
     rng = random.Random(seed_of(rng_seed, "script"))
@@ -359,6 +379,13 @@ def random_script(rng_seed: int, n_ops: int = 40, max_live: int = 8, max_append:
             ops.append(Op("free", (b,)))
             live.remove(b)
             del ln[b]
+        elif r < 0.92 and truncates:
+            k = rng.randint(1, min(2, len(live)))
+            tgt = tuple(rng.sample(live, k))
+            nl = tuple(rng.randint(0, ln[b]) for b in tgt)
+            ops.append(Op("truncate", tgt, new_lens=nl))
+            for b, n in zip(tgt, nl):
+                ln[b] = n
         else:
             ops.append(Op("new", (nxt,)))
             live.append(nxt)

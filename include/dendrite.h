@@ -157,6 +157,21 @@ int dendrite_tree_attn_decode(dendrite_pool* pool, const void* Q, int32_t n_q_he
  */
 int dendrite_free(dendrite_pool* pool, const int32_t* branches, int32_t n_branches, void* stream);
 
+/*
+ * Rollback: branch i keeps only its first new_lens[i] tokens (host int32
+ * arrays; 0 <= new_lens[i] <= current length; no duplicate branches).  This is
+ * the reject step of speculative decoding (DSpark blog, section 第二层:
+ * predict, verify in parallel, accept or roll back).  Table entries past
+ * ceil(new_len / block_size) each drop one reference; blocks that reach zero
+ * are pushed on the free stack in descending id order, as for free.  A kept
+ * tail block that is now partially valid and still shared is copied on the
+ * next append.  Branches forked from this one earlier keep everything they
+ * share with it.  Accepting one draft path and discarding its siblings is a
+ * truncate of the winner plus a free of the others.
+ */
+int dendrite_truncate(dendrite_pool* pool, const int32_t* branches, const int32_t* new_lens,
+                      int32_t n_branches, void* stream);
+
 /* Wait for the pool's work on `stream`, then return its sticky device status. */
 int dendrite_sync(dendrite_pool* pool, void* stream);
 

@@ -162,6 +162,30 @@ class BlockPool:
         for blk in sorted(released, reverse=True):
             self._push(blk)
 
+    def truncate(self, branches: Sequence[int], new_lens: Sequence[int]) -> None:
+        """Roll each branch back to its first new_len tokens (speculative
+        decoding's reject step: DSpark blog, section "第二层：预测 + 并行 + 验证
+        + 回滚", Accept / Rollback).  Table entries past ceil(new_len / bs)
+        drop one reference; the kept tail block, if partially valid now, is
+        copied on the next append when still shared.  Released blocks of the
+        call are pushed in descending id order, as for free."""
+        if len(set(branches)) != len(branches):
+            raise ValueError("duplicate branch in one truncate")
+        for b, n in zip(branches, new_lens):
+            if not 0 <= n <= self.len[b]:
+                raise ValueError("new length out of range")
+        released = []
+        for b, n in zip(branches, new_lens):
+            keep = -(-n // self.bs)
+            for blk in self.table[b][keep:]:
+                self.refcount[blk] -= 1
+                if self.refcount[blk] == 0:
+                    released.append(blk)
+            del self.table[b][keep:]
+            self.len[b] = n
+        for blk in sorted(released, reverse=True):
+            self._push(blk)
+
     # ---------------------------------------------------------- inspection
     def read_branch_bits(self, h: int):
         """K and V bits ``[len][n_kv][d]`` of branch ``h`` read through its table."""
@@ -196,4 +220,6 @@ def run_script_pool(w, num_blocks: int, kv_source=None, stop=None) -> BlockPool:
             pool.append(op.branches, op.n_new, bits_of(K), bits_of(V))
         elif op.kind == "free":
             pool.free(op.branches)
+        elif op.kind == "truncate":
+            pool.truncate(op.branches, op.new_lens)
     return pool

@@ -101,6 +101,15 @@ class KVTree:
     def free(self, h: int) -> None:
         del self.nodes[h]
 
+    def truncate(self, h: int, n: int) -> None:
+        """Roll branch ``h`` back to its first ``n`` positions (the reject step
+        of one parallel verification, DSpark blog, section 第二层).  The branch
+        continues as a new leaf cut from its old node at position n, so any
+        child forked from the old node keeps seeing what it saw."""
+        old = self.nodes[h]
+        assert 0 <= n <= old.length()
+        self.nodes[h] = _Node(old, n, self.n_kv, self.d)
+
     def length(self, h: int) -> int:
         return self.nodes[h].length()
 
@@ -199,4 +208,7 @@ def run_script_tree(w, kv_source=None) -> KVTree:
         elif op.kind == "free":
             for b in op.branches:
                 tree.free(b)
+        elif op.kind == "truncate":
+            for b, n in zip(op.branches, op.new_lens):
+                tree.truncate(b, n)
     return tree

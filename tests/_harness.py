@@ -45,6 +45,10 @@ def oracle_tree(w, ids: Iterable[int], device="cpu") -> KVTree:
                 if b in keep:
                     k, v = w.kv_one(idx, pos, device)
                     tree.append(b, k.cpu(), v.cpu())
+        elif op.kind == "truncate":
+            for b, n in zip(op.branches, op.new_lens):
+                if b in keep:
+                    tree.truncate(b, n)
     return tree
 
 

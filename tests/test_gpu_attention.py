@@ -107,6 +107,23 @@ def test_repeated_calls_reuse_the_plan_and_agree():
     pool.close()
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_trees_with_rollbacks_bf16(seed):
+    w = W.random_script(200 + seed, n_ops=30, max_live=8, max_append=90, n_kv=2, n_q=8, d=128, bs=16,
+                        dtype=torch.bfloat16, q_len=1 + seed % 2, seed=seed, truncates=True)
+    run_and_check(w, TOL_BF16)
+
+
+def test_speculative_accept_and_rollback():
+    """Verify 3 draft paths of 8 tokens, keep 5 tokens of path 1, drop the others,
+    then decode one more token on the winner."""
+    ops = [W.Op("new", (0,)), W.Op("append", (0,), 700), W.Op("fork", (0,), children=((1, 2, 3),)),
+           W.Op("append", (1, 2, 3), 8), W.Op("truncate", (2,), new_lens=(705,)), W.Op("free", (1, 3)),
+           W.Op("append", (2,), 1)]
+    w = W.Workload("accept", 8, 32, 128, 16, torch.bfloat16, ops, (0, 2), 1)
+    run_and_check(w, TOL_BF16)
+
+
 def test_attention_after_free_of_shared_parent():
     ops = [W.Op("new", (0,)), W.Op("append", (0,), 100), W.Op("fork", (0,), children=((1, 2),)),
            W.Op("free", (0,)), W.Op("append", (1, 2), 30)]

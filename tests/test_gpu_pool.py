@@ -89,6 +89,37 @@ def test_random_scripts_match_oracle_after_every_op(seed, dtype):
     pool.close()
 
 
+def test_golden_truncate_case_on_gpu():
+    g = GOLDEN["truncate_case"]
+    ops = [W.Op("new", (0,)), W.Op("append", (0,), 20), W.Op("fork", (0,), children=((1, 2),)),
+           W.Op("append", (1,), 20), W.Op("append", (2,), 8), W.Op("truncate", (1, 2), new_lens=(22, 20)),
+           W.Op("free", (0,)), W.Op("append", (1,), 3), W.Op("append", (2,), 1)]
+    w = W.Workload("trunc", 2, 4, 64, 16, torch.float32, ops, (1, 2))
+    pool = Pool(64, 16, 2, 64, torch.float32, max_branches=8, max_blocks_per_branch=16)
+    h = run_script(pool, w)
+    pool.sync()
+    for b, tab in g["tables"].items():
+        assert pool.read_table(h[int(b)]) == tab
+    rc = pool.read_refcounts()
+    assert rc[:len(g["refcount_prefix"])] == g["refcount_prefix"]
+    assert pool.read_free_stack()[-2:] == g["free_stack_top"]
+    ref = run_script_pool(w, 64, kv_source=_gpu_kv(w))
+    pool_state_matches(pool, h, ref)
+    pool.close()
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_scripts_with_rollbacks_match_oracle(seed):
+    w = W.random_script(100 + seed, n_ops=30, max_live=8, max_append=40, n_kv=2, n_q=8, d=128, bs=16,
+                        dtype=torch.bfloat16, truncates=True)
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    ref = run_script_pool(w, pool.num_blocks, kv_source=_gpu_kv(w))
+    pool.sync()
+    pool_state_matches(pool, h, ref)
+    pool.close()
+
+
 def test_three_holders_of_one_tail_follow_argument_order():
     # root of 40 tokens (tail half full) forked 3 ways, root freed: refcount 3 = holders,
     # so in argument order [c3, c1, c2] the first two copy and the last writes in place

@@ -71,6 +71,43 @@ def test_golden_tiny_cow_states(variant):
     assert pool.free_stack() == list(range(N_TINY - 1, -1, -1))
 
 
+def test_golden_truncate_case():
+    g = GOLDEN["truncate_case"]
+    pool = BlockPool(64, 16, 2, 64, np.uint32)
+    rng = np.random.default_rng(0)
+    z = lambda n: rng.integers(0, 2**31, size=(1, n, 2, 64), dtype=np.uint32)
+    pool.new_branch(0)
+    pool.append([0], 20, z(20), z(20))
+    pool.fork([0], [[1, 2]])
+    pool.append([1], 20, z(20), z(20))
+    pool.append([2], 8, z(8), z(8))
+    pool.truncate([1, 2], [22, 20])
+    pool.free([0])
+    pool.append([1], 3, z(3), z(3))
+    pool.append([2], 1, z(1), z(1))
+    assert {str(k): v for k, v in pool.table.items()} == g["tables"]
+    assert {str(k): v for k, v in pool.len.items()} == g["lens"]
+    rp = g["refcount_prefix"]
+    assert pool.refcount[:len(rp)].tolist() == rp and int(pool.refcount[len(rp):].sum()) == 0
+    assert pool.free_stack()[-2:] == g["free_stack_top"]
+    assert pool.used_blocks() == g["used_blocks"]
+    check_invariants(pool)
+
+
+@pytest.mark.parametrize("seed", range(15))
+def test_invariants_with_rollbacks(seed):
+    w = W.random_script(seed, n_ops=40, max_live=8, max_append=12, n_kv=2, n_q=4, d=4, bs=4, truncates=True)
+    N = w.blocks_upper_bound() + 3
+    for stop in range(1, len(w.ops) + 1):
+        check_invariants(run_script_pool(w, N, stop=stop))
+    pool = run_script_pool(w, N)
+    tree = run_script_tree(w)
+    for b in pool.table:
+        Kb, _ = pool.read_branch_bits(b)
+        Kt, _ = tree.materialise(b)
+        assert np.array_equal(Kb.view(np.float32).astype(np.float64), Kt)
+
+
 def test_sequential_calls_give_same_state_as_one_call():
     # variant c with the two appends issued as separate calls
     w = W.tiny_cow("c")

@@ -40,6 +40,9 @@ def naive_copy_replay(w):
         elif op.kind == "free":
             for b in op.branches:
                 del seqs[b]
+        elif op.kind == "truncate":
+            for b, n in zip(op.branches, op.new_lens):
+                seqs[b] = (seqs[b][0][:n], seqs[b][1][:n])
     return seqs
 
 
@@ -90,6 +93,30 @@ def test_tree_equals_dense_attention_on_concatenated_sequence(s):
     assert got.keys() == ref.keys() and got
     for b in got:
         np.testing.assert_allclose(got[b], ref[b].astype(np.float64), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("s", range(8))
+def test_tree_with_rollbacks_equals_dense_attention(s):
+    w = W.random_script(50 + s, n_ops=18, max_live=5, max_append=10, n_kv=2, n_q=4, d=8, bs=4,
+                        q_len=1 + s % 2, seed=300 + s, truncates=True)
+    assert any(op.kind == "truncate" for op in w.ops) or s > 5
+    got, ref = tree_outputs(w), brute_outputs(w)
+    for b in got:
+        np.testing.assert_allclose(got[b], ref[b].astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_rollback_leaves_children_of_the_old_branch_unchanged():
+    rng = np.random.default_rng(11)
+    t = KVTree(2, 8)
+    t.new_root(0)
+    t.append(0, _rand((12, 2, 8), rng), _rand((12, 2, 8), rng))
+    t.fork(0, [1])
+    Q = _rand((1, 4, 8), rng)
+    before = t.attend(1, Q)
+    t.truncate(0, 5)
+    t.append(0, _rand((9, 2, 8), rng), _rand((9, 2, 8), rng))
+    assert np.array_equal(t.attend(1, Q), before)
+    assert t.length(0) == 14
 
 
 def test_tiny_workloads_match_brute_force():
