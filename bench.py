@@ -236,7 +236,8 @@ def run_ours(args):
     # ---- per-kernel device times (profiling events inside the library; one
     # synchronised step at a time so the events of each call can be read)
     pool.set_profiling(True)
-    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "free", "attn_total")}
+    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
+                            "attn_total")}
     plan_us = []
     for i in range(min(args.steps, 100)):
         flush_l2()
@@ -296,7 +297,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
 
-    gpu_launches = 7 * args.steps   # fork 1 + append 2 + attention 2 + free 2 per timed step
+    gpu_launches = 6 * args.steps   # fork 1 + append 2 (meta, copy) + attention 2 (partial, merge) + free 1
     line = {
         "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
         "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,

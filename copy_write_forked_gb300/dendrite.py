@@ -23,7 +23,7 @@ ERRORS = {
     -1: "EINVAL", -2: "ENOMEM", -3: "EBADHANDLE", -4: "ELIMIT", -5: "EDTYPE",
     -6: "ECUDA", -7: "ETIMEOUT", -8: "ECORRUPT",
 }
-TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "reserved", "free", "attn_total")
+TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total")
 FP32, BF16 = 0, 1
 
 _LIB = None

@@ -206,8 +206,8 @@ int dendrite_pool_info(dendrite_pool* pool, int64_t* num_blocks, int32_t* block_
  * the caller's stream.  dendrite_last_timings() synchronises on them and
  * returns the device milliseconds of the most recent call of each kind:
  *   ms[0] fork, ms[1] append metadata, ms[2] append copy/scatter,
- *   ms[3] attention kernel (partials with the merge fused in), ms[4] reserved,
- *   ms[5] free (both phases), ms[6] whole attention call.
+ *   ms[3] attention partial kernel, ms[4] log-sum-exp merge kernel,
+ *   ms[5] free (or truncate), ms[6] whole attention call (partial + merge).
  * Entries with no recorded call are set to -1.                                */
 #define DENDRITE_N_TIMINGS 7
 int dendrite_set_profiling(dendrite_pool* pool, int32_t enable);
