@@ -348,7 +348,7 @@ def run_attention_only(args):
     g.build()
     from copy_write_forked_gb300.runner import pool_for, run_script
     w, desc = other_workload(args.workload)
-    pool = pool_for(w)
+    pool = pool_for(w, tc_min_rows=args.tc_min_rows)
     h = run_script(pool, w, device=dev)
     br = [h[b] for b in w.query]
     Q = w.q(dev)
@@ -360,13 +360,15 @@ def run_attention_only(args):
         flush_r.max()
         pool.tree_attn_decode(Q, br, out=out)
     pool.set_profiling(True)
-    part, tot = [], []
+    part, tot, tcms = [], [], []
     for _ in range(args.steps):
         flush_r.max()
         pool.tree_attn_decode(Q, br, out=out)
         tm = pool.last_timings()
         part.append(tm["attn_partial"])
         tot.append(tm["attn_total"])
+        if tm.get("attn_tc") is not None:
+            tcms.append(tm["attn_tc"])
     pool.sync()
     st = pool.last_plan_stats()
     unique = w.unique_kv_bytes() + Q.numel() * Q.element_size()
@@ -380,7 +382,10 @@ def run_attention_only(args):
             "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
             "config": {"workload": desc, "step": "tree decode attention on a prebuilt tree (plan cached)",
                        "l2": "flushed between calls (256 MiB read)"},
-            "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": ach, "peak": peak,
+            "tc_kernel_ms": statistics.median(tcms) if tcms else None,
+            "roofline": {"bound": "hbm",
+                         "kernel": ("k_attn_partial_tc + " if st["n_tc_units"] else "") + "k_attn_partial_bf16",
+                         "achieved": ach, "peak": peak,
                          "peak_source": src, "unit": "GB/s", "frac": ach / peak, "algorithmic_bytes": unique},
             "plan": st}
     print(json.dumps(line), flush=True)
@@ -536,6 +541,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tc-min-rows", type=int, default=0,
+                    help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
     ap.add_argument("--workload", default="beam", choices=["beam", "mcts", "specverify", "stress"],
                     help="beam = the full-path step (default JSON line); others time tree attention only")
     args = ap.parse_args()

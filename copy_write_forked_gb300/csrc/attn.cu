@@ -39,124 +39,19 @@
 #include <cmath>
 #include <cstring>
 
-#include "dendrite_internal.h"
+#include "attn_common.cuh"
 
 using namespace dendrite;
 
 namespace {
 
-constexpr int D = 128;
-constexpr int BS = 16;
 constexpr int NSTAGE = 3;
-constexpr int HALF_BYTES = BS * 64 * 2;          // one 64-column half of a K or V tile
 constexpr int SLOT_BYTES = 4 * HALF_BYTES;       // K (2 halves) + V (2 halves) of one tile
 constexpr int STAGE_BYTES = 4 * SLOT_BYTES;
 constexpr int NCONS = 4;
 constexpr int THREADS = (NCONS + 1) * 32;
 constexpr int ML_BYTES = NCONS * 16 * 2 * 4;
 constexpr size_t SMEM_BF16 = 1024 + (size_t)NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8 + ML_BYTES;
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
-
-struct AttnArgs {
-    AttnPlanDev plan;
-    const void* Q;
-    void* out;
-    const int32_t* table;
-    const float* pool_k;   // fp32 kernel
-    const float* pool_v;
-    const void* pool_kv[2];   // K and V pool bases (bf16 kernel's L2 prefetches)
-    float* part_acc;       // [partial rows][head_dim]
-    float2* part_ml;       // [partial rows] (m, l)
-    DevMeta* meta;
-    int32_t bpb;
-    int32_t n_kv;
-    int32_t head_dim;
-    int32_t n_blocks;
-    float scale_log2;      // log2(e) / sqrt(head_dim)
-};
-
-// ------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait: true when the phase with `parity` completed; false on
-// timeout or when another role of the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
-        }
-    }
-    return false;
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-        "%4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ float bf16_pair_sum(uint32_t v) {
-    return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
-}
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Byte offset of element (token t, column d) inside one swizzled K or V tile:
-// two 64-column halves of 16 rows x 128 bytes, 16-byte chunks XOR-ed with
-// (row & 7) as TMA's 128-byte swizzle lays them out.
-__device__ __forceinline__ uint32_t swz(int t, int d) {
-    return (uint32_t)((d >> 6) * HALF_BYTES + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4) + (d & 7) * 2);
-}
 
 
 // ============================================================ bf16 kernel
@@ -588,7 +483,7 @@ __global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
     const int32_t o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int32_t n_out = pl.n_queried * pl.q_len * pl.n_q_heads;
     if (o >= n_out || a.meta->status) return;
-    const int G = pl.group, RM = pl.q_len * G;
+    const int G = pl.group;
     const int32_t qi = o / (pl.q_len * pl.n_q_heads);
     const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
     const int32_t j = rem / pl.n_q_heads, hq = rem - j * pl.n_q_heads;
@@ -603,12 +498,13 @@ __global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
         const int32_t e = e0 + lane;
         int32_t nch = 0, base = 0, stride = 0;
         if (e < pend) {
-            const int4 pe = __ldg(reinterpret_cast<const int4*>(pl.path) + e);   // unit_base, ngroups, sr0
+            // unit_base, ngroups, first segment row, rows per group
+            const int4 pe = __ldg(reinterpret_cast<const int4*>(pl.path) + e);
             const int32_t sr = pe.z + j * G + g;
-            const int32_t grp = sr / pl.max_rows;
+            const int32_t grp = sr / pe.w;
             const AttnUnit U = pl.units[pe.x + h * pe.y + grp];
             nch = U.nchunks;
-            base = U.prow_base + (sr - grp * pl.max_rows);
+            base = U.prow_base + (sr - grp * pe.w);
             stride = U.n_rows;
         }
         int32_t incl = nch;
@@ -682,34 +578,108 @@ struct HostPlan {
     std::vector<AttnMember> members;
     std::vector<AttnUnit> units;
     std::vector<AttnRow> rows;
-    std::vector<int32_t> cta_begin, cta_unit, path_off, path;
+    std::vector<int32_t> cta_begin, cta_unit, tc_cta_begin, tc_cta_unit, path_off, path;
     std::vector<int64_t> cuts;
     int64_t tiles = 0, unique_tiles = 0;
+    int32_t n_tc_units = 0;
     size_t partial_rows = 0;
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
         segs.clear(); members.clear(); units.clear(); rows.clear(); cta_begin.clear(); cta_unit.clear();
-        path_off.clear(); path.clear(); cuts.clear();
+        tc_cta_begin.clear(); tc_cta_unit.clear(); path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
+        n_tc_units = 0;
         partial_rows = 0;
     }
 };
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-// Partition weights, fitted to per-CTA timelines on GB300: a tile of a unit
-// with rt row tiles costs about (1 + rt) units (HBM time plus mma time: 0.25 us
-// for rt = 1 vs 0.61 us for rt = 4 per CTA), and every chunk boundary (partial
-// store, combine, next unit's Q) about as much as 8 one-row-tile tiles.
-constexpr int64_t kUnitStartWeight = 16;
+// Partition weights, fitted to per-CTA timelines on GB300.  mma.sync class: a
+// tile of a unit with rt row tiles of 16 costs about (1 + rt) units (HBM time
+// plus mma time: 0.25 us for rt = 1 vs 0.61 us for rt = 4 per CTA), and every
+// chunk boundary (partial store, combine, next unit's Q) about as much as 8
+// one-row-tile tiles.  tcgen05 class (one CTA per SM): a tile costs about
+// (1 + rt) with rt row tiles of 128; a chunk boundary drains the MMA pipeline
+// and stores up to 256 partial rows of 520 bytes.
+struct ClassWeights {
+    int64_t unit_start;
+    int64_t min_per_cta;   // smallest total weight worth a CTA of its own
+};
+constexpr ClassWeights kSmallWeights{16, 8};
+constexpr ClassWeights kTcWeights{24, 32};
 inline int64_t tile_weight(int rt) { return 1 + rt; }
 
+// Stream-K split of one class's tile list (units [u_lo, u_hi), tiles
+// [0, T)) into at most max_ctas CTAs of about equal weight (tile_weight per
+// tile plus unit_start per unit start).  Cuts are made strictly increasing so
+// that no CTA is empty.  Fills begin[C + 1], cunit[C] and each unit's cfirst
+// and nchunks.
+void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_t weight, int max_ctas,
+                     const ClassWeights& cw_, std::vector<int32_t>& begin, std::vector<int32_t>& cunit) {
+    begin.clear();
+    cunit.clear();
+    if (u_lo == u_hi) {
+        begin.push_back(0);
+        return;
+    }
+    const int C0 = (int)std::max<int64_t>(
+        1, std::min<int64_t>(max_ctas, (weight + cw_.min_per_cta - 1) / cw_.min_per_cta));
+    hp.cuts.clear();
+    hp.cuts.push_back(0);
+    {
+        int c = 1;
+        int64_t cw = 0;
+        for (int32_t ui = u_lo; ui < u_hi; ++ui) {
+            const AttnUnit& U = hp.units[ui];
+            const int64_t nb = U.n_blk;
+            const int64_t tw = tile_weight(U.rt);
+            const int64_t uw = cw_.unit_start + nb * tw;
+            while (c < C0) {
+                const int64_t target = (weight * c + C0 - 1) / C0;
+                if (target >= cw + uw) break;
+                const int64_t k = std::max<int64_t>(0, (target - cw - cw_.unit_start + tw - 1) / tw);
+                const int64_t cut = U.tile_off + std::min<int64_t>(k, nb);
+                if (cut > hp.cuts.back() && cut < T) hp.cuts.push_back(cut);
+                ++c;
+            }
+            cw += uw;
+        }
+    }
+    hp.cuts.push_back(T);
+    const int C = (int)hp.cuts.size() - 1;
+    begin.resize(C + 1);
+    for (int i = 0; i <= C; ++i) begin[i] = (int32_t)hp.cuts[i];
+    cunit.resize(C);
+    {
+        int32_t u = u_lo;
+        for (int c = 0; c < C; ++c) {
+            while (u + 1 < u_hi && hp.units[u].tile_off + hp.units[u].n_blk <= begin[c]) ++u;
+            cunit[c] = u;
+        }
+    }
+    int c = 0;
+    for (int32_t ui = u_lo; ui < u_hi; ++ui) {
+        AttnUnit& U = hp.units[ui];
+        const int32_t last = U.tile_off + U.n_blk - 1;
+        while (begin[c + 1] <= U.tile_off) ++c;
+        int cl = c;
+        while (begin[cl + 1] <= last) ++cl;
+        U.cfirst = c;
+        U.nchunks = cl - c + 1;
+    }
+}
+
+// max_ctas: CTAs of the mma.sync/fp32 kernel; max_tc_ctas: of the tcgen05
+// kernel (0 when it is not used).
 int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
-               HostPlan& hp) {
+               int max_tc_ctas, HostPlan& hp) {
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
     const int32_t RM = q_len * G;
-    const int max_rows = p->dtype == DENDRITE_BF16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    const bool bf16 = p->dtype == DENDRITE_BF16;
+    const int small_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    const bool tc_on = bf16 && max_tc_ctas > 0 && p->tc_min_rows >= 0;
     const int32_t n_nodes = (int32_t)p->nodes.size();
     hp.parent.resize(n_nodes);
     hp.fork_len.resize(n_nodes);
@@ -723,119 +693,87 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     for (int32_t i = 0; i < n; ++i) hp.queried[i] = p->br[branches[i]].node;
     plan_segments(n_nodes, hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
                   hp.psegs, hp.seg_members);
-    // segments, their members and their units (kv head major, then row group)
-    int64_t tile_off = 0, weight = 0;
-    for (const Segment& sg : hp.psegs) {
-        const int32_t rows_per_head = sg.n_members * RM;
-        AttnSeg S;
-        S.table_row = p->nodes[sg.rep_node].handle;
-        S.blk_start = sg.block_start;
-        S.n_blk = sg.block_count;
-        S.mem_off = (int32_t)hp.members.size();
-        S.n_mem = sg.n_members;
-        S.unit_base = (int32_t)hp.units.size();
-        S.ngroups = (rows_per_head + max_rows - 1) / max_rows;
-        S.pad = 0;
-        for (int32_t k = 0; k < sg.n_members; ++k) {
-            const int32_t qi = hp.seg_members[sg.member_offset + k];
-            hp.members.push_back({qi, p->br[branches[qi]].len});
-        }
-        hp.unique_tiles += (int64_t)sg.block_count * nkv;
-        const int32_t seg_index = (int32_t)hp.segs.size();
-        for (int32_t h = 0; h < nkv; ++h) {
-            for (int32_t grp = 0; grp < S.ngroups; ++grp) {
-                AttnUnit U{};
-                U.seg = seg_index;
-                U.kv_head = h;
-                U.row_lo = grp * max_rows;
-                U.n_rows = std::min(max_rows, rows_per_head - U.row_lo);
-                U.rt = U.n_rows <= 16 ? 1 : U.n_rows <= 32 ? 2 : 4;
-                U.tile_off = (int32_t)tile_off;
-                U.table_row = S.table_row;
-                U.blk_start = S.blk_start;
-                U.n_blk = S.n_blk;
-                U.row_off = (int32_t)hp.rows.size();
-                // rows: segment row sr -> member sr / RM, token (sr % RM) / G, group sr % G
-                {
-                    int32_t mi = U.row_lo / RM, rem = U.row_lo % RM;
-                    int32_t j = rem / G, g = rem % G;
-                    for (int32_t r = 0; r < U.n_rows; ++r) {
-                        const AttnMember& M = hp.members[S.mem_off + mi];
-                        hp.rows.push_back({(M.qi * q_len + j) * nq + h * G + g, M.len - q_len + j + 1});
-                        if (++g == G) {
-                            g = 0;
-                            if (++j == q_len) {
-                                j = 0;
-                                ++mi;
+    // Segments, their members and their units (kv head major, then row
+    // group), tensor-core segments first: pass 0 takes the segments read by
+    // more than tc_min_rows rows per kv head, pass 1 the rest.
+    int64_t weight[2] = {0, 0}, class_tiles[2] = {0, 0};
+    for (int pass = 0; pass < 2; ++pass) {
+        int64_t tile_off = 0;
+        for (const Segment& sg : hp.psegs) {
+            const int32_t rows_per_head = sg.n_members * RM;
+            const bool tc = tc_on && rows_per_head > p->tc_min_rows;
+            if (tc != (pass == 0)) continue;
+            const int32_t group_rows = tc ? kMaxUnitRowsTc : small_rows;
+            const ClassWeights& cwt = tc ? kTcWeights : kSmallWeights;
+            AttnSeg S;
+            S.table_row = p->nodes[sg.rep_node].handle;
+            S.blk_start = sg.block_start;
+            S.n_blk = sg.block_count;
+            S.mem_off = (int32_t)hp.members.size();
+            S.n_mem = sg.n_members;
+            S.unit_base = (int32_t)hp.units.size();
+            S.ngroups = (rows_per_head + group_rows - 1) / group_rows;
+            S.group_rows = group_rows;
+            for (int32_t k = 0; k < sg.n_members; ++k) {
+                const int32_t qi = hp.seg_members[sg.member_offset + k];
+                hp.members.push_back({qi, p->br[branches[qi]].len});
+            }
+            hp.unique_tiles += (int64_t)sg.block_count * nkv;
+            const int32_t seg_index = (int32_t)hp.segs.size();
+            for (int32_t h = 0; h < nkv; ++h) {
+                for (int32_t grp = 0; grp < S.ngroups; ++grp) {
+                    AttnUnit U{};
+                    U.seg = seg_index;
+                    U.kv_head = h;
+                    U.row_lo = grp * group_rows;
+                    U.n_rows = std::min(group_rows, rows_per_head - U.row_lo);
+                    U.rt = tc ? (U.n_rows + 127) / 128 : U.n_rows <= 16 ? 1 : U.n_rows <= 32 ? 2 : 4;
+                    U.tile_off = (int32_t)tile_off;
+                    U.table_row = S.table_row;
+                    U.blk_start = S.blk_start;
+                    U.n_blk = S.n_blk;
+                    U.row_off = (int32_t)hp.rows.size();
+                    // rows: segment row sr -> member sr / RM, token (sr % RM) / G, group sr % G
+                    {
+                        int32_t mi = U.row_lo / RM, rem = U.row_lo % RM;
+                        int32_t j = rem / G, g = rem % G;
+                        for (int32_t r = 0; r < U.n_rows; ++r) {
+                            const AttnMember& M = hp.members[S.mem_off + mi];
+                            hp.rows.push_back({(M.qi * q_len + j) * nq + h * G + g, M.len - q_len + j + 1});
+                            if (++g == G) {
+                                g = 0;
+                                if (++j == q_len) {
+                                    j = 0;
+                                    ++mi;
+                                }
                             }
                         }
                     }
+                    tile_off += S.n_blk;
+                    weight[pass] += cwt.unit_start + (int64_t)S.n_blk * tile_weight(U.rt);
+                    hp.units.push_back(U);
                 }
-                tile_off += S.n_blk;
-                weight += kUnitStartWeight + (int64_t)S.n_blk * tile_weight(U.rt);
-                hp.units.push_back(U);
             }
+            hp.segs.push_back(S);
         }
-        hp.segs.push_back(S);
+        class_tiles[pass] = tile_off;
+        if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
+        if (pass == 0) hp.n_tc_units = (int32_t)hp.units.size();
     }
-    if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
-    hp.tiles = tile_off;
-    // even split of the weighted tile list (tile_weight per tile plus
-    // kUnitStartWeight per unit start); cuts are made strictly increasing so
-    // that no CTA is empty.
-    const int64_t T = tile_off;
-    const int C0 = (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + 7) / 8));
-    hp.cuts.push_back(0);
-    {
-        int c = 1;
-        int64_t cw = 0;
-        for (const AttnUnit& U : hp.units) {
-            const int64_t nb = hp.segs[U.seg].n_blk;
-            const int64_t tw = tile_weight(U.rt);
-            const int64_t uw = kUnitStartWeight + nb * tw;
-            while (c < C0) {
-                const int64_t target = (weight * c + C0 - 1) / C0;
-                if (target >= cw + uw) break;
-                const int64_t k = std::max<int64_t>(0, (target - cw - kUnitStartWeight + tw - 1) / tw);
-                const int64_t cut = U.tile_off + std::min<int64_t>(k, nb);
-                if (cut > hp.cuts.back() && cut < T) hp.cuts.push_back(cut);
-                ++c;
-            }
-            cw += uw;
-        }
-    }
-    hp.cuts.push_back(T);
-    const int C = (int)hp.cuts.size() - 1;
-    hp.cta_begin.resize(C + 1);
-    for (int i = 0; i <= C; ++i) hp.cta_begin[i] = (int32_t)hp.cuts[i];
-    hp.cta_unit.resize(C);
-    {
-        size_t u = 0;
-        for (int c = 0; c < C; ++c) {
-            while (u + 1 < hp.units.size() &&
-                   hp.units[u].tile_off + hp.segs[hp.units[u].seg].n_blk <= hp.cta_begin[c])
-                ++u;
-            hp.cta_unit[c] = (int32_t)u;
-        }
-    }
-    // chunks and partial rows per unit
+    hp.tiles = class_tiles[0] + class_tiles[1];
+    partition_class(hp, 0, hp.n_tc_units, class_tiles[0], weight[0], max_tc_ctas, kTcWeights, hp.tc_cta_begin,
+                    hp.tc_cta_unit);
+    partition_class(hp, hp.n_tc_units, (int32_t)hp.units.size(), class_tiles[1], weight[1], max_ctas, kSmallWeights,
+                    hp.cta_begin, hp.cta_unit);
+    // partial rows per unit
     size_t prow = 0;
-    {
-        int c = 0;
-        for (AttnUnit& U : hp.units) {
-            const int32_t last = U.tile_off + hp.segs[U.seg].n_blk - 1;
-            while (hp.cta_begin[c + 1] <= U.tile_off) ++c;
-            int cl = c;
-            while (hp.cta_begin[cl + 1] <= last) ++cl;
-            U.cfirst = c;
-            U.nchunks = cl - c + 1;
-            U.prow_base = (int32_t)prow;
-            prow += (size_t)U.nchunks * U.n_rows;
-        }
+    for (AttnUnit& U : hp.units) {
+        U.prow_base = (int32_t)prow;
+        prow += (size_t)U.nchunks * U.n_rows;
     }
     if (prow >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
     hp.partial_rows = prow;
-    // path of every queried branch: (segment, member index) pairs
+    // path of every queried branch: one entry per segment it reads
     hp.path_off.assign(n + 1, 0);
     for (const AttnSeg& S : hp.segs)
         for (int32_t k = 0; k < S.n_mem; ++k) hp.path_off[hp.members[S.mem_off + k].qi + 1]++;
@@ -849,7 +787,7 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
             hp.path[4 * e] = S.unit_base;
             hp.path[4 * e + 1] = S.ngroups;
             hp.path[4 * e + 2] = k * RM;
-            hp.path[4 * e + 3] = si;
+            hp.path[4 * e + 3] = S.group_rows;
         }
     }
     for (int32_t i = 0; i < n; ++i)
@@ -886,6 +824,130 @@ int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
     static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
     std::memcpy(out, &m, sizeof(m));
     return DENDRITE_OK;
+}
+
+// Byte layout of an uploaded plan: the sections of HostPlan one after the
+// other, each 16-byte aligned.  off[k] is the start of section k, off[kPlanSections]
+// the total size.
+constexpr int kPlanSections = 10;
+size_t plan_layout(const HostPlan& hp, size_t (&off)[kPlanSections + 1]) {
+    const size_t sz[kPlanSections] = {
+        hp.segs.size() * sizeof(AttnSeg),  hp.members.size() * sizeof(AttnMember),
+        hp.units.size() * sizeof(AttnUnit), hp.cta_begin.size() * 4,
+        hp.cta_unit.size() * 4,             hp.tc_cta_begin.size() * 4,
+        hp.tc_cta_unit.size() * 4,          hp.path_off.size() * 4,
+        hp.path.size() * 4,                 hp.rows.size() * sizeof(AttnRow)};
+    size_t b = 0;
+    for (int k = 0; k < kPlanSections; ++k) {
+        off[k] = b;
+        b = align16(b + sz[k]);
+    }
+    off[kPlanSections] = b;
+    return b;
+}
+
+void plan_pack(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], char* h) {
+    auto put = [&](int k, const void* src, size_t bytes) {
+        if (bytes) std::memcpy(h + off[k], src, bytes);
+    };
+    put(0, hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
+    put(1, hp.members.data(), hp.members.size() * sizeof(AttnMember));
+    put(2, hp.units.data(), hp.units.size() * sizeof(AttnUnit));
+    put(3, hp.cta_begin.data(), hp.cta_begin.size() * 4);
+    put(4, hp.cta_unit.data(), hp.cta_unit.size() * 4);
+    put(5, hp.tc_cta_begin.data(), hp.tc_cta_begin.size() * 4);
+    put(6, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
+    put(7, hp.path_off.data(), hp.path_off.size() * 4);
+    put(8, hp.path.data(), hp.path.size() * 4);
+    put(9, hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
+}
+
+AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], const char* d, int32_t n,
+                      int32_t q_len, int32_t nq, int32_t group) {
+    AttnPlanDev v{};
+    v.segs = reinterpret_cast<const AttnSeg*>(d + off[0]);
+    v.members = reinterpret_cast<const AttnMember*>(d + off[1]);
+    v.units = reinterpret_cast<const AttnUnit*>(d + off[2]);
+    v.cta_begin = reinterpret_cast<const int32_t*>(d + off[3]);
+    v.cta_unit = reinterpret_cast<const int32_t*>(d + off[4]);
+    v.tc_cta_begin = reinterpret_cast<const int32_t*>(d + off[5]);
+    v.tc_cta_unit = reinterpret_cast<const int32_t*>(d + off[6]);
+    v.path_off = reinterpret_cast<const int32_t*>(d + off[7]);
+    v.path = reinterpret_cast<const int32_t*>(d + off[8]);
+    v.rows = reinterpret_cast<const AttnRow*>(d + off[9]);
+    v.n_units = (int32_t)hp.units.size();
+    v.n_ctas = (int32_t)hp.cta_unit.size();
+    v.n_tc_units = hp.n_tc_units;
+    v.n_tc_ctas = (int32_t)hp.tc_cta_unit.size();
+    v.n_queried = n;
+    v.q_len = q_len;
+    v.n_q_heads = nq;
+    v.group = group;
+    return v;
+}
+
+// CTAs the tensor-core kernel may use on this pool (0: not used).
+int tc_ctas(const dendrite_pool* p) {
+    return (p->dtype == DENDRITE_BF16 && p->tc_ready && p->tc_min_rows >= 0) ? p->sm_count : 0;
+}
+
+// The partial kernels of one attention call (tensor-core class, then the
+// mma.sync or fp32 class), then the merge.  pdl_small: launch the mma.sync
+// kernel with programmatic stream serialisation.
+int launch_attention(dendrite_pool* p, const AttnArgs& a, cudaStream_t s, bool pdl_small) {
+    const bool bf16 = p->dtype == DENDRITE_BF16;
+    prof_begin(p, T_ATTN_TOTAL, s);
+    prof_begin(p, T_ATTN_PARTIAL, s);
+    CUtensorMap mk, mv;
+    std::memcpy(&mk, p->tmap_k, sizeof(mk));
+    std::memcpy(&mv, p->tmap_v, sizeof(mv));
+    if (a.plan.n_tc_ctas > 0) {
+        prof_begin(p, T_ATTN_TC, s);
+        DENDRITE_TRY(launch_attn_tc(mk, mv, a, a.plan.n_tc_ctas, s));
+        prof_end(p, T_ATTN_TC, s);
+    } else {
+        p->ev_recorded[T_ATTN_TC] = false;   // this call ran no tensor-core kernel
+    }
+    if (a.plan.n_ctas > 0) {
+        if (bf16) {
+            if (pdl_small)
+                DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk,
+                                         mv, a));
+            else
+                k_attn_partial_bf16<<<a.plan.n_ctas, THREADS, SMEM_BF16, s>>>(mk, mv, a);
+        } else {
+            DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(a.plan.n_ctas), dim3(128),
+                                     2 * BS * p->head_dim * sizeof(float), s, a));
+        }
+    }
+    prof_end(p, T_ATTN_PARTIAL, s);
+    prof_begin(p, T_ATTN_MERGE, s);
+    {
+        const int32_t n_out = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
+        const unsigned grid = (unsigned)((n_out + 7) / 8);
+        if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, a));
+        else DENDRITE_CUDA(launch_pdl(k_attn_merge<float>, dim3(grid), dim3(256), 0, s, a));
+    }
+    prof_end(p, T_ATTN_MERGE, s);
+    prof_end(p, T_ATTN_TOTAL, s);
+    DENDRITE_CUDA(cudaGetLastError());
+    return DENDRITE_OK;
+}
+
+AttnArgs attn_args(const dendrite_pool* p, const void* Q, void* out) {
+    AttnArgs a{};
+    a.Q = Q;
+    a.out = out;
+    a.table = p->d_table;
+    a.pool_k = static_cast<const float*>(p->d_k);
+    a.pool_v = static_cast<const float*>(p->d_v);
+    a.meta = p->d_meta;
+    a.bpb = p->bpb;
+    a.n_kv = p->n_kv;
+    a.head_dim = p->head_dim;
+    a.n_blocks = (int32_t)p->num_blocks;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
+    return a;
 }
 
 int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows) {
@@ -934,6 +996,7 @@ int attn_setup(dendrite_pool* p) {
         int occ = 0;
         DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_bf16, THREADS, SMEM_BF16));
         p->attn_ctas_per_sm = std::max(1, occ);
+        p->tc_ready = attn_tc_setup() == DENDRITE_OK;
     } else {
         const size_t sm = 2 * BS * p->head_dim * sizeof(float);
         int occ = 0;
@@ -973,7 +1036,6 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         if (std::adjacent_find(s.begin(), s.end()) != s.end()) return DENDRITE_EINVAL;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    const bool bf16 = p->dtype == DENDRITE_BF16;
     const int max_ctas = p->sm_count * p->attn_ctas_per_sm;
     PlanCache& pc = p->plan;
     const bool hit = pc.valid && pc.version == p->version && pc.q_len == q_len && pc.n_q_heads == n_q_heads &&
@@ -982,48 +1044,15 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         const auto t0 = std::chrono::steady_clock::now();
         static thread_local HostPlan hp;
         hp.clear();
-        DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, hp));
-        const int32_t C = (int32_t)hp.cta_unit.size();
-        size_t off[9];
-        size_t b = 0;
-        off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
-        off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
-        off[2] = b; b = align16(b + hp.units.size() * sizeof(AttnUnit));
-        off[3] = b; b = align16(b + hp.cta_begin.size() * 4);
-        off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
-        off[5] = b; b = align16(b + hp.path_off.size() * 4);
-        off[6] = b; b = align16(b + hp.path.size() * 4);
-        off[7] = b; b = align16(b + hp.rows.size() * sizeof(AttnRow));
-        off[8] = b;
+        DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp));
+        size_t off[kPlanSections + 1];
+        const size_t b = plan_layout(hp, off);
         DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
-        char* h = p->h_plan;
-        std::memcpy(h + off[0], hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
-        std::memcpy(h + off[1], hp.members.data(), hp.members.size() * sizeof(AttnMember));
-        std::memcpy(h + off[2], hp.units.data(), hp.units.size() * sizeof(AttnUnit));
-        std::memcpy(h + off[3], hp.cta_begin.data(), hp.cta_begin.size() * 4);
-        std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
-        std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
-        std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
-        std::memcpy(h + off[7], hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
-        DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, h, b, cudaMemcpyHostToDevice, s));
+        plan_pack(hp, off, p->h_plan);
+        DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, p->h_plan, b, cudaMemcpyHostToDevice, s));
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
-        char* d = p->d_plan;
-        pc.dev.segs = reinterpret_cast<const AttnSeg*>(d + off[0]);
-        pc.dev.members = reinterpret_cast<const AttnMember*>(d + off[1]);
-        pc.dev.units = reinterpret_cast<const AttnUnit*>(d + off[2]);
-        pc.dev.cta_begin = reinterpret_cast<const int32_t*>(d + off[3]);
-        pc.dev.cta_unit = reinterpret_cast<const int32_t*>(d + off[4]);
-        pc.dev.path_off = reinterpret_cast<const int32_t*>(d + off[5]);
-        pc.dev.path = reinterpret_cast<const int32_t*>(d + off[6]);
-        pc.dev.rows = reinterpret_cast<const AttnRow*>(d + off[7]);
-        pc.dev.n_units = (int32_t)hp.units.size();
-        pc.dev.n_ctas = C;
-        pc.dev.n_queried = n;
-        pc.dev.q_len = q_len;
-        pc.dev.n_q_heads = n_q_heads;
-        pc.dev.group = n_q_heads / p->n_kv;
-        pc.dev.max_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+        pc.dev = plan_view(hp, off, p->d_plan, n, q_len, n_q_heads, n_q_heads / p->n_kv);
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
         pc.version = p->version;
@@ -1032,55 +1061,21 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
         pc.branches.assign(branches, branches + n);
         pc.stats.n_segments = (int32_t)hp.segs.size();
         pc.stats.n_units = (int32_t)hp.units.size();
-        pc.stats.n_ctas = C;
+        pc.stats.n_ctas = pc.dev.n_ctas;
         pc.stats.n_partials = (int32_t)hp.partial_rows;
         pc.stats.tiles = hp.tiles;
         pc.stats.unique_tiles = hp.unique_tiles;
+        pc.stats.n_tc_units = hp.n_tc_units;
+        pc.stats.n_tc_ctas = pc.dev.n_tc_ctas;
         pc.stats.plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
     } else {
         pc.stats.plan_us = 0.0;
     }
-    AttnArgs a;
+    AttnArgs a = attn_args(p, Q, out);
     a.plan = pc.dev;
-    a.Q = Q;
-    a.out = out;
-    a.table = p->d_table;
-    a.pool_kv[0] = p->d_k;
-    a.pool_kv[1] = p->d_v;
-    a.pool_k = static_cast<const float*>(p->d_k);
-    a.pool_v = static_cast<const float*>(p->d_v);
     a.part_acc = p->d_partial;
     a.part_ml = reinterpret_cast<float2*>(p->d_partial + p->partial_rows_cap * p->head_dim);
-    a.meta = p->d_meta;
-    a.bpb = p->bpb;
-    a.n_kv = p->n_kv;
-    a.head_dim = p->head_dim;
-    a.n_blocks = (int32_t)p->num_blocks;
-    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
-    prof_begin(p, T_ATTN_TOTAL, s);
-    prof_begin(p, T_ATTN_PARTIAL, s);
-    if (bf16) {
-        CUtensorMap mk, mv;
-        std::memcpy(&mk, p->tmap_k, sizeof(mk));
-        std::memcpy(&mv, p->tmap_v, sizeof(mv));
-        k_attn_partial_bf16<<<pc.dev.n_ctas, THREADS, SMEM_BF16, s>>>(mk, mv, a);
-    } else {
-        DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(pc.dev.n_ctas), dim3(128),
-                                 2 * BS * p->head_dim * sizeof(float), s, a));
-    }
-    prof_end(p, T_ATTN_PARTIAL, s);
-    prof_begin(p, T_ATTN_MERGE, s);
-    {
-        const int32_t n_out = n * q_len * n_q_heads;
-        const unsigned grid = (unsigned)((n_out + 7) / 8);
-        if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, a));
-        else DENDRITE_CUDA(launch_pdl(k_attn_merge<float>, dim3(grid), dim3(256), 0, s, a));
-    }
-    prof_end(p, T_ATTN_MERGE, s);
-    prof_end(p, T_ATTN_TOTAL, s);
-    DENDRITE_CUDA(cudaGetLastError());
-    DENDRITE_CUDA(cudaGetLastError());
-    return DENDRITE_OK;
+    return launch_attention(p, a, s, false);
 }
 
 extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* out) {
@@ -1152,79 +1147,21 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     unsigned char* scratch = nullptr;
     DENDRITE_TRY(noalloc_scratch(p->device, &scratch));
     cudaStream_t s = (cudaStream_t)stream;
-    const bool bf16 = p->dtype == DENDRITE_BF16;
     static thread_local HostPlan hp;
     hp.clear();
-    DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, hp));
+    DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, tc_ctas(p), hp));
     // scratch layout: plan sections, then partial acc rows, then partial (m, l)
-    size_t off[9];
-    size_t b = 0;
-    off[0] = b; b = align16(b + hp.segs.size() * sizeof(AttnSeg));
-    off[1] = b; b = align16(b + hp.members.size() * sizeof(AttnMember));
-    off[2] = b; b = align16(b + hp.units.size() * sizeof(AttnUnit));
-    off[3] = b; b = align16(b + hp.cta_begin.size() * 4);
-    off[4] = b; b = align16(b + hp.cta_unit.size() * 4);
-    off[5] = b; b = align16(b + hp.path_off.size() * 4);
-    off[6] = b; b = align16(b + hp.path.size() * 4);
-    off[7] = b; b = align16(b + hp.rows.size() * sizeof(AttnRow));
+    size_t off[kPlanSections + 1];
+    const size_t b = plan_layout(hp, off);
     const size_t plan_bytes = (b + 255) & ~size_t(255);
     const size_t acc_bytes = hp.partial_rows * p->head_dim * sizeof(float);
     const size_t ml_bytes = hp.partial_rows * sizeof(float2);
     if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
-    unsigned char* h = g_noalloc_host;
-    std::memcpy(h + off[0], hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
-    std::memcpy(h + off[1], hp.members.data(), hp.members.size() * sizeof(AttnMember));
-    std::memcpy(h + off[2], hp.units.data(), hp.units.size() * sizeof(AttnUnit));
-    std::memcpy(h + off[3], hp.cta_begin.data(), hp.cta_begin.size() * 4);
-    std::memcpy(h + off[4], hp.cta_unit.data(), hp.cta_unit.size() * 4);
-    std::memcpy(h + off[5], hp.path_off.data(), hp.path_off.size() * 4);
-    std::memcpy(h + off[6], hp.path.data(), hp.path.size() * 4);
-    std::memcpy(h + off[7], hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
-    DENDRITE_CUDA(cudaMemcpyAsync(scratch, h, b, cudaMemcpyHostToDevice, s));
-    AttnArgs a;
-    a.plan.segs = reinterpret_cast<const AttnSeg*>(scratch + off[0]);
-    a.plan.members = reinterpret_cast<const AttnMember*>(scratch + off[1]);
-    a.plan.units = reinterpret_cast<const AttnUnit*>(scratch + off[2]);
-    a.plan.cta_begin = reinterpret_cast<const int32_t*>(scratch + off[3]);
-    a.plan.cta_unit = reinterpret_cast<const int32_t*>(scratch + off[4]);
-    a.plan.path_off = reinterpret_cast<const int32_t*>(scratch + off[5]);
-    a.plan.path = reinterpret_cast<const int32_t*>(scratch + off[6]);
-    a.plan.rows = reinterpret_cast<const AttnRow*>(scratch + off[7]);
-    a.plan.n_units = (int32_t)hp.units.size();
-    a.plan.n_ctas = (int32_t)hp.cta_unit.size();
-    a.plan.n_queried = n;
-    a.plan.q_len = q_len;
-    a.plan.n_q_heads = n_q_heads;
-    a.plan.group = n_q_heads / p->n_kv;
-    a.plan.max_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
-    a.plan.pad = 0;
-    a.Q = Q;
-    a.out = out;
-    a.table = p->d_table;
-    a.pool_kv[0] = p->d_k;
-    a.pool_kv[1] = p->d_v;
-    a.pool_k = static_cast<const float*>(p->d_k);
-    a.pool_v = static_cast<const float*>(p->d_v);
+    plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));
+    DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, b, cudaMemcpyHostToDevice, s));
+    AttnArgs a = attn_args(p, Q, out);
+    a.plan = plan_view(hp, off, reinterpret_cast<const char*>(scratch), n, q_len, n_q_heads, n_q_heads / p->n_kv);
     a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);
     a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
-    a.meta = p->d_meta;
-    a.bpb = p->bpb;
-    a.n_kv = p->n_kv;
-    a.head_dim = p->head_dim;
-    a.n_blocks = (int32_t)p->num_blocks;
-    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
-    if (bf16) {
-        CUtensorMap mk, mv;
-        std::memcpy(&mk, p->tmap_k, sizeof(mk));
-        std::memcpy(&mv, p->tmap_v, sizeof(mv));
-        DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
-    } else {
-        DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(a.plan.n_ctas), dim3(128),
-                                 2 * BS * p->head_dim * sizeof(float), s, a));
-    }
-    const int32_t n_out = n * q_len * n_q_heads;
-    const unsigned grid = (unsigned)((n_out + 7) / 8);
-    if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, a));
-    else DENDRITE_CUDA(launch_pdl(k_attn_merge<float>, dim3(grid), dim3(256), 0, s, a));
-    return DENDRITE_OK;
+    return launch_attention(p, a, s, true);
 }

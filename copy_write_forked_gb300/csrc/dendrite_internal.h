@@ -17,8 +17,10 @@ namespace dendrite {
 
 // ------------------------------------------------------------------ limits
 constexpr int kBlockSize = 16;        // tokens per block (= attention tile height)
-constexpr int kMaxUnitRowsBf16 = 64;  // rows per attention work unit (4 row tiles of 16)
+constexpr int kMaxUnitRowsBf16 = 64;  // rows per mma.sync attention unit (4 row tiles of 16)
 constexpr int kMaxUnitRowsF32 = 16;
+constexpr int kMaxUnitRowsTc = 256;   // rows per tcgen05 attention unit (2 row tiles of 128)
+constexpr int kTcMinRowsDefault = 64; // segments with more rows per kv head use the tcgen05 kernel
 constexpr int kAppendMetaThreads = 1024;
 constexpr int kFreeCollectThreads = 1024;
 
@@ -44,7 +46,7 @@ struct AttnSeg {
     int32_t n_mem;
     int32_t unit_base;
     int32_t ngroups;
-    int32_t pad;
+    int32_t group_rows; // rows per row group (kMaxUnitRowsTc for tensor-core segments)
 };
 
 // A queried branch as a segment member: its index in the query list and length.
@@ -64,9 +66,9 @@ struct AttnUnit {
     int32_t kv_head;
     int32_t row_lo;
     int32_t n_rows;     // 1..max rows per unit
-    int32_t rt;         // row tiles of 16 (1, 2 or 4)
-    int32_t tile_off;   // global index of the unit's first tile
-    int32_t cfirst;     // CTA holding the unit's first tile
+    int32_t rt;         // row tiles: of 16 rows (1, 2 or 4), of 128 rows in tc units (1 or 2)
+    int32_t tile_off;   // index of the unit's first tile within its class's tile list
+    int32_t cfirst;     // CTA (of its class's kernel) holding the unit's first tile
     int32_t nchunks;    // CTAs its tiles are split over (all non-empty)
     int32_t prow_base;  // first partial row; chunk k uses rows prow_base + k * n_rows ..
     int32_t table_row;  // branch handle whose table row holds the segment's block ids
@@ -89,19 +91,24 @@ struct AttnPlanDev {
     const AttnMember* members;
     const AttnUnit* units;
     const AttnRow* rows;
-    const int32_t* cta_begin;   // [n_ctas + 1] strictly increasing tile boundaries
-    const int32_t* cta_unit;    // [n_ctas] unit holding cta_begin[c]
-    const int32_t* path_off;    // [n_queried + 1] into path
-    const int32_t* path;        // per path entry: (first unit of the segment, row groups per kv head,
-                                //  first segment row of the member, segment index)
+    // Units [0, n_tc_units) run on the tcgen05 kernel, the rest on the
+    // mma.sync (or fp32) kernel; each class has its own tile numbering and
+    // its own CTA partition.
+    const int32_t* cta_begin;      // [n_ctas + 1] strictly increasing tile boundaries
+    const int32_t* cta_unit;       // [n_ctas] unit holding cta_begin[c]
+    const int32_t* tc_cta_begin;   // [n_tc_ctas + 1], same for the tc class
+    const int32_t* tc_cta_unit;    // [n_tc_ctas]
+    const int32_t* path_off;       // [n_queried + 1] into path
+    const int32_t* path;           // per path entry: (first unit of the segment, row groups per kv head,
+                                   //  first segment row of the member, rows per row group)
     int32_t n_units;
     int32_t n_ctas;
+    int32_t n_tc_units;
+    int32_t n_tc_ctas;
     int32_t n_queried;
     int32_t q_len;
     int32_t n_q_heads;
-    int32_t group;              // G = n_q_heads / n_kv
-    int32_t max_rows;           // rows per unit (row-group size)
-    int32_t pad;
+    int32_t group;                 // G = n_q_heads / n_kv
 };
 
 // ------------------------------------------------------- host bookkeeping
@@ -148,7 +155,7 @@ private:
 };
 
 enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_ATTN_MERGE, T_FREE,
-                  T_ATTN_TOTAL, T_COUNT };
+                  T_ATTN_TOTAL, T_ATTN_TC, T_COUNT };
 
 struct PlanCache {
     bool valid = false;
@@ -170,6 +177,7 @@ struct dendrite_pool {
     int device = 0;
     int sm_count = 0;
     int attn_ctas_per_sm = 1;
+    int32_t tc_min_rows = dendrite::kTcMinRowsDefault;   // < 0: tensor-core attention kernel off
 
     // device state
     void* d_k = nullptr;
@@ -187,6 +195,7 @@ struct dendrite_pool {
     alignas(64) unsigned char tmap_k[128];
     alignas(64) unsigned char tmap_v[128];
     bool tmaps_ok = false;
+    bool tc_ready = false;           // tcgen05 attention kernel configured for this device
 
     // attention workspace (grow-only)
     char* d_plan = nullptr;

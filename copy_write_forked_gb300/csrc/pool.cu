@@ -662,10 +662,11 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     }
     int32_t max_branches = 4096, bpb = 4096;
     if (opts) {
-        for (int i = 0; i < 6; ++i)
+        for (int i = 0; i < 5; ++i)
             if (opts->reserved[i]) return DENDRITE_EINVAL;
         if (opts->max_branches) max_branches = opts->max_branches;
         if (opts->max_blocks_per_branch) bpb = opts->max_blocks_per_branch;
+        if (opts->tc_min_rows < -1) return DENDRITE_EINVAL;
     }
     if (max_branches < 1 || bpb < 1 || (int64_t)max_branches * bpb > (int64_t)1 << 34) return DENDRITE_EINVAL;
 
@@ -678,6 +679,7 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     p->elt = dtype == DENDRITE_BF16 ? 2 : 4;
     p->max_branches = max_branches;
     p->bpb = bpb;
+    if (opts && opts->tc_min_rows) p->tc_min_rows = opts->tc_min_rows;
     int rc = DENDRITE_OK;
     auto fail = [&](int code) {
         dendrite_pool_destroy(p);
@@ -688,6 +690,11 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     const size_t pool_bytes = (size_t)num_blocks * n_kv_heads * block_size * head_dim * p->elt;
     if (cudaMalloc(&p->d_k, pool_bytes) != cudaSuccess || cudaMalloc(&p->d_v, pool_bytes) != cudaSuccess)
         return fail(cuda_err(cudaErrorMemoryAllocation));
+    // Slots past a branch's length are read by the attention tiles and given
+    // weight zero; they must hold finite values (0 x NaN is NaN).  Zero them
+    // once here; afterwards they only ever hold appended rows.
+    if (cudaMemset(p->d_k, 0, pool_bytes) != cudaSuccess || cudaMemset(p->d_v, 0, pool_bytes) != cudaSuccess)
+        return fail(cuda_err(cudaErrorUnknown));
     const size_t nb4 = (size_t)num_blocks * 4;
     if (cudaMalloc(&p->d_refcount, nb4) != cudaSuccess || cudaMalloc(&p->d_stack, nb4) != cudaSuccess ||
         cudaMalloc(&p->d_holders, nb4) != cudaSuccess || cudaMalloc(&p->d_last, nb4) != cudaSuccess ||

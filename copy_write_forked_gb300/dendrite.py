@@ -23,7 +23,8 @@ ERRORS = {
     -1: "EINVAL", -2: "ENOMEM", -3: "EBADHANDLE", -4: "ELIMIT", -5: "EDTYPE",
     -6: "ECUDA", -7: "ETIMEOUT", -8: "ECORRUPT",
 }
-TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total")
+TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total",
+                "attn_tc")
 FP32, BF16 = 0, 1
 
 _LIB = None
@@ -41,12 +42,14 @@ class DendriteError(RuntimeError):
 
 
 class _Opts(ctypes.Structure):
-    _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("reserved", _i32 * 6)]
+    _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("tc_min_rows", _i32),
+                ("reserved", _i32 * 5)]
 
 
 class _PlanStats(ctypes.Structure):
     _fields_ = [("n_segments", _i32), ("n_units", _i32), ("n_ctas", _i32), ("n_partials", _i32),
-                ("tiles", _i64), ("unique_tiles", _i64), ("plan_us", ctypes.c_double)]
+                ("tiles", _i64), ("unique_tiles", _i64), ("plan_us", ctypes.c_double), ("n_tc_units", _i32),
+                ("n_tc_ctas", _i32)]
 
 
 class _Segment(ctypes.Structure):
@@ -137,14 +140,14 @@ class Pool:
 
     def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
                  dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
-                 max_blocks_per_branch: int = 4096, device=None):
+                 max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0):
         if dtype not in _DT:
             raise DendriteError(-5, f"dtype {dtype}")
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
                                    torch.device(device).index or 0)
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
-        opts = _Opts(int(max_branches), int(max_blocks_per_branch))
+        opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows))
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
             _check(lib().dendrite_pool_create(self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim,

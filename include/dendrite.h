@@ -70,7 +70,11 @@ typedef struct dendrite_pool dendrite_pool;
 typedef struct dendrite_pool_opts {
     int32_t max_branches;          /* live handles at once (default 4096)                 */
     int32_t max_blocks_per_branch; /* block-table row length (default 4096 = 64K tokens)  */
-    int32_t reserved[6];           /* must be zero                                         */
+    int32_t tc_min_rows;           /* bf16 attention: sharing segments read by more than  *
+                                    * this many query rows per KV head run on the tcgen05 *
+                                    * (tensor memory) kernel, the others on the mma.sync  *
+                                    * kernel.  0 = default (64); -1 = never.               */
+    int32_t reserved[5];           /* must be zero                                         */
 } dendrite_pool_opts;
 
 /*
@@ -206,10 +210,11 @@ int dendrite_pool_info(dendrite_pool* pool, int64_t* num_blocks, int32_t* block_
  * the caller's stream.  dendrite_last_timings() synchronises on them and
  * returns the device milliseconds of the most recent call of each kind:
  *   ms[0] fork, ms[1] append metadata, ms[2] append copy/scatter,
- *   ms[3] attention partial kernel, ms[4] log-sum-exp merge kernel,
- *   ms[5] free (or truncate), ms[6] whole attention call (partial + merge).
+ *   ms[3] attention partial kernels, ms[4] log-sum-exp merge kernel,
+ *   ms[5] free (or truncate), ms[6] whole attention call (partial + merge),
+ *   ms[7] the tcgen05 partial kernel alone (part of ms[3]).
  * Entries with no recorded call are set to -1.                                */
-#define DENDRITE_N_TIMINGS 7
+#define DENDRITE_N_TIMINGS 8
 int dendrite_set_profiling(dendrite_pool* pool, int32_t enable);
 int dendrite_last_timings(dendrite_pool* pool, float* ms, int32_t n);
 
@@ -222,6 +227,8 @@ typedef struct dendrite_plan_stats {
     int64_t tiles;          /* (block, kv head) tiles streamed by the partial kernel */
     int64_t unique_tiles;   /* distinct (block, kv head) tiles among them            */
     double  plan_us;        /* host time spent building the plan (0 if cached)      */
+    int32_t n_tc_units;     /* units among n_units run on the tcgen05 kernel        */
+    int32_t n_tc_ctas;      /* CTAs of the tcgen05 kernel (not counted in n_ctas)   */
 } dendrite_plan_stats;
 int dendrite_last_plan_stats(dendrite_pool* pool, dendrite_plan_stats* out);
 
