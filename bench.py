@@ -239,9 +239,21 @@ def run_ours(args):
     kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
                             "attn_total")}
     plan_us = []
+
+    def step_profiled():
+        # A second L2 flush sits right before the attention call: the device
+        # works through it while the host builds the plan and launches, so the
+        # events around the attention kernels time the kernels, not the host.
+        kids = pool.fork_batch(roots, [Wd] * R)
+        br = [c for ks in kids for c in ks]
+        pool.append_kv(br, Kd, Vd)
+        flush_l2()
+        pool.tree_attn_decode(Q, br, out=out)
+        pool.free(br)
+
     for i in range(min(args.steps, 100)):
         flush_l2()
-        step()
+        step_profiled()
         tm = pool.last_timings()
         plan_us.append(pool.last_plan_stats()["plan_us"])
         for k in kern:
@@ -325,6 +337,100 @@ def run_ours(args):
     pool.close()
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_decode_layers(args):
+    """The beam step through all 32 layers of a Llama-3-8B-shaped model: one
+    fork, one append_begin (block decisions for every layer), then per layer
+    append_layer (that layer's rows) and tree attention over that layer (the
+    plan is built for layer 0 and reused), then one free.  Synthetic K/V per
+    layer, resident in HBM; L2 flushed before every step."""
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__ as g
+    g.build()
+    from copy_write_forked_gb300.dendrite import Pool
+    NL = 32
+    w = beam_workload(seed=rank)
+    R, P, Wd, Dv = (w.meta[k] for k in ("requests", "prefix", "width", "divergent"))
+    nq, nkv, d, bs = w.n_q_heads, w.n_kv_heads, w.head_dim, w.block_size
+    nblocks = R * (P // bs + 1) + R * Wd * (Dv // bs + 2) + 64
+    pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R * (Wd + 1) + 8,
+                max_blocks_per_branch=(P + Dv) // bs + 8, n_layers=NL)
+    roots = [pool.new_branch() for _ in range(R)]
+    prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
+    div_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == Dv)
+    pool.append_begin(roots, P)
+    for l in range(NL):
+        Kp, Vp = w.kv(prefill_idx, dev, layer=l)
+        pool.append_layer(l, Kp, Vp)
+        del Kp, Vp
+    Kd = [w.kv(div_idx, dev, layer=l) for l in range(NL)]
+    Q = w.q(dev)
+    outs = [torch.empty_like(Q) for _ in range(NL)]
+    stream = torch.cuda.current_stream()
+    flush_r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        kids = pool.fork_batch(roots, [Wd] * R)
+        br = [c for ks in kids for c in ks]
+        pool.append_begin(br, Dv)
+        for l in range(NL):
+            pool.append_layer(l, Kd[l][0], Kd[l][1])
+            pool.tree_attn_decode(Q, br, out=outs[l], layer=l)
+        pool.free(br)
+
+    for _ in range(args.warmup):
+        flush_r.max()
+        step()
+    pool.sync()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_r.max()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    # per-layer attention kernels, one synchronised step
+    pool.set_profiling(True)
+    kids = pool.fork_batch(roots, [Wd] * R)
+    br = [c for ks in kids for c in ks]
+    pool.append_begin(br, Dv)
+    part, plan_us = [], []
+    for l in range(NL):
+        pool.append_layer(l, Kd[l][0], Kd[l][1])
+        flush_r.max()
+        pool.tree_attn_decode(Q, br, out=outs[l], layer=l)
+        part.append(pool.last_timings()["attn_partial"])
+        plan_us.append(pool.last_plan_stats()["plan_us"])
+    pool.free(br)
+    pool.set_profiling(False)
+    pool.sync()
+    unique = w.unique_kv_bytes() + Q.numel() * Q.element_size()
+    peak, src = read_peaks()
+    pk = statistics.median(part)
+    n_queries = len(w.query)
+    line = {"metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
+            "workload": "decode32", "value": n_queries * NL / (step_ms / 1e3), "unit": "branch-layer-queries/s",
+            "ms_per_step": step_ms, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+            "data": "synthetic (Q/K/V ~ N(0,1), seeded per layer)",
+            "config": {"workload": "beam step (8 x 4096 prefix, fork 4, 256 divergent) through 32 layers: "
+                                   "fork, append_begin, 32 x (append_layer, tree attention), free",
+                       "l2": "flushed before every step"},
+            "per_layer_partial_kernel_ms": pk,
+            "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": unique / (pk / 1e3) / 1e9,
+                         "peak": peak, "peak_source": src, "unit": "GB/s",
+                         "frac": unique / (pk / 1e3) / 1e9 / peak, "algorithmic_bytes": unique},
+            "plan_us_layer0": plan_us[0], "plan_us_other_layers_max": max(plan_us[1:]),
+            "gpu_launches_per_step": 1 + 1 + NL * 3 + 1}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    pool.close()
+
 
 
 def other_workload(name):
@@ -543,11 +649,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
-    ap.add_argument("--workload", default="beam", choices=["beam", "mcts", "specverify", "stress"],
+    ap.add_argument("--workload", default="beam", choices=["beam", "mcts", "specverify", "stress", "decode32"],
                     help="beam = the full-path step (default JSON line); others time tree attention only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.impl == "ours" and args.workload == "decode32":
+        run_decode_layers(args)
+        return
     if args.impl == "ours" and args.workload != "beam":
         run_attention_only(args)
         return

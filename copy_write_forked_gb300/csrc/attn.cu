@@ -894,13 +894,15 @@ int tc_ctas(const dendrite_pool* p) {
 // The partial kernels of one attention call (tensor-core class, then the
 // mma.sync or fp32 class), then the merge.  pdl_small: launch the mma.sync
 // kernel with programmatic stream serialisation.
-int launch_attention(dendrite_pool* p, const AttnArgs& a, cudaStream_t s, bool pdl_small) {
+int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStream_t s, bool pdl_small) {
     const bool bf16 = p->dtype == DENDRITE_BF16;
     prof_begin(p, T_ATTN_TOTAL, s);
     prof_begin(p, T_ATTN_PARTIAL, s);
-    CUtensorMap mk, mv;
-    std::memcpy(&mk, p->tmap_k, sizeof(mk));
-    std::memcpy(&mv, p->tmap_v, sizeof(mv));
+    CUtensorMap mk{}, mv{};
+    if (bf16) {
+        std::memcpy(&mk, p->tmap_k[layer].bytes, sizeof(mk));
+        std::memcpy(&mv, p->tmap_v[layer].bytes, sizeof(mv));
+    }
     if (a.plan.n_tc_ctas > 0) {
         prof_begin(p, T_ATTN_TC, s);
         DENDRITE_TRY(launch_attn_tc(mk, mv, a, a.plan.n_tc_ctas, s));
@@ -934,13 +936,13 @@ int launch_attention(dendrite_pool* p, const AttnArgs& a, cudaStream_t s, bool p
     return DENDRITE_OK;
 }
 
-AttnArgs attn_args(const dendrite_pool* p, const void* Q, void* out) {
+AttnArgs attn_args(const dendrite_pool* p, int32_t layer, const void* Q, void* out) {
     AttnArgs a{};
     a.Q = Q;
     a.out = out;
     a.table = p->d_table;
-    a.pool_k = static_cast<const float*>(p->d_k);
-    a.pool_v = static_cast<const float*>(p->d_v);
+    a.pool_k = reinterpret_cast<const float*>(static_cast<const char*>(p->d_k) + (size_t)layer * p->layer_bytes);
+    a.pool_v = reinterpret_cast<const float*>(static_cast<const char*>(p->d_v) + (size_t)layer * p->layer_bytes);
     a.meta = p->d_meta;
     a.bpb = p->bpb;
     a.n_kv = p->n_kv;
@@ -988,8 +990,13 @@ namespace dendrite {
 
 int attn_setup(dendrite_pool* p) {
     if (p->dtype == DENDRITE_BF16) {
-        DENDRITE_TRY(encode_pool_map(p, p->d_k, p->tmap_k));
-        DENDRITE_TRY(encode_pool_map(p, p->d_v, p->tmap_v));
+        p->tmap_k.resize(p->n_layers);
+        p->tmap_v.resize(p->n_layers);
+        for (int32_t l = 0; l < p->n_layers; ++l) {
+            const size_t off = (size_t)l * p->layer_bytes;
+            DENDRITE_TRY(encode_pool_map(p, static_cast<char*>(p->d_k) + off, p->tmap_k[l].bytes));
+            DENDRITE_TRY(encode_pool_map(p, static_cast<char*>(p->d_v) + off, p->tmap_v[l].bytes));
+        }
         p->tmaps_ok = true;
         DENDRITE_CUDA(cudaFuncSetAttribute(k_attn_partial_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BF16));
@@ -1019,8 +1026,16 @@ void attn_teardown(dendrite_pool* p) {
 
 extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_t n_q_heads, int32_t q_len,
                                          const int32_t* branches, int32_t n, void* out, void* stream) {
+    return dendrite_tree_attn_decode_layer(p, 0, Q, n_q_heads, q_len, branches, n, out, stream);
+}
+
+extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, const void* Q, int32_t n_q_heads,
+                                               int32_t q_len, const int32_t* branches, int32_t n, void* out,
+                                               void* stream) {
     if (!p) return DENDRITE_EINVAL;
     if (p->poisoned) return p->poisoned;
+    if (layer < 0 || layer >= p->n_layers) return DENDRITE_EINVAL;
+    if (p->pending.active && !p->pending.layer_done[layer]) return DENDRITE_EINVAL;
     DENDRITE_CUDA(cudaSetDevice(p->device));
     if (!Q || !out || !branches || n <= 0 || q_len <= 0 || n_q_heads <= 0) return DENDRITE_EINVAL;
     if (n_q_heads % p->n_kv) return DENDRITE_EINVAL;
@@ -1071,11 +1086,11 @@ extern "C" int dendrite_tree_attn_decode(dendrite_pool* p, const void* Q, int32_
     } else {
         pc.stats.plan_us = 0.0;
     }
-    AttnArgs a = attn_args(p, Q, out);
+    AttnArgs a = attn_args(p, layer, Q, out);
     a.plan = pc.dev;
     a.part_acc = p->d_partial;
     a.part_ml = reinterpret_cast<float2*>(p->d_partial + p->partial_rows_cap * p->head_dim);
-    return launch_attention(p, a, s, false);
+    return launch_attention(p, layer, a, s, false);
 }
 
 extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* out) {
@@ -1131,6 +1146,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
                                                  void* stream) {
     if (!p) return DENDRITE_EINVAL;
     if (p->poisoned) return p->poisoned;
+    if (p->pending.active && !p->pending.layer_done[0]) return DENDRITE_EINVAL;
     DENDRITE_CUDA(cudaSetDevice(p->device));
     if (!Q || !out || !branches || n <= 0 || q_len <= 0 || n_q_heads <= 0) return DENDRITE_EINVAL;
     if (n_q_heads % p->n_kv) return DENDRITE_EINVAL;
@@ -1159,9 +1175,9 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
     plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));
     DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, b, cudaMemcpyHostToDevice, s));
-    AttnArgs a = attn_args(p, Q, out);
+    AttnArgs a = attn_args(p, 0, Q, out);
     a.plan = plan_view(hp, off, reinterpret_cast<const char*>(scratch), n, q_len, n_q_heads, n_q_heads / p->n_kv);
     a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);
     a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
-    return launch_attention(p, a, s, true);
+    return launch_attention(p, 0, a, s, true);
 }

@@ -157,6 +157,22 @@ private:
 enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_ATTN_MERGE, T_FREE,
                   T_ATTN_TOTAL, T_ATTN_TC, T_COUNT };
 
+// 128-byte opaque CUtensorMap storage.
+struct alignas(64) TensorMapBlob {
+    unsigned char bytes[128];
+};
+
+// A split append (dendrite_append_begin) whose rows are not all written yet.
+struct PendingAppend {
+    bool active = false;
+    std::vector<int32_t> branches;
+    std::vector<int32_t> lens;        // lengths before the append
+    int32_t n_new = 0;
+    int64_t touched = 0;              // (branch, block) pairs the rows land in
+    std::vector<uint8_t> layer_done;
+    int32_t n_done = 0;
+};
+
 struct PlanCache {
     bool valid = false;
     uint64_t version = 0;
@@ -191,9 +207,13 @@ struct dendrite_pool {
     int32_t* d_released = nullptr;   // [num_blocks] flags set by free phase A
     int32_t* d_call_i32 = nullptr;   // [4 * max_branches] per-call scratch (offsets, cow src/dst)
 
-    // tensor maps for the bf16 attention kernel (opaque 128-byte blobs)
-    alignas(64) unsigned char tmap_k[128];
-    alignas(64) unsigned char tmap_v[128];
+    // layers: layer l's K pool starts at d_k + l * layer_bytes (same for V)
+    int32_t n_layers = 1;
+    size_t layer_bytes = 0;
+
+    // tensor maps of every layer's K and V pool for the bf16 attention
+    // kernels (opaque 128-byte blobs)
+    std::vector<dendrite::TensorMapBlob> tmap_k, tmap_v;
     bool tmaps_ok = false;
     bool tc_ready = false;           // tcgen05 attention kernel configured for this device
 
@@ -216,6 +236,7 @@ struct dendrite_pool {
     int32_t poisoned = 0;
 
     dendrite::Staging staging;
+    dendrite::PendingAppend pending;
 
     // profiling
     bool profiling = false;

@@ -281,14 +281,20 @@ k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t 
 // of a copied-on-write tail (if any) and scatters the new rows into their
 // slots with 16-byte vector moves.  tile_pre[i] is the exclusive prefix of
 // touched blocks per branch (host computed; depends only on lengths).
+// blockIdx.y selects the layer: the input rows of layer y start y * in_layer
+// 16-byte words after Kin / Vin, its pool y * pool_layer words after Kp / Vp.
 template <typename A>
 __global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb, int32_t n_kv,
                               int32_t row_vec, int32_t n_blocks, const int32_t* __restrict__ table,
-                              const int32_t* __restrict__ call, const uint4* __restrict__ Kin,
-                              const uint4* __restrict__ Vin, uint4* __restrict__ Kp, uint4* __restrict__ Vp,
-                              const DevMeta* meta) {
+                              const int32_t* __restrict__ call, const uint4* __restrict__ Kin0,
+                              const uint4* __restrict__ Vin0, uint4* __restrict__ Kp0, uint4* __restrict__ Vp0,
+                              int64_t in_layer, int64_t pool_layer, const DevMeta* meta) {
     pdl_wait();
     if (meta->status) return;
+    const uint4* __restrict__ Kin = Kin0 + blockIdx.y * in_layer;
+    const uint4* __restrict__ Vin = Vin0 + blockIdx.y * in_layer;
+    uint4* __restrict__ Kp = Kp0 + blockIdx.y * pool_layer;
+    uint4* __restrict__ Vp = Vp0 + blockIdx.y * pool_layer;
     // args: branch[n], len[n], tile prefix[n]
     const int32_t* cow_src = call + n;
     const int64_t tile = blockIdx.x;
@@ -643,6 +649,93 @@ int launch_fork_param(dendrite_pool* p, const std::vector<int32_t>& child, const
 
 }  // namespace
 
+namespace {
+
+// Host checks of an append: live, distinct branches and table capacity.
+// touched: the (branch, block) pairs the new rows land in.
+int append_check(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t n_new, int64_t* touched) {
+    DENDRITE_TRY(check_unique_live(p, branches, n));
+    const int32_t bs = p->block_size;
+    int64_t t = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t L = p->br[branches[i]].len;
+        if (L + n_new > INT32_MAX / 2) return DENDRITE_ELIMIT;
+        if ((L + n_new + bs - 1) / bs > p->bpb) return DENDRITE_ELIMIT;
+        t += (L + n_new - 1) / bs - L / bs + 1;
+    }
+    if (t * p->n_kv > INT32_MAX) return DENDRITE_ELIMIT;
+    *touched = t;
+    return DENDRITE_OK;
+}
+
+// Launches the metadata kernel (meta) and/or the copy kernel (copy) of an
+// append whose branches had lengths lens[] before it.  The copy writes layers
+// [layer0, layer0 + n_layers_in) from K/V (layer y's rows in_layer 16-byte
+// words after layer y - 1's).
+int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens, int32_t n, int32_t n_new,
+                  int64_t touched, bool copy, const void* K, const void* V, int32_t layer0, int32_t n_layers_in,
+                  int64_t in_layer, cudaStream_t s, bool meta = true) {
+    const int32_t bs = p->block_size;
+    // args: branch[n], len[n], tile prefix[n]
+    constexpr int CAP = 768;
+    const int32_t row_vec = p->head_dim * p->elt / 16;
+    const unsigned grid = (unsigned)(touched * p->n_kv);
+    const int64_t pool_layer = (int64_t)(p->layer_bytes / 16);
+    auto fill = [&](int32_t* a) {
+        int32_t acc = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int32_t L = lens[i];
+            a[i] = branches[i];
+            a[n + i] = L;
+            a[2 * n + i] = acc;
+            acc += (L + n_new - 1) / bs - L / bs + 1;
+        }
+    };
+    auto launch = [&](auto args) -> int {
+        if (meta) {
+            prof_begin(p, T_APPEND_META, s);
+            DENDRITE_CUDA(launch_pdl(k_append_meta<decltype(args)>, dim3(1), dim3(kAppendMetaThreads), 0, s, args,
+                                     n, n_new, bs, p->bpb, (int32_t)p->num_blocks, p->d_table, p->d_refcount,
+                                     p->d_stack, p->d_holders, p->d_last, p->d_call_i32, p->d_meta));
+            prof_end(p, T_APPEND_META, s);
+        }
+        if (copy) {
+            prof_begin(p, T_APPEND_COPY, s);
+            uint4* kp = reinterpret_cast<uint4*>(static_cast<char*>(p->d_k) + (size_t)layer0 * p->layer_bytes);
+            uint4* vp = reinterpret_cast<uint4*>(static_cast<char*>(p->d_v) + (size_t)layer0 * p->layer_bytes);
+            DENDRITE_CUDA(launch_pdl(k_append_copy<decltype(args)>, dim3(grid, (unsigned)n_layers_in), dim3(128), 0,
+                                     s, args, n, n_new, bs, p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks,
+                                     (const int32_t*)p->d_table, (const int32_t*)p->d_call_i32, (const uint4*)K,
+                                     (const uint4*)V, kp, vp, in_layer, pool_layer, (const DevMeta*)p->d_meta));
+            prof_end(p, T_APPEND_COPY, s);
+        }
+        return DENDRITE_OK;
+    };
+    if (3 * n <= CAP) {
+        ParamArgs<CAP> a;
+        fill(a.v);
+        return launch(a);
+    }
+    char *h, *d;
+    const size_t bytes = (size_t)n * 12;
+    DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
+    fill((int32_t*)h);
+    DENDRITE_TRY(p->staging.upload(s, h, bytes));
+    DENDRITE_TRY(launch(GlobalArgs{(const int32_t*)d}));
+    return p->staging.release(s);
+}
+
+void append_commit_lengths(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t n_new) {
+    for (int32_t i = 0; i < n; ++i) {
+        Branch& b = p->br[branches[i]];
+        b.len += n_new;
+        p->nodes[b.node].len = b.len;
+    }
+    p->version++;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* dendrite_version(void) { return "dendrite-gb300 0.1.0 (sm_103a)"; }
@@ -662,11 +755,12 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     }
     int32_t max_branches = 4096, bpb = 4096;
     if (opts) {
-        for (int i = 0; i < 5; ++i)
-            if (opts->reserved[i]) return DENDRITE_EINVAL;
+        for (int32_t r : opts->reserved)
+            if (r) return DENDRITE_EINVAL;
         if (opts->max_branches) max_branches = opts->max_branches;
         if (opts->max_blocks_per_branch) bpb = opts->max_blocks_per_branch;
         if (opts->tc_min_rows < -1) return DENDRITE_EINVAL;
+        if (opts->n_layers < 0 || opts->n_layers > 1024) return DENDRITE_EINVAL;
     }
     if (max_branches < 1 || bpb < 1 || (int64_t)max_branches * bpb > (int64_t)1 << 34) return DENDRITE_EINVAL;
 
@@ -680,6 +774,7 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     p->max_branches = max_branches;
     p->bpb = bpb;
     if (opts && opts->tc_min_rows) p->tc_min_rows = opts->tc_min_rows;
+    if (opts && opts->n_layers) p->n_layers = opts->n_layers;
     int rc = DENDRITE_OK;
     auto fail = [&](int code) {
         dendrite_pool_destroy(p);
@@ -687,7 +782,8 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     };
     if (cudaGetDevice(&p->device) != cudaSuccess) return fail(cuda_err(cudaErrorNoDevice));
     cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device);
-    const size_t pool_bytes = (size_t)num_blocks * n_kv_heads * block_size * head_dim * p->elt;
+    p->layer_bytes = (size_t)num_blocks * n_kv_heads * block_size * head_dim * p->elt;
+    const size_t pool_bytes = p->layer_bytes * p->n_layers;
     if (cudaMalloc(&p->d_k, pool_bytes) != cudaSuccess || cudaMalloc(&p->d_v, pool_bytes) != cudaSuccess)
         return fail(cuda_err(cudaErrorMemoryAllocation));
     // Slots past a branch's length are read by the attention tiles and given
@@ -823,68 +919,61 @@ int dendrite_fork(dendrite_pool* p, int32_t parent, int32_t n_children, int32_t*
 int dendrite_append_kv(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t n_new, const void* K,
                        const void* V, void* stream) {
     DENDRITE_TRY(prelude(p));
+    if (p->pending.active) return DENDRITE_EINVAL;
     if (n < 0 || n_new < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
     if (n == 0 || n_new == 0) return DENDRITE_OK;
     if (!K || !V) return DENDRITE_EINVAL;
     if (((uintptr_t)K | (uintptr_t)V) & 15) return DENDRITE_EINVAL;
-    DENDRITE_TRY(check_unique_live(p, branches, n));
-    const int32_t bs = p->block_size;
     int64_t touched = 0;
-    for (int32_t i = 0; i < n; ++i) {
-        const int64_t L = p->br[branches[i]].len;
-        if (L + n_new > INT32_MAX / 2) return DENDRITE_ELIMIT;
-        if ((L + n_new + bs - 1) / bs > p->bpb) return DENDRITE_ELIMIT;
-        touched += (L + n_new - 1) / bs - L / bs + 1;
-    }
-    if (touched * p->n_kv > INT32_MAX) return DENDRITE_ELIMIT;
+    DENDRITE_TRY(append_check(p, branches, n, n_new, &touched));
     cudaStream_t s = (cudaStream_t)stream;
-    // args: branch[n], len[n], tile prefix[n]
-    constexpr int CAP = 768;
-    const int32_t row_vec = p->head_dim * p->elt / 16;
-    const unsigned grid = (unsigned)(touched * p->n_kv);
-    auto fill = [&](int32_t* a) {
-        int32_t acc = 0;
-        for (int32_t i = 0; i < n; ++i) {
-            const int32_t L = p->br[branches[i]].len;
-            a[i] = branches[i];
-            a[n + i] = L;
-            a[2 * n + i] = acc;
-            acc += (L + n_new - 1) / bs - L / bs + 1;
-        }
-    };
-    auto launch = [&](auto args) -> int {
-        prof_begin(p, T_APPEND_META, s);
-        DENDRITE_CUDA(launch_pdl(k_append_meta<decltype(args)>, dim3(1), dim3(kAppendMetaThreads), 0, s, args, n,
-                                 n_new, bs, p->bpb, (int32_t)p->num_blocks, p->d_table, p->d_refcount, p->d_stack,
-                                 p->d_holders, p->d_last, p->d_call_i32, p->d_meta));
-        prof_end(p, T_APPEND_META, s);
-        prof_begin(p, T_APPEND_COPY, s);
-        DENDRITE_CUDA(launch_pdl(k_append_copy<decltype(args)>, dim3(grid), dim3(128), 0, s, args, n, n_new, bs,
-                                 p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks, (const int32_t*)p->d_table,
-                                 (const int32_t*)p->d_call_i32, (const uint4*)K, (const uint4*)V, (uint4*)p->d_k,
-                                 (uint4*)p->d_v, (const DevMeta*)p->d_meta));
-        prof_end(p, T_APPEND_COPY, s);
-        return DENDRITE_OK;
-    };
-    if (3 * n <= CAP) {
-        ParamArgs<CAP> a;
-        fill(a.v);
-        DENDRITE_TRY(launch(a));
-    } else {
-        char *h, *d;
-        const size_t bytes = (size_t)n * 12;
-        DENDRITE_TRY(p->staging.reserve(bytes, &h, &d));
-        fill((int32_t*)h);
-        DENDRITE_TRY(p->staging.upload(s, h, bytes));
-        DENDRITE_TRY(launch(GlobalArgs{(const int32_t*)d}));
-        DENDRITE_TRY(p->staging.release(s));
-    }
-    for (int32_t i = 0; i < n; ++i) {
-        Branch& b = p->br[branches[i]];
-        b.len += n_new;
-        p->nodes[b.node].len = b.len;
-    }
-    p->version++;
+    std::vector<int32_t> lens(n);
+    for (int32_t i = 0; i < n; ++i) lens[i] = p->br[branches[i]].len;
+    const int64_t in_layer = (int64_t)n * n_new * p->n_kv * p->head_dim * p->elt / 16;
+    DENDRITE_TRY(append_launch(p, branches, lens.data(), n, n_new, touched, true, K, V, 0, p->n_layers, in_layer, s));
+    append_commit_lengths(p, branches, n, n_new);
+    return DENDRITE_OK;
+}
+
+int dendrite_append_begin(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t n_new, void* stream) {
+    DENDRITE_TRY(prelude(p));
+    if (p->pending.active) return DENDRITE_EINVAL;
+    if (n < 0 || n_new < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
+    if (n == 0 || n_new == 0) return DENDRITE_OK;
+    int64_t touched = 0;
+    DENDRITE_TRY(append_check(p, branches, n, n_new, &touched));
+    cudaStream_t s = (cudaStream_t)stream;
+    PendingAppend& pa = p->pending;
+    pa.branches.assign(branches, branches + n);
+    pa.lens.resize(n);
+    for (int32_t i = 0; i < n; ++i) pa.lens[i] = p->br[branches[i]].len;
+    DENDRITE_TRY(append_launch(p, branches, pa.lens.data(), n, n_new, touched, false, nullptr, nullptr, 0, 0, 0, s));
+    pa.n_new = n_new;
+    pa.touched = touched;
+    pa.layer_done.assign(p->n_layers, 0);
+    pa.n_done = 0;
+    pa.active = true;
+    append_commit_lengths(p, branches, n, n_new);
+    return DENDRITE_OK;
+}
+
+int dendrite_append_layer(dendrite_pool* p, int32_t layer, const void* K, const void* V, void* stream) {
+    DENDRITE_TRY(prelude(p));
+    PendingAppend& pa = p->pending;
+    if (!pa.active || layer < 0 || layer >= p->n_layers || pa.layer_done[layer]) return DENDRITE_EINVAL;
+    if (!K || !V || (((uintptr_t)K | (uintptr_t)V) & 15)) return DENDRITE_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int32_t n = (int32_t)pa.branches.size();
+    DENDRITE_TRY(append_launch(p, pa.branches.data(), pa.lens.data(), n, pa.n_new, pa.touched, true, K, V, layer, 1,
+                               0, s, /*meta=*/false));
+    pa.layer_done[layer] = 1;
+    if (++pa.n_done == p->n_layers) pa.active = false;
+    return DENDRITE_OK;
+}
+
+int dendrite_pool_layers(dendrite_pool* p, int32_t* n_layers) {
+    if (!p || !n_layers) return DENDRITE_EINVAL;
+    *n_layers = p->n_layers;
     return DENDRITE_OK;
 }
 
@@ -936,6 +1025,7 @@ extern "C" {
 
 int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* stream) {
     DENDRITE_TRY(prelude(p));
+    if (p->pending.active) return DENDRITE_EINVAL;
     if (n < 0 || (n > 0 && !branches)) return DENDRITE_EINVAL;
     if (n == 0) return DENDRITE_OK;
     DENDRITE_TRY(check_unique_live(p, branches, n));
@@ -963,6 +1053,7 @@ int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* st
 int dendrite_truncate(dendrite_pool* p, const int32_t* branches, const int32_t* new_lens, int32_t n,
                       void* stream) {
     DENDRITE_TRY(prelude(p));
+    if (p->pending.active) return DENDRITE_EINVAL;
     if (n < 0 || (n > 0 && (!branches || !new_lens))) return DENDRITE_EINVAL;
     if (n == 0) return DENDRITE_OK;
     DENDRITE_TRY(check_unique_live(p, branches, n));
@@ -1047,14 +1138,21 @@ int dendrite_read_free_stack(dendrite_pool* p, int32_t* out, int32_t* top_out, v
     return DENDRITE_OK;
 }
 
-int dendrite_read_block(dendrite_pool* p, int32_t block, void* k_out, void* v_out, void* stream) {
+int dendrite_read_block_layer(dendrite_pool* p, int32_t layer, int32_t block, void* k_out, void* v_out,
+                              void* stream) {
     if (!p || !k_out || !v_out || block < 0 || block >= p->num_blocks) return DENDRITE_EINVAL;
+    if (layer < 0 || layer >= p->n_layers) return DENDRITE_EINVAL;
     DENDRITE_CUDA(cudaSetDevice(p->device));
     DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
     const size_t bytes = (size_t)p->n_kv * p->block_size * p->head_dim * p->elt;
-    DENDRITE_CUDA(cudaMemcpy(k_out, (char*)p->d_k + bytes * block, bytes, cudaMemcpyDeviceToHost));
-    DENDRITE_CUDA(cudaMemcpy(v_out, (char*)p->d_v + bytes * block, bytes, cudaMemcpyDeviceToHost));
+    const size_t off = (size_t)layer * p->layer_bytes + bytes * block;
+    DENDRITE_CUDA(cudaMemcpy(k_out, (char*)p->d_k + off, bytes, cudaMemcpyDeviceToHost));
+    DENDRITE_CUDA(cudaMemcpy(v_out, (char*)p->d_v + off, bytes, cudaMemcpyDeviceToHost));
     return DENDRITE_OK;
+}
+
+int dendrite_read_block(dendrite_pool* p, int32_t block, void* k_out, void* v_out, void* stream) {
+    return dendrite_read_block_layer(p, 0, block, k_out, v_out, stream);
 }
 
 int dendrite_pool_info(dendrite_pool* p, int64_t* num_blocks, int32_t* block_size, int32_t* n_kv_heads,

@@ -43,7 +43,7 @@ class DendriteError(RuntimeError):
 
 class _Opts(ctypes.Structure):
     _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("tc_min_rows", _i32),
-                ("reserved", _i32 * 5)]
+                ("n_layers", _i32), ("reserved", _i32 * 4)]
 
 
 class _PlanStats(ctypes.Structure):
@@ -64,6 +64,11 @@ _SIGS = {
     "dendrite_fork": [_p, _i32, _i32, _pi32, _p],
     "dendrite_fork_batch": [_p, _pi32, _pi32, _i32, _pi32, _p],
     "dendrite_append_kv": [_p, _pi32, _i32, _i32, _p, _p, _p],
+    "dendrite_append_begin": [_p, _pi32, _i32, _i32, _p],
+    "dendrite_append_layer": [_p, _i32, _p, _p, _p],
+    "dendrite_tree_attn_decode_layer": [_p, _i32, _p, _i32, _i32, _pi32, _i32, _p, _p],
+    "dendrite_read_block_layer": [_p, _i32, _i32, _p, _p, _p],
+    "dendrite_pool_layers": [_p, _pi32],
     "dendrite_tree_attn_decode": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_tree_attn_decode_noalloc": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_free": [_p, _pi32, _i32, _p],
@@ -140,14 +145,15 @@ class Pool:
 
     def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
                  dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
-                 max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0):
+                 max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0, n_layers: int = 1):
         if dtype not in _DT:
             raise DendriteError(-5, f"dtype {dtype}")
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
                                    torch.device(device).index or 0)
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
-        opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows))
+        opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows), int(n_layers))
+        self.n_layers = int(n_layers)
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
             _check(lib().dendrite_pool_create(self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim,
@@ -203,19 +209,38 @@ class Pool:
             raise DendriteError(-1, f"{name} must be a contiguous {self.dtype} CUDA tensor")
 
     def append_kv(self, branches: Sequence[int], K: torch.Tensor, V: torch.Tensor, stream=None) -> None:
-        """K, V: ``[n_branches][n_new][n_kv_heads][head_dim]``."""
+        """K, V: ``[n_branches][n_new][n_kv_heads][head_dim]``; for a pool of
+        several layers ``[n_layers][n_branches][n_new][n_kv_heads][head_dim]``."""
         self._check_tensor(K, "K")
         self._check_tensor(V, "V")
         nb = len(branches)
-        if K.shape != V.shape or K.dim() != 4 or K.shape[0] != nb or K.shape[2] != self.n_kv_heads \
-                or K.shape[3] != self.head_dim:
+        want = 4 if self.n_layers == 1 else 5
+        if K.shape != V.shape or K.dim() != want or (want == 5 and K.shape[0] != self.n_layers):
+            raise DendriteError(-1, f"K/V shape {tuple(K.shape)}")
+        k4 = K.shape[-4:]
+        if k4[0] != nb or k4[2] != self.n_kv_heads or k4[3] != self.head_dim:
             raise DendriteError(-1, f"K/V shape {tuple(K.shape)}")
         ba = _arr(branches)
-        _check(lib().dendrite_append_kv(self._h, _ptr(ba), nb, K.shape[1], K.data_ptr(), V.data_ptr(),
+        _check(lib().dendrite_append_kv(self._h, _ptr(ba), nb, k4[1], K.data_ptr(), V.data_ptr(),
                                         _stream_ptr(stream, self._dev)), "append_kv")
 
+    def append_begin(self, branches: Sequence[int], n_new: int, stream=None) -> None:
+        """Block decisions and new lengths of an append, for every layer; rows follow per layer."""
+        ba = _arr(branches)
+        _check(lib().dendrite_append_begin(self._h, _ptr(ba), len(branches), int(n_new),
+                                           _stream_ptr(stream, self._dev)), "append_begin")
+
+    def append_layer(self, layer: int, K: torch.Tensor, V: torch.Tensor, stream=None) -> None:
+        """Rows of the pending append for one layer: K, V ``[n_branches][n_new][n_kv_heads][head_dim]``."""
+        self._check_tensor(K, "K")
+        self._check_tensor(V, "V")
+        if K.shape != V.shape or K.dim() != 4 or K.shape[2] != self.n_kv_heads or K.shape[3] != self.head_dim:
+            raise DendriteError(-1, f"K/V shape {tuple(K.shape)}")
+        _check(lib().dendrite_append_layer(self._h, int(layer), K.data_ptr(), V.data_ptr(),
+                                           _stream_ptr(stream, self._dev)), "append_layer")
+
     def tree_attn_decode(self, Q: torch.Tensor, branches: Sequence[int], out: Optional[torch.Tensor] = None,
-                         stream=None) -> torch.Tensor:
+                         stream=None, layer: int = 0) -> torch.Tensor:
         """Q: ``[n_branches][q_len][n_q_heads][head_dim]``; returns out of the same shape."""
         self._check_tensor(Q, "Q")
         if Q.dim() != 4 or Q.shape[0] != len(branches) or Q.shape[3] != self.head_dim:
@@ -226,8 +251,9 @@ class Pool:
         if out.shape != Q.shape:
             raise DendriteError(-1, "out shape")
         ba = _arr(branches)
-        _check(lib().dendrite_tree_attn_decode(self._h, Q.data_ptr(), Q.shape[2], Q.shape[1], _ptr(ba),
-                                               len(branches), out.data_ptr(), _stream_ptr(stream, self._dev)),
+        _check(lib().dendrite_tree_attn_decode_layer(self._h, int(layer), Q.data_ptr(), Q.shape[2], Q.shape[1],
+                                                     _ptr(ba), len(branches), out.data_ptr(),
+                                                     _stream_ptr(stream, self._dev)),
                "tree_attn_decode")
         return out
 
@@ -295,12 +321,12 @@ class Pool:
                "read_free_stack")
         return list(buf[:top.value])
 
-    def read_block(self, blk: int, stream=None):
+    def read_block(self, blk: int, stream=None, layer: int = 0):
         shape = (self.n_kv_heads, self.block_size, self.head_dim)
         k = torch.empty(shape, dtype=self.dtype)
         v = torch.empty(shape, dtype=self.dtype)
-        _check(lib().dendrite_read_block(self._h, int(blk), k.data_ptr(), v.data_ptr(),
-                                         _stream_ptr(stream, self._dev)), "read_block")
+        _check(lib().dendrite_read_block_layer(self._h, int(layer), int(blk), k.data_ptr(), v.data_ptr(),
+                                               _stream_ptr(stream, self._dev)), "read_block")
         return k, v
 
     # --------------------------------------------------------- profiling

@@ -11,8 +11,14 @@ import torch
 from .dendrite import Pool
 
 
-def run_script(pool: Pool, w, device="cuda", stop: Optional[int] = None, stream=None) -> Dict[int, int]:
+def run_script(pool: Pool, w, device="cuda", stop: Optional[int] = None, stream=None,
+               split_layers: bool = False, layer_order=None) -> Dict[int, int]:
+    """Replays ``w`` on ``pool``.  On a pool of several layers every append
+    carries all layers: in one call, or with ``split_layers`` as
+    ``append_begin`` followed by one ``append_layer`` per layer (in
+    ``layer_order``, default ascending)."""
     h: Dict[int, int] = {}
+    nl = getattr(pool, "n_layers", 1)
     for idx, op in enumerate(w.ops[:stop]):
         if op.kind == "new":
             h[op.branches[0]] = pool.new_branch()
@@ -24,8 +30,18 @@ def run_script(pool: Pool, w, device="cuda", stop: Optional[int] = None, stream=
         elif op.kind == "append":
             if op.n_new == 0:
                 continue
-            K, V = w.kv(idx, device)
-            pool.append_kv([h[b] for b in op.branches], K, V, stream=stream)
+            br = [h[b] for b in op.branches]
+            if split_layers:
+                pool.append_begin(br, op.n_new, stream=stream)
+                for l in (layer_order if layer_order is not None else range(nl)):
+                    K, V = w.kv(idx, device, layer=l)
+                    pool.append_layer(l, K, V, stream=stream)
+            elif nl == 1:
+                K, V = w.kv(idx, device)
+                pool.append_kv(br, K, V, stream=stream)
+            else:
+                K, V = w.kv_layers(idx, nl, device)
+                pool.append_kv(br, K, V, stream=stream)
         elif op.kind == "free":
             pool.free([h[b] for b in op.branches], stream=stream)
             for b in op.branches:

@@ -73,27 +73,35 @@ class Workload:
     meta: Dict[str, object] = field(default_factory=dict)
 
     # ---------------------------------------------------------------- values
-    def kv(self, op_index: int, device="cpu") -> Tuple[torch.Tensor, torch.Tensor]:
+    def kv(self, op_index: int, device="cpu", layer: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
         """K, V for append op ``op_index``: ``[n_branches][n_new][n_kv][d]``.
 
         Each branch's slice is drawn from its own generator, so any slice can
-        be regenerated alone (:meth:`kv_one`)."""
+        be regenerated alone (:meth:`kv_one`).  ``layer`` selects the model
+        layer (each layer draws its own values)."""
         op = self.ops[op_index]
         assert op.kind == "append"
         nb = len(op.branches)
         K = torch.empty((nb, op.n_new, self.n_kv_heads, self.head_dim), dtype=self.dtype, device=device)
         V = torch.empty_like(K)
         for i in range(nb):
-            k, v = self.kv_one(op_index, i, device)
+            k, v = self.kv_one(op_index, i, device, layer)
             K[i].copy_(k)
             V[i].copy_(v)
         return K, V
 
-    def kv_one(self, op_index: int, pos: int, device="cpu") -> Tuple[torch.Tensor, torch.Tensor]:
+    def kv_layers(self, op_index: int, n_layers: int, device="cpu") -> Tuple[torch.Tensor, torch.Tensor]:
+        """K, V of every layer: ``[n_layers][n_branches][n_new][n_kv][d]``."""
+        kv = [self.kv(op_index, device, l) for l in range(n_layers)]
+        return torch.stack([k for k, _ in kv]), torch.stack([v for _, v in kv])
+
+    def kv_one(self, op_index: int, pos: int, device="cpu", layer: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
         """K, V slice ``[n_new][n_kv][d]`` of the ``pos``-th branch of an append op."""
         op = self.ops[op_index]
         g = torch.Generator(device=device)
-        g.manual_seed(seed_of(self.seed, "kv", op_index, pos))
+        # layer 0 keeps the single-layer seed, so one-layer runs are unchanged
+        g.manual_seed(seed_of(self.seed, "kv", op_index, pos) if layer == 0 else
+                      seed_of(self.seed, "kv", op_index, pos, "layer", layer))
         x = torch.randn((2, op.n_new, self.n_kv_heads, self.head_dim), generator=g,
                         device=device, dtype=torch.float32)
         x = x.to(self.dtype)

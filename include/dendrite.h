@@ -74,7 +74,10 @@ typedef struct dendrite_pool_opts {
                                     * this many query rows per KV head run on the tcgen05 *
                                     * (tensor memory) kernel, the others on the mma.sync  *
                                     * kernel.  0 = default (64); -1 = never.               */
-    int32_t reserved[5];           /* must be zero                                         */
+    int32_t n_layers;              /* model layers held (0 = 1): every layer has its own  *
+                                    * K and V pools; block ids, tables, refcounts and the *
+                                    * free stack are shared by all layers.                */
+    int32_t reserved[4];           /* must be zero                                         */
 } dendrite_pool_opts;
 
 /*
@@ -84,7 +87,7 @@ typedef struct dendrite_pool_opts {
  *   n_kv_heads  KV heads per token (1..64).
  *   head_dim    bf16: 128.  fp32: a multiple of 32, at most 256.
  *   dtype       DENDRITE_FP32 or DENDRITE_BF16.
- * Device layout: K and V pools are [num_blocks][n_kv_heads][block_size][head_dim]
+ * Device layout: K and V pools are [n_layers][num_blocks][n_kv_heads][block_size][head_dim]
  * (one (block, head) tile is contiguous); refcount int32[num_blocks]; the free
  * stack int32[num_blocks] starts as [num_blocks-1, ..., 0] so block 0 is handed
  * out first; block tables int32[max_branches][max_blocks_per_branch] (-1 = empty).
@@ -132,9 +135,35 @@ int dendrite_fork_batch(dendrite_pool* pool, const int32_t* parents, const int32
  * order.  All-or-nothing: if the pool has too few free blocks the call
  * applies nothing and the pool reports DENDRITE_ENOMEM (sticky).
  * n_new == 0 is a no-op.
+ * A pool of n_layers > 1 takes every layer at once: K, V are
+ * [n_layers][n_branches][n_new][n_kv_heads][head_dim]; the copy-on-write and
+ * allocation decisions are made once and applied to every layer.
+ * DENDRITE_EINVAL while a split append (below) is pending.
  */
 int dendrite_append_kv(dendrite_pool* pool, const int32_t* branches, int32_t n_branches,
                        int32_t n_new, const void* K, const void* V, void* stream);
+
+/*
+ * Split append for a decode step through a multi-layer model, where layer l's
+ * K and V only exist once layer l has run.  No counterpart on the pages: it
+ * is dendrite_append_kv cut at its one natural seam (the block decisions are
+ * the same for every layer; only the rows differ).
+ *   dendrite_append_begin: the copy-on-write decisions, block allocation,
+ *     table and refcount updates and the new lengths, for all layers at once
+ *     (same rules, order and all-or-nothing behaviour as dendrite_append_kv).
+ *     No rows are written yet.
+ *   dendrite_append_layer: writes layer `layer`'s rows of the pending append
+ *     (K, V: [n_branches][n_new][n_kv_heads][head_dim] as in dendrite_append_kv)
+ *     and that layer's copy-on-write slot copies.  Each layer exactly once, in
+ *     any order; the append stops being pending when every layer is written.
+ * While an append is pending: dendrite_append_kv, dendrite_append_begin,
+ * dendrite_free and dendrite_truncate return DENDRITE_EINVAL, and attention
+ * on a layer whose rows are not written yet returns DENDRITE_EINVAL.
+ * Forks are allowed (a child shares the pending rows like any other).
+ */
+int dendrite_append_begin(dendrite_pool* pool, const int32_t* branches, int32_t n_branches,
+                          int32_t n_new, void* stream);
+int dendrite_append_layer(dendrite_pool* pool, int32_t layer, const void* K, const void* V, void* stream);
 
 /*
  * Tree decode attention (Dendrite article, section 技术深度解析: attention
@@ -149,9 +178,21 @@ int dendrite_append_kv(dendrite_pool* pool, const int32_t* branches, int32_t n_b
  * several queried branches are read from HBM once for all of them (split-KV
  * partials, then a log-sum-exp merge).  The plan built from the branch tree is
  * cached until the tree changes.  `branches` may not hold duplicates.
+ * Reads layer 0 of a multi-layer pool.
  */
 int dendrite_tree_attn_decode(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,
                               const int32_t* branches, int32_t n_branches, void* out, void* stream);
+
+/*
+ * The same attention over layer `layer` (0 <= layer < n_layers) of a
+ * multi-layer pool.  The plan depends only on the tree and the queried
+ * branches, so the calls of one decode step for layers 0..n_layers-1 build it
+ * once and reuse it.  DENDRITE_EINVAL if a pending split append has not
+ * written this layer's rows yet.
+ */
+int dendrite_tree_attn_decode_layer(dendrite_pool* pool, int32_t layer, const void* Q, int32_t n_q_heads,
+                                    int32_t q_len, const int32_t* branches, int32_t n_branches, void* out,
+                                    void* stream);
 
 /*
  * Free branches (host int32[n_branches], no duplicates): every block of each
@@ -198,8 +239,13 @@ int dendrite_read_refcounts(dendrite_pool* pool, int32_t* out, void* stream);
 int dendrite_read_free_stack(dendrite_pool* pool, int32_t* out, int32_t* top_out, void* stream);
 
 /* Copy one block's K and V ([n_kv_heads][block_size][head_dim], pool dtype)
- * to host buffers k_out / v_out. */
+ * to host buffers k_out / v_out (layer 0; dendrite_read_block_layer for any). */
 int dendrite_read_block(dendrite_pool* pool, int32_t block, void* k_out, void* v_out, void* stream);
+int dendrite_read_block_layer(dendrite_pool* pool, int32_t layer, int32_t block, void* k_out, void* v_out,
+                              void* stream);
+
+/* Number of layers the pool holds. */
+int dendrite_pool_layers(dendrite_pool* pool, int32_t* n_layers);
 
 /* Pool geometry: num_blocks, block_size, n_kv_heads, head_dim, dtype. */
 int dendrite_pool_info(dendrite_pool* pool, int64_t* num_blocks, int32_t* block_size,

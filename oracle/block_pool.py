@@ -29,6 +29,11 @@ supports):
 4. The parent of a fork stays live and keeps its references.
 5. An append that would need more blocks than are free changes nothing and
    raises :class:`PoolExhausted` (all-or-nothing).
+6. Layers (the pages describe one attention layer): a pool of n_layers keeps
+   one K and one V array per layer, and one set of block ids, tables,
+   refcounts and free stack for all of them, since every layer of a decoded
+   token lives at the same position.  An append allocates once and writes
+   (and copies on write) every layer.
 """
 from __future__ import annotations
 
@@ -56,13 +61,17 @@ def bits_of(t) -> np.ndarray:
 
 class BlockPool:
     def __init__(self, num_blocks: int, block_size: int, n_kv_heads: int, head_dim: int,
-                 bits_dtype=np.uint16):
+                 bits_dtype=np.uint16, n_layers: int = 1):
         self.N = num_blocks
         self.bs = block_size
         self.n_kv = n_kv_heads
         self.d = head_dim
-        self.K = np.zeros((num_blocks, n_kv_heads, block_size, head_dim), dtype=bits_dtype)
-        self.V = np.zeros_like(self.K)
+        self.n_layers = n_layers
+        # per layer [num_blocks][n_kv][block_size][head_dim]; K / V are layer 0
+        self.KL = np.zeros((n_layers, num_blocks, n_kv_heads, block_size, head_dim), dtype=bits_dtype)
+        self.VL = np.zeros_like(self.KL)
+        self.K = self.KL[0]
+        self.V = self.VL[0]
         self.refcount = np.zeros(num_blocks, dtype=np.int64)
         self.stack = list(range(num_blocks - 1, -1, -1))   # S[0..N-1]
         self.top = num_blocks
@@ -118,11 +127,17 @@ class BlockPool:
     def append(self, branches: Sequence[int], n_new: int, K_bits: np.ndarray,
                V_bits: np.ndarray) -> None:
         """Append ``n_new`` rows to every branch; ``K_bits``/``V_bits`` are
-        ``[n_branches][n_new][n_kv][d]`` raw bit patterns."""
+        ``[n_branches][n_new][n_kv][d]`` raw bit patterns, with a leading
+        ``[n_layers]`` axis for a pool of several layers."""
         if len(set(branches)) != len(branches):
             raise ValueError("duplicate branch in one append")
         if n_new == 0:
             return
+        K_bits = np.asarray(K_bits)
+        V_bits = np.asarray(V_bits)
+        if K_bits.ndim == 4:
+            K_bits, V_bits = K_bits[None], V_bits[None]
+        assert K_bits.shape[0] == self.n_layers
         if self._demand(branches, n_new) > self.top:
             raise PoolExhausted("not enough free blocks")
         bs = self.bs
@@ -134,8 +149,8 @@ class BlockPool:
                 tail = tab[L // bs]
                 if self.refcount[tail] > 1:
                     new = self._pop()
-                    self.K[new, :, :fill] = self.K[tail, :, :fill]
-                    self.V[new, :, :fill] = self.V[tail, :, :fill]
+                    self.KL[:, new, :, :fill] = self.KL[:, tail, :, :fill]
+                    self.VL[:, new, :, :fill] = self.VL[:, tail, :, :fill]
                     self.refcount[tail] -= 1
                     self.refcount[new] = 1
                     tab[L // bs] = new
@@ -145,8 +160,8 @@ class BlockPool:
                     new = self._pop()
                     self.refcount[new] = 1
                     tab.append(new)
-                self.K[tab[bi], :, slot] = K_bits[i, t]
-                self.V[tab[bi], :, slot] = V_bits[i, t]
+                self.KL[:, tab[bi], :, slot] = K_bits[:, i, t]
+                self.VL[:, tab[bi], :, slot] = V_bits[:, i, t]
             self.len[b] = L + n_new
 
     def free(self, branches: Sequence[int]) -> None:
@@ -187,27 +202,31 @@ class BlockPool:
             self._push(blk)
 
     # ---------------------------------------------------------- inspection
-    def read_branch_bits(self, h: int):
-        """K and V bits ``[len][n_kv][d]`` of branch ``h`` read through its table."""
+    def read_branch_bits(self, h: int, layer: int = 0):
+        """K and V bits ``[len][n_kv][d]`` of branch ``h`` in ``layer``, read through its table."""
         L = self.len[h]
         K = np.empty((L, self.n_kv, self.d), dtype=self.K.dtype)
         V = np.empty_like(K)
         for pos in range(L):
             blk = self.table[h][pos // self.bs]
-            K[pos] = self.K[blk, :, pos % self.bs]
-            V[pos] = self.V[blk, :, pos % self.bs]
+            K[pos] = self.KL[layer, blk, :, pos % self.bs]
+            V[pos] = self.VL[layer, blk, :, pos % self.bs]
         return K, V
 
     def used_blocks(self) -> int:
         return self.N - self.top
 
 
-def run_script_pool(w, num_blocks: int, kv_source=None, stop=None) -> BlockPool:
+def run_script_pool(w, num_blocks: int, kv_source=None, stop=None, n_layers: int = 1,
+                    device="cpu") -> BlockPool:
     """Replay a workload script (logical ids as handles) on a fresh pool.
-    ``stop``: replay only the first ``stop`` ops."""
+    ``stop``: replay only the first ``stop`` ops.  With ``n_layers`` > 1 an
+    append carries every layer's rows (``w.kv(idx, device, layer=l)``;
+    ``device`` picks the generator, so it must be where the GPU run drew its
+    values)."""
     import torch
     bits = np.uint16 if w.dtype == torch.bfloat16 else np.uint32
-    pool = BlockPool(num_blocks, w.block_size, w.n_kv_heads, w.head_dim, bits)
+    pool = BlockPool(num_blocks, w.block_size, w.n_kv_heads, w.head_dim, bits, n_layers)
     for idx, op in enumerate(w.ops[:stop]):
         if op.kind == "new":
             pool.new_branch(op.branches[0])
@@ -216,8 +235,13 @@ def run_script_pool(w, num_blocks: int, kv_source=None, stop=None) -> BlockPool:
         elif op.kind == "append":
             if op.n_new == 0:
                 continue
-            K, V = kv_source(idx) if kv_source else w.kv(idx)
-            pool.append(op.branches, op.n_new, bits_of(K), bits_of(V))
+            if n_layers == 1:
+                K, V = kv_source(idx) if kv_source else w.kv(idx)
+                pool.append(op.branches, op.n_new, bits_of(K), bits_of(V))
+            else:
+                kv = [w.kv(idx, device, layer=l) for l in range(n_layers)]
+                pool.append(op.branches, op.n_new, np.stack([bits_of(k) for k, _ in kv]),
+                            np.stack([bits_of(v) for _, v in kv]))
         elif op.kind == "free":
             pool.free(op.branches)
         elif op.kind == "truncate":

@@ -28,9 +28,10 @@ def ancestors(w, ids: Iterable[int]) -> Set[int]:
     return out
 
 
-def oracle_tree(w, ids: Iterable[int], device="cpu") -> KVTree:
+def oracle_tree(w, ids: Iterable[int], device="cpu", layer: int = 0) -> KVTree:
     """O1 tree holding only the ancestor chains of ``ids``; each append slice
-    is regenerated from its own seed on ``device`` (the values the GPU got)."""
+    is regenerated from its own seed on ``device`` (the values the GPU got),
+    for model layer ``layer``."""
     keep = ancestors(w, ids)
     tree = KVTree(w.n_kv_heads, w.head_dim)
     for idx, op in enumerate(w.ops):
@@ -43,7 +44,7 @@ def oracle_tree(w, ids: Iterable[int], device="cpu") -> KVTree:
         elif op.kind == "append" and op.n_new:
             for pos, b in enumerate(op.branches):
                 if b in keep:
-                    k, v = w.kv_one(idx, pos, device)
+                    k, v = w.kv_one(idx, pos, device, layer)
                     tree.append(b, k.cpu(), v.cpu())
         elif op.kind == "truncate":
             for b, n in zip(op.branches, op.new_lens):
@@ -59,7 +60,7 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device="cuda",
-                    strict: bool = False) -> float:
+                    strict: bool = False, layer: int = 0) -> float:
     """Max |GPU - oracle| over the sampled query positions (indices into w.query).
 
     ``tol`` bounds the arithmetic.  A bf16 output is also rounded to bf16 when
@@ -68,7 +69,7 @@ def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device=
     keys); unless ``strict``, that half ulp of the exact result is added to
     the bound element by element."""
     ids = [w.query[i] for i in sample]
-    tree = oracle_tree(w, ids, device)
+    tree = oracle_tree(w, ids, device, layer)
     worst = 0.0
     for i in sample:
         q = w.q_one(i, device).cpu()
@@ -82,8 +83,9 @@ def check_attention(w, out: torch.Tensor, sample: List[int], tol: float, device=
     return worst
 
 
-def pool_state_matches(pool, h: Dict[int, int], ref, check_bytes=True) -> None:
-    """Bit-exact comparison of the device pool against the O2 model."""
+def pool_state_matches(pool, h: Dict[int, int], ref, check_bytes=True, layers=(0,)) -> None:
+    """Bit-exact comparison of the device pool against the O2 model (the
+    payload of every layer in ``layers``)."""
     for b, tab in ref.table.items():
         assert pool.read_table(h[b]) == tab, ("table", b)
     assert pool.read_refcounts() == ref.refcount.tolist()
@@ -94,9 +96,10 @@ def pool_state_matches(pool, h: Dict[int, int], ref, check_bytes=True) -> None:
     for b, tab in ref.table.items():
         for pos in range(ref.len[b]):
             valid.setdefault(tab[pos // ref.bs], set()).add(pos % ref.bs)
-    for blk, slots in valid.items():
-        k, v = pool.read_block(blk)
-        kb, vb = bits_of(k), bits_of(v)
-        sl = sorted(slots)
-        assert np.array_equal(kb[:, sl], ref.K[blk][:, sl]), ("K bytes", blk)
-        assert np.array_equal(vb[:, sl], ref.V[blk][:, sl]), ("V bytes", blk)
+    for layer in layers:
+        for blk, slots in valid.items():
+            k, v = pool.read_block(blk, layer=layer)
+            kb, vb = bits_of(k), bits_of(v)
+            sl = sorted(slots)
+            assert np.array_equal(kb[:, sl], ref.KL[layer][blk][:, sl]), ("K bytes", layer, blk)
+            assert np.array_equal(vb[:, sl], ref.VL[layer][blk][:, sl]), ("V bytes", layer, blk)

@@ -90,8 +90,8 @@ class _Ramp(W.Workload):
     (base 2) across stages: the lazy-rescale path of the tcgen05 kernel runs
     many times.  Values stay N(0, 1)."""
 
-    def kv_one(self, op_index, pos, device="cpu"):
-        k, v = super().kv_one(op_index, pos, device)
+    def kv_one(self, op_index, pos, device="cpu", layer=0):
+        k, v = super().kv_one(op_index, pos, device, layer)
         n = k.shape[0]
         start = sum(op.n_new for op in self.ops[:op_index] if op.kind == "append")
         u = torch.ones(self.head_dim, device=device) / self.head_dim ** 0.5
