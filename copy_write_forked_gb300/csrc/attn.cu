@@ -572,6 +572,17 @@ __global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
         }
 }
 
+// ============================================================ plan upload
+// Copies the plan from the pool's pinned host buffer (device-accessible) to
+// its device copy.  A kernel rather than cudaMemcpyAsync: the copy engines
+// may be busy with the caller's own host-to-device traffic on other streams,
+// and a few KB of plan should not queue behind it.
+__global__ void __launch_bounds__(256) k_plan_upload(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                     int64_t n16) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 // ============================================================ host planning
 struct HostPlan {
     std::vector<AttnSeg> segs;
@@ -1065,7 +1076,13 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
         plan_pack(hp, off, p->h_plan);
-        DENDRITE_CUDA(cudaMemcpyAsync(p->d_plan, p->h_plan, b, cudaMemcpyHostToDevice, s));
+        {
+            const int64_t n16 = (int64_t)(b / 16);
+            const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
+            k_plan_upload<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(p->h_plan),
+                                               reinterpret_cast<uint4*>(p->d_plan), n16);
+            DENDRITE_CUDA(cudaGetLastError());
+        }
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
         pc.dev = plan_view(hp, off, p->d_plan, n, q_len, n_q_heads, n_q_heads / p->n_kv);
         pc.n_partial_rows = hp.partial_rows;
