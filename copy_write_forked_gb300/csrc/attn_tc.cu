@@ -11,11 +11,12 @@
 //   S_r = Q_r K^T   M = 128 rows, N = 16..64 tokens, K = head_dim 128
 //   O_r += P_r V    M = 128 rows, N = head_dim 128,  K = 16..64 tokens
 //
-// Warp roles (320 threads, one CTA per SM):
+// Warp roles (352 threads, one CTA per SM):
 //   warp 0      TMA producer: streams 64-token stages of K and V (4 blocks of
-//               16 tokens) into a 3-stage ring, block ids prefetched 32 tiles
+//               16 tokens) into a 4-stage ring, block ids fetched 32 tiles
 //               at a time.
-//   warp 1      TMEM owner; lane 0 issues every tcgen05.mma and commit.
+//   warp 1      TMEM owner; lane 0 issues the S MMAs and their commits.
+//   warp 10     lane 0 issues the P V MMAs and their commits.
 //   warps 2-9   softmax, one query row per thread (warps 2-5 row tile 0,
 //               warps 6-9 row tile 1): read the row of S from TMEM, mask,
 //               exponentiate (base 2), write P (bf16) to shared memory in the
@@ -52,7 +53,9 @@ constexpr int TC_STAGE = 4 * TC_HALF;                        // K half 0, K half
 constexpr int TC_QTILE = 128 * D * 2;                        // 128 rows x 128 columns bf16 = 32 KiB
 constexpr int TC_PBUF = 128 * TC_TOK * 2;                    // 128 rows x 64 tokens bf16 = 16 KiB
 constexpr int TC_ROWTILES = 2;
-constexpr int TC_THREADS = (2 + 4 * TC_ROWTILES) * 32;
+constexpr int TC_SOFTMAX_WARP0 = 2;
+constexpr int TC_PV_WARP = TC_SOFTMAX_WARP0 + 4 * TC_ROWTILES;   // 10
+constexpr int TC_THREADS = (TC_PV_WARP + 1) * 32;
 constexpr int OFF_Q = TC_NSTAGE * TC_STAGE;
 constexpr int OFF_P = OFF_Q + TC_ROWTILES * TC_QTILE;
 constexpr int OFF_BAR = OFF_P + TC_ROWTILES * TC_PBUF;
@@ -67,7 +70,8 @@ enum {
     B_PV_DONE = B_P_FULL + 2,
     B_Q_FULL = B_PV_DONE + 2,
     B_FINAL = B_Q_FULL + 2,
-    B_COUNT = B_FINAL + 1
+    B_FINAL_PV = B_FINAL + 1,
+    B_COUNT = B_FINAL_PV + 1
 };
 constexpr int SMEM_TC = 1024 + OFF_BAR + B_COUNT * 8 + 16;
 static_assert(SMEM_TC <= 227 * 1024, "shared memory budget");
@@ -147,9 +151,20 @@ __device__ __forceinline__ void reg_tie(uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait by one thread; on failure marks the CTA aborted and records
 // DENDRITE_ETIMEOUT (a no-op when another error is already recorded).
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abortp, DevMeta* meta) {
+    if (mbar_test(bar, parity)) return true;   // usually complete already
     if (*abortp) return false;
     if (mbar_wait(bar, parity, abortp)) return true;
     *abortp = 1;
@@ -189,7 +204,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_NSTAGE; ++s) {
             mbar_init(bar(B_KV_FULL + s), 1);
-            mbar_init(bar(B_KV_EMPTY + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), 2);   // the S issuer's and the PV issuer's commits
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(B_S_FULL + i), 1);
@@ -201,6 +216,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         for (int r = 0; r < TC_ROWTILES; ++r) mbar_init(bar(B_Q_FULL + r), 4);
         mbar_init(bar(B_FINAL), 1);
+        mbar_init(bar(B_FINAL_PV), 1);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
@@ -297,8 +313,15 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int s = 0; s < TC_NSTAGE; ++s)
                 if (issued >> s & 1u) drain_wait(bar(B_KV_FULL + s), parity_bits >> s & 1u);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == TC_PV_WARP) {
+        // ------------------------------------------------------ MMA issuers
+        // Two single-thread issuers, each with its own chain of waits: warp 1
+        // issues S(k) = Q K^T of every stage as soon as its K and V landed and
+        // the S buffer it overwrites was read (S runs at most two stages ahead
+        // of the softmax); warp 10 issues O += P V of stage k as soon as P(k)
+        // is in shared memory.  A stage goes back to the producer once both
+        // have committed it.
+        const bool s_role = warp == 1;
         if (lane == 0) {
             const uint32_t sQ = base + OFF_Q, sP = base + OFF_P;
             int32_t g = 0, jsS[2] = {0, 0}, jsP[2] = {0, 0}, qc[2] = {0, 0};
@@ -310,76 +333,75 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 if (t >= uend) { ++u; continue; }
                 const int32_t cend = min(t_end, uend);
                 const int RT = U.rt;
-                for (int r = 0; r < RT && ok; ++r) ok = thread_wait(bar(B_Q_FULL + r), (uint32_t)qc[r]++ & 1u, abortp, a.meta);
                 const int32_t nst = (cend - t + 3) >> 2;
-                // Per chunk: S(0) and S(1), then for every stage k: PV(k) of
-                // each row tile as soon as its P(k) is in shared memory, the
-                // stage back to the producer, and S(k + 2) into the S buffer
-                // that S(k) occupied (the softmax read it before writing P(k)).
-                // S thus runs two stages ahead of the softmax, and every wait
-                // suspends the thread instead of spinning.
-                auto issue_s = [&](int32_t k) {
-                    const int32_t gg = g + k;
-                    const int slot = gg % TC_NSTAGE;
-                    ok = ok && thread_wait(bar(B_KV_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
+                if (s_role) {
                     for (int r = 0; r < RT && ok; ++r)
-                        ok = thread_wait(bar(B_S_FREE + 2 * r + (jsS[r] & 1)), ((uint32_t)(jsS[r] >> 1) & 1u) ^ 1u,
-                                         abortp, a.meta);
-                    if (!ok) return;
-                    tc_fence_after();
-                    const int ntiles = min(4, cend - (t + 4 * k));
-                    const uint32_t stage = base + slot * TC_STAGE;
-                    const uint32_t id = idesc_bf16(128, 16 * ntiles, 0, 0);
-                    for (int r = 0; r < RT; ++r) {
-                        const int b = jsS[r] & 1;
-                        const uint32_t dS = tmem + r * 256 + 128 + b * 64;
-                        const uint32_t q = sQ + r * TC_QTILE;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            const uint32_t koff = (kk >> 2) * TC_HALF + (kk & 3) * 32;
-                            umma_bf16(dS, sdesc(q + qoff, 16, 1024), sdesc(stage + koff, 16, 1024), id, kk > 0);
-                        }
-                        umma_commit(bar(B_S_FULL + 2 * r + b));
-                        ++jsS[r];
-                    }
-                    any = true;
-                };
-                issue_s(0);
-                if (nst > 1) issue_s(1);
-                for (int32_t k = 0; k < nst && ok; ++k) {
-                    const int32_t gg = g + k;
-                    const int ntiles = min(4, cend - (t + 4 * k));
-                    const uint32_t vst = base + (gg % TC_NSTAGE) * TC_STAGE + 2 * TC_HALF;
-                    const uint32_t id = idesc_bf16(128, 128, 0, 1);
-                    for (int r = 0; r < RT && ok; ++r) {
-                        ok = thread_wait(bar(B_P_FULL + r), (uint32_t)jsP[r] & 1u, abortp, a.meta);
+                        ok = thread_wait(bar(B_Q_FULL + r), (uint32_t)qc[r]++ & 1u, abortp, a.meta);
+                    for (int32_t k = 0; k < nst && ok; ++k) {
+                        const int32_t gg = g + k;
+                        const int slot = gg % TC_NSTAGE;
+                        ok = thread_wait(bar(B_KV_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
+                        for (int r = 0; r < RT && ok; ++r)
+                            ok = thread_wait(bar(B_S_FREE + 2 * r + (jsS[r] & 1)),
+                                             ((uint32_t)(jsS[r] >> 1) & 1u) ^ 1u, abortp, a.meta);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t p = sP + r * TC_PBUF;
-                        for (int kk = 0; kk < ntiles; ++kk)
-                            umma_bf16(tmem + r * 256, sdesc(p + kk * 32, 16, 1024),
-                                      sdesc(vst + kk * 2048, TC_HALF, 1024), id, kk > 0 || k > 0);
-                        umma_commit(bar(B_PV_DONE + r));
-                        ++jsP[r];
+                        const int ntiles = min(4, cend - (t + 4 * k));
+                        const uint32_t stage = base + slot * TC_STAGE;
+                        const uint32_t id = idesc_bf16(128, 16 * ntiles, 0, 0);
+                        for (int r = 0; r < RT; ++r) {
+                            const int b = jsS[r] & 1;
+                            const uint32_t dS = tmem + r * 256 + 128 + b * 64;
+                            const uint32_t q = sQ + r * TC_QTILE;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                const uint32_t koff = (kk >> 2) * TC_HALF + (kk & 3) * 32;
+                                umma_bf16(dS, sdesc(q + qoff, 16, 1024), sdesc(stage + koff, 16, 1024), id,
+                                          kk > 0);
+                            }
+                            umma_commit(bar(B_S_FULL + 2 * r + b));
+                            ++jsS[r];
+                        }
+                        umma_commit(bar(B_KV_EMPTY + slot));
+                        any = true;
                     }
-                    if (!ok) break;
-                    umma_commit(bar(B_KV_EMPTY + gg % TC_NSTAGE));
-                    if (k + 2 < nst) issue_s(k + 2);
+                } else {
+                    for (int32_t k = 0; k < nst && ok; ++k) {
+                        const int32_t gg = g + k;
+                        const int ntiles = min(4, cend - (t + 4 * k));
+                        const uint32_t vst = base + (gg % TC_NSTAGE) * TC_STAGE + 2 * TC_HALF;
+                        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+                        for (int r = 0; r < RT && ok; ++r) {
+                            ok = thread_wait(bar(B_P_FULL + r), (uint32_t)jsP[r] & 1u, abortp, a.meta);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t p = sP + r * TC_PBUF;
+                            for (int kk = 0; kk < ntiles; ++kk)
+                                umma_bf16(tmem + r * 256, sdesc(p + kk * 32, 16, 1024),
+                                          sdesc(vst + kk * 2048, TC_HALF, 1024), id, kk > 0 || k > 0);
+                            umma_commit(bar(B_PV_DONE + r));
+                            ++jsP[r];
+                            any = true;
+                        }
+                        if (!ok) break;
+                        umma_commit(bar(B_KV_EMPTY + gg % TC_NSTAGE));
+                    }
                 }
                 g += nst;
                 t = cend;
                 ++u;
             }
-            if (any) {   // every MMA issued has finished before the TMEM is freed
-                umma_commit(bar(B_FINAL));
-                drain_wait(bar(B_FINAL), 0);
+            if (any) {   // every MMA this thread issued has finished before the TMEM is freed
+                const uint32_t fb = bar(s_role ? B_FINAL : B_FINAL_PV);
+                umma_commit(fb);
+                drain_wait(fb, 0);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------ softmax
-        const int r = (warp - 2) >> 2;
+        const int r = (warp - TC_SOFTMAX_WARP0) >> 2;
         const int sub = warp & 3;                 // TMEM lanes 32 sub .. 32 sub + 31
         const int trow = sub * 32 + lane;         // row within the row tile
         const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16) + r * 256;
