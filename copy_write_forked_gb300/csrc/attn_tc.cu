@@ -11,10 +11,10 @@
 //   S_r = Q_r K^T   M = 128 rows, N = 16..64 tokens, K = head_dim 128
 //   O_r += P_r V    M = 128 rows, N = head_dim 128,  K = 16..64 tokens
 //
-// Warp roles (352 threads, one CTA per SM):
-//   warp 0      TMA producer: streams 64-token stages of K and V (4 blocks of
-//               16 tokens) into a 4-stage ring, block ids fetched 32 tiles
-//               at a time.
+// Warp roles (384 threads, one CTA per SM):
+//   warps 0, 11 TMA producers: stream 64-token stages (4 blocks of 16 tokens)
+//               of K and of V into two 4-stage rings, block ids fetched 32
+//               tiles at a time.
 //   warp 1      TMEM owner; lane 0 issues the S MMAs and their commits.
 //   warp 10     lane 0 issues the P V MMAs and their commits.
 //   warps 2-9   softmax, one query row per thread (warps 2-5 row tile 0,
@@ -49,22 +49,28 @@ namespace {
 constexpr int TC_NSTAGE = 4;
 constexpr int TC_TOK = 64;                                   // tokens per stage (4 blocks)
 constexpr int TC_HALF = TC_TOK * 128;                        // 64 tokens x 64 columns bf16 = 8 KiB
-constexpr int TC_STAGE = 4 * TC_HALF;                        // K half 0, K half 1, V half 0, V half 1
+constexpr int TC_RING_STAGE = 2 * TC_HALF;                   // K (or V) of a stage: half 0, half 1
 constexpr int TC_QTILE = 128 * D * 2;                        // 128 rows x 128 columns bf16 = 32 KiB
 constexpr int TC_PBUF = 128 * TC_TOK * 2;                    // 128 rows x 64 tokens bf16 = 16 KiB
 constexpr int TC_ROWTILES = 2;
 constexpr int TC_SOFTMAX_WARP0 = 2;
 constexpr int TC_PV_WARP = TC_SOFTMAX_WARP0 + 4 * TC_ROWTILES;   // 10
-constexpr int TC_THREADS = (TC_PV_WARP + 1) * 32;
-constexpr int OFF_Q = TC_NSTAGE * TC_STAGE;
+constexpr int TC_V_WARP = TC_PV_WARP + 1;                          // 11
+constexpr int TC_THREADS = (TC_V_WARP + 1) * 32;
+// K ring, then V ring: each TC_NSTAGE stages of 64 tokens
+constexpr int OFF_K = 0;
+constexpr int OFF_V = TC_NSTAGE * TC_RING_STAGE;
+constexpr int OFF_Q = 2 * TC_NSTAGE * TC_RING_STAGE;
 constexpr int OFF_P = OFF_Q + TC_ROWTILES * TC_QTILE;
 constexpr int OFF_BAR = OFF_P + TC_ROWTILES * TC_PBUF;
 // mbarriers; S buffers are indexed 2 r + b (row tile r, buffer b), the
 // P buffer and O accumulator by r
 enum {
-    B_KV_FULL = 0,
-    B_KV_EMPTY = B_KV_FULL + TC_NSTAGE,
-    B_S_FULL = B_KV_EMPTY + TC_NSTAGE,
+    B_K_FULL = 0,
+    B_K_EMPTY = B_K_FULL + TC_NSTAGE,
+    B_V_FULL = B_K_EMPTY + TC_NSTAGE,
+    B_V_EMPTY = B_V_FULL + TC_NSTAGE,
+    B_S_FULL = B_V_EMPTY + TC_NSTAGE,
     B_S_FREE = B_S_FULL + 4,
     B_P_FULL = B_S_FREE + 4,
     B_PV_DONE = B_P_FULL + 2,
@@ -203,8 +209,10 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_NSTAGE; ++s) {
-            mbar_init(bar(B_KV_FULL + s), 1);
-            mbar_init(bar(B_KV_EMPTY + s), 2);   // the S issuer's and the PV issuer's commits
+            mbar_init(bar(B_K_FULL + s), 1);
+            mbar_init(bar(B_K_EMPTY + s), 1);    // the S issuer's commit
+            mbar_init(bar(B_V_FULL + s), 1);
+            mbar_init(bar(B_V_EMPTY + s), 1);    // the PV issuer's commit
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(B_S_FULL + i), 1);
@@ -242,10 +250,16 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int32_t u0 = pl.tc_cta_unit[c];
     volatile int* abortp = &abort_flag;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        // Lane i < ntiles issues tile i of the stage: K and V, two 64-column
-        // halves each, at token offset 16 i of the stage's four 8 KiB halves.
+    if (warp == 0 || warp == TC_V_WARP) {
+        // ------------------------------------------------------ producers
+        // Warp 0 streams K into the K ring, warp 11 V into the V ring, so a
+        // K slot is refilled as soon as its S is done and a V slot as soon as
+        // its P V is done.  Lane i < ntiles issues tile i of the stage: two
+        // 64-column halves at token offset 16 i of the stage's two 8 KiB halves.
+        const bool k_role = warp == 0;
+        const CUtensorMap* tmap = k_role ? &tmK : &tmV;
+        const uint32_t ring = base + (k_role ? OFF_K : OFF_V);
+        const int b_full = k_role ? B_K_FULL : B_V_FULL, b_empty = k_role ? B_K_EMPTY : B_V_EMPTY;
         uint32_t issued = 0, parity_bits = 0;
         int32_t g = 0;
         int32_t t = t_begin, u = u0;
@@ -273,7 +287,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     const int32_t pa = __shfl_sync(0xffffffffu, cur, idx & 31);
                     const int32_t pb = __shfl_sync(0xffffffffu, nxt, idx & 31);
                     const int32_t pblk = idx < 32 ? pa : pb;
-                    if (lane < 4 && pst + lane < cend && (uint32_t)pblk < (uint32_t)a.n_blocks) {
+                    if (k_role && lane < 4 && pst + lane < cend && (uint32_t)pblk < (uint32_t)a.n_blocks) {
                         const int32_t prow = (pblk * a.n_kv + U.kv_head) * BS;
                         tma_prefetch_3d(&tmK, 0, 0, prow);
                         tma_prefetch_3d(&tmK, 0, 1, prow);
@@ -285,10 +299,10 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 const uint32_t ph = (uint32_t)(g / TC_NSTAGE) & 1u;
                 const int ntiles = min(4, cend - st);
                 int ok = 1;
-                if (lane == 0) ok = thread_wait(bar(B_KV_EMPTY + slot), ph ^ 1u, abortp, a.meta);
+                if (lane == 0) ok = thread_wait(bar(b_empty + slot), ph ^ 1u, abortp, a.meta);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                if (lane == 0) mbar_expect_tx(bar(B_KV_FULL + slot), (uint32_t)(ntiles * 4 * HALF_BYTES));
+                if (lane == 0) mbar_expect_tx(bar(b_full + slot), (uint32_t)(ntiles * 2 * HALF_BYTES));
                 __syncwarp();
                 if (lane < ntiles) {
                     if ((uint32_t)blk >= (uint32_t)a.n_blocks) {   // broken table: poison, read zeros
@@ -296,12 +310,10 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                         blk = -1;
                     }
                     const int32_t row0 = (blk * a.n_kv + U.kv_head) * BS;
-                    const uint32_t dst = base + slot * TC_STAGE + lane * HALF_BYTES;
-                    const uint32_t fb = bar(B_KV_FULL + slot);
-                    tma_load_3d(dst, &tmK, 0, 0, row0, fb);
-                    tma_load_3d(dst + TC_HALF, &tmK, 0, 1, row0, fb);
-                    tma_load_3d(dst + 2 * TC_HALF, &tmV, 0, 0, row0, fb);
-                    tma_load_3d(dst + 3 * TC_HALF, &tmV, 0, 1, row0, fb);
+                    const uint32_t dst = ring + slot * TC_RING_STAGE + lane * HALF_BYTES;
+                    const uint32_t fb = bar(b_full + slot);
+                    tma_load_3d(dst, tmap, 0, 0, row0, fb);
+                    tma_load_3d(dst + TC_HALF, tmap, 0, 1, row0, fb);
                 }
                 issued |= 1u << slot;
                 parity_bits = (parity_bits & ~(1u << slot)) | (ph << slot);
@@ -311,7 +323,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         if (lane == 0 && *abortp) {   // copies still in flight land before the CTA exits
             for (int s = 0; s < TC_NSTAGE; ++s)
-                if (issued >> s & 1u) drain_wait(bar(B_KV_FULL + s), parity_bits >> s & 1u);
+                if (issued >> s & 1u) drain_wait(bar(b_full + s), parity_bits >> s & 1u);
         }
     } else if (warp == 1 || warp == TC_PV_WARP) {
         // ------------------------------------------------------ MMA issuers
@@ -340,14 +352,14 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     for (int32_t k = 0; k < nst && ok; ++k) {
                         const int32_t gg = g + k;
                         const int slot = gg % TC_NSTAGE;
-                        ok = thread_wait(bar(B_KV_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
+                        ok = thread_wait(bar(B_K_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
                         for (int r = 0; r < RT && ok; ++r)
                             ok = thread_wait(bar(B_S_FREE + 2 * r + (jsS[r] & 1)),
                                              ((uint32_t)(jsS[r] >> 1) & 1u) ^ 1u, abortp, a.meta);
                         if (!ok) break;
                         tc_fence_after();
                         const int ntiles = min(4, cend - (t + 4 * k));
-                        const uint32_t stage = base + slot * TC_STAGE;
+                        const uint32_t stage = base + OFF_K + slot * TC_RING_STAGE;
                         const uint32_t id = idesc_bf16(128, 16 * ntiles, 0, 0);
                         for (int r = 0; r < RT; ++r) {
                             const int b = jsS[r] & 1;
@@ -363,15 +375,17 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                             umma_commit(bar(B_S_FULL + 2 * r + b));
                             ++jsS[r];
                         }
-                        umma_commit(bar(B_KV_EMPTY + slot));
+                        umma_commit(bar(B_K_EMPTY + slot));
                         any = true;
                     }
                 } else {
                     for (int32_t k = 0; k < nst && ok; ++k) {
                         const int32_t gg = g + k;
                         const int ntiles = min(4, cend - (t + 4 * k));
-                        const uint32_t vst = base + (gg % TC_NSTAGE) * TC_STAGE + 2 * TC_HALF;
+                        const int slot = gg % TC_NSTAGE;
+                        const uint32_t vst = base + OFF_V + slot * TC_RING_STAGE;
                         const uint32_t id = idesc_bf16(128, 128, 0, 1);
+                        ok = thread_wait(bar(B_V_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
                         for (int r = 0; r < RT && ok; ++r) {
                             ok = thread_wait(bar(B_P_FULL + r), (uint32_t)jsP[r] & 1u, abortp, a.meta);
                             if (!ok) break;
@@ -385,7 +399,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                             any = true;
                         }
                         if (!ok) break;
-                        umma_commit(bar(B_KV_EMPTY + gg % TC_NSTAGE));
+                        umma_commit(bar(B_V_EMPTY + slot));
                     }
                 }
                 g += nst;
