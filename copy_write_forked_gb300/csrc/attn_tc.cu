@@ -11,12 +11,13 @@
 //   S_r = Q_r K^T   M = 128 rows, N = 16..64 tokens, K = head_dim 128
 //   O_r += P_r V    M = 128 rows, N = head_dim 128,  K = 16..64 tokens
 //
-// Warp roles (384 threads, one CTA per SM):
+// Warp roles (448 threads, one CTA per SM):
 //   warps 0, 11 TMA producers: stream 64-token stages (4 blocks of 16 tokens)
 //               of K and of V into two 4-stage rings, block ids fetched 32
 //               tiles at a time.
-//   warp 1      TMEM owner; lane 0 issues the S MMAs and their commits.
-//   warp 10     lane 0 issues the P V MMAs and their commits.
+//   warps 1, 12 TMEM owner (warp 1); lane 0 issues the S MMAs of row tile
+//               0 (warp 1) or 1 (warp 12) and their commits.
+//   warps 10, 13 lane 0 issues the P V MMAs of row tile 0 or 1.
 //   warps 2-9   softmax, one query row per thread (warps 2-5 row tile 0,
 //               warps 6-9 row tile 1): read the row of S from TMEM, mask,
 //               exponentiate (base 2), write P (bf16) to shared memory in the
@@ -56,7 +57,9 @@ constexpr int TC_ROWTILES = 2;
 constexpr int TC_SOFTMAX_WARP0 = 2;
 constexpr int TC_PV_WARP = TC_SOFTMAX_WARP0 + 4 * TC_ROWTILES;   // 10
 constexpr int TC_V_WARP = TC_PV_WARP + 1;                          // 11
-constexpr int TC_THREADS = (TC_V_WARP + 1) * 32;
+constexpr int TC_S1_WARP = TC_V_WARP + 1;                          // 12
+constexpr int TC_PV1_WARP = TC_S1_WARP + 1;                        // 13
+constexpr int TC_THREADS = (TC_PV1_WARP + 1) * 32;
 // K ring, then V ring: each TC_NSTAGE stages of 64 tokens
 constexpr int OFF_K = 0;
 constexpr int OFF_V = TC_NSTAGE * TC_RING_STAGE;
@@ -75,9 +78,8 @@ enum {
     B_P_FULL = B_S_FREE + 4,
     B_PV_DONE = B_P_FULL + 2,
     B_Q_FULL = B_PV_DONE + 2,
-    B_FINAL = B_Q_FULL + 2,
-    B_FINAL_PV = B_FINAL + 1,
-    B_COUNT = B_FINAL_PV + 1
+    B_FINAL = B_Q_FULL + 2,   // one per issuer: S0, PV0, S1, PV1
+    B_COUNT = B_FINAL + 4
 };
 constexpr int SMEM_TC = 1024 + OFF_BAR + B_COUNT * 8 + 16;
 static_assert(SMEM_TC <= 227 * 1024, "shared memory budget");
@@ -210,9 +212,9 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_NSTAGE; ++s) {
             mbar_init(bar(B_K_FULL + s), 1);
-            mbar_init(bar(B_K_EMPTY + s), 1);    // the S issuer's commit
+            mbar_init(bar(B_K_EMPTY + s), 2);    // both S issuers (row tiles 0 and 1)
             mbar_init(bar(B_V_FULL + s), 1);
-            mbar_init(bar(B_V_EMPTY + s), 1);    // the PV issuer's commit
+            mbar_init(bar(B_V_EMPTY + s), 2);    // both PV issuers
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(B_S_FULL + i), 1);
@@ -223,8 +225,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             mbar_init(bar(B_PV_DONE + r), 1);
         }
         for (int r = 0; r < TC_ROWTILES; ++r) mbar_init(bar(B_Q_FULL + r), 4);
-        mbar_init(bar(B_FINAL), 1);
-        mbar_init(bar(B_FINAL_PV), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_FINAL + i), 1);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
@@ -325,18 +326,22 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int s = 0; s < TC_NSTAGE; ++s)
                 if (issued >> s & 1u) drain_wait(bar(b_full + s), parity_bits >> s & 1u);
         }
-    } else if (warp == 1 || warp == TC_PV_WARP) {
+    } else if (warp == 1 || warp == TC_PV_WARP || warp == TC_S1_WARP || warp == TC_PV1_WARP) {
         // ------------------------------------------------------ MMA issuers
-        // Two single-thread issuers, each with its own chain of waits: warp 1
-        // issues S(k) = Q K^T of every stage as soon as its K and V landed and
-        // the S buffer it overwrites was read (S runs at most two stages ahead
-        // of the softmax); warp 10 issues O += P V of stage k as soon as P(k)
-        // is in shared memory.  A stage goes back to the producer once both
-        // have committed it.
-        const bool s_role = warp == 1;
+        // Four single-thread issuers, one chain of waits each: for row tile
+        // r, an S issuer (warp 1 for r = 0, warp 12 for r = 1) issues
+        // S_r(k) = Q_r K^T as soon as stage k's K landed and the S buffer it
+        // overwrites was read (S runs at most two stages ahead of the
+        // softmax), and a PV issuer (warp 10, warp 13) issues O_r += P_r V as
+        // soon as stage k's V landed and P_r(k) is in shared memory.  A ring
+        // slot goes back to its producer once both issuers of its kind have
+        // committed it; the issuer of a row tile a unit does not have simply
+        // arrives.
+        const bool s_role = warp == 1 || warp == TC_S1_WARP;
+        const int my_r = (warp == 1 || warp == TC_PV_WARP) ? 0 : 1;
         if (lane == 0) {
-            const uint32_t sQ = base + OFF_Q, sP = base + OFF_P;
-            int32_t g = 0, jsS[2] = {0, 0}, jsP[2] = {0, 0}, qc[2] = {0, 0};
+            const uint32_t sQ = base + OFF_Q + my_r * TC_QTILE, sP = base + OFF_P + my_r * TC_PBUF;
+            int32_t g = 0, js = 0, qc = 0;
             bool ok = true, any = false;
             int32_t t = t_begin, u = u0;
             while (ok && t < t_end) {
@@ -344,62 +349,56 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 const int32_t uend = U.tile_off + U.n_blk;
                 if (t >= uend) { ++u; continue; }
                 const int32_t cend = min(t_end, uend);
-                const int RT = U.rt;
+                const bool active = my_r < U.rt;
                 const int32_t nst = (cend - t + 3) >> 2;
-                if (s_role) {
-                    for (int r = 0; r < RT && ok; ++r)
-                        ok = thread_wait(bar(B_Q_FULL + r), (uint32_t)qc[r]++ & 1u, abortp, a.meta);
-                    for (int32_t k = 0; k < nst && ok; ++k) {
-                        const int32_t gg = g + k;
-                        const int slot = gg % TC_NSTAGE;
-                        ok = thread_wait(bar(B_K_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
-                        for (int r = 0; r < RT && ok; ++r)
-                            ok = thread_wait(bar(B_S_FREE + 2 * r + (jsS[r] & 1)),
-                                             ((uint32_t)(jsS[r] >> 1) & 1u) ^ 1u, abortp, a.meta);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const int ntiles = min(4, cend - (t + 4 * k));
-                        const uint32_t stage = base + OFF_K + slot * TC_RING_STAGE;
-                        const uint32_t id = idesc_bf16(128, 16 * ntiles, 0, 0);
-                        for (int r = 0; r < RT; ++r) {
-                            const int b = jsS[r] & 1;
-                            const uint32_t dS = tmem + r * 256 + 128 + b * 64;
-                            const uint32_t q = sQ + r * TC_QTILE;
+                if (s_role && active) ok = thread_wait(bar(B_Q_FULL + my_r), (uint32_t)qc++ & 1u, abortp, a.meta);
+                for (int32_t k = 0; k < nst && ok; ++k) {
+                    const int32_t gg = g + k;
+                    const int slot = gg % TC_NSTAGE;
+                    const uint32_t ph = (uint32_t)(gg / TC_NSTAGE) & 1u;
+                    const int ntiles = min(4, cend - (t + 4 * k));
+                    if (s_role) {
+                        ok = thread_wait(bar(B_K_FULL + slot), ph, abortp, a.meta);
+                        if (ok && active) {
+                            const int b = js & 1;
+                            ok = thread_wait(bar(B_S_FREE + 2 * my_r + b), ((uint32_t)(js >> 1) & 1u) ^ 1u, abortp,
+                                             a.meta);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t stage = base + OFF_K + slot * TC_RING_STAGE;
+                            const uint32_t id = idesc_bf16(128, 16 * ntiles, 0, 0);
+                            const uint32_t dS = tmem + my_r * 256 + 128 + b * 64;
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
                                 const uint32_t koff = (kk >> 2) * TC_HALF + (kk & 3) * 32;
-                                umma_bf16(dS, sdesc(q + qoff, 16, 1024), sdesc(stage + koff, 16, 1024), id,
-                                          kk > 0);
+                                umma_bf16(dS, sdesc(sQ + qoff, 16, 1024), sdesc(stage + koff, 16, 1024), id, kk > 0);
                             }
-                            umma_commit(bar(B_S_FULL + 2 * r + b));
-                            ++jsS[r];
+                            umma_commit(bar(B_S_FULL + 2 * my_r + b));
+                            umma_commit(bar(B_K_EMPTY + slot));
+                            ++js;
+                            any = true;
+                        } else if (ok) {
+                            mbar_arrive(bar(B_K_EMPTY + slot));
                         }
-                        umma_commit(bar(B_K_EMPTY + slot));
-                        any = true;
-                    }
-                } else {
-                    for (int32_t k = 0; k < nst && ok; ++k) {
-                        const int32_t gg = g + k;
-                        const int ntiles = min(4, cend - (t + 4 * k));
-                        const int slot = gg % TC_NSTAGE;
-                        const uint32_t vst = base + OFF_V + slot * TC_RING_STAGE;
-                        const uint32_t id = idesc_bf16(128, 128, 0, 1);
-                        ok = thread_wait(bar(B_V_FULL + slot), (uint32_t)(gg / TC_NSTAGE) & 1u, abortp, a.meta);
-                        for (int r = 0; r < RT && ok; ++r) {
-                            ok = thread_wait(bar(B_P_FULL + r), (uint32_t)jsP[r] & 1u, abortp, a.meta);
+                    } else {
+                        ok = thread_wait(bar(B_V_FULL + slot), ph, abortp, a.meta);
+                        if (ok && active) {
+                            ok = thread_wait(bar(B_P_FULL + my_r), (uint32_t)js & 1u, abortp, a.meta);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint32_t p = sP + r * TC_PBUF;
+                            const uint32_t vst = base + OFF_V + slot * TC_RING_STAGE;
+                            const uint32_t id = idesc_bf16(128, 128, 0, 1);
                             for (int kk = 0; kk < ntiles; ++kk)
-                                umma_bf16(tmem + r * 256, sdesc(p + kk * 32, 16, 1024),
+                                umma_bf16(tmem + my_r * 256, sdesc(sP + kk * 32, 16, 1024),
                                           sdesc(vst + kk * 2048, TC_HALF, 1024), id, kk > 0 || k > 0);
-                            umma_commit(bar(B_PV_DONE + r));
-                            ++jsP[r];
+                            umma_commit(bar(B_PV_DONE + my_r));
+                            umma_commit(bar(B_V_EMPTY + slot));
+                            ++js;
                             any = true;
+                        } else if (ok) {
+                            mbar_arrive(bar(B_V_EMPTY + slot));
                         }
-                        if (!ok) break;
-                        umma_commit(bar(B_V_EMPTY + slot));
                     }
                 }
                 g += nst;
@@ -407,7 +406,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 ++u;
             }
             if (any) {   // every MMA this thread issued has finished before the TMEM is freed
-                const uint32_t fb = bar(s_role ? B_FINAL : B_FINAL_PV);
+                const uint32_t fb = bar(B_FINAL + (s_role ? 0 : 1) + 2 * my_r);
                 umma_commit(fb);
                 drain_wait(fb, 0);
             }
