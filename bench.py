@@ -494,11 +494,12 @@ def run_attention_only(args):
     pool.tree_attn_decode(Q, br, out=out)        # builds the plan (and sizes the workspace)
     plan_first_us = pool.last_plan_stats()["plan_us"]
     rb = []
+    Qr = Q.flip(0).contiguous()
     for _ in range(5):                           # rebuilds: another branch order misses the plan cache
-        pool.tree_attn_decode(Q.flip(0).contiguous(), br[::-1], out=out)
-        rb.append(pool.last_plan_stats()["plan_us"])
-        pool.tree_attn_decode(Q, br, out=out)
-        rb.append(pool.last_plan_stats()["plan_us"])
+        for qq, bb in ((Qr, br[::-1]), (Q, br)):
+            pool.sync()                          # the device idle: time the planning alone
+            pool.tree_attn_decode(qq, bb, out=out)
+            rb.append(pool.last_plan_stats()["plan_us"])
     pool.sync()
     for _ in range(args.warmup):
         flush_r.max()

@@ -583,12 +583,32 @@ __global__ void __launch_bounds__(256) k_plan_upload(const uint4* __restrict__ s
         dst[i] = src[i];
 }
 
+// Row records of every unit: segment row sr of unit U is member sr / (q_len G),
+// query token (sr % (q_len G)) / G and head group sr % G; it reads Q/out row
+// (member, token, kv head, group) and sees positions < len - q_len + token + 1.
+__global__ void __launch_bounds__(128) k_plan_rows(const AttnPlanDev pl) {
+    AttnRow* rows = const_cast<AttnRow*>(pl.rows);
+    const int32_t G = pl.group, RM = pl.q_len * G;
+    for (int32_t u = blockIdx.x; u < pl.n_units; u += gridDim.x) {
+        const AttnUnit U = pl.units[u];
+        const int32_t mem_off = pl.segs[U.seg].mem_off;
+        for (int32_t r = threadIdx.x; r < U.n_rows; r += blockDim.x) {
+            const int32_t sr = U.row_lo + r;
+            const int32_t mi = sr / RM, rem = sr - mi * RM;
+            const int32_t j = rem / G, g = rem - j * G;
+            const AttnMember M = pl.members[mem_off + mi];
+            rows[U.row_off + r] = AttnRow{(M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * G + g,
+                                          M.len - pl.q_len + j + 1};
+        }
+    }
+}
+
 // ============================================================ host planning
 struct HostPlan {
     std::vector<AttnSeg> segs;
     std::vector<AttnMember> members;
     std::vector<AttnUnit> units;
-    std::vector<AttnRow> rows;
+    size_t n_rows = 0;    // row records of all units (built on the device)
     std::vector<int32_t> cta_begin, cta_unit, tc_cta_begin, tc_cta_unit, path_off, path;
     std::vector<int64_t> cuts;
     int64_t tiles = 0, unique_tiles = 0;
@@ -597,7 +617,7 @@ struct HostPlan {
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
-        segs.clear(); members.clear(); units.clear(); rows.clear(); cta_begin.clear(); cta_unit.clear();
+        segs.clear(); members.clear(); units.clear(); n_rows = 0; cta_begin.clear(); cta_unit.clear();
         tc_cta_begin.clear(); tc_cta_unit.clear(); path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         n_tc_units = 0;
@@ -706,7 +726,23 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
                   hp.psegs, hp.seg_members);
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by
-    // more than tc_min_rows rows per kv head, pass 1 the rest.
+    // more than tc_min_rows rows per kv head, pass 1 the rest.  The unit and
+    // member arrays are sized first and filled in place.
+    size_t n_units_total = 0, n_members_total = 0;
+    for (const Segment& sg : hp.psegs) {
+        const int32_t rows_per_head = sg.n_members * RM;
+        const int32_t group_rows = (tc_on && rows_per_head > p->tc_min_rows) ? kMaxUnitRowsTc : small_rows;
+        n_units_total += (size_t)nkv * ((rows_per_head + group_rows - 1) / group_rows);
+        n_members_total += sg.n_members;
+    }
+    if (n_units_total >= (size_t)INT32_MAX / 2) return DENDRITE_ELIMIT;
+    hp.units.resize(n_units_total);
+    hp.members.resize(n_members_total);
+    hp.segs.reserve(hp.psegs.size());
+    AttnUnit* up = hp.units.data();
+    AttnMember* mp = hp.members.data();
+    int32_t n_mem = 0, n_unit = 0;
+    int64_t n_rows = 0;
     int64_t weight[2] = {0, 0}, class_tiles[2] = {0, 0};
     for (int pass = 0; pass < 2; ++pass) {
         int64_t tile_off = 0;
@@ -720,57 +756,46 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
             S.table_row = p->nodes[sg.rep_node].handle;
             S.blk_start = sg.block_start;
             S.n_blk = sg.block_count;
-            S.mem_off = (int32_t)hp.members.size();
+            S.mem_off = n_mem;
             S.n_mem = sg.n_members;
-            S.unit_base = (int32_t)hp.units.size();
+            S.unit_base = n_unit;
             S.ngroups = (rows_per_head + group_rows - 1) / group_rows;
             S.group_rows = group_rows;
             for (int32_t k = 0; k < sg.n_members; ++k) {
                 const int32_t qi = hp.seg_members[sg.member_offset + k];
-                hp.members.push_back({qi, p->br[branches[qi]].len});
+                mp[n_mem++] = AttnMember{qi, p->br[branches[qi]].len};
             }
             hp.unique_tiles += (int64_t)sg.block_count * nkv;
             const int32_t seg_index = (int32_t)hp.segs.size();
             for (int32_t h = 0; h < nkv; ++h) {
                 for (int32_t grp = 0; grp < S.ngroups; ++grp) {
-                    AttnUnit U{};
+                    AttnUnit& U = up[n_unit++];
                     U.seg = seg_index;
                     U.kv_head = h;
                     U.row_lo = grp * group_rows;
                     U.n_rows = std::min(group_rows, rows_per_head - U.row_lo);
                     U.rt = tc ? (U.n_rows + 127) / 128 : U.n_rows <= 16 ? 1 : U.n_rows <= 32 ? 2 : 4;
                     U.tile_off = (int32_t)tile_off;
+                    U.cfirst = U.nchunks = U.prow_base = 0;
                     U.table_row = S.table_row;
                     U.blk_start = S.blk_start;
                     U.n_blk = S.n_blk;
-                    U.row_off = (int32_t)hp.rows.size();
-                    // rows: segment row sr -> member sr / RM, token (sr % RM) / G, group sr % G
-                    {
-                        int32_t mi = U.row_lo / RM, rem = U.row_lo % RM;
-                        int32_t j = rem / G, g = rem % G;
-                        for (int32_t r = 0; r < U.n_rows; ++r) {
-                            const AttnMember& M = hp.members[S.mem_off + mi];
-                            hp.rows.push_back({(M.qi * q_len + j) * nq + h * G + g, M.len - q_len + j + 1});
-                            if (++g == G) {
-                                g = 0;
-                                if (++j == q_len) {
-                                    j = 0;
-                                    ++mi;
-                                }
-                            }
-                        }
-                    }
+                    // the unit's row records are filled on the device (k_plan_rows)
+                    U.row_off = (int32_t)n_rows;
+                    U.pad[0] = U.pad[1] = U.pad[2] = 0;
+                    n_rows += U.n_rows;
                     tile_off += S.n_blk;
                     weight[pass] += cwt.unit_start + (int64_t)S.n_blk * tile_weight(U.rt);
-                    hp.units.push_back(U);
                 }
             }
             hp.segs.push_back(S);
         }
         class_tiles[pass] = tile_off;
         if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
-        if (pass == 0) hp.n_tc_units = (int32_t)hp.units.size();
+        if (pass == 0) hp.n_tc_units = n_unit;
     }
+    if (n_rows >= INT32_MAX / 2) return DENDRITE_ELIMIT;
+    hp.n_rows = (size_t)n_rows;
     hp.tiles = class_tiles[0] + class_tiles[1];
     partition_class(hp, 0, hp.n_tc_units, class_tiles[0], weight[0], max_tc_ctas, kTcWeights, hp.tc_cta_begin,
                     hp.tc_cta_unit);
@@ -847,7 +872,7 @@ size_t plan_layout(const HostPlan& hp, size_t (&off)[kPlanSections + 1]) {
         hp.units.size() * sizeof(AttnUnit), hp.cta_begin.size() * 4,
         hp.cta_unit.size() * 4,             hp.tc_cta_begin.size() * 4,
         hp.tc_cta_unit.size() * 4,          hp.path_off.size() * 4,
-        hp.path.size() * 4,                 hp.rows.size() * sizeof(AttnRow)};
+        hp.path.size() * 4,                 hp.n_rows * sizeof(AttnRow)};
     size_t b = 0;
     for (int k = 0; k < kPlanSections; ++k) {
         off[k] = b;
@@ -870,7 +895,7 @@ void plan_pack(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], char*
     put(6, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
     put(7, hp.path_off.data(), hp.path_off.size() * 4);
     put(8, hp.path.data(), hp.path.size() * 4);
-    put(9, hp.rows.data(), hp.rows.size() * sizeof(AttnRow));
+    // section 9 (rows) is written on the device by k_plan_rows
 }
 
 AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], const char* d, int32_t n,
@@ -895,6 +920,13 @@ AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1]
     v.n_q_heads = nq;
     v.group = group;
     return v;
+}
+
+int launch_plan_rows(const AttnPlanDev& pl, cudaStream_t s) {
+    if (pl.n_units == 0) return DENDRITE_OK;
+    const unsigned grid = (unsigned)std::min<int32_t>(pl.n_units, 2048);
+    k_plan_rows<<<grid, 128, 0, s>>>(pl);
+    return cudaGetLastError() == cudaSuccess ? DENDRITE_OK : DENDRITE_ECUDA;
 }
 
 // CTAs the tensor-core kernel may use on this pool (0: not used).
@@ -976,11 +1008,13 @@ int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows) {
     }
     if (plan_bytes > p->h_plan_cap) {
         size_t cap = std::max<size_t>(plan_bytes * 2, 1 << 20);
-        DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));
-        if (p->h_plan) cudaFreeHost(p->h_plan);
-        p->h_plan = nullptr;
+        for (int i = 0; i < 2; ++i) {
+            DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied[i]));
+            if (p->h_plan[i]) cudaFreeHost(p->h_plan[i]);
+            p->h_plan[i] = nullptr;
+        }
         p->h_plan_cap = 0;
-        DENDRITE_CUDA(cudaMallocHost(&p->h_plan, cap));
+        for (int i = 0; i < 2; ++i) DENDRITE_CUDA(cudaMallocHost(&p->h_plan[i], cap));
         p->h_plan_cap = cap;
     }
     if (partial_rows > p->partial_rows_cap) {
@@ -1026,10 +1060,12 @@ int attn_setup(dendrite_pool* p) {
 
 void attn_teardown(dendrite_pool* p) {
     if (p->d_plan) cudaFree(p->d_plan);
-    if (p->h_plan) cudaFreeHost(p->h_plan);
+    for (char*& h : p->h_plan) {
+        if (h) cudaFreeHost(h);
+        h = nullptr;
+    }
     if (p->d_partial) cudaFree(p->d_partial);
     p->d_plan = nullptr;
-    p->h_plan = nullptr;
     p->d_partial = nullptr;
 }
 
@@ -1074,17 +1110,23 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         size_t off[kPlanSections + 1];
         const size_t b = plan_layout(hp, off);
         DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
-        DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied));   // the pinned buffer is free again
-        plan_pack(hp, off, p->h_plan);
+        // two pinned buffers in turn: this build only waits for the upload
+        // of the build before the previous one
+        const int ib = p->plan_buf;
+        p->plan_buf ^= 1;
+        DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied[ib]));
+        plan_pack(hp, off, p->h_plan[ib]);
         {
-            const int64_t n16 = (int64_t)(b / 16);
+            // everything but the row records (the last section, built on the device)
+            const int64_t n16 = (int64_t)(off[kPlanSections - 1] / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
-            k_plan_upload<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(p->h_plan),
+            k_plan_upload<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(p->h_plan[ib]),
                                                reinterpret_cast<uint4*>(p->d_plan), n16);
             DENDRITE_CUDA(cudaGetLastError());
         }
-        DENDRITE_CUDA(cudaEventRecord(p->plan_copied, s));
+        DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
         pc.dev = plan_view(hp, off, p->d_plan, n, q_len, n_q_heads, n_q_heads / p->n_kv);
+        DENDRITE_TRY(launch_plan_rows(pc.dev, s));
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
         pc.version = p->version;
@@ -1191,9 +1233,11 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     const size_t ml_bytes = hp.partial_rows * sizeof(float2);
     if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
     plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));
-    DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, b, cudaMemcpyHostToDevice, s));
+    // everything but the row records (the last section, built on the device)
+    DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, off[kPlanSections - 1], cudaMemcpyHostToDevice, s));
     AttnArgs a = attn_args(p, 0, Q, out);
     a.plan = plan_view(hp, off, reinterpret_cast<const char*>(scratch), n, q_len, n_q_heads, n_q_heads / p->n_kv);
+    DENDRITE_TRY(launch_plan_rows(a.plan, s));
     a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);
     a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
     return launch_attention(p, 0, a, s, true);

@@ -220,9 +220,10 @@ struct dendrite_pool {
     // attention workspace (grow-only)
     char* d_plan = nullptr;
     size_t plan_cap = 0;
-    char* h_plan = nullptr;          // pinned
-    size_t h_plan_cap = 0;
-    cudaEvent_t plan_copied = nullptr;
+    char* h_plan[2] = {nullptr, nullptr};      // pinned, used alternately by plan builds
+    size_t h_plan_cap = 0;                     // capacity of each
+    cudaEvent_t plan_copied[2] = {nullptr, nullptr};
+    int plan_buf = 0;                          // buffer the next plan build packs into
     float* d_partial = nullptr;      // partial rows: [rows][head_dim] acc then [rows][2] (m, l)
     size_t partial_rows_cap = 0;
     dendrite::PlanCache plan;

@@ -32,8 +32,8 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
     segs.clear();
     members.clear();
     struct Rec { int32_t grp, cap, member; };
-    static thread_local std::vector<int32_t> slot, order, mem;
-    static thread_local std::vector<Rec> recs;
+    static thread_local std::vector<int32_t> slot, order, mem, count;
+    static thread_local std::vector<Rec> recs, sorted;
     slot.assign(n_nodes, -1);
     order.clear();
     recs.clear();
@@ -55,30 +55,51 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
             node = parent[node];
         }
     }
-    // group by owner (first-visit order), caps descending
-    std::sort(recs.begin(), recs.end(), [](const Rec& a, const Rec& b) {
-        if (a.grp != b.grp) return a.grp < b.grp;
-        if (a.cap != b.cap) return a.cap > b.cap;
-        return a.member < b.member;
-    });
-    for (size_t g0 = 0; g0 < recs.size();) {
-        size_t g1 = g0;
-        while (g1 < recs.size() && recs[g1].grp == recs[g0].grp) ++g1;
-        const int32_t node = order[recs[g0].grp];
+    // group by owner (first-visit order) with one counting pass; within a
+    // group the records stay in increasing member order
+    const int32_t n_grp = (int32_t)order.size();
+    count.assign(n_grp + 1, 0);
+    for (const Rec& r : recs) count[r.grp + 1]++;
+    for (int32_t g = 0; g < n_grp; ++g) count[g + 1] += count[g];
+    sorted.resize(recs.size());
+    {
+        static thread_local std::vector<int32_t> cursor;
+        cursor.assign(count.begin(), count.end() - 1);
+        for (const Rec& r : recs) sorted[cursor[r.grp]++] = r;
+    }
+    for (int32_t gi = 0; gi < n_grp; ++gi) {
+        const size_t g0 = count[gi], g1 = count[gi + 1];
+        const int32_t node = order[gi];
         const int32_t start = parent[node] >= 0 ? fork_len[node] / bs : 0;
-        // ascending cuts: the smallest cap first; members of [lo, cut) are the
-        // records with cap >= cut, i.e. a prefix of the group
+        bool uniform = true;
+        for (size_t k = g0 + 1; k < g1 && uniform; ++k) uniform = sorted[k].cap == sorted[g0].cap;
+        if (uniform) {   // every member reads [start, cap): one segment, members already in order
+            Segment sg;
+            sg.block_start = start;
+            sg.block_count = sorted[g0].cap - start;
+            sg.member_offset = (int32_t)members.size();
+            for (size_t k = g0; k < g1; ++k) members.push_back(sorted[k].member);
+            sg.n_members = (int32_t)(g1 - g0);
+            sg.rep_node = queried[sorted[g0].member];
+            segs.push_back(sg);
+            continue;
+        }
+        // caps descending (members ascending within a cap); the ascending
+        // cuts then take the smallest cap first, and the members of
+        // [lo, cut) are the records with cap >= cut, a prefix of the group
+        std::stable_sort(sorted.begin() + g0, sorted.begin() + g1,
+                         [](const Rec& a, const Rec& b) { return a.cap > b.cap; });
         int32_t lo = start;
         size_t end = g1;
         while (end > g0) {
-            const int32_t cut = recs[end - 1].cap;
+            const int32_t cut = sorted[end - 1].cap;
             if (cut > lo) {
                 Segment sg;
                 sg.block_start = lo;
                 sg.block_count = cut - lo;
                 sg.member_offset = (int32_t)members.size();
                 mem.clear();
-                for (size_t k = g0; k < end; ++k) mem.push_back(recs[k].member);
+                for (size_t k = g0; k < end; ++k) mem.push_back(sorted[k].member);
                 std::sort(mem.begin(), mem.end());
                 members.insert(members.end(), mem.begin(), mem.end());
                 sg.n_members = (int32_t)mem.size();
@@ -86,9 +107,8 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
                 segs.push_back(sg);
                 lo = cut;
             }
-            while (end > g0 && recs[end - 1].cap == cut) --end;
+            while (end > g0 && sorted[end - 1].cap == cut) --end;
         }
-        g0 = g1;
     }
 }
 

@@ -803,7 +803,8 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     for (int k = 0; k < T_COUNT; ++k)
         if (cudaEventCreate(&p->ev[k][0]) != cudaSuccess || cudaEventCreate(&p->ev[k][1]) != cudaSuccess)
             return fail(cuda_err(cudaErrorUnknown));
-    if (cudaEventCreateWithFlags(&p->plan_copied, cudaEventDisableTiming) != cudaSuccess)
+    if (cudaEventCreateWithFlags(&p->plan_copied[0], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->plan_copied[1], cudaEventDisableTiming) != cudaSuccess)
         return fail(cuda_err(cudaErrorUnknown));
     k_init<<<std::max(1, std::min(4 * p->sm_count, (int)((num_blocks + 255) / 256))), 256>>>(
         p->d_stack, p->d_refcount, p->d_holders, p->d_last, p->d_released, num_blocks, p->d_table,
@@ -831,7 +832,8 @@ int dendrite_pool_destroy(dendrite_pool* p) {
     for (int k = 0; k < T_COUNT; ++k)
         for (int j = 0; j < 2; ++j)
             if (p->ev[k][j]) cudaEventDestroy(p->ev[k][j]);
-    if (p->plan_copied) cudaEventDestroy(p->plan_copied);
+    for (cudaEvent_t e : p->plan_copied)
+        if (e) cudaEventDestroy(e);
     cudaGetLastError();
     delete p;
     return DENDRITE_OK;
