@@ -38,6 +38,13 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # ------------------------------------------------------------------ helpers
+
+# DRAM bytes (read + write) per launch of k_attn_partial_bf16 on this step,
+# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` over three
+# launches (profiles/attn_partial_bf16_beam.md); to be re-taken whenever that
+# kernel changes.
+BEAM_PARTIAL_TRAFFIC_BYTES = 169_690_000
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -346,7 +353,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
         "config": dict(config_of(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
         "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": BEAM_PARTIAL_TRAFFIC_BYTES,
                      "algorithmic_bytes": unique_kv + q_bytes, "kernel_ms": attn_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": world * n_queries / (e2e / 1e3), "unit": "branch-queries/s", "ms_per_step": e2e,
