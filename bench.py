@@ -345,7 +345,9 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
 
-    gpu_launches = 6 * args.steps   # fork 1 + append 2 (meta, copy) + attention 2 (partial, merge) + free 1
+    # fork 1 + append 2 (meta, copy) + attention 4 (the step's new tree needs a new
+    # plan: upload and row expansion, then partial and merge) + free 1
+    gpu_launches = 8 * args.steps
     line = {
         "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
         "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
@@ -463,7 +465,7 @@ def run_decode_layers(args):
                          "peak": peak, "peak_source": src, "unit": "GB/s",
                          "frac": unique / (pk / 1e3) / 1e9 / peak, "algorithmic_bytes": unique},
             "plan_us_layer0": plan_us[0], "plan_us_other_layers_max": max(plan_us[1:]),
-            "gpu_launches_per_step": 1 + 1 + NL * 3 + 1}
+            "gpu_launches_per_step": 1 + 1 + 2 + NL * 3 + 1}   # + plan upload and row expansion at layer 0
     if rank == 0:
         print(json.dumps(line), flush=True)
     pool.close()
