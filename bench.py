@@ -154,7 +154,7 @@ def config_of(w):
             "requests": m["requests"], "prefix_tokens": m["prefix"], "fork_width": m["width"],
             "divergent_tokens": m["divergent"], "branch_queries_per_step": len(w.query),
             "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
-            "block_size": w.block_size, "l2": "flushed between steps (256 MiB write)",
+            "block_size": w.block_size, "l2": "flushed before every step (read-only pass over 256 MiB)",
             "step": "fork + CoW append + tree decode attention + free"}
 
 
