@@ -85,10 +85,6 @@ constexpr int SMEM_TC = 1024 + OFF_BAR + B_COUNT * 8 + 16;
 static_assert(SMEM_TC <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.f;
-// The producer asks L2 for the tiles this many tiles beyond the stage it is
-// about to load, so that under full load the loads into the ring find their
-// data in L2 instead of waiting the whole DRAM latency in shared memory.
-constexpr int TC_PREFETCH_TILES = 16;
 
 // ------------------------------------------------------------- tcgen05 helpers
 // Shared-memory matrix descriptor, 128-byte swizzle: start >> 4 in bits
@@ -282,20 +278,6 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     nxt = nxt_base + lane < cend ? trow[nxt_base + lane] : 0;
                 }
                 int32_t blk = __shfl_sync(0xffffffffu, cur, (st - cur_base) + (lane & 3));
-                {
-                    const int32_t pst = st + TC_PREFETCH_TILES;
-                    const int idx = pst - cur_base + (lane & 3);   // < 64: inside cur or nxt
-                    const int32_t pa = __shfl_sync(0xffffffffu, cur, idx & 31);
-                    const int32_t pb = __shfl_sync(0xffffffffu, nxt, idx & 31);
-                    const int32_t pblk = idx < 32 ? pa : pb;
-                    if (k_role && lane < 4 && pst + lane < cend && (uint32_t)pblk < (uint32_t)a.n_blocks) {
-                        const int32_t prow = (pblk * a.n_kv + U.kv_head) * BS;
-                        tma_prefetch_3d(&tmK, 0, 0, prow);
-                        tma_prefetch_3d(&tmK, 0, 1, prow);
-                        tma_prefetch_3d(&tmV, 0, 0, prow);
-                        tma_prefetch_3d(&tmV, 0, 1, prow);
-                    }
-                }
                 const int slot = g % TC_NSTAGE;
                 const uint32_t ph = (uint32_t)(g / TC_NSTAGE) & 1u;
                 const int ntiles = min(4, cend - st);

@@ -84,3 +84,24 @@ def test_noalloc_rejects_work_beyond_its_scratch():
     assert _call(lib().dendrite_tree_attn_decode, pool, Q, kids, out) == 0
     pool.sync()
     pool.close()
+
+
+def test_noalloc_with_tensor_core_units_matches():
+    # 40 branches x G 4 = 160 rows per KV head on the prefix: tcgen05 class,
+    # whose plan section and partial rows live in the fixed array as well
+    w = W.beam(requests=1, prefix=400, width=40, divergent=11)
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    br = [h[b] for b in w.query]
+    Q = w.q("cuda")
+    ref = torch.empty_like(Q)
+    assert _call(lib().dendrite_tree_attn_decode, pool, Q, br, ref) == 0
+    assert pool.last_plan_stats()["n_tc_units"] == 8
+    for _ in range(2):
+        got = torch.full_like(Q, float("nan"))
+        assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, got) == 0
+        torch.cuda.synchronize()
+        assert torch.isfinite(got.float()).all()
+        assert (got.float() - ref.float()).abs().max().item() <= TOL
+    pool.sync()
+    pool.close()
