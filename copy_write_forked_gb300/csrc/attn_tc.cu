@@ -403,9 +403,30 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         unsigned char* sQ = sm + OFF_Q + r * TC_QTILE;
         unsigned char* sP = sm + OFF_P + r * TC_PBUF;
         const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
+        const int row = r * 128 + trow;
+        // This thread's row of a unit's Q into the K-major swizzled tile, and
+        // the row's record.  A unit's Q is staged as soon as the previous
+        // chunk's last S was read (no S MMA of it is pending then), before
+        // that chunk's epilogue, so the next chunk's S overlaps the epilogue.
+        auto stage_q = [&](const AttnUnit& V) -> AttnRow {
+            const bool v_ok = row < V.n_rows;
+            const AttnRow RR = v_ok ? pl.rows[V.row_off + row] : AttnRow{0, 0};
+            const uint4* q = reinterpret_cast<const uint4*>(Q + (int64_t)RR.q_row * D);
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint4 v = v_ok ? __ldg(q + ch) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sQ + (ch >> 3) * 16384 + trow * 128 + (((ch & 7) ^ (trow & 7)) << 4)) = v;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_Q_FULL + r));
+            return RR;
+        };
         int32_t js = 0;
         bool ok = true;
         int32_t t = t_begin, u = u0;
+        int32_t staged_u = -1;      // unit whose Q is already in the tile
+        AttnRow staged_R{0, 0};
         while (ok && t < t_end) {
             const AttnUnit U = pl.units[u];
             const int32_t uend = U.tile_off + U.n_blk;
@@ -416,22 +437,8 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 ++u;
                 continue;
             }
-            const int row = r * 128 + trow;
             const bool valid = row < U.n_rows;
-            const AttnRow R = valid ? pl.rows[U.row_off + row] : AttnRow{0, 0};
-            // this row of Q into the K-major swizzled tile (the previous
-            // chunk's MMAs all finished: its last PV was waited for)
-            {
-                const uint4* q = reinterpret_cast<const uint4*>(Q + (int64_t)R.q_row * D);
-#pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    const uint4 v = valid ? __ldg(q + ch) : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(sQ + (ch >> 3) * 16384 + trow * 128 + (((ch & 7) ^ (trow & 7)) << 4)) = v;
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_Q_FULL + r));
-            }
+            const AttnRow R = staged_u == u ? staged_R : stage_q(U);
             const int32_t nst = (cend - t + 3) >> 2;
             float m_ref = -INFINITY, l = 0.f;
             for (int32_t k = 0; k < nst && ok; ++k, ++js) {
@@ -537,6 +544,22 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 if (lane == 0) mbar_arrive(bar(B_P_FULL + r));
             }
             if (!ok) break;
+            // the next chunk this row tile works on: stage its Q now
+            {
+                int32_t t2 = cend, u2 = u + 1;
+                while (t2 < t_end) {
+                    const AttnUnit& V = pl.units[u2];
+                    const int32_t e2 = V.tile_off + V.n_blk;
+                    if (t2 >= e2) { ++u2; continue; }
+                    if (r < V.rt) break;
+                    t2 = min(t_end, e2);
+                    ++u2;
+                }
+                if (t2 < t_end) {
+                    staged_R = stage_q(pl.units[u2]);
+                    staged_u = u2;
+                }
+            }
             // chunk done: O after the last PV -> partial row
             ok = warp_wait(bar(B_PV_DONE + r), (uint32_t)(js - 1) & 1u, abortp, a.meta);
             if (!ok) break;
