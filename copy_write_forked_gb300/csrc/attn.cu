@@ -935,9 +935,11 @@ int tc_ctas(const dendrite_pool* p) {
 }
 
 // The partial kernels of one attention call (tensor-core class, then the
-// mma.sync or fp32 class), then the merge.  pdl_small: launch the mma.sync
-// kernel with programmatic stream serialisation.
-int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStream_t s, bool pdl_small) {
+// mma.sync or fp32 class), then the merge.  The mma.sync, fp32 and merge
+// kernels are launched with programmatic stream serialisation: their
+// prologues overlap the previous kernel's tail, and they wait for its results
+// (griddepcontrol.wait) before reading anything.
+int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStream_t s) {
     const bool bf16 = p->dtype == DENDRITE_BF16;
     prof_begin(p, T_ATTN_TOTAL, s);
     prof_begin(p, T_ATTN_PARTIAL, s);
@@ -955,11 +957,7 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     }
     if (a.plan.n_ctas > 0) {
         if (bf16) {
-            if (pdl_small)
-                DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk,
-                                         mv, a));
-            else
-                k_attn_partial_bf16<<<a.plan.n_ctas, THREADS, SMEM_BF16, s>>>(mk, mv, a);
+            DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
         } else {
             DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(a.plan.n_ctas), dim3(128),
                                      2 * BS * p->head_dim * sizeof(float), s, a));
@@ -1149,7 +1147,7 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
     a.plan = pc.dev;
     a.part_acc = p->d_partial;
     a.part_ml = reinterpret_cast<float2*>(p->d_partial + p->partial_rows_cap * p->head_dim);
-    return launch_attention(p, layer, a, s, false);
+    return launch_attention(p, layer, a, s);
 }
 
 extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* out) {
@@ -1240,5 +1238,5 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     DENDRITE_TRY(launch_plan_rows(a.plan, s));
     a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);
     a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
-    return launch_attention(p, 0, a, s, true);
+    return launch_attention(p, 0, a, s);
 }
