@@ -1240,3 +1240,35 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
     return launch_attention(p, 0, a, s);
 }
+
+// ====================================================== bounded-wait self-test
+// One thread waits on an mbarrier that nothing arrives at, through the same
+// bounded wait the attention kernels use.  The wait gives up after its time
+// limit and the pool records DENDRITE_ETIMEOUT; the device itself never
+// faults or hangs.
+namespace {
+
+__global__ void k_wait_selftest(DevMeta* meta) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, &abort_flag))
+        atomicCAS(&meta->status, 0, DENDRITE_ETIMEOUT);
+}
+
+}  // namespace
+
+extern "C" int dendrite_selftest_bounded_wait(dendrite_pool* p, void* stream) {
+    if (!p) return DENDRITE_EINVAL;
+    if (p->poisoned) return p->poisoned;
+    DENDRITE_CUDA(cudaSetDevice(p->device));
+    k_wait_selftest<<<1, 32, 0, (cudaStream_t)stream>>>(p->d_meta);
+    DENDRITE_CUDA(cudaGetLastError());
+    return DENDRITE_OK;
+}
+

@@ -69,6 +69,7 @@ _SIGS = {
     "dendrite_tree_attn_decode_layer": [_p, _i32, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_read_block_layer": [_p, _i32, _i32, _p, _p, _p],
     "dendrite_pool_layers": [_p, _pi32],
+    "dendrite_selftest_bounded_wait": [_p, _p],
     "dendrite_tree_attn_decode": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_tree_attn_decode_noalloc": [_p, _p, _i32, _i32, _pi32, _i32, _p, _p],
     "dendrite_free": [_p, _pi32, _i32, _p],

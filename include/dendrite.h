@@ -244,6 +244,16 @@ int dendrite_read_block(dendrite_pool* pool, int32_t block, void* k_out, void* v
 int dendrite_read_block_layer(dendrite_pool* pool, int32_t layer, int32_t block, void* k_out, void* v_out,
                               void* stream);
 
+/*
+ * Test hook for the device-side failure handling (no counterpart on the
+ * pages): launches one thread that waits on an mbarrier nothing arrives at,
+ * through the bounded wait every attention kernel uses (about 2 s of
+ * %globaltimer).  When it gives up the pool records DENDRITE_ETIMEOUT, which
+ * dendrite_sync then returns and every later call of the pool reports (the
+ * pool is poisoned).  The device and the CUDA context stay usable.
+ */
+int dendrite_selftest_bounded_wait(dendrite_pool* pool, void* stream);
+
 /* Number of layers the pool holds. */
 int dendrite_pool_layers(dendrite_pool* pool, int32_t* n_layers);
 
