@@ -475,8 +475,11 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
 //     M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum acc_i 2^(m_i - M) / L
 // with the acc rows fetched four partials at a time.  Partial rows are read
 // through L2 only (they were written by the previous kernel).
-template <typename T>
-__global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
+// WIDE (head_dim 128): lane l owns columns 4 l .. 4 l + 3, so a partial row is
+// one 16-byte load per lane, eight partials are in flight per warp, and four
+// CTAs fit on an SM.
+template <typename T, bool WIDE>
+__global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const AttnPlanDev& pl = a.plan;
     const int lane = threadIdx.x & 31;
@@ -543,26 +546,61 @@ __global__ void __launch_bounds__(256) k_attn_merge(const AttnArgs a) {
             for (int k = 0; k < 8; ++k) acc[k] *= sc;
             M = Mn;
             const int nb = min(32, total - p0);
-            for (int q = 0; q < nb; q += 4) {
-                float wq[4];
-                float v[4][8];
+            if constexpr (WIDE) {
+                for (int q = 0; q < nb; q += 8) {
+                    float wq[8];
+                    float4 v[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int src = min(q + u, nb - 1);
-                    const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
-                    wq[u] = (q + u < nb) ? __shfl_sync(0xffffffffu, w, src) : 0.f;
-                    const float* row = a.part_acc + (int64_t)pr * d;
+                    for (int u = 0; u < 8; ++u) {
+                        const int src = min(q + u, nb - 1);
+                        const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
+                        const float ww = __shfl_sync(0xffffffffu, w, src);
+                        wq[u] = q + u < nb ? ww : 0.f;
+                        v[u] = q + u < nb ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)pr * D) + lane)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[u][k] = k < nj ? __ldcg(row + lane + 32 * k) : 0.f;
+                    for (int u = 0; u < 8; ++u) {
+                        acc[0] = fmaf(v[u].x, wq[u], acc[0]);
+                        acc[1] = fmaf(v[u].y, wq[u], acc[1]);
+                        acc[2] = fmaf(v[u].z, wq[u], acc[2]);
+                        acc[3] = fmaf(v[u].w, wq[u], acc[3]);
+                    }
                 }
+            } else {
+                for (int q = 0; q < nb; q += 4) {
+                    float wq[4];
+                    float v[4][8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 4; ++u) {
+                        const int src = min(q + u, nb - 1);
+                        const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
+                        wq[u] = (q + u < nb) ? __shfl_sync(0xffffffffu, w, src) : 0.f;
+                        const float* row = a.part_acc + (int64_t)pr * d;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) acc[k] = fmaf(v[u][k], wq[u], acc[k]);
+                        for (int k = 0; k < 8; ++k) v[u][k] = k < nj ? __ldcg(row + lane + 32 * k) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) acc[k] = fmaf(v[u][k], wq[u], acc[k]);
+                }
             }
         }
     }
     const float inv = 1.f / L;
+    if constexpr (WIDE) {
+        T* dst = static_cast<T*>(a.out) + (int64_t)o * D + 4 * lane;
+        if constexpr (sizeof(T) == 2) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        } else {
+            *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        }
+        return;
+    }
     T* dst = static_cast<T*>(a.out) + (int64_t)o * d;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -968,8 +1006,9 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     {
         const int32_t n_out = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
         const unsigned grid = (unsigned)((n_out + 7) / 8);
-        if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, a));
-        else DENDRITE_CUDA(launch_pdl(k_attn_merge<float>, dim3(grid), dim3(256), 0, s, a));
+        if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16, true>, dim3(grid), dim3(256), 0, s, a));
+        else if (p->head_dim == D) DENDRITE_CUDA(launch_pdl(k_attn_merge<float, true>, dim3(grid), dim3(256), 0, s, a));
+        else DENDRITE_CUDA(launch_pdl(k_attn_merge<float, false>, dim3(grid), dim3(256), 0, s, a));
     }
     prof_end(p, T_ATTN_MERGE, s);
     prof_end(p, T_ATTN_TOTAL, s);
