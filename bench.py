@@ -493,7 +493,7 @@ def run_attention_only(args):
     g.build()
     from copy_write_forked_gb300.runner import pool_for, run_script
     w, desc = other_workload(args.workload)
-    pool = pool_for(w, tc_min_rows=args.tc_min_rows)
+    pool = pool_for(w, tc_min_rows=args.tc_min_rows, fold_segments=args.fold_segments)
     h = run_script(pool, w, device=dev)
     br = [h[b] for b in w.query]
     Q = w.q(dev)
@@ -699,6 +699,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
+    ap.add_argument("--fold-segments", type=int, default=0,
+                    help="fold short shared segments into the ones that follow (0: default, k: below k percent "
+                         "of the estimate, -1: off)")
     ap.add_argument("--workload", default="beam", choices=["beam", "mcts", "specverify", "stress", "decode32"],
                     help="beam = the full-path step (default JSON line); others time tree attention only")
     args = ap.parse_args()

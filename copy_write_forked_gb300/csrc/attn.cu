@@ -762,6 +762,12 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     for (int32_t i = 0; i < n; ++i) hp.queried[i] = p->br[branches[i]].node;
     plan_segments(n_nodes, hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
                   hp.psegs, hp.seg_members);
+    // distinct tiles: the sharing segments before folding read each (block,
+    // kv head) pair once
+    for (const Segment& sg : hp.psegs) hp.unique_tiles += (int64_t)sg.block_count * nkv;
+    if (p->fold_pct >= 0)
+        fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, hp.queried.data(), n,
+                      hp.psegs, hp.seg_members);
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by
     // more than tc_min_rows rows per kv head, pass 1 the rest.  The unit and
@@ -803,7 +809,6 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
                 const int32_t qi = hp.seg_members[sg.member_offset + k];
                 mp[n_mem++] = AttnMember{qi, p->br[branches[qi]].len};
             }
-            hp.unique_tiles += (int64_t)sg.block_count * nkv;
             const int32_t seg_index = (int32_t)hp.segs.size();
             for (int32_t h = 0; h < nkv; ++h) {
                 for (int32_t grp = 0; grp < S.ngroups; ++grp) {

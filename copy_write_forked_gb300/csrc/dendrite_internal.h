@@ -21,6 +21,7 @@ constexpr int kMaxUnitRowsBf16 = 64;  // rows per mma.sync attention unit (4 row
 constexpr int kMaxUnitRowsF32 = 16;
 constexpr int kMaxUnitRowsTc = 256;   // rows per tcgen05 attention unit (2 row tiles of 128)
 constexpr int kTcMinRowsDefault = 64; // segments with more rows per kv head use the tcgen05 kernel
+constexpr int32_t kFoldPctDefault = 100;  // fold a segment when that is estimated cheaper
 constexpr int kAppendMetaThreads = 1024;
 constexpr int kFreeCollectThreads = 1024;
 
@@ -194,6 +195,7 @@ struct dendrite_pool {
     int sm_count = 0;
     int attn_ctas_per_sm = 1;
     int32_t tc_min_rows = dendrite::kTcMinRowsDefault;   // < 0: tensor-core attention kernel off
+    int32_t fold_pct = dendrite::kFoldPctDefault;        // < 0: segments are never folded
 
     // device state
     void* d_k = nullptr;
@@ -283,6 +285,19 @@ struct Segment {
 void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
                    const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
                    std::vector<Segment>& segs, std::vector<int32_t>& members);
+// How the attention plan will split a segment's rows, for the folding estimate:
+// more than tc_rows rows per kv head (tc_rows < 0: never) go to the tcgen05
+// kernel in groups of 256, the others to the small-row kernel in groups of
+// small_rows.  fold_pct: fold when the estimate after folding is below this
+// percentage of the estimate before.
+struct FoldParams {
+    int32_t rows_per_member;
+    int32_t tc_rows;
+    int32_t small_rows;
+    int32_t fold_pct;
+};
+void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queried, std::vector<Segment>& segs,
+                   std::vector<int32_t>& members);
 
 // Attention (attn.cu)
 int attn_setup(dendrite_pool* p);      // tensor maps, occupancy

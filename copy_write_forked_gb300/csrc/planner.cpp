@@ -112,14 +112,160 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
     }
 }
 
+
+// Folding.  Every segment costs each of its rows a partial (max, sum, acc) row,
+// written by a partial kernel and read again by the merge, plus a fresh load of
+// the row's query, and each of its row groups a unit start.  In a deep tree of
+// short nodes (MCTS: 32 tokens a node) most segments are two blocks long and
+// these per-row and per-unit costs outweigh the reading of the blocks.  Folding
+// a segment s lets every segment that follows s in some member's path read s's
+// range again with its own rows: each following segment is extended down to
+// s's first block, s's own units and partial rows disappear, and its blocks are
+// read once per following segment (mostly from L2, as the units of those
+// segments run next to one another).  Members whose path ends in s keep a
+// segment of their own over s's range.  The segments still read every
+// (member, block) pair exactly once, and each is still read through one
+// physical block per position for all its members, because every member of a
+// following segment is a member of s.  Decisions run in increasing block
+// order, so a segment's range already includes what was folded into it when
+// its own turn comes.
+namespace {
+
+// Estimated SM time, in ns, of one kv head's row group of `rows` rows: per
+// 16-token block, and per unit (start, query load, partial rows written and
+// merged).  Fitted to per-CTA timelines of the partial kernels on GB300.
+int64_t group_block_ns(bool tc, int32_t rows) {
+    if (tc) return rows <= 128 ? 275 : 325;
+    const int32_t rt = rows <= 16 ? 1 : rows <= 32 ? 2 : 4;
+    return 60 * (1 + rt);
+}
+int64_t group_unit_ns(bool tc, int32_t rows) { return (tc ? 3000 : 1000) + 29 * (int64_t)rows; }
+
+// Estimate for R rows over T blocks, split into row groups as the plan splits
+// them; with_units adds the per-unit part.
+int64_t estimate_ns(const FoldParams& fp, int64_t T, int64_t R, bool with_units) {
+    const bool tc = fp.tc_rows >= 0 && R > fp.tc_rows;
+    const int32_t g = tc ? kMaxUnitRowsTc : fp.small_rows;
+    int64_t ns = 0;
+    for (int64_t r0 = 0; r0 < R; r0 += g) {
+        const int32_t rows = (int32_t)std::min<int64_t>(g, R - r0);
+        ns += T * group_block_ns(tc, rows) + (with_units ? group_unit_ns(tc, rows) : 0);
+    }
+    return ns;
+}
+
+}  // namespace
+
+void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queried, std::vector<Segment>& segs,
+                   std::vector<int32_t>& members) {
+    const int32_t S = (int32_t)segs.size();
+    if (fp.fold_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
+    static thread_local std::vector<int32_t> moff, mseg, prev, koff, kseg, eoff, emem, order, ext;
+    static thread_local std::vector<char> folded;
+    // every member's segments, in block order
+    moff.assign(n_queried + 1, 0);
+    for (const Segment& sg : segs)
+        for (int32_t k = 0; k < sg.n_members; ++k) moff[members[sg.member_offset + k] + 1]++;
+    for (int32_t q = 0; q < n_queried; ++q) moff[q + 1] += moff[q];
+    mseg.resize(moff[n_queried]);
+    {
+        static thread_local std::vector<int32_t> cur;
+        cur.assign(moff.begin(), moff.end() - 1);
+        for (int32_t si = 0; si < S; ++si)
+            for (int32_t k = 0; k < segs[si].n_members; ++k) mseg[cur[members[segs[si].member_offset + k]]++] = si;
+    }
+    for (int32_t q = 0; q < n_queried; ++q)
+        std::sort(mseg.begin() + moff[q], mseg.begin() + moff[q + 1],
+                  [&](int32_t a, int32_t b) { return segs[a].block_start < segs[b].block_start; });
+    // the segment before each segment (the same for all its members), the
+    // segments after each segment, and the members whose path ends there
+    prev.assign(S, -1);
+    koff.assign(S + 1, 0);
+    eoff.assign(S + 1, 0);
+    for (int32_t q = 0; q < n_queried; ++q) {
+        for (int32_t e = moff[q] + 1; e < moff[q + 1]; ++e) prev[mseg[e]] = mseg[e - 1];
+        if (moff[q + 1] > moff[q]) eoff[mseg[moff[q + 1] - 1] + 1]++;
+    }
+    for (int32_t si = 0; si < S; ++si)
+        if (prev[si] >= 0) koff[prev[si] + 1]++;
+    for (int32_t si = 0; si < S; ++si) {
+        koff[si + 1] += koff[si];
+        eoff[si + 1] += eoff[si];
+    }
+    kseg.resize(koff[S]);
+    emem.resize(eoff[S]);
+    {
+        static thread_local std::vector<int32_t> kc, ec;
+        kc.assign(koff.begin(), koff.end() - 1);
+        ec.assign(eoff.begin(), eoff.end() - 1);
+        for (int32_t si = 0; si < S; ++si)
+            if (prev[si] >= 0) kseg[kc[prev[si]]++] = si;
+        for (int32_t q = 0; q < n_queried; ++q)   // ascending member order
+            if (moff[q + 1] > moff[q]) emem[ec[mseg[moff[q + 1] - 1]]++] = q;
+    }
+    // decide in increasing block order
+    order.resize(S);
+    for (int32_t si = 0; si < S; ++si) order[si] = si;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int32_t a, int32_t b) { return segs[a].block_start < segs[b].block_start; });
+    ext.resize(S);
+    for (int32_t si = 0; si < S; ++si) ext[si] = segs[si].block_start;
+    folded.assign(S, 0);
+    const int64_t rpm = fp.rows_per_member;
+    bool any = false;
+    for (const int32_t si : order) {
+        if (koff[si + 1] == koff[si]) continue;   // nothing follows it
+        const Segment& sg = segs[si];
+        const int64_t T = (int64_t)sg.block_start + sg.block_count - ext[si];
+        const int64_t keep = estimate_ns(fp, T, sg.n_members * rpm, true);
+        int64_t fold = 0;
+        for (int32_t k = koff[si]; k < koff[si + 1]; ++k)
+            fold += estimate_ns(fp, T, segs[kseg[k]].n_members * rpm, false);
+        if (eoff[si + 1] > eoff[si]) fold += estimate_ns(fp, T, (eoff[si + 1] - eoff[si]) * rpm, true);
+        if (fold * 100 < keep * fp.fold_pct) {
+            folded[si] = 1;
+            any = true;
+            for (int32_t k = koff[si]; k < koff[si + 1]; ++k) ext[kseg[k]] = ext[si];
+        }
+    }
+    if (!any) return;
+    // rebuild in the original order; a folded segment's place goes to the
+    // segment of the members that end in it, if any
+    static thread_local std::vector<Segment> out;
+    static thread_local std::vector<int32_t> out_members;
+    out.clear();
+    out_members.clear();
+    for (int32_t si = 0; si < S; ++si) {
+        const Segment& sg = segs[si];
+        const int32_t end = sg.block_start + sg.block_count;
+        Segment o;
+        o.block_start = ext[si];
+        o.block_count = end - ext[si];
+        o.member_offset = (int32_t)out_members.size();
+        if (!folded[si]) {
+            o.rep_node = sg.rep_node;
+            o.n_members = sg.n_members;
+            out_members.insert(out_members.end(), members.begin() + sg.member_offset,
+                               members.begin() + sg.member_offset + sg.n_members);
+        } else {
+            if (eoff[si + 1] == eoff[si]) continue;
+            o.rep_node = queried[emem[eoff[si]]];
+            o.n_members = eoff[si + 1] - eoff[si];
+            out_members.insert(out_members.end(), emem.begin() + eoff[si], emem.begin() + eoff[si + 1]);
+        }
+        out.push_back(o);
+    }
+    segs.swap(out);
+    members.swap(out_members);
+}
+
 }  // namespace dendrite
 
-extern "C" int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
-                                      const int32_t* len, int32_t block_size,
-                                      const int32_t* queried, int32_t n_queried,
-                                      dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
-                                      int32_t* members, int32_t member_cap, int32_t* n_members) {
-    if (n_nodes < 0 || n_queried < 0 || block_size <= 0 || !n_segs || !n_members) return DENDRITE_EINVAL;
+namespace {
+
+int check_forest(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len, const int32_t* len,
+                 int32_t block_size, const int32_t* queried, int32_t n_queried) {
+    if (n_nodes < 0 || n_queried < 0 || block_size <= 0) return DENDRITE_EINVAL;
     if (n_nodes > 0 && (!parent || !fork_len || !len)) return DENDRITE_EINVAL;
     if (n_queried > 0 && !queried) return DENDRITE_EINVAL;
     for (int32_t i = 0; i < n_nodes; ++i) {
@@ -137,9 +283,11 @@ extern "C" int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, co
         if (queried[q] < 0 || queried[q] >= n_nodes || seen[queried[q]]) return DENDRITE_EINVAL;
         seen[queried[q]] = 1;
     }
-    std::vector<dendrite::Segment> s;
-    std::vector<int32_t> m;
-    dendrite::plan_segments(n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
+    return DENDRITE_OK;
+}
+
+int export_segments(const std::vector<dendrite::Segment>& s, const std::vector<int32_t>& m, dendrite_segment* segs,
+                    int32_t seg_cap, int32_t* n_segs, int32_t* members, int32_t member_cap, int32_t* n_members) {
     *n_segs = (int32_t)s.size();
     *n_members = (int32_t)m.size();
     if ((int32_t)s.size() > seg_cap || (int32_t)m.size() > member_cap) return DENDRITE_ELIMIT;
@@ -152,4 +300,37 @@ extern "C" int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, co
     }
     if (!m.empty()) std::memcpy(members, m.data(), m.size() * sizeof(int32_t));
     return DENDRITE_OK;
+}
+
+}  // namespace
+
+extern "C" int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                                      const int32_t* len, int32_t block_size,
+                                      const int32_t* queried, int32_t n_queried,
+                                      dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
+                                      int32_t* members, int32_t member_cap, int32_t* n_members) {
+    if (!n_segs || !n_members) return DENDRITE_EINVAL;
+    DENDRITE_TRY(check_forest(n_nodes, parent, fork_len, len, block_size, queried, n_queried));
+    std::vector<dendrite::Segment> s;
+    std::vector<int32_t> m;
+    dendrite::plan_segments(n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
+    return export_segments(s, m, segs, seg_cap, n_segs, members, member_cap, n_members);
+}
+
+extern "C" int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                                             const int32_t* len, int32_t block_size,
+                                             const int32_t* queried, int32_t n_queried,
+                                             int32_t rows_per_member, int32_t tc_min_rows, int32_t fold_pct,
+                                             dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
+                                             int32_t* members, int32_t member_cap, int32_t* n_members) {
+    if (!n_segs || !n_members || rows_per_member <= 0 || tc_min_rows < -1 || fold_pct < -1) return DENDRITE_EINVAL;
+    DENDRITE_TRY(check_forest(n_nodes, parent, fork_len, len, block_size, queried, n_queried));
+    std::vector<dendrite::Segment> s;
+    std::vector<int32_t> m;
+    dendrite::plan_segments(n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
+    const dendrite::FoldParams fp{rows_per_member, tc_min_rows == 0 ? dendrite::kTcMinRowsDefault : tc_min_rows,
+                                  dendrite::kMaxUnitRowsBf16,
+                                  fold_pct == 0 ? dendrite::kFoldPctDefault : fold_pct};
+    dendrite::fold_segments(fp, queried, n_queried, s, m);
+    return export_segments(s, m, segs, seg_cap, n_segs, members, member_cap, n_members);
 }

@@ -43,7 +43,7 @@ class DendriteError(RuntimeError):
 
 class _Opts(ctypes.Structure):
     _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("tc_min_rows", _i32),
-                ("n_layers", _i32), ("reserved", _i32 * 4)]
+                ("n_layers", _i32), ("fold_segments", _i32), ("reserved", _i32 * 3)]
 
 
 class _PlanStats(ctypes.Structure):
@@ -86,6 +86,8 @@ _SIGS = {
     "dendrite_last_plan_stats": [_p, ctypes.POINTER(_PlanStats)],
     "dendrite_plan_segments": [_i32, _pi32, _pi32, _pi32, _i32, _pi32, _i32, ctypes.POINTER(_Segment), _i32,
                                _pi32, _pi32, _i32, _pi32],
+    "dendrite_plan_segments_folded": [_i32, _pi32, _pi32, _pi32, _i32, _pi32, _i32, _i32, _i32, _i32,
+                                      ctypes.POINTER(_Segment), _i32, _pi32, _pi32, _i32, _pi32],
 }
 
 
@@ -146,14 +148,16 @@ class Pool:
 
     def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
                  dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
-                 max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0, n_layers: int = 1):
+                 max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0, n_layers: int = 1,
+                 fold_segments: int = 0):
         if dtype not in _DT:
             raise DendriteError(-5, f"dtype {dtype}")
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
                                    torch.device(device).index or 0)
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
-        opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows), int(n_layers))
+        opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows), int(n_layers),
+                     int(fold_segments))
         self.n_layers = int(n_layers)
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
@@ -346,21 +350,27 @@ class Pool:
 
 
 def plan_segments(parent: Sequence[int], fork_len: Sequence[int], length: Sequence[int], block_size: int,
-                  queried: Sequence[int]):
-    """Host planner (no GPU): returns a list of (rep, block_start, block_count, members)."""
+                  queried: Sequence[int], rows_per_member: int = 0, tc_min_rows: int = 0, fold_pct: int = 0):
+    """Host planner (no GPU): returns a list of (rep, block_start, block_count, members).
+    rows_per_member > 0: the folded segments the bf16 attention call reads
+    (dendrite_plan_segments_folded), else the maximal sharing segments."""
     n = len(parent)
     ns, nm = ctypes.c_int32(), ctypes.c_int32()
     L = lib()
     pa, fa, la, qa = _arr(parent), _arr(fork_len), _arr(length), _arr(queried)
-    rc = L.dendrite_plan_segments(n, _ptr(pa), _ptr(fa), _ptr(la), block_size, _ptr(qa),
-                                  len(queried), None, 0, ctypes.addressof(ns), None, 0, ctypes.addressof(nm))
+    head = (n, _ptr(pa), _ptr(fa), _ptr(la), block_size, _ptr(qa), len(queried))
+    if rows_per_member > 0:
+        fn, name = L.dendrite_plan_segments_folded, "plan_segments_folded"
+        head = head + (int(rows_per_member), int(tc_min_rows), int(fold_pct))
+    else:
+        fn, name = L.dendrite_plan_segments, "plan_segments"
+    rc = fn(*head, None, 0, ctypes.addressof(ns), None, 0, ctypes.addressof(nm))
     if rc not in (0, -4):
-        _check(rc, "plan_segments")
+        _check(rc, name)
     segs = (_Segment * max(1, ns.value))()
     mem = (ctypes.c_int32 * max(1, nm.value))()
-    _check(L.dendrite_plan_segments(n, _ptr(pa), _ptr(fa), _ptr(la), block_size, _ptr(qa),
-                                    len(queried), segs, ns.value, ctypes.addressof(ns), ctypes.addressof(mem),
-                                    nm.value, ctypes.addressof(nm)), "plan_segments")
+    _check(fn(*head, segs, ns.value, ctypes.addressof(ns), ctypes.addressof(mem), nm.value, ctypes.addressof(nm)),
+           name)
     out = []
     for s in segs[:ns.value]:
         out.append((s.rep, s.block_start, s.block_count, list(mem[s.member_offset:s.member_offset + s.n_members])))

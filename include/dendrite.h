@@ -77,7 +77,14 @@ typedef struct dendrite_pool_opts {
     int32_t n_layers;              /* model layers held (0 = 1): every layer has its own  *
                                     * K and V pools; block ids, tables, refcounts and the *
                                     * free stack are shared by all layers.                */
-    int32_t reserved[4];           /* must be zero                                         */
+    int32_t fold_segments;         /* attention planning: a short sharing segment whose   *
+                                    * rows continue into several longer ones is read      *
+                                    * again by each of them instead of producing partial  *
+                                    * rows of its own, when an estimate of the kernels'   *
+                                    * time says that is cheaper.  0 = default (fold when  *
+                                    * the estimate drops); k > 0 = fold when it drops     *
+                                    * below k percent; -1 = never.                        */
+    int32_t reserved[3];           /* must be zero                                         */
 } dendrite_pool_opts;
 
 /*
@@ -317,6 +324,31 @@ int dendrite_plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t
                            const int32_t* queried, int32_t n_queried,
                            dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
                            int32_t* members, int32_t member_cap, int32_t* n_members);
+
+/*
+ * The segments the bf16 attention call actually reads: those of
+ * dendrite_plan_segments after folding (pool option fold_segments).  A
+ * segment s is folded when the segments that follow it in its members' block
+ * order (each holding a subset of s's members) are estimated to read s's
+ * blocks again with their own rows faster than s's own row groups cost: every
+ * following segment is then extended down to s's first block, and the members
+ * whose blocks end in s keep a segment over s's range.  The result still has
+ * each queried branch read each of its logical blocks exactly once, and every
+ * position of a segment is the same physical block for all its members; it is
+ * no longer maximal.
+ *   rows_per_member  query rows per KV head of one member (q_len x GQA group), > 0.
+ *   tc_min_rows      as the pool option (0 = default, -1 = no tcgen05 class).
+ *   fold_pct         as the pool option fold_segments (0 = default, -1 = never).
+ * Other arguments, results and errors as dendrite_plan_segments; segments keep
+ * their order, a folded segment's place going to the segment of the members
+ * that end in it, if any.
+ */
+int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                                  const int32_t* len, int32_t block_size,
+                                  const int32_t* queried, int32_t n_queried,
+                                  int32_t rows_per_member, int32_t tc_min_rows, int32_t fold_pct,
+                                  dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
+                                  int32_t* members, int32_t member_cap, int32_t* n_members);
 
 /* ------------------------------------------------- allocation-free variant
  * No counterpart on the pages: this entry point exists for callers that must
