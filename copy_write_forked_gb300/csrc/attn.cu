@@ -485,7 +485,10 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
     const int lane = threadIdx.x & 31;
     const int32_t o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int32_t n_out = pl.n_queried * pl.q_len * pl.n_q_heads;
-    if (o >= n_out || a.meta->status) return;
+    if (o >= n_out) return;
+    // the status word is checked only before the store, so that its load
+    // overlaps the plan loads (the plan is always readable)
+    const int32_t status = *reinterpret_cast<volatile const int32_t*>(&a.meta->status);
     const int G = pl.group;
     const int32_t qi = o / (pl.q_len * pl.n_q_heads);
     const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
@@ -529,6 +532,17 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
             const int32_t ex = __shfl_sync(0xffffffffu, excl, ent);
             const bool valid = pidx < total;
             const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
+            const int nb = min(32, total - p0);
+            // the first eight acc rows go out with the (m, l) loads
+            float4 v[8];
+            if constexpr (WIDE) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int32_t pr = __shfl_sync(0xffffffffu, prow, min(u, nb - 1));
+                    v[u] = u < nb ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)pr * D) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
             float2 ml = valid ? __ldcg(a.part_ml + prow) : make_float2(-INFINITY, 0.f);
             // running max over this batch
             float mb = ml.x;
@@ -545,19 +559,20 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
 #pragma unroll
             for (int k = 0; k < 8; ++k) acc[k] *= sc;
             M = Mn;
-            const int nb = min(32, total - p0);
             if constexpr (WIDE) {
                 for (int q = 0; q < nb; q += 8) {
                     float wq[8];
-                    float4 v[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int src = min(q + u, nb - 1);
-                        const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
                         const float ww = __shfl_sync(0xffffffffu, w, src);
                         wq[u] = q + u < nb ? ww : 0.f;
-                        v[u] = q + u < nb ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)pr * D) + lane)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (q > 0) {
+                            const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
+                            v[u] = q + u < nb
+                                       ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)pr * D) + lane)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
                     }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
@@ -588,6 +603,7 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
             }
         }
     }
+    if (status) return;
     const float inv = 1.f / L;
     if constexpr (WIDE) {
         T* dst = static_cast<T*>(a.out) + (int64_t)o * D + 4 * lane;

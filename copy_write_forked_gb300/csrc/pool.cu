@@ -176,20 +176,29 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp
 // so with r = refcount[tail] and k holders in the call, holder number j
 // (0-based, argument order) copies iff r - j > 1.  Since r >= k, only the last
 // holder can write in place, and only when r == k.
+//
+// The kernel is a chain of dependent memory round trips, so it keeps them
+// few: with at most one branch per thread the tail id, the decision and the
+// stack offset stay in registers, and the table rows are written by one warp
+// per branch with its lanes over the new blocks (one stack read per lane
+// rather than one per block in turn).
 template <typename A>
 __global__ void __launch_bounds__(kAppendMetaThreads)
 k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb,
               int32_t n_blocks, int32_t* table, int32_t* refcount, const int32_t* stack, int32_t* holders,
               int32_t* last, int32_t* call, DevMeta* meta) {
-    __shared__ int32_t warp_sums[kAppendMetaThreads / 32];
+    constexpr int NT = kAppendMetaThreads, NW = NT / 32;
+    __shared__ int32_t warp_sums[NW];
     __shared__ int32_t chunk_total;
     __shared__ int32_t status0, top0, bad;
+    __shared__ int32_t s_off[NT], s_src[NT];
     // args: branch[n], len[n]
-    int32_t* offs = call;              // [n] first stack offset of each branch
-    int32_t* cow_src = call + n;       // [n] copied tail (-1 = none)
-    int32_t* cow_dst = call + 2 * n;   // [n] its copy
+    int32_t* offs = call;              // [n] first stack offset of each branch (n > NT only)
+    int32_t* cow_src = call + n;       // [n] copied tail (-1 = none), read by the copy kernel
+    const int32_t t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const bool one = n <= NT;          // branch t of thread t: per-branch values in registers
     pdl_wait();
-    if (threadIdx.x == 0) {
+    if (t == 0) {
         status0 = meta->status;
         top0 = meta->top;
         bad = 0;
@@ -198,7 +207,8 @@ k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t 
     if (status0) return;
     // holders of each shared tail within the call; a tail id that is not a
     // block id poisons the pool instead of being dereferenced
-    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    int32_t my_tail = -1;
+    for (int32_t i = t; i < n; i += NT) {
         const int32_t L = args[n + i];
         if (L % bs) {
             const int32_t tail = table[(int64_t)args[i] * bpb + L / bs];
@@ -207,70 +217,91 @@ k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t 
             } else {
                 atomicAdd(holders + tail, 1);
                 atomicMax(last + tail, i);
+                my_tail = tail;
             }
         }
     }
     __syncthreads();
     if (bad) {
-        if (threadIdx.x == 0) set_status(meta, DENDRITE_ECORRUPT);
+        if (t == 0) set_status(meta, DENDRITE_ECORRUPT);
         return;
     }
-    int32_t carry = 0;
-    for (int32_t base = 0; base < n; base += blockDim.x) {
-        const int32_t i = base + threadIdx.x;
-        int32_t demand = 0;
+    // decisions and one exclusive scan of the blocks each branch takes
+    int32_t carry = 0, my_off = 0, my_src = -1;
+    for (int32_t base = 0; base < n; base += NT) {
+        const int32_t i = base + t;
+        int32_t demand = 0, src = -1;
         if (i < n) {
             const int32_t L = args[n + i];
-            int32_t cow = 0, tail = -1;
             if (L % bs) {
-                tail = table[(int64_t)args[i] * bpb + L / bs];
-                cow = !(refcount[tail] == holders[tail] && last[tail] == i);
+                const int32_t tail = one ? my_tail : table[(int64_t)args[i] * bpb + L / bs];
+                const bool cow = !(__ldcg(refcount + tail) == __ldcg(holders + tail) && __ldcg(last + tail) == i);
+                src = cow ? tail : -1;
             }
-            demand = cow + (L + n_new + bs - 1) / bs - (L + bs - 1) / bs;
-            cow_src[i] = cow ? tail : -1;
+            demand = (src >= 0) + (L + n_new + bs - 1) / bs - (L + bs - 1) / bs;
+            cow_src[i] = src;
         }
-        const int32_t ex = block_exclusive_scan<kAppendMetaThreads>(demand, warp_sums, &chunk_total);
-        if (i < n) offs[i] = carry + ex;
+        const int32_t ex = block_exclusive_scan<NT>(demand, warp_sums, &chunk_total);
+        if (i < n) {
+            if (one) {
+                my_off = ex;
+                my_src = src;
+            } else {
+                offs[i] = carry + ex;
+            }
+        }
         carry += chunk_total;
         __syncthreads();
     }
     const bool fits = carry <= top0;
     if (fits) {
-        for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
-            const int32_t b = args[i], L = args[n + i];
-            int32_t o = offs[i];
-            int32_t* row = table + (int64_t)b * bpb;
-            const int32_t src = cow_src[i];
-            if (src >= 0) {
-                const int32_t blk = stack[top0 - 1 - o];
-                ++o;
-                atomicSub(refcount + src, 1);
-                refcount[blk] = 1;
-                row[L / bs] = blk;
-                cow_dst[i] = blk;
-            } else {
-                cow_dst[i] = -1;
+        for (int32_t base = 0; base < n; base += NT) {
+            const int32_t i = base + t;
+            if (i < n) {
+                s_off[t] = one ? my_off : __ldcg(offs + i);
+                s_src[t] = one ? my_src : __ldcg(cow_src + i);
             }
-            const int32_t nb0 = (L + bs - 1) / bs, nb1 = (L + n_new + bs - 1) / bs;
-            for (int32_t k = nb0; k < nb1; ++k, ++o) {
-                const int32_t blk = stack[top0 - 1 - o];
-                refcount[blk] = 1;
-                row[k] = blk;
+            __syncthreads();
+            const int32_t cnt = min(NT, n - base);
+            for (int32_t k = warp; k < cnt; k += NW) {
+                const int32_t b = args[base + k], L = args[n + base + k];
+                int32_t o = s_off[k];
+                const int32_t src = s_src[k];
+                int32_t* row = table + (int64_t)b * bpb;
+                if (src >= 0) {
+                    if (lane == 0) {
+                        const int32_t blk = stack[top0 - 1 - o];
+                        atomicSub(refcount + src, 1);
+                        refcount[blk] = 1;
+                        row[L / bs] = blk;
+                    }
+                    ++o;
+                }
+                const int32_t nb0 = (L + bs - 1) / bs, nb1 = (L + n_new + bs - 1) / bs;
+                for (int32_t j = nb0 + lane; j < nb1; j += 32) {
+                    const int32_t blk = stack[top0 - 1 - (o + j - nb0)];
+                    refcount[blk] = 1;
+                    row[j] = blk;
+                }
             }
+            __syncthreads();
         }
     }
-    __syncthreads();
-    // reset the holder scratch for the next call (a copied tail's id is in
-    // cow_src, an in-place tail is still in the table)
-    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    // reset the holder scratch for the next call (the original tail id: a
+    // copied tail's is in cow_src, an in-place tail is still in the table)
+    for (int32_t i = t; i < n; i += NT) {
         const int32_t L = args[n + i];
         if (L % bs) {
-            const int32_t tail = cow_src[i] >= 0 ? cow_src[i] : table[(int64_t)args[i] * bpb + L / bs];
+            int32_t tail = my_tail;
+            if (!one) {
+                const int32_t src = __ldcg(cow_src + i);
+                tail = src >= 0 ? src : table[(int64_t)args[i] * bpb + L / bs];
+            }
             holders[tail] = 0;
             last[tail] = -1;
         }
     }
-    if (threadIdx.x == 0) {
+    if (t == 0) {
         if (fits) meta->top = top0 - carry;
         else set_status(meta, DENDRITE_ENOMEM);
     }
@@ -371,19 +402,24 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
     __shared__ int32_t chunk_total;
     __shared__ int32_t st, is_last, lo, hi, top0, cnt;
     pdl_wait();
-    if (threadIdx.x == 0) st = meta->status;
-    __syncthreads();
-    if (st) return;
     // args: branch[n], entry prefix[n], first released entry[n]
     const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+    int32_t* slot = nullptr;
+    int32_t blk = -1;
     if (e < total) {
         int32_t l = 0, h = n - 1;
         while (l < h) {
             const int32_t mid = (l + h + 1) >> 1;
             if (args[n + mid] <= e) l = mid; else h = mid - 1;
         }
-        int32_t* slot = table + (int64_t)args[l] * bpb + args[2 * n + l] + (e - args[n + l]);
-        const int32_t blk = *slot;
+        slot = table + (int64_t)args[l] * bpb + args[2 * n + l] + (e - args[n + l]);
+        blk = *slot;   // loaded together with the status word; nothing is written before it is checked
+    }
+    // one decision per CTA (a status set by another CTA meanwhile may be seen
+    // by some threads only)
+    if (__syncthreads_or(*reinterpret_cast<volatile const int32_t*>(&meta->status) != 0)) return;
+    bool rel = false;
+    if (slot) {
         *slot = -1;
         if ((uint32_t)blk >= (uint32_t)n_blocks) {
             set_status(meta, DENDRITE_ECORRUPT);
@@ -391,18 +427,35 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
             const int32_t old = atomicSub(refcount + blk, 1);
             if (old == 1) {
                 released[blk] = 1;
-                atomicMin(&meta->rel_lo, blk);
-                atomicMax(&meta->rel_hi, blk);
-                atomicAdd(&meta->rel_count, 1);
+                rel = true;
             } else if (old < 1) {
                 set_status(meta, DENDRITE_ECORRUPT);
             }
         }
     }
+    // one lane per warp folds the warp's released ids into the call's range
+    {
+        const unsigned m = __ballot_sync(0xffffffffu, rel);
+        if (m) {
+            const int32_t wlo = __reduce_min_sync(0xffffffffu, rel ? blk : INT_MAX);
+            const int32_t whi = __reduce_max_sync(0xffffffffu, rel ? blk : -1);
+            if ((threadIdx.x & 31) == 0) {
+                atomicMin(&meta->rel_lo, wlo);
+                atomicMax(&meta->rel_hi, whi);
+                atomicAdd(&meta->rel_count, __popc(m));
+            }
+        }
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        is_last = atomicAdd(&meta->rel_done, 1) == (int32_t)gridDim.x - 1;
+        // a single CTA is its own last one: the barrier above already ordered
+        // its threads' updates
+        if (gridDim.x == 1) {
+            is_last = 1;
+        } else {
+            __threadfence();
+            is_last = atomicAdd(&meta->rel_done, 1) == (int32_t)gridDim.x - 1;
+        }
         if (is_last) {
             __threadfence();
             lo = atomicAdd(&meta->rel_lo, 0);

@@ -56,7 +56,10 @@ def test_mcts_2048_500_iterations():
     w = W.mcts()
     assert len(w.query) == 1501
     err, st = run_full(w, n_sample=48)
-    assert st["n_segments"] == 2001
+    # 2001 sharing segments (the root's 128 blocks and 2000 nodes of 2 blocks);
+    # the plan folds many short ones into the segments that follow them
+    assert st["unique_tiles"] == (128 + 2000 * 2) * 8
+    assert st["n_segments"] < 2001
 
 
 def test_spec_verify_8192_3_paths_8_drafts():
