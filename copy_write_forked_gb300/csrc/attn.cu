@@ -172,8 +172,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         {
             const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
             const bool v0 = row0 < U.n_rows, v1 = row1 < U.n_rows;
-            const AttnRow R0 = v0 ? pl.rows[U.row_off + row0] : AttnRow{0, 0};
-            const AttnRow R1 = v1 ? pl.rows[U.row_off + row1] : AttnRow{0, 0};
+            const AttnRow R0 = v0 ? unit_row(pl, U, row0) : AttnRow{0, 0};
+            const AttnRow R1 = v1 ? unit_row(pl, U, row1) : AttnRow{0, 0};
             lim0 = R0.limit;
             lim1 = R1.limit;
             const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R0.q_row * D);
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
         for (int rr = 0; rr < 4; ++rr) {
             const int row = warp + 4 * rr;
             const bool v = row < U.n_rows;
-            const AttnRow R = v ? pl.rows[U.row_off + row] : AttnRow{0, 0};
+            const AttnRow R = v ? unit_row(pl, U, row) : AttnRow{0, 0};
             lim[rr] = R.limit;
             m[rr] = -INFINITY;
             l[rr] = 0.f;
@@ -637,32 +637,11 @@ __global__ void __launch_bounds__(256) k_plan_upload(const uint4* __restrict__ s
         dst[i] = src[i];
 }
 
-// Row records of every unit: segment row sr of unit U is member sr / (q_len G),
-// query token (sr % (q_len G)) / G and head group sr % G; it reads Q/out row
-// (member, token, kv head, group) and sees positions < len - q_len + token + 1.
-__global__ void __launch_bounds__(128) k_plan_rows(const AttnPlanDev pl) {
-    AttnRow* rows = const_cast<AttnRow*>(pl.rows);
-    const int32_t G = pl.group, RM = pl.q_len * G;
-    for (int32_t u = blockIdx.x; u < pl.n_units; u += gridDim.x) {
-        const AttnUnit U = pl.units[u];
-        const int32_t mem_off = pl.segs[U.seg].mem_off;
-        for (int32_t r = threadIdx.x; r < U.n_rows; r += blockDim.x) {
-            const int32_t sr = U.row_lo + r;
-            const int32_t mi = sr / RM, rem = sr - mi * RM;
-            const int32_t j = rem / G, g = rem - j * G;
-            const AttnMember M = pl.members[mem_off + mi];
-            rows[U.row_off + r] = AttnRow{(M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * G + g,
-                                          M.len - pl.q_len + j + 1};
-        }
-    }
-}
-
 // ============================================================ host planning
 struct HostPlan {
     std::vector<AttnSeg> segs;
     std::vector<AttnMember> members;
     std::vector<AttnUnit> units;
-    size_t n_rows = 0;    // row records of all units (built on the device)
     std::vector<int32_t> cta_begin, cta_unit, tc_cta_begin, tc_cta_unit, path_off, path;
     std::vector<int64_t> cuts;
     int64_t tiles = 0, unique_tiles = 0;
@@ -671,7 +650,7 @@ struct HostPlan {
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
-        segs.clear(); members.clear(); units.clear(); n_rows = 0; cta_begin.clear(); cta_unit.clear();
+        segs.clear(); members.clear(); units.clear(); cta_begin.clear(); cta_unit.clear();
         tc_cta_begin.clear(); tc_cta_unit.clear(); path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         n_tc_units = 0;
@@ -790,6 +769,7 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     // member arrays are sized first and filled in place.
     size_t n_units_total = 0, n_members_total = 0;
     for (const Segment& sg : hp.psegs) {
+        if ((int64_t)sg.n_members * RM >= (int64_t)1 << 24) return DENDRITE_ELIMIT;   // rows as exact fp32
         const int32_t rows_per_head = sg.n_members * RM;
         const int32_t group_rows = (tc_on && rows_per_head > p->tc_min_rows) ? kMaxUnitRowsTc : small_rows;
         n_units_total += (size_t)nkv * ((rows_per_head + group_rows - 1) / group_rows);
@@ -839,8 +819,7 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
                     U.table_row = S.table_row;
                     U.blk_start = S.blk_start;
                     U.n_blk = S.n_blk;
-                    // the unit's row records are filled on the device (k_plan_rows)
-                    U.row_off = (int32_t)n_rows;
+                    U.mem_off = S.mem_off;
                     U.pad[0] = U.pad[1] = U.pad[2] = 0;
                     n_rows += U.n_rows;
                     tile_off += S.n_blk;
@@ -854,7 +833,6 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
         if (pass == 0) hp.n_tc_units = n_unit;
     }
     if (n_rows >= INT32_MAX / 2) return DENDRITE_ELIMIT;
-    hp.n_rows = (size_t)n_rows;
     hp.tiles = class_tiles[0] + class_tiles[1];
     partition_class(hp, 0, hp.n_tc_units, class_tiles[0], weight[0], max_tc_ctas, kTcWeights, hp.tc_cta_begin,
                     hp.tc_cta_unit);
@@ -924,14 +902,14 @@ int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
 // Byte layout of an uploaded plan: the sections of HostPlan one after the
 // other, each 16-byte aligned.  off[k] is the start of section k, off[kPlanSections]
 // the total size.
-constexpr int kPlanSections = 10;
+constexpr int kPlanSections = 9;
 size_t plan_layout(const HostPlan& hp, size_t (&off)[kPlanSections + 1]) {
     const size_t sz[kPlanSections] = {
         hp.segs.size() * sizeof(AttnSeg),  hp.members.size() * sizeof(AttnMember),
         hp.units.size() * sizeof(AttnUnit), hp.cta_begin.size() * 4,
         hp.cta_unit.size() * 4,             hp.tc_cta_begin.size() * 4,
         hp.tc_cta_unit.size() * 4,          hp.path_off.size() * 4,
-        hp.path.size() * 4,                 hp.n_rows * sizeof(AttnRow)};
+        hp.path.size() * 4};
     size_t b = 0;
     for (int k = 0; k < kPlanSections; ++k) {
         off[k] = b;
@@ -954,7 +932,6 @@ void plan_pack(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], char*
     put(6, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
     put(7, hp.path_off.data(), hp.path_off.size() * 4);
     put(8, hp.path.data(), hp.path.size() * 4);
-    // section 9 (rows) is written on the device by k_plan_rows
 }
 
 AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], const char* d, int32_t n,
@@ -969,7 +946,6 @@ AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1]
     v.tc_cta_unit = reinterpret_cast<const int32_t*>(d + off[6]);
     v.path_off = reinterpret_cast<const int32_t*>(d + off[7]);
     v.path = reinterpret_cast<const int32_t*>(d + off[8]);
-    v.rows = reinterpret_cast<const AttnRow*>(d + off[9]);
     v.n_units = (int32_t)hp.units.size();
     v.n_ctas = (int32_t)hp.cta_unit.size();
     v.n_tc_units = hp.n_tc_units;
@@ -978,14 +954,9 @@ AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1]
     v.q_len = q_len;
     v.n_q_heads = nq;
     v.group = group;
+    v.rcp_rows_per_member = 1.0f / (float)(q_len * group);
+    v.rcp_group = 1.0f / (float)group;
     return v;
-}
-
-int launch_plan_rows(const AttnPlanDev& pl, cudaStream_t s) {
-    if (pl.n_units == 0) return DENDRITE_OK;
-    const unsigned grid = (unsigned)std::min<int32_t>(pl.n_units, 2048);
-    k_plan_rows<<<grid, 128, 0, s>>>(pl);
-    return cudaGetLastError() == cudaSuccess ? DENDRITE_OK : DENDRITE_ECUDA;
 }
 
 // CTAs the tensor-core kernel may use on this pool (0: not used).
@@ -1175,8 +1146,7 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied[ib]));
         plan_pack(hp, off, p->h_plan[ib]);
         {
-            // everything but the row records (the last section, built on the device)
-            const int64_t n16 = (int64_t)(off[kPlanSections - 1] / 16);
+            const int64_t n16 = (int64_t)(off[kPlanSections] / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
             k_plan_upload<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(p->h_plan[ib]),
                                                reinterpret_cast<uint4*>(p->d_plan), n16);
@@ -1184,7 +1154,6 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         }
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
         pc.dev = plan_view(hp, off, p->d_plan, n, q_len, n_q_heads, n_q_heads / p->n_kv);
-        DENDRITE_TRY(launch_plan_rows(pc.dev, s));
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
         pc.version = p->version;
@@ -1291,11 +1260,9 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     const size_t ml_bytes = hp.partial_rows * sizeof(float2);
     if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
     plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));
-    // everything but the row records (the last section, built on the device)
-    DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, off[kPlanSections - 1], cudaMemcpyHostToDevice, s));
+    DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, off[kPlanSections], cudaMemcpyHostToDevice, s));
     AttnArgs a = attn_args(p, 0, Q, out);
     a.plan = plan_view(hp, off, reinterpret_cast<const char*>(scratch), n, q_len, n_q_heads, n_q_heads / p->n_kv);
-    DENDRITE_TRY(launch_plan_rows(a.plan, s));
     a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);
     a.part_ml = reinterpret_cast<float2*>(scratch + plan_bytes + acc_bytes);
     return launch_attention(p, 0, a, s);

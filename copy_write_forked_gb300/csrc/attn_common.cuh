@@ -10,6 +10,31 @@
 
 namespace dendrite {
 
+// Row r of unit U: segment row sr = row_lo + r belongs to member sr / (q_len G),
+// query token j = (sr % (q_len G)) / G and head group g = sr % G; it reads the
+// Q/out row (member, token, kv head, group) and sees positions
+// < len - q_len + j + 1.
+// The two divisions use the divisors' fp32 reciprocals (the host limits
+// segment rows to 2^24, so sr converts exactly and the estimate is off by at
+// most one, which one remainder test corrects): integer division by a
+// run-time divisor would sit on the dependent chain from the unit record to
+// the Q load.
+__device__ __forceinline__ int32_t div_rcp(int32_t n, int32_t d, float rcp) {
+    int32_t q = __float2int_rz(__int2float_rz(n) * rcp);
+    const int32_t r = n - q * d;
+    q += (r >= d) - (r < 0);
+    return q;
+}
+
+__device__ __forceinline__ AttnRow unit_row(const AttnPlanDev& pl, const AttnUnit& U, int32_t r) {
+    const int32_t G = pl.group, RM = pl.q_len * G;
+    const int32_t sr = U.row_lo + r;
+    const int32_t mi = div_rcp(sr, RM, pl.rcp_rows_per_member), rem = sr - mi * RM;
+    const int32_t j = div_rcp(rem, G, pl.rcp_group), g = rem - j * G;
+    const AttnMember M = pl.members[U.mem_off + mi];
+    return AttnRow{(M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * G + g, M.len - pl.q_len + j + 1};
+}
+
 struct AttnArgs {
     AttnPlanDev plan;
     const void* Q;

@@ -410,7 +410,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // that chunk's epilogue, so the next chunk's S overlaps the epilogue.
         auto stage_q = [&](const AttnUnit& V) -> AttnRow {
             const bool v_ok = row < V.n_rows;
-            const AttnRow RR = v_ok ? pl.rows[V.row_off + row] : AttnRow{0, 0};
+            const AttnRow RR = v_ok ? unit_row(pl, V, row) : AttnRow{0, 0};
             const uint4* q = reinterpret_cast<const uint4*>(Q + (int64_t)RR.q_row * D);
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {

@@ -59,9 +59,9 @@ struct AttnMember {
 // One attention work unit: a (segment, kv head, row group).  Its rows are
 // segment rows [row_lo, row_lo + n_rows); segment row sr belongs to member
 // sr / (q_len * G), query token (sr % (q_len * G)) / G and head group g = sr % G.
-// The segment's table row and block range are repeated here so the partial
-// kernel needs no second lookup, and rows[row_off ..) hold each row's Q/out
-// row and visibility limit.
+// The segment's table row, block range and first member are repeated here so
+// the partial kernels need no second lookup; a row's Q/out row and visibility
+// limit follow from its member (unit_row).
 struct AttnUnit {
     int32_t seg;
     int32_t kv_head;
@@ -75,12 +75,12 @@ struct AttnUnit {
     int32_t table_row;  // branch handle whose table row holds the segment's block ids
     int32_t blk_start;  // first logical block of the segment
     int32_t n_blk;      // blocks (tiles) of the segment
-    int32_t row_off;    // first entry of the unit's rows in the row list
+    int32_t mem_off;    // the segment's first entry in the member list
     int32_t pad[3];
 };
 static_assert(sizeof(AttnUnit) == 64, "AttnUnit layout");
 
-// One query row of a unit.
+// One query row of a unit (computed by unit_row).
 struct AttnRow {
     int32_t q_row;   // row of Q/out viewed as [rows][head_dim]
     int32_t limit;   // visible positions: the row sees positions < limit
@@ -91,7 +91,6 @@ struct AttnPlanDev {
     const AttnSeg* segs;
     const AttnMember* members;
     const AttnUnit* units;
-    const AttnRow* rows;
     // Units [0, n_tc_units) run on the tcgen05 kernel, the rest on the
     // mma.sync (or fp32) kernel; each class has its own tile numbering and
     // its own CTA partition.
@@ -110,6 +109,8 @@ struct AttnPlanDev {
     int32_t q_len;
     int32_t n_q_heads;
     int32_t group;                 // G = n_q_heads / n_kv
+    float rcp_rows_per_member;     // 1 / (q_len G)
+    float rcp_group;               // 1 / G
 };
 
 // ------------------------------------------------------- host bookkeeping

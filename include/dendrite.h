@@ -182,9 +182,13 @@ int dendrite_append_layer(dendrite_pool* pool, int32_t layer, const void* K, con
  *   q_len >= 1: the queries are the branch's last q_len positions; query j sees
  *        positions <= len - q_len + j.  Every branch needs len >= q_len.
  * out = softmax(q K^T / sqrt(head_dim)) V per query row.  Blocks shared by
- * several queried branches are read from HBM once for all of them (split-KV
- * partials, then a log-sum-exp merge).  The plan built from the branch tree is
- * cached until the tree changes.  `branches` may not hold duplicates.
+ * several queried branches are streamed once for all of them (split-KV
+ * partials, then a log-sum-exp merge); a short shared range may instead be
+ * read again by each longer range that follows it (pool option
+ * fold_segments).  The plan built from the branch tree is cached until the
+ * tree changes.  `branches` may not hold duplicates.
+ * DENDRITE_ELIMIT if a shared range would be read by 2^24 or more query rows
+ * per KV head, or the plan outgrows 32-bit indices.
  * Reads layer 0 of a multi-layer pool.
  */
 int dendrite_tree_attn_decode(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,
