@@ -75,17 +75,18 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs of the previous kernel are ready
+    pdl_trigger();
+    // this CTA's share of the plan is loaded together with the status word
+    const AttnPlanDev& pl = a.plan;
+    const int c = blockIdx.x;
+    const int32_t t_begin = pl.cta_begin[c], t_end = pl.cta_begin[c + 1];
+    const int32_t u0 = pl.cta_unit[c];
     if (threadIdx.x == 0) {
         abort_flag = a.meta->status != 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     if (abort_flag) return;
-
-    const AttnPlanDev& pl = a.plan;
-    const int c = blockIdx.x;
-    const int32_t t_begin = pl.cta_begin[c], t_end = pl.cta_begin[c + 1];
-    const int32_t u0 = pl.cta_unit[c];
     volatile int* abortp = &abort_flag;
 
     if (warp == NCONS) {
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int st0;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
     if (threadIdx.x == 0) st0 = a.meta->status;
     __syncthreads();
     if (st0) return;
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
 template <typename T, bool WIDE>
 __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
     const AttnPlanDev& pl = a.plan;
     const int lane = threadIdx.x & 31;
     const int32_t o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -628,13 +631,23 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
 
 // ============================================================ plan upload
 // Copies the plan from the pool's pinned host buffer (device-accessible) to
-// its device copy.  A kernel rather than cudaMemcpyAsync: the copy engines
-// may be busy with the caller's own host-to-device traffic on other streams,
-// and a few KB of plan should not queue behind it.
+// one of its two device copies.  A kernel rather than cudaMemcpyAsync: the
+// copy engines may be busy with the caller's own host-to-device traffic on
+// other streams, and a few KB of plan should not queue behind it.
+// Launched as a programmatic dependent, it copies while the previous kernel
+// (usually the append's copy kernel) is still running: it reads only the
+// pinned buffer and writes only the device copy that the plan before the
+// previous one used, whose kernels are complete by the time the previous
+// kernel lets dependents launch (every kernel of the library does that only
+// after its own griddepcontrol.wait).  It then waits for the previous kernel
+// like any other, so the attention kernels after it see that kernel's
+// results.
 __global__ void __launch_bounds__(256) k_plan_upload(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                      int64_t n16) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
         dst[i] = src[i];
+    pdl_trigger();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ============================================================ host planning
@@ -1028,10 +1041,12 @@ int ensure_capacity(dendrite_pool* p, size_t plan_bytes, size_t partial_rows) {
     if (plan_bytes > p->plan_cap) {
         size_t cap = std::max<size_t>(plan_bytes * 2, 1 << 20);
         DENDRITE_CUDA(cudaDeviceSynchronize());
-        if (p->d_plan) cudaFree(p->d_plan);
-        p->d_plan = nullptr;
+        for (char*& d : p->d_plan) {
+            if (d) cudaFree(d);
+            d = nullptr;
+        }
         p->plan_cap = 0;
-        DENDRITE_CUDA(cudaMalloc(&p->d_plan, cap));
+        for (char*& d : p->d_plan) DENDRITE_CUDA(cudaMalloc(&d, cap));
         p->plan_cap = cap;
         p->plan.valid = false;
     }
@@ -1088,13 +1103,15 @@ int attn_setup(dendrite_pool* p) {
 }
 
 void attn_teardown(dendrite_pool* p) {
-    if (p->d_plan) cudaFree(p->d_plan);
+    for (char*& d : p->d_plan) {
+        if (d) cudaFree(d);
+        d = nullptr;
+    }
     for (char*& h : p->h_plan) {
         if (h) cudaFreeHost(h);
         h = nullptr;
     }
     if (p->d_partial) cudaFree(p->d_partial);
-    p->d_plan = nullptr;
     p->d_partial = nullptr;
 }
 
@@ -1148,12 +1165,12 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         {
             const int64_t n16 = (int64_t)(off[kPlanSections] / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
-            k_plan_upload<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(p->h_plan[ib]),
-                                               reinterpret_cast<uint4*>(p->d_plan), n16);
-            DENDRITE_CUDA(cudaGetLastError());
+            DENDRITE_CUDA(launch_pdl(k_plan_upload, dim3(grid), dim3(256), 0, s,
+                                     reinterpret_cast<const uint4*>(p->h_plan[ib]),
+                                     reinterpret_cast<uint4*>(p->d_plan[ib]), n16));
         }
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
-        pc.dev = plan_view(hp, off, p->d_plan, n, q_len, n_q_heads, n_q_heads / p->n_kv);
+        pc.dev = plan_view(hp, off, p->d_plan[ib], n, q_len, n_q_heads, n_q_heads / p->n_kv);
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
         pc.version = p->version;

@@ -10,6 +10,14 @@
 
 namespace dendrite {
 
+// Lets the next kernel in the stream, when launched as a programmatic
+// dependent, start its prologue; it still waits (griddepcontrol.wait) for
+// this whole grid to finish before it reads anything.  Every kernel of the
+// library calls it only after its own griddepcontrol.wait, except the plan
+// upload (see there), so when a kernel lets dependents launch, every kernel
+// before it in the stream has finished.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Row r of unit U: segment row sr = row_lo + r belongs to member sr / (q_len G),
 // query token j = (sr % (q_len G)) / G and head group g = sr % G; it reads the
 // Q/out row (member, token, kv head, group) and sees positions

@@ -224,6 +224,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_FINAL + i), 1);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
     if (threadIdx.x == 0) {
         abort_flag = a.meta->status != 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

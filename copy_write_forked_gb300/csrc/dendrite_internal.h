@@ -221,8 +221,8 @@ struct dendrite_pool {
     bool tc_ready = false;           // tcgen05 attention kernel configured for this device
 
     // attention workspace (grow-only)
-    char* d_plan = nullptr;
-    size_t plan_cap = 0;
+    char* d_plan[2] = {nullptr, nullptr};      // device copies, used alternately by plan builds
+    size_t plan_cap = 0;                       // capacity of each
     char* h_plan[2] = {nullptr, nullptr};      // pinned, used alternately by plan builds
     size_t h_plan_cap = 0;                     // capacity of each
     cudaEvent_t plan_copied[2] = {nullptr, nullptr};

@@ -35,7 +35,13 @@ __device__ __forceinline__ void set_status(DevMeta* m, int32_t code) {
     atomicCAS(&m->status, 0, code);
 }
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Programmatic dependent launch: every kernel here first waits for the
+// previous kernel in the stream (pdl_wait), then lets the next one launch its
+// prologue (it still waits for this whole grid before reading anything).
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Per-call argument arrays: small ones travel as kernel parameters (no copy
 // on the stream), large ones are staged in device memory.
