@@ -528,7 +528,8 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
             // lane p: partial p of this batch -> its partial row
             const int32_t pidx = p0 + lane;
             int32_t ent = 0;
-            for (int k = 0; k < 32; ++k) ent += (__shfl_sync(0xffffffffu, incl, k) <= pidx) ? 1 : 0;
+            const int n_ent = min(32, pend - e0);   // lanes past it hold no chunks
+            for (int k = 0; k < n_ent; ++k) ent += (__shfl_sync(0xffffffffu, incl, k) <= pidx) ? 1 : 0;
             ent = min(ent, 31);
             const int32_t eb = __shfl_sync(0xffffffffu, base, ent);
             const int32_t es = __shfl_sync(0xffffffffu, stride, ent);

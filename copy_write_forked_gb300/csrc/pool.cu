@@ -209,21 +209,22 @@ k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t 
         top0 = meta->top;
         bad = 0;
     }
+    // with one branch per thread, its tail id is loaded with the status word
+    int32_t my_tail = -1;
+    if (one && t < n && args[n + t] % bs) my_tail = table[(int64_t)args[t] * bpb + args[n + t] / bs];
     __syncthreads();
     if (status0) return;
     // holders of each shared tail within the call; a tail id that is not a
     // block id poisons the pool instead of being dereferenced
-    int32_t my_tail = -1;
     for (int32_t i = t; i < n; i += NT) {
         const int32_t L = args[n + i];
         if (L % bs) {
-            const int32_t tail = table[(int64_t)args[i] * bpb + L / bs];
+            const int32_t tail = one ? my_tail : table[(int64_t)args[i] * bpb + L / bs];
             if ((uint32_t)tail >= (uint32_t)n_blocks) {
                 bad = 1;
             } else {
                 atomicAdd(holders + tail, 1);
                 atomicMax(last + tail, i);
-                my_tail = tail;
             }
         }
     }
@@ -314,27 +315,27 @@ k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t 
 }
 
 // ------------------------------------------------------- append, phase 2
-// One CTA per (branch, touched block, kv head) tile: copies the valid slots
-// of a copied-on-write tail (if any) and scatters the new rows into their
-// slots with 16-byte vector moves.  tile_pre[i] is the exclusive prefix of
+// One CTA at a time per (branch, touched block, kv head) tile: copies the
+// valid slots of a copied-on-write tail (if any) and scatters the new rows
+// into their slots with 16-byte vector moves.  tile_pre[i] is the exclusive prefix of
 // touched blocks per branch (host computed; depends only on lengths).
 // blockIdx.y selects the layer: the input rows of layer y start y * in_layer
 // 16-byte words after Kin / Vin, its pool y * pool_layer words after Kp / Vp.
 template <typename A>
-__global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb, int32_t n_kv,
+__global__ void __launch_bounds__(128, 16) k_append_copy(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t bs, int32_t bpb, int32_t n_kv,
                               int32_t row_vec, int32_t n_blocks, const int32_t* __restrict__ table,
                               const int32_t* __restrict__ call, const uint4* __restrict__ Kin0,
                               const uint4* __restrict__ Vin0, uint4* __restrict__ Kp0, uint4* __restrict__ Vp0,
-                              int64_t in_layer, int64_t pool_layer, const DevMeta* meta) {
+                              int64_t in_layer, int64_t pool_layer, const DevMeta* meta, int64_t n_tiles) {
     pdl_wait();
-    if (meta->status) return;
+    // a grid of at most 16 CTAs per SM strides over the tiles
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     const uint4* __restrict__ Kin = Kin0 + blockIdx.y * in_layer;
     const uint4* __restrict__ Vin = Vin0 + blockIdx.y * in_layer;
     uint4* __restrict__ Kp = Kp0 + blockIdx.y * pool_layer;
     uint4* __restrict__ Vp = Vp0 + blockIdx.y * pool_layer;
     // args: branch[n], len[n], tile prefix[n]
     const int32_t* cow_src = call + n;
-    const int64_t tile = blockIdx.x;
     const int32_t h = (int32_t)(tile % n_kv);
     const int32_t t = (int32_t)(tile / n_kv);   // touched-block index over the call
     // branch i with tile_pre[i] <= t < tile_pre[i+1]
@@ -346,44 +347,59 @@ __global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t
     const int32_t i = lo;
     const int32_t L = args[n + i];
     const int32_t lblk = L / bs + (t - args[2 * n + i]);
-    const int32_t dst = table[(int64_t)args[i] * bpb + lblk];
-    if ((uint32_t)dst >= (uint32_t)n_blocks || cow_src[i] >= n_blocks) {
-        if (threadIdx.x == 0) atomicCAS(const_cast<int32_t*>(&meta->status), 0, DENDRITE_ECORRUPT);
-        return;
-    }
     const int32_t s0 = lblk == L / bs ? L % bs : 0;
     const int32_t s1 = min(bs, L + n_new - lblk * bs);
     const int64_t tile_vec = (int64_t)bs * row_vec;
-    uint4* kd = Kp + ((int64_t)dst * n_kv + h) * tile_vec;
-    uint4* vd = Vp + ((int64_t)dst * n_kv + h) * tile_vec;
-    // copy of the shared tail's valid slots, then the new rows (token
-    // lblk*bs + s - L of branch i); each thread issues its loads before its
-    // stores so the moves of a tile are in flight together
-    const bool cow = lblk == L / bs && cow_src[i] >= 0;
-    const uint4* ks = cow ? Kp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec : nullptr;
-    const uint4* vs = cow ? Vp + ((int64_t)cow_src[i] * n_kv + h) * tile_vec : nullptr;
     const int32_t total = s1 * row_vec;   // slots [0, s1) of the destination tile
-    constexpr int U = 4;
-    for (int32_t e0 = threadIdx.x; e0 < total; e0 += U * blockDim.x) {
-        uint4 kv[U], vv[U];
-        int32_t idx[U];
+    // Slots s >= s0 take the new rows (token lblk*bs + s - L of branch i),
+    // slots s < s0 of a copied-on-write tail its source's rows.  The first
+    // batch of new rows is loaded together with the status word, the
+    // destination block id and the copy-on-write source, none of which its
+    // addresses depend on; each thread issues its loads before its stores so
+    // the moves of a tile are in flight together.
+    constexpr int U = 2;   // 2 x 128 threads cover a bf16 tile of head_dim 128 (256 slots)
+    uint4 kv[U], vv[U];
+    int32_t idx[U];
+    auto gather = [&](int32_t e0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int32_t e = e0 + u * blockDim.x;
-            idx[u] = -1;
+            const int32_t e = e0 + u * (int32_t)blockDim.x;
+            idx[u] = e < total ? e : -1;
             if (e >= total) continue;
             const int32_t s = e / row_vec, v = e % row_vec;
-            if (s < s0) {
-                if (!cow) continue;
-                kv[u] = ks[e];
-                vv[u] = vs[e];
-            } else {
+            if (s >= s0) {
                 const int64_t tok = (int64_t)lblk * bs + s - L;
                 const int64_t src = (((int64_t)i * n_new + tok) * n_kv + h) * row_vec + v;
                 kv[u] = __ldg(Kin + src);
                 vv[u] = __ldg(Vin + src);
             }
-            idx[u] = e;
+        }
+    };
+    const int32_t status = meta->status;
+    const int32_t dst = table[(int64_t)args[i] * bpb + lblk];
+    const int32_t csrc = lblk == L / bs ? cow_src[i] : -1;
+    gather(threadIdx.x);
+    if (status) return;
+    if ((uint32_t)dst >= (uint32_t)n_blocks || csrc >= n_blocks) {
+        if (threadIdx.x == 0) atomicCAS(const_cast<int32_t*>(&meta->status), 0, DENDRITE_ECORRUPT);
+        return;
+    }
+    uint4* kd = Kp + ((int64_t)dst * n_kv + h) * tile_vec;
+    uint4* vd = Vp + ((int64_t)dst * n_kv + h) * tile_vec;
+    const bool cow = csrc >= 0;
+    const uint4* ks = cow ? Kp + ((int64_t)csrc * n_kv + h) * tile_vec : nullptr;
+    const uint4* vs = cow ? Vp + ((int64_t)csrc * n_kv + h) * tile_vec : nullptr;
+    for (int32_t e0 = threadIdx.x; e0 < total; e0 += U * blockDim.x) {
+        if (e0 != (int32_t)threadIdx.x) gather(e0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (idx[u] < 0 || idx[u] / row_vec >= s0) continue;
+            if (!cow) {            // an in-place tail keeps its rows
+                idx[u] = -1;
+                continue;
+            }
+            kv[u] = ks[idx[u]];
+            vv[u] = vs[idx[u]];
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -391,6 +407,7 @@ __global__ void k_append_copy(const __grid_constant__ A args, int32_t n, int32_t
             kd[idx[u]] = kv[u];
             vd[idx[u]] = vv[u];
         }
+    }
     }
 }
 
@@ -738,7 +755,8 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
     // args: branch[n], len[n], tile prefix[n]
     constexpr int CAP = 768;
     const int32_t row_vec = p->head_dim * p->elt / 16;
-    const unsigned grid = (unsigned)(touched * p->n_kv);
+    const int64_t n_tiles = touched * p->n_kv;
+    const unsigned grid = (unsigned)std::min<int64_t>(n_tiles, (int64_t)p->sm_count * 16);
     const int64_t pool_layer = (int64_t)(p->layer_bytes / 16);
     auto fill = [&](int32_t* a) {
         int32_t acc = 0;
@@ -765,7 +783,7 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
             DENDRITE_CUDA(launch_pdl(k_append_copy<decltype(args)>, dim3(grid, (unsigned)n_layers_in), dim3(128), 0,
                                      s, args, n, n_new, bs, p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks,
                                      (const int32_t*)p->d_table, (const int32_t*)p->d_call_i32, (const uint4*)K,
-                                     (const uint4*)V, kp, vp, in_layer, pool_layer, (const DevMeta*)p->d_meta));
+                                     (const uint4*)V, kp, vp, in_layer, pool_layer, (const DevMeta*)p->d_meta, n_tiles));
             prof_end(p, T_APPEND_COPY, s);
         }
         return DENDRITE_OK;
