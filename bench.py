@@ -40,10 +40,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ------------------------------------------------------------------ helpers
 
 # DRAM bytes (read + write) per launch of k_attn_partial_bf16 on this step,
-# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` over three
-# launches (profiles/attn_partial_bf16_beam.md); to be re-taken whenever that
+# from one ncu capture of the kernel as it is now (dram__bytes_read.sum
+# 168.27 MB + dram__bytes_write.sum 3.73 MB); to be re-taken whenever that
 # kernel changes.
-BEAM_PARTIAL_TRAFFIC_BYTES = 169_690_000
+BEAM_PARTIAL_TRAFFIC_BYTES = 171_990_000
 
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
