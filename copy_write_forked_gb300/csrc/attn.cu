@@ -678,20 +678,26 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 // tile of a unit with rt row tiles of 16 costs about (1 + rt) units (HBM time
 // plus mma time: 0.25 us for rt = 1 vs 0.61 us for rt = 4 per CTA), and every
 // chunk boundary (partial store, combine, next unit's Q) about as much as 8
-// one-row-tile tiles.  tcgen05 class (one CTA per SM): a tile costs about
-// (1 + rt) with rt row tiles of 128; a chunk boundary drains the MMA pipeline
-// and stores up to 256 partial rows of 520 bytes.
+// one-row-tile tiles plus a quarter tile per row (its query load, combine
+// and partial store grow with the rows: MCTS, whose units hold 4 to 64 rows,
+// 292 -> 283 us with the row term).  tcgen05 class (one CTA per SM): a tile
+// costs about (1 + rt) with rt row tiles of 128; a chunk boundary drains the
+// MMA pipeline and stores up to 256 partial rows of 520 bytes.
 struct ClassWeights {
     int64_t unit_start;
-    int64_t min_per_cta;   // smallest total weight worth a CTA of its own
+    int64_t rows_per_weight;   // a unit start also weighs n_rows / rows_per_weight (0: no row term)
+    int64_t min_per_cta;       // smallest total weight worth a CTA of its own
 };
-constexpr ClassWeights kSmallWeights{16, 8};
-constexpr ClassWeights kTcWeights{24, 32};
+constexpr ClassWeights kSmallWeights{16, 2, 8};
+constexpr ClassWeights kTcWeights{24, 0, 32};
 inline int64_t tile_weight(int rt) { return 1 + rt; }
+inline int64_t start_weight(const ClassWeights& cw, int32_t n_rows) {
+    return cw.unit_start + (cw.rows_per_weight ? n_rows / cw.rows_per_weight : 0);
+}
 
 // Stream-K split of one class's tile list (units [u_lo, u_hi), tiles
 // [0, T)) into at most max_ctas CTAs of about equal weight (tile_weight per
-// tile plus unit_start per unit start).  Cuts are made strictly increasing so
+// tile plus start_weight per unit start).  Cuts are made strictly increasing so
 // that no CTA is empty.  Fills begin[C + 1], cunit[C] and each unit's cfirst
 // and nchunks.
 void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_t weight, int max_ctas,
@@ -713,11 +719,12 @@ void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_
             const AttnUnit& U = hp.units[ui];
             const int64_t nb = U.n_blk;
             const int64_t tw = tile_weight(U.rt);
-            const int64_t uw = cw_.unit_start + nb * tw;
+            const int64_t us = start_weight(cw_, U.n_rows);
+            const int64_t uw = us + nb * tw;
             while (c < C0) {
                 const int64_t target = (weight * c + C0 - 1) / C0;
                 if (target >= cw + uw) break;
-                const int64_t k = std::max<int64_t>(0, (target - cw - cw_.unit_start + tw - 1) / tw);
+                const int64_t k = std::max<int64_t>(0, (target - cw - us + tw - 1) / tw);
                 const int64_t cut = U.tile_off + std::min<int64_t>(k, nb);
                 if (cut > hp.cuts.back() && cut < T) hp.cuts.push_back(cut);
                 ++c;
@@ -837,7 +844,7 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
                     U.pad[0] = U.pad[1] = U.pad[2] = 0;
                     n_rows += U.n_rows;
                     tile_off += S.n_blk;
-                    weight[pass] += cwt.unit_start + (int64_t)S.n_blk * tile_weight(U.rt);
+                    weight[pass] += start_weight(cwt, U.n_rows) + (int64_t)S.n_blk * tile_weight(U.rt);
                 }
             }
             hp.segs.push_back(S);
