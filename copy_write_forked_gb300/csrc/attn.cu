@@ -630,6 +630,148 @@ __global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs
         }
 }
 
+// Grouped merge (head_dim 128): one warp per (branch qi, query token j, KV
+// head h) and NG = min(G, 4) consecutive query heads g0 .. g0 + NG - 1 of its
+// GQA group.  Those heads are NG consecutive rows of every unit the branch
+// reads, so they share the unit lookups and the chunk enumeration: the
+// partial of row g0 + i is always the one of row g0 plus i.  The plan keeps
+// such a run of rows inside one row group when G <= 4 divides 16 or G is a
+// multiple of 4 (row groups hold 16, 64 or 256 rows); other group sizes use
+// the per-row kernel above.  Lane l owns columns 4 l .. 4 l + 3.
+template <typename T, int NG>
+__global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
+    const AttnPlanDev& pl = a.plan;
+    const int lane = threadIdx.x & 31;
+    const int G = pl.group, gchunks = G / NG, n_kv = pl.n_q_heads / G;
+    const int32_t w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int32_t n_w = pl.n_queried * pl.q_len * n_kv * gchunks;
+    if (w >= n_w) return;
+    int32_t x = w;
+    const int gc = x % gchunks;
+    x /= gchunks;
+    const int h = x % n_kv;
+    x /= n_kv;
+    const int j = x % pl.q_len;
+    const int32_t qi = x / pl.q_len;
+    const int g0 = gc * NG;
+    // the status word is checked only before the store, so that its load
+    // overlaps the plan loads (the plan is always readable)
+    const int32_t status = *reinterpret_cast<volatile const int32_t*>(&a.meta->status);
+    const int32_t pbeg = pl.path_off[qi], pend = pl.path_off[qi + 1];
+    float M[NG], L[NG];
+    float4 acc[NG];
+#pragma unroll
+    for (int i = 0; i < NG; ++i) {
+        M[i] = -INFINITY;
+        L[i] = 0.f;
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int32_t e0 = pbeg; e0 < pend; e0 += 32) {
+        // lane e: one path entry -> its unit's chunks for row g0
+        const int32_t e = e0 + lane;
+        int32_t nch = 0, base = 0, stride = 0;
+        if (e < pend) {
+            const int4 pe = __ldg(reinterpret_cast<const int4*>(pl.path) + e);
+            const int32_t sr = pe.z + j * G + g0;
+            const int32_t grp = sr / pe.w;
+            const AttnUnit U = pl.units[pe.x + h * pe.y + grp];
+            nch = U.nchunks;
+            base = U.prow_base + (sr - grp * pe.w);
+            stride = U.n_rows;
+        }
+        int32_t incl = nch;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        const int32_t excl = incl - nch;
+        const int n_ent = min(32, pend - e0);   // lanes past it hold no chunks
+        for (int32_t p0 = 0; p0 < total; p0 += 32) {
+            // lane p: partial p of this batch -> its partial row for g0
+            const int32_t pidx = p0 + lane;
+            int32_t ent = 0;
+            for (int k = 0; k < n_ent; ++k) ent += (__shfl_sync(0xffffffffu, incl, k) <= pidx) ? 1 : 0;
+            ent = min(ent, 31);
+            const int32_t eb = __shfl_sync(0xffffffffu, base, ent);
+            const int32_t es = __shfl_sync(0xffffffffu, stride, ent);
+            const int32_t ex = __shfl_sync(0xffffffffu, excl, ent);
+            const bool valid = pidx < total;
+            const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
+            const int nb = min(32, total - p0);
+            float2 ml[NG];
+#pragma unroll
+            for (int i = 0; i < NG; ++i) ml[i] = valid ? __ldcg(a.part_ml + prow + i) : make_float2(-INFINITY, 0.f);
+            float wt[NG];
+#pragma unroll
+            for (int i = 0; i < NG; ++i) {
+                float mb = ml[i].x;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+                const float Mn = fmaxf(M[i], mb);
+                const float Mu = Mn == -INFINITY ? 0.f : Mn;
+                const float sc = exp2f(M[i] - Mu);   // rescale of the running state
+                wt[i] = ml[i].x == -INFINITY ? 0.f : exp2f(ml[i].x - Mu);
+                float lw = wt[i] * ml[i].y;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+                L[i] = L[i] * sc + lw;
+                acc[i].x *= sc;
+                acc[i].y *= sc;
+                acc[i].z *= sc;
+                acc[i].w *= sc;
+                M[i] = Mn;
+            }
+            // acc rows, eight (partial, head) pairs in flight
+            constexpr int PER = 8 / NG;   // partials per batch of eight loads
+            for (int q = 0; q < nb; q += PER) {
+                float4 v[PER][NG];
+                float wq[PER][NG];
+#pragma unroll
+                for (int u = 0; u < PER; ++u) {
+                    const int src = min(q + u, nb - 1);
+                    const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
+#pragma unroll
+                    for (int i = 0; i < NG; ++i) {
+                        const float ww = __shfl_sync(0xffffffffu, wt[i], src);
+                        wq[u][i] = q + u < nb ? ww : 0.f;
+                        v[u][i] = q + u < nb
+                                      ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)(pr + i) * D) + lane)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < PER; ++u)
+#pragma unroll
+                    for (int i = 0; i < NG; ++i) {
+                        acc[i].x = fmaf(v[u][i].x, wq[u][i], acc[i].x);
+                        acc[i].y = fmaf(v[u][i].y, wq[u][i], acc[i].y);
+                        acc[i].z = fmaf(v[u][i].z, wq[u][i], acc[i].z);
+                        acc[i].w = fmaf(v[u][i].w, wq[u][i], acc[i].w);
+                    }
+            }
+        }
+    }
+    if (status) return;
+#pragma unroll
+    for (int i = 0; i < NG; ++i) {
+        const float inv = 1.f / L[i];
+        const int64_t o = ((int64_t)qi * pl.q_len + j) * pl.n_q_heads + h * G + g0 + i;
+        T* dst = static_cast<T*>(a.out) + o * D + 4 * lane;
+        if constexpr (sizeof(T) == 2) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        } else {
+            *reinterpret_cast<float4*>(dst) = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+        }
+    }
+}
+
 // ============================================================ plan upload
 // Copies the plan from the pool's pinned host buffer (device-accessible) to
 // one of its two device copies.  A kernel rather than cudaMemcpyAsync: the
@@ -1019,7 +1161,23 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     {
         const int32_t n_out = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
         const unsigned grid = (unsigned)((n_out + 7) / 8);
-        if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16, true>, dim3(grid), dim3(256), 0, s, a));
+        const int G = a.plan.group;
+        const int ng = G >= 4 ? (G % 4 == 0 ? 4 : 0) : (G == 1 || G == 2 ? G : 0);   // rows per grouped warp
+        // the grouped merge shares lookups among a group's heads but runs a
+        // quarter of the warps; a small merge (beam: 1,024 rows) keeps one
+        // row per warp, where the warps' latency chains overlap better
+        if (p->head_dim == D && ng > 0 && (int64_t)n_out / ng >= (int64_t)16 * p->sm_count) {
+            const unsigned ggrid = (unsigned)((n_out / ng + 7) / 8);
+            if (bf16) {
+                if (ng == 4) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 4>, dim3(ggrid), dim3(256), 0, s, a));
+                else if (ng == 2) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 2>, dim3(ggrid), dim3(256), 0, s, a));
+                else DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 1>, dim3(ggrid), dim3(256), 0, s, a));
+            } else {
+                if (ng == 4) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<float, 4>, dim3(ggrid), dim3(256), 0, s, a));
+                else if (ng == 2) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<float, 2>, dim3(ggrid), dim3(256), 0, s, a));
+                else DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<float, 1>, dim3(ggrid), dim3(256), 0, s, a));
+            }
+        } else if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16, true>, dim3(grid), dim3(256), 0, s, a));
         else if (p->head_dim == D) DENDRITE_CUDA(launch_pdl(k_attn_merge<float, true>, dim3(grid), dim3(256), 0, s, a));
         else DENDRITE_CUDA(launch_pdl(k_attn_merge<float, false>, dim3(grid), dim3(256), 0, s, a));
     }

@@ -76,6 +76,39 @@ def test_gqa_group_8_and_group_1():
         run_and_check(w, TOL_BF16)
 
 
+def grouped_merge_runs(w):
+    """Whether the attention call merges a GQA group's heads together: a
+    group of 1, 2 or a multiple of 4 heads, and at least 16 grouped warps per
+    SM (smaller merges keep one row per warp)."""
+    G = w.n_q_heads // w.n_kv_heads
+    ng = 4 if G % 4 == 0 else (G if G in (1, 2) else 0)
+    n_out = len(w.query) * w.q_len * w.n_q_heads
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return w.head_dim == 128 and ng > 0 and n_out // ng >= 16 * sms
+
+
+@pytest.mark.parametrize("n_kv, n_q", [(8, 32), (8, 16), (8, 8), (2, 32), (4, 24)])
+def test_grouped_merge_bf16(n_kv, n_q):
+    # 48 branches x 8 draft tokens: GQA groups of 4, 2, 1, 16 and 6 heads
+    # (the last one merges a row per warp)
+    w = W.spec_verify(requests=16, prefix=200, paths=3, draft=8, n_kv=n_kv, n_q=n_q, seed=n_q)
+    assert grouped_merge_runs(w) == (n_q // n_kv != 6)
+    run_and_check(w, TOL_BF16)
+
+
+def test_grouped_merge_fp32_head_dim_128():
+    w = W.spec_verify(requests=16, prefix=120, paths=3, draft=8, n_kv=8, n_q=32, dtype=torch.float32, seed=3)
+    assert grouped_merge_runs(w)
+    run_and_check(w, TOL_F32)
+
+
+@pytest.mark.parametrize("n_kv, n_q", [(2, 6), (1, 12)])
+def test_small_merges_odd_groups(n_kv, n_q):
+    w = W.random_script(7 + n_q, n_ops=30, max_live=8, max_append=60, n_kv=n_kv, n_q=n_q, d=128, bs=16,
+                        dtype=torch.bfloat16, q_len=2, seed=n_q)
+    run_and_check(w, TOL_BF16)
+
+
 def test_mcts_small():
     w = W.mcts(root=256, iters=60, width=4, per_node=32, max_depth=6)
     run_and_check(w, TOL_BF16)
