@@ -45,6 +45,12 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel changes.
 BEAM_PARTIAL_TRAFFIC_BYTES = 171_990_000
 
+def quantile(xs, q):
+    """The q-quantile of xs (nearest rank)."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -533,7 +539,10 @@ def run_attention_only(args):
     nq = len(w.query) * w.q_len
     line = {"metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
             "workload": args.workload, "value": nq / (tot_ms / 1e3), "unit": "branch-queries/s",
-            "ms_per_call": tot_ms, "partial_kernel_ms": pk_ms, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_call": tot_ms, "partial_kernel_ms": pk_ms,
+            "p10_p90_ms": {"call": [quantile(tot, 0.1), quantile(tot, 0.9)],
+                           "partial_kernels": [quantile(part, 0.1), quantile(part, 0.9)]},
+            "steps": args.steps, "warmup": args.warmup,
             "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
             "config": {"workload": desc, "step": "tree decode attention on a prebuilt tree (plan cached)",
                        "l2": "flushed between calls (256 MiB read)"},
