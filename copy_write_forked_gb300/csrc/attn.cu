@@ -54,6 +54,178 @@ constexpr int ML_BYTES = NCONS * 16 * 2 * 4;
 constexpr size_t SMEM_BF16 = 1024 + (size_t)NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8 + ML_BYTES;
 
 
+// ------------------------------------------------ consumer side of one chunk
+// The P = 4 / rt consumer warps of a row tile split head_dim: warp w owns row
+// tile r = w / P and columns [(w % P) NCOL, (w % P + 1) NCOL), NCOL = 128 / P,
+// and runs every tile of every stage.  Each of those warps computes the row
+// tile's scores and softmax in full (identical bits in all of them), and its
+// own slice of P V, so at the chunk's end every warp stores its slice of the
+// partial rows directly: no exchange between warps, and fewer accumulator
+// registers (128 / P columns per row).
+struct ConsumerCtx {
+    const AttnArgs* a;
+    uint32_t base, bar_full, bar_empty;
+    volatile int* abortp;
+    int warp, lane, c;
+};
+
+template <int P>
+__device__ __forceinline__ void consume_chunk(const ConsumerCtx& x, const AttnUnit& U, int32_t t, int32_t cend,
+                                              int32_t& stage) {
+    constexpr int NCOL = D / P, NT = NCOL / 8;   // columns and 8-column n-tiles of this warp
+    const AttnArgs& a = *x.a;
+    const AttnPlanDev& pl = a.plan;
+    const int warp = x.warp, lane = x.lane;
+    const int r = warp / P, col0 = (warp % P) * NCOL;
+    const float NEG_INF = -INFINITY;
+    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
+    // query fragments of rows r*16 + lane/4 (+8), and their visibility limits
+    uint32_t qa[8][4];
+    int32_t lim0 = 0, lim1 = 0;
+    {
+        const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
+        const bool v0 = row0 < U.n_rows, v1 = row1 < U.n_rows;
+        const AttnRow R0 = v0 ? unit_row(pl, U, row0) : AttnRow{0, 0};
+        const AttnRow R1 = v1 ? unit_row(pl, U, row1) : AttnRow{0, 0};
+        lim0 = R0.limit;
+        lim1 = R1.limit;
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R0.q_row * D);
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(Q + (int64_t)R1.q_row * D);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int w = ks * 8 + (lane & 3);   // 32-bit word index of column ks*16 + 2*(lane&3)
+            qa[ks][0] = v0 ? q0[w] : 0u;
+            qa[ks][1] = v1 ? q1[w] : 0u;
+            qa[ks][2] = v0 ? q0[w + 4] : 0u;
+            qa[ks][3] = v1 ? q1[w + 4] : 0u;
+        }
+    }
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+    for (int32_t st = t; st < cend; st += 4, ++stage) {
+        const int slot = stage % NSTAGE;
+        const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
+        const int ntiles = min(4, cend - st);
+        const bool last = st + 4 >= cend;
+        bool ok = !*x.abortp;
+        if (ok) {
+            ok = mbar_wait(x.bar_full + 8 * slot, ph, x.abortp);
+            if (!ok) {
+                *x.abortp = 1;
+                atomicCAS(&a.meta->status, 0, DENDRITE_ETIMEOUT);
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok) && !*x.abortp;
+        for (int ti = 0; ok && ti < ntiles; ++ti) {
+            const uint32_t kt = x.base + slot * STAGE_BYTES + ti * SLOT_BYTES;
+            const uint32_t vt = kt + 2 * HALF_BYTES;
+            // S = Q K^T (16 rows x 16 tokens)
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3;
+                const int tok = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kt + swz(tok, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+                    mma16816(sc[0], qa[ks], b0, b1);
+                    mma16816(sc[1], qa[ks], b2, b3);
+                }
+            }
+            // scale, mask by per-row visibility, online softmax
+            const int32_t pos0 = (U.blk_start + (st - U.tile_off) + ti) * BS + (lane & 3) * 2;
+            float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int32_t pos = pos0 + nt * 8 + e;
+                    sc[nt][e] = pos < lim0 ? sc[nt][e] * a.scale_log2 : NEG_INF;
+                    sc[nt][2 + e] = pos < lim1 ? sc[nt][2 + e] * a.scale_log2 : NEG_INF;
+                    mx0 = fmaxf(mx0, sc[nt][e]);
+                    mx1 = fmaxf(mx1, sc[nt][2 + e]);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float u0s = n0 == NEG_INF ? 0.f : n0, u1s = n1 == NEG_INF ? 0.f : n1;
+            const float al0 = exp2f(m0 - u0s), al1 = exp2f(m1 - u1s);
+            m0 = n0;
+            m1 = n1;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    sc[nt][e] = exp2f(sc[nt][e] - u0s);
+                    sc[nt][2 + e] = exp2f(sc[nt][2 + e] - u1s);
+                }
+            }
+            // P goes to the tensor cores in bf16; the row sums use the same
+            // rounded weights so numerator and denominator stay consistent
+            uint32_t pa[4];
+            pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+            pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+            pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+            pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+            const float ps0 = bf16_pair_sum(pa[0]) + bf16_pair_sum(pa[2]);
+            const float ps1 = bf16_pair_sum(pa[1]) + bf16_pair_sum(pa[3]);
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                o[n][0] *= al0;
+                o[n][1] *= al0;
+                o[n][2] *= al1;
+                o[n][3] *= al1;
+            }
+            // O[:, col0 : col0 + NCOL] += P V[:, col0 : col0 + NCOL]
+            {
+                const int mi = lane >> 3;
+                const int tok = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vt + swz(tok, col0 + np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
+                    mma16816(o[2 * np], pa, b0, b1);
+                    mma16816(o[2 * np + 1], pa, b2, b3);
+                }
+            }
+        }
+
+        if (last) {
+            // ---------------------------------------- end of this unit's chunk
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            const int32_t prow0 = U.prow_base + (x.c - U.cfirst) * U.n_rows;
+            if (ok) {
+                const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
+                if (row0 < U.n_rows) {
+                    float* dst = a.part_acc + (int64_t)(prow0 + row0) * D + col0 + (lane & 3) * 2;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][0], o[n][1]);
+                    if (col0 == 0 && (lane & 3) == 0) a.part_ml[prow0 + row0] = make_float2(m0, l0);
+                }
+                if (row1 < U.n_rows) {
+                    float* dst = a.part_acc + (int64_t)(prow0 + row1) * D + col0 + (lane & 3) * 2;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2], o[n][3]);
+                    if (col0 == 0 && (lane & 3) == 0) a.part_ml[prow0 + row1] = make_float2(m1, l1);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x.bar_empty + 8 * slot);
+    }
+}
+
 // ============================================================ bf16 kernel
 __global__ void __launch_bounds__(THREADS, 2)
 k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -153,19 +325,34 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
 
     // ---------------------------------------------------------- consumers
-    // Warp w owns row tile r = w / P of the unit (P = 4 / rt) and, within
-    // each stage, the tiles p, p + P, ... where p = w % P.
+    // Units of up to 16 rows (one row tile): warp w takes tiles w, w + 4, ...
+    // of each stage and the four warps combine their states at the chunk's
+    // end.  Units of 32 or 64 rows: consume_chunk (the warps of a row tile
+    // split head_dim instead).  Splitting head_dim for 16-row units too made
+    // every warp compute each tile's scores, which the beam step could not
+    // afford (34.7 -> 40.8 us); for 32 rows it wins (spec-verify leaves).
     const float NEG_INF = -INFINITY;
     const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
     int32_t stage = 0;
     int32_t t = t_begin, u = u0;
+    const ConsumerCtx ctx{&a, base, bar_full, bar_empty, abortp, warp, lane, c};
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
         const int32_t uend = U.tile_off + U.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
-        const int P = 4 / U.rt;
-        const int r = warp / P, pidx = warp % P;
+        if (U.rt != 1) {
+            // 32 or 64 rows: the warps of a row tile split head_dim (no exchange)
+            if (U.rt == 2) consume_chunk<2>(ctx, U, t, cend, stage);
+            else consume_chunk<1>(ctx, U, t, cend, stage);
+            t = cend;
+            ++u;
+            continue;
+        }
+        // up to 16 rows: the four warps split each stage's tiles and combine
+        // their states at the chunk's end
+        constexpr int P = 4;
+        const int r = 0, pidx = warp;
 
         // query fragments of rows r*16 + lane/4 (+8), and their visibility limits
         uint32_t qa[8][4];
@@ -293,78 +480,58 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
                 const int32_t prow0 = U.prow_base + (c - U.cfirst) * U.n_rows;
-                if (P == 1) {
-                    if (ok) {
-                        const int row0 = r * 16 + (lane >> 2), row1 = row0 + 8;
-                        if (row0 < U.n_rows) {
-                            float* dst = a.part_acc + (int64_t)(prow0 + row0) * D + (lane & 3) * 2;
+                // combine the P warps of each row tile through this stage's buffer
+                consumer_sync();   // every warp is done reading the stage's K/V
+                float* ob = reinterpret_cast<float*>(sm + slot * STAGE_BYTES) + warp * 16 * D;
+                {
+                    const int ra = lane >> 2, rb = ra + 8;
 #pragma unroll
-                            for (int n = 0; n < 16; ++n)
-                                *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][0], o[n][1]);
-                            if ((lane & 3) == 0) a.part_ml[prow0 + row0] = make_float2(m0, l0);
-                        }
-                        if (row1 < U.n_rows) {
-                            float* dst = a.part_acc + (int64_t)(prow0 + row1) * D + (lane & 3) * 2;
-#pragma unroll
-                            for (int n = 0; n < 16; ++n)
-                                *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][2], o[n][3]);
-                            if ((lane & 3) == 0) a.part_ml[prow0 + row1] = make_float2(m1, l1);
-                        }
+                    for (int n = 0; n < 16; ++n) {
+                        const int col = n * 8 + (lane & 3) * 2;
+                        *reinterpret_cast<float2*>(ob + ra * D + (col ^ ((ra & 7) << 3))) =
+                            make_float2(o[n][0], o[n][1]);
+                        *reinterpret_cast<float2*>(ob + rb * D + (col ^ ((rb & 7) << 3))) =
+                            make_float2(o[n][2], o[n][3]);
                     }
-                } else {
-                    // combine the P warps of each row tile through this stage's buffer
-                    consumer_sync();   // every warp is done reading the stage's K/V
-                    float* ob = reinterpret_cast<float*>(sm + slot * STAGE_BYTES) + warp * 16 * D;
-                    {
-                        const int ra = lane >> 2, rb = ra + 8;
-#pragma unroll
-                        for (int n = 0; n < 16; ++n) {
-                            const int col = n * 8 + (lane & 3) * 2;
-                            *reinterpret_cast<float2*>(ob + ra * D + (col ^ ((ra & 7) << 3))) =
-                                make_float2(o[n][0], o[n][1]);
-                            *reinterpret_cast<float2*>(ob + rb * D + (col ^ ((rb & 7) << 3))) =
-                                make_float2(o[n][2], o[n][3]);
-                        }
-                        if ((lane & 3) == 0) {
-                            ml[(warp * 16 + ra) * 2] = m0;
-                            ml[(warp * 16 + ra) * 2 + 1] = l0;
-                            ml[(warp * 16 + rb) * 2] = m1;
-                            ml[(warp * 16 + rb) * 2 + 1] = l1;
-                        }
+                    if ((lane & 3) == 0) {
+                        ml[(warp * 16 + ra) * 2] = m0;
+                        ml[(warp * 16 + ra) * 2 + 1] = l0;
+                        ml[(warp * 16 + rb) * 2] = m1;
+                        ml[(warp * 16 + rb) * 2 + 1] = l1;
                     }
-                    consumer_sync();
-                    if (ok) {
-                        const float* obase = reinterpret_cast<const float*>(sm + slot * STAGE_BYTES);
-                        const int items = U.rt * 16 * (D / 4);
-                        for (int idx = threadIdx.x; idx < items; idx += NCONS * 32) {
-                            const int rr = idx / (16 * (D / 4));
-                            const int row = (idx / (D / 4)) % 16;
-                            const int d = (idx % (D / 4)) * 4;
-                            const int grow = rr * 16 + row;
-                            if (grow >= U.n_rows) continue;
-                            float M = NEG_INF;
-                            for (int p2 = 0; p2 < P; ++p2) M = fmaxf(M, ml[((rr * P + p2) * 16 + row) * 2]);
-                            const float Mu = M == NEG_INF ? 0.f : M;
-                            float L = 0.f;
-                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int p2 = 0; p2 < P; ++p2) {
-                                const int w2 = rr * P + p2;
-                                const float wgt = exp2f(ml[(w2 * 16 + row) * 2] - Mu);
-                                L += ml[(w2 * 16 + row) * 2 + 1] * wgt;
-                                const float4 v = *reinterpret_cast<const float4*>(
-                                    obase + (w2 * 16 + row) * D + (d ^ ((row & 7) << 3)));
-                                acc.x += v.x * wgt;
-                                acc.y += v.y * wgt;
-                                acc.z += v.z * wgt;
-                                acc.w += v.w * wgt;
-                            }
-                            *reinterpret_cast<float4*>(a.part_acc + (int64_t)(prow0 + grow) * D + d) = acc;
-                            if (d == 0) a.part_ml[prow0 + grow] = make_float2(M, L);
-                        }
-                    }
-                    fence_async_smem();
-                    consumer_sync();   // buffer free again before it is handed back to TMA
                 }
+                consumer_sync();
+                if (ok) {
+                    const float* obase = reinterpret_cast<const float*>(sm + slot * STAGE_BYTES);
+                    const int items = 16 * (D / 4);   // one row tile
+                    for (int idx = threadIdx.x; idx < items; idx += NCONS * 32) {
+                        const int rr = idx / (16 * (D / 4));
+                        const int row = (idx / (D / 4)) % 16;
+                        const int d = (idx % (D / 4)) * 4;
+                        const int grow = rr * 16 + row;
+                        if (grow >= U.n_rows) continue;
+                        float M = NEG_INF;
+                        for (int p2 = 0; p2 < P; ++p2) M = fmaxf(M, ml[((rr * P + p2) * 16 + row) * 2]);
+                        const float Mu = M == NEG_INF ? 0.f : M;
+                        float L = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int p2 = 0; p2 < P; ++p2) {
+                            const int w2 = rr * P + p2;
+                            const float wgt = exp2f(ml[(w2 * 16 + row) * 2] - Mu);
+                            L += ml[(w2 * 16 + row) * 2 + 1] * wgt;
+                            const float4 v = *reinterpret_cast<const float4*>(
+                                obase + (w2 * 16 + row) * D + (d ^ ((row & 7) << 3)));
+                            acc.x += v.x * wgt;
+                            acc.y += v.y * wgt;
+                            acc.z += v.z * wgt;
+                            acc.w += v.w * wgt;
+                        }
+                        *reinterpret_cast<float4*>(a.part_acc + (int64_t)(prow0 + grow) * D + d) = acc;
+                        if (d == 0) a.part_ml[prow0 + grow] = make_float2(M, L);
+                    }
+                }
+                fence_async_smem();
+                consumer_sync();   // buffer free again before it is handed back to TMA
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
