@@ -41,9 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of k_attn_partial_bf16 on this step,
 # from one ncu capture of the kernel as it is now (dram__bytes_read.sum
-# 168.27 MB + dram__bytes_write.sum 3.73 MB); to be re-taken whenever that
+# 168.27 MB + dram__bytes_write.sum 4.62 MB); to be re-taken whenever that
 # kernel changes.
-BEAM_PARTIAL_TRAFFIC_BYTES = 171_990_000
+BEAM_PARTIAL_TRAFFIC_BYTES = 172_880_000
 
 def quantile(xs, q):
     """The q-quantile of xs (nearest rank)."""
