@@ -174,9 +174,23 @@ void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queri
         for (int32_t si = 0; si < S; ++si)
             for (int32_t k = 0; k < segs[si].n_members; ++k) mseg[cur[members[segs[si].member_offset + k]]++] = si;
     }
-    for (int32_t q = 0; q < n_queried; ++q)
-        std::sort(mseg.begin() + moff[q], mseg.begin() + moff[q + 1],
-                  [&](int32_t a, int32_t b) { return segs[a].block_start < segs[b].block_start; });
+    for (int32_t q = 0; q < n_queried; ++q) {
+        // a member usually reads a handful of segments (its tree depth)
+        if (moff[q + 1] - moff[q] > 32) {
+            std::sort(mseg.begin() + moff[q], mseg.begin() + moff[q + 1],
+                      [&](int32_t a, int32_t b) { return segs[a].block_start < segs[b].block_start; });
+            continue;
+        }
+        for (int32_t e = moff[q] + 1; e < moff[q + 1]; ++e) {   // insertion sort
+            const int32_t v = mseg[e], key = segs[v].block_start;
+            int32_t k = e - 1;
+            while (k >= moff[q] && segs[mseg[k]].block_start > key) {
+                mseg[k + 1] = mseg[k];
+                --k;
+            }
+            mseg[k + 1] = v;
+        }
+    }
     // the segment before each segment (the same for all its members), the
     // segments after each segment, and the members whose path ends there
     prev.assign(S, -1);
@@ -204,10 +218,17 @@ void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queri
             if (moff[q + 1] > moff[q]) emem[ec[mseg[moff[q + 1] - 1]]++] = q;
     }
     // decide in increasing block order
-    order.resize(S);
-    for (int32_t si = 0; si < S; ++si) order[si] = si;
-    std::stable_sort(order.begin(), order.end(),
-                     [&](int32_t a, int32_t b) { return segs[a].block_start < segs[b].block_start; });
+    {
+        // counting sort by first block (stable)
+        int32_t max_start = 0;
+        for (const Segment& sg : segs) max_start = std::max(max_start, sg.block_start);
+        static thread_local std::vector<int32_t> cnt;
+        cnt.assign((size_t)max_start + 2, 0);
+        for (const Segment& sg : segs) cnt[sg.block_start + 1]++;
+        for (int32_t b = 0; b <= max_start; ++b) cnt[b + 1] += cnt[b];
+        order.resize(S);
+        for (int32_t si = 0; si < S; ++si) order[cnt[segs[si].block_start]++] = si;
+    }
     ext.resize(S);
     for (int32_t si = 0; si < S; ++si) ext[si] = segs[si].block_start;
     folded.assign(S, 0);
