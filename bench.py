@@ -351,9 +351,9 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
 
-    # fork 1 + append 2 (meta, copy) + attention 4 (the step's new tree needs a new
-    # plan: upload and row expansion, then partial and merge) + free 1
-    gpu_launches = 8 * args.steps
+    # fork 1 + append 2 (meta, copy) + attention 3 (the step's new tree needs a new
+    # plan: its upload, then partial and merge) + free 1
+    gpu_launches = 7 * args.steps
     line = {
         "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
         "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
@@ -471,7 +471,7 @@ def run_decode_layers(args):
                          "peak": peak, "peak_source": src, "unit": "GB/s",
                          "frac": unique / (pk / 1e3) / 1e9 / peak, "algorithmic_bytes": unique},
             "plan_us_layer0": plan_us[0], "plan_us_other_layers_max": max(plan_us[1:]),
-            "gpu_launches_per_step": 1 + 1 + 2 + NL * 3 + 1}   # + plan upload and row expansion at layer 0
+            "gpu_launches_per_step": 1 + 1 + 1 + NL * 3 + 1}   # fork, append metadata, plan upload (layer 0), per layer copy + partial + merge, free
     if rank == 0:
         print(json.dumps(line), flush=True)
     pool.close()
