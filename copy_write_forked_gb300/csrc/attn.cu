@@ -645,10 +645,11 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
 // with the acc rows fetched four partials at a time.  Partial rows are read
 // through L2 only (they were written by the previous kernel).
 // WIDE (head_dim 128): lane l owns columns 4 l .. 4 l + 3, so a partial row is
-// one 16-byte load per lane, eight partials are in flight per warp, and four
-// CTAs fit on an SM.
+// one 16-byte load per lane and eight partials are in flight per warp; the
+// launch bound leaves it 128 registers (at 64 it spilled, and the beam step
+// took 2 us longer).
 template <typename T, bool WIDE>
-__global__ void __launch_bounds__(256, WIDE ? 4 : 1) k_attn_merge(const AttnArgs a) {
+__global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     pdl_trigger();
     const AttnPlanDev& pl = a.plan;

@@ -472,20 +472,23 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
     __syncthreads();
     if (threadIdx.x == 0) {
         // a single CTA is its own last one: the barrier above already ordered
-        // its threads' updates
+        // its threads' updates.  Otherwise one acquire-release increment both
+        // publishes this CTA's updates (ordered before it by the barrier) and,
+        // in the last CTA, makes every other CTA's updates visible.
         if (gridDim.x == 1) {
             is_last = 1;
         } else {
-            __threadfence();
-            is_last = atomicAdd(&meta->rel_done, 1) == (int32_t)gridDim.x - 1;
+            int32_t prev;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(&meta->rel_done) : "memory");
+            is_last = prev == (int32_t)gridDim.x - 1;
         }
         if (is_last) {
-            __threadfence();
-            lo = atomicAdd(&meta->rel_lo, 0);
-            hi = atomicAdd(&meta->rel_hi, 0);
-            cnt = atomicAdd(&meta->rel_count, 0);
-            top0 = atomicAdd(&meta->top, 0);
-            st = atomicAdd(&meta->status, 0);
+            volatile DevMeta* vm = meta;
+            lo = vm->rel_lo;
+            hi = vm->rel_hi;
+            cnt = vm->rel_count;
+            top0 = vm->top;
+            st = vm->status;
         }
     }
     __syncthreads();
