@@ -45,11 +45,11 @@ def test_mcts_folded_plans_match_and_drop_partials():
     o_all, st_all = run(w, FOLD_ALL, TOL_BF16)
     assert st_def["n_partials"] < st_off["n_partials"]
     assert st_all["n_partials"] <= st_def["n_partials"]
-    # without folding every streamed tile is distinct; folding re-reads some
-    # tiles but leaves the distinct ones unchanged
-    assert st_off["tiles"] == st_off["unique_tiles"]
+    # folding changes which tiles are streamed (and how often: every row
+    # group of a unit streams its tiles) but not the distinct tiles
     assert st_def["unique_tiles"] == st_all["unique_tiles"] == st_off["unique_tiles"]
-    assert st_off["unique_tiles"] < st_def["tiles"] <= st_all["tiles"]
+    for st in (st_off, st_def, st_all):
+        assert st["tiles"] >= st["unique_tiles"]
     assert st_def["n_tc_units"] > 0
     for o in (o_def, o_all):
         assert (o.float() - o_off.float()).abs().max().item() <= 2 * TOL_BF16
