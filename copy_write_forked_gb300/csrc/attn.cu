@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include "attn_common.cuh"
 
@@ -1290,6 +1291,24 @@ AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1]
     return v;
 }
 
+// The same plan view over another copy of the plan bytes.
+AttnPlanDev plan_rebase(AttnPlanDev v, const char* from, const char* to) {
+    auto mv = [&](auto*& ptr) {
+        using P = std::remove_reference_t<decltype(ptr)>;
+        ptr = reinterpret_cast<P>(to + (reinterpret_cast<const char*>(ptr) - from));
+    };
+    mv(v.segs);
+    mv(v.members);
+    mv(v.units);
+    mv(v.cta_begin);
+    mv(v.cta_unit);
+    mv(v.tc_cta_begin);
+    mv(v.tc_cta_unit);
+    mv(v.path_off);
+    mv(v.path);
+    return v;
+}
+
 // CTAs the tensor-core kernel may use on this pool (0: not used).
 int tc_ctas(const dendrite_pool* p) {
     return (p->dtype == DENDRITE_BF16 && p->tc_ready && p->tc_min_rows >= 0) ? p->sm_count : 0;
@@ -1480,9 +1499,37 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
     cudaStream_t s = (cudaStream_t)stream;
     const int max_ctas = p->sm_count * p->attn_ctas_per_sm;
     PlanCache& pc = p->plan;
-    const bool hit = pc.valid && pc.version == p->version && pc.q_len == q_len && pc.n_q_heads == n_q_heads &&
-                     (int32_t)pc.branches.size() == n && std::equal(branches, branches + n, pc.branches.begin());
-    if (!hit) {
+    const bool same_query = pc.valid && pc.q_len == q_len && pc.n_q_heads == n_q_heads &&
+                            (int32_t)pc.branches.size() == n && std::equal(branches, branches + n, pc.branches.begin());
+    const bool hit = same_query && pc.version == p->version;
+    // Only appends since the plan was built, and no queried branch reached a
+    // new block: the segments, units and partition are unchanged, and only
+    // the members' lengths (their rows' visibility limits) need refreshing.
+    bool refresh = !hit && same_query && pc.shape_version == p->shape_version;
+    for (int32_t i = 0; refresh && i < n; ++i)
+        refresh = (p->br[branches[i]].len + p->block_size - 1) / p->block_size == pc.n_blocks[i];
+    if (refresh) {
+        const auto t0 = std::chrono::steady_clock::now();
+        const int ib = p->plan_buf;
+        p->plan_buf ^= 1;
+        DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied[ib]));
+        if (ib != pc.buf) std::memcpy(p->h_plan[ib], p->h_plan[pc.buf], pc.bytes);
+        AttnMember* m = reinterpret_cast<AttnMember*>(p->h_plan[ib] + pc.members_off);
+        for (int32_t e = 0; e < pc.n_members; ++e) m[e].len = p->br[branches[m[e].qi]].len;
+        {
+            const int64_t n16 = (int64_t)(pc.bytes / 16);
+            const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
+            DENDRITE_CUDA(launch_pdl(k_plan_upload, dim3(grid), dim3(256), 0, s,
+                                     reinterpret_cast<const uint4*>(p->h_plan[ib]),
+                                     reinterpret_cast<uint4*>(p->d_plan[ib]), n16));
+        }
+        DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
+        pc.dev = plan_rebase(pc.dev, p->d_plan[pc.buf], p->d_plan[ib]);
+        pc.buf = ib;
+        pc.version = p->version;
+        pc.stats.refreshed = 1;
+        pc.stats.plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    } else if (!hit) {
         const auto t0 = std::chrono::steady_clock::now();
         static thread_local HostPlan hp;
         hp.clear();
@@ -1508,6 +1555,13 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
         pc.version = p->version;
+        pc.shape_version = p->shape_version;
+        pc.buf = ib;
+        pc.bytes = off[kPlanSections];
+        pc.members_off = off[1];
+        pc.n_members = (int32_t)hp.members.size();
+        pc.n_blocks.resize(n);
+        for (int32_t i = 0; i < n; ++i) pc.n_blocks[i] = (p->br[branches[i]].len + p->block_size - 1) / p->block_size;
         pc.q_len = q_len;
         pc.n_q_heads = n_q_heads;
         pc.branches.assign(branches, branches + n);
@@ -1519,8 +1573,10 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         pc.stats.unique_tiles = hp.unique_tiles;
         pc.stats.n_tc_units = hp.n_tc_units;
         pc.stats.n_tc_ctas = pc.dev.n_tc_ctas;
+        pc.stats.refreshed = 0;
         pc.stats.plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
     } else {
+        pc.stats.refreshed = 0;
         pc.stats.plan_us = 0.0;
     }
     AttnArgs a = attn_args(p, layer, Q, out);

@@ -177,11 +177,16 @@ struct PendingAppend {
 
 struct PlanCache {
     bool valid = false;
-    uint64_t version = 0;
+    uint64_t version = 0, shape_version = 0;
     int32_t q_len = 0, n_q_heads = 0;
     std::vector<int32_t> branches;
+    std::vector<int32_t> n_blocks;   // each queried branch's block count when the plan was built
     AttnPlanDev dev{};
     size_t n_partial_rows = 0;
+    int buf = 0;                     // plan buffer pair holding the plan
+    size_t bytes = 0;                // packed plan size
+    size_t members_off = 0;          // byte offset of the member list in the packed plan
+    int32_t n_members = 0;
     dendrite_plan_stats stats{};
 };
 
@@ -236,7 +241,8 @@ struct dendrite_pool {
     std::vector<int32_t> free_handles;
     std::vector<dendrite::Node> nodes;
     std::vector<int32_t> free_nodes;
-    uint64_t version = 1;
+    uint64_t version = 1;          // any change to the tree or its lengths
+    uint64_t shape_version = 1;    // any change but appends (forks, frees, truncations, new branches)
     int32_t poisoned = 0;
 
     dendrite::Staging staging;

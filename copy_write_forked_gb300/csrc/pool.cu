@@ -929,6 +929,7 @@ int dendrite_branch_new(dendrite_pool* p, int32_t* out) {
     p->br[h].len = 0;
     p->br[h].node = new_node(p, -1, 0, h);
     p->version++;
+    p->shape_version++;   // the tree's shape changed, not only lengths
     *out = h;
     return DENDRITE_OK;
 }
@@ -969,6 +970,7 @@ int dendrite_fork_batch(dendrite_pool* p, const int32_t* parents, const int32_t*
         }
     }
     p->version++;
+    p->shape_version++;   // the tree's shape changed, not only lengths
     prof_begin(p, T_FORK, s);
     int rc;
     const size_t n = child.size();
@@ -1130,6 +1132,7 @@ int dendrite_free(dendrite_pool* p, const int32_t* branches, int32_t n, void* st
         drop_node_ref(p, node);
     }
     p->version++;
+    p->shape_version++;   // the tree's shape changed, not only lengths
     return DENDRITE_OK;
 }
 
@@ -1166,6 +1169,7 @@ int dendrite_truncate(dendrite_pool* p, const int32_t* branches, const int32_t* 
         drop_node_ref(p, old);
     }
     p->version++;
+    p->shape_version++;   // the tree's shape changed, not only lengths
     return DENDRITE_OK;
 }
 

@@ -49,7 +49,7 @@ class _Opts(ctypes.Structure):
 class _PlanStats(ctypes.Structure):
     _fields_ = [("n_segments", _i32), ("n_units", _i32), ("n_ctas", _i32), ("n_partials", _i32),
                 ("tiles", _i64), ("unique_tiles", _i64), ("plan_us", ctypes.c_double), ("n_tc_units", _i32),
-                ("n_tc_ctas", _i32)]
+                ("n_tc_ctas", _i32), ("refreshed", _i32), ("reserved", _i32)]
 
 
 class _Segment(ctypes.Structure):

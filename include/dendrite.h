@@ -186,7 +186,9 @@ int dendrite_append_layer(dendrite_pool* pool, int32_t layer, const void* K, con
  * partials, then a log-sum-exp merge); a short shared range may instead be
  * read again by each longer range that follows it (pool option
  * fold_segments).  The plan built from the branch tree is cached until the
- * tree changes.  `branches` may not hold duplicates.
+ * tree changes; after appends alone, where no queried branch reached a new
+ * block, only its members' lengths are refreshed.  `branches` may not hold
+ * duplicates.
  * DENDRITE_ELIMIT if a shared range would be read by 2^24 or more query rows
  * per KV head, or the plan outgrows 32-bit indices.
  * Reads layer 0 of a multi-layer pool.
@@ -293,9 +295,14 @@ typedef struct dendrite_plan_stats {
     int32_t n_partials;     /* partial triples written                              */
     int64_t tiles;          /* (block, kv head) tiles streamed by the partial kernel */
     int64_t unique_tiles;   /* distinct (block, kv head) tiles among them            */
-    double  plan_us;        /* host time spent building the plan (0 if cached)      */
+    double  plan_us;        /* host time spent building or refreshing the plan      *
+                             * (0 if it was reused as it was)                        */
     int32_t n_tc_units;     /* units among n_units run on the tcgen05 kernel        */
     int32_t n_tc_ctas;      /* CTAs of the tcgen05 kernel (not counted in n_ctas)   */
+    int32_t refreshed;      /* 1: the cached plan only had its members' lengths     *
+                             * refreshed (only appends since it was built, and no   *
+                             * queried branch reached a new block); 0 otherwise     */
+    int32_t reserved;
 } dendrite_plan_stats;
 int dendrite_last_plan_stats(dendrite_pool* pool, dendrite_plan_stats* out);
 

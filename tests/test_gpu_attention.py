@@ -109,6 +109,45 @@ def test_small_merges_odd_groups(n_kv, n_q):
     run_and_check(w, TOL_BF16)
 
 
+@pytest.mark.parametrize("make", [lambda: W.beam(requests=2, prefix=100, width=3, divergent=5),
+                                  lambda: W.spec_verify(requests=2, prefix=100, paths=3, draft=8)])
+def test_appends_within_blocks_refresh_the_plan(make):
+    """A decode loop without forks: every step appends one token to each
+    queried branch and attends again.  While no queried branch reaches a new
+    block the cached plan only has its lengths refreshed; the step that
+    crosses a block boundary rebuilds it.  Every step matches the oracle."""
+    base = make()
+    extra = [W.Op("append", tuple(base.query), 1) for _ in range(10)]
+    w_full = W.Workload(base.name + "_decode", base.n_kv_heads, base.n_q_heads, base.head_dim, base.block_size,
+                        base.dtype, list(base.ops) + extra, base.query, base.q_len, base.seed)
+    pool = pool_for(w_full)
+    h = run_script(pool, base)
+    br = [h[b] for b in base.query]
+    Q = base.q("cuda")
+    pool.tree_attn_decode(Q, br)
+    assert pool.last_plan_stats()["refreshed"] == 0
+    lens = {b: l for b, l in base.lengths().items()}
+    seen = set()
+    for k in range(len(extra)):
+        idx = len(base.ops) + k
+        blocks_before = {b: -(-lens[b] // 16) for b in base.query}
+        K, V = w_full.kv(idx, "cuda")
+        pool.append_kv(br, K, V)
+        for b in base.query:
+            lens[b] += 1
+        out = pool.tree_attn_decode(Q, br)
+        pool.sync()
+        st = pool.last_plan_stats()
+        crossed = any(-(-lens[b] // 16) != blocks_before[b] for b in base.query)
+        assert st["refreshed"] == (0 if crossed else 1), (k, crossed)
+        seen.add(st["refreshed"])
+        w_k = W.Workload(w_full.name, w_full.n_kv_heads, w_full.n_q_heads, w_full.head_dim, w_full.block_size,
+                         w_full.dtype, w_full.ops[:idx + 1], w_full.query, w_full.q_len, w_full.seed)
+        check_attention(w_k, out, list(range(len(base.query))), TOL_BF16)
+    assert seen == {0, 1}
+    pool.close()
+
+
 def test_mcts_small():
     w = W.mcts(root=256, iters=60, width=4, per_node=32, max_depth=6)
     run_and_check(w, TOL_BF16)
