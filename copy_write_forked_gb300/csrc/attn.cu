@@ -1093,7 +1093,8 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     // kv head) pair once
     for (const Segment& sg : hp.psegs) hp.unique_tiles += (int64_t)sg.block_count * nkv;
     if (p->fold_pct >= 0)
-        fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, hp.queried.data(), n,
+        fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, n_nodes,
+                      hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
                       hp.psegs, hp.seg_members);
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by

@@ -288,6 +288,7 @@ struct Segment {
     int32_t block_count;
     int32_t member_offset;
     int32_t n_members;
+    int32_t owner;      // node whose blocks these are (a node's segments are consecutive, ascending)
 };
 void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
                    const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
@@ -303,8 +304,9 @@ struct FoldParams {
     int32_t small_rows;
     int32_t fold_pct;
 };
-void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queried, std::vector<Segment>& segs,
-                   std::vector<int32_t>& members);
+void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                   const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
+                   std::vector<Segment>& segs, std::vector<int32_t>& members);
 
 // Attention (attn.cu)
 int attn_setup(dendrite_pool* p);      // tensor maps, occupancy

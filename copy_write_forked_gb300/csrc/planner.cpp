@@ -81,6 +81,7 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
             for (size_t k = g0; k < g1; ++k) members.push_back(sorted[k].member);
             sg.n_members = (int32_t)(g1 - g0);
             sg.rep_node = queried[sorted[g0].member];
+            sg.owner = node;
             segs.push_back(sg);
             continue;
         }
@@ -104,6 +105,7 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
                 members.insert(members.end(), mem.begin(), mem.end());
                 sg.n_members = (int32_t)mem.size();
                 sg.rep_node = queried[mem.front()];
+                sg.owner = node;
                 segs.push_back(sg);
                 lo = cut;
             }
@@ -156,52 +158,58 @@ int64_t estimate_ns(const FoldParams& fp, int64_t T, int64_t R, bool with_units)
 
 }  // namespace
 
-void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queried, std::vector<Segment>& segs,
-                   std::vector<int32_t>& members) {
+void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                   const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
+                   std::vector<Segment>& segs, std::vector<int32_t>& members) {
     const int32_t S = (int32_t)segs.size();
     if (fp.fold_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
-    static thread_local std::vector<int32_t> moff, mseg, prev, koff, kseg, eoff, emem, order, ext;
+    static thread_local std::vector<int32_t> node_first, node_count, prev, koff, kseg, eoff, emem, order, ext;
     static thread_local std::vector<char> folded;
-    // every member's segments, in block order
-    moff.assign(n_queried + 1, 0);
-    for (const Segment& sg : segs)
-        for (int32_t k = 0; k < sg.n_members; ++k) moff[members[sg.member_offset + k] + 1]++;
-    for (int32_t q = 0; q < n_queried; ++q) moff[q + 1] += moff[q];
-    mseg.resize(moff[n_queried]);
-    {
-        static thread_local std::vector<int32_t> cur;
-        cur.assign(moff.begin(), moff.end() - 1);
-        for (int32_t si = 0; si < S; ++si)
-            for (int32_t k = 0; k < segs[si].n_members; ++k) mseg[cur[members[segs[si].member_offset + k]]++] = si;
+    const int32_t bs = block_size;
+    // each owner node's segments (consecutive in segs, in ascending blocks)
+    node_first.assign(n_nodes, -1);
+    node_count.assign(n_nodes, 0);
+    for (int32_t si = 0; si < S; ++si) {
+        const int32_t o = segs[si].owner;
+        if (node_first[o] < 0) node_first[o] = si;
+        node_count[o]++;
     }
-    for (int32_t q = 0; q < n_queried; ++q) {
-        // a member usually reads a handful of segments (its tree depth)
-        if (moff[q + 1] - moff[q] > 32) {
-            std::sort(mseg.begin() + moff[q], mseg.begin() + moff[q + 1],
-                      [&](int32_t a, int32_t b) { return segs[a].block_start < segs[b].block_start; });
+    // The segment before each segment in its members' block order (the same
+    // for all of them): the previous segment of the same owner, or for an
+    // owner's first segment, the segment ending at its first block in the
+    // group of the nearest ancestor that owns the block before it.
+    prev.assign(S, -1);
+    for (int32_t si = 0; si < S; ++si) {
+        const Segment& sg = segs[si];
+        if (si > node_first[sg.owner]) {
+            prev[si] = si - 1;
             continue;
         }
-        for (int32_t e = moff[q] + 1; e < moff[q + 1]; ++e) {   // insertion sort
-            const int32_t v = mseg[e], key = segs[v].block_start;
-            int32_t k = e - 1;
-            while (k >= moff[q] && segs[mseg[k]].block_start > key) {
-                mseg[k + 1] = mseg[k];
-                --k;
-            }
-            mseg[k + 1] = v;
+        const int32_t b = sg.block_start;
+        if (b == 0) continue;
+        int32_t a = parent[sg.owner];
+        while (a >= 0 && parent[a] >= 0 && fork_len[a] / bs > b - 1) a = parent[a];
+        if (a < 0 || node_first[a] < 0) continue;
+        // the owner's segment that ends at b
+        int32_t lo = node_first[a], hi = node_first[a] + node_count[a] - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (segs[mid].block_start <= b - 1) lo = mid; else hi = mid - 1;
         }
+        if (segs[lo].block_start + segs[lo].block_count == b) prev[si] = lo;
     }
-    // the segment before each segment (the same for all its members), the
-    // segments after each segment, and the members whose path ends there
-    prev.assign(S, -1);
+    // the segments after each segment, and the members whose blocks end there
     koff.assign(S + 1, 0);
     eoff.assign(S + 1, 0);
-    for (int32_t q = 0; q < n_queried; ++q) {
-        for (int32_t e = moff[q] + 1; e < moff[q + 1]; ++e) prev[mseg[e]] = mseg[e - 1];
-        if (moff[q + 1] > moff[q]) eoff[mseg[moff[q + 1] - 1] + 1]++;
-    }
-    for (int32_t si = 0; si < S; ++si)
+    for (int32_t si = 0; si < S; ++si) {
         if (prev[si] >= 0) koff[prev[si] + 1]++;
+        const Segment& sg = segs[si];
+        const int32_t end = sg.block_start + sg.block_count;
+        for (int32_t k = 0; k < sg.n_members; ++k) {
+            const int32_t m = members[sg.member_offset + k];
+            if ((len[queried[m]] + bs - 1) / bs == end) eoff[si + 1]++;
+        }
+    }
     for (int32_t si = 0; si < S; ++si) {
         koff[si + 1] += koff[si];
         eoff[si + 1] += eoff[si];
@@ -209,13 +217,19 @@ void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queri
     kseg.resize(koff[S]);
     emem.resize(eoff[S]);
     {
-        static thread_local std::vector<int32_t> kc, ec;
+        static thread_local std::vector<int32_t> kc;
         kc.assign(koff.begin(), koff.end() - 1);
-        ec.assign(eoff.begin(), eoff.end() - 1);
         for (int32_t si = 0; si < S; ++si)
             if (prev[si] >= 0) kseg[kc[prev[si]]++] = si;
-        for (int32_t q = 0; q < n_queried; ++q)   // ascending member order
-            if (moff[q + 1] > moff[q]) emem[ec[mseg[moff[q + 1] - 1]]++] = q;
+        int32_t e = 0;
+        for (int32_t si = 0; si < S; ++si) {   // members stay in ascending order within a segment
+            const Segment& sg = segs[si];
+            const int32_t end = sg.block_start + sg.block_count;
+            for (int32_t k = 0; k < sg.n_members; ++k) {
+                const int32_t m = members[sg.member_offset + k];
+                if ((len[queried[m]] + bs - 1) / bs == end) emem[e++] = m;
+            }
+        }
     }
     // decide in increasing block order
     {
@@ -264,12 +278,14 @@ void fold_segments(const FoldParams& fp, const int32_t* queried, int32_t n_queri
         o.block_count = end - ext[si];
         o.member_offset = (int32_t)out_members.size();
         if (!folded[si]) {
+            o.owner = sg.owner;
             o.rep_node = sg.rep_node;
             o.n_members = sg.n_members;
             out_members.insert(out_members.end(), members.begin() + sg.member_offset,
                                members.begin() + sg.member_offset + sg.n_members);
         } else {
             if (eoff[si + 1] == eoff[si]) continue;
+            o.owner = sg.owner;
             o.rep_node = queried[emem[eoff[si]]];
             o.n_members = eoff[si + 1] - eoff[si];
             out_members.insert(out_members.end(), emem.begin() + eoff[si], emem.begin() + eoff[si + 1]);
@@ -352,6 +368,6 @@ extern "C" int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* par
     const dendrite::FoldParams fp{rows_per_member, tc_min_rows == 0 ? dendrite::kTcMinRowsDefault : tc_min_rows,
                                   dendrite::kMaxUnitRowsBf16,
                                   fold_pct == 0 ? dendrite::kFoldPctDefault : fold_pct};
-    dendrite::fold_segments(fp, queried, n_queried, s, m);
+    dendrite::fold_segments(fp, n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
     return export_segments(s, m, segs, seg_cap, n_segs, members, member_cap, n_members);
 }
