@@ -32,9 +32,11 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
     segs.clear();
     members.clear();
     struct Rec { int32_t grp, cap, member; };
-    static thread_local std::vector<int32_t> slot, order, mem, count;
+    static thread_local std::vector<int32_t> slot, order, mem, count, first_block;
     static thread_local std::vector<Rec> recs, sorted;
     slot.assign(n_nodes, -1);
+    first_block.resize(n_nodes);   // a node's first own block (0 for a root)
+    for (int32_t i = 0; i < n_nodes; ++i) first_block[i] = parent[i] >= 0 ? fork_len[i] / bs : 0;
     order.clear();
     recs.clear();
     // walk every queried branch up to its root: owner node -> [start, cap)
@@ -42,7 +44,7 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
         int32_t node = queried[qi];
         int32_t cap = (len[node] + bs - 1) / bs;
         while (cap > 0) {
-            const int32_t start = parent[node] >= 0 ? fork_len[node] / bs : 0;
+            const int32_t start = first_block[node];
             if (start < cap) {
                 if (slot[node] < 0) {
                     slot[node] = (int32_t)order.size();
@@ -67,10 +69,11 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
         cursor.assign(count.begin(), count.end() - 1);
         for (const Rec& r : recs) sorted[cursor[r.grp]++] = r;
     }
+    members.reserve(recs.size());
     for (int32_t gi = 0; gi < n_grp; ++gi) {
         const size_t g0 = count[gi], g1 = count[gi + 1];
         const int32_t node = order[gi];
-        const int32_t start = parent[node] >= 0 ? fork_len[node] / bs : 0;
+        const int32_t start = first_block[node];
         bool uniform = true;
         for (size_t k = g0 + 1; k < g1 && uniform; ++k) uniform = sorted[k].cap == sorted[g0].cap;
         if (uniform) {   // every member reads [start, cap): one segment, members already in order
