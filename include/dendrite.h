@@ -12,8 +12,10 @@
  *     (refcount > 1) first copies that block (copy-on-write).
  *   - Decode attention walks the tree: keys/values of the shared ancestor path
  *     and of the branch's own leaf path.  Shared-prefix blocks are streamed
- *     from HBM once for all descendant queries; partial (max, sum, acc)
- *     triples are merged with a log-sum-exp step.
+ *     from HBM once for all descendant queries (short shared ranges in trees
+ *     of short nodes may instead be re-read by the ranges that follow them:
+ *     pool option fold_segments); partial (max, sum, acc) triples are merged
+ *     with a log-sum-exp step.
  *
  * Conventions (all calls):
  *   - Every call returns an int: DENDRITE_OK (0) or a negative error code.
@@ -54,7 +56,7 @@ extern "C" {
 #define DENDRITE_EINVAL      -1  /* bad argument (size, layout, duplicate branch, ...) */
 #define DENDRITE_ENOMEM      -2  /* block pool exhausted (found on the device; sticky) */
 #define DENDRITE_EBADHANDLE  -3  /* handle not live */
-#define DENDRITE_ELIMIT      -4  /* branch count or per-branch table capacity exceeded */
+#define DENDRITE_ELIMIT      -4  /* capacity exceeded: branches, table row, plan size, scratch */
 #define DENDRITE_EDTYPE      -5  /* unsupported dtype / head_dim / block_size combination */
 #define DENDRITE_ECUDA       -6  /* a CUDA runtime call failed */
 #define DENDRITE_ETIMEOUT    -7  /* a bounded device wait gave up (sticky) */
