@@ -11,7 +11,7 @@ import torch
 from copy_write_forked_gb300 import workloads as W
 from copy_write_forked_gb300.dendrite import DendriteError, Pool
 from copy_write_forked_gb300.runner import pool_for, run_script
-from oracle.block_pool import BlockPool, bits_of, run_script_pool
+from oracle.block_pool import BlockPool, PoolExhausted, bits_of, run_script_pool
 
 from _harness import pool_state_matches
 
@@ -233,3 +233,73 @@ def test_fork_chain_cow_stress_small():
         pool.sync()
         assert pool.read_free_stack() == list(range(pool.num_blocks - 1, -1, -1))
         pool.close()
+
+
+CAPACITY = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "capacity_cases.json")))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("name", ["exact_fit_copies", "one_short_copies", "exact_fit_last_holder_in_place",
+                                  "one_short_in_place"])
+def test_capacity_boundary_matches_oracle(name, dtype):
+    """Pools sized at exactly an append's block demand, and one block short:
+    the exact fit succeeds with the stack emptied, the short one is refused
+    (ENOMEM, sticky) with tables, refcounts and stack as before; both
+    compared with the hand-derived states and with O2 bit for bit."""
+    c = CAPACITY["cases"][name]
+    d = 128 if dtype == torch.bfloat16 else 32
+    bits = np.uint16 if dtype == torch.bfloat16 else np.uint32
+    N = c["num_blocks"]
+    pool = Pool(N, 16, 1, d, dtype, max_branches=8, max_blocks_per_branch=8)
+    ref = BlockPool(N, 16, 1, d, bits)
+    g = torch.Generator(device="cuda").manual_seed(11)
+    h = {}
+    refused = None
+    for i, (kind, branches, *rest) in enumerate(c["script"]):
+        if kind == "new":
+            h[branches[0]] = pool.new_branch()
+            ref.new_branch(branches[0])
+        elif kind == "fork":
+            for lid, hid in zip(rest[0], pool.fork(h[branches[0]], len(rest[0]))):
+                h[lid] = hid
+            ref.fork(branches, [rest[0]])
+        elif kind == "free":
+            pool.free([h[b] for b in branches])
+            ref.free(branches)
+            for b in branches:
+                del h[b]
+        elif kind == "append":
+            n = rest[0]
+            K = torch.randn((len(branches), n, 1, d), generator=g, device="cuda").to(dtype)
+            V = torch.randn((len(branches), n, 1, d), generator=g, device="cuda").to(dtype)
+            pool.append_kv([h[b] for b in branches], K, V)
+            try:
+                ref.append(branches, n, bits_of(K), bits_of(V))
+            except PoolExhausted:
+                refused = i
+    assert refused == c.get("exhausted_at_op")
+    if refused is None:
+        pool.sync()
+        for b, tab in c["tables"].items():
+            assert pool.read_table(h[int(b)]) == tab
+        assert pool.read_refcounts() == c["refcounts"]
+        assert pool.read_free_stack() == c["free_stack"]
+        for dst, src, fill in c["cow_copies"]:
+            kd, vd = pool.read_block(dst)
+            ks, vs = pool.read_block(src)
+            assert torch.equal(kd[:, :fill], ks[:, :fill]) and torch.equal(vd[:, :fill], vs[:, :fill])
+        pool_state_matches(pool, h, ref)
+    else:
+        assert pool.sync_status() == -2                  # ENOMEM, sticky
+        with pytest.raises(DendriteError) as e:
+            pool.sync()
+        assert e.value.name == "ENOMEM"
+        # the refused append applied nothing: tables (up to the old length),
+        # refcounts and the stack are the oracle's, which are the derived ones
+        for b, tab in c["tables"].items():
+            got = pool.read_table(h[int(b)])
+            assert got[:len(tab)] == tab and all(x == -1 for x in got[len(tab):])
+            assert ref.table[int(b)] == tab
+        assert pool.read_refcounts() == c["refcounts"] == ref.refcount.tolist()
+        assert pool.read_free_stack() == c["free_stack"] == ref.free_stack()
+    pool.close()

@@ -248,3 +248,89 @@ def test_pins_catch_fork_without_refcount(monkeypatch):
     monkeypatch.setattr(BlockPool, "fork", fork_norc)
     with pytest.raises(AssertionError):
         test_invariants_hold_after_every_op_and_free_all_restores(3)
+
+
+# ------------------------------------------------------- capacity boundary
+
+CAPACITY = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "capacity_cases.json")))
+
+
+def _replay_capacity_case(name):
+    """Replays one hand-derived capacity case on O2 (fp32 payload, 1 KV head,
+    head_dim 4); returns the pool and whether the last append was refused."""
+    c = CAPACITY["cases"][name]
+    pool = BlockPool(c["num_blocks"], CAPACITY["setting"]["block_size"], 1, 4, np.uint32)
+    rng = np.random.default_rng(7)
+    refused = None
+    for i, (kind, branches, *rest) in enumerate(c["script"]):
+        if kind == "new":
+            pool.new_branch(branches[0])
+        elif kind == "fork":
+            pool.fork(branches, [rest[0]])
+        elif kind == "free":
+            pool.free(branches)
+        elif kind == "append":
+            n = rest[0]
+            z = lambda: rng.integers(0, 2**31, size=(len(branches), n, 1, 4), dtype=np.uint32)
+            try:
+                pool.append(branches, n, z(), z())
+            except PoolExhausted:
+                refused = i
+    return c, pool, refused
+
+
+@pytest.mark.parametrize("name", ["exact_fit_copies", "one_short_copies", "exact_fit_last_holder_in_place",
+                                  "one_short_in_place"])
+def test_capacity_boundary_cases(name):
+    """An append whose demand equals the free count succeeds and empties the
+    stack; one block fewer and it is refused with nothing changed.  The last
+    holder of a shared tail whose refcount equals its holders is charged no
+    copy (it writes in place)."""
+    c, pool, refused = _replay_capacity_case(name)
+    assert refused == c.get("exhausted_at_op")
+    assert {str(k): v for k, v in pool.table.items()} == c["tables"]
+    assert {str(k): v for k, v in pool.len.items()} == c["lens"]
+    assert pool.refcount.tolist() == c["refcounts"]
+    assert pool.free_stack() == c["free_stack"]
+    assert pool.top == len(c["free_stack"])
+    for dst, src, fill in c["cow_copies"]:
+        assert np.array_equal(pool.K[dst, :, :fill], pool.K[src, :, :fill])
+        assert np.array_equal(pool.V[dst, :, :fill], pool.V[src, :, :fill])
+    check_invariants(pool)
+
+
+def _all_capacity_cases():
+    for name in CAPACITY["cases"]:
+        test_capacity_boundary_cases(name)
+
+
+def test_pins_catch_refusing_an_exact_fit(monkeypatch):
+    # plant: "demand >= free" refuses (demand + 1 > free is the same test)
+    orig = BlockPool._demand
+    monkeypatch.setattr(BlockPool, "_demand", lambda self, b, n: orig(self, b, n) + 1)
+    with pytest.raises(AssertionError):
+        _all_capacity_cases()
+
+
+def test_pins_catch_charging_the_in_place_holder_a_copy(monkeypatch):
+    # plant: every holder of a partial tail is charged a copy, the last one included
+    def demand_all_copy(self, branches, n_new):
+        total = 0
+        for b in branches:
+            L = self.len[b]
+            if L % self.bs and n_new > 0:
+                total += 1
+            total += -(-(L + n_new) // self.bs) - (-(-L // self.bs))
+        return total
+    monkeypatch.setattr(BlockPool, "_demand", demand_all_copy)
+    with pytest.raises(AssertionError):
+        _all_capacity_cases()
+
+
+def test_pins_catch_a_demand_that_ignores_the_copy(monkeypatch):
+    # plant: the copy of a shared tail is not counted, so a one-short call is let through
+    def demand_no_copy(self, branches, n_new):
+        return sum(-(-(self.len[b] + n_new) // self.bs) - (-(-self.len[b] // self.bs)) for b in branches)
+    monkeypatch.setattr(BlockPool, "_demand", demand_no_copy)
+    with pytest.raises((AssertionError, IndexError)):
+        _all_capacity_cases()
