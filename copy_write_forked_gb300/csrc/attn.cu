@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <type_traits>
 
 #include "attn_common.cuh"
@@ -1612,7 +1613,11 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host staging of the plan upload: plain host memory, so cudaMemcpyAsync has
 // finished reading it when it returns and the next call may overwrite it.
+// One buffer serves every thread and device, so packing a plan into it and
+// handing it to cudaMemcpyAsync happen under g_noalloc_host_mu: two threads
+// that each drive their own pool never upload each other's plans.
 alignas(256) unsigned char g_noalloc_host[kNoAllocScratchBytes];
+std::mutex g_noalloc_host_mu;
 
 constexpr int kNoAllocMaxDevices = 64;
 void* g_noalloc_dev[kNoAllocMaxDevices] = {};
@@ -1667,8 +1672,11 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     const size_t acc_bytes = hp.partial_rows * p->head_dim * sizeof(float);
     const size_t ml_bytes = hp.partial_rows * sizeof(float2);
     if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
-    plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));
-    DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, off[kPlanSections], cudaMemcpyHostToDevice, s));
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_host_mu);
+        plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));
+        DENDRITE_CUDA(cudaMemcpyAsync(scratch, g_noalloc_host, off[kPlanSections], cudaMemcpyHostToDevice, s));
+    }
     AttnArgs a = attn_args(p, 0, Q, out);
     a.plan = plan_view(hp, off, reinterpret_cast<const char*>(scratch), n, q_len, n_q_heads, n_q_heads / p->n_kv);
     a.part_acc = reinterpret_cast<float*>(scratch + plan_bytes);

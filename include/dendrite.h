@@ -377,7 +377,15 @@ int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* parent, const 
  * (16 MiB) that every GPU loading the library holds until the process exits.
  * The call itself calls no cudaMalloc, cudaFree, cudaMallocHost or other
  * allocating CUDA or torch routine; its host-side planning reuses per-thread
- * host buffers.  It does not use or grow the pool's attention workspace.
+ * host buffers.  It does not use or grow the pool's attention workspace, and
+ * it neither reads nor updates the pool's plan cache: every call builds its
+ * plan anew, and dendrite_last_plan_stats keeps describing the last
+ * dendrite_tree_attn_decode call.
+ *   - The plan goes up with a cudaMemcpyAsync from one process-wide pageable
+ *     host buffer, under a lock held while the plan is packed and copied, so
+ *     threads that drive different pools do not mix their plans.  Such a
+ *     copy first waits for the work queued earlier on `stream`: the call
+ *     blocks the host until then.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) once for that device; make that first call before
  *     any stream capture.
@@ -386,10 +394,11 @@ int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* parent, const 
  *     rows of head_dim 128).
  *   - Nothing in the array needs to start at zero: each call writes the plan
  *     and every partial row before reading them.
- *   - All calls share the one array per device and it keeps the last call's
- *     contents: calls whose GPU work overlaps (other streams, other pools on
- *     the same device, other threads) race on it and must be ordered by the
- *     caller.
+ *   - All calls share the one device array per device and it keeps the last
+ *     call's contents: calls whose GPU work overlaps on one device (other
+ *     streams, other pools on the same device, other threads) race on it and
+ *     must be ordered by the caller.  Calls on different devices do not
+ *     share device scratch.
  */
 #define DENDRITE_NOALLOC_SCRATCH_BYTES (16u << 20)
 int dendrite_tree_attn_decode_noalloc(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,

@@ -105,3 +105,34 @@ def test_noalloc_with_tensor_core_units_matches():
         assert (got.float() - ref.float()).abs().max().item() <= TOL
     pool.sync()
     pool.close()
+
+
+def test_noalloc_calls_allocate_no_device_memory():
+    """On a fresh pool that has never run the regular entry point, repeated
+    allocation-free calls leave the device's free memory unchanged (after one
+    first call, which looks up the array's address and may load the kernels);
+    the regular entry point's first call then has to size the pool's
+    workspace, so that workspace was still empty."""
+    w = W.beam(requests=2, prefix=200, width=3, divergent=21)
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    br = [h[b] for b in w.query]
+    Q = w.q("cuda")
+    outs = [torch.full_like(Q, float("nan")) for _ in range(4)]
+    ref = torch.empty_like(Q)
+    pool.sync()
+    assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, outs[0]) == 0
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for o in outs[1:]:
+        assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, o) == 0
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 == free0
+    assert _call(lib().dendrite_tree_attn_decode, pool, Q, br, ref) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] < free1
+    for o in outs:
+        assert (o.float() - ref.float()).abs().max().item() <= TOL
+    pool.sync()
+    pool.close()
