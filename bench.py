@@ -1,30 +1,41 @@
 #!/usr/bin/env python3
 """Benchmark of the copy-on-write tree KV cache hot path on GB300.
 
-Workload (default): Llama-3-8B-shaped attention layer (32 Q heads, 8 KV heads,
-head_dim 128, bf16, block_size 16); 8 independent requests with a 4096-token
-shared prefix, forked 4 ways, each branch 256 divergent tokens, one decode
-query per branch.  The prefixes are prefilled once before timing (resident in
-HBM).  One step is one pass of the whole path over that batch:
+Workload (default, ``--workload stress``): Llama-3-8B-shaped attention layer
+(32 Q heads, 8 KV heads, head_dim 128, bf16, block_size 16); 16 independent
+requests with a 32768-token shared prefix, forked 64 ways, each branch 1024
+divergent tokens, one decode query per branch (1024 branch queries).  The
+prefixes are prefilled once before timing (resident in HBM).  One step is one
+pass of the whole path over that batch:
 
-    fork (8 parents x 4 children, batched)  ->  copy-on-write append of the
-    256 divergent tokens of all 32 branches  ->  tree decode attention (plan,
-    shared-prefix + leaf partials, log-sum-exp merge)  ->  free of the 32 branches
+    fork (16 parents x 64 children, batched)  ->  copy-on-write append of the
+    1024 divergent tokens of all 1024 branches  ->  tree decode attention
+    (plan, shared-prefix + leaf partials, log-sum-exp merge)  ->  free of the
+    1024 branches
 
-`value` is branch-queries per second of step time (32 queries per step per
-GPU; all ranks summed).  The roofline entry covers the dominant kernel, the
-attention partial kernel: unique KV bytes (each shared block counted once)
-plus Q read and partial/out bytes excluded, over its CUDA-event duration.
+``--workload beam`` runs the same step on 8 requests x 4096-token prefix,
+fork 4, 256 divergent tokens.  ``mcts``, ``specverify`` and ``stressattn`` time
+tree attention alone on a prebuilt tree; ``decode32`` runs the beam step
+through 32 layers; ``forks`` times the 100,000 batched forks of the stress
+configuration alone.
 
-`--impl reference` times the fp64 CPU oracle (single thread) on a bounded
-sample of the same workload: the tree attention of the 4 branches of one
-request per step.
+`value` is branch-queries per second of step time (all ranks summed).  The
+``roofline`` entry covers the kernel that takes the most time in the step,
+with its algorithmic bytes over its CUDA-event duration; ``roofline_attention``
+covers the attention partial kernels against the unique KV bytes (each shared
+block counted once) plus Q.
+
+`--impl reference` times the fp64 CPU oracle on the host cores: every step,
+one worker process per core runs the oracle's tree attention of one branch of
+the same workload.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -35,15 +46,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
+W_SEED_DECODE = 4242          # seed of the decode step's new K/V rows
+METRIC = "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us"
 
 
 # ------------------------------------------------------------------ helpers
-
-# DRAM bytes (read + write) per launch of k_attn_partial_bf16 on this step,
-# from one ncu capture of the kernel as it is now (dram__bytes_read.sum
-# 168.27 MB + dram__bytes_write.sum 4.62 MB); to be re-taken whenever that
-# kernel changes.
-BEAM_PARTIAL_TRAFFIC_BYTES = 172_880_000
 
 def quantile(xs, q):
     """The q-quantile of xs (nearest rank)."""
@@ -81,6 +88,38 @@ def read_peaks():
         except Exception:
             pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+# Kernel -> source file, for matching a recorded ncu capture to the code it was taken on.
+KERNEL_SOURCES = {
+    "k_append_copy": "copy_write_forked_gb300/csrc/pool.cu",
+    "k_attn_partial_tc": "copy_write_forked_gb300/csrc/attn_tc.cu",
+    "k_attn_partial_bf16": "copy_write_forked_gb300/csrc/attn.cu",
+}
+
+
+def source_sha(kernel: str) -> str:
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of ``kernel`` on ``workload`` from
+    the ncu table in profiles/ncu_traffic.md, if it was taken on the current
+    source of that kernel's file; None otherwise (no capture, or the kernel's
+    source changed since)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha(kernel)
+    for line in open(path):
+        f = [x.strip() for x in line.strip().strip("|").split("|")]
+        if len(f) >= 7 and f[0] == kernel and f[1] == workload and f[2] == sha:
+            try:
+                return int(f[6].replace(",", ""))
+            except ValueError:
+                return None
+    return None
 
 
 class ClockSampler:
@@ -148,23 +187,57 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "window": window}
 
 
-# ------------------------------------------------------------ workload
-def beam_workload(seed: int):
+# ------------------------------------------------------------ workloads
+FULL_PATH = {
+    # name: (requests, prefix, fork width, divergent tokens, description)
+    "stress": (16, 32768, 64, 1024, "large fork + CoW stress, Llama-3-8B attention layer: 16 requests x "
+                                    "32768-token prefix, fork 64, 1024 divergent tokens per branch"),
+    "beam": (8, 4096, 4, 256, "beam-like 4-way fork, Llama-3-8B attention layer: 8 requests x 4096-token "
+                              "prefix, fork 4, 256 divergent tokens per branch"),
+}
+
+
+def full_path_workload(name: str, seed: int = 0, requests=None):
     from copy_write_forked_gb300 import workloads as W
-    return W.beam(requests=8, prefix=4096, width=4, divergent=256, seed=seed)
+    R, P, Wd, Dv, _ = FULL_PATH[name]
+    w = W.beam(requests=requests or R, prefix=P, width=Wd, divergent=Dv, seed=seed)
+    if name == "stress":
+        w.name = f"stress_r{requests or R}_p{P}_w{Wd}_div{Dv}"
+    return w
 
 
-def config_of(w):
+def config_of(w, name):
     m = w.meta
-    return {"workload": "beam-like 4-way fork, Llama-3-8B attention layer", "name": w.name,
-            "requests": m["requests"], "prefix_tokens": m["prefix"], "fork_width": m["width"],
+    big = w.unique_kv_bytes() > (256 << 20)
+    return {"workload": FULL_PATH[name][4] if m["requests"] == FULL_PATH[name][0] else
+            FULL_PATH[name][4] + f" (reduced to {m['requests']} requests)",
+            "name": w.name, "requests": m["requests"], "prefix_tokens": m["prefix"], "fork_width": m["width"],
             "divergent_tokens": m["divergent"], "branch_queries_per_step": len(w.query),
             "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
-            "block_size": w.block_size, "l2": "flushed before every step (read-only pass over 256 MiB)",
-            "step": "fork + CoW append + tree decode attention + free"}
+            "block_size": w.block_size,
+            "l2": ("not flushed: inputs larger than L2 (%.1f GB of unique KV read and %.1f GB of new rows "
+                   "written per step)" % (w.unique_kv_bytes() / 1e9, _divergent_bytes(w) / 1e9)) if big else
+                  "flushed before every step (read-only pass over 256 MiB)",
+            "step": "fork + CoW append of the divergent tokens + tree decode attention + free "
+                    "(the tree below each fork is rebuilt by every step; the prefixes stay resident)"}
+
+
+def _divergent_bytes(w):
+    m = w.meta
+    return 2 * len(w.query) * m["divergent"] * w.n_kv_heads * w.head_dim * 2
 
 
 # ---------------------------------------------------------- our arm
+def _step_desc(kind):
+    if kind == "decode":
+        return ("decode step on the prebuilt tree: every leaf forks one child (batched fork), each child "
+                "appends one new token (copy-on-write of the leaf's partially filled tail block), tree decode "
+                "attention for the children, free of the old leaves (the children are the next step's leaves; "
+                "each step adds one token per branch)")
+    return ("fork of the prefixes + CoW append of all divergent tokens + tree decode attention + free (the tree "
+            "below each fork is rebuilt by every step; the prefixes stay resident)")
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -176,43 +249,84 @@ def run_ours(args):
     import __graft_entry__ as g
     g.build()
     from copy_write_forked_gb300.dendrite import Pool
-    from copy_write_forked_gb300 import workloads as W
 
-    w = beam_workload(seed=rank)
+    name, kind = args.workload, args.step
+    w = full_path_workload(name, seed=rank, requests=args.requests)
     R, P, Wd, Dv = (w.meta[k] for k in ("requests", "prefix", "width", "divergent"))
     nq, nkv, d = w.n_q_heads, w.n_kv_heads, w.head_dim
     bs = w.block_size
-    nblocks = R * (P // bs + 1) + R * Wd * (Dv // bs + 2) + 64
-    pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R * (Wd + 1) + 8,
-                max_blocks_per_branch=(P + Dv) // bs + 8)
-    # prefill (untimed): the 8 prefixes, resident in HBM
+    nl = R * Wd                                   # branches queried per step
+    n_prof = min(args.steps, 100 if name == "beam" else 20)
+    e2e_steps = args.steps if name == "beam" else min(args.steps, 50)
+    # decode steps the run takes in all (warm-up, timed, profiled, e2e warm-up and timed, check)
+    total_steps = args.warmup + args.steps + n_prof + 2 * args.warmup + e2e_steps + 2
+    grow = total_steps if kind == "decode" else 0
+    nblocks = R * (P // bs + 1) + nl * (Dv // bs + 3 + grow // bs) + 64
+    pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R + 2 * nl + 16,
+                max_blocks_per_branch=(P + Dv + grow) // bs + 8)
+    # prefill (untimed): the prefixes, resident in HBM
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
     Kp, Vp = w.kv(prefill_idx, dev)
     pool.append_kv(roots, Kp, Vp)
+    pool.sync()
     del Kp, Vp
     div_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == Dv)
-    Kd, Vd = w.kv(div_idx, dev)            # divergent tokens of the 32 branches, resident
+    Kd, Vd = w.kv(div_idx, dev)            # divergent tokens of all branches
     Q = w.q(dev)
     out = torch.empty_like(Q)
     stream = torch.cuda.current_stream()
+    state = {"leaves": None, "s": 0}
+    if kind == "decode":
+        # the tree of the configuration, built once: fork, divergent tokens
+        kids = pool.fork_batch(roots, [Wd] * R)
+        state["leaves"] = [c for ks in kids for c in ks]
+        pool.append_kv(state["leaves"], Kd, Vd)
+        pool.sync()
+        del Kd, Vd
+        gen = torch.Generator(device=dev).manual_seed(W_SEED_DECODE + rank)
+        Kn = torch.randn((nl, 1, nkv, d), generator=gen, device=dev).to(torch.bfloat16)
+        Vn = torch.randn((nl, 1, nkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    else:
+        Kn, Vn = Kd, Vd
     pool.sync()
-
+    big = w.unique_kv_bytes() > (256 << 20)
     flush_r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
 
     def flush_l2():
         # read-only pass over 256 MiB (2x L2): evicts the cache and leaves it
-        # holding clean lines, so no write-back lands inside the next step
-        flush_r.max()
+        # holding clean lines, so no write-back lands inside the next step.
+        # Workloads whose inputs are far larger than L2 skip it.
+        if not big:
+            flush_r.max()
 
-    def step():
-        kids = pool.fork_batch(roots, [Wd] * R)
-        br = [c for ks in kids for c in ks]
-        pool.append_kv(br, Kd, Vd)
-        pool.tree_attn_decode(Q, br, out=out)
-        pool.free(br)
+    def step(K=None, V=None, Qs=None, o=None):
+        K = Kn if K is None else K
+        V = Vn if V is None else V
+        Qs = Q if Qs is None else Qs
+        o = out if o is None else o
+        if kind == "decode":
+            kids = pool.fork_batch(state["leaves"], [1] * nl)
+            br = [ks[0] for ks in kids]
+            pool.append_kv(br, K, V)
+            pool.tree_attn_decode(Qs, br, out=o)
+            pool.free(state["leaves"])
+            state["leaves"] = br
+            state["s"] += 1
+        else:
+            kids = pool.fork_batch(roots, [Wd] * R)
+            br = [c for ks in kids for c in ks]
+            pool.append_kv(br, K, V)
+            pool.tree_attn_decode(Qs, br, out=o)
+            pool.free(br)
         return br
 
+    def unique_tokens():
+        # tokens the next step's queries see, each shared one once
+        extra = state["s"] + 1 if kind == "decode" else 0
+        return R * P + nl * (Dv + extra)
+
+    kv_tok = 2 * nkv * d * 2                        # K + V bytes of one token
     clk = ClockSampler(local).__enter__()
     pool.set_profiling(False)
     for _ in range(args.warmup):
@@ -225,10 +339,12 @@ def run_ours(args):
 
     # ---- timed region: K steps enqueued back to back, one event pair per step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    tok_timed = []
     t_clk0 = time.time()
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush_l2()
+        tok_timed.append(unique_tokens())
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -243,53 +359,88 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
     ms = max_over_ranks(ms, world, dev)
-    n_queries = len(w.query)
-    value = world * n_queries / (ms / 1e3)
+    value = world * nl / (ms / 1e3)
+    ref_out = out.clone()
 
     # ---- per-kernel device times (profiling events inside the library; one
     # synchronised step at a time so the events of each call can be read)
     pool.set_profiling(True)
-    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free",
-                            "attn_total")}
-    plan_us = []
+    kern = {k: [] for k in ("fork", "append_meta", "append_copy", "attn_partial", "attn_tc", "attn_merge",
+                            "free", "attn_total")}
+    plan_us, tok_prof = [], []
+    orig_attn = pool.tree_attn_decode
 
-    def step_profiled():
-        # A second L2 flush sits right before the attention call: the device
-        # works through it while the host builds the plan and launches, so the
+    def attn_after_flush(*a, **k):
+        # A read pass sits right before the attention call: the device works
+        # through it while the host builds the plan and launches, so the
         # events around the attention kernels time the kernels, not the host.
-        kids = pool.fork_batch(roots, [Wd] * R)
-        br = [c for ks in kids for c in ks]
-        pool.append_kv(br, Kd, Vd)
-        flush_l2()
-        pool.tree_attn_decode(Q, br, out=out)
-        pool.free(br)
+        flush_r.max()
+        return orig_attn(*a, **k)
 
-    for i in range(min(args.steps, 100)):
+    pool.tree_attn_decode = attn_after_flush
+    for i in range(n_prof):
         flush_l2()
-        step_profiled()
+        tok_prof.append(unique_tokens())
+        step()
         tm = pool.last_timings()
         plan_us.append(pool.last_plan_stats()["plan_us"])
         for k in kern:
             if tm.get(k) is not None:
                 kern[k].append(tm[k])
+    pool.tree_attn_decode = orig_attn
     pool.set_profiling(False)
+    km = {k: (statistics.mean(v) if v else None) for k, v in kern.items()}
 
-    # roofline of the attention partial kernel
-    unique_kv = w.unique_kv_bytes()
-    q_bytes = Q.numel() * Q.element_size()
-    attn_ms = statistics.mean(kern["attn_partial"])
-    achieved = (unique_kv + q_bytes) / (attn_ms / 1e3) / 1e9
     peak, peak_src = read_peaks()
     plan = pool.last_plan_stats()
+    q_bytes = Q.numel() * Q.element_size()
+    uniq = statistics.mean(tok_prof) * kv_tok
+    # algorithmic bytes per launch of each of the step's large kernels
+    append_bytes = 2 * (Kn.numel() + Vn.numel()) * Kn.element_size()     # rows read once and written once
+    tc_ms = km["attn_tc"] or 0.0
+    mma_ms = km["attn_partial"] - tc_ms
+    prefix_bytes = R * P * kv_tok                     # shared prefixes: the tcgen05 class when it exists
+    cand = {"k_append_copy": (km["append_copy"], append_bytes, "new K and V rows read once and written once")}
+    if tc_ms:
+        cand["k_attn_partial_tc"] = (tc_ms, prefix_bytes + q_bytes,
+                                     "unique KV of the shared prefixes (each block once) + Q")
+        cand["k_attn_partial_bf16"] = (mma_ms, uniq - prefix_bytes + q_bytes,
+                                       "unique KV of the branches' own blocks + Q")
+    else:
+        cand["k_attn_partial_bf16"] = (mma_ms, uniq + q_bytes, "unique KV (each shared block once) + Q")
+    dom = max(cand, key=lambda k: cand[k][0])
+
+    def roof(kernel, kms, nbytes, what, traffic):
+        ach = nbytes / (kms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": kernel, "achieved": ach, "peak": peak, "peak_source": peak_src,
+                "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                "algorithmic_bytes": nbytes, "bytes_counted": what, "kernel_ms": kms}
+
+    traffic_key = w.name + ("" if kind == "divergent" else "_decode")
+    roofline = roof(dom, *cand[dom], recorded_traffic(dom, traffic_key))
+    attn_roof = roof(("k_attn_partial_tc + " if tc_ms else "") + "k_attn_partial_bf16", km["attn_partial"],
+                     uniq + q_bytes, "unique KV (each shared block once) + Q", None)
+    attn_roof["per_kernel"] = {k: roof(k, *cand[k], recorded_traffic(k, traffic_key))
+                               for k in cand if k.startswith("k_attn")}
+    attn_roof["call_ms"] = km["attn_total"]
+    attn_roof["call_frac"] = (uniq + q_bytes) / (km["attn_total"] / 1e3) / 1e9 / peak
 
     # ----- e2e through the public API with host buffers (pinned), H2D + D2H inside
     # the timed region.  A copy stream brings step i + 1's K, V and Q in while
     # the compute stream runs step i (two device buffer sets); the result of
     # every step is read back to pinned host memory on the compute stream.
-    Kh, Vh, Qh = Kd.cpu().pin_memory(), Vd.cpu().pin_memory(), Q.cpu().pin_memory()
-    outh = [torch.empty(Q.shape, dtype=Q.dtype).pin_memory() for _ in range(2)]
-    bufs = [(torch.empty_like(Kd), torch.empty_like(Vd), torch.empty_like(Q), torch.empty_like(Q))
-            for _ in range(2)]
+    Kh = torch.empty(Kn.shape, dtype=Kn.dtype, pin_memory=True)
+    Vh = torch.empty(Vn.shape, dtype=Vn.dtype, pin_memory=True)
+    Qh = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
+    Kh.copy_(Kn)
+    Vh.copy_(Vn)
+    Qh.copy_(Q)
+    if kind == "divergent":
+        del Kd, Vd
+    Kn = Vn = None
+    outh = [torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True) for _ in range(2)]
+    bufs = [(torch.empty(Kh.shape, dtype=Kh.dtype, device=dev), torch.empty(Vh.shape, dtype=Vh.dtype, device=dev),
+             torch.empty_like(Q), torch.empty_like(Q)) for _ in range(2)]
     copy_stream = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer set j landed
     ev_used = [torch.cuda.Event() for _ in range(2)]   # step using buffer set j finished
@@ -308,20 +459,19 @@ def run_ours(args):
     def e2e_step(j):
         K2, V2, Q2, o2 = bufs[j]
         stream.wait_event(ev_in[j])
-        kids = pool.fork_batch(roots, [Wd] * R)
-        br = [c for ks in kids for c in ks]
-        pool.append_kv(br, K2, V2)
-        pool.tree_attn_decode(Q2, br, out=o2)
+        br = step(K2, V2, Q2, o2)
         outh[j].copy_(o2, non_blocking=True)
-        pool.free(br)
         ev_used[j].record(stream)
+        return br
 
     def e2e_run(n):
         bring_in(0)
+        br = None
         for i in range(n):
             if i + 1 < n:
                 bring_in((i + 1) % 2)
-            e2e_step(i % 2)
+            br = e2e_step(i % 2)
+        return br
 
     for _ in range(args.warmup):
         flush_l2()
@@ -332,54 +482,73 @@ def run_ours(args):
     e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     e2e_ev[0].record(stream)
     copy_stream.wait_stream(stream)
-    e2e_run(args.steps)
+    last_br = e2e_run(e2e_steps)
     stream.wait_stream(copy_stream)
     e2e_ev[1].record(stream)
     torch.cuda.synchronize()
-    e2e = max_over_ranks(e2e_ev[0].elapsed_time(e2e_ev[1]) / args.steps, world, dev)
+    e2e = max_over_ranks(e2e_ev[0].elapsed_time(e2e_ev[1]) / e2e_steps, world, dev)
     h2d = (Kh.numel() + Vh.numel() + Qh.numel()) * 2
     d2h = outh[0].numel() * 2
-    # the inputs are exact copies, so the last step's output matches the device-resident run's
-    if (outh[(args.steps - 1) % 2].to(dev).float() - out.float()).abs().max().item() > 1e-2:
-        raise RuntimeError("e2e output differs from the device-resident step")
-
-    # ----- fork latency at depth 500 blocks (tail half full), 1 and 4 children
-    fork = fork_latency(dev) if rank == 0 else {}
+    # The last e2e step's output equals, bit for bit, the device-resident
+    # attention of the same queries over the same tree (same plan, same kernels).
+    if kind == "decode":
+        chk = torch.empty_like(Q)
+        pool.tree_attn_decode(Q, last_br, out=chk)
+    else:
+        chk = ref_out         # every divergent step rebuilds the same tree
+    torch.cuda.synchronize()
+    if not torch.equal(outh[(e2e_steps - 1) % 2].to(dev), chk):
+        raise RuntimeError("e2e output differs from the device-resident attention")
     pool.sync()
+    pool.close()
+    del bufs, Kh, Vh, outh
+    torch.cuda.empty_cache()
+
+    # ----- fork latency at depths 1..500 blocks (tail half full), 1 and 4 children,
+    # and the 100,000 batched forks with copy-on-write appends of the stress configuration
+    fork = fork_latency(dev) if rank == 0 else {}
+    forks100k = fork_stress_timed(dev) if rank == 0 and not args.no_fork_stress else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.cpu_seconds)
+        cpu = cpu_baseline(args.cpu_seconds, name)
 
-    # fork 1 + append 2 (meta, copy) + attention 3 (the step's new tree needs a new
-    # plan: its upload, then partial and merge) + free 1
-    gpu_launches = 7 * args.steps
+    # fork 1 + append 2 (meta, copy) + attention (a new tree needs a new plan:
+    # its upload, the tcgen05 kernel when the plan has such units, the
+    # mma.sync kernel, the merge) + free 1
+    per_step = 1 + 2 + (4 if plan["n_tc_units"] else 3) + 1
+    cfg = config_of(w, name)
+    cfg["step"] = _step_desc(kind)
+    if kind == "decode":
+        # each branch's decoded tokens beyond the configuration's, first and last timed step
+        cfg["decoded_tokens_per_branch_timed"] = [(tok_timed[0] - R * P) // nl - Dv - 1,
+                                                  (tok_timed[-1] - R * P) // nl - Dv - 1]
+    cfg["unique_kv_bytes_timed_mean"] = statistics.mean(tok_timed) * kv_tok
     line = {
-        "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
+        "metric": METRIC,
         "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
-        "config": dict(config_of(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-        "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": BEAM_PARTIAL_TRAFFIC_BYTES,
-                     "algorithmic_bytes": unique_kv + q_bytes, "kernel_ms": attn_ms},
+        "config": dict(cfg, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": roofline,
+        "roofline_attention": attn_roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * n_queries / (e2e / 1e3), "unit": "branch-queries/s", "ms_per_step": e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": gpu_launches,
+        "e2e": {"value": world * nl / (e2e / 1e3), "unit": "branch-queries/s", "ms_per_step": e2e,
+                "steps": e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": per_step * args.steps,
         "clocks": clocks,
-        "kernels_ms": {k: (statistics.mean(v) if v else None) for k, v in kern.items()},
-        "attn_branch_queries_per_s": n_queries / (statistics.mean(kern["attn_total"]) / 1e3),
+        "kernels_ms": km,
+        "attn_branch_queries_per_s": nl / (km["attn_total"] / 1e3),
         "plan": {"segments": plan["n_segments"], "units": plan["n_units"], "ctas": plan["n_ctas"],
+                 "tc_units": plan["n_tc_units"], "tc_ctas": plan["n_tc_ctas"],
                  "partials": plan["n_partials"], "tiles": plan["tiles"], "unique_tiles": plan["unique_tiles"],
                  "host_plan_us_mean": statistics.mean(plan_us)},
         "fork_us": fork,
+        "forks_100k": forks100k,
         "wall_s": wall,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    pool.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -398,7 +567,7 @@ def run_decode_layers(args):
     g.build()
     from copy_write_forked_gb300.dendrite import Pool
     NL = 32
-    w = beam_workload(seed=rank)
+    w = full_path_workload("beam", seed=rank)
     R, P, Wd, Dv = (w.meta[k] for k in ("requests", "prefix", "width", "divergent"))
     nq, nkv, d, bs = w.n_q_heads, w.n_kv_heads, w.head_dim, w.block_size
     nblocks = R * (P // bs + 1) + R * Wd * (Dv // bs + 2) + 64
@@ -484,7 +653,7 @@ def other_workload(name):
         return W.mcts(), "MCTS tree: root 2048, 500 iterations of fork 4 x 32 tokens, one query per live leaf"
     if name == "specverify":
         return W.spec_verify(), "speculative verification: 32 x prefix 8192, 3 draft paths x 8 tokens, q_len 8"
-    if name == "stress":
+    if name == "stressattn":
         return W.fork_stress_attention(), "stress: 16 x prefix 32768, fork 64 x 1024 tokens"
     raise ValueError(name)
 
@@ -615,30 +784,66 @@ def fork_latency(dev, reps=200):
     return res
 
 
-# ------------------------------------------------------------ oracle arm
-def _oracle_sample(seconds: float):
-    """Runs in a fresh single-threaded process: the oracle's tree attention on
-    branches of the beam workload until `seconds` of CPU work are spent."""
+def fork_stress_timed(dev, batches=5000):
+    """The 100,000 batched forks of the stress configuration: chains of 1, 10,
+    50, 100 and 500 blocks with a half-full tail block; every batch forks each
+    chain 4 ways in one call (20 forks), appends one token to every child (each
+    copies its chain's shared half block) and frees the children.  Timed with
+    CUDA events around all batches (the device work of 3 calls per batch)."""
     import torch
-    torch.set_num_threads(1)
     from copy_write_forked_gb300 import workloads as W
-    from oracle import KVTree
-    w = beam_workload(seed=0)
-    ids = list(w.query[:4])                 # the 4 branches of request 0
-    tree = _oracle_request_tree(w, 0)
-    Q = [w.q_one(i) for i in range(4)]
-    n = 0
+    from copy_write_forked_gb300.dendrite import Pool
+    depths = (1, 10, 50, 100, 500)
+    N = sum(depths) + len(depths) + 64
+    pool = Pool(N, 16, 8, 128, torch.bfloat16, max_branches=64, max_blocks_per_branch=512)
+    roots = []
+    for d in depths:
+        r = pool.new_branch()
+        roots.append(r)
+        L = W.fork_chain_script(d)
+        K = torch.randn(1, L, 8, 128, device=dev).bfloat16()
+        pool.append_kv([r], K, K)
+    Kt = torch.randn(4 * len(roots), 1, 8, 128, device=dev).bfloat16()
+    stream = torch.cuda.current_stream()
+
+    def batch():
+        kids = pool.fork_batch(roots, [4] * len(roots))
+        flat = [c for ks in kids for c in ks]
+        pool.append_kv(flat, Kt, Kt)
+        pool.free(flat)
+        return len(flat)
+
+    for _ in range(50):
+        batch()
+    pool.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
-    while True:
-        tree.attend(ids[n % 4], Q[n % 4])
-        n += 1
-        dt = time.perf_counter() - t0
-        if dt >= seconds:
-            break
-    return n, dt
+    e0.record(stream)
+    forks = sum(batch() for _ in range(batches))
+    e1.record(stream)
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    t2 = time.perf_counter()
+    dev_ms = e0.elapsed_time(e1)
+    pool.sync()
+    pool.close()
+    return {"forks": forks, "batches": batches, "depths_blocks": list(depths), "children_per_chain": 4,
+            "device_ms": dev_ms, "wall_ms": (t2 - t0) * 1e3, "host_issue_ms": (t1 - t0) * 1e3,
+            "us_per_fork_device": dev_ms * 1e3 / forks, "us_per_batch_device": dev_ms * 1e3 / batches,
+            "forks_per_s_device": forks / (dev_ms / 1e3),
+            "per_batch": "fork_batch (5 chains x 4 children) + append of 1 token to 20 children "
+                         "(each copies a 32 KiB shared half block) + free of the 20 children"}
 
 
-def _oracle_request_tree(w, req):
+# ------------------------------------------------------------ oracle arm
+# The oracle runs in worker processes of their own (fresh interpreters, one
+# thread each), one per host core used: each rebuilds the ancestor chain of
+# one branch of the workload in the oracle's logical tree, then answers
+# "step" (one fp64 tree attention of its branch) and "run <seconds>" (as many
+# as fit) commands on stdin.
+
+def _oracle_branch_tree(w, req, child):
+    """The oracle's tree of one request, holding only the queried child's own rows."""
     from oracle import KVTree
     pre = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == w.meta["prefix"])
     div = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == w.meta["divergent"])
@@ -647,101 +852,228 @@ def _oracle_request_tree(w, req):
     tree.new_root(req)
     k, v = w.kv_one(pre, req)
     tree.append(req, k, v)
-    kids = [w.query[req * width + j] for j in range(width)]
-    tree.fork(req, kids)
-    for j, c in enumerate(kids):
-        k, v = w.kv_one(div, req * width + j)
-        tree.append(c, k, v)
-    return tree
+    qi = req * width + child
+    bid = w.query[qi]
+    tree.fork(req, [bid])
+    k, v = w.kv_one(div, qi)
+    tree.append(bid, k, v)
+    return tree, bid, w.q_one(qi)
 
 
-def cpu_baseline(seconds: float):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import sys, json; sys.path.insert(0, %r); import bench; n, dt = bench._oracle_sample(%f); "
-            "print(json.dumps([n, dt]))" % (ROOT, seconds))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
-    if r.returncode != 0:
-        return {"error": r.stderr[-300:]}
-    n, dt = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": n / dt, "unit": "branch-queries/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} branch queries (fp64 tree attention, 4352-token branches of request 0 of the "
-                      f"beam workload) in {dt:.1f} s, single thread"}
+def _oracle_worker(name, index):
+    import torch
+    torch.set_num_threads(1)
+    w = full_path_workload(name, seed=0)
+    R, width = w.meta["requests"], w.meta["width"]
+    tree, bid, q = _oracle_branch_tree(w, index % R, (index // R) % width)
+    tree.attend(bid, q)
+    print("ready", flush=True)
+    for line in sys.stdin:
+        cmd = line.split()
+        if not cmd or cmd[0] == "quit":
+            break
+        if cmd[0] == "step":
+            t0 = time.perf_counter()
+            tree.attend(bid, q)
+            print(json.dumps(time.perf_counter() - t0), flush=True)
+        elif cmd[0] == "run":
+            secs, n = float(cmd[1]), 0
+            t0 = time.perf_counter()
+            while True:
+                tree.attend(bid, q)
+                n += 1
+                if time.perf_counter() - t0 >= secs:
+                    break
+            print(json.dumps([n, time.perf_counter() - t0]), flush=True)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _mem_available_bytes():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+class OracleWorkers:
+    """n single-threaded oracle processes, each holding one branch's chain."""
+
+    PER_WORKER_BYTES = {"stress": 3 << 30, "beam": 1 << 29}
+
+    def __init__(self, name, n):
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        env.pop("CUDA_VISIBLE_DEVICES", None)
+        code = "import sys; sys.path.insert(0, %r); import bench; bench._oracle_worker(%r, %%d)" % (ROOT, name)
+        self.procs = [subprocess.Popen([sys.executable, "-c", code % i], stdin=subprocess.PIPE,
+                                       stdout=subprocess.PIPE, text=True, env=env) for i in range(n)]
+        for p in self.procs:
+            if p.stdout.readline().strip() != "ready":
+                self.close()
+                raise RuntimeError("oracle worker failed to start")
+
+    @classmethod
+    def fit(cls, name, want):
+        """How many workers the host's cores and available memory allow."""
+        n = max(1, min(want, host_cores()))
+        avail = _mem_available_bytes()
+        if avail:
+            n = max(1, min(n, int(avail * 0.6) // cls.PER_WORKER_BYTES[name]))
+        return n
+
+    def _all(self, cmd):
+        for p in self.procs:
+            p.stdin.write(cmd + "\n")
+            p.stdin.flush()
+        return [json.loads(p.stdout.readline()) for p in self.procs]
+
+    def step(self):
+        return self._all("step")
+
+    def run(self, seconds):
+        return self._all("run %f" % seconds)
+
+    def close(self):
+        for p in self.procs:
+            try:
+                p.stdin.write("quit\n")
+                p.stdin.flush()
+            except Exception:
+                pass
+        for p in self.procs:
+            try:
+                p.wait(timeout=30)
+            except Exception:
+                p.kill()
+
+
+def _branch_tokens(name):
+    R, P, Wd, Dv, _ = FULL_PATH[name]
+    return P + Dv
+
+
+def cpu_baseline(seconds: float, name: str):
+    """The oracle as it stands on a bounded sample of the workload: fp64 tree
+    attention of single branches for about ``seconds`` per leg, first on one
+    core, then on every host core (one worker per core, each on its own
+    branch).  The all-cores figure is the reported value."""
+    res = {}
+    for leg, want in (("single", 1), ("all", host_cores())):
+        n = OracleWorkers.fit(name, want)
+        pool = OracleWorkers(name, n)
+        try:
+            out = pool.run(seconds)
+        finally:
+            pool.close()
+        q = sum(c for c, _ in out)
+        dt = max(t for _, t in out)
+        res[leg] = {"value": q / dt, "cores": n, "queries": q, "seconds": dt}
+    a, s1 = res["all"], res["single"]
+    tok = _branch_tokens(name)
+    return {"value": a["value"], "unit": "branch-queries/s", "cores": a["cores"], "kind": "oracle",
+            "host_cores": host_cores(),
+            "sample": f"{a['queries']} branch queries in {a['seconds']:.1f} s on {a['cores']} worker processes "
+                      f"(one thread each, each on its own {tok}-token branch of the {name} workload; fp64 "
+                      f"materialise + softmax(qK^T/sqrt(d))V over 32 heads)",
+            "single_thread": {"value": s1["value"], "cores": 1,
+                              "sample": f"{s1['queries']} branch queries in {s1['seconds']:.1f} s, one thread"}}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import torch
-    torch.set_num_threads(1)
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
-    from copy_write_forked_gb300 import workloads as W
-    w = beam_workload(seed=0)
-    tree = _oracle_request_tree(w, 0)
-    ids = list(w.query[:4])
-    Q = [w.q_one(i) for i in range(4)]
-
-    k = [0]
-
-    def step():
-        # one branch query (round robin over the 4 branches of request 0)
-        j = k[0] % 4
-        tree.attend(ids[j], Q[j])
-        k[0] += 1
-
-    for _ in range(args.warmup):
-        step()
-    t = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        step()
-        t.append(time.perf_counter() - t0)
+    name = args.workload if args.workload in FULL_PATH else "stress"
+    w = full_path_workload(name, seed=0)
+    n = OracleWorkers.fit(name, host_cores())
+    pool = OracleWorkers(name, n)
+    try:
+        for _ in range(args.warmup):
+            pool.step()
+        t = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            pool.step()
+            t.append(time.perf_counter() - t0)
+    finally:
+        pool.close()
     ms = statistics.mean(t) * 1e3
-    value = 1 / (ms / 1e3)
-    line = {"impl": "reference",
-            "metric": "tree decode attn branch-queries/s & HBM GB/s (unique KV) vs peak; fork us",
+    value = n / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC,
             "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
-            "config": dict(config_of(w), parallelism="single thread"),
-            "cpu_baseline": {"value": value, "unit": "branch-queries/s", "cores": 1, "kind": "oracle",
-                             "sample": "per step: fp64 tree attention (materialise + softmax(qK^T/sqrt(d))V, "
-                                       "32 heads) of one 4352-token branch of request 0, single thread"},
+            "config": dict(config_of(w, name), parallelism=f"{n} host worker processes"),
+            "cpu_baseline": {"value": value, "unit": "branch-queries/s", "cores": n, "kind": "oracle",
+                             "sample": f"per step: {n} fp64 tree attentions (materialise + softmax(qK^T/sqrt(d))V, "
+                                       f"32 heads), one per worker process, each on its own "
+                                       f"{_branch_tokens(name)}-token branch of the {name} workload"},
             "e2e": {"value": value, "unit": "branch-queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_forks(args):
+    """The 100,000 batched forks alone, plus fork latency by depth."""
+    import torch
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__ as g
+    g.build()
+    line = {"metric": METRIC, "workload": "forks", "forks_100k": fork_stress_timed(dev),
+            "fork_us": fork_latency(dev)}
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fork-stress", action="store_true")
+    ap.add_argument("--step", default="decode", choices=["decode", "divergent"],
+                    help="full-path workloads: 'decode' (default) forks every leaf of the prebuilt tree once, "
+                         "appends one token per child, attends and frees the old leaves; 'divergent' rebuilds "
+                         "the tree below the prefixes (fork + append of all divergent tokens) every step")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="full-path workloads: fewer requests than the configuration (a smaller case for ncu)")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
     ap.add_argument("--fold-segments", type=int, default=0,
                     help="fold short shared segments into the ones that follow (0: default, k: below k percent "
                          "of the estimate, -1: off)")
-    ap.add_argument("--workload", default="beam", choices=["beam", "mcts", "specverify", "stress", "decode32"],
-                    help="beam = the full-path step (default JSON line); others time tree attention only")
+    ap.add_argument("--workload", default="stress",
+                    choices=["stress", "beam", "mcts", "specverify", "stressattn", "decode32", "forks"],
+                    help="stress (default) and beam: the full-path step; mcts, specverify, stressattn: tree "
+                         "attention alone; decode32: the beam step through 32 layers; forks: the 100,000 "
+                         "batched forks and fork latency")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "ours" and args.workload == "decode32":
-        run_decode_layers(args)
-        return
-    if args.impl == "ours" and args.workload != "beam":
-        run_attention_only(args)
-        return
     if args.impl == "reference":
-        # the oracle runs single-threaded: pin BLAS/OpenMP pools before numpy loads
+        # the oracle runs single-threaded per worker: pin BLAS/OpenMP pools before numpy loads
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[k] = "1"
         run_reference(args)
-    else:
+    elif args.workload == "decode32":
+        run_decode_layers(args)
+    elif args.workload == "forks":
+        run_forks(args)
+    elif args.workload in FULL_PATH:
         run_ours(args)
+    else:
+        run_attention_only(args)
 
 
 if __name__ == "__main__":
