@@ -1028,8 +1028,8 @@ def run_forks(args):
     dev = torch.device("cuda", local)
     import __graft_entry__ as g
     g.build()
-    line = {"metric": METRIC, "workload": "forks", "forks_100k": fork_stress_timed(dev),
-            "fork_us": fork_latency(dev)}
+    line = {"metric": METRIC, "workload": "forks", "forks_100k": fork_stress_timed(dev, args.fork_batches),
+            "fork_us": fork_latency(dev, args.fork_reps)}
     print(json.dumps(line), flush=True)
 
 
@@ -1042,6 +1042,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fork-stress", action="store_true")
+    ap.add_argument("--fork-reps", type=int, default=200, help="--workload forks: calls per fork-latency point")
+    ap.add_argument("--fork-batches", type=int, default=5000,
+                    help="--workload forks: batches of the timed fork stress (20 forks each)")
     ap.add_argument("--step", default="decode", choices=["decode", "divergent"],
                     help="full-path workloads: 'decode' (default) forks every leaf of the prebuilt tree once, "
                          "appends one token per child, attends and frees the old leaves; 'divergent' rebuilds "

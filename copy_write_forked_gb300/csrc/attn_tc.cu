@@ -11,6 +11,13 @@
 //   S_r = Q_r K^T   M = 128 rows, N = 16..64 tokens, K = head_dim 128
 //   O_r += P_r V    M = 128 rows, N = head_dim 128,  K = 16..64 tokens
 //
+// P_r is never staged in shared memory: the softmax writes it (bf16, two per
+// 32-bit column) over the S buffer it was computed from, and the P V
+// product reads its A operand from tensor memory.  Each row tile has two S/P
+// buffers, so the softmax of stage k + 1 writes its P while P V of stage k
+// still runs; an S buffer is reused for stage k + 2 once P V of stage k,
+// which read P from it, has completed.
+//
 // Warp roles (448 threads, one CTA per SM):
 //   warps 0, 11 TMA producers: stream 64-token stages (4 blocks of 16 tokens)
 //               of K and of V into two 4-stage rings, block ids fetched 32
@@ -20,11 +27,11 @@
 //   warps 10, 13 lane 0 issues the P V MMAs of row tile 0 or 1.
 //   warps 2-9   softmax, one query row per thread (warps 2-5 row tile 0,
 //               warps 6-9 row tile 1): read the row of S from TMEM, mask,
-//               exponentiate (base 2), write P (bf16) to shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads, keep (m, l).
+//               exponentiate (base 2), write P (bf16) back into the first 32
+//               columns of the same S buffer, keep (m, l).
 // TMEM (512 columns): row tile r holds O_r in columns [256 r, 256 r + 128)
-// and two S buffers of 64 columns after it, so the MMA of S for the next
-// stage overlaps the softmax of this one.
+// and two S/P buffers of 64 columns after it, so the MMA of S for the next
+// stage overlaps the softmax of this one and P V of the previous one.
 //
 // Online softmax with a lazy reference: each row keeps a reference max m and
 // rescales O (a TMEM read-modify-write) only when a stage's max exceeds m by
@@ -52,7 +59,6 @@ constexpr int TC_TOK = 64;                                   // tokens per stage
 constexpr int TC_HALF = TC_TOK * 128;                        // 64 tokens x 64 columns bf16 = 8 KiB
 constexpr int TC_RING_STAGE = 2 * TC_HALF;                   // K (or V) of a stage: half 0, half 1
 constexpr int TC_QTILE = 128 * D * 2;                        // 128 rows x 128 columns bf16 = 32 KiB
-constexpr int TC_PBUF = 128 * TC_TOK * 2;                    // 128 rows x 64 tokens bf16 = 16 KiB
 constexpr int TC_ROWTILES = 2;
 constexpr int TC_SOFTMAX_WARP0 = 2;
 constexpr int TC_PV_WARP = TC_SOFTMAX_WARP0 + 4 * TC_ROWTILES;   // 10
@@ -64,20 +70,19 @@ constexpr int TC_THREADS = (TC_PV1_WARP + 1) * 32;
 constexpr int OFF_K = 0;
 constexpr int OFF_V = TC_NSTAGE * TC_RING_STAGE;
 constexpr int OFF_Q = 2 * TC_NSTAGE * TC_RING_STAGE;
-constexpr int OFF_P = OFF_Q + TC_ROWTILES * TC_QTILE;
-constexpr int OFF_BAR = OFF_P + TC_ROWTILES * TC_PBUF;
-// mbarriers; S buffers are indexed 2 r + b (row tile r, buffer b), the
-// P buffer and O accumulator by r
+constexpr int OFF_BAR = OFF_Q + TC_ROWTILES * TC_QTILE;
+// mbarriers; S/P buffers are indexed 2 r + b (row tile r, buffer b):
+// S_FULL when S is in the buffer, P_FULL when P overwrote it, PV_DONE when
+// the P V product that read that P has completed (the buffer is free again)
 enum {
     B_K_FULL = 0,
     B_K_EMPTY = B_K_FULL + TC_NSTAGE,
     B_V_FULL = B_K_EMPTY + TC_NSTAGE,
     B_V_EMPTY = B_V_FULL + TC_NSTAGE,
     B_S_FULL = B_V_EMPTY + TC_NSTAGE,
-    B_S_FREE = B_S_FULL + 4,
-    B_P_FULL = B_S_FREE + 4,
-    B_PV_DONE = B_P_FULL + 2,
-    B_Q_FULL = B_PV_DONE + 2,
+    B_P_FULL = B_S_FULL + 4,
+    B_PV_DONE = B_P_FULL + 4,
+    B_Q_FULL = B_PV_DONE + 4,
     B_FINAL = B_Q_FULL + 2,   // one per issuer: S0, PV0, S1, PV1
     B_COUNT = B_FINAL + 4
 };
@@ -105,6 +110,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+        : "memory");
+}
+// The same with A (M x K, two bf16 per 32-bit column, row i in lane i) read
+// from tensor memory at a_tmem.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)acc)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -214,11 +228,8 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(B_S_FULL + i), 1);
-            mbar_init(bar(B_S_FREE + i), 4);
-        }
-        for (int r = 0; r < TC_ROWTILES; ++r) {
-            mbar_init(bar(B_P_FULL + r), 4);
-            mbar_init(bar(B_PV_DONE + r), 1);
+            mbar_init(bar(B_P_FULL + i), 4);     // the row tile's four softmax warps
+            mbar_init(bar(B_PV_DONE + i), 1);
         }
         for (int r = 0; r < TC_ROWTILES; ++r) mbar_init(bar(B_Q_FULL + r), 4);
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_FINAL + i), 1);
@@ -313,17 +324,17 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // ------------------------------------------------------ MMA issuers
         // Four single-thread issuers, one chain of waits each: for row tile
         // r, an S issuer (warp 1 for r = 0, warp 12 for r = 1) issues
-        // S_r(k) = Q_r K^T as soon as stage k's K landed and the S buffer it
-        // overwrites was read (S runs at most two stages ahead of the
-        // softmax), and a PV issuer (warp 10, warp 13) issues O_r += P_r V as
-        // soon as stage k's V landed and P_r(k) is in shared memory.  A ring
+        // S_r(k) = Q_r K^T as soon as stage k's K landed and the P V of
+        // stage k - 2, which read the buffer S_r(k) overwrites, completed;
+        // a PV issuer (warp 10, warp 13) issues O_r += P_r V as soon as stage
+        // k's V landed and P_r(k) is in tensor memory.  A ring
         // slot goes back to its producer once both issuers of its kind have
         // committed it; the issuer of a row tile a unit does not have simply
         // arrives.
         const bool s_role = warp == 1 || warp == TC_S1_WARP;
         const int my_r = (warp == 1 || warp == TC_PV_WARP) ? 0 : 1;
         if (lane == 0) {
-            const uint32_t sQ = base + OFF_Q + my_r * TC_QTILE, sP = base + OFF_P + my_r * TC_PBUF;
+            const uint32_t sQ = base + OFF_Q + my_r * TC_QTILE;
             int32_t g = 0, js = 0, qc = 0;
             bool ok = true, any = false;
             int32_t t = t_begin, u = u0;
@@ -344,7 +355,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                         ok = thread_wait(bar(B_K_FULL + slot), ph, abortp, a.meta);
                         if (ok && active) {
                             const int b = js & 1;
-                            ok = thread_wait(bar(B_S_FREE + 2 * my_r + b), ((uint32_t)(js >> 1) & 1u) ^ 1u, abortp,
+                            ok = thread_wait(bar(B_PV_DONE + 2 * my_r + b), ((uint32_t)(js >> 1) & 1u) ^ 1u, abortp,
                                              a.meta);
                             if (!ok) break;
                             tc_fence_after();
@@ -367,15 +378,17 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     } else {
                         ok = thread_wait(bar(B_V_FULL + slot), ph, abortp, a.meta);
                         if (ok && active) {
-                            ok = thread_wait(bar(B_P_FULL + my_r), (uint32_t)js & 1u, abortp, a.meta);
+                            const int b = js & 1;
+                            ok = thread_wait(bar(B_P_FULL + 2 * my_r + b), (uint32_t)(js >> 1) & 1u, abortp, a.meta);
                             if (!ok) break;
                             tc_fence_after();
                             const uint32_t vst = base + OFF_V + slot * TC_RING_STAGE;
                             const uint32_t id = idesc_bf16(128, 128, 0, 1);
+                            const uint32_t tP = tmem + my_r * 256 + 128 + b * 64;   // 16 tokens per 8 columns
                             for (int kk = 0; kk < ntiles; ++kk)
-                                umma_bf16(tmem + my_r * 256, sdesc(sP + kk * 32, 16, 1024),
-                                          sdesc(vst + kk * 2048, TC_HALF, 1024), id, kk > 0 || k > 0);
-                            umma_commit(bar(B_PV_DONE + my_r));
+                                umma_bf16_ta(tmem + my_r * 256, tP + kk * 8, sdesc(vst + kk * 2048, TC_HALF, 1024), id,
+                                             kk > 0 || k > 0);
+                            umma_commit(bar(B_PV_DONE + 2 * my_r + b));
                             umma_commit(bar(B_V_EMPTY + slot));
                             ++js;
                             any = true;
@@ -402,7 +415,6 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int trow = sub * 32 + lane;         // row within the row tile
         const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16) + r * 256;
         unsigned char* sQ = sm + OFF_Q + r * TC_QTILE;
-        unsigned char* sP = sm + OFF_P + r * TC_PBUF;
         const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
         const int row = r * 128 + trow;
         // This thread's row of a unit's Q into the K-major swizzled tile, and
@@ -462,9 +474,6 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                         s[32 + i] = __uint_as_float(v1[i]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_S_FREE + 2 * r + b));
                 // mask stage columns past the chunk and positions the row does
                 // not see (only stages some row of the warp does not fully see)
                 const int32_t pos0 = (U.blk_start + (st - U.tile_off)) * BS;
@@ -492,7 +501,8 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     const bool need = mx > m_ref + RESCALE_THRESHOLD;
                     if (__any_sync(0xffffffffu, need)) {
                         // O holds the PV of the previous stage once it completes
-                        ok = warp_wait(bar(B_PV_DONE + r), (uint32_t)(js - 1) & 1u, abortp, a.meta);
+                        ok = warp_wait(bar(B_PV_DONE + 2 * r + ((js - 1) & 1)), (uint32_t)((js - 1) >> 1) & 1u,
+                                       abortp, a.meta);
                         if (!ok) break;
                         tc_fence_after();
                         const float alpha = need ? ex2_approx(m_ref - mx) : 1.f;
@@ -527,22 +537,13 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     }
                     l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
                 }
-                // the P buffer is free once the previous stage's PV has finished
-                if (js >= 1) {
-                    ok = warp_wait(bar(B_PV_DONE + r), (uint32_t)(js - 1) & 1u, abortp, a.meta);
-                    if (!ok) break;
-                }
-                {
-                    unsigned char* prow = sP + trow * 128;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4*>(prow + ((ch ^ (trow & 7)) << 4)) =
-                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                }
-                fence_async_smem();
+                // P over the S it came from (token 2 i in the low half of
+                // column i); unused columns past the chunk hold P = 0
+                tmem_st32(tl + 128 + b * 64, pk);
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_P_FULL + r));
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + 2 * r + b));
             }
             if (!ok) break;
             // the next chunk this row tile works on: stage its Q now
@@ -562,7 +563,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
             }
             // chunk done: O after the last PV -> partial row
-            ok = warp_wait(bar(B_PV_DONE + r), (uint32_t)(js - 1) & 1u, abortp, a.meta);
+            ok = warp_wait(bar(B_PV_DONE + 2 * r + ((js - 1) & 1)), (uint32_t)((js - 1) >> 1) & 1u, abortp, a.meta);
             if (!ok) break;
             tc_fence_after();
             const int32_t prow = U.prow_base + (c - U.cfirst) * U.n_rows + row;
