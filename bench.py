@@ -739,6 +739,87 @@ def run_attention_only(args):
     pool.close()
 
 
+def run_mcts_loop(args):
+    """The MCTS demo's loop as a decode loop: root prompt of 2048 tokens; each
+    iteration forks a uniformly chosen live leaf of depth < 12 into 4
+    children, appends 32 tokens to each, and runs tree decode attention for
+    every live leaf (a new query set, so a new plan, every iteration).  Per
+    iteration: the host time of planning (inside the attention call), the
+    attention call's device time, and the wall time of the iteration's three
+    calls up to the attention's completion."""
+    import torch
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__ as g
+    g.build()
+    from copy_write_forked_gb300 import workloads as W
+    from copy_write_forked_gb300.runner import pool_for
+    w = W.mcts(iters=args.mcts_iters)
+    pool = pool_for(w, fold_segments=args.fold_segments)
+    gen = torch.Generator(device=dev).manual_seed(77)
+    maxq = len(w.query)
+    Qall = torch.randn((maxq, 1, w.n_q_heads, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(Qall)
+    h = {}
+    live = []
+    rows = []
+    pool.set_profiling(True)
+    ops = w.ops
+    i = 0
+    while i < len(ops):
+        op = ops[i]
+        if op.kind == "new":
+            h[op.branches[0]] = pool.new_branch()
+            live.append(op.branches[0])
+        elif op.kind == "append":            # the root prompt
+            K, V = w.kv(i, dev)
+            pool.append_kv([h[b] for b in op.branches], K, V)
+        else:                                # one iteration: fork, then the children's append
+            nxt = ops[i + 1]
+            K, V = w.kv(i + 1, dev)
+            pool.sync()
+            t0 = time.perf_counter()
+            kids = pool.fork_batch([h[p] for p in op.branches], [len(c) for c in op.children])
+            for ch, hs in zip(op.children, kids):
+                h.update(zip(ch, hs))
+            for p, ch in zip(op.branches, op.children):
+                live.remove(p)
+                live.extend(ch)
+            pool.append_kv([h[b] for b in nxt.branches], K, V)
+            q = sorted(live)
+            n = len(q)
+            pool.tree_attn_decode(Qall[:n], [h[b] for b in q], out=out[:n])
+            pool.sync()
+            t1 = time.perf_counter()
+            tm = pool.last_timings()
+            st = pool.last_plan_stats()
+            rows.append({"leaves": n, "plan_us": st["plan_us"], "call_us": tm["attn_total"] * 1e3,
+                         "wall_us": (t1 - t0) * 1e6})
+            i += 1
+        i += 1
+    pool.set_profiling(False)
+    pool.close()
+    last = rows[-100:]
+    line = {"metric": METRIC, "workload": "mctsloop",
+            "config": {"workload": "MCTS loop: root 2048, %d iterations of fork 4 x 32 tokens, tree decode "
+                                   "attention over every live leaf after each iteration" % args.mcts_iters,
+                       "timing": "per iteration, host plan time inside the attention call; device time of the "
+                                 "attention call (CUDA events); wall time of fork + append + attention up to "
+                                 "completion"},
+            "iterations": len(rows),
+            "last100": {"leaves_mean": statistics.mean(r["leaves"] for r in last),
+                        "host_plan_us_mean": statistics.mean(r["plan_us"] for r in last),
+                        "gpu_call_us_mean": statistics.mean(r["call_us"] for r in last),
+                        "wall_us_mean": statistics.mean(r["wall_us"] for r in last)},
+            "all": {"host_plan_us_mean": statistics.mean(r["plan_us"] for r in rows),
+                    "gpu_call_us_mean": statistics.mean(r["call_us"] for r in rows),
+                    "plan_below_call_fraction": sum(r["plan_us"] < r["call_us"] for r in rows) / len(rows)},
+            "host_plan_vs_gpu_call_last100": statistics.mean(r["plan_us"] for r in last) /
+                                             statistics.mean(r["call_us"] for r in last)}
+    print(json.dumps(line), flush=True)
+
+
 def fork_latency(dev, reps=200):
     """Fork of a chain of `depth` blocks whose tail block is half full, with 1
     and 4 children (then freed).  Three views per call: the host time of the C
@@ -1049,6 +1130,7 @@ def main():
                     help="full-path workloads: 'decode' (default) forks every leaf of the prebuilt tree once, "
                          "appends one token per child, attends and frees the old leaves; 'divergent' rebuilds "
                          "the tree below the prefixes (fork + append of all divergent tokens) every step")
+    ap.add_argument("--mcts-iters", type=int, default=500, help="--workload mctsloop: iterations")
     ap.add_argument("--requests", type=int, default=None,
                     help="full-path workloads: fewer requests than the configuration (a smaller case for ncu)")
     ap.add_argument("--tc-min-rows", type=int, default=0,
@@ -1057,10 +1139,11 @@ def main():
                     help="fold short shared segments into the ones that follow (0: default, k: below k percent "
                          "of the estimate, -1: off)")
     ap.add_argument("--workload", default="stress",
-                    choices=["stress", "beam", "mcts", "specverify", "stressattn", "decode32", "forks"],
+                    choices=["stress", "beam", "mcts", "specverify", "stressattn", "decode32", "forks", "mctsloop"],
                     help="stress (default) and beam: the full-path step; mcts, specverify, stressattn: tree "
                          "attention alone; decode32: the beam step through 32 layers; forks: the 100,000 "
-                         "batched forks and fork latency")
+                         "batched forks and fork latency; mctsloop: the MCTS demo's fork / append / attend "
+                         "loop with host planning against the device call")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1073,6 +1156,8 @@ def main():
         run_decode_layers(args)
     elif args.workload == "forks":
         run_forks(args)
+    elif args.workload == "mctsloop":
+        run_mcts_loop(args)
     elif args.workload in FULL_PATH:
         run_ours(args)
     else:

@@ -56,6 +56,121 @@ constexpr int ML_BYTES = NCONS * 16 * 2 * 4;
 constexpr size_t SMEM_BF16 = 1024 + (size_t)NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8 + ML_BYTES;
 
 
+// ------------------------------------------------ log-sum-exp merge of one row
+// One warp merges output row o (branch qi, query token j, query head h*G + g)
+// of head_dim 128: the row's partials are the chunks of one unit per segment
+// on the branch's path; lanes enumerate them (lane e takes path entry e, a
+// warp scan turns chunk counts into partial indices), load every (m, l) at
+// once, and reduce
+//     M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum acc_i 2^(m_i - M) / L
+// with lane l owning columns 4 l .. 4 l + 3 (one 16-byte load per partial
+// row), eight acc rows in flight.  Partial rows are read through L2 only.
+// Nothing is stored when the pool's status word is set.
+template <typename T>
+__device__ __forceinline__ void merge_row_wide(const AttnArgs& a, int32_t o, int lane, int32_t status) {
+    const AttnPlanDev& pl = a.plan;
+    const int G = pl.group;
+    const int32_t qi = o / (pl.q_len * pl.n_q_heads);
+    const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
+    const int32_t j = rem / pl.n_q_heads, hq = rem - j * pl.n_q_heads;
+    const int32_t h = hq / G, g = hq - h * G;
+    const int32_t pbeg = pl.path_off[qi], pend = pl.path_off[qi + 1];
+    float M = -INFINITY, L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int32_t e0 = pbeg; e0 < pend; e0 += 32) {
+        // lane e: one path entry -> its unit's chunks for this row
+        const int32_t e = e0 + lane;
+        int32_t nch = 0, base = 0, stride = 0;
+        if (e < pend) {
+            // unit_base, ngroups, first segment row, rows per group
+            const int4 pe = __ldg(reinterpret_cast<const int4*>(pl.path) + e);
+            const int32_t sr = pe.z + j * G + g;
+            const int32_t grp = sr / pe.w;
+            const AttnUnit U = pl.units[pe.x + h * pe.y + grp];
+            nch = U.nchunks;
+            base = U.prow_base + (sr - grp * pe.w);
+            stride = U.n_rows;
+        }
+        int32_t incl = nch;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        const int32_t excl = incl - nch;
+        for (int32_t p0 = 0; p0 < total; p0 += 32) {
+            // lane p: partial p of this batch -> its partial row
+            const int32_t pidx = p0 + lane;
+            int32_t ent = 0;
+            const int n_ent = min(32, pend - e0);   // lanes past it hold no chunks
+            for (int k = 0; k < n_ent; ++k) ent += (__shfl_sync(0xffffffffu, incl, k) <= pidx) ? 1 : 0;
+            ent = min(ent, 31);
+            const int32_t eb = __shfl_sync(0xffffffffu, base, ent);
+            const int32_t es = __shfl_sync(0xffffffffu, stride, ent);
+            const int32_t ex = __shfl_sync(0xffffffffu, excl, ent);
+            const bool valid = pidx < total;
+            const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
+            const int nb = min(32, total - p0);
+            // the first eight acc rows go out with the (m, l) loads
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int32_t pr = __shfl_sync(0xffffffffu, prow, min(u, nb - 1));
+                v[u] = u < nb ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)pr * D) + lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float2 ml = valid ? __ldcg(a.part_ml + prow) : make_float2(-INFINITY, 0.f);
+            // running max over this batch
+            float mb = ml.x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+            const float Mn = fmaxf(M, mb);
+            const float Mu = Mn == -INFINITY ? 0.f : Mn;
+            const float sc = exp2f(M - Mu);   // rescale of the running state
+            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mu);
+            float lw = w * ml.y;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+            L = L * sc + lw;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] *= sc;
+            M = Mn;
+            for (int q = 0; q < nb; q += 8) {
+                float wq[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int src = min(q + u, nb - 1);
+                    const float ww = __shfl_sync(0xffffffffu, w, src);
+                    wq[u] = q + u < nb ? ww : 0.f;
+                    if (q > 0) {
+                        const int32_t pr = __shfl_sync(0xffffffffu, prow, src);
+                        v[u] = q + u < nb
+                                   ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (int64_t)pr * D) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    acc[0] = fmaf(v[u].x, wq[u], acc[0]);
+                    acc[1] = fmaf(v[u].y, wq[u], acc[1]);
+                    acc[2] = fmaf(v[u].z, wq[u], acc[2]);
+                    acc[3] = fmaf(v[u].w, wq[u], acc[3]);
+                }
+            }
+        }
+    }
+    if (status) return;
+    const float inv = 1.f / L;
+    T* dst = static_cast<T*>(a.out) + (int64_t)o * D + 4 * lane;
+    if constexpr (sizeof(T) == 2) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    } else {
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    }
+}
+
 // ------------------------------------------------ consumer side of one chunk
 // The P = 4 / rt consumer warps of a row tile split head_dim: warp w owns row
 // tile r = w / P and columns [(w % P) NCOL, (w % P + 1) NCOL), NCOL = 128 / P,
@@ -662,6 +777,10 @@ __global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs
     // the status word is checked only before the store, so that its load
     // overlaps the plan loads (the plan is always readable)
     const int32_t status = *reinterpret_cast<volatile const int32_t*>(&a.meta->status);
+    if constexpr (WIDE) {
+        merge_row_wide<T>(a, o, lane, status);
+        return;
+    }
     const int G = pl.group;
     const int32_t qi = o / (pl.q_len * pl.n_q_heads);
     const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
@@ -975,8 +1094,9 @@ struct HostPlan {
     size_t partial_rows = 0;
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
-    void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes
-        segs.clear(); members.clear(); units.clear(); cta_begin.clear(); cta_unit.clear();
+    void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes; the unit and
+                     // member arrays keep their size too (build_plan resizes and fills them in place)
+        segs.clear(); cta_begin.clear(); cta_unit.clear();
         tc_cta_begin.clear(); tc_cta_unit.clear(); path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         n_tc_units = 0;
@@ -997,14 +1117,14 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 // MMA pipeline and stores up to 256 partial rows of 520 bytes.
 struct ClassWeights {
     int64_t unit_start;
-    int64_t rows_per_weight;   // a unit start also weighs n_rows / rows_per_weight (0: no row term)
+    int32_t row_shift;         // a unit start also weighs n_rows >> row_shift (-1: no row term)
     int64_t min_per_cta;       // smallest total weight worth a CTA of its own
 };
-constexpr ClassWeights kSmallWeights{16, 2, 8};
-constexpr ClassWeights kTcWeights{24, 0, 32};
+constexpr ClassWeights kSmallWeights{16, 1, 8};
+constexpr ClassWeights kTcWeights{24, -1, 32};
 inline int64_t tile_weight(int rt) { return 1 + rt; }
 inline int64_t start_weight(const ClassWeights& cw, int32_t n_rows) {
-    return cw.unit_start + (cw.rows_per_weight ? n_rows / cw.rows_per_weight : 0);
+    return cw.unit_start + (cw.row_shift >= 0 ? (n_rows >> cw.row_shift) : 0);
 }
 
 // Stream-K split of one class's tile list (units [u_lo, u_hi), tiles
@@ -1025,7 +1145,9 @@ void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_
     hp.cuts.clear();
     hp.cuts.push_back(0);
     {
+        // the weight at which cut c falls; one division per cut, not per unit
         int c = 1;
+        int64_t target = C0 > 1 ? (weight + C0 - 1) / C0 : INT64_MAX;
         int64_t cw = 0;
         for (int32_t ui = u_lo; ui < u_hi; ++ui) {
             const AttnUnit& U = hp.units[ui];
@@ -1033,13 +1155,12 @@ void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_
             const int64_t tw = tile_weight(U.rt);
             const int64_t us = start_weight(cw_, U.n_rows);
             const int64_t uw = us + nb * tw;
-            while (c < C0) {
-                const int64_t target = (weight * c + C0 - 1) / C0;
-                if (target >= cw + uw) break;
+            while (c < C0 && target < cw + uw) {
                 const int64_t k = std::max<int64_t>(0, (target - cw - us + tw - 1) / tw);
                 const int64_t cut = U.tile_off + std::min<int64_t>(k, nb);
                 if (cut > hp.cuts.back() && cut < T) hp.cuts.push_back(cut);
                 ++c;
+                target = c < C0 ? (weight * c + C0 - 1) / C0 : INT64_MAX;
             }
             cw += uw;
         }
@@ -1068,8 +1189,12 @@ void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_
     }
 }
 
+int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
+                int max_tc_ctas, HostPlan& hp);
+
 // max_ctas: CTAs of the mma.sync/fp32 kernel; max_tc_ctas: of the tcgen05
-// kernel (0 when it is not used).
+// kernel (0 when it is not used).  The segments (after folding) are left in
+// hp.psegs / hp.seg_members.
 int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
                int max_tc_ctas, HostPlan& hp) {
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
@@ -1097,6 +1222,19 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
         fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, n_nodes,
                       hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
                       hp.psegs, hp.seg_members);
+    return build_units(p, branches, n, q_len, nq, max_ctas, max_tc_ctas, hp);
+}
+
+// The plan's units, CTA partitions, partial rows and paths from the segments
+// in hp.psegs / hp.seg_members (hp.tiles and the arrays are rebuilt;
+// hp.unique_tiles is left as it is).
+int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
+                int max_tc_ctas, HostPlan& hp) {
+    const int32_t G = nq / p->n_kv, nkv = p->n_kv;
+    const int32_t RM = q_len * G;
+    const bool bf16 = p->dtype == DENDRITE_BF16;
+    const int small_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    const bool tc_on = bf16 && max_tc_ctas > 0 && p->tc_min_rows >= 0;
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by
     // more than tc_min_rows rows per kv head, pass 1 the rest.  The unit and
@@ -1507,9 +1645,19 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
     // Only appends since the plan was built, and no queried branch reached a
     // new block: the segments, units and partition are unchanged, and only
     // the members' lengths (their rows' visibility limits) need refreshing.
-    bool refresh = !hit && same_query && pc.shape_version == p->shape_version;
-    for (int32_t i = 0; refresh && i < n; ++i)
-        refresh = (p->br[branches[i]].len + p->block_size - 1) / p->block_size == pc.n_blocks[i];
+    // Appends alone, and some queried branches reached new blocks: when each
+    // of those branches' last segment is its own (read by it alone, ending at
+    // its last block), the segments stay as they are but for those segments'
+    // lengths, and only the units, partition and paths are rebuilt.
+    const bool appends_only = !hit && same_query && pc.shape_version == p->shape_version;
+    bool refresh = appends_only, grow = appends_only;
+    for (int32_t i = 0; appends_only && i < n; ++i) {
+        const int32_t nb = (p->br[branches[i]].len + p->block_size - 1) / p->block_size;
+        if (nb == pc.n_blocks[i]) continue;
+        refresh = false;
+        if (nb < pc.n_blocks[i] || pc.last_seg[i] < 0) grow = false;
+    }
+    grow = grow && !refresh;
     if (refresh) {
         const auto t0 = std::chrono::steady_clock::now();
         const int ib = p->plan_buf;
@@ -1535,7 +1683,20 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         const auto t0 = std::chrono::steady_clock::now();
         static thread_local HostPlan hp;
         hp.clear();
-        DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp));
+        if (grow) {
+            hp.psegs = pc.segs;
+            hp.seg_members = pc.seg_members;
+            hp.unique_tiles = pc.unique_tiles;
+            for (int32_t i = 0; i < n; ++i) {
+                const int32_t d = (p->br[branches[i]].len + p->block_size - 1) / p->block_size - pc.n_blocks[i];
+                if (!d) continue;
+                hp.psegs[pc.last_seg[i]].block_count += d;
+                hp.unique_tiles += (int64_t)d * p->n_kv;
+            }
+            DENDRITE_TRY(build_units(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp));
+        } else {
+            DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp));
+        }
         size_t off[kPlanSections + 1];
         const size_t b = plan_layout(hp, off);
         DENDRITE_TRY(ensure_capacity(p, b, hp.partial_rows));
@@ -1564,6 +1725,18 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         pc.n_members = (int32_t)hp.members.size();
         pc.n_blocks.resize(n);
         for (int32_t i = 0; i < n; ++i) pc.n_blocks[i] = (p->br[branches[i]].len + p->block_size - 1) / p->block_size;
+        pc.segs = hp.psegs;
+        pc.seg_members = hp.seg_members;
+        pc.unique_tiles = hp.unique_tiles;
+        if (!grow) {   // grown segments still end at their branch's last block
+            pc.last_seg.assign(n, -1);
+            for (int32_t si = 0; si < (int32_t)hp.psegs.size(); ++si) {
+                const Segment& sg = hp.psegs[si];
+                if (sg.n_members != 1) continue;
+                const int32_t m = hp.seg_members[sg.member_offset];
+                if (sg.block_start + sg.block_count == pc.n_blocks[m]) pc.last_seg[m] = si;
+            }
+        }
         pc.q_len = q_len;
         pc.n_q_heads = n_q_heads;
         pc.branches.assign(branches, branches + n);
@@ -1575,7 +1748,7 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         pc.stats.unique_tiles = hp.unique_tiles;
         pc.stats.n_tc_units = hp.n_tc_units;
         pc.stats.n_tc_ctas = pc.dev.n_tc_ctas;
-        pc.stats.refreshed = 0;
+        pc.stats.refreshed = grow ? 2 : 0;
         pc.stats.plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
     } else {
         pc.stats.refreshed = 0;

@@ -175,6 +175,16 @@ struct PendingAppend {
     int32_t n_done = 0;
 };
 
+// A sharing segment found by the planner (planner.cpp).
+struct Segment {
+    int32_t rep_node;
+    int32_t block_start;
+    int32_t block_count;
+    int32_t member_offset;
+    int32_t n_members;
+    int32_t owner;      // node whose blocks these are (a node's segments are consecutive, ascending)
+};
+
 struct PlanCache {
     bool valid = false;
     uint64_t version = 0, shape_version = 0;
@@ -188,6 +198,14 @@ struct PlanCache {
     size_t members_off = 0;          // byte offset of the member list in the packed plan
     int32_t n_members = 0;
     dendrite_plan_stats stats{};
+    // The plan's segments (after folding) and, per queried branch, the index
+    // of its last segment when that segment is read by that branch alone and
+    // ends at its last block (-1 otherwise): appends that take such branches
+    // into new blocks only lengthen those segments.
+    std::vector<Segment> segs;
+    std::vector<int32_t> seg_members;
+    std::vector<int32_t> last_seg;
+    int64_t unique_tiles = 0;
 };
 
 }  // namespace dendrite
@@ -281,15 +299,7 @@ void prof_begin(dendrite_pool* p, TimingKind k, cudaStream_t s);
 void prof_end(dendrite_pool* p, TimingKind k, cudaStream_t s);
 int check_live(const dendrite_pool* p, int32_t h);
 
-// Planner (planner.cpp): segments over the node forest.
-struct Segment {
-    int32_t rep_node;
-    int32_t block_start;
-    int32_t block_count;
-    int32_t member_offset;
-    int32_t n_members;
-    int32_t owner;      // node whose blocks these are (a node's segments are consecutive, ascending)
-};
+// Planner (planner.cpp): segments over the node forest (struct Segment above).
 void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
                    const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
                    std::vector<Segment>& segs, std::vector<int32_t>& members);

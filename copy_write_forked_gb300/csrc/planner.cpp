@@ -166,9 +166,12 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
                    std::vector<Segment>& segs, std::vector<int32_t>& members) {
     const int32_t S = (int32_t)segs.size();
     if (fp.fold_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
-    static thread_local std::vector<int32_t> node_first, node_count, prev, koff, kseg, eoff, emem, order, ext;
+    static thread_local std::vector<int32_t> node_first, node_count, prev, koff, kseg, eoff, emem, order, ext, qblocks;
     static thread_local std::vector<char> folded;
     const int32_t bs = block_size;
+    // each queried branch's block count
+    qblocks.resize(n_queried);
+    for (int32_t q = 0; q < n_queried; ++q) qblocks[q] = (len[queried[q]] + bs - 1) / bs;
     // each owner node's segments (consecutive in segs, in ascending blocks)
     node_first.assign(n_nodes, -1);
     node_count.assign(n_nodes, 0);
@@ -208,10 +211,8 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
         if (prev[si] >= 0) koff[prev[si] + 1]++;
         const Segment& sg = segs[si];
         const int32_t end = sg.block_start + sg.block_count;
-        for (int32_t k = 0; k < sg.n_members; ++k) {
-            const int32_t m = members[sg.member_offset + k];
-            if ((len[queried[m]] + bs - 1) / bs == end) eoff[si + 1]++;
-        }
+        for (int32_t k = 0; k < sg.n_members; ++k)
+            if (qblocks[members[sg.member_offset + k]] == end) eoff[si + 1]++;
     }
     for (int32_t si = 0; si < S; ++si) {
         koff[si + 1] += koff[si];
@@ -230,7 +231,7 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
             const int32_t end = sg.block_start + sg.block_count;
             for (int32_t k = 0; k < sg.n_members; ++k) {
                 const int32_t m = members[sg.member_offset + k];
-                if ((len[queried[m]] + bs - 1) / bs == end) emem[e++] = m;
+                if (qblocks[m] == end) emem[e++] = m;
             }
         }
     }

@@ -189,7 +189,9 @@ int dendrite_append_layer(dendrite_pool* pool, int32_t layer, const void* K, con
  * read again by each longer range that follows it (pool option
  * fold_segments).  The plan built from the branch tree is cached until the
  * tree changes; after appends alone, where no queried branch reached a new
- * block, only its members' lengths are refreshed.  `branches` may not hold
+ * block, only its members' lengths are refreshed, and where some did, the
+ * cached sharing segments are lengthened instead of found again when each of
+ * those branches reads its last segment alone.  `branches` may not hold
  * duplicates.
  * DENDRITE_ELIMIT if a shared range would be read by 2^24 or more query rows
  * per KV head, or the plan outgrows 32-bit indices.
@@ -303,7 +305,11 @@ typedef struct dendrite_plan_stats {
     int32_t n_tc_ctas;      /* CTAs of the tcgen05 kernel (not counted in n_ctas)   */
     int32_t refreshed;      /* 1: the cached plan only had its members' lengths     *
                              * refreshed (only appends since it was built, and no   *
-                             * queried branch reached a new block); 0 otherwise     */
+                             * queried branch reached a new block); 2: only appends *
+                             * since it was built and the branches that reached new *
+                             * blocks each read their last segment alone, so the    *
+                             * cached segments were lengthened and only the units,  *
+                             * CTA partition and paths rebuilt; 0: built anew       */
     int32_t reserved;
 } dendrite_plan_stats;
 int dendrite_last_plan_stats(dendrite_pool* pool, dendrite_plan_stats* out);

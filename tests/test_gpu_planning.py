@@ -1,0 +1,158 @@
+"""Planning in fork-heavy loops, through the C-ABI library against the fp64
+oracle at every step: the MCTS demo's loop (dendrite demo.tape, section "MCTS
+demo": pick a leaf, fork it four ways, extend each child, then decode every
+live leaf), where every iteration changes the queried set and so needs a new
+plan, and decode loops whose appends cross into new blocks."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from copy_write_forked_gb300 import workloads as W
+from copy_write_forked_gb300.runner import pool_for
+from oracle import KVTree
+
+from _harness import half_ulp_bf16
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+    torch.cuda.set_device(0)
+
+
+def _check(tree, leaf_ids, Q, out, sample):
+    for i in sample:
+        ref = tree.attend(leaf_ids[i], Q[i].cpu())
+        got = out[i].double().cpu().numpy()
+        err = np.abs(got - ref)
+        assert np.isfinite(got).all()
+        assert (err <= TOL + half_ulp_bf16(ref)).all(), (i, float(err.max()))
+
+
+@pytest.mark.parametrize("fold", [0, -1])
+def test_mcts_loop_matches_oracle_every_iteration(fold):
+    """60 iterations of fork 4 / append 32 / attend over every live leaf; each
+    iteration's outputs are compared with the oracle's for the 4 new children
+    and 4 other live leaves."""
+    w = W.mcts(root=512, iters=60)
+    pool = pool_for(w, fold_segments=fold)
+    tree = KVTree(w.n_kv_heads, w.head_dim)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    h, live = {}, []
+    rng = random.Random(3)
+    iters = 0
+    ops = w.ops
+    i = 0
+    while i < len(ops):
+        op = ops[i]
+        if op.kind == "new":
+            h[op.branches[0]] = pool.new_branch()
+            tree.new_root(op.branches[0])
+            live.append(op.branches[0])
+        elif op.kind == "append":
+            K, V = w.kv(i, "cuda")
+            pool.append_kv([h[b] for b in op.branches], K, V)
+            for j, b in enumerate(op.branches):
+                tree.append(b, K[j].cpu(), V[j].cpu())
+        else:
+            kids = pool.fork_batch([h[p] for p in op.branches], [len(c) for c in op.children])
+            for p, ch, hs in zip(op.branches, op.children, kids):
+                h.update(zip(ch, hs))
+                tree.fork(p, list(ch))
+                live.remove(p)
+                live.extend(ch)
+            nxt = ops[i + 1]
+            K, V = w.kv(i + 1, "cuda")
+            pool.append_kv([h[b] for b in nxt.branches], K, V)
+            for j, b in enumerate(nxt.branches):
+                tree.append(b, K[j].cpu(), V[j].cpu())
+            q = sorted(live)
+            Q = torch.randn((len(q), 1, w.n_q_heads, w.head_dim), generator=gen, device="cuda").bfloat16()
+            out = pool.tree_attn_decode(Q, [h[b] for b in q])
+            pool.sync()
+            new = [q.index(c) for c in nxt.branches]
+            others = rng.sample(range(len(q)), min(4, len(q)))
+            _check(tree, q, Q, out, sorted(set(new + others)))
+            iters += 1
+            i += 1
+        i += 1
+    assert iters == 60
+    pool.close()
+
+
+def _extend(w, ops, query=None):
+    return W.Workload(w.name + "_ext", w.n_kv_heads, w.n_q_heads, w.head_dim, w.block_size, w.dtype,
+                      list(w.ops) + list(ops), tuple(query if query is not None else w.query), w.q_len, w.seed)
+
+
+@pytest.mark.parametrize("step_tokens", [1, 7, 23])
+def test_block_crossing_appends_lengthen_cached_segments(step_tokens):
+    """Decode steps of 1, 7 or 23 tokens per branch: a step whose appends take
+    branches into new blocks reuses the cached segments (stats.refreshed 2),
+    with the same segments, tiles and partial rows as a plan built anew, and
+    every step matches the oracle."""
+    from _harness import check_attention
+    from copy_write_forked_gb300.runner import run_script
+    base = W.beam(requests=2, prefix=90, width=3, divergent=13)
+    # enough steps to cross at least one block boundary (the leaves start at 103 tokens)
+    steps = [W.Op("append", tuple(base.query), step_tokens) for _ in range(max(6, 24 // step_tokens))]
+    w_full = _extend(base, steps)
+    pool = pool_for(w_full)
+    h = run_script(pool, base)
+    br = [h[b] for b in base.query]
+    Q = base.q("cuda")
+    pool.tree_attn_decode(Q, br)
+    seen = set()
+    for k in range(len(steps)):
+        idx = len(base.ops) + k
+        K, V = w_full.kv(idx, "cuda")
+        pool.append_kv(br, K, V)
+        out = pool.tree_attn_decode(Q, br)
+        pool.sync()
+        st = pool.last_plan_stats()
+        seen.add(st["refreshed"])
+        w_k = W.Workload(w_full.name, w_full.n_kv_heads, w_full.n_q_heads, w_full.head_dim, w_full.block_size,
+                         w_full.dtype, w_full.ops[:idx + 1], w_full.query, w_full.q_len, w_full.seed)
+        check_attention(w_k, out, list(range(len(base.query))), TOL)
+        if st["refreshed"] == 2:
+            # a plan built anew for the same tree (another query order misses the cache)
+            perm = list(range(len(br)))[::-1]
+            pool.tree_attn_decode(Q[perm].contiguous(), [br[i] for i in perm])
+            fresh = pool.last_plan_stats()
+            assert fresh["refreshed"] == 0
+            for key in ("n_segments", "n_units", "n_partials", "tiles", "unique_tiles"):
+                assert fresh[key] == st[key], key
+            pool.tree_attn_decode(Q, br)          # the cached order again: a plain rebuild
+            assert pool.last_plan_stats()["refreshed"] == 0
+    assert 2 in seen
+    pool.close()
+
+
+def test_block_crossing_of_a_shared_last_segment_rebuilds():
+    """A queried parent whose last block range is also read by a queried child
+    (forked at its full, block-aligned length) is not lengthened in place: the
+    step that takes the parent into a new block builds the plan anew."""
+    from _harness import check_attention
+    from copy_write_forked_gb300.runner import run_script
+    ops = [W.Op("new", (0,)), W.Op("append", (0,), 48), W.Op("fork", (0,), children=((1,),)),
+           W.Op("append", (1,), 5)]
+    base = W.Workload("shared_last", 2, 8, 128, 16, torch.bfloat16, ops, (0, 1))
+    w_full = _extend(base, [W.Op("append", (0, 1), 1)])
+    pool = pool_for(w_full)
+    h = run_script(pool, base)
+    br = [h[0], h[1]]
+    Q = base.q("cuda")
+    pool.tree_attn_decode(Q, br)
+    K, V = w_full.kv(len(base.ops), "cuda")
+    pool.append_kv(br, K, V)
+    out = pool.tree_attn_decode(Q, br)
+    pool.sync()
+    assert pool.last_plan_stats()["refreshed"] == 0
+    check_attention(w_full, out, [0, 1], TOL)
+    pool.close()
