@@ -22,7 +22,14 @@ Two models, both written from the pages' statement of the method:
   fork (table copy + refcount increment), the append that copies a shared
   partial tail block only when its refcount is above 1, and free.
 
-Parity status: both models are pinned (see ``tests/test_oracle_*.py``) by
+* :mod:`oracle.turbo_quant` (O3) -- compressed KV rows (dendrite demo.tape,
+  section "TurboQuant": "TurboQuant KV compression (PolarQuant + QJL)"):
+  the pages give only the names, three test names and a ratio, so the steps
+  follow the published methods they name (random Walsh-Hadamard rotation,
+  the recursive polar transform with quantized angles, a one-bit QJL sketch
+  of the key residual) and attention over the compressed rows.
+
+Parity status: all three models are pinned (see ``tests/test_oracle_*.py``) by
 brute force on tiny inputs, closed forms, invariants and hand-derived worked
 states; no page prints a numeric attention output, so there is no printed
 value to pin against.
