@@ -262,8 +262,10 @@ def run_ours(args):
     total_steps = args.warmup + args.steps + n_prof + 2 * args.warmup + e2e_steps + 2
     grow = total_steps if kind == "decode" else 0
     nblocks = R * (P // bs + 1) + nl * (Dv // bs + 3 + grow // bs) + 64
+    from copy_write_forked_gb300 import workloads as W
     pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R + 2 * nl + 16,
-                max_blocks_per_branch=(P + Dv + grow) // bs + 8)
+                max_blocks_per_branch=(P + Dv + grow) // bs + 8,
+                turbo=W.turbo_codec(rank) if args.turbo else None)
     # prefill (untimed): the prefixes, resident in HBM
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
@@ -326,7 +328,8 @@ def run_ours(args):
         extra = state["s"] + 1 if kind == "decode" else 0
         return R * P + nl * (Dv + extra)
 
-    kv_tok = 2 * nkv * d * 2                        # K + V bytes of one token
+    # K + V bytes of one token in the pool (the records of a compressed pool)
+    kv_tok = nkv * (96 + 64) if args.turbo else 2 * nkv * d * 2
     clk = ClockSampler(local).__enter__()
     pool.set_profiling(False)
     for _ in range(args.warmup):
@@ -519,6 +522,9 @@ def run_ours(args):
     per_step = 1 + 2 + (4 if plan["n_tc_units"] else 3) + 1
     cfg = config_of(w, name)
     cfg["step"] = _step_desc(kind)
+    if args.turbo:
+        cfg["kv_storage"] = ("compressed blocks (TurboQuant records: 96-byte keys, 64-byte values per token and "
+                             "head, 3.2x smaller than bf16); algorithmic bytes count the records")
     if kind == "decode":
         # each branch's decoded tokens beyond the configuration's, first and last timed step
         cfg["decoded_tokens_per_branch_timed"] = [(tok_timed[0] - R * P) // nl - Dv - 1,
@@ -857,10 +863,11 @@ def fork_latency(dev, reps=200):
                     host.append((t1 - t0) * 1e6)
                     rt.append((t2 - t0) * 1e6)
                 pool.free(list(out))
+            skip = min(5, len(host) // 2)      # the first calls warm up
             res[f"depth{depth}_children{nc}"] = {
-                "host_call_us": statistics.median(host[5:]),
-                "gpu_event_us": statistics.median(gpu[5:]),
-                "round_trip_us": statistics.median(rt[5:])}
+                "host_call_us": statistics.median(host[skip:]),
+                "gpu_event_us": statistics.median(gpu[skip:]),
+                "round_trip_us": statistics.median(rt[skip:])}
         pool.close()
     return res
 
@@ -1126,6 +1133,8 @@ def main():
     ap.add_argument("--fork-reps", type=int, default=200, help="--workload forks: calls per fork-latency point")
     ap.add_argument("--fork-batches", type=int, default=5000,
                     help="--workload forks: batches of the timed fork stress (20 forks each)")
+    ap.add_argument("--turbo", action="store_true",
+                    help="full-path workloads on a pool of compressed blocks (TurboQuant records)")
     ap.add_argument("--step", default="decode", choices=["decode", "divergent"],
                     help="full-path workloads: 'decode' (default) forks every leaf of the prebuilt tree once, "
                          "appends one token per child, attends and frees the old leaves; 'divergent' rebuilds "

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libdendrite.so")
-SOURCES = ["pool.cu", "attn.cu", "attn_tc.cu", "planner.cpp"]
+SOURCES = ["pool.cu", "attn.cu", "attn_tc.cu", "turbo.cu", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -42,6 +42,7 @@
 #include <type_traits>
 
 #include "attn_common.cuh"
+#include "turbo.h"
 
 using namespace dendrite;
 
@@ -161,13 +162,25 @@ __device__ __forceinline__ void merge_row_wide(const AttnArgs& a, int32_t o, int
     }
     if (status) return;
     const float inv = 1.f / L;
+    float y[4] = {acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv};
+    if (a.tq_signs) {
+        // compressed pools: the partials live in the rotated space; rotate
+        // the merged row back, out = s * (H y) / sqrt(128)
+        tq_fwht(y, lane);
+        const float4 sg = __ldg(reinterpret_cast<const float4*>(a.tq_signs) + lane);
+        const float c = 0.0883883476483184405501055452631f;
+        y[0] = y[0] * c * sg.x;
+        y[1] = y[1] * c * sg.y;
+        y[2] = y[2] * c * sg.z;
+        y[3] = y[3] * c * sg.w;
+    }
     T* dst = static_cast<T*>(a.out) + (int64_t)o * D + 4 * lane;
     if constexpr (sizeof(T) == 2) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
         *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
     } else {
-        *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
     }
 }
 
@@ -1475,7 +1488,10 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     } else {
         p->ev_recorded[T_ATTN_TC] = false;   // this call ran no tensor-core kernel
     }
-    if (a.plan.n_ctas > 0) {
+    const int32_t n_out_rows = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
+    if (p->dtype == DENDRITE_TURBO) {
+        DENDRITE_TRY(launch_turbo_partials(a, a.Q, n_out_rows, p->d_tq_signs, p->d_tq_S, p->d_tq_qs, s));
+    } else if (a.plan.n_ctas > 0) {
         if (bf16) {
             DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
         } else {
@@ -1493,7 +1509,10 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
         // the grouped merge shares lookups among a group's heads but runs a
         // quarter of the warps; a small merge (beam: 1,024 rows) keeps one
         // row per warp, where the warps' latency chains overlap better
-        if (p->head_dim == D && ng > 0 && (int64_t)n_out / ng >= (int64_t)16 * p->sm_count) {
+        if (p->dtype == DENDRITE_TURBO) {
+            // rows of compressed pools are rotated back by the per-row merge
+            DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16, true>, dim3(grid), dim3(256), 0, s, a));
+        } else if (p->head_dim == D && ng > 0 && (int64_t)n_out / ng >= (int64_t)16 * p->sm_count) {
             const unsigned ggrid = (unsigned)((n_out / ng + 7) / 8);
             if (bf16) {
                 if (ng == 4) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 4>, dim3(ggrid), dim3(256), 0, s, a));
@@ -1520,7 +1539,8 @@ AttnArgs attn_args(const dendrite_pool* p, int32_t layer, const void* Q, void* o
     a.out = out;
     a.table = p->d_table;
     a.pool_k = reinterpret_cast<const float*>(static_cast<const char*>(p->d_k) + (size_t)layer * p->layer_bytes);
-    a.pool_v = reinterpret_cast<const float*>(static_cast<const char*>(p->d_v) + (size_t)layer * p->layer_bytes);
+    a.pool_v = reinterpret_cast<const float*>(static_cast<const char*>(p->d_v) + (size_t)layer * p->layer_bytes_v);
+    a.tq_signs = p->dtype == DENDRITE_TURBO ? p->d_tq_signs : nullptr;
     a.meta = p->d_meta;
     a.bpb = p->bpb;
     a.n_kv = p->n_kv;
@@ -1586,6 +1606,8 @@ int attn_setup(dendrite_pool* p) {
         DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_bf16, THREADS, SMEM_BF16));
         p->attn_ctas_per_sm = std::max(1, occ);
         p->tc_ready = attn_tc_setup() == DENDRITE_OK;
+    } else if (p->dtype == DENDRITE_TURBO) {
+        p->attn_ctas_per_sm = turbo_ctas_per_sm();
     } else {
         const size_t sm = 2 * BS * p->head_dim * sizeof(float);
         int occ = 0;
@@ -1606,6 +1628,8 @@ void attn_teardown(dendrite_pool* p) {
     }
     if (p->d_partial) cudaFree(p->d_partial);
     p->d_partial = nullptr;
+    if (p->d_tq_qs) cudaFree(p->d_tq_qs);
+    p->d_tq_qs = nullptr;
 }
 
 }  // namespace dendrite
@@ -1754,6 +1778,18 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         pc.stats.refreshed = 0;
         pc.stats.plan_us = 0.0;
     }
+    if (p->dtype == DENDRITE_TURBO) {   // rotated queries and their QJL projections
+        const size_t rows = (size_t)n * q_len * n_q_heads;
+        if (rows > p->tq_qs_rows) {
+            const size_t cap = std::max<size_t>(rows * 3 / 2, 4096);
+            DENDRITE_CUDA(cudaDeviceSynchronize());
+            if (p->d_tq_qs) cudaFree(p->d_tq_qs);
+            p->d_tq_qs = nullptr;
+            p->tq_qs_rows = 0;
+            DENDRITE_CUDA(cudaMalloc(&p->d_tq_qs, cap * 2 * kTurboDim * sizeof(float)));
+            p->tq_qs_rows = cap;
+        }
+    }
     AttnArgs a = attn_args(p, layer, Q, out);
     a.plan = pc.dev;
     a.part_acc = p->d_partial;
@@ -1817,6 +1853,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
                                                  int32_t q_len, const int32_t* branches, int32_t n, void* out,
                                                  void* stream) {
     if (!p) return DENDRITE_EINVAL;
+    if (p->dtype == DENDRITE_TURBO) return DENDRITE_EDTYPE;   // needs the pool's query workspace
     if (p->poisoned) return p->poisoned;
     if (p->pending.active && !p->pending.layer_done[0]) return DENDRITE_EINVAL;
     DENDRITE_CUDA(cudaSetDevice(p->device));

@@ -58,6 +58,7 @@ struct AttnArgs {
     int32_t head_dim;
     int32_t n_blocks;
     float scale_log2;      // log2(e) / sqrt(head_dim)
+    const float* tq_signs; // compressed pools: rotation signs [128] (the merge rotates rows back); else null
 };
 
 // Tensor-core (tcgen05) partial kernel for units of many query rows; see

@@ -233,9 +233,16 @@ struct dendrite_pool {
     int32_t* d_released = nullptr;   // [num_blocks] flags set by free phase A
     int32_t* d_call_i32 = nullptr;   // [4 * max_branches] per-call scratch (offsets, cow sources)
 
-    // layers: layer l's K pool starts at d_k + l * layer_bytes (same for V)
+    // layers: layer l's K pool starts at d_k + l * layer_bytes, its V pool at
+    // d_v + l * layer_bytes_v (the same except for compressed pools)
     int32_t n_layers = 1;
-    size_t layer_bytes = 0;
+    size_t layer_bytes = 0, layer_bytes_v = 0;
+    // compressed pools (DENDRITE_TURBO): rotation signs [128] and QJL matrix
+    // [128][128] on the device; rotated queries and projections of a call
+    float* d_tq_signs = nullptr;
+    float* d_tq_S = nullptr;
+    float* d_tq_qs = nullptr;
+    size_t tq_qs_rows = 0;
 
     // tensor maps of every layer's K and V pool for the bf16 attention
     // kernels (opaque 128-byte blobs)

@@ -25,6 +25,7 @@
 #include <unordered_set>
 
 #include "dendrite_internal.h"
+#include "turbo.h"
 
 using namespace dendrite;
 
@@ -49,10 +50,12 @@ template <int CAP>
 struct ParamArgs {
     int32_t v[CAP];
     __device__ __forceinline__ int32_t operator[](int64_t i) const { return v[i]; }
+    const int32_t* dev_ptr() const { return nullptr; }
 };
 struct GlobalArgs {
     const int32_t* p;
     __device__ __forceinline__ int32_t operator[](int64_t i) const { return p[i]; }
+    const int32_t* dev_ptr() const { return p; }
 };
 
 __global__ void k_init(int32_t* stack, int32_t* refcount, int32_t* holders, int32_t* last,
@@ -779,7 +782,34 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
                                      p->d_stack, p->d_holders, p->d_last, p->d_call_i32, p->d_meta));
             prof_end(p, T_APPEND_META, s);
         }
-        if (copy) {
+        if (copy && p->dtype == DENDRITE_TURBO) {
+            prof_begin(p, T_APPEND_COPY, s);
+            TurboAppend t{};
+            t.args = args.dev_ptr();
+            t.n = n;
+            t.n_new = n_new;
+            t.bs = bs;
+            t.bpb = p->bpb;
+            t.n_kv = p->n_kv;
+            t.n_blocks = (int32_t)p->num_blocks;
+            t.table = p->d_table;
+            t.call = p->d_call_i32;
+            t.K = static_cast<const __nv_bfloat16*>(K);
+            t.V = static_cast<const __nv_bfloat16*>(V);
+            t.kp = static_cast<unsigned char*>(p->d_k) + (size_t)layer0 * p->layer_bytes;
+            t.vp = static_cast<unsigned char*>(p->d_v) + (size_t)layer0 * p->layer_bytes_v;
+            t.in_layer = in_layer * 8;   // 16-byte words -> bf16 elements
+            t.kp_layer = (int64_t)p->layer_bytes;
+            t.vp_layer = (int64_t)p->layer_bytes_v;
+            t.signs = p->d_tq_signs;
+            t.S = p->d_tq_S;
+            t.meta = p->d_meta;
+            t.n_tiles = n_tiles;
+            t.n_layers_in = n_layers_in;
+            t.sm_count = p->sm_count;
+            DENDRITE_TRY(launch_append_turbo(t, s));
+            prof_end(p, T_APPEND_COPY, s);
+        } else if (copy) {
             prof_begin(p, T_APPEND_COPY, s);
             uint4* kp = reinterpret_cast<uint4*>(static_cast<char*>(p->d_k) + (size_t)layer0 * p->layer_bytes);
             uint4* vp = reinterpret_cast<uint4*>(static_cast<char*>(p->d_v) + (size_t)layer0 * p->layer_bytes);
@@ -791,7 +821,8 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
         }
         return DENDRITE_OK;
     };
-    if (3 * n <= CAP) {
+    // compressed pools encode from device-resident arguments
+    if (3 * n <= CAP && !(copy && p->dtype == DENDRITE_TURBO)) {
         ParamArgs<CAP> a;
         fill(a.v);
         return launch(a);
@@ -820,13 +851,22 @@ extern "C" {
 
 const char* dendrite_version(void) { return "dendrite-gb300 0.1.0 (sm_103a)"; }
 
-int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int32_t head_dim,
-                         int32_t dtype, const dendrite_pool_opts* opts, dendrite_pool** out) {
+}  // extern "C"
+
+namespace {
+
+int pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int32_t head_dim, int32_t dtype,
+                const float* tq_signs, const float* tq_S, const dendrite_pool_opts* opts, dendrite_pool** out) {
     if (!out) return DENDRITE_EINVAL;
     *out = nullptr;
     if (num_blocks <= 0 || num_blocks >= INT32_MAX || n_kv_heads < 1 || n_kv_heads > 64) return DENDRITE_EINVAL;
     if (block_size != kBlockSize) return DENDRITE_EDTYPE;
-    if (dtype == DENDRITE_BF16) {
+    if (dtype == DENDRITE_TURBO) {
+        if (head_dim != kTurboDim) return DENDRITE_EDTYPE;
+        if (!tq_signs || !tq_S) return DENDRITE_EINVAL;
+        for (int i = 0; i < kTurboDim; ++i)
+            if (tq_signs[i] != 1.f && tq_signs[i] != -1.f) return DENDRITE_EINVAL;
+    } else if (dtype == DENDRITE_BF16) {
         if (head_dim != 128) return DENDRITE_EDTYPE;
     } else if (dtype == DENDRITE_FP32) {
         if (head_dim <= 0 || head_dim > 256 || head_dim % 32) return DENDRITE_EDTYPE;
@@ -850,7 +890,7 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     p->n_kv = n_kv_heads;
     p->head_dim = head_dim;
     p->dtype = dtype;
-    p->elt = dtype == DENDRITE_BF16 ? 2 : 4;
+    p->elt = dtype == DENDRITE_FP32 ? 4 : 2;   // compressed pools take bf16 rows
     p->max_branches = max_branches;
     p->bpb = bpb;
     if (opts && opts->tc_min_rows) p->tc_min_rows = opts->tc_min_rows;
@@ -863,15 +903,32 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     };
     if (cudaGetDevice(&p->device) != cudaSuccess) return fail(cuda_err(cudaErrorNoDevice));
     cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device);
-    p->layer_bytes = (size_t)num_blocks * n_kv_heads * block_size * head_dim * p->elt;
-    const size_t pool_bytes = p->layer_bytes * p->n_layers;
-    if (cudaMalloc(&p->d_k, pool_bytes) != cudaSuccess || cudaMalloc(&p->d_v, pool_bytes) != cudaSuccess)
+    const size_t slots = (size_t)num_blocks * n_kv_heads * block_size;
+    if (dtype == DENDRITE_TURBO) {
+        p->layer_bytes = slots * kTurboKeyBytes;
+        p->layer_bytes_v = slots * kTurboValueBytes;
+    } else {
+        p->layer_bytes = p->layer_bytes_v = slots * head_dim * p->elt;
+    }
+    const size_t k_bytes = p->layer_bytes * p->n_layers, v_bytes = p->layer_bytes_v * p->n_layers;
+    if (cudaMalloc(&p->d_k, k_bytes) != cudaSuccess || cudaMalloc(&p->d_v, v_bytes) != cudaSuccess)
         return fail(cuda_err(cudaErrorMemoryAllocation));
     // Slots past a branch's length are read by the attention tiles and given
-    // weight zero; they must hold finite values (0 x NaN is NaN).  Zero them
-    // once here; afterwards they only ever hold appended rows.
-    if (cudaMemset(p->d_k, 0, pool_bytes) != cudaSuccess || cudaMemset(p->d_v, 0, pool_bytes) != cudaSuccess)
+    // weight zero; they must hold finite values (0 x NaN is NaN; a zero record
+    // decodes to a zero row).  Zero them once here; afterwards they only ever
+    // hold appended rows.
+    if (cudaMemset(p->d_k, 0, k_bytes) != cudaSuccess || cudaMemset(p->d_v, 0, v_bytes) != cudaSuccess)
         return fail(cuda_err(cudaErrorUnknown));
+    if (dtype == DENDRITE_TURBO) {
+        if (cudaMalloc(&p->d_tq_signs, kTurboDim * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&p->d_tq_S, (size_t)kTurboQjlBits * kTurboDim * sizeof(float)) != cudaSuccess)
+            return fail(cuda_err(cudaErrorMemoryAllocation));
+        if (cudaMemcpy(p->d_tq_signs, tq_signs, kTurboDim * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(p->d_tq_S, tq_S, (size_t)kTurboQjlBits * kTurboDim * sizeof(float),
+                       cudaMemcpyHostToDevice) != cudaSuccess)
+            return fail(cuda_err(cudaErrorUnknown));
+        if ((rc = turbo_setup_tables()) != DENDRITE_OK) return fail(rc);
+    }
     const size_t nb4 = (size_t)num_blocks * 4;
     if (cudaMalloc(&p->d_refcount, nb4) != cudaSuccess || cudaMalloc(&p->d_stack, nb4) != cudaSuccess ||
         cudaMalloc(&p->d_holders, nb4) != cudaSuccess || cudaMalloc(&p->d_last, nb4) != cudaSuccess ||
@@ -900,6 +957,23 @@ int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_he
     return DENDRITE_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int32_t head_dim,
+                         int32_t dtype, const dendrite_pool_opts* opts, dendrite_pool** out) {
+    if (dtype == DENDRITE_TURBO) return DENDRITE_EINVAL;   // needs its codec: dendrite_pool_create_turbo
+    return pool_create(num_blocks, block_size, n_kv_heads, head_dim, dtype, nullptr, nullptr, opts, out);
+}
+
+int dendrite_pool_create_turbo(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int32_t head_dim,
+                               const float* rot_signs, const float* qjl_matrix, const dendrite_pool_opts* opts,
+                               dendrite_pool** out) {
+    return pool_create(num_blocks, block_size, n_kv_heads, head_dim, DENDRITE_TURBO, rot_signs, qjl_matrix, opts,
+                       out);
+}
+
 int dendrite_pool_destroy(dendrite_pool* p) {
     if (!p) return DENDRITE_EINVAL;
     cudaSetDevice(p->device);
@@ -907,7 +981,7 @@ int dendrite_pool_destroy(dendrite_pool* p) {
     attn_teardown(p);
     p->staging.destroy();
     void* bufs[] = {p->d_k, p->d_v, p->d_refcount, p->d_stack, p->d_holders, p->d_last,
-                    p->d_released, p->d_table, p->d_call_i32, p->d_meta};
+                    p->d_released, p->d_table, p->d_call_i32, p->d_meta, p->d_tq_signs, p->d_tq_S};
     for (void* b : bufs)
         if (b) cudaFree(b);
     for (int k = 0; k < T_COUNT; ++k)
@@ -1231,10 +1305,11 @@ int dendrite_read_block_layer(dendrite_pool* p, int32_t layer, int32_t block, vo
     if (layer < 0 || layer >= p->n_layers) return DENDRITE_EINVAL;
     DENDRITE_CUDA(cudaSetDevice(p->device));
     DENDRITE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
-    const size_t bytes = (size_t)p->n_kv * p->block_size * p->head_dim * p->elt;
-    const size_t off = (size_t)layer * p->layer_bytes + bytes * block;
-    DENDRITE_CUDA(cudaMemcpy(k_out, (char*)p->d_k + off, bytes, cudaMemcpyDeviceToHost));
-    DENDRITE_CUDA(cudaMemcpy(v_out, (char*)p->d_v + off, bytes, cudaMemcpyDeviceToHost));
+    const size_t kb = p->layer_bytes / p->num_blocks, vb = p->layer_bytes_v / p->num_blocks;   // per block
+    DENDRITE_CUDA(cudaMemcpy(k_out, (char*)p->d_k + (size_t)layer * p->layer_bytes + kb * block, kb,
+                             cudaMemcpyDeviceToHost));
+    DENDRITE_CUDA(cudaMemcpy(v_out, (char*)p->d_v + (size_t)layer * p->layer_bytes_v + vb * block, vb,
+                             cudaMemcpyDeviceToHost));
     return DENDRITE_OK;
 }
 

@@ -25,7 +25,8 @@ ERRORS = {
 }
 TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total",
                 "attn_tc")
-FP32, BF16 = 0, 1
+FP32, BF16, TURBO = 0, 1, 2
+TURBO_KEY_BYTES, TURBO_VALUE_BYTES = 96, 64
 
 _LIB = None
 _i32 = ctypes.c_int32
@@ -59,6 +60,7 @@ class _Segment(ctypes.Structure):
 
 _SIGS = {
     "dendrite_pool_create": [_i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_Opts), ctypes.POINTER(_p)],
+    "dendrite_pool_create_turbo": [_i64, _i32, _i32, _i32, _p, _p, ctypes.POINTER(_Opts), ctypes.POINTER(_p)],
     "dendrite_pool_destroy": [_p],
     "dendrite_branch_new": [_p, _pi32],
     "dendrite_fork": [_p, _i32, _i32, _pi32, _p],
@@ -149,8 +151,11 @@ class Pool:
     def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
                  dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
                  max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0, n_layers: int = 1,
-                 fold_segments: int = 0):
-        if dtype not in _DT:
+                 fold_segments: int = 0, turbo=None):
+        """``turbo``: (rotation signs [128], QJL matrix [128][128]) to store
+        compressed blocks (dendrite_pool_create_turbo); the calls then take
+        bf16 tensors."""
+        if dtype not in _DT or (turbo is not None and dtype != torch.bfloat16):
             raise DendriteError(-5, f"dtype {dtype}")
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
                                    torch.device(device).index or 0)
@@ -159,10 +164,20 @@ class Pool:
         opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows), int(n_layers),
                      int(fold_segments))
         self.n_layers = int(n_layers)
+        self.turbo = turbo is not None
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
-            _check(lib().dendrite_pool_create(self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim,
-                                              _DT[dtype], ctypes.byref(opts), ctypes.byref(h)), "pool_create")
+            if self.turbo:
+                signs = torch.as_tensor(turbo[0], dtype=torch.float32).contiguous().cpu()
+                S = torch.as_tensor(turbo[1], dtype=torch.float32).contiguous().cpu()
+                if signs.numel() != self.head_dim or S.shape != (128, self.head_dim):
+                    raise DendriteError(-1, "turbo codec shapes")
+                _check(lib().dendrite_pool_create_turbo(self.num_blocks, self.block_size, self.n_kv_heads,
+                                                        self.head_dim, signs.data_ptr(), S.data_ptr(),
+                                                        ctypes.byref(opts), ctypes.byref(h)), "pool_create_turbo")
+            else:
+                _check(lib().dendrite_pool_create(self.num_blocks, self.block_size, self.n_kv_heads, self.head_dim,
+                                                  _DT[dtype], ctypes.byref(opts), ctypes.byref(h)), "pool_create")
         self._h = h
         self._dev = self.device.index
 
@@ -327,9 +342,16 @@ class Pool:
         return list(buf[:top.value])
 
     def read_block(self, blk: int, stream=None, layer: int = 0):
-        shape = (self.n_kv_heads, self.block_size, self.head_dim)
-        k = torch.empty(shape, dtype=self.dtype)
-        v = torch.empty(shape, dtype=self.dtype)
+        """K and V of a block: [n_kv_heads][block_size][head_dim] in the pool
+        dtype, or the raw records ([...][96] and [...][64] uint8) of a
+        compressed pool."""
+        if self.turbo:
+            k = torch.empty((self.n_kv_heads, self.block_size, TURBO_KEY_BYTES), dtype=torch.uint8)
+            v = torch.empty((self.n_kv_heads, self.block_size, TURBO_VALUE_BYTES), dtype=torch.uint8)
+        else:
+            shape = (self.n_kv_heads, self.block_size, self.head_dim)
+            k = torch.empty(shape, dtype=self.dtype)
+            v = torch.empty(shape, dtype=self.dtype)
         _check(lib().dendrite_read_block_layer(self._h, int(layer), int(blk), k.data_ptr(), v.data_ptr(),
                                                _stream_ptr(stream, self._dev)), "read_block")
         return k, v

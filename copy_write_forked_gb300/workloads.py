@@ -29,7 +29,7 @@ import torch
 __all__ = [
     "Op", "Workload", "seed_of",
     "tiny_cow", "beam", "mcts", "spec_verify", "fork_stress_attention",
-    "fork_chain_script", "random_script",
+    "fork_chain_script", "random_script", "turbo_codec",
 ]
 
 
@@ -407,3 +407,13 @@ def random_script(rng_seed: int, n_ops: int = 40, max_live: int = 8, max_append:
             ln[b] += q_len
     return Workload(f"random_{rng_seed}", n_kv, n_q, d, bs, dtype, ops, tuple(sorted(live)),
                     q_len, seed)
+
+
+def turbo_codec(seed: int = 0, head_dim: int = 128, qjl_rows: int = 128):
+    """The random draws of a compressed pool's codec, seeded: rotation signs
+    (float32 [head_dim], each +1 or -1) and the QJL matrix (float32
+    [qjl_rows][head_dim], i.i.d. N(0, 1))."""
+    g = torch.Generator().manual_seed(seed_of(seed, "turbo"))
+    signs = (torch.randint(0, 2, (head_dim,), generator=g) * 2 - 1).to(torch.float32)
+    S = torch.randn((qjl_rows, head_dim), generator=g, dtype=torch.float32)
+    return signs, S

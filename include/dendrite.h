@@ -65,6 +65,8 @@ extern "C" {
 /* ------------------------------------------------------------------ dtypes */
 #define DENDRITE_FP32  0   /* fp32 K/V/Q/out; attention in fp32 FMA (no TF32)          */
 #define DENDRITE_BF16  1   /* bf16 K/V/Q/out; attention on tensor cores, fp32 accumulate */
+#define DENDRITE_TURBO 2   /* compressed blocks (dendrite_pool_create_turbo): bf16 K/V/Q/out
+                            * in the calls, TurboQuant records in the pool               */
 
 typedef struct dendrite_pool dendrite_pool;
 
@@ -105,6 +107,42 @@ typedef struct dendrite_pool_opts {
 int dendrite_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads,
                          int32_t head_dim, int32_t dtype, const dendrite_pool_opts* opts,
                          dendrite_pool** out);
+
+/*
+ * A pool whose blocks hold compressed rows (dendrite demo.tape, section
+ * "TurboQuant": "TurboQuant KV compression (PolarQuant + QJL)"; the pages
+ * name the methods and give a 3.05x ratio at head_dim 128, not the
+ * algorithm, so the steps follow the published PolarQuant, QJL and
+ * TurboQuant methods):
+ *   - every K and V row r (head_dim 128) is rotated, x = H (s * r) / sqrt(128),
+ *     H the Walsh-Hadamard matrix and s = rot_signs (host float[128], each
+ *     +1 or -1);
+ *   - the recursive polar transform of x is stored as its norm (fp32), 64
+ *     level-1 angle codes of 4 bits (16 equal bins of [0, 2 pi)) and 63 codes
+ *     of 3 bits for the angles of levels 2..7 (8 equal bins of
+ *     [pi/4 - w, pi/4 + w], w = min(pi/4, 1.6 / sqrt(k - 1)) for halves of
+ *     k = 2^(level - 1) coordinates);
+ *   - a key row also stores sign(S e) (128 bits) and |e| (fp32) for its
+ *     residual e = x - x_hat, S = qjl_matrix (host float[128][128], row-major,
+ *     normally i.i.d. N(0, 1)), and attention scores it as
+ *     <q', x_hat> + sqrt(pi/2)/128 |e| <S q', sign(S e)> with q' the rotated
+ *     query.
+ * Records: a value row is 64 bytes (norm; 32 bytes of 4-bit codes, code i in
+ * byte 4 + i/2, low nibble for even i; 24 bytes holding the 3-bit codes of
+ * levels 2..7 in level order, code i at bit 3 i of a little-endian stream;
+ * 4 zero bytes); a key row is 96 bytes (the value layout, then the 128 sign
+ * bits, bit j in byte 64 + j/8 at bit j % 8, then |e|, then 12 zero bytes).
+ * K + V take 160 bytes per token and head instead of 512 in bf16 (3.2x).
+ * The encoder takes its bin and sign decisions in fp32, one rounded operation
+ * at a time in a fixed order, so records depend only on the input bits.
+ * K and V of dendrite_append_kv / _append_layer, and Q and out of the
+ * attention calls, are bf16; dendrite_read_block returns the raw records
+ * ([n_kv_heads][block_size][96] and [...][64] bytes).  head_dim must be 128;
+ * other arguments and errors as dendrite_pool_create (dtype DENDRITE_TURBO).
+ */
+int dendrite_pool_create_turbo(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int32_t head_dim,
+                               const float* rot_signs, const float* qjl_matrix, const dendrite_pool_opts* opts,
+                               dendrite_pool** out);
 
 /* Synchronises the device, then releases everything the pool owns. */
 int dendrite_pool_destroy(dendrite_pool* pool);
@@ -255,8 +293,9 @@ int dendrite_read_refcounts(dendrite_pool* pool, int32_t* out, void* stream);
  * out[num_blocks]; *top_out receives its size. */
 int dendrite_read_free_stack(dendrite_pool* pool, int32_t* out, int32_t* top_out, void* stream);
 
-/* Copy one block's K and V ([n_kv_heads][block_size][head_dim], pool dtype)
- * to host buffers k_out / v_out (layer 0; dendrite_read_block_layer for any). */
+/* Copy one block's K and V ([n_kv_heads][block_size][head_dim], pool dtype;
+ * the records for DENDRITE_TURBO pools) to host buffers k_out / v_out
+ * (layer 0; dendrite_read_block_layer for any). */
 int dendrite_read_block(dendrite_pool* pool, int32_t block, void* k_out, void* v_out, void* stream);
 int dendrite_read_block_layer(dendrite_pool* pool, int32_t layer, int32_t block, void* k_out, void* v_out,
                               void* stream);
@@ -398,6 +437,7 @@ int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* parent, const 
  *   - A call whose plan plus partial rows exceed the array returns
  *     DENDRITE_ELIMIT and launches nothing (roughly: more than ~30,000 partial
  *     rows of head_dim 128).
+ *   - Pools of compressed blocks (DENDRITE_TURBO) return DENDRITE_EDTYPE.
  *   - Nothing in the array needs to start at zero: each call writes the plan
  *     and every partial row before reading them.
  *   - All calls share the one device array per device and it keeps the last
