@@ -265,7 +265,7 @@ def run_ours(args):
     from copy_write_forked_gb300 import workloads as W
     pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R + 2 * nl + 16,
                 max_blocks_per_branch=(P + Dv + grow) // bs + 8,
-                turbo=W.turbo_codec(rank) if args.turbo else None)
+                turbo=W.turbo_codec(rank) if args.turbo else None, device_planning=args.device_planning)
     # prefill (untimed): the prefixes, resident in HBM
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
@@ -535,7 +535,9 @@ def run_ours(args):
         "value": value, "unit": "branch-queries/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
-        "config": dict(cfg, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "config": dict(cfg, parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       planning={-1: "host", 0: "units and CTA split on the device from 2048 units",
+                                 1: "units and CTA split on the device"}[args.device_planning]),
         "roofline": roofline,
         "roofline_attention": attn_roof,
         "cpu_baseline": cpu,
@@ -578,7 +580,7 @@ def run_decode_layers(args):
     nq, nkv, d, bs = w.n_q_heads, w.n_kv_heads, w.head_dim, w.block_size
     nblocks = R * (P // bs + 1) + R * Wd * (Dv // bs + 2) + 64
     pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R * (Wd + 1) + 8,
-                max_blocks_per_branch=(P + Dv) // bs + 8, n_layers=NL)
+                max_blocks_per_branch=(P + Dv) // bs + 8, n_layers=NL, device_planning=args.device_planning)
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
     div_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == Dv)
@@ -675,7 +677,8 @@ def run_attention_only(args):
     from copy_write_forked_gb300.runner import pool_for, run_script
     w, desc = other_workload(args.workload)
     pool = pool_for(w, extra_blocks=len(w.query) + 16, tc_min_rows=args.tc_min_rows,
-                    fold_segments=args.fold_segments)   # room for one more token per queried branch
+                    fold_segments=args.fold_segments,   # room for one more token per queried branch
+                    device_planning=args.device_planning)
     h = run_script(pool, w, device=dev)
     br = [h[b] for b in w.query]
     Q = w.q(dev)
@@ -762,7 +765,7 @@ def run_mcts_loop(args):
     from copy_write_forked_gb300 import workloads as W
     from copy_write_forked_gb300.runner import pool_for
     w = W.mcts(iters=args.mcts_iters)
-    pool = pool_for(w, fold_segments=args.fold_segments)
+    pool = pool_for(w, fold_segments=args.fold_segments, device_planning=args.device_planning)
     gen = torch.Generator(device=dev).manual_seed(77)
     maxq = len(w.query)
     Qall = torch.randn((maxq, 1, w.n_q_heads, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
@@ -1144,6 +1147,9 @@ def main():
                     help="full-path workloads: fewer requests than the configuration (a smaller case for ncu)")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
+    ap.add_argument("--device-planning", type=int, default=0, choices=[-1, 0, 1],
+                    help="bf16 attention plans: expand units and the CTA split on the device (1), on the host (-1), "
+                         "or on the device from 2048 units up (0, default)")
     ap.add_argument("--fold-segments", type=int, default=0,
                     help="fold short shared segments into the ones that follow (0: default, k: below k percent "
                          "of the estimate, -1: off)")

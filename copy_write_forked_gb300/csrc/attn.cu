@@ -381,6 +381,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     // this CTA's share of the plan is loaded together with the status word
     const AttnPlanDev& pl = a.plan;
     const int c = blockIdx.x;
+    if (pl.counts && c >= pl.counts[0]) return;   // past the split expanded on the device
     const int32_t t_begin = pl.cta_begin[c], t_end = pl.cta_begin[c + 1];
     const int32_t u0 = pl.cta_unit[c];
     if (threadIdx.x == 0) {
@@ -1074,6 +1075,285 @@ __global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a)
     }
 }
 
+// ============================================================ host planning
+// A segment as the unit expansion reads it (host or device): its units are
+// unit_base + kv head * ngroups + row group, its tiles (class numbering)
+// tile_base + that local unit index * n_blk, and the weight of the class's
+// units before it wbase.  Row groups 0 .. ngroups - 2 hold group_rows rows,
+// the last one rows_last.
+struct SegPlan {
+    int64_t wbase;                 // the three search keys first: one 16-byte load
+    int32_t tile_base, unit_base;
+    int32_t ngroups, group_rows, rows_last, n_blk;
+    int32_t rt_full, rt_last, table_row, blk_start;
+    int32_t mem_off;
+    int32_t row_base;         // rows of all units before this segment's (tensor-core class first)
+    int32_t w_full, w_last;   // weight of one unit of a full row group / of the last one
+};
+static_assert(sizeof(SegPlan) == 64, "SegPlan layout");
+
+// A class of units (0: tcgen05, 1: mma.sync / fp32) for the CTA split.
+struct PlanClass {
+    int64_t weight;             // total weight of its units
+    int32_t tiles;              // its tiles
+    int32_t c0;                 // CTAs the split aims at (cuts are made at c0 - 1 targets)
+    int32_t u_lo, u_hi;         // its units
+    int32_t s_lo, s_hi;         // its segments in the SegPlan list
+    int32_t unit_start, row_shift;   // the class's unit-start weight terms
+};
+struct PlanHeader {
+    PlanClass cls[2];
+    int32_t n_units, n_segs, n_rows, pad;   // n_rows: rows of all units (one chunk each)
+};
+
+
+// ====================================================== device plan expansion
+// Expands a plan's segment list (SegPlan, class-relative offsets) into its
+// work units and splits each class's tiles over CTAs on the device, writing
+// exactly what the host expansion writes (build_units, partition_class):
+//   - for c = 1 .. c0 - 1, the weight target ceil(weight c / c0) falls in one
+//     unit, which starts at weight w after start weight us and has tiles of
+//     weight tw; the cut candidate is its first tile plus
+//     min(n_blk, max(0, ceil((target - w - us) / tw))).  Candidates do not
+//     decrease with c, so the host's rule (keep a candidate above the last
+//     kept cut and below the class's tiles) keeps exactly the candidates
+//     that exceed their predecessor (0 for the first) and lie below the
+//     tiles; a scan over those flags places them;
+//   - each CTA's first unit, each unit's first CTA and number of chunks;
+//   - each unit's first partial row.  Over the units before u, a unit holds
+//     one chunk of its rows plus one more per CTA boundary inside it, so
+//     prow_base(u) = (rows of the units before u) + (rows of the unit each
+//     interior boundary before u falls in); the first term is the segment's
+//     row base plus the rows before u in its segment, the second a prefix
+//     over the (at most kMaxExpandCtas) boundaries of each class.
+// Every CTA computes the splits (a few binary searches per thread) and then
+// expands its own kExpandUnits units, so no step needs a grid-wide scan.  The
+// searches run over the segments' keys (weight, first tile, first unit),
+// which each CTA first copies to shared memory: kMaxExpandSegs segments at
+// most (the host checks).
+constexpr int kMaxExpandCtas = 1024;
+constexpr int kMaxExpandSegs = 8192;
+constexpr int kExpandThreads = 256;
+constexpr int kExpandUnits = 256;   // units per expansion CTA
+
+struct ExpandArgs {
+    const SegPlan* sp;
+    const PlanHeader* hdr;
+    AttnUnit* units;
+    int32_t* begin;      // mma.sync class CTA split [c0 + 1]
+    int32_t* cunit;      // [c0]
+    int32_t* tc_begin;
+    int32_t* tc_cunit;
+    int32_t* counts;     // [4]: CTAs of each class, partial rows (low, high)
+    const DevMeta* meta;
+    int32_t nkv;
+};
+
+// The segment of class [s_lo, s_hi) whose key range holds x: the last one
+// with key(s) <= x (key nondecreasing in s).
+template <typename F>
+__device__ __forceinline__ int32_t seg_search(int32_t s_lo, int32_t s_hi, F key, int64_t x) {
+    int32_t lo = s_lo, hi = s_hi - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (key(mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Exclusive scan of one int per thread over the CTA (kExpandThreads threads);
+// returns the thread's prefix and leaves the total in *total.
+__device__ __forceinline__ int32_t expand_scan(int32_t v, int32_t* warp_tot, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    int32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kExpandThreads / 32; ++w) {
+        const int32_t t = warp_tot[w];
+        before += w < warp ? t : 0;
+        all += t;
+    }
+    __syncthreads();   // warp_tot is reused by the next scan
+    *total = all;
+    return before + inc - v;
+}
+
+__global__ void __launch_bounds__(kExpandThreads) k_plan_expand(const ExpandArgs x) {
+    constexpr int PER = kMaxExpandCtas / kExpandThreads;   // candidates per thread
+    __shared__ int32_t s_cand[kMaxExpandCtas];
+    __shared__ int32_t s_begin[2][kMaxExpandCtas + 1];
+    __shared__ int32_t s_pre[2][kMaxExpandCtas + 1];   // rows of the interior boundaries 1..i
+    __shared__ int32_t s_nc[2];
+    __shared__ int32_t s_warp[kExpandThreads / 32];
+    extern __shared__ int64_t s_keys[];                 // wbase[n_segs], then tile_base, unit_base
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
+    const int tid = threadIdx.x;
+    if (x.meta->status) return;
+    const PlanHeader hdr = *x.hdr;
+    const SegPlan* sp = x.sp;
+    const int32_t nkv = x.nkv;
+    const int32_t n_segs = hdr.n_segs;
+    int64_t* s_wb = s_keys;
+    int32_t* s_tb = reinterpret_cast<int32_t*>(s_keys + n_segs);
+    int32_t* s_ub = s_tb + n_segs;
+    for (int32_t i = tid; i < n_segs; i += kExpandThreads) {
+        const int4 k = *reinterpret_cast<const int4*>(sp + i);
+        s_wb[i] = (int64_t)(((uint64_t)(uint32_t)k.y << 32) | (uint32_t)k.x);
+        s_tb[i] = k.z;
+        s_ub[i] = k.w;
+    }
+    __syncthreads();
+    // ------------------------------------------------------------ CTA splits
+    for (int cls = 0; cls < 2; ++cls) {
+        const PlanClass pc = hdr.cls[cls];
+        for (int32_t c = 1 + tid; c < pc.c0; c += kExpandThreads) {
+            const int64_t target = (pc.weight * c + pc.c0 - 1) / pc.c0;
+            int32_t cut = pc.tiles;   // no unit holds the target: never kept
+            if (target < pc.weight) {
+                const int32_t si = seg_search(pc.s_lo, pc.s_hi, [&](int32_t k) { return s_wb[k]; }, target);
+                const SegPlan g = sp[si];
+                const int64_t w_head = (int64_t)(g.ngroups - 1) * g.w_full + g.w_last;
+                const int64_t r = target - g.wbase;
+                const int32_t h = (int32_t)min(r / w_head, (int64_t)(nkv - 1));
+                const int64_t r2 = r - h * w_head;
+                const int32_t grp = r2 < (int64_t)(g.ngroups - 1) * g.w_full ? (int32_t)(r2 / g.w_full) : g.ngroups - 1;
+                const int64_t w = g.wbase + h * w_head + (int64_t)grp * g.w_full;
+                const bool last = grp == g.ngroups - 1;
+                const int32_t rows = last ? g.rows_last : g.group_rows;
+                const int64_t us = pc.unit_start + (pc.row_shift >= 0 ? (rows >> pc.row_shift) : 0);
+                const int64_t tw = 1 + (last ? g.rt_last : g.rt_full);
+                const int64_t k = max((int64_t)0, (target - w - us + tw - 1) / tw);
+                cut = g.tile_base + (h * g.ngroups + grp) * g.n_blk + (int32_t)min(k, (int64_t)g.n_blk);
+            }
+            s_cand[c] = cut;
+        }
+        __syncthreads();
+        // keep flags of this thread's run of candidates c = 1 + PER tid ...
+        int32_t keep = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int32_t c = 1 + PER * tid + i;
+            if (c < pc.c0) {
+                const int32_t cut = s_cand[c], prev = c > 1 ? s_cand[c - 1] : 0;
+                keep |= (cut > prev && cut < pc.tiles) << i;
+            }
+        }
+        int32_t n_kept = 0;
+        int32_t pos = 1 + expand_scan(__popc(keep), s_warp, &n_kept);
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if (keep >> i & 1) s_begin[cls][pos++] = s_cand[1 + PER * tid + i];
+        if (tid == 0) {
+            s_begin[cls][0] = 0;
+            s_begin[cls][n_kept + 1] = pc.tiles;
+            s_nc[cls] = pc.c0 > 0 ? n_kept + 1 : 0;
+        }
+        __syncthreads();
+        // rows of the unit each interior boundary falls in (0 at a unit start)
+        const int32_t C = s_nc[cls];
+        int32_t run = 0;
+        int32_t rows_at[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int32_t b_i = 1 + PER * tid + i;   // boundary index 1 .. C - 1
+            rows_at[i] = 0;
+            if (b_i < C) {
+                const int32_t b = s_begin[cls][b_i];
+                const int32_t si = seg_search(pc.s_lo, pc.s_hi, [&](int32_t k) { return (int64_t)s_tb[k]; }, b);
+                const SegPlan g = sp[si];
+                const int32_t k = (b - g.tile_base) / g.n_blk;
+                const bool interior = b - g.tile_base != k * g.n_blk;
+                const bool last = k % g.ngroups == g.ngroups - 1;
+                rows_at[i] = interior ? (last ? g.rows_last : g.group_rows) : 0;
+            }
+            run += rows_at[i];
+        }
+        int32_t tot = 0;
+        int32_t acc = expand_scan(run, s_warp, &tot);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int32_t b_i = 1 + PER * tid + i;
+            acc += rows_at[i];
+            if (b_i < C) s_pre[cls][b_i] = acc;
+        }
+        if (tid == 0) {
+            s_pre[cls][0] = 0;
+            s_pre[cls][kMaxExpandCtas] = tot;   // all interior boundaries of the class
+        }
+        __syncthreads();
+    }
+    // ----------------------------------------- CTA arrays and counts (CTA 0)
+    if (blockIdx.x == 0) {
+        for (int cls = 0; cls < 2; ++cls) {
+            const PlanClass pc = hdr.cls[cls];
+            const int32_t C = s_nc[cls];
+            int32_t* bg = cls == 0 ? x.tc_begin : x.begin;
+            int32_t* cu = cls == 0 ? x.tc_cunit : x.cunit;
+            for (int32_t c = tid; c <= C && C > 0; c += kExpandThreads) bg[c] = s_begin[cls][c];
+            if (C == 0 && tid == 0) bg[0] = 0;   // an empty class still has begin[0]
+            for (int32_t c = tid; c < C; c += kExpandThreads) {
+                const int32_t b = s_begin[cls][c];
+                const int32_t si = seg_search(pc.s_lo, pc.s_hi, [&](int32_t k) { return (int64_t)s_tb[k]; }, b);
+                const SegPlan g = sp[si];
+                cu[c] = g.unit_base + (b - g.tile_base) / g.n_blk;
+            }
+        }
+        if (tid == 0) {
+            const int64_t rows = (int64_t)hdr.n_rows + s_pre[0][kMaxExpandCtas] + s_pre[1][kMaxExpandCtas];
+            x.counts[0] = s_nc[1];
+            x.counts[1] = s_nc[0];
+            x.counts[2] = (int32_t)(rows & 0xffffffff);
+            x.counts[3] = (int32_t)(rows >> 32);
+        }
+    }
+    // ------------------------------------------------------ this CTA's units
+    const int32_t u = blockIdx.x * kExpandUnits + tid;
+    if (u >= hdr.n_units) return;
+    const int cls = u < hdr.cls[0].u_hi ? 0 : 1;
+    const PlanClass& pc = hdr.cls[cls];
+    const int32_t si = seg_search(pc.s_lo, pc.s_hi, [&](int32_t k) { return (int64_t)s_ub[k]; }, u);
+    const SegPlan g = sp[si];
+    const int32_t k = u - g.unit_base;
+    const int32_t h = k / g.ngroups, grp = k - h * g.ngroups;
+    const bool last = grp == g.ngroups - 1;
+    AttnUnit U;
+    U.seg = si;
+    U.kv_head = h;
+    U.row_lo = grp * g.group_rows;
+    U.n_rows = last ? g.rows_last : g.group_rows;
+    U.rt = last ? g.rt_last : g.rt_full;
+    U.tile_off = g.tile_base + k * g.n_blk;
+    // first CTA: begin[c] <= tile_off < begin[c + 1]; last CTA likewise for the last tile
+    const int32_t C = s_nc[cls];
+    auto cta_of = [&](int32_t t) {
+        int32_t lo = 0, hi = C - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (s_begin[cls][mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+    U.cfirst = cta_of(U.tile_off);
+    U.nchunks = cta_of(U.tile_off + g.n_blk - 1) - U.cfirst + 1;
+    const int32_t rows_per_head = (g.ngroups - 1) * g.group_rows + g.rows_last;
+    U.prow_base = g.row_base + h * rows_per_head + grp * g.group_rows + s_pre[cls][U.cfirst] +
+                  (cls == 1 ? s_pre[0][kMaxExpandCtas] : 0);
+    U.table_row = g.table_row;
+    U.blk_start = g.blk_start;
+    U.n_blk = g.n_blk;
+    U.mem_off = g.mem_off;
+    U.pad[0] = U.pad[1] = U.pad[2] = 0;
+    x.units[u] = U;
+}
+
 // ============================================================ plan upload
 // Copies the plan from the pool's pinned host buffer (device-accessible) to
 // one of its two device copies.  A kernel rather than cudaMemcpyAsync: the
@@ -1107,9 +1387,12 @@ struct HostPlan {
     size_t partial_rows = 0;
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
+    std::vector<SegPlan> segplan;
+    PlanHeader hdr{};
+    bool device = false;       // units and CTA split left to the device
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes; the unit and
                      // member arrays keep their size too (build_plan resizes and fills them in place)
-        segs.clear(); cta_begin.clear(); cta_unit.clear();
+        segs.clear(); cta_begin.clear(); cta_unit.clear(); segplan.clear(); device = false;
         tc_cta_begin.clear(); tc_cta_unit.clear(); path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         n_tc_units = 0;
@@ -1203,13 +1486,13 @@ void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_
 }
 
 int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
-                int max_tc_ctas, HostPlan& hp);
+                int max_tc_ctas, HostPlan& hp, bool allow_device);
 
 // max_ctas: CTAs of the mma.sync/fp32 kernel; max_tc_ctas: of the tcgen05
 // kernel (0 when it is not used).  The segments (after folding) are left in
 // hp.psegs / hp.seg_members.
 int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
-               int max_tc_ctas, HostPlan& hp) {
+               int max_tc_ctas, HostPlan& hp, bool allow_device) {
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
     const int32_t RM = q_len * G;
     const bool bf16 = p->dtype == DENDRITE_BF16;
@@ -1235,14 +1518,26 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
         fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, n_nodes,
                       hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
                       hp.psegs, hp.seg_members);
-    return build_units(p, branches, n, q_len, nq, max_ctas, max_tc_ctas, hp);
+    return build_units(p, branches, n, q_len, nq, max_ctas, max_tc_ctas, hp, allow_device);
 }
+
+// Number of CTAs a class's split aims at: one per min_per_cta of weight, at
+// most max_ctas, at least one.
+int32_t class_ctas(int64_t weight, int max_ctas, const ClassWeights& cw) {
+    return (int32_t)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + cw.min_per_cta - 1) / cw.min_per_cta));
+}
+
+// bf16 plans of at least this many units are expanded on the device by default
+constexpr int32_t kDevicePlanMinUnits = 2048;
 
 // The plan's units, CTA partitions, partial rows and paths from the segments
 // in hp.psegs / hp.seg_members (hp.tiles and the arrays are rebuilt;
-// hp.unique_tiles is left as it is).
+// hp.unique_tiles is left as it is).  With allow_device and the pool's
+// device_planning setting, a bf16 plan leaves the units and CTA split to
+// k_plan_expand (hp.device): the host then fills the segment list (SegPlan)
+// that kernel reads, and space for what it writes.
 int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
-                int max_tc_ctas, HostPlan& hp) {
+                int max_tc_ctas, HostPlan& hp, bool allow_device) {
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
     const int32_t RM = q_len * G;
     const bool bf16 = p->dtype == DENDRITE_BF16;
@@ -1250,8 +1545,7 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
     const bool tc_on = bf16 && max_tc_ctas > 0 && p->tc_min_rows >= 0;
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by
-    // more than tc_min_rows rows per kv head, pass 1 the rest.  The unit and
-    // member arrays are sized first and filled in place.
+    // more than tc_min_rows rows per kv head, pass 1 the rest.
     size_t n_units_total = 0, n_members_total = 0;
     for (const Segment& sg : hp.psegs) {
         if ((int64_t)sg.n_members * RM >= (int64_t)1 << 24) return DENDRITE_ELIMIT;   // rows as exact fp32
@@ -1261,22 +1555,30 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
         n_members_total += sg.n_members;
     }
     if (n_units_total >= (size_t)INT32_MAX / 2) return DENDRITE_ELIMIT;
+    hp.device = allow_device && bf16 && max_ctas <= kMaxExpandCtas && max_tc_ctas <= kMaxExpandCtas &&
+                hp.psegs.size() <= (size_t)kMaxExpandSegs &&
+                (p->device_planning > 0 || (p->device_planning == 0 && n_units_total >= (size_t)kDevicePlanMinUnits));
     hp.units.resize(n_units_total);
     hp.members.resize(n_members_total);
     hp.segs.reserve(hp.psegs.size());
-    AttnUnit* up = hp.units.data();
+    hp.segplan.reserve(hp.psegs.size());
     AttnMember* mp = hp.members.data();
     int32_t n_mem = 0, n_unit = 0;
     int64_t n_rows = 0;
-    int64_t weight[2] = {0, 0}, class_tiles[2] = {0, 0};
     for (int pass = 0; pass < 2; ++pass) {
-        int64_t tile_off = 0;
+        PlanClass& pc = hp.hdr.cls[pass];
+        const ClassWeights& cwt = pass == 0 ? kTcWeights : kSmallWeights;
+        pc = PlanClass{};
+        pc.u_lo = n_unit;
+        pc.s_lo = (int32_t)hp.segplan.size();
+        pc.unit_start = (int32_t)cwt.unit_start;
+        pc.row_shift = cwt.row_shift;
+        int64_t tile_off = 0, weight = 0;
         for (const Segment& sg : hp.psegs) {
             const int32_t rows_per_head = sg.n_members * RM;
             const bool tc = tc_on && rows_per_head > p->tc_min_rows;
             if (tc != (pass == 0)) continue;
             const int32_t group_rows = tc ? kMaxUnitRowsTc : small_rows;
-            const ClassWeights& cwt = tc ? kTcWeights : kSmallWeights;
             AttnSeg S;
             S.table_row = p->nodes[sg.rep_node].handle;
             S.blk_start = sg.block_start;
@@ -1290,47 +1592,91 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
                 const int32_t qi = hp.seg_members[sg.member_offset + k];
                 mp[n_mem++] = AttnMember{qi, p->br[branches[qi]].len};
             }
-            const int32_t seg_index = (int32_t)hp.segs.size();
-            for (int32_t h = 0; h < nkv; ++h) {
-                for (int32_t grp = 0; grp < S.ngroups; ++grp) {
-                    AttnUnit& U = up[n_unit++];
-                    U.seg = seg_index;
-                    U.kv_head = h;
-                    U.row_lo = grp * group_rows;
-                    U.n_rows = std::min(group_rows, rows_per_head - U.row_lo);
-                    U.rt = tc ? (U.n_rows + 127) / 128 : U.n_rows <= 16 ? 1 : U.n_rows <= 32 ? 2 : 4;
-                    U.tile_off = (int32_t)tile_off;
-                    U.cfirst = U.nchunks = U.prow_base = 0;
-                    U.table_row = S.table_row;
-                    U.blk_start = S.blk_start;
-                    U.n_blk = S.n_blk;
-                    U.mem_off = S.mem_off;
-                    U.pad[0] = U.pad[1] = U.pad[2] = 0;
-                    n_rows += U.n_rows;
-                    tile_off += S.n_blk;
-                    weight[pass] += start_weight(cwt, U.n_rows) + (int64_t)S.n_blk * tile_weight(U.rt);
-                }
-            }
+            auto rt_of = [&](int32_t rows) { return tc ? (rows + 127) / 128 : rows <= 16 ? 1 : rows <= 32 ? 2 : 4; };
+            SegPlan sp;
+            sp.unit_base = S.unit_base;
+            sp.ngroups = S.ngroups;
+            sp.group_rows = group_rows;
+            sp.rows_last = rows_per_head - (S.ngroups - 1) * group_rows;
+            sp.n_blk = S.n_blk;
+            sp.tile_base = (int32_t)tile_off;
+            sp.rt_full = rt_of(group_rows);
+            sp.rt_last = rt_of(sp.rows_last);
+            sp.table_row = S.table_row;
+            sp.blk_start = S.blk_start;
+            sp.mem_off = S.mem_off;
+            sp.row_base = (int32_t)n_rows;
+            sp.wbase = weight;
+            sp.w_full = (int32_t)(start_weight(cwt, group_rows) + (int64_t)S.n_blk * tile_weight(sp.rt_full));
+            sp.w_last = (int32_t)(start_weight(cwt, sp.rows_last) + (int64_t)S.n_blk * tile_weight(sp.rt_last));
+            hp.segplan.push_back(sp);
+            const int64_t units = (int64_t)nkv * S.ngroups;
+            n_unit += (int32_t)units;
+            n_rows += (int64_t)nkv * rows_per_head;
+            tile_off += units * S.n_blk;
+            weight += (int64_t)nkv * ((int64_t)(S.ngroups - 1) * sp.w_full + sp.w_last);
             hp.segs.push_back(S);
         }
-        class_tiles[pass] = tile_off;
         if (tile_off >= INT32_MAX / 2) return DENDRITE_ELIMIT;
+        pc.u_hi = n_unit;
+        pc.s_hi = (int32_t)hp.segplan.size();
+        pc.tiles = (int32_t)tile_off;
+        pc.weight = weight;
+        const int maxc = pass == 0 ? max_tc_ctas : max_ctas;
+        pc.c0 = pc.u_hi > pc.u_lo ? class_ctas(weight, maxc, cwt) : 0;
         if (pass == 0) hp.n_tc_units = n_unit;
     }
     if (n_rows >= INT32_MAX / 2) return DENDRITE_ELIMIT;
-    hp.tiles = class_tiles[0] + class_tiles[1];
-    partition_class(hp, 0, hp.n_tc_units, class_tiles[0], weight[0], max_tc_ctas, kTcWeights, hp.tc_cta_begin,
-                    hp.tc_cta_unit);
-    partition_class(hp, hp.n_tc_units, (int32_t)hp.units.size(), class_tiles[1], weight[1], max_ctas, kSmallWeights,
-                    hp.cta_begin, hp.cta_unit);
-    // partial rows per unit
-    size_t prow = 0;
-    for (AttnUnit& U : hp.units) {
-        U.prow_base = (int32_t)prow;
-        prow += (size_t)U.nchunks * U.n_rows;
+    hp.hdr.n_units = n_unit;
+    hp.hdr.n_segs = (int32_t)hp.segplan.size();
+    hp.hdr.n_rows = (int32_t)n_rows;
+    hp.tiles = (int64_t)hp.hdr.cls[0].tiles + hp.hdr.cls[1].tiles;
+    if (hp.device) {
+        // space for what k_plan_expand writes; the partial rows bounded by one
+        // extra chunk of a unit's rows per CTA boundary
+        hp.cta_begin.assign((size_t)std::max(hp.hdr.cls[1].c0, 1) + 1, 0);
+        hp.cta_unit.assign((size_t)std::max(hp.hdr.cls[1].c0, 1), 0);
+        hp.tc_cta_begin.assign((size_t)hp.hdr.cls[0].c0 + 1, 0);
+        hp.tc_cta_unit.assign((size_t)hp.hdr.cls[0].c0, 0);
+        hp.partial_rows = (size_t)n_rows + (size_t)std::max(hp.hdr.cls[1].c0 - 1, 0) * small_rows +
+                          (size_t)std::max(hp.hdr.cls[0].c0 - 1, 0) * kMaxUnitRowsTc;
+    } else {
+        for (size_t si = 0; si < hp.segplan.size(); ++si) {
+            const SegPlan& sp = hp.segplan[si];
+            const int32_t rows_per_head = (sp.ngroups - 1) * sp.group_rows + sp.rows_last;
+            for (int32_t h = 0; h < nkv; ++h) {
+                for (int32_t grp = 0; grp < sp.ngroups; ++grp) {
+                    const int32_t k = h * sp.ngroups + grp;
+                    AttnUnit& U = hp.units[sp.unit_base + k];
+                    U.seg = (int32_t)si;
+                    U.kv_head = h;
+                    U.row_lo = grp * sp.group_rows;
+                    U.n_rows = std::min(sp.group_rows, rows_per_head - U.row_lo);
+                    U.rt = grp + 1 < sp.ngroups ? sp.rt_full : sp.rt_last;
+                    U.tile_off = sp.tile_base + k * sp.n_blk;
+                    U.cfirst = U.nchunks = U.prow_base = 0;
+                    U.table_row = sp.table_row;
+                    U.blk_start = sp.blk_start;
+                    U.n_blk = sp.n_blk;
+                    U.mem_off = sp.mem_off;
+                    U.pad[0] = U.pad[1] = U.pad[2] = 0;
+                }
+            }
+        }
+        partition_class(hp, 0, hp.n_tc_units, hp.hdr.cls[0].tiles, hp.hdr.cls[0].weight, max_tc_ctas, kTcWeights,
+                        hp.tc_cta_begin, hp.tc_cta_unit);
+        partition_class(hp, hp.n_tc_units, (int32_t)hp.units.size(), hp.hdr.cls[1].tiles, hp.hdr.cls[1].weight,
+                        max_ctas, kSmallWeights, hp.cta_begin, hp.cta_unit);
+        // partial rows per unit
+        size_t prow = 0;
+        for (AttnUnit& U : hp.units) {
+            U.prow_base = (int32_t)prow;
+            prow += (size_t)U.nchunks * U.n_rows;
+        }
+        if (prow >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
+        hp.partial_rows = prow;
     }
-    if (prow >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
-    hp.partial_rows = prow;
+    if (hp.partial_rows >= (size_t)INT32_MAX) return DENDRITE_ELIMIT;
     // path of every queried branch: one entry per segment it reads
     hp.path_off.assign(n + 1, 0);
     for (const AttnSeg& S : hp.segs)
@@ -1385,16 +1731,23 @@ int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
 }
 
 // Byte layout of an uploaded plan: the sections of HostPlan one after the
-// other, each 16-byte aligned.  off[k] is the start of section k, off[kPlanSections]
-// the total size.
-constexpr int kPlanSections = 9;
+// other, each 16-byte aligned.  off[k] is the start of section k,
+// off[kPlanSections] the total size.  The sections the host always writes
+// come first (segments, members, paths, the segment list and header of the
+// device expansion); from kPlanDeviceSection on, the units, CTA splits and
+// counts, which k_plan_expand writes when the plan is expanded on the device
+// (only the prefix before them is then uploaded).
+constexpr int kPlanSections = 12;
+constexpr int kPlanDeviceSection = 6;
 size_t plan_layout(const HostPlan& hp, size_t (&off)[kPlanSections + 1]) {
     const size_t sz[kPlanSections] = {
-        hp.segs.size() * sizeof(AttnSeg),  hp.members.size() * sizeof(AttnMember),
-        hp.units.size() * sizeof(AttnUnit), hp.cta_begin.size() * 4,
-        hp.cta_unit.size() * 4,             hp.tc_cta_begin.size() * 4,
-        hp.tc_cta_unit.size() * 4,          hp.path_off.size() * 4,
-        hp.path.size() * 4};
+        hp.segs.size() * sizeof(AttnSeg),     hp.members.size() * sizeof(AttnMember),
+        hp.path_off.size() * 4,               hp.path.size() * 4,
+        hp.device ? hp.segplan.size() * sizeof(SegPlan) : 0,
+        hp.device ? sizeof(PlanHeader) : 0,
+        hp.units.size() * sizeof(AttnUnit),   hp.cta_begin.size() * 4,
+        hp.cta_unit.size() * 4,               hp.tc_cta_begin.size() * 4,
+        hp.tc_cta_unit.size() * 4,            hp.device ? 4 * sizeof(int32_t) : 0};
     size_t b = 0;
     for (int k = 0; k < kPlanSections; ++k) {
         off[k] = b;
@@ -1404,19 +1757,29 @@ size_t plan_layout(const HostPlan& hp, size_t (&off)[kPlanSections + 1]) {
     return b;
 }
 
+// Bytes of the packed plan the host writes and uploads.
+size_t plan_upload_bytes(const HostPlan& hp, const size_t (&off)[kPlanSections + 1]) {
+    return hp.device ? off[kPlanDeviceSection] : off[kPlanSections];
+}
+
 void plan_pack(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], char* h) {
     auto put = [&](int k, const void* src, size_t bytes) {
         if (bytes) std::memcpy(h + off[k], src, bytes);
     };
     put(0, hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
     put(1, hp.members.data(), hp.members.size() * sizeof(AttnMember));
-    put(2, hp.units.data(), hp.units.size() * sizeof(AttnUnit));
-    put(3, hp.cta_begin.data(), hp.cta_begin.size() * 4);
-    put(4, hp.cta_unit.data(), hp.cta_unit.size() * 4);
-    put(5, hp.tc_cta_begin.data(), hp.tc_cta_begin.size() * 4);
-    put(6, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
-    put(7, hp.path_off.data(), hp.path_off.size() * 4);
-    put(8, hp.path.data(), hp.path.size() * 4);
+    put(2, hp.path_off.data(), hp.path_off.size() * 4);
+    put(3, hp.path.data(), hp.path.size() * 4);
+    if (hp.device) {
+        put(4, hp.segplan.data(), hp.segplan.size() * sizeof(SegPlan));
+        put(5, &hp.hdr, sizeof(PlanHeader));
+        return;
+    }
+    put(6, hp.units.data(), hp.units.size() * sizeof(AttnUnit));
+    put(7, hp.cta_begin.data(), hp.cta_begin.size() * 4);
+    put(8, hp.cta_unit.data(), hp.cta_unit.size() * 4);
+    put(9, hp.tc_cta_begin.data(), hp.tc_cta_begin.size() * 4);
+    put(10, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
 }
 
 AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], const char* d, int32_t n,
@@ -1424,13 +1787,14 @@ AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1]
     AttnPlanDev v{};
     v.segs = reinterpret_cast<const AttnSeg*>(d + off[0]);
     v.members = reinterpret_cast<const AttnMember*>(d + off[1]);
-    v.units = reinterpret_cast<const AttnUnit*>(d + off[2]);
-    v.cta_begin = reinterpret_cast<const int32_t*>(d + off[3]);
-    v.cta_unit = reinterpret_cast<const int32_t*>(d + off[4]);
-    v.tc_cta_begin = reinterpret_cast<const int32_t*>(d + off[5]);
-    v.tc_cta_unit = reinterpret_cast<const int32_t*>(d + off[6]);
-    v.path_off = reinterpret_cast<const int32_t*>(d + off[7]);
-    v.path = reinterpret_cast<const int32_t*>(d + off[8]);
+    v.path_off = reinterpret_cast<const int32_t*>(d + off[2]);
+    v.path = reinterpret_cast<const int32_t*>(d + off[3]);
+    v.units = reinterpret_cast<const AttnUnit*>(d + off[6]);
+    v.cta_begin = reinterpret_cast<const int32_t*>(d + off[7]);
+    v.cta_unit = reinterpret_cast<const int32_t*>(d + off[8]);
+    v.tc_cta_begin = reinterpret_cast<const int32_t*>(d + off[9]);
+    v.tc_cta_unit = reinterpret_cast<const int32_t*>(d + off[10]);
+    v.counts = hp.device ? reinterpret_cast<const int32_t*>(d + off[11]) : nullptr;
     v.n_units = (int32_t)hp.units.size();
     v.n_ctas = (int32_t)hp.cta_unit.size();
     v.n_tc_units = hp.n_tc_units;
@@ -1459,7 +1823,28 @@ AttnPlanDev plan_rebase(AttnPlanDev v, const char* from, const char* to) {
     mv(v.tc_cta_unit);
     mv(v.path_off);
     mv(v.path);
+    if (v.counts) mv(v.counts);
     return v;
+}
+
+// Launches k_plan_expand over the plan copy at d (section offsets off), after
+// the upload that wrote its host sections.
+int launch_plan_expand(dendrite_pool* p, char* d, const size_t* off, int32_t n_units, int32_t n_segs,
+                       cudaStream_t s) {
+    ExpandArgs x{};
+    x.sp = reinterpret_cast<const SegPlan*>(d + off[4]);
+    x.hdr = reinterpret_cast<const PlanHeader*>(d + off[5]);
+    x.units = reinterpret_cast<AttnUnit*>(d + off[6]);
+    x.begin = reinterpret_cast<int32_t*>(d + off[7]);
+    x.cunit = reinterpret_cast<int32_t*>(d + off[8]);
+    x.tc_begin = reinterpret_cast<int32_t*>(d + off[9]);
+    x.tc_cunit = reinterpret_cast<int32_t*>(d + off[10]);
+    x.counts = reinterpret_cast<int32_t*>(d + off[11]);
+    x.meta = p->d_meta;
+    x.nkv = p->n_kv;
+    DENDRITE_CUDA(launch_pdl(k_plan_expand, dim3((unsigned)std::max(1, (n_units + kExpandUnits - 1) / kExpandUnits)),
+                             dim3(kExpandThreads), (size_t)n_segs * 16, s, x));
+    return DENDRITE_OK;
 }
 
 // CTAs the tensor-core kernel may use on this pool (0: not used).
@@ -1606,6 +1991,8 @@ int attn_setup(dendrite_pool* p) {
         DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_bf16, THREADS, SMEM_BF16));
         p->attn_ctas_per_sm = std::max(1, occ);
         p->tc_ready = attn_tc_setup() == DENDRITE_OK;
+        DENDRITE_CUDA(cudaFuncSetAttribute(k_plan_expand, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kMaxExpandSegs * 16));
     } else if (p->dtype == DENDRITE_TURBO) {
         p->attn_ctas_per_sm = turbo_ctas_per_sm();
     } else {
@@ -1687,17 +2074,19 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         const int ib = p->plan_buf;
         p->plan_buf ^= 1;
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied[ib]));
-        if (ib != pc.buf) std::memcpy(p->h_plan[ib], p->h_plan[pc.buf], pc.bytes);
+        if (ib != pc.buf) std::memcpy(p->h_plan[ib], p->h_plan[pc.buf], pc.upload_bytes);
         AttnMember* m = reinterpret_cast<AttnMember*>(p->h_plan[ib] + pc.members_off);
         for (int32_t e = 0; e < pc.n_members; ++e) m[e].len = p->br[branches[m[e].qi]].len;
         {
-            const int64_t n16 = (int64_t)(pc.bytes / 16);
+            const int64_t n16 = (int64_t)(pc.upload_bytes / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
             DENDRITE_CUDA(launch_pdl(k_plan_upload, dim3(grid), dim3(256), 0, s,
                                      reinterpret_cast<const uint4*>(p->h_plan[ib]),
                                      reinterpret_cast<uint4*>(p->d_plan[ib]), n16));
         }
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
+        // the other device copy holds an older plan's units: expand again
+        if (pc.device) DENDRITE_TRY(launch_plan_expand(p, p->d_plan[ib], pc.sec_off, pc.dev.n_units, pc.n_segplan, s));
         pc.dev = plan_rebase(pc.dev, p->d_plan[pc.buf], p->d_plan[ib]);
         pc.buf = ib;
         pc.version = p->version;
@@ -1717,9 +2106,9 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
                 hp.psegs[pc.last_seg[i]].block_count += d;
                 hp.unique_tiles += (int64_t)d * p->n_kv;
             }
-            DENDRITE_TRY(build_units(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp));
+            DENDRITE_TRY(build_units(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp, true));
         } else {
-            DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp));
+            DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp, true));
         }
         size_t off[kPlanSections + 1];
         const size_t b = plan_layout(hp, off);
@@ -1730,17 +2119,23 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         p->plan_buf ^= 1;
         DENDRITE_CUDA(cudaEventSynchronize(p->plan_copied[ib]));
         plan_pack(hp, off, p->h_plan[ib]);
+        const size_t up_bytes = plan_upload_bytes(hp, off);
         {
-            const int64_t n16 = (int64_t)(off[kPlanSections] / 16);
+            const int64_t n16 = (int64_t)(up_bytes / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
             DENDRITE_CUDA(launch_pdl(k_plan_upload, dim3(grid), dim3(256), 0, s,
                                      reinterpret_cast<const uint4*>(p->h_plan[ib]),
                                      reinterpret_cast<uint4*>(p->d_plan[ib]), n16));
         }
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
+        if (hp.device) DENDRITE_TRY(launch_plan_expand(p, p->d_plan[ib], off, hp.hdr.n_units, hp.hdr.n_segs, s));
         pc.dev = plan_view(hp, off, p->d_plan[ib], n, q_len, n_q_heads, n_q_heads / p->n_kv);
         pc.n_partial_rows = hp.partial_rows;
         pc.valid = true;
+        pc.device = hp.device;
+        pc.n_segplan = hp.hdr.n_segs;
+        pc.upload_bytes = up_bytes;
+        for (int k = 0; k <= kPlanSections; ++k) pc.sec_off[k] = off[k];
         pc.version = p->version;
         pc.shape_version = p->shape_version;
         pc.buf = ib;
@@ -1800,7 +2195,17 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
 extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* out) {
     if (!p || !out) return DENDRITE_EINVAL;
     if (!p->plan.valid) return DENDRITE_EINVAL;
-    *out = p->plan.stats;
+    PlanCache& pc = p->plan;
+    if (pc.device) {   // the CTA counts and partial rows were computed on the device
+        int32_t c[4];
+        DENDRITE_CUDA(cudaSetDevice(p->device));
+        DENDRITE_CUDA(cudaDeviceSynchronize());
+        DENDRITE_CUDA(cudaMemcpy(c, p->d_plan[pc.buf] + pc.sec_off[11], sizeof(c), cudaMemcpyDeviceToHost));
+        pc.stats.n_ctas = c[0];
+        pc.stats.n_tc_ctas = c[1];
+        pc.stats.n_partials = c[2];
+    }
+    *out = pc.stats;
     return DENDRITE_OK;
 }
 
@@ -1874,7 +2279,8 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     cudaStream_t s = (cudaStream_t)stream;
     static thread_local HostPlan hp;
     hp.clear();
-    DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, tc_ctas(p), hp));
+    DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, tc_ctas(p), hp,
+                            false));
     // scratch layout: plan sections, then partial acc rows, then partial (m, l)
     size_t off[kPlanSections + 1];
     const size_t b = plan_layout(hp, off);

@@ -236,6 +236,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     pdl_trigger();
+    if (a.plan.counts && (int32_t)blockIdx.x >= a.plan.counts[1]) return;   // past the device-expanded split
     if (threadIdx.x == 0) {
         abort_flag = a.meta->status != 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

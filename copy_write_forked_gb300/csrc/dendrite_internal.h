@@ -101,6 +101,9 @@ struct AttnPlanDev {
     const int32_t* path_off;       // [n_queried + 1] into path
     const int32_t* path;           // per path entry: (first unit of the segment, row groups per kv head,
                                    //  first segment row of the member, rows per row group)
+    const int32_t* counts;         // plans expanded on the device: [0] CTAs of the mma.sync class,
+                                   // [1] CTAs of the tc class, [2], [3] partial rows (low, high 32 bits);
+                                   // CTAs at or past a class's count exit at once.  Null otherwise.
     int32_t n_units;
     int32_t n_ctas;
     int32_t n_tc_units;
@@ -187,6 +190,10 @@ struct Segment {
 
 struct PlanCache {
     bool valid = false;
+    bool device = false;             // units and CTA split expanded on the device
+    int32_t n_segplan = 0;           // segments of the device expansion's list
+    size_t upload_bytes = 0;         // host-written prefix of the packed plan
+    size_t sec_off[16] = {};         // section offsets of the packed plan
     uint64_t version = 0, shape_version = 0;
     int32_t q_len = 0, n_q_heads = 0;
     std::vector<int32_t> branches;
@@ -220,6 +227,7 @@ struct dendrite_pool {
     int attn_ctas_per_sm = 1;
     int32_t tc_min_rows = dendrite::kTcMinRowsDefault;   // < 0: tensor-core attention kernel off
     int32_t fold_pct = dendrite::kFoldPctDefault;        // < 0: segments are never folded
+    int32_t device_planning = 0;                         // 0 auto, 1 always, -1 never (bf16 plans)
 
     // device state
     void* d_k = nullptr;

@@ -21,6 +21,8 @@
 // The encoder's decisions (bins, signs) are taken in fp32 with one rounded
 // operation at a time (__fmul_rn / __fadd_rn / __fsqrt_rn, no contraction)
 // in a fixed order, so the codes depend only on the input bits.
+#include <cuda_fp16.h>
+
 #include "attn_common.cuh"
 #include "turbo.h"
 
@@ -202,26 +204,6 @@ __device__ __forceinline__ void tq_encode_row(float (&x)[4], bool key, const flo
     if (lane >= 21 && lane < 24) rec[lane] = 0u;
 }
 
-// Unpacks the polar part of a record (words rec[0..15]) into the per-lane
-// layout of tq_polar_encode: level-1 codes 2 lane, 2 lane + 1, the upper-level
-// codes of the nodes this lane holds, the norm (every lane).
-__device__ __forceinline__ void tq_unpack_polar(const uint32_t* rec, int lane, int& c1a, int& c1b, int (&cu)[6],
-                                                float& norm) {
-    norm = __uint_as_float(rec[0]);
-    const uint32_t byte = (rec[1 + (lane >> 2)] >> (8 * (lane & 3))) & 0xFFu;
-    c1a = (int)(byte & 15);
-    c1b = (int)(byte >> 4);
-    const int first[6] = {0, 32, 48, 56, 60, 62};
-#pragma unroll
-    for (int L = 2; L <= 7; ++L) {
-        const bool holder = (lane & ((1 << (L - 2)) - 1)) == 0;
-        const int j = lane >> (L - 2);
-        const int q = 3 * (first[L - 2] + j);
-        const uint64_t two = (uint64_t)rec[9 + (q >> 5)] | ((q >> 5) < 5 ? (uint64_t)rec[10 + (q >> 5)] << 32 : 0ull);
-        cu[L - 2] = holder ? (int)((two >> (q & 31)) & 7u) : 0;
-    }
-}
-
 // ------------------------------------------------------------------- append
 // A grid of CTAs strides over the touched (branch, block, kv head) tiles of
 // an append into a compressed pool, as the uncompressed copy kernel does; in
@@ -306,8 +288,10 @@ __global__ void __launch_bounds__(128) k_append_turbo(
 }
 
 // ------------------------------------------------------------------ queries
-// One warp per query row o: qs[o][0..128) = R q (rotated query),
-// qs[o][128..256) = S R q (its QJL projections), fp32.
+// One warp per query row o.  With q' = R q (the rotated query) and z = S q'
+// (its QJL projections), row o of qs (1024 bytes) holds q' / max|q'| and
+// z / max|z| in fp16 (128 + 128 halves), then the two scales (float2).  The
+// scaled halves lie in [-1, 1], so no query overflows fp16.
 __global__ void __launch_bounds__(256) k_turbo_query(const __nv_bfloat16* __restrict__ Q, int32_t n_rows,
                                                       const float* __restrict__ signs, const float* __restrict__ S,
                                                       float* __restrict__ qs, const DevMeta* meta) {
@@ -329,8 +313,6 @@ __global__ void __launch_bounds__(256) k_turbo_query(const __nv_bfloat16* __rest
     const float inv = 0.0883883476483184405501055452631f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) x[k] *= inv;
-    float* dst = qs + (int64_t)o * 256;
-    *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
     const float4* S4 = reinterpret_cast<const float4*>(S);
     float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -344,28 +326,142 @@ __global__ void __launch_bounds__(256) k_turbo_query(const __nv_bfloat16* __rest
             z[k] = fmaf(s.x, xi[0], fmaf(s.y, xi[1], fmaf(s.z, xi[2], fmaf(s.w, xi[3], z[k]))));
         }
     }
-    *reinterpret_cast<float4*>(dst + 128 + 4 * lane) = make_float4(z[0], z[1], z[2], z[3]);
+    float qm = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    float zm = fmaxf(fmaxf(fabsf(z[0]), fabsf(z[1])), fmaxf(fabsf(z[2]), fabsf(z[3])));
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        qm = fmaxf(qm, __shfl_xor_sync(FULL, qm, m));
+        zm = fmaxf(zm, __shfl_xor_sync(FULL, zm, m));
+    }
+    qm = qm > 0.f ? qm : 1.f;
+    zm = zm > 0.f ? zm : 1.f;
+    const float rq = 1.f / qm, rz = 1.f / zm;
+    unsigned char* row = reinterpret_cast<unsigned char*>(qs) + (int64_t)o * 1024;
+    const __half2 a = __floats2half2_rn(x[0] * rq, x[1] * rq), b = __floats2half2_rn(x[2] * rq, x[3] * rq);
+    const __half2 c = __floats2half2_rn(z[0] * rz, z[1] * rz), d = __floats2half2_rn(z[2] * rz, z[3] * rz);
+    *reinterpret_cast<uint2*>(row + 8 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    *reinterpret_cast<uint2*>(row + 256 + 8 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&c), *reinterpret_cast<const uint32_t*>(&d));
+    if (lane == 0) *reinterpret_cast<float2*>(row + 512) = make_float2(qm, zm);
 }
 
 // ---------------------------------------------------------- partial kernel
-// The plan's units (at most 16 rows) over compressed tiles.  Per tile the CTA
-// loads the 16 key and 16 value records of the (block, kv head), decodes them
-// into fp32 rows of the rotated space in shared memory (warp w decodes slots
-// w, w + 4, ...), then warp w serves rows w, w + 4, w + 8, w + 12 of the unit:
-// per position, the score <q', k_hat> + sqrt(pi/2)/128 |e| <S q', sign(S e)>
-// (lane l takes columns l + 32 j of both sums), an online softmax in base 2,
-// and acc += p v_hat.  Partial rows stay in the rotated space.
-__global__ void __launch_bounds__(128) k_attn_partial_turbo(const AttnArgs a, const float* __restrict__ qs) {
-    __shared__ __align__(16) uint32_t krec[16][24];
-    __shared__ __align__(16) uint32_t vrec[16][16];
-    __shared__ __align__(16) float kd[16][128];
-    __shared__ __align__(16) float vd[16][128];
-    __shared__ float enorm[16];
+// The plan's units (at most 16 rows) over compressed tiles, on the tensor
+// cores.  The CTA's four warps take the chunk's tiles in turn (warp w: tiles
+// w, w + 4, ...), each with its own online-softmax state, and merge at the
+// end of the chunk.  Per tile a warp
+//   - copies the 16 key and 16 value records into shared memory (cp.async,
+//     one tile ahead);
+//   - decodes them into the unit-norm rows u = x_hat / |x_hat| in fp16 (a
+//     lane expands one level-4 node: 16 coordinates, multiplying the angle
+//     factors down from the root), swizzled for ldmatrix;
+//   - S1 = Q' U_k^T and S2 = Z sign(S E)^T with mma.sync m16n8k16 (fp16 in,
+//     fp32 accumulate; the sign matrix is built from the key bits in
+//     registers), the score of row r and token t being
+//     qmax_r |k_t| S1 + sqrt(pi/2)/128 zmax_r |e_t| S2 (times 1/sqrt(d),
+//     in base 2), then the online softmax;
+//   - acc += P' U_v with P' = p |v_t| / vs, vs the largest value norm the
+//     warp has seen (a running scale folded into the softmax rescale), so P'
+//     stays in [0, 1] in fp16 and acc = (sum p v_hat) / vs.
+// Partial rows stay in the rotated space.
+constexpr int TQ_WARPS = 4;
+constexpr int TQ_REC_ROW = 96;                       // smem stride of a key or value record
+constexpr int TQ_STAGE = 2 * BS * TQ_REC_ROW;        // key then value records of one tile
+constexpr int TQ_DEC_TILE = BS * 256;                // one decoded 16 x 128 fp16 tile
+constexpr int TQ_SCR_ROW = 136;                      // floats per row of the merge scratch
+constexpr int TQ_DEC_BYTES = BS * TQ_SCR_ROW * 4;    // decoded K and V tiles, later the merge scratch
+static_assert(TQ_DEC_BYTES >= 2 * TQ_DEC_TILE, "merge scratch overlays the decoded tiles");
+constexpr int TQ_WARP_BYTES = 2 * TQ_STAGE + TQ_DEC_BYTES;
+constexpr int TQ_Q_OFF = TQ_WARPS * TQ_WARP_BYTES;   // 16 query rows x 512 bytes (swizzled)
+constexpr int TQ_TAB_OFF = TQ_Q_OFF + 16 * 512;      // 64 (cos, sin) pairs
+constexpr int TQ_QSC_OFF = TQ_TAB_OFF + 64 * 8;      // per row (qmax, zmax) scales
+constexpr int TQ_ML_OFF = TQ_QSC_OFF + 16 * 8;       // per warp and row (m, l)
+constexpr int TQ_SMEM = TQ_ML_OFF + TQ_WARPS * 16 * 8;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+// Two QJL sign bits (bit 0: lower k) as a pair of fp16 +-1: a set bit is +1.
+__device__ __forceinline__ uint32_t sign_pair(uint32_t x) {
+    return 0xBC00BC00u ^ (((x & 3u) * 0x40008000u) & 0x80008000u);
+}
+// Byte offset of (row t, column d) in a decoded fp16 tile: 16-byte chunks
+// XOR-ed with t & 7, so that ldmatrix's eight rows hit distinct banks.
+__device__ __forceinline__ uint32_t tq_swz(int t, int d) {
+    return (uint32_t)(t * 256 + ((((d >> 3) ^ (t & 7))) << 4) + (d & 7) * 2);
+}
+
+// Decodes coordinates 16 j .. 16 j + 15 of a record's unit-norm row: the
+// product of the angle factors on the path from the root (level 7) to each
+// coordinate, in that order.  tab: (cos, sin) of the bin centres, levels 7
+// down to 2 (8 each) then level 1 (16).
+__device__ __forceinline__ void tq_decode16(const uint32_t* rec, int j, const float2* tab, uint4& lo, uint4& hi) {
+    auto bits = [&](int pos, int n) {
+        const int w = pos >> 5;
+        return __funnelshift_r(rec[9 + w], rec[10 + w], pos & 31) & ((1u << n) - 1u);
+    };
+    const uint32_t c7 = bits(186, 3), c6 = bits(180 + 3 * (j >> 2), 3), c5 = bits(168 + 3 * (j >> 1), 3);
+    const uint32_t c4 = bits(144 + 3 * j, 3), c3 = bits(96 + 6 * j, 6), c2 = bits(12 * j, 12);
+    const uint32_t c1 = rec[1 + j];
+    const float2 t7 = tab[c7], t6 = tab[8 + c6], t5 = tab[16 + c5], t4 = tab[24 + c4];
+    float r = (j & 4) ? t7.y : t7.x;
+    r *= (j & 2) ? t6.y : t6.x;
+    r *= (j & 1) ? t5.y : t5.x;
+    float r3[2] = {r * t4.x, r * t4.y};
+    float r2[4], r1[8], x[16];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 t3 = tab[32 + ((c3 >> (3 * i)) & 7u)];
+        r2[2 * i] = r3[i] * t3.x;
+        r2[2 * i + 1] = r3[i] * t3.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t2 = tab[40 + ((c2 >> (3 * i)) & 7u)];
+        r1[2 * i] = r2[i] * t2.x;
+        r1[2 * i + 1] = r2[i] * t2.y;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 t1 = tab[48 + ((c1 >> (4 * k)) & 15u)];
+        x[2 * k] = r1[k] * t1.x;
+        x[2 * k + 1] = r1[k] * t1.y;
+    }
+    lo = make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+    hi = make_uint4(pack_half2(x[8], x[9]), pack_half2(x[10], x[11]), pack_half2(x[12], x[13]),
+                    pack_half2(x[14], x[15]));
+}
+
+__global__ void __launch_bounds__(128, 3) k_attn_partial_turbo(const AttnArgs a, const float* __restrict__ qs) {
+    extern __shared__ __align__(16) unsigned char tq_smem[];
     __shared__ int st0;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     pdl_trigger();
-    if (threadIdx.x == 0) st0 = a.meta->status;
+    if (tid == 0) st0 = a.meta->status;
+    float2* tab = reinterpret_cast<float2*>(tq_smem + TQ_TAB_OFF);
+    if (tid < 64) {
+        const int L = tid < 48 ? 7 - (tid >> 3) : 1;   // levels 7 .. 2, then level 1
+        const int c = tid < 48 ? (tid & 7) : tid - 48;
+        tab[tid] = L == 1 ? make_float2(c_tq.cos1[c], c_tq.sin1[c])
+                          : make_float2(c_tq.cos_up[L - 2][c], c_tq.sin_up[L - 2][c]);
+    }
     __syncthreads();
     if (st0) return;
     const AttnPlanDev& pl = a.plan;
@@ -376,88 +472,278 @@ __global__ void __launch_bounds__(128) k_attn_partial_turbo(const AttnArgs a, co
     const unsigned char* KP = reinterpret_cast<const unsigned char*>(a.pool_k);
     const unsigned char* VP = reinterpret_cast<const unsigned char*>(a.pool_v);
     const float qjl_c = 0.0097916591f;   // sqrt(pi / 2) / 128
+    const uint32_t sbase = smem_u32(tq_smem);
+    const uint32_t wbase = sbase + warp * TQ_WARP_BYTES;
+    const uint32_t qbase = sbase + TQ_Q_OFF;
+    unsigned char* wptr = tq_smem + warp * TQ_WARP_BYTES;
+    const float2* qsc = reinterpret_cast<const float2*>(tq_smem + TQ_QSC_OFF);
+    float2* sml = reinterpret_cast<float2*>(tq_smem + TQ_ML_OFF);
+    const float NEG_INF = -INFINITY;
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
         const int32_t uend = U.tile_off + U.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
-        float qr[4][4], sq[4][4], acc[4][4], m[4], l[4];
-        int32_t lim[4];
+        // ---- the unit's query rows: fp16 tile (swizzled) and scales
+        {
+            const int r = tid >> 3, cc = tid & 7;
+            const bool v = r < U.n_rows;
+            const AttnRow R = v ? unit_row(pl, U, r) : AttnRow{0, 0};
+            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(qs) +
+                                                              (int64_t)R.q_row * 1024);
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int row = warp + 4 * rr;
-            const bool v = row < U.n_rows;
-            const AttnRow R = v ? unit_row(pl, U, row) : AttnRow{0, 0};
-            lim[rr] = R.limit;
-            m[rr] = -INFINITY;
-            l[rr] = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                qr[rr][j] = v ? qs[(int64_t)R.q_row * 256 + lane + 32 * j] : 0.f;
-                sq[rr][j] = v ? qs[(int64_t)R.q_row * 256 + 128 + lane + 32 * j] : 0.f;
-                acc[rr][j] = 0.f;
+            for (int k = 0; k < 4; ++k) {
+                const int ch = cc + 8 * k;
+                const uint4 val = v ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(tq_smem + TQ_Q_OFF + r * 512 + ((ch ^ (r & 7)) << 4)) = val;
             }
+            if (cc == 0)
+                reinterpret_cast<float2*>(tq_smem + TQ_QSC_OFF)[r] =
+                    v ? *reinterpret_cast<const float2*>(reinterpret_cast<const unsigned char*>(src) + 512)
+                      : make_float2(0.f, 0.f);
         }
-        for (int32_t tt = t; tt < cend; ++tt) {
+        __syncthreads();
+        const int r0 = lane >> 2, r1 = r0 + 8;
+        int32_t lim0 = 0, lim1 = 0;
+        if (r0 < U.n_rows) lim0 = unit_row(pl, U, r0).limit;
+        if (r1 < U.n_rows) lim1 = unit_row(pl, U, r1).limit;
+        const float2 sc0 = qsc[r0], sc1 = qsc[r1];
+        const float a0 = sc0.x * a.scale_log2, a1 = sc1.x * a.scale_log2;
+        const float b0 = qjl_c * sc0.y * a.scale_log2, b1 = qjl_c * sc1.y * a.scale_log2;
+        float o[16][4];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f, vs = 0.f;
+        // ---- this warp's tiles
+        auto issue = [&](int32_t tt, int stage) {
             const int32_t lb = U.blk_start + (tt - U.tile_off);
             int32_t blk = a.table[(int64_t)U.table_row * a.bpb + lb];
             if ((uint32_t)blk >= (uint32_t)a.n_blocks) {
-                if (threadIdx.x == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
+                if (lane == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                 blk = 0;   // read a valid block; the pool is poisoned anyway
             }
-            const uint4* kg = reinterpret_cast<const uint4*>(KP + ((int64_t)blk * a.n_kv + U.kv_head) * BS * KREC);
-            const uint4* vg = reinterpret_cast<const uint4*>(VP + ((int64_t)blk * a.n_kv + U.kv_head) * BS * VREC);
-            __syncthreads();
-            for (int e = threadIdx.x; e < BS * KREC / 16; e += blockDim.x) reinterpret_cast<uint4*>(krec)[e] = kg[e];
-            for (int e = threadIdx.x; e < BS * VREC / 16; e += blockDim.x) reinterpret_cast<uint4*>(vrec)[e] = vg[e];
-            __syncthreads();
-            for (int slot = warp; slot < BS; slot += 4) {
-                int c1a, c1b, cu[6];
-                float nrm, xh[4];
-                tq_unpack_polar(krec[slot], lane, c1a, c1b, cu, nrm);
-                tq_polar_decode32(nrm, c1a, c1b, cu, lane, xh);
-                *reinterpret_cast<float4*>(&kd[slot][4 * lane]) = make_float4(xh[0], xh[1], xh[2], xh[3]);
-                tq_unpack_polar(vrec[slot], lane, c1a, c1b, cu, nrm);
-                tq_polar_decode32(nrm, c1a, c1b, cu, lane, xh);
-                *reinterpret_cast<float4*>(&vd[slot][4 * lane]) = make_float4(xh[0], xh[1], xh[2], xh[3]);
-                if (lane == 0) enorm[slot] = __uint_as_float(krec[slot][20]);
+            const unsigned char* kg = KP + ((int64_t)blk * a.n_kv + U.kv_head) * BS * KREC;
+            const unsigned char* vg = VP + ((int64_t)blk * a.n_kv + U.kv_head) * BS * VREC;
+            const uint32_t dst = wbase + stage * TQ_STAGE;
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {   // key records: 96 chunks of 16 bytes
+                const int ch = lane + 32 * i, row = ch / 6, col = ch - 6 * row;
+                cp_async16(dst + row * TQ_REC_ROW + col * 16, kg + ch * 16);
             }
-            __syncthreads();
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                if (warp + 4 * rr >= U.n_rows) continue;
-                for (int tok = 0; tok < BS; ++tok) {
-                    if (lb * BS + tok >= lim[rr]) break;
-                    float dq = 0.f, dj = 0.f;
+            for (int i = 0; i < 2; ++i) {   // value records: 64 chunks
+                const int ch = lane + 32 * i, row = ch >> 2, col = ch & 3;
+                cp_async16(dst + BS * TQ_REC_ROW + row * TQ_REC_ROW + col * 16, vg + ch * 16);
+            }
+        };
+        int32_t tt = t + warp;
+        if (tt < cend) issue(tt, 0);
+        cp_async_commit();
+        for (int it = 0; tt < cend; tt += TQ_WARPS, ++it) {
+            if (tt + TQ_WARPS < cend) issue(tt + TQ_WARPS, (it + 1) & 1);
+            cp_async_commit();
+            cp_async_wait1();
+            __syncwarp();
+            const unsigned char* rk = wptr + (it & 1) * TQ_STAGE;   // key records
+            const unsigned char* rv = rk + BS * TQ_REC_ROW;          // value records
+            unsigned char* dk = wptr + 2 * TQ_STAGE;                 // decoded K
+            unsigned char* dv = dk + TQ_DEC_TILE;                    // decoded V
+            // decode: pass p takes rows 4 p + lane / 8, level-4 node lane % 8
+            {
+                const int j = lane & 7;
+#pragma unroll 1
+                for (int pss = 0; pss < 8; ++pss) {
+                    const int row = (pss & 3) * 4 + (lane >> 3);
+                    const bool isv = pss >= 4;
+                    const uint32_t* rec = reinterpret_cast<const uint32_t*>((isv ? rv : rk) + row * TQ_REC_ROW);
+                    uint4 lo, hi;
+                    tq_decode16(rec, j, tab, lo, hi);
+                    unsigned char* d = isv ? dv : dk;
+                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j)) = lo;
+                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + 8)) = hi;
+                }
+            }
+            // per-token scalars of this lane's columns: tokens 2 (lane % 4) + e + 8 nt
+            float kn[2][2], en[2][2], vn[2][2];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        dq = fmaf(qr[rr][j], kd[tok][lane + 32 * j], dq);
-                        const bool bit = (krec[tok][16 + j] >> lane) & 1u;
-                        dj += bit ? sq[rr][j] : -sq[rr][j];
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = 2 * (lane & 3) + e + 8 * nt;
+                    const uint32_t* kr = reinterpret_cast<const uint32_t*>(rk + tok * TQ_REC_ROW);
+                    kn[nt][e] = __uint_as_float(kr[0]);
+                    en[nt][e] = __uint_as_float(kr[20]);
+                    vn[nt][e] = __uint_as_float(reinterpret_cast<const uint32_t*>(rv + tok * TQ_REC_ROW)[0]);
+                }
+            }
+            // the QJL bits of tokens lane / 4 and 8 + lane / 4
+            uint32_t qb[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const uint32_t* kr = reinterpret_cast<const uint32_t*>(rk + ((lane >> 2) + 8 * nt) * TQ_REC_ROW);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) qb[nt][w] = kr[16 + w] >> (2 * (lane & 3));
+            }
+            __syncwarp();
+            // S1 = Q' U_k^T, S2 = Z sign^T (16 rows x 16 tokens each)
+            float s1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const uint32_t kt = wbase + 2 * TQ_STAGE;
+                const int mi = lane >> 3;
+                const int tokl = (mi >> 1) * 8 + (lane & 7);
+                const int qr = lane & 15, qh = lane >> 4;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t qa[4], za[4], kb0, kb1, kb2, kb3;
+                    ldsm_x4(qbase + qr * 512 + (((2 * ks + qh) ^ (qr & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
+                    ldsm_x4(qbase + qr * 512 + (((16 + 2 * ks + qh) ^ (qr & 7)) << 4), za[0], za[1], za[2], za[3]);
+                    ldsm_x4(kt + tq_swz(tokl, ks * 16 + (mi & 1) * 8), kb0, kb1, kb2, kb3);
+                    mma16816_f16(s1[0], qa, kb0, kb1);
+                    mma16816_f16(s1[1], qa, kb2, kb3);
+                    const int sh = (ks & 1) * 16;
+                    mma16816_f16(s2[0], za, sign_pair(qb[0][ks >> 1] >> sh), sign_pair(qb[0][ks >> 1] >> (sh + 8)));
+                    mma16816_f16(s2[1], za, sign_pair(qb[1][ks >> 1] >> sh), sign_pair(qb[1][ks >> 1] >> (sh + 8)));
+                }
+            }
+            // scores, mask, online softmax
+            const int32_t pos0 = (U.blk_start + (tt - U.tile_off)) * BS + 2 * (lane & 3);
+            float sc[2][4];
+            float mx0 = NEG_INF, mx1 = NEG_INF, vmax = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int32_t pos = pos0 + 8 * nt + e;
+                    const float v0 = a0 * (kn[nt][e] * s1[nt][e]) + b0 * (en[nt][e] * s2[nt][e]);
+                    const float v1 = a1 * (kn[nt][e] * s1[nt][2 + e]) + b1 * (en[nt][e] * s2[nt][2 + e]);
+                    sc[nt][e] = pos < lim0 ? v0 : NEG_INF;
+                    sc[nt][2 + e] = pos < lim1 ? v1 : NEG_INF;
+                    mx0 = fmaxf(mx0, sc[nt][e]);
+                    mx1 = fmaxf(mx1, sc[nt][2 + e]);
+                    vmax = fmaxf(vmax, vn[nt][e]);
+                }
+            }
+#pragma unroll
+            for (int m = 1; m <= 2; m <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, m));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, m));
+                vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, m));
+            }
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float u0s = n0 == NEG_INF ? 0.f : n0, u1s = n1 == NEG_INF ? 0.f : n1;
+            const float al0 = exp2f(m0 - u0s), al1 = exp2f(m1 - u1s);
+            m0 = n0;
+            m1 = n1;
+            const float vs_new = fmaxf(fmaxf(vs, vmax), 1e-30f);
+            const float rv_new = 1.f / vs_new;
+            const float g = vs * rv_new;
+            const float g0 = al0 * g, g1 = al1 * g;
+            vs = vs_new;
+            float ps0 = 0.f, ps1 = 0.f;
+            uint32_t pa[4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float p[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    p[e] = exp2f(sc[nt][e] - u0s);
+                    p[2 + e] = exp2f(sc[nt][2 + e] - u1s);
+                    ps0 += p[e];
+                    ps1 += p[2 + e];
+                }
+                const float w0 = vn[nt][0] * rv_new, w1 = vn[nt][1] * rv_new;
+                pa[2 * nt] = pack_half2(p[0] * w0, p[1] * w1);
+                pa[2 * nt + 1] = pack_half2(p[2] * w0, p[3] * w1);
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+            if (!__all_sync(FULL, g0 == 1.f && g1 == 1.f)) {
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= g0;
+                    o[n][1] *= g0;
+                    o[n][2] *= g1;
+                    o[n][3] *= g1;
+                }
+            }
+            // acc += P' U_v
+            {
+                const uint32_t vt = wbase + 2 * TQ_STAGE + TQ_DEC_TILE;
+                const int mi = lane >> 3;
+                const int tokl = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    uint32_t v0r, v1r, v2r, v3r;
+                    ldsm_x4_t(vt + tq_swz(tokl, np * 16 + (mi >> 1) * 8), v0r, v1r, v2r, v3r);
+                    mma16816_f16(o[2 * np], pa, v0r, v1r);
+                    mma16816_f16(o[2 * np + 1], pa, v2r, v3r);
+                }
+            }
+            __syncwarp();   // records and decoded tiles are reused by the next tile
+        }
+        cp_async_wait0();
+        // ---- merge the four warps' states and write the partial rows
+        l0 += __shfl_xor_sync(FULL, l0, 1);
+        l0 += __shfl_xor_sync(FULL, l0, 2);
+        l1 += __shfl_xor_sync(FULL, l1, 1);
+        l1 += __shfl_xor_sync(FULL, l1, 2);
+        if ((lane & 3) == 0) {
+            sml[warp * 16 + r0] = make_float2(m0, l0);
+            sml[warp * 16 + r1] = make_float2(m1, l1);
+        }
+        __syncthreads();
+        {
+            float M0 = NEG_INF, M1 = NEG_INF;
+#pragma unroll
+            for (int w = 0; w < TQ_WARPS; ++w) {
+                M0 = fmaxf(M0, sml[w * 16 + r0].x);
+                M1 = fmaxf(M1, sml[w * 16 + r1].x);
+            }
+            const float f0 = m0 == NEG_INF ? 0.f : exp2f(m0 - M0) * vs;
+            const float f1 = m1 == NEG_INF ? 0.f : exp2f(m1 - M1) * vs;
+            float* scr = reinterpret_cast<float*>(wptr + 2 * TQ_STAGE);
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                const int col = 8 * n + 2 * (lane & 3);
+                *reinterpret_cast<float2*>(scr + r0 * TQ_SCR_ROW + col) = make_float2(o[n][0] * f0, o[n][1] * f0);
+                *reinterpret_cast<float2*>(scr + r1 * TQ_SCR_ROW + col) = make_float2(o[n][2] * f1, o[n][3] * f1);
+            }
+        }
+        __syncthreads();
+        {
+            const int r = tid >> 3, cc = tid & 7;
+            const int32_t prow = U.prow_base + (c - U.cfirst) * U.n_rows + r;
+            if (r < U.n_rows) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int col = 4 * cc + 32 * k;
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int w = 0; w < TQ_WARPS; ++w) {
+                        const float4 v = *reinterpret_cast<const float4*>(tq_smem + w * TQ_WARP_BYTES + 2 * TQ_STAGE +
+                                                                          (r * TQ_SCR_ROW + col) * 4);
+                        sum.x += v.x;
+                        sum.y += v.y;
+                        sum.z += v.z;
+                        sum.w += v.w;
                     }
-                    float dot = fmaf(qjl_c * enorm[tok], dj, dq);
+                    *reinterpret_cast<float4*>(a.part_acc + (int64_t)prow * D + col) = sum;
+                }
+                if (cc == 0) {
+                    float M = NEG_INF, L = 0.f;
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(FULL, dot, o);
-                    const float sc = dot * a.scale_log2;
-                    const float mn = fmaxf(m[rr], sc);
-                    const float al = exp2f(m[rr] - mn);
-                    const float p = exp2f(sc - mn);
-                    l[rr] = l[rr] * al + p;
+                    for (int w = 0; w < TQ_WARPS; ++w) M = fmaxf(M, sml[w * 16 + r].x);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[rr][j] = fmaf(p, vd[tok][lane + 32 * j], acc[rr][j] * al);
-                    m[rr] = mn;
+                    for (int w = 0; w < TQ_WARPS; ++w) {
+                        const float2 ml = sml[w * 16 + r];
+                        L += ml.x == NEG_INF ? 0.f : ml.y * exp2f(ml.x - M);
+                    }
+                    a.part_ml[prow] = make_float2(M, L);
                 }
             }
         }
-        const int32_t prow0 = U.prow_base + (c - U.cfirst) * U.n_rows;
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int row = warp + 4 * rr;
-            if (row >= U.n_rows) continue;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) a.part_acc[(int64_t)(prow0 + row) * D + lane + 32 * j] = acc[rr][j];
-            if (lane == 0) a.part_ml[prow0 + row] = make_float2(m[rr], l[rr]);
-        }
+        __syncthreads();   // the next unit rewrites the query tile and the scratch
         t = cend;
         ++u;
     }
@@ -502,6 +788,7 @@ int launch_turbo_partials(const AttnArgs& a, const void* Q, int32_t n_rows, cons
     if (a.plan.n_ctas > 0) {
         cfg.gridDim = dim3((unsigned)a.plan.n_ctas);
         cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = TQ_SMEM;
         if (cudaLaunchKernelEx(&cfg, k_attn_partial_turbo, a, (const float*)qs) != cudaSuccess) return DENDRITE_ECUDA;
     }
     return DENDRITE_OK;
@@ -509,7 +796,11 @@ int launch_turbo_partials(const AttnArgs& a, const void* Q, int32_t n_rows, cons
 
 int turbo_ctas_per_sm() {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_turbo, 128, 0) != cudaSuccess) return 1;
+    if (cudaFuncSetAttribute(k_attn_partial_turbo, cudaFuncAttributeMaxDynamicSharedMemorySize, TQ_SMEM) !=
+        cudaSuccess)
+        return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_turbo, 128, TQ_SMEM) != cudaSuccess)
+        return 1;
     return std::max(1, occ);
 }
 

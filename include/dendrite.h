@@ -88,7 +88,13 @@ typedef struct dendrite_pool_opts {
                                     * time says that is cheaper.  0 = default (fold when  *
                                     * the estimate drops); k > 0 = fold when it drops     *
                                     * below k percent; -1 = never.                        */
-    int32_t reserved[3];           /* must be zero                                         */
+    int32_t device_planning;       /* bf16 attention plans: expand the sharing segments   *
+                                    * into work units and split them over CTAs on the GPU *
+                                    * (a one-CTA kernel before the partial kernels) rather *
+                                    * than on the host.  0 = default (plans of at least   *
+                                    * 2048 units), 1 = always, -1 = never.  The result is *
+                                    * the same plan either way.                           */
+    int32_t reserved[2];           /* must be zero                                         */
 } dendrite_pool_opts;
 
 /*

@@ -35,13 +35,14 @@ def _check(tree, leaf_ids, Q, out, sample):
         assert (err <= TOL + half_ulp_bf16(ref)).all(), (i, float(err.max()))
 
 
-@pytest.mark.parametrize("fold", [0, -1])
-def test_mcts_loop_matches_oracle_every_iteration(fold):
+@pytest.mark.parametrize("fold,dev", [(0, 0), (-1, 0), (0, 1)])
+def test_mcts_loop_matches_oracle_every_iteration(fold, dev):
     """60 iterations of fork 4 / append 32 / attend over every live leaf; each
     iteration's outputs are compared with the oracle's for the 4 new children
-    and 4 other live leaves."""
+    and 4 other live leaves.  dev 1: every plan's units and CTA split are
+    expanded on the device."""
     w = W.mcts(root=512, iters=60)
-    pool = pool_for(w, fold_segments=fold)
+    pool = pool_for(w, fold_segments=fold, device_planning=dev)
     tree = KVTree(w.n_kv_heads, w.head_dim)
     gen = torch.Generator(device="cuda").manual_seed(5)
     h, live = {}, []
@@ -91,8 +92,8 @@ def _extend(w, ops, query=None):
                       list(w.ops) + list(ops), tuple(query if query is not None else w.query), w.q_len, w.seed)
 
 
-@pytest.mark.parametrize("step_tokens", [1, 7, 23])
-def test_block_crossing_appends_lengthen_cached_segments(step_tokens):
+@pytest.mark.parametrize("step_tokens,dev", [(1, 0), (7, 0), (23, 0), (7, 1)])
+def test_block_crossing_appends_lengthen_cached_segments(step_tokens, dev):
     """Decode steps of 1, 7 or 23 tokens per branch: a step whose appends take
     branches into new blocks reuses the cached segments (stats.refreshed 2),
     with the same segments, tiles and partial rows as a plan built anew, and
@@ -103,7 +104,7 @@ def test_block_crossing_appends_lengthen_cached_segments(step_tokens):
     # enough steps to cross at least one block boundary (the leaves start at 103 tokens)
     steps = [W.Op("append", tuple(base.query), step_tokens) for _ in range(max(6, 24 // step_tokens))]
     w_full = _extend(base, steps)
-    pool = pool_for(w_full)
+    pool = pool_for(w_full, device_planning=dev)
     h = run_script(pool, base)
     br = [h[b] for b in base.query]
     Q = base.q("cuda")
@@ -156,3 +157,49 @@ def test_block_crossing_of_a_shared_last_segment_rebuilds():
     assert pool.last_plan_stats()["refreshed"] == 0
     check_attention(w_full, out, [0, 1], TOL)
     pool.close()
+
+
+STAT_KEYS = ("n_segments", "n_units", "n_ctas", "n_tc_ctas", "n_partials", "tiles", "unique_tiles")
+
+
+def _device_cases():
+    bf = dict(n_kv=8, n_q=32, d=128, bs=16, dtype=torch.bfloat16)
+    return [
+        ("mcts", lambda: W.mcts(root=512, iters=120)),
+        ("beam", lambda: W.beam(requests=4, prefix=1024, width=4, divergent=64)),
+        ("spec_verify", lambda: W.spec_verify(requests=4, prefix=2048)),
+        ("fork_stress", lambda: W.fork_stress_attention(requests=2, prefix=4096, width=16, divergent=256)),
+    ] + [(f"random_{k}", (lambda k=k: W.random_script(k, n_ops=60, max_live=24, max_append=300, **bf)))
+         for k in range(6)]
+
+
+@pytest.mark.parametrize("name,make", _device_cases(), ids=[c[0] for c in _device_cases()])
+@pytest.mark.parametrize("fold", [0, -1])
+def test_device_expansion_equals_host_expansion(name, make, fold):
+    """The same call planned with the units and CTA split expanded on the
+    device (device_planning 1) and on the host (-1): bit-identical outputs,
+    the same CTA counts and partial rows, and oracle parity."""
+    from _harness import check_attention
+    from copy_write_forked_gb300.runner import run_script
+    w = make()
+    outs, stats = [], []
+    for dev in (1, -1):
+        pool = pool_for(w, fold_segments=fold, device_planning=dev)
+        h = run_script(pool, w)
+        br = [h[b] for b in w.query]
+        Q = w.q("cuda")
+        out = pool.tree_attn_decode(Q, br)
+        pool.sync()
+        outs.append(out.clone())
+        stats.append(pool.last_plan_stats())
+        # a second call on the unchanged tree reuses the plan (and its device copy)
+        again = pool.tree_attn_decode(Q, br)
+        pool.sync()
+        assert torch.equal(again, out)
+        pool.close()
+    assert torch.equal(outs[0], outs[1]), name
+    for key in STAT_KEYS:
+        assert stats[0][key] == stats[1][key], (name, key, stats[0][key], stats[1][key])
+    rng = random.Random(len(w.query))
+    sample = sorted(rng.sample(range(len(w.query)), min(6, len(w.query))))
+    check_attention(w, outs[0], sample, TOL)

@@ -130,6 +130,19 @@ def test_beam_shaped_tree_over_compressed_rows():
     pool.close()
 
 
+@pytest.mark.parametrize("prefix,divergent", [(1500, 300), (4096, 16)])
+def test_long_shared_prefix_over_compressed_rows(prefix, divergent):
+    """Long prefixes: every warp of a CTA takes many tiles of a unit (the
+    per-warp softmax states, the running value scale and the end-of-chunk
+    merge of four warps all carry weight)."""
+    w = W.beam(requests=2, prefix=prefix, width=4, divergent=divergent)
+    ts, tS, signs, S = _codec(11)
+    pool = pool_for(w, turbo=(ts, tS))
+    h = run_script(pool, w)
+    _check_attention(pool, h, w, signs, S, sample=[0, 2, 5, 7])
+    pool.close()
+
+
 def test_multilayer_split_append_encodes_every_layer():
     w = W.beam(requests=1, prefix=40, width=2, divergent=9, n_kv=2, n_q=4)
     ts, tS, signs, S = _codec(3)
