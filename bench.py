@@ -522,6 +522,10 @@ def run_ours(args):
     per_step = 1 + 2 + (4 if plan["n_tc_units"] else 3) + 1
     cfg = config_of(w, name)
     cfg["step"] = _step_desc(kind)
+    if kind == "decode" and w.unique_kv_bytes() > (256 << 20):
+        cfg["l2"] = ("not flushed: inputs larger than L2 (%.1f GB of unique KV read per step; each branch writes "
+                     "one new token and copies its parent's partially filled tail block)"
+                     % (statistics.mean(tok_timed) * kv_tok / 1e9))
     if args.turbo:
         cfg["kv_storage"] = ("compressed blocks (TurboQuant records: 96-byte keys, 64-byte values per token and "
                              "head, 3.2x smaller than bf16); algorithmic bytes count the records")
@@ -623,11 +627,16 @@ def run_decode_layers(args):
     br = [c for ks in kids for c in ks]
     pool.append_begin(br, Dv)
     part, plan_us = [], []
+    layer_ms = {k: [] for k in ("append_copy", "attn_partial", "attn_merge", "attn_total")}
     for l in range(NL):
         pool.append_layer(l, Kd[l][0], Kd[l][1])
         flush_r.max()
         pool.tree_attn_decode(Q, br, out=outs[l], layer=l)
-        part.append(pool.last_timings()["attn_partial"])
+        tm = pool.last_timings()
+        part.append(tm["attn_partial"])
+        for k in layer_ms:
+            if tm.get(k) is not None:
+                layer_ms[k].append(tm[k])
         plan_us.append(pool.last_plan_stats()["plan_us"])
     pool.free(br)
     pool.set_profiling(False)
@@ -644,6 +653,8 @@ def run_decode_layers(args):
                                    "fork, append_begin, 32 x (append_layer, tree attention), free",
                        "l2": "flushed before every step"},
             "per_layer_partial_kernel_ms": pk,
+            "per_layer_kernel_ms_median": {k: (statistics.median(v) if v else None) for k, v in layer_ms.items()},
+            "per_layer_ms": step_ms / NL,
             "roofline": {"bound": "hbm", "kernel": "k_attn_partial_bf16", "achieved": unique / (pk / 1e3) / 1e9,
                          "peak": peak, "peak_source": src, "unit": "GB/s",
                          "frac": unique / (pk / 1e3) / 1e9 / peak, "algorithmic_bytes": unique},

@@ -67,9 +67,22 @@ constexpr size_t SMEM_BF16 = 1024 + (size_t)NSTAGE * STAGE_BYTES + 2 * NSTAGE * 
 // with lane l owning columns 4 l .. 4 l + 3 (one 16-byte load per partial
 // row), eight acc rows in flight.  Partial rows are read through L2 only.
 // Nothing is stored when the pool's status word is set.
+// Waits (once per thread) for the partial kernel before the first read of its
+// partial rows or of the status word: the plan lookups before it (path, units,
+// chunk enumeration) overlap the partial kernel's tail.  Every kernel that
+// wrote the plan completed before the partial kernel passed its own wait,
+// which comes before it lets the merge launch.
+__device__ __forceinline__ void wait_partials(bool& waited) {
+    if (!waited) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+    }
+}
+
 template <typename T>
-__device__ __forceinline__ void merge_row_wide(const AttnArgs& a, int32_t o, int lane, int32_t status) {
+__device__ __forceinline__ void merge_row_wide(const AttnArgs& a, int32_t o, int lane) {
     const AttnPlanDev& pl = a.plan;
+    bool waited = false;
     const int G = pl.group;
     const int32_t qi = o / (pl.q_len * pl.n_q_heads);
     const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
@@ -112,6 +125,7 @@ __device__ __forceinline__ void merge_row_wide(const AttnArgs& a, int32_t o, int
             const bool valid = pidx < total;
             const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
             const int nb = min(32, total - p0);
+            wait_partials(waited);
             // the first eight acc rows go out with the (m, l) loads
             float4 v[8];
 #pragma unroll
@@ -160,7 +174,8 @@ __device__ __forceinline__ void merge_row_wide(const AttnArgs& a, int32_t o, int
             }
         }
     }
-    if (status) return;
+    wait_partials(waited);
+    if (*reinterpret_cast<volatile const int32_t*>(&a.meta->status)) return;
     const float inv = 1.f / L;
     float y[4] = {acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv};
     if (a.tq_signs) {
@@ -781,20 +796,17 @@ __global__ void __launch_bounds__(128) k_attn_partial_f32(const AttnArgs a) {
 // took 2 us longer).
 template <typename T, bool WIDE>
 __global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs a) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     pdl_trigger();
     const AttnPlanDev& pl = a.plan;
     const int lane = threadIdx.x & 31;
     const int32_t o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int32_t n_out = pl.n_queried * pl.q_len * pl.n_q_heads;
     if (o >= n_out) return;
-    // the status word is checked only before the store, so that its load
-    // overlaps the plan loads (the plan is always readable)
-    const int32_t status = *reinterpret_cast<volatile const int32_t*>(&a.meta->status);
     if constexpr (WIDE) {
-        merge_row_wide<T>(a, o, lane, status);
+        merge_row_wide<T>(a, o, lane);
         return;
     }
+    bool waited = false;
     const int G = pl.group;
     const int32_t qi = o / (pl.q_len * pl.n_q_heads);
     const int32_t rem = o - qi * pl.q_len * pl.n_q_heads;
@@ -840,6 +852,7 @@ __global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs
             const bool valid = pidx < total;
             const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
             const int nb = min(32, total - p0);
+            wait_partials(waited);
             // the first eight acc rows go out with the (m, l) loads
             float4 v[8];
             if constexpr (WIDE) {
@@ -910,7 +923,8 @@ __global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs
             }
         }
     }
-    if (status) return;
+    wait_partials(waited);
+    if (*reinterpret_cast<volatile const int32_t*>(&a.meta->status)) return;
     const float inv = 1.f / L;
     if constexpr (WIDE) {
         T* dst = static_cast<T*>(a.out) + (int64_t)o * D + 4 * lane;
@@ -943,7 +957,6 @@ __global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs
 // the per-row kernel above.  Lane l owns columns 4 l .. 4 l + 3.
 template <typename T, int NG>
 __global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     pdl_trigger();
     const AttnPlanDev& pl = a.plan;
     const int lane = threadIdx.x & 31;
@@ -959,9 +972,7 @@ __global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a)
     const int j = x % pl.q_len;
     const int32_t qi = x / pl.q_len;
     const int g0 = gc * NG;
-    // the status word is checked only before the store, so that its load
-    // overlaps the plan loads (the plan is always readable)
-    const int32_t status = *reinterpret_cast<volatile const int32_t*>(&a.meta->status);
+    bool waited = false;
     const int32_t pbeg = pl.path_off[qi], pend = pl.path_off[qi + 1];
     float M[NG], L[NG];
     float4 acc[NG];
@@ -1005,6 +1016,7 @@ __global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a)
             const bool valid = pidx < total;
             const int32_t prow = valid ? eb + (pidx - ex) * es : 0;
             const int nb = min(32, total - p0);
+            wait_partials(waited);
             float2 ml[NG];
 #pragma unroll
             for (int i = 0; i < NG; ++i) ml[i] = valid ? __ldcg(a.part_ml + prow + i) : make_float2(-INFINITY, 0.f);
@@ -1058,7 +1070,8 @@ __global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a)
             }
         }
     }
-    if (status) return;
+    wait_partials(waited);
+    if (*reinterpret_cast<volatile const int32_t*>(&a.meta->status)) return;
 #pragma unroll
     for (int i = 0; i < NG; ++i) {
         const float inv = 1.f / L[i];
@@ -1362,11 +1375,13 @@ __global__ void __launch_bounds__(kExpandThreads) k_plan_expand(const ExpandArgs
 // Launched as a programmatic dependent, it copies while the previous kernel
 // (usually the append's copy kernel) is still running: it reads only the
 // pinned buffer and writes only the device copy that the plan before the
-// previous one used, whose kernels are complete by the time the previous
-// kernel lets dependents launch (every kernel of the library does that only
-// after its own griddepcontrol.wait).  It then waits for the previous kernel
-// like any other, so the attention kernels after it see that kernel's
-// results.
+// previous one used.  The kernels of that older call are complete by the
+// time the previous kernel lets dependents launch: every kernel of the
+// library does so only after its own griddepcontrol.wait, except this upload
+// and the merge, which does so at its start but is itself launched only
+// after the partial kernel passed its wait, so that every kernel before the
+// merge's own call is complete.  It then waits for the previous kernel like
+// any other, so the attention kernels after it see that kernel's results.
 __global__ void __launch_bounds__(256) k_plan_upload(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                      int64_t n16) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)

@@ -410,14 +410,23 @@ __device__ __forceinline__ uint32_t tq_swz(int t, int d) {
 // Decodes coordinates 16 j .. 16 j + 15 of a record's unit-norm row: the
 // product of the angle factors on the path from the root (level 7) to each
 // coordinate, in that order.  tab: (cos, sin) of the bin centres, levels 7
-// down to 2 (8 each) then level 1 (16).
+// down to 2 (8 each) then level 1 (16).  The 3-bit codes come from two
+// 16-byte loads of record words 8..15 (stream word k is record word 9 + k):
+// level 2 nodes 4j..4j+3 at stream bit 12 j, level 3 nodes 2j, 2j+1 at
+// 96 + 6 j, level 4 node j at 144 + 3 j, level 5 node j/2 at 168 + 3 (j/2),
+// level 6 node j/4 at 180 + 3 (j/4), level 7 at 186.
 __device__ __forceinline__ void tq_decode16(const uint32_t* rec, int j, const float2* tab, uint4& lo, uint4& hi) {
-    auto bits = [&](int pos, int n) {
-        const int w = pos >> 5;
-        return __funnelshift_r(rec[9 + w], rec[10 + w], pos & 31) & ((1u << n) - 1u);
-    };
-    const uint32_t c7 = bits(186, 3), c6 = bits(180 + 3 * (j >> 2), 3), c5 = bits(168 + 3 * (j >> 1), 3);
-    const uint32_t c4 = bits(144 + 3 * j, 3), c3 = bits(96 + 6 * j, 6), c2 = bits(12 * j, 12);
+    const uint4 A = *reinterpret_cast<const uint4*>(rec + 8);
+    const uint4 B = *reinterpret_cast<const uint4*>(rec + 12);
+    const uint32_t s0 = A.y, s1 = A.z, s2 = A.w, s3 = B.x, s4 = B.y, s5 = B.z;
+    const uint32_t c7 = (s5 >> 26) & 7u;
+    const uint32_t c6 = (s5 >> (20 + 3 * (j >> 2))) & 7u;
+    const uint32_t c5 = (s5 >> (8 + 3 * (j >> 1))) & 7u;
+    const uint32_t c4 = (uint32_t)(((((uint64_t)s5) << 32) | s4) >> (16 + 3 * j)) & 7u;
+    const uint32_t c3 = (uint32_t)(((((uint64_t)s4) << 32) | s3) >> (6 * j)) & 63u;
+    const int p2 = 12 * j;
+    const uint32_t lo2 = p2 < 32 ? s0 : (p2 < 64 ? s1 : s2), hi2 = p2 < 32 ? s1 : (p2 < 64 ? s2 : s3);
+    const uint32_t c2 = __funnelshift_r(lo2, hi2, p2 & 31) & 0xFFFu;
     const uint32_t c1 = rec[1 + j];
     const float2 t7 = tab[c7], t6 = tab[8 + c6], t5 = tab[16 + c5], t4 = tab[24 + c4];
     float r = (j & 4) ? t7.y : t7.x;
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(128, 3) k_attn_partial_turbo(const AttnArgs a,
             // decode: pass p takes rows 4 p + lane / 8, level-4 node lane % 8
             {
                 const int j = lane & 7;
-#pragma unroll 1
+#pragma unroll 2
                 for (int pss = 0; pss < 8; ++pss) {
                     const int row = (pss & 3) * 4 + (lane >> 3);
                     const bool isv = pss >= 4;
@@ -559,8 +568,12 @@ __global__ void __launch_bounds__(128, 3) k_attn_partial_turbo(const AttnArgs a,
                     uint4 lo, hi;
                     tq_decode16(rec, j, tab, lo, hi);
                     unsigned char* d = isv ? dv : dk;
-                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j)) = lo;
-                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + 8)) = hi;
+                    // lanes 4..7 of a row store their upper chunk first: each
+                    // quarter-warp's eight 16-byte stores then fall in eight
+                    // distinct bank groups
+                    const bool up = j >= 4;
+                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + (up ? 8 : 0))) = up ? hi : lo;
+                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + (up ? 0 : 8))) = up ? lo : hi;
                 }
             }
             // per-token scalars of this lane's columns: tokens 2 (lane % 4) + e + 8 nt
