@@ -540,7 +540,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Q/K/V ~ N(0,1), seeded)",
         "config": dict(cfg, parallelism=f"replicas x{world}" if world > 1 else "single GPU",
-                       planning={-1: "host", 0: "units and CTA split on the device from 2048 units",
+                       planning={-1: "host", 0: "default (units and CTA split on the device for plans of "
+                                                 "2048+ units averaging under 32 tiles per unit)",
                                  1: "units and CTA split on the device"}[args.device_planning]),
         "roofline": roofline,
         "roofline_attention": attn_roof,
@@ -1160,7 +1161,7 @@ def main():
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
     ap.add_argument("--device-planning", type=int, default=0, choices=[-1, 0, 1],
                     help="bf16 attention plans: expand units and the CTA split on the device (1), on the host (-1), "
-                         "or on the device from 2048 units up (0, default)")
+                         "or by the library's default rule (0)")
     ap.add_argument("--fold-segments", type=int, default=0,
                     help="fold short shared segments into the ones that follow (0: default, k: below k percent "
                          "of the estimate, -1: off)")

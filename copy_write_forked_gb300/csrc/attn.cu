@@ -1144,6 +1144,11 @@ struct PlanHeader {
 // searches run over the segments' keys (weight, first tile, first unit),
 // which each CTA first copies to shared memory: kMaxExpandSegs segments at
 // most (the host checks).
+// It reads the segment list and header from the device copy the upload
+// wrote, after waiting for that upload.  (Reading them from the pinned host
+// buffer before the wait, to run alongside the append's copy, measured
+// slower on the stress plan: the dependent host reads cost more than the
+// overlap won.)
 constexpr int kMaxExpandCtas = 1024;
 constexpr int kMaxExpandSegs = 8192;
 constexpr int kExpandThreads = 256;
@@ -1158,7 +1163,6 @@ struct ExpandArgs {
     int32_t* tc_begin;
     int32_t* tc_cunit;
     int32_t* counts;     // [4]: CTAs of each class, partial rows (low, high)
-    const DevMeta* meta;
     int32_t nkv;
 };
 
@@ -1209,7 +1213,6 @@ __global__ void __launch_bounds__(kExpandThreads) k_plan_expand(const ExpandArgs
     asm volatile("griddepcontrol.wait;" ::: "memory");
     pdl_trigger();
     const int tid = threadIdx.x;
-    if (x.meta->status) return;
     const PlanHeader hdr = *x.hdr;
     const SegPlan* sp = x.sp;
     const int32_t nkv = x.nkv;
@@ -1329,42 +1332,43 @@ __global__ void __launch_bounds__(kExpandThreads) k_plan_expand(const ExpandArgs
     }
     // ------------------------------------------------------ this CTA's units
     const int32_t u = blockIdx.x * kExpandUnits + tid;
-    if (u >= hdr.n_units) return;
-    const int cls = u < hdr.cls[0].u_hi ? 0 : 1;
-    const PlanClass& pc = hdr.cls[cls];
-    const int32_t si = seg_search(pc.s_lo, pc.s_hi, [&](int32_t k) { return (int64_t)s_ub[k]; }, u);
-    const SegPlan g = sp[si];
-    const int32_t k = u - g.unit_base;
-    const int32_t h = k / g.ngroups, grp = k - h * g.ngroups;
-    const bool last = grp == g.ngroups - 1;
-    AttnUnit U;
-    U.seg = si;
-    U.kv_head = h;
-    U.row_lo = grp * g.group_rows;
-    U.n_rows = last ? g.rows_last : g.group_rows;
-    U.rt = last ? g.rt_last : g.rt_full;
-    U.tile_off = g.tile_base + k * g.n_blk;
-    // first CTA: begin[c] <= tile_off < begin[c + 1]; last CTA likewise for the last tile
-    const int32_t C = s_nc[cls];
-    auto cta_of = [&](int32_t t) {
-        int32_t lo = 0, hi = C - 1;
-        while (lo < hi) {
-            const int32_t mid = (lo + hi + 1) >> 1;
-            if (s_begin[cls][mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        return lo;
-    };
-    U.cfirst = cta_of(U.tile_off);
-    U.nchunks = cta_of(U.tile_off + g.n_blk - 1) - U.cfirst + 1;
-    const int32_t rows_per_head = (g.ngroups - 1) * g.group_rows + g.rows_last;
-    U.prow_base = g.row_base + h * rows_per_head + grp * g.group_rows + s_pre[cls][U.cfirst] +
-                  (cls == 1 ? s_pre[0][kMaxExpandCtas] : 0);
-    U.table_row = g.table_row;
-    U.blk_start = g.blk_start;
-    U.n_blk = g.n_blk;
-    U.mem_off = g.mem_off;
-    U.pad[0] = U.pad[1] = U.pad[2] = 0;
-    x.units[u] = U;
+    if (u < hdr.n_units) {
+        const int cls = u < hdr.cls[0].u_hi ? 0 : 1;
+        const PlanClass& pc = hdr.cls[cls];
+        const int32_t si = seg_search(pc.s_lo, pc.s_hi, [&](int32_t k) { return (int64_t)s_ub[k]; }, u);
+        const SegPlan g = sp[si];
+        const int32_t k = u - g.unit_base;
+        const int32_t h = k / g.ngroups, grp = k - h * g.ngroups;
+        const bool last = grp == g.ngroups - 1;
+        AttnUnit U;
+        U.seg = si;
+        U.kv_head = h;
+        U.row_lo = grp * g.group_rows;
+        U.n_rows = last ? g.rows_last : g.group_rows;
+        U.rt = last ? g.rt_last : g.rt_full;
+        U.tile_off = g.tile_base + k * g.n_blk;
+        // first CTA: begin[c] <= tile_off < begin[c + 1]; last CTA likewise for the last tile
+        const int32_t C = s_nc[cls];
+        auto cta_of = [&](int32_t t) {
+            int32_t lo = 0, hi = C - 1;
+            while (lo < hi) {
+                const int32_t mid = (lo + hi + 1) >> 1;
+                if (s_begin[cls][mid] <= t) lo = mid; else hi = mid - 1;
+            }
+            return lo;
+        };
+        U.cfirst = cta_of(U.tile_off);
+        U.nchunks = cta_of(U.tile_off + g.n_blk - 1) - U.cfirst + 1;
+        const int32_t rows_per_head = (g.ngroups - 1) * g.group_rows + g.rows_last;
+        U.prow_base = g.row_base + h * rows_per_head + grp * g.group_rows + s_pre[cls][U.cfirst] +
+                      (cls == 1 ? s_pre[0][kMaxExpandCtas] : 0);
+        U.table_row = g.table_row;
+        U.blk_start = g.blk_start;
+        U.n_blk = g.n_blk;
+        U.mem_off = g.mem_off;
+        U.pad[0] = U.pad[1] = U.pad[2] = 0;
+        x.units[u] = U;
+    }
 }
 
 // ============================================================ plan upload
@@ -1542,8 +1546,10 @@ int32_t class_ctas(int64_t weight, int max_ctas, const ClassWeights& cw) {
     return (int32_t)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + cw.min_per_cta - 1) / cw.min_per_cta));
 }
 
-// bf16 plans of at least this many units are expanded on the device by default
+// bf16 plans of at least this many units, with fewer tiles per unit than
+// this on average, are expanded on the device by default
 constexpr int32_t kDevicePlanMinUnits = 2048;
+constexpr int32_t kDevicePlanMaxTilesPerUnit = 32;
 
 // The plan's units, CTA partitions, partial rows and paths from the segments
 // in hp.psegs / hp.seg_members (hp.tiles and the arrays are rebuilt;
@@ -1561,18 +1567,27 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by
     // more than tc_min_rows rows per kv head, pass 1 the rest.
-    size_t n_units_total = 0, n_members_total = 0;
+    size_t n_units_total = 0, n_members_total = 0, n_tiles_total = 0;
     for (const Segment& sg : hp.psegs) {
         if ((int64_t)sg.n_members * RM >= (int64_t)1 << 24) return DENDRITE_ELIMIT;   // rows as exact fp32
         const int32_t rows_per_head = sg.n_members * RM;
         const int32_t group_rows = (tc_on && rows_per_head > p->tc_min_rows) ? kMaxUnitRowsTc : small_rows;
-        n_units_total += (size_t)nkv * ((rows_per_head + group_rows - 1) / group_rows);
+        const size_t units = (size_t)nkv * ((rows_per_head + group_rows - 1) / group_rows);
+        n_units_total += units;
+        n_tiles_total += units * (size_t)sg.block_count;
         n_members_total += sg.n_members;
     }
     if (n_units_total >= (size_t)INT32_MAX / 2) return DENDRITE_ELIMIT;
+    // By default only plans whose host expansion rivals the kernels' work go
+    // to the device: many units (the expansion's cost) of few tiles each (the
+    // kernels' work).  Elsewhere the host expansion hides behind the device's
+    // work, while the expansion kernel would sit between the upload and the
+    // partial kernels.
     hp.device = allow_device && bf16 && max_ctas <= kMaxExpandCtas && max_tc_ctas <= kMaxExpandCtas &&
                 hp.psegs.size() <= (size_t)kMaxExpandSegs &&
-                (p->device_planning > 0 || (p->device_planning == 0 && n_units_total >= (size_t)kDevicePlanMinUnits));
+                (p->device_planning > 0 ||
+                 (p->device_planning == 0 && n_units_total >= (size_t)kDevicePlanMinUnits &&
+                  n_tiles_total < (size_t)kDevicePlanMaxTilesPerUnit * n_units_total));
     hp.units.resize(n_units_total);
     hp.members.resize(n_members_total);
     hp.segs.reserve(hp.psegs.size());
@@ -1855,7 +1870,6 @@ int launch_plan_expand(dendrite_pool* p, char* d, const size_t* off, int32_t n_u
     x.tc_begin = reinterpret_cast<int32_t*>(d + off[9]);
     x.tc_cunit = reinterpret_cast<int32_t*>(d + off[10]);
     x.counts = reinterpret_cast<int32_t*>(d + off[11]);
-    x.meta = p->d_meta;
     x.nkv = p->n_kv;
     DENDRITE_CUDA(launch_pdl(k_plan_expand, dim3((unsigned)std::max(1, (n_units + kExpandUnits - 1) / kExpandUnits)),
                              dim3(kExpandThreads), (size_t)n_segs * 16, s, x));
@@ -2101,7 +2115,8 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         }
         DENDRITE_CUDA(cudaEventRecord(p->plan_copied[ib], s));
         // the other device copy holds an older plan's units: expand again
-        if (pc.device) DENDRITE_TRY(launch_plan_expand(p, p->d_plan[ib], pc.sec_off, pc.dev.n_units, pc.n_segplan, s));
+        if (pc.device)
+            DENDRITE_TRY(launch_plan_expand(p, p->d_plan[ib], pc.sec_off, pc.dev.n_units, pc.n_segplan, s));
         pc.dev = plan_rebase(pc.dev, p->d_plan[pc.buf], p->d_plan[ib]);
         pc.buf = ib;
         pc.version = p->version;

@@ -31,59 +31,85 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
                    std::vector<Segment>& segs, std::vector<int32_t>& members) {
     segs.clear();
     members.clear();
-    struct Rec { int32_t grp, cap, member; };
-    static thread_local std::vector<int32_t> slot, order, mem, count, first_block;
-    static thread_local std::vector<Rec> recs, sorted;
+    struct Rec { int32_t cap, member; };
+    static thread_local std::vector<int32_t> slot, order, cnt, cap0, cur, mem, first_block, flat;
+    static thread_local std::vector<char> mixed;
+    static thread_local std::vector<Rec> recs;
     slot.assign(n_nodes, -1);
     first_block.resize(n_nodes);   // a node's first own block (0 for a root)
     for (int32_t i = 0; i < n_nodes; ++i) first_block[i] = parent[i] >= 0 ? fork_len[i] / bs : 0;
     order.clear();
-    recs.clear();
-    // walk every queried branch up to its root: owner node -> [start, cap)
+    cnt.clear();
+    cap0.clear();
+    mixed.clear();
+    // Walk every queried branch up to its root (owner node -> [start, cap)),
+    // twice.  The first walk numbers the owners in first-visit order, counts
+    // each one's records and notes whether all its records share one cap;
+    // the second writes each owner's members (in increasing member order)
+    // into its own range, and their caps for owners with several.
+    int32_t n_rec = 0;
     for (int32_t qi = 0; qi < n_queried; ++qi) {
         int32_t node = queried[qi];
         int32_t cap = (len[node] + bs - 1) / bs;
         while (cap > 0) {
             const int32_t start = first_block[node];
             if (start < cap) {
-                if (slot[node] < 0) {
-                    slot[node] = (int32_t)order.size();
+                int32_t g = slot[node];
+                if (g < 0) {
+                    g = slot[node] = (int32_t)order.size();
                     order.push_back(node);
+                    cnt.push_back(0);
+                    cap0.push_back(cap);
+                    mixed.push_back(0);
                 }
-                recs.push_back({slot[node], cap, qi});
+                cnt[g]++;
+                mixed[g] |= cap != cap0[g];
+                ++n_rec;
             }
             if (parent[node] < 0) break;
             cap = std::min(cap, start);
             node = parent[node];
         }
     }
-    // group by owner (first-visit order) with one counting pass; within a
-    // group the records stay in increasing member order
     const int32_t n_grp = (int32_t)order.size();
-    count.assign(n_grp + 1, 0);
-    for (const Rec& r : recs) count[r.grp + 1]++;
-    for (int32_t g = 0; g < n_grp; ++g) count[g + 1] += count[g];
-    sorted.resize(recs.size());
+    cur.resize(n_grp + 1);
+    cur[0] = 0;
+    for (int32_t g = 0; g < n_grp; ++g) cur[g + 1] = cur[g] + cnt[g];
+    flat.resize(n_rec);
+    recs.resize(n_rec);
     {
-        static thread_local std::vector<int32_t> cursor;
-        cursor.assign(count.begin(), count.end() - 1);
-        for (const Rec& r : recs) sorted[cursor[r.grp]++] = r;
+        static thread_local std::vector<int32_t> pos;
+        pos.assign(cur.begin(), cur.end() - 1);
+        for (int32_t qi = 0; qi < n_queried; ++qi) {
+            int32_t node = queried[qi];
+            int32_t cap = (len[node] + bs - 1) / bs;
+            while (cap > 0) {
+                const int32_t start = first_block[node];
+                if (start < cap) {
+                    const int32_t g = slot[node];
+                    const int32_t at = pos[g]++;
+                    flat[at] = qi;
+                    if (mixed[g]) recs[at] = Rec{cap, qi};
+                }
+                if (parent[node] < 0) break;
+                cap = std::min(cap, start);
+                node = parent[node];
+            }
+        }
     }
-    members.reserve(recs.size());
+    members.reserve(n_rec);
     for (int32_t gi = 0; gi < n_grp; ++gi) {
-        const size_t g0 = count[gi], g1 = count[gi + 1];
+        const int32_t g0 = cur[gi], g1 = cur[gi + 1];
         const int32_t node = order[gi];
         const int32_t start = first_block[node];
-        bool uniform = true;
-        for (size_t k = g0 + 1; k < g1 && uniform; ++k) uniform = sorted[k].cap == sorted[g0].cap;
-        if (uniform) {   // every member reads [start, cap): one segment, members already in order
+        if (!mixed[gi]) {   // every member reads [start, cap): one segment, members already in order
             Segment sg;
             sg.block_start = start;
-            sg.block_count = sorted[g0].cap - start;
+            sg.block_count = cap0[gi] - start;
             sg.member_offset = (int32_t)members.size();
-            for (size_t k = g0; k < g1; ++k) members.push_back(sorted[k].member);
-            sg.n_members = (int32_t)(g1 - g0);
-            sg.rep_node = queried[sorted[g0].member];
+            members.insert(members.end(), flat.begin() + g0, flat.begin() + g1);
+            sg.n_members = g1 - g0;
+            sg.rep_node = queried[flat[g0]];
             sg.owner = node;
             segs.push_back(sg);
             continue;
@@ -91,19 +117,19 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
         // caps descending (members ascending within a cap); the ascending
         // cuts then take the smallest cap first, and the members of
         // [lo, cut) are the records with cap >= cut, a prefix of the group
-        std::stable_sort(sorted.begin() + g0, sorted.begin() + g1,
+        std::stable_sort(recs.begin() + g0, recs.begin() + g1,
                          [](const Rec& a, const Rec& b) { return a.cap > b.cap; });
         int32_t lo = start;
-        size_t end = g1;
+        int32_t end = g1;
         while (end > g0) {
-            const int32_t cut = sorted[end - 1].cap;
+            const int32_t cut = recs[end - 1].cap;
             if (cut > lo) {
                 Segment sg;
                 sg.block_start = lo;
                 sg.block_count = cut - lo;
                 sg.member_offset = (int32_t)members.size();
                 mem.clear();
-                for (size_t k = g0; k < end; ++k) mem.push_back(sorted[k].member);
+                for (int32_t k = g0; k < end; ++k) mem.push_back(recs[k].member);
                 std::sort(mem.begin(), mem.end());
                 members.insert(members.end(), mem.begin(), mem.end());
                 sg.n_members = (int32_t)mem.size();
@@ -112,7 +138,7 @@ void plan_segments(int32_t n_nodes, const int32_t* parent, const int32_t* fork_l
                 segs.push_back(sg);
                 lo = cut;
             }
-            while (end > g0 && sorted[end - 1].cap == cut) --end;
+            while (end > g0 && recs[end - 1].cap == cut) --end;
         }
     }
 }
@@ -151,11 +177,9 @@ int64_t group_unit_ns(bool tc, int32_t rows) { return (tc ? 3000 : 1000) + 29 * 
 int64_t estimate_ns(const FoldParams& fp, int64_t T, int64_t R, bool with_units) {
     const bool tc = fp.tc_rows >= 0 && R > fp.tc_rows;
     const int32_t g = tc ? kMaxUnitRowsTc : fp.small_rows;
-    int64_t ns = 0;
-    for (int64_t r0 = 0; r0 < R; r0 += g) {
-        const int32_t rows = (int32_t)std::min<int64_t>(g, R - r0);
-        ns += T * group_block_ns(tc, rows) + (with_units ? group_unit_ns(tc, rows) : 0);
-    }
+    const int64_t full = R / g, rem = R - full * g;
+    int64_t ns = full * (T * group_block_ns(tc, g) + (with_units ? group_unit_ns(tc, g) : 0));
+    if (rem) ns += T * group_block_ns(tc, (int32_t)rem) + (with_units ? group_unit_ns(tc, (int32_t)rem) : 0);
     return ns;
 }
 
@@ -206,34 +230,31 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
     }
     // the segments after each segment, and the members whose blocks end there
     koff.assign(S + 1, 0);
-    eoff.assign(S + 1, 0);
-    for (int32_t si = 0; si < S; ++si) {
-        if (prev[si] >= 0) koff[prev[si] + 1]++;
-        const Segment& sg = segs[si];
-        const int32_t end = sg.block_start + sg.block_count;
-        for (int32_t k = 0; k < sg.n_members; ++k)
-            if (qblocks[members[sg.member_offset + k]] == end) eoff[si + 1]++;
+    eoff.resize(S + 1);
+    emem.resize(members.size());
+    {
+        int32_t e = 0;
+        for (int32_t si = 0; si < S; ++si) {   // members stay in ascending order within a segment
+            if (prev[si] >= 0) koff[prev[si] + 1]++;
+            const Segment& sg = segs[si];
+            const int32_t end = sg.block_start + sg.block_count;
+            eoff[si] = e;
+            const int32_t* mp = members.data() + sg.member_offset;
+            for (int32_t k = 0; k < sg.n_members; ++k) {
+                const int32_t m = mp[k];
+                emem[e] = m;
+                e += qblocks[m] == end;
+            }
+        }
+        eoff[S] = e;
     }
-    for (int32_t si = 0; si < S; ++si) {
-        koff[si + 1] += koff[si];
-        eoff[si + 1] += eoff[si];
-    }
+    for (int32_t si = 0; si < S; ++si) koff[si + 1] += koff[si];
     kseg.resize(koff[S]);
-    emem.resize(eoff[S]);
     {
         static thread_local std::vector<int32_t> kc;
         kc.assign(koff.begin(), koff.end() - 1);
         for (int32_t si = 0; si < S; ++si)
             if (prev[si] >= 0) kseg[kc[prev[si]]++] = si;
-        int32_t e = 0;
-        for (int32_t si = 0; si < S; ++si) {   // members stay in ascending order within a segment
-            const Segment& sg = segs[si];
-            const int32_t end = sg.block_start + sg.block_count;
-            for (int32_t k = 0; k < sg.n_members; ++k) {
-                const int32_t m = members[sg.member_offset + k];
-                if (qblocks[m] == end) emem[e++] = m;
-            }
-        }
     }
     // decide in increasing block order
     {

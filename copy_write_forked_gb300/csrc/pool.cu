@@ -415,50 +415,16 @@ __global__ void __launch_bounds__(128, 16) k_append_copy(const __grid_constant__
 }
 
 // ------------------------------------------------------- free / truncate
-// One thread per released table entry (branch i releases its entries
-// [start_i, start_i + count_i)) drops one reference and clears the entry; an
-// entry whose refcount reaches zero marks its block released.  The last CTA
-// to finish then pushes the released blocks onto the free stack in
-// descending id order (a block scan over [rel_lo, rel_hi] from the top down).
-template <typename A>
-__global__ void __launch_bounds__(kFreeCollectThreads)
-k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, int32_t n_blocks, int32_t* table,
-       int32_t* refcount, int32_t* released, int32_t* stack, DevMeta* meta) {
+// The end of a free kernel: thread (rel, blk) released block blk if rel.  One
+// lane per warp folds the warp's released ids into the call's range; the last
+// CTA to finish pushes the released blocks onto the free stack in descending
+// id order (a block scan over [rel_lo, rel_hi] from the top down).
+__device__ __forceinline__ void free_collect(bool rel, int32_t blk, int32_t* released, int32_t* stack,
+                                             DevMeta* meta, int32_t n_blocks) {
     __shared__ int32_t warp_sums[kFreeCollectThreads / 32];
     __shared__ int32_t chunk_total;
     __shared__ int32_t st, is_last, lo, hi, top0, cnt;
-    pdl_wait();
-    // args: branch[n], entry prefix[n], first released entry[n]
-    const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
-    int32_t* slot = nullptr;
-    int32_t blk = -1;
-    if (e < total) {
-        int32_t l = 0, h = n - 1;
-        while (l < h) {
-            const int32_t mid = (l + h + 1) >> 1;
-            if (args[n + mid] <= e) l = mid; else h = mid - 1;
-        }
-        slot = table + (int64_t)args[l] * bpb + args[2 * n + l] + (e - args[n + l]);
-        blk = *slot;   // loaded together with the status word; nothing is written before it is checked
-    }
-    // one decision per CTA (a status set by another CTA meanwhile may be seen
-    // by some threads only)
-    if (__syncthreads_or(*reinterpret_cast<volatile const int32_t*>(&meta->status) != 0)) return;
-    bool rel = false;
-    if (slot) {
-        *slot = -1;
-        if ((uint32_t)blk >= (uint32_t)n_blocks) {
-            set_status(meta, DENDRITE_ECORRUPT);
-        } else {
-            const int32_t old = atomicSub(refcount + blk, 1);
-            if (old == 1) {
-                released[blk] = 1;
-                rel = true;
-            } else if (old < 1) {
-                set_status(meta, DENDRITE_ECORRUPT);
-            }
-        }
-    }
+    const int32_t n_ctas = (int32_t)(gridDim.x * gridDim.y);
     // one lane per warp folds the warp's released ids into the call's range
     {
         const unsigned m = __ballot_sync(0xffffffffu, rel);
@@ -478,12 +444,12 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
         // its threads' updates.  Otherwise one acquire-release increment both
         // publishes this CTA's updates (ordered before it by the barrier) and,
         // in the last CTA, makes every other CTA's updates visible.
-        if (gridDim.x == 1) {
+        if (n_ctas == 1) {
             is_last = 1;
         } else {
             int32_t prev;
             asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(&meta->rel_done) : "memory");
-            is_last = prev == (int32_t)gridDim.x - 1;
+            is_last = prev == n_ctas - 1;
         }
         if (is_last) {
             volatile DevMeta* vm = meta;
@@ -497,13 +463,34 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
     __syncthreads();
     if (!is_last) return;
     if (!st && cnt > 0) {
+        // the flags of [lo, hi] in 32-flag groups aligned to 32, from the top
+        // group down: thread t of a pass takes one group (eight 16-byte
+        // loads), and a block scan of the groups' counts places its released
+        // ids, highest first.  Flags outside [lo, hi] are zero.
         int32_t carry = 0;
-        for (int32_t base = 0; base <= hi - lo; base += blockDim.x) {
-            const int32_t j = hi - (base + (int32_t)threadIdx.x);
-            const int32_t f = (j >= lo) ? __ldcg(released + j) : 0;
-            const int32_t ex = block_exclusive_scan<kFreeCollectThreads>(f, warp_sums, &chunk_total);
-            if (f) {
-                stack[top0 + carry + ex] = j;
+        const int32_t g_hi = hi >> 5, g_lo = lo >> 5;
+        for (int32_t g0 = g_hi; g0 >= g_lo; g0 -= (int32_t)blockDim.x) {
+            const int32_t g = g0 - (int32_t)threadIdx.x;
+            uint32_t mask = 0;   // bit k: flag of id 32 g + k
+            if (g >= g_lo) {
+                const int32_t b0 = g << 5;
+                if (b0 + 32 <= n_blocks) {
+                    const int4* f4 = reinterpret_cast<const int4*>(released + b0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int4 f = __ldcg(f4 + q);
+                        mask |= ((uint32_t)(f.x != 0) | ((uint32_t)(f.y != 0) << 1) | ((uint32_t)(f.z != 0) << 2) |
+                                 ((uint32_t)(f.w != 0) << 3)) << (4 * q);
+                    }
+                } else {
+                    for (int k = 0; b0 + k < n_blocks && k < 32; ++k) mask |= (uint32_t)(__ldcg(released + b0 + k) != 0) << k;
+                }
+            }
+            const int32_t ex = block_exclusive_scan<kFreeCollectThreads>(__popc(mask), warp_sums, &chunk_total);
+            int32_t o = top0 + carry + ex;
+            for (uint32_t m = mask; m; m &= ~(1u << (31 - __clz(m)))) {   // highest id first
+                const int32_t j = (g << 5) + (31 - __clz(m));
+                stack[o++] = j;
                 released[j] = 0;
             }
             carry += chunk_total;
@@ -517,6 +504,105 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
         meta->rel_count = 0;
         meta->rel_done = 0;
     }
+}
+
+// One thread per released table entry (branch i releases its entries
+// [start_i, start_i + count_i)) drops one reference and clears the entry; an
+// entry whose refcount reaches zero marks its block released.  The last CTA
+// to finish then pushes the released blocks onto the free stack in
+// descending id order (a block scan over [rel_lo, rel_hi] from the top down).
+template <typename A>
+__global__ void __launch_bounds__(kFreeCollectThreads)
+k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, int32_t n_blocks, int32_t* table,
+       int32_t* refcount, int32_t* released, int32_t* stack, DevMeta* meta) {
+    pdl_wait();
+    // args: branch[n], entry prefix[n], first released entry[n]
+    const int32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+    int32_t* slot = nullptr;
+    int32_t blk = -1;
+    if (e < total) {
+        int32_t l = 0, h = n - 1;
+        while (l < h) {
+            const int32_t mid = (l + h + 1) >> 1;
+            if (args[n + mid] <= e) l = mid; else h = mid - 1;
+        }
+        slot = table + (int64_t)args[l] * bpb + args[2 * n + l] + (e - args[n + l]);
+        blk = *slot;   // loaded together with the status word; nothing is written before it is checked
+    }
+    // one decision per CTA, from one status load (a status set by another
+    // CTA meanwhile may be seen by some CTAs only)
+    if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile const int32_t*>(&meta->status) != 0))
+        return;
+    bool rel = false;
+    if (slot) {
+        *slot = -1;
+        if ((uint32_t)blk >= (uint32_t)n_blocks) {
+            set_status(meta, DENDRITE_ECORRUPT);
+        } else {
+            const int32_t old = atomicSub(refcount + blk, 1);
+            if (old == 1) {
+                released[blk] = 1;
+                rel = true;
+            } else if (old < 1) {
+                set_status(meta, DENDRITE_ECORRUPT);
+            }
+        }
+    }
+    free_collect(rel, blk, released, stack, meta, n_blocks);
+}
+
+// Frees of many branches whose rows share blocks (siblings of one prompt): a
+// CTA takes 32 branches x 32 of their entries.  Warp w reads and clears
+// branch w's entries (coalesced); transposed through shared memory, warp w
+// then takes entry w of the 32 branches, and lanes holding the same block
+// drop their references with one atomic.  args as for k_free;
+// blockIdx.y: entry chunk.
+template <typename A>
+__global__ void __launch_bounds__(kFreeCollectThreads)
+k_free_tiles(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, int32_t n_blocks,
+             int32_t* table, int32_t* refcount, int32_t* released, int32_t* stack, DevMeta* meta) {
+    static_assert(kFreeCollectThreads == 1024, "one warp per branch row of a 32 x 32 tile");
+    __shared__ int32_t tile[32][33];
+    pdl_wait();
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t i = blockIdx.x * 32 + w;
+    const int32_t pos = blockIdx.y * 32 + lane;
+    int32_t* slot = nullptr;
+    int32_t blk = -1;
+    if (i < n) {
+        const int32_t c0 = args[n + i], c1 = i + 1 < n ? args[n + i + 1] : total;
+        if (pos < c1 - c0) {
+            slot = table + (int64_t)args[i] * bpb + args[2 * n + i] + pos;
+            blk = *slot;
+        }
+    }
+    if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile const int32_t*>(&meta->status) != 0))
+        return;
+    if (slot) {
+        *slot = -1;
+        if ((uint32_t)blk >= (uint32_t)n_blocks) {
+            set_status(meta, DENDRITE_ECORRUPT);
+            blk = -1;
+        }
+    } else {
+        blk = -1;
+    }
+    tile[w][lane] = blk;
+    __syncthreads();
+    const int32_t b = tile[lane][w];
+    const unsigned grp = __match_any_sync(0xffffffffu, b);
+    bool rel = false;
+    if (b >= 0 && lane == __ffs(grp) - 1) {
+        const int32_t c = __popc(grp);
+        const int32_t old = atomicSub(refcount + b, c);
+        if (old == c) {
+            released[b] = 1;
+            rel = true;
+        } else if (old < c) {
+            set_status(meta, DENDRITE_ECORRUPT);
+        }
+    }
+    free_collect(rel, b, released, stack, meta, n_blocks);
 }
 
 }  // namespace
@@ -1146,9 +1232,15 @@ namespace {
 int release_entries(dendrite_pool* p, const int32_t* branches, const int32_t* start, const int32_t* end,
                     int32_t n, cudaStream_t s) {
     int64_t total = 0;
-    for (int32_t i = 0; i < n; ++i) total += end[i] - start[i];
+    int32_t max_count = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        total += end[i] - start[i];
+        max_count = std::max(max_count, end[i] - start[i]);
+    }
     if (total > INT32_MAX / 2) return DENDRITE_ELIMIT;
     if (total == 0) return DENDRITE_OK;
+    // many branches: 32 x 32 tiles (one atomic per block shared within a tile)
+    const bool tiles = n >= 32 && (max_count + 31) / 32 <= 65535;
     auto fill = [&](int32_t* a) {
         int32_t acc = 0;
         for (int32_t i = 0; i < n; ++i) {
@@ -1160,6 +1252,14 @@ int release_entries(dendrite_pool* p, const int32_t* branches, const int32_t* st
     };
     const unsigned grid = (unsigned)((total + kFreeCollectThreads - 1) / kFreeCollectThreads);
     auto launch = [&](auto args) -> int {
+        if (tiles) {
+            DENDRITE_CUDA(launch_pdl(k_free_tiles<decltype(args)>,
+                                     dim3((unsigned)((n + 31) / 32), (unsigned)((max_count + 31) / 32)),
+                                     dim3(kFreeCollectThreads), 0, s, args, n, (int32_t)total, p->bpb,
+                                     (int32_t)p->num_blocks, p->d_table, p->d_refcount, p->d_released, p->d_stack,
+                                     p->d_meta));
+            return DENDRITE_OK;
+        }
         DENDRITE_CUDA(launch_pdl(k_free<decltype(args)>, dim3(grid), dim3(kFreeCollectThreads), 0, s, args, n,
                                  (int32_t)total, p->bpb, (int32_t)p->num_blocks, p->d_table, p->d_refcount,
                                  p->d_released, p->d_stack, p->d_meta));

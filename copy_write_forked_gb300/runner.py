@@ -12,14 +12,18 @@ from .dendrite import Pool
 
 
 def run_script(pool: Pool, w, device="cuda", stop: Optional[int] = None, stream=None,
-               split_layers: bool = False, layer_order=None) -> Dict[int, int]:
-    """Replays ``w`` on ``pool``.  On a pool of several layers every append
-    carries all layers: in one call, or with ``split_layers`` as
-    ``append_begin`` followed by one ``append_layer`` per layer (in
-    ``layer_order``, default ascending)."""
-    h: Dict[int, int] = {}
+               split_layers: bool = False, layer_order=None, start: int = 0,
+               handles: Optional[Dict[int, int]] = None) -> Dict[int, int]:
+    """Replays ``w`` on ``pool`` (ops ``start`` .. ``stop``; ``handles`` maps
+    the logical ids of earlier ops, and is updated in place).  On a pool of
+    several layers every append carries all layers: in one call, or with
+    ``split_layers`` as ``append_begin`` followed by one ``append_layer`` per
+    layer (in ``layer_order``, default ascending)."""
+    h: Dict[int, int] = handles if handles is not None else {}
     nl = getattr(pool, "n_layers", 1)
     for idx, op in enumerate(w.ops[:stop]):
+        if idx < start:
+            continue
         if op.kind == "new":
             h[op.branches[0]] = pool.new_branch()
         elif op.kind == "fork":

@@ -90,10 +90,12 @@ typedef struct dendrite_pool_opts {
                                     * below k percent; -1 = never.                        */
     int32_t device_planning;       /* bf16 attention plans: expand the sharing segments   *
                                     * into work units and split them over CTAs on the GPU *
-                                    * (a one-CTA kernel before the partial kernels) rather *
-                                    * than on the host.  0 = default (plans of at least   *
-                                    * 2048 units), 1 = always, -1 = never.  The result is *
-                                    * the same plan either way.                           */
+                                    * (a kernel between the plan upload and the partial   *
+                                    * kernels) rather than on the host.  0 = default      *
+                                    * (plans of at least 2048 units averaging fewer than  *
+                                    * 32 tiles per unit, whose host expansion rivals the  *
+                                    * kernels' work), 1 = always, -1 = never.  The result *
+                                    * is the same plan either way.                        */
     int32_t reserved[2];           /* must be zero                                         */
 } dendrite_pool_opts;
 

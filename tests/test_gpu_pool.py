@@ -149,6 +149,47 @@ def test_large_fork_batch_uses_device_argument_path():
     pool.close()
 
 
+def test_batched_forks_and_frees_of_siblings_match_oracle():
+    """The shape of a decode step over many leaves that share two prompts'
+    prefixes: every step forks each of 300 leaves once (one call of 300
+    pairs), appends one token to every child (a copy of each leaf's partial
+    tail) and frees the 300 old leaves in one call; finally everything is
+    freed in one call.  Calls of this size take the tiled fork and free
+    kernels, whose lanes drop or take the references of a block shared
+    within a tile with one atomic; tables, refcounts, the free stack and
+    every valid slot match O2 after each step, and the last free returns
+    every block to the stack."""
+    ops = [W.Op("new", (0,)), W.Op("new", (1,)), W.Op("append", (0, 1), 100),
+           W.Op("fork", (0, 1), children=(tuple(range(2, 152)), tuple(range(152, 302)))),
+           W.Op("append", tuple(range(2, 302)), 5)]
+    leaves = list(range(2, 302))
+    nxt = 302
+    checkpoints = []
+    for step in range(3):
+        kids = tuple(range(nxt, nxt + len(leaves)))
+        nxt += len(leaves)
+        ops.append(W.Op("fork", tuple(leaves), children=tuple((c,) for c in kids)))
+        ops.append(W.Op("append", kids, 1))
+        ops.append(W.Op("free", tuple(leaves)))
+        leaves = list(kids)
+        checkpoints.append(len(ops))
+    ops.append(W.Op("free", tuple([0, 1] + leaves)))
+    checkpoints.append(len(ops))
+    w = W.Workload("siblings", 2, 8, 128, 16, torch.bfloat16, ops, (0,))
+    pool = pool_for(w, max_branches=nxt + 8)
+    h = {}
+    done = 0
+    for stop in checkpoints:
+        run_script(pool, w, stop=stop, start=done, handles=h)
+        done = stop
+        ref = run_script_pool(w, pool.num_blocks, kv_source=_gpu_kv(w), stop=stop)
+        pool.sync()
+        pool_state_matches(pool, h, ref)
+    assert sorted(pool.read_free_stack()) == list(range(pool.num_blocks))
+    assert sum(pool.read_refcounts()) == 0
+    pool.close()
+
+
 def test_exhausted_pool_applies_nothing_and_is_sticky():
     pool = Pool(6, 16, 1, 128, torch.bfloat16, max_branches=8, max_blocks_per_branch=8)
     r = pool.new_branch()
