@@ -1895,6 +1895,23 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
         std::memcpy(&mk, p->tmap_k[layer].bytes, sizeof(mk));
         std::memcpy(&mv, p->tmap_v[layer].bytes, sizeof(mv));
     }
+    // Both partial classes: the tcgen05 and the mma.sync kernel write
+    // disjoint partial rows and read only the plan and the pool, so the
+    // mma.sync kernel runs on the pool's side stream beside the tcgen05 one
+    // (its CTAs take the SMs that the tcgen05 kernel's first CTAs to finish
+    // leave), and the caller's stream waits for it before the merge.
+    const bool beside = bf16 && a.plan.n_tc_ctas > 0 && a.plan.n_ctas > 0 && p->side;
+    if (beside) {
+        DENDRITE_CUDA(cudaEventRecord(p->ev_fork, s));
+        DENDRITE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+        prof_begin(p, T_ATTN_MMA_SIDE, p->side);
+        k_attn_partial_bf16<<<dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, p->side>>>(mk, mv, a);
+        DENDRITE_CUDA(cudaGetLastError());
+        prof_end(p, T_ATTN_MMA_SIDE, p->side);
+        DENDRITE_CUDA(cudaEventRecord(p->ev_join, p->side));
+    } else {
+        p->ev_recorded[T_ATTN_MMA_SIDE] = false;
+    }
     if (a.plan.n_tc_ctas > 0) {
         prof_begin(p, T_ATTN_TC, s);
         DENDRITE_TRY(launch_attn_tc(mk, mv, a, a.plan.n_tc_ctas, s));
@@ -1902,8 +1919,11 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     } else {
         p->ev_recorded[T_ATTN_TC] = false;   // this call ran no tensor-core kernel
     }
+    if (beside) DENDRITE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));
     const int32_t n_out_rows = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
-    if (p->dtype == DENDRITE_TURBO) {
+    if (beside) {
+        // launched above
+    } else if (p->dtype == DENDRITE_TURBO) {
         DENDRITE_TRY(launch_turbo_partials(a, a.Q, n_out_rows, p->d_tq_signs, p->d_tq_S, p->d_tq_qs, s));
     } else if (a.plan.n_ctas > 0) {
         if (bf16) {
@@ -1916,6 +1936,13 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     prof_end(p, T_ATTN_PARTIAL, s);
     prof_begin(p, T_ATTN_MERGE, s);
     {
+        // after a join from the side stream the merge is an ordinary launch:
+        // its dependence is on an event, not on the previous kernel alone
+        auto mlaunch = [&](auto kernel, unsigned g) -> cudaError_t {
+            if (!beside) return launch_pdl(kernel, dim3(g), dim3(256), 0, s, a);
+            kernel<<<dim3(g), dim3(256), 0, s>>>(a);
+            return cudaGetLastError();
+        };
         const int32_t n_out = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
         const unsigned grid = (unsigned)((n_out + 7) / 8);
         const int G = a.plan.group;
@@ -1925,21 +1952,21 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
         // row per warp, where the warps' latency chains overlap better
         if (p->dtype == DENDRITE_TURBO) {
             // rows of compressed pools are rotated back by the per-row merge
-            DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16, true>, dim3(grid), dim3(256), 0, s, a));
+            DENDRITE_CUDA(mlaunch(k_attn_merge<__nv_bfloat16, true>, grid));
         } else if (p->head_dim == D && ng > 0 && (int64_t)n_out / ng >= (int64_t)16 * p->sm_count) {
             const unsigned ggrid = (unsigned)((n_out / ng + 7) / 8);
             if (bf16) {
-                if (ng == 4) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 4>, dim3(ggrid), dim3(256), 0, s, a));
-                else if (ng == 2) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 2>, dim3(ggrid), dim3(256), 0, s, a));
-                else DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<__nv_bfloat16, 1>, dim3(ggrid), dim3(256), 0, s, a));
+                if (ng == 4) DENDRITE_CUDA(mlaunch(k_attn_merge_grouped<__nv_bfloat16, 4>, ggrid));
+                else if (ng == 2) DENDRITE_CUDA(mlaunch(k_attn_merge_grouped<__nv_bfloat16, 2>, ggrid));
+                else DENDRITE_CUDA(mlaunch(k_attn_merge_grouped<__nv_bfloat16, 1>, ggrid));
             } else {
-                if (ng == 4) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<float, 4>, dim3(ggrid), dim3(256), 0, s, a));
-                else if (ng == 2) DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<float, 2>, dim3(ggrid), dim3(256), 0, s, a));
-                else DENDRITE_CUDA(launch_pdl(k_attn_merge_grouped<float, 1>, dim3(ggrid), dim3(256), 0, s, a));
+                if (ng == 4) DENDRITE_CUDA(mlaunch(k_attn_merge_grouped<float, 4>, ggrid));
+                else if (ng == 2) DENDRITE_CUDA(mlaunch(k_attn_merge_grouped<float, 2>, ggrid));
+                else DENDRITE_CUDA(mlaunch(k_attn_merge_grouped<float, 1>, ggrid));
             }
-        } else if (bf16) DENDRITE_CUDA(launch_pdl(k_attn_merge<__nv_bfloat16, true>, dim3(grid), dim3(256), 0, s, a));
-        else if (p->head_dim == D) DENDRITE_CUDA(launch_pdl(k_attn_merge<float, true>, dim3(grid), dim3(256), 0, s, a));
-        else DENDRITE_CUDA(launch_pdl(k_attn_merge<float, false>, dim3(grid), dim3(256), 0, s, a));
+        } else if (bf16) DENDRITE_CUDA(mlaunch(k_attn_merge<__nv_bfloat16, true>, grid));
+        else if (p->head_dim == D) DENDRITE_CUDA(mlaunch(k_attn_merge<float, true>, grid));
+        else DENDRITE_CUDA(mlaunch(k_attn_merge<float, false>, grid));
     }
     prof_end(p, T_ATTN_MERGE, s);
     prof_end(p, T_ATTN_TOTAL, s);

@@ -160,7 +160,7 @@ private:
 };
 
 enum TimingKind { T_FORK = 0, T_APPEND_META, T_APPEND_COPY, T_ATTN_PARTIAL, T_ATTN_MERGE, T_FREE,
-                  T_ATTN_TOTAL, T_ATTN_TC, T_COUNT };
+                  T_ATTN_TOTAL, T_ATTN_TC, T_ATTN_MMA_SIDE, T_COUNT };
 
 // 128-byte opaque CUtensorMap storage.
 struct alignas(64) TensorMapBlob {
@@ -264,6 +264,10 @@ struct dendrite_pool {
     char* h_plan[2] = {nullptr, nullptr};      // pinned, used alternately by plan builds
     size_t h_plan_cap = 0;                     // capacity of each
     cudaEvent_t plan_copied[2] = {nullptr, nullptr};
+    // the mma.sync partial kernel runs beside the tcgen05 one on this stream
+    // (forked from and joined back into the caller's stream)
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int plan_buf = 0;                          // buffer the next plan build packs into
     float* d_partial = nullptr;      // partial rows: [rows][head_dim] acc then [rows][2] (m, l)
     size_t partial_rows_cap = 0;

@@ -264,7 +264,36 @@ k_append_meta(const __grid_constant__ A args, int32_t n, int32_t n_new, int32_t 
         __syncthreads();
     }
     const bool fits = carry <= top0;
-    if (fits) {
+    // small appends with one branch per thread (decode steps: one token, at
+    // most a copied tail and one new block each): every thread writes its own
+    // branch's entries, so the whole call is one round of stack reads instead
+    // of one per branch of a warp
+    int32_t my_demand = 0;
+    if (one && t < n) {
+        const int32_t L = args[n + t];
+        my_demand = (my_src >= 0) + (L + n_new + bs - 1) / bs - (L + bs - 1) / bs;
+    }
+    const bool per_thread = one && !__syncthreads_or(my_demand > 4);
+    if (fits && per_thread) {
+        if (t < n) {
+            const int32_t b = args[t], L = args[n + t];
+            int32_t o = my_off;
+            int32_t* row = table + (int64_t)b * bpb;
+            if (my_src >= 0) {
+                const int32_t blk = stack[top0 - 1 - o];
+                atomicSub(refcount + my_src, 1);
+                refcount[blk] = 1;
+                row[L / bs] = blk;
+                ++o;
+            }
+            const int32_t nb0 = (L + bs - 1) / bs, nb1 = (L + n_new + bs - 1) / bs;
+            for (int32_t j = nb0; j < nb1; ++j) {
+                const int32_t blk = stack[top0 - 1 - (o + j - nb0)];
+                refcount[blk] = 1;
+                row[j] = blk;
+            }
+        }
+    } else if (fits) {
         for (int32_t base = 0; base < n; base += NT) {
             const int32_t i = base + t;
             if (i < n) {
@@ -1030,7 +1059,10 @@ int pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int3
         if (cudaEventCreate(&p->ev[k][0]) != cudaSuccess || cudaEventCreate(&p->ev[k][1]) != cudaSuccess)
             return fail(cuda_err(cudaErrorUnknown));
     if (cudaEventCreateWithFlags(&p->plan_copied[0], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p->plan_copied[1], cudaEventDisableTiming) != cudaSuccess)
+        cudaEventCreateWithFlags(&p->plan_copied[1], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess)
         return fail(cuda_err(cudaErrorUnknown));
     k_init<<<std::max(1, std::min(4 * p->sm_count, (int)((num_blocks + 255) / 256))), 256>>>(
         p->d_stack, p->d_refcount, p->d_holders, p->d_last, p->d_released, num_blocks, p->d_table,
@@ -1077,6 +1109,9 @@ int dendrite_pool_destroy(dendrite_pool* p) {
             if (p->ev[k][j]) cudaEventDestroy(p->ev[k][j]);
     for (cudaEvent_t e : p->plan_copied)
         if (e) cudaEventDestroy(e);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->side) cudaStreamDestroy(p->side);
     cudaGetLastError();
     delete p;
     return DENDRITE_OK;

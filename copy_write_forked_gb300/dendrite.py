@@ -24,7 +24,7 @@ ERRORS = {
     -6: "ECUDA", -7: "ETIMEOUT", -8: "ECORRUPT",
 }
 TIMING_NAMES = ("fork", "append_meta", "append_copy", "attn_partial", "attn_merge", "free", "attn_total",
-                "attn_tc")
+                "attn_tc", "attn_mma_side")
 FP32, BF16, TURBO = 0, 1, 2
 TURBO_KEY_BYTES, TURBO_VALUE_BYTES = 96, 64
 

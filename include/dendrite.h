@@ -332,9 +332,11 @@ int dendrite_pool_info(dendrite_pool* pool, int64_t* num_blocks, int32_t* block_
  *   ms[0] fork, ms[1] append metadata, ms[2] append copy/scatter,
  *   ms[3] attention partial kernels, ms[4] log-sum-exp merge kernel,
  *   ms[5] free (or truncate), ms[6] whole attention call (partial + merge),
- *   ms[7] the tcgen05 partial kernel alone (part of ms[3]).
+ *   ms[7] the tcgen05 partial kernel alone (part of ms[3]),
+ *   ms[8] the mma.sync partial kernel alone when it ran beside the tcgen05
+ *   kernel (events on the pool's side stream; ms[3] then spans both).
  * Entries with no recorded call are set to -1.                                */
-#define DENDRITE_N_TIMINGS 8
+#define DENDRITE_N_TIMINGS 9
 int dendrite_set_profiling(dendrite_pool* pool, int32_t enable);
 int dendrite_last_timings(dendrite_pool* pool, float* ms, int32_t n);
 
