@@ -1888,7 +1888,6 @@ int tc_ctas(const dendrite_pool* p) {
 // (griddepcontrol.wait) before reading anything.
 int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStream_t s) {
     const bool bf16 = p->dtype == DENDRITE_BF16;
-    prof_begin(p, T_ATTN_TOTAL, s);
     prof_begin(p, T_ATTN_PARTIAL, s);
     CUtensorMap mk{}, mv{};
     if (bf16) {
@@ -2104,6 +2103,9 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         if (std::adjacent_find(s.begin(), s.end()) != s.end()) return DENDRITE_EINVAL;
     }
     cudaStream_t s = (cudaStream_t)stream;
+    // the whole call's device work, plan upload and expansion included (its
+    // events start after the host has built the plan)
+    bool began = false;
     const int max_ctas = p->sm_count * p->attn_ctas_per_sm;
     PlanCache& pc = p->plan;
     const bool same_query = pc.valid && pc.q_len == q_len && pc.n_q_heads == n_q_heads &&
@@ -2136,6 +2138,8 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         {
             const int64_t n16 = (int64_t)(pc.upload_bytes / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
+            prof_begin(p, T_ATTN_TOTAL, s);
+            began = true;
             DENDRITE_CUDA(launch_pdl(k_plan_upload, dim3(grid), dim3(256), 0, s,
                                      reinterpret_cast<const uint4*>(p->h_plan[ib]),
                                      reinterpret_cast<uint4*>(p->d_plan[ib]), n16));
@@ -2180,6 +2184,8 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         {
             const int64_t n16 = (int64_t)(up_bytes / 16);
             const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (n16 + 255) / 256));
+            prof_begin(p, T_ATTN_TOTAL, s);
+            began = true;
             DENDRITE_CUDA(launch_pdl(k_plan_upload, dim3(grid), dim3(256), 0, s,
                                      reinterpret_cast<const uint4*>(p->h_plan[ib]),
                                      reinterpret_cast<uint4*>(p->d_plan[ib]), n16));
@@ -2246,6 +2252,7 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
     a.plan = pc.dev;
     a.part_acc = p->d_partial;
     a.part_ml = reinterpret_cast<float2*>(p->d_partial + p->partial_rows_cap * p->head_dim);
+    if (!began) prof_begin(p, T_ATTN_TOTAL, s);
     return launch_attention(p, layer, a, s);
 }
 
@@ -2345,6 +2352,7 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
     const size_t acc_bytes = hp.partial_rows * p->head_dim * sizeof(float);
     const size_t ml_bytes = hp.partial_rows * sizeof(float2);
     if (plan_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes) return DENDRITE_ELIMIT;
+    prof_begin(p, T_ATTN_TOTAL, s);
     {
         std::lock_guard<std::mutex> lock(g_noalloc_host_mu);
         plan_pack(hp, off, reinterpret_cast<char*>(g_noalloc_host));

@@ -286,7 +286,7 @@ struct dendrite_pool {
     dendrite::PendingAppend pending;
 
     // profiling
-    bool profiling = false;
+    int profiling = 0;   // 0 off, 1 every kernel, 2 whole attention calls only
     cudaEvent_t ev[dendrite::T_COUNT][2] = {};
     bool ev_recorded[dendrite::T_COUNT] = {};
 };

@@ -645,11 +645,17 @@ int cuda_err(cudaError_t e) {
     return DENDRITE_ECUDA;
 }
 
+// Level 2 records only whole attention calls: events between a call's
+// kernels would end the overlap of each kernel's start with the previous
+// one's tail (programmatic dependent launch) and time a slower call.
+static bool prof_on(const dendrite_pool* p, TimingKind k) {
+    return p->profiling == 1 || (p->profiling == 2 && k == T_ATTN_TOTAL);
+}
 void prof_begin(dendrite_pool* p, TimingKind k, cudaStream_t s) {
-    if (p->profiling) cudaEventRecord(p->ev[k][0], s);
+    if (prof_on(p, k)) cudaEventRecord(p->ev[k][0], s);
 }
 void prof_end(dendrite_pool* p, TimingKind k, cudaStream_t s) {
-    if (p->profiling) {
+    if (prof_on(p, k)) {
         cudaEventRecord(p->ev[k][1], s);
         p->ev_recorded[k] = true;
     }
@@ -1467,7 +1473,8 @@ int dendrite_pool_info(dendrite_pool* p, int64_t* num_blocks, int32_t* block_siz
 
 int dendrite_set_profiling(dendrite_pool* p, int32_t enable) {
     if (!p) return DENDRITE_EINVAL;
-    p->profiling = enable != 0;
+    if (enable < 0 || enable > 2) return DENDRITE_EINVAL;
+    p->profiling = enable;
     for (int k = 0; k < T_COUNT; ++k) p->ev_recorded[k] = false;
     return DENDRITE_OK;
 }

@@ -357,8 +357,10 @@ class Pool:
         return k, v
 
     # --------------------------------------------------------- profiling
-    def set_profiling(self, enable: bool) -> None:
-        _check(lib().dendrite_set_profiling(self._h, 1 if enable else 0), "set_profiling")
+    def set_profiling(self, enable) -> None:
+        """True/1: events around every kernel; 2: around whole attention calls only."""
+        level = 2 if enable == 2 else (1 if enable else 0)
+        _check(lib().dendrite_set_profiling(self._h, level), "set_profiling")
 
     def last_timings(self) -> dict:
         buf = (ctypes.c_float * len(TIMING_NAMES))()

@@ -326,12 +326,16 @@ int dendrite_pool_info(dendrite_pool* pool, int64_t* num_blocks, int32_t* block_
                        int32_t* n_kv_heads, int32_t* head_dim, int32_t* dtype);
 
 /* ------------------------------------------------------------ profiling
- * When enabled, each call records CUDA events around each of its kernels on
- * the caller's stream.  dendrite_last_timings() synchronises on them and
+ * With enable = 1, each call records CUDA events around each of its kernels
+ * on the caller's stream; with enable = 2, only around whole attention calls
+ * (ms[6]), so that a call's kernels keep overlapping one another as they do
+ * unprofiled; 0 turns profiling off (other values: DENDRITE_EINVAL).
+ * dendrite_last_timings() synchronises on them and
  * returns the device milliseconds of the most recent call of each kind:
  *   ms[0] fork, ms[1] append metadata, ms[2] append copy/scatter,
  *   ms[3] attention partial kernels, ms[4] log-sum-exp merge kernel,
- *   ms[5] free (or truncate), ms[6] whole attention call (partial + merge),
+ *   ms[5] free (or truncate), ms[6] whole attention call (plan upload and
+ *   expansion when the call builds a plan, partial kernels, merge),
  *   ms[7] the tcgen05 partial kernel alone (part of ms[3]),
  *   ms[8] the mma.sync partial kernel alone when it ran beside the tcgen05
  *   kernel (events on the pool's side stream; ms[3] then spans both).
