@@ -129,6 +129,7 @@ struct Node {
     int32_t len = 0;
     int32_t handle = -1;
     int32_t refs = 0;   // (live handle ? 1 : 0) + number of child nodes
+    int32_t first_child = -1, next_sib = -1, prev_sib = -1;   // the child nodes, as a list
 };
 
 // Pinned host -> device staging ring for per-call argument arrays.

@@ -779,6 +779,29 @@ int Staging::release(cudaStream_t stream) {
 // ================================================================ host API
 namespace {
 
+// A node's child nodes form a doubly linked list (first_child, next_sib,
+// prev_sib), so that a node left with one child can hand its place to it.
+void link_child(dendrite_pool* p, int32_t parent, int32_t id) {
+    Node& n = p->nodes[id];
+    n.parent = parent;
+    n.prev_sib = -1;
+    n.next_sib = -1;
+    if (parent < 0) return;
+    Node& par = p->nodes[parent];
+    n.next_sib = par.first_child;
+    if (par.first_child >= 0) p->nodes[par.first_child].prev_sib = id;
+    par.first_child = id;
+}
+
+void unlink_child(dendrite_pool* p, int32_t id) {
+    Node& n = p->nodes[id];
+    if (n.parent < 0) return;
+    if (n.prev_sib >= 0) p->nodes[n.prev_sib].next_sib = n.next_sib;
+    else p->nodes[n.parent].first_child = n.next_sib;
+    if (n.next_sib >= 0) p->nodes[n.next_sib].prev_sib = n.prev_sib;
+    n.prev_sib = n.next_sib = -1;
+}
+
 int32_t new_node(dendrite_pool* p, int32_t parent, int32_t fork_len, int32_t handle) {
     int32_t id;
     if (!p->free_nodes.empty()) {
@@ -789,20 +812,45 @@ int32_t new_node(dendrite_pool* p, int32_t parent, int32_t fork_len, int32_t han
         p->nodes.emplace_back();
     }
     Node& n = p->nodes[id];
-    n.parent = parent;
+    n = Node();
     n.fork_len = fork_len;
     n.len = fork_len;
     n.handle = handle;
     n.refs = 1;
+    link_child(p, parent, id);
     if (parent >= 0) p->nodes[parent].refs++;
     return id;
 }
 
+// Drops one reference of node id: its handle or one of its child nodes.  A
+// node with no references left is freed (and drops its reference on its
+// parent).  A node left with no handle and one child node is spliced out:
+// the child takes its place under its parent and its fork position, so the
+// child's own range starts where the node's did.  That changes no branch's
+// blocks and which branches share them (the node's own blocks were read by
+// the child's subtree alone), and it keeps the chain from a branch to its
+// root as short as the tree's real forks, however many times its leaves
+// were forked and freed (a decode loop that forks every leaf at every step
+// would otherwise add a node per branch per step).
 void drop_node_ref(dendrite_pool* p, int32_t id) {
     while (id >= 0) {
         Node& n = p->nodes[id];
-        if (--n.refs > 0) return;
+        if (--n.refs > 0) {
+            if (n.refs == 1 && n.handle < 0 && n.first_child >= 0) {
+                const int32_t c = n.first_child, up = n.parent, fl = n.fork_len;
+                unlink_child(p, c);
+                unlink_child(p, id);
+                // (a child cut below the node's own start, by a truncation,
+                // already starts earlier and keeps its position)
+                p->nodes[c].fork_len = std::min(p->nodes[c].fork_len, fl);
+                link_child(p, up, c);
+                p->nodes[id] = Node();
+                p->free_nodes.push_back(id);
+            }
+            return;
+        }
         const int32_t up = n.parent;
+        unlink_child(p, id);
         n = Node();
         p->free_nodes.push_back(id);
         id = up;

@@ -203,3 +203,59 @@ def test_device_expansion_equals_host_expansion(name, make, fold):
     rng = random.Random(len(w.query))
     sample = sorted(rng.sample(range(len(w.query)), min(6, len(w.query))))
     check_attention(w, outs[0], sample, TOL)
+
+
+def test_decode_loop_forking_every_leaf_keeps_the_tree_flat():
+    """A decode loop that forks every leaf once per step, appends a token to
+    each child and frees the old leaves (the bench's decode step): the host
+    tree splices out the freed leaves' nodes, so the plan keeps the shape of
+    the real forks (one segment per prefix and one per leaf, step after
+    step) instead of growing a node per branch per step; the attention
+    matches the oracle along the way."""
+    from copy_write_forked_gb300.dendrite import Pool
+    R, P, Wd, nkv, nq, d = 2, 200, 4, 8, 32, 128
+    steps = 40
+    pool = Pool(R * (P // 16 + 2) + R * Wd * (steps // 16 + 4) + 64, 16, nkv, d, torch.bfloat16,
+                max_branches=R + 2 * R * Wd + 16, max_blocks_per_branch=(P + steps) // 16 + 8)
+    tree = KVTree(nkv, d)
+    gen = torch.Generator(device="cuda").manual_seed(11)
+
+    def rows(n, t):
+        return (torch.randn((n, t, nkv, d), generator=gen, device="cuda").bfloat16(),
+                torch.randn((n, t, nkv, d), generator=gen, device="cuda").bfloat16())
+
+    roots = [pool.new_branch() for _ in range(R)]
+    ids = {h: h for h in roots}
+    for h in roots:
+        tree.new_root(h)
+    K, V = rows(R, P)
+    pool.append_kv(roots, K, V)
+    for j, h in enumerate(roots):
+        tree.append(h, K[j].cpu(), V[j].cpu())
+    kids = pool.fork_batch(roots, [Wd] * R)
+    leaves = []
+    for h, ks in zip(roots, kids):
+        tree.fork(h, ks)
+        leaves.extend(ks)
+    segs = []
+    Q = torch.randn((len(leaves), 1, nq, d), generator=gen, device="cuda").bfloat16()
+    for step in range(steps):
+        kids = pool.fork_batch(leaves, [1] * len(leaves))
+        br = [k[0] for k in kids]
+        for lf, c in zip(leaves, br):
+            tree.fork(lf, [c])
+        K, V = rows(len(br), 1)
+        pool.append_kv(br, K, V)
+        for j, c in enumerate(br):
+            tree.append(c, K[j].cpu(), V[j].cpu())
+        out = pool.tree_attn_decode(Q, br)
+        pool.sync()
+        segs.append(pool.last_plan_stats()["n_segments"])
+        if step in (0, 17, steps - 1):
+            _check(tree, br, Q, out, range(len(br)))
+        pool.free(leaves)
+        for lf in leaves:
+            tree.free(lf)
+        leaves = br
+    assert len(set(segs)) == 1 and segs[0] <= R + R * Wd, segs
+    pool.close()
