@@ -312,8 +312,7 @@ def run_ours(args):
         Qs = Q if Qs is None else Qs
         o = out if o is None else o
         if kind == "decode":
-            kids = pool.fork_batch(state["leaves"], [1] * nl)
-            br = [ks[0] for ks in kids]
+            br = pool.fork_each(state["leaves"])
             pool.append_kv(br, K, V)
             pool.tree_attn_decode(Qs, br, out=o)
             if check is not None:

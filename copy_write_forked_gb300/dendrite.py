@@ -213,16 +213,35 @@ class Pool:
         return list(out)
 
     def fork_batch(self, parents: Sequence[int], n_children: Sequence[int], stream=None) -> List[List[int]]:
-        total = sum(int(n) for n in n_children)
-        out = array.array("i", bytes(4 * max(1, total)))
+        n_par = len(parents)
         pa, na = _arr(parents), _arr(n_children)
-        _check(lib().dendrite_fork_batch(self._h, _ptr(pa), _ptr(na), len(parents), _ptr(out),
+        total = sum(na) if n_par else 0
+        out = array.array("i", bytes(4 * max(1, total)))
+        _check(lib().dendrite_fork_batch(self._h, _ptr(pa), _ptr(na), n_par, _ptr(out),
                                          _stream_ptr(stream, self._dev)), "fork_batch")
+        if n_par == 0:
+            return []
+        flat = out.tolist()
+        if total == len(na):
+            return [[x] for x in flat]
         res, k = [], 0
-        for n in n_children:
-            res.append(out[k:k + n].tolist())
+        for n in na:
+            res.append(flat[k:k + n])
             k += n
         return res
+
+    def fork_each(self, parents: Sequence[int], stream=None) -> List[int]:
+        """One child per parent (dendrite_fork_batch with every count 1): the
+        children's handles, in the parents' order."""
+        pa = _arr(parents)
+        n = len(pa)
+        if n == 0:
+            return []
+        na = array.array("i", [1]) * n
+        out = array.array("i", bytes(4 * n))
+        _check(lib().dendrite_fork_batch(self._h, _ptr(pa), _ptr(na), n, _ptr(out),
+                                         _stream_ptr(stream, self._dev)), "fork_each")
+        return out.tolist()
 
     def _check_tensor(self, t: torch.Tensor, name: str) -> None:
         if not t.is_cuda or t.dtype != self.dtype or not t.is_contiguous():

@@ -190,6 +190,26 @@ def test_batched_forks_and_frees_of_siblings_match_oracle():
     pool.close()
 
 
+def test_fork_each_is_fork_batch_with_one_child_each():
+    """Pool.fork_each(parents) forks one child per parent: the same tables,
+    lengths and refcounts as fork_batch with every count 1, children in the
+    parents' order; an empty call forks nothing."""
+    states = []
+    for use_each in (True, False):
+        pool = Pool(64, 16, 2, 64, torch.float32, max_branches=16, max_blocks_per_branch=8)
+        a, b = pool.new_branch(), pool.new_branch()
+        K = torch.randn(2, 37, 2, 64, device="cuda")
+        pool.append_kv([a, b], K, K)
+        kids = pool.fork_each([b, a]) if use_each else [k[0] for k in pool.fork_batch([b, a], [1, 1])]
+        assert (pool.fork_each([]) if use_each else pool.fork_batch([], [])) == []
+        pool.sync()
+        states.append(([pool.read_table(k) for k in kids], [pool.branch_len(k) for k in kids],
+                       pool.read_refcounts(), pool.read_table(b), pool.read_table(a)))
+        assert states[-1][0] == [pool.read_table(b), pool.read_table(a)]
+        pool.close()
+    assert states[0] == states[1]
+
+
 def test_exhausted_pool_applies_nothing_and_is_sticky():
     pool = Pool(6, 16, 1, 128, torch.bfloat16, max_branches=8, max_blocks_per_branch=8)
     r = pool.new_branch()
