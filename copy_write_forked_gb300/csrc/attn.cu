@@ -1896,21 +1896,14 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     }
     // Both partial classes: the tcgen05 and the mma.sync kernel write
     // disjoint partial rows and read only the plan and the pool, so the
-    // mma.sync kernel runs on the pool's side stream beside the tcgen05 one
-    // (its CTAs take the SMs that the tcgen05 kernel's first CTAs to finish
-    // leave), and the caller's stream waits for it before the merge.
+    // mma.sync kernel runs on the pool's side stream (lowest priority) beside
+    // the tcgen05 one: its CTAs take the SMs that the tcgen05 kernel's first
+    // CTAs to finish leave, and the caller's stream waits for it before the
+    // merge.
     const bool beside = bf16 && a.plan.n_tc_ctas > 0 && a.plan.n_ctas > 0 && p->side;
-    if (beside) {
-        DENDRITE_CUDA(cudaEventRecord(p->ev_fork, s));
-        DENDRITE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
-        prof_begin(p, T_ATTN_MMA_SIDE, p->side);
-        k_attn_partial_bf16<<<dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, p->side>>>(mk, mv, a);
-        DENDRITE_CUDA(cudaGetLastError());
-        prof_end(p, T_ATTN_MMA_SIDE, p->side);
-        DENDRITE_CUDA(cudaEventRecord(p->ev_join, p->side));
-    } else {
-        p->ev_recorded[T_ATTN_MMA_SIDE] = false;
-    }
+    if (beside) DENDRITE_CUDA(cudaEventRecord(p->ev_fork, s));
+    // the tcgen05 kernel is submitted first, so that its CTAs are placed
+    // before the side stream's
     if (a.plan.n_tc_ctas > 0) {
         prof_begin(p, T_ATTN_TC, s);
         DENDRITE_TRY(launch_attn_tc(mk, mv, a, a.plan.n_tc_ctas, s));
@@ -1918,7 +1911,17 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     } else {
         p->ev_recorded[T_ATTN_TC] = false;   // this call ran no tensor-core kernel
     }
-    if (beside) DENDRITE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));
+    if (beside) {
+        DENDRITE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+        prof_begin(p, T_ATTN_MMA_SIDE, p->side);
+        k_attn_partial_bf16<<<dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, p->side>>>(mk, mv, a);
+        DENDRITE_CUDA(cudaGetLastError());
+        prof_end(p, T_ATTN_MMA_SIDE, p->side);
+        DENDRITE_CUDA(cudaEventRecord(p->ev_join, p->side));
+        DENDRITE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));
+    } else {
+        p->ev_recorded[T_ATTN_MMA_SIDE] = false;
+    }
     const int32_t n_out_rows = a.plan.n_queried * a.plan.q_len * a.plan.n_q_heads;
     if (beside) {
         // launched above

@@ -1112,11 +1112,16 @@ int pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int3
     for (int k = 0; k < T_COUNT; ++k)
         if (cudaEventCreate(&p->ev[k][0]) != cudaSuccess || cudaEventCreate(&p->ev[k][1]) != cudaSuccess)
             return fail(cuda_err(cudaErrorUnknown));
+    // the side stream (the mma.sync partial kernel beside the tcgen05 one) at
+    // the lowest priority: the tcgen05 kernel's CTAs take the SMs first and
+    // the mma.sync CTAs fill what they leave
+    int lo_prio = 0, hi_prio = 0;
     if (cudaEventCreateWithFlags(&p->plan_copied[0], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p->plan_copied[1], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess)
+        cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, lo_prio) != cudaSuccess)
         return fail(cuda_err(cudaErrorUnknown));
     k_init<<<std::max(1, std::min(4 * p->sm_count, (int)((num_blocks + 255) / 256))), 256>>>(
         p->d_stack, p->d_refcount, p->d_holders, p->d_last, p->d_released, num_blocks, p->d_table,

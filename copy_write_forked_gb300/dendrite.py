@@ -233,10 +233,10 @@ class Pool:
     def fork_each(self, parents: Sequence[int], stream=None) -> List[int]:
         """One child per parent (dendrite_fork_batch with every count 1): the
         children's handles, in the parents' order."""
-        pa = _arr(parents)
-        n = len(pa)
+        n = len(parents)
         if n == 0:
             return []
+        pa = _arr(parents)
         na = array.array("i", [1]) * n
         out = array.array("i", bytes(4 * n))
         _check(lib().dendrite_fork_batch(self._h, _ptr(pa), _ptr(na), n, _ptr(out),
