@@ -493,12 +493,18 @@ def run_ours(args):
             Q2.copy_(Qh, non_blocking=True)
             ev_in[j].record(copy_stream)
 
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # step using buffer set j computed its output
+
     def e2e_step(j, check=None):
         K2, V2, Q2, o2 = bufs[j]
         stream.wait_event(ev_in[j])
         br = step(K2, V2, Q2, o2, check=check)
-        outh[j].copy_(o2, non_blocking=True)
-        ev_used[j].record(stream)
+        # the result goes back on the copy stream, beside the next step
+        ev_done[j].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_done[j])
+            outh[j].copy_(o2, non_blocking=True)
+            ev_used[j].record(copy_stream)
         return br
 
     def e2e_run(n, check=None):
