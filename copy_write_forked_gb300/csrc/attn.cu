@@ -954,9 +954,12 @@ __global__ void __launch_bounds__(256, WIDE ? 2 : 1) k_attn_merge(const AttnArgs
 // partial of row g0 + i is always the one of row g0 plus i.  The plan keeps
 // such a run of rows inside one row group when G <= 4 divides 16 or G is a
 // multiple of 4 (row groups hold 16, 64 or 256 rows); other group sizes use
-// the per-row kernel above.  Lane l owns columns 4 l .. 4 l + 3.
+// the per-row kernel above.  Lane l owns columns 4 l .. 4 l + 3.  The kernel
+// is a chain of dependent loads, so it runs three CTAs per SM (80 registers;
+// with four heads one partial's loads in flight at a time, a 28-byte spill):
+// stress merge 29 -> 24 us, MCTS call 271 -> 264 us against two CTAs per SM.
 template <typename T, int NG>
-__global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a) {
+__global__ void __launch_bounds__(256, 3) k_attn_merge_grouped(const AttnArgs a) {
     pdl_trigger();
     const AttnPlanDev& pl = a.plan;
     const int lane = threadIdx.x & 31;
@@ -1041,7 +1044,7 @@ __global__ void __launch_bounds__(256, 2) k_attn_merge_grouped(const AttnArgs a)
                 M[i] = Mn;
             }
             // acc rows, eight (partial, head) pairs in flight
-            constexpr int PER = 8 / NG;   // partials per batch of eight loads
+            constexpr int PER = NG >= 4 ? 1 : 8 / NG;   // partials per batch of loads (register budget)
             for (int q = 0; q < nb; q += PER) {
                 float4 v[PER][NG];
                 float wq[PER][NG];
