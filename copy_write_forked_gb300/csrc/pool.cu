@@ -444,29 +444,29 @@ __global__ void __launch_bounds__(128, 16) k_append_copy(const __grid_constant__
 }
 
 // ------------------------------------------------------- free / truncate
-// The end of a free kernel: thread (rel, blk) released block blk if rel.  One
-// lane per warp folds the warp's released ids into the call's range; the last
-// CTA to finish pushes the released blocks onto the free stack in descending
-// id order (a block scan over [rel_lo, rel_hi] from the top down).
-__device__ __forceinline__ void free_collect(bool rel, int32_t blk, int32_t* released, int32_t* stack,
-                                             DevMeta* meta, int32_t n_blocks) {
+// The end of a free kernel.  free_fold: thread (rel, blk) released block blk
+// if rel; one lane per warp folds the warp's released ids into the call's
+// range (any number of times per thread).  free_finish: the last CTA to
+// finish pushes the released blocks onto the free stack in descending id
+// order (a block scan over [rel_lo, rel_hi] from the top down).
+__device__ __forceinline__ void free_fold(bool rel, int32_t blk, DevMeta* meta) {
+    const unsigned m = __ballot_sync(0xffffffffu, rel);
+    if (m) {
+        const int32_t wlo = __reduce_min_sync(0xffffffffu, rel ? blk : INT_MAX);
+        const int32_t whi = __reduce_max_sync(0xffffffffu, rel ? blk : -1);
+        if ((threadIdx.x & 31) == 0) {
+            atomicMin(&meta->rel_lo, wlo);
+            atomicMax(&meta->rel_hi, whi);
+            atomicAdd(&meta->rel_count, __popc(m));
+        }
+    }
+}
+
+__device__ __forceinline__ void free_finish(int32_t* released, int32_t* stack, DevMeta* meta, int32_t n_blocks) {
     __shared__ int32_t warp_sums[kFreeCollectThreads / 32];
     __shared__ int32_t chunk_total;
     __shared__ int32_t st, is_last, lo, hi, top0, cnt;
     const int32_t n_ctas = (int32_t)(gridDim.x * gridDim.y);
-    // one lane per warp folds the warp's released ids into the call's range
-    {
-        const unsigned m = __ballot_sync(0xffffffffu, rel);
-        if (m) {
-            const int32_t wlo = __reduce_min_sync(0xffffffffu, rel ? blk : INT_MAX);
-            const int32_t whi = __reduce_max_sync(0xffffffffu, rel ? blk : -1);
-            if ((threadIdx.x & 31) == 0) {
-                atomicMin(&meta->rel_lo, wlo);
-                atomicMax(&meta->rel_hi, whi);
-                atomicAdd(&meta->rel_count, __popc(m));
-            }
-        }
-    }
     __syncthreads();
     if (threadIdx.x == 0) {
         // a single CTA is its own last one: the barrier above already ordered
@@ -577,61 +577,70 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
             }
         }
     }
-    free_collect(rel, blk, released, stack, meta, n_blocks);
+    free_fold(rel, blk, meta);
+    free_finish(released, stack, meta, n_blocks);
 }
 
 // Frees of many branches whose rows share blocks (siblings of one prompt): a
-// CTA takes 32 branches x 32 of their entries.  Warp w reads and clears
-// branch w's entries (coalesced); transposed through shared memory, warp w
-// then takes entry w of the 32 branches, and lanes holding the same block
-// drop their references with one atomic.  args as for k_free;
-// blockIdx.y: entry chunk.
+// CTA takes 32 branches x kFreeTileEntries of their entries.  Warp w reads and
+// clears branch w's entries (coalesced, four per lane); transposed through
+// shared memory, warp w then takes entries w, w + 32, ... of the 32
+// branches, and lanes holding the same block drop their references with one
+// atomic.  args as for k_free; blockIdx.y: entry chunk.
+constexpr int kFreeTileEntries = 128;
 template <typename A>
 __global__ void __launch_bounds__(kFreeCollectThreads)
 k_free_tiles(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, int32_t n_blocks,
              int32_t* table, int32_t* refcount, int32_t* released, int32_t* stack, DevMeta* meta) {
-    static_assert(kFreeCollectThreads == 1024, "one warp per branch row of a 32 x 32 tile");
-    __shared__ int32_t tile[32][33];
+    static_assert(kFreeCollectThreads == 1024, "one warp per branch row of a 32-branch tile");
+    constexpr int PER = kFreeTileEntries / 32;
+    __shared__ int32_t tile[32][kFreeTileEntries + 1];
     pdl_wait();
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t i = blockIdx.x * 32 + w;
-    const int32_t pos = blockIdx.y * 32 + lane;
-    int32_t* slot = nullptr;
-    int32_t blk = -1;
+    const int32_t pos0 = blockIdx.y * kFreeTileEntries + lane;
+    int32_t* row = nullptr;
+    int32_t count = 0;
     if (i < n) {
         const int32_t c0 = args[n + i], c1 = i + 1 < n ? args[n + i + 1] : total;
-        if (pos < c1 - c0) {
-            slot = table + (int64_t)args[i] * bpb + args[2 * n + i] + pos;
-            blk = *slot;
-        }
+        count = c1 - c0;
+        row = table + (int64_t)args[i] * bpb + args[2 * n + i];
     }
+    int32_t blk[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) blk[k] = (row && pos0 + 32 * k < count) ? row[pos0 + 32 * k] : -1;
     if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile const int32_t*>(&meta->status) != 0))
         return;
-    if (slot) {
-        *slot = -1;
-        if ((uint32_t)blk >= (uint32_t)n_blocks) {
-            set_status(meta, DENDRITE_ECORRUPT);
-            blk = -1;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        if (row && pos0 + 32 * k < count) {
+            row[pos0 + 32 * k] = -1;
+            if ((uint32_t)blk[k] >= (uint32_t)n_blocks) {
+                set_status(meta, DENDRITE_ECORRUPT);
+                blk[k] = -1;
+            }
         }
-    } else {
-        blk = -1;
+        tile[w][lane + 32 * k] = blk[k];
     }
-    tile[w][lane] = blk;
     __syncthreads();
-    const int32_t b = tile[lane][w];
-    const unsigned grp = __match_any_sync(0xffffffffu, b);
-    bool rel = false;
-    if (b >= 0 && lane == __ffs(grp) - 1) {
-        const int32_t c = __popc(grp);
-        const int32_t old = atomicSub(refcount + b, c);
-        if (old == c) {
-            released[b] = 1;
-            rel = true;
-        } else if (old < c) {
-            set_status(meta, DENDRITE_ECORRUPT);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int32_t b = tile[lane][w + 32 * k];
+        const unsigned grp = __match_any_sync(0xffffffffu, b);
+        bool rel = false;
+        if (b >= 0 && lane == __ffs(grp) - 1) {
+            const int32_t c = __popc(grp);
+            const int32_t old = atomicSub(refcount + b, c);
+            if (old == c) {
+                released[b] = 1;
+                rel = true;
+            } else if (old < c) {
+                set_status(meta, DENDRITE_ECORRUPT);
+            }
         }
+        free_fold(rel, b, meta);
     }
-    free_collect(rel, b, released, stack, meta, n_blocks);
+    free_finish(released, stack, meta, n_blocks);
 }
 
 }  // namespace
@@ -1333,8 +1342,8 @@ int release_entries(dendrite_pool* p, const int32_t* branches, const int32_t* st
     }
     if (total > INT32_MAX / 2) return DENDRITE_ELIMIT;
     if (total == 0) return DENDRITE_OK;
-    // many branches: 32 x 32 tiles (one atomic per block shared within a tile)
-    const bool tiles = n >= 32 && (max_count + 31) / 32 <= 65535;
+    // many branches: 32-branch tiles (one atomic per block shared within a tile)
+    const bool tiles = n >= 32 && (max_count + kFreeTileEntries - 1) / kFreeTileEntries <= 65535;
     auto fill = [&](int32_t* a) {
         int32_t acc = 0;
         for (int32_t i = 0; i < n; ++i) {
@@ -1348,7 +1357,8 @@ int release_entries(dendrite_pool* p, const int32_t* branches, const int32_t* st
     auto launch = [&](auto args) -> int {
         if (tiles) {
             DENDRITE_CUDA(launch_pdl(k_free_tiles<decltype(args)>,
-                                     dim3((unsigned)((n + 31) / 32), (unsigned)((max_count + 31) / 32)),
+                                     dim3((unsigned)((n + 31) / 32),
+                                          (unsigned)((max_count + kFreeTileEntries - 1) / kFreeTileEntries)),
                                      dim3(kFreeCollectThreads), 0, s, args, n, (int32_t)total, p->bpb,
                                      (int32_t)p->num_blocks, p->d_table, p->d_refcount, p->d_released, p->d_stack,
                                      p->d_meta));
