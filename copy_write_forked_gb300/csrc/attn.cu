@@ -1509,6 +1509,7 @@ void partition_class(HostPlan& hp, int32_t u_lo, int32_t u_hi, int64_t T, int64_
 
 int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
                 int max_tc_ctas, HostPlan& hp, bool allow_device);
+int unit_rows_small(const dendrite_pool* p);
 
 // max_ctas: CTAs of the mma.sync/fp32 kernel; max_tc_ctas: of the tcgen05
 // kernel (0 when it is not used).  The segments (after folding) are left in
@@ -1518,7 +1519,7 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
     const int32_t RM = q_len * G;
     const bool bf16 = p->dtype == DENDRITE_BF16;
-    const int small_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    const int small_rows = unit_rows_small(p);
     const bool tc_on = bf16 && max_tc_ctas > 0 && p->tc_min_rows >= 0;
     const int32_t n_nodes = (int32_t)p->nodes.size();
     hp.parent.resize(n_nodes);
@@ -1549,6 +1550,14 @@ int32_t class_ctas(int64_t weight, int max_ctas, const ClassWeights& cw) {
     return (int32_t)std::max<int64_t>(1, std::min<int64_t>(max_ctas, (weight + cw.min_per_cta - 1) / cw.min_per_cta));
 }
 
+// Rows per unit of the mma.sync (bf16: 4 row tiles of 16) or compressed
+// (64: the CTA decodes each tile once for its four warps' row tiles) partial
+// kernels, and of the fp32 kernel (16).
+int unit_rows_small(const dendrite_pool* p) {
+    return p->dtype == DENDRITE_BF16 ? kMaxUnitRowsBf16 : p->dtype == DENDRITE_TURBO ? kMaxUnitRowsTurbo
+                                                                                    : kMaxUnitRowsF32;
+}
+
 // bf16 plans of at least this many units, with fewer tiles per unit than
 // this on average, are expanded on the device by default
 constexpr int32_t kDevicePlanMinUnits = 2048;
@@ -1565,7 +1574,7 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
     const int32_t RM = q_len * G;
     const bool bf16 = p->dtype == DENDRITE_BF16;
-    const int small_rows = bf16 ? kMaxUnitRowsBf16 : kMaxUnitRowsF32;
+    const int small_rows = unit_rows_small(p);
     const bool tc_on = bf16 && max_tc_ctas > 0 && p->tc_min_rows >= 0;
     // Segments, their members and their units (kv head major, then row
     // group), tensor-core segments first: pass 0 takes the segments read by

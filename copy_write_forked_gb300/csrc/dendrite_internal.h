@@ -19,6 +19,7 @@ namespace dendrite {
 constexpr int kBlockSize = 16;        // tokens per block (= attention tile height)
 constexpr int kMaxUnitRowsBf16 = 64;  // rows per mma.sync attention unit (4 row tiles of 16)
 constexpr int kMaxUnitRowsF32 = 16;
+constexpr int kMaxUnitRowsTurbo = 64;  // rows per compressed-pool unit (4 warps x 16 rows)
 constexpr int kMaxUnitRowsTc = 256;   // rows per tcgen05 attention unit (2 row tiles of 128)
 constexpr int kTcMinRowsDefault = 64; // segments with more rows per kv head use the tcgen05 kernel
 constexpr int32_t kFoldPctDefault = 100;  // fold a segment when that is estimated cheaper

@@ -457,6 +457,164 @@ __device__ __forceinline__ void tq_decode16(const uint32_t* rec, int j, const fl
                     pack_half2(x[14], x[15]));
 }
 
+// One warp's rows against one tile: 16 query rows (fp16 at qrows, row stride
+// 512 bytes, chunks XOR-ed with row & 7) against the tile's 16 tokens (key and
+// value records at rk / rv, decoded unit rows at kt / vt).  pos0: position of
+// the lane's first column; a0/a1, b0/b1: the rows' score scales.
+struct TqRows {
+    float o[16][4];
+    float m0, m1, l0, l1, vs;
+};
+
+__device__ __forceinline__ void tq_tile(TqRows& st, uint32_t qrows, const unsigned char* rk,
+                                        const unsigned char* rv, uint32_t kt, uint32_t vt, int32_t pos0,
+                                        int32_t lim0, int32_t lim1, float a0, float a1, float b0, float b1,
+                                        int lane) {
+    const float NEG_INF = -INFINITY;
+    // per-token scalars of this lane's columns: tokens 2 (lane % 4) + e + 8 nt
+    float kn[2][2], en[2][2], vn[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int tok = 2 * (lane & 3) + e + 8 * nt;
+            const uint32_t* kr = reinterpret_cast<const uint32_t*>(rk + tok * TQ_REC_ROW);
+            kn[nt][e] = __uint_as_float(kr[0]);
+            en[nt][e] = __uint_as_float(kr[20]);
+            vn[nt][e] = __uint_as_float(reinterpret_cast<const uint32_t*>(rv + tok * TQ_REC_ROW)[0]);
+        }
+    }
+    // the QJL bits of tokens lane / 4 and 8 + lane / 4
+    uint32_t qb[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t* kr = reinterpret_cast<const uint32_t*>(rk + ((lane >> 2) + 8 * nt) * TQ_REC_ROW);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) qb[nt][w] = kr[16 + w] >> (2 * (lane & 3));
+    }
+    // S1 = Q' U_k^T, S2 = Z sign^T (16 rows x 16 tokens each)
+    float s1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+        const int mi = lane >> 3;
+        const int tokl = (mi >> 1) * 8 + (lane & 7);
+        const int qr = lane & 15, qh = lane >> 4;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t qa[4], za[4], kb0, kb1, kb2, kb3;
+            ldsm_x4(qrows + qr * 512 + (((2 * ks + qh) ^ (qr & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
+            ldsm_x4(qrows + qr * 512 + (((16 + 2 * ks + qh) ^ (qr & 7)) << 4), za[0], za[1], za[2], za[3]);
+            ldsm_x4(kt + tq_swz(tokl, ks * 16 + (mi & 1) * 8), kb0, kb1, kb2, kb3);
+            mma16816_f16(s1[0], qa, kb0, kb1);
+            mma16816_f16(s1[1], qa, kb2, kb3);
+            const int sh = (ks & 1) * 16;
+            mma16816_f16(s2[0], za, sign_pair(qb[0][ks >> 1] >> sh), sign_pair(qb[0][ks >> 1] >> (sh + 8)));
+            mma16816_f16(s2[1], za, sign_pair(qb[1][ks >> 1] >> sh), sign_pair(qb[1][ks >> 1] >> (sh + 8)));
+        }
+    }
+    // scores, mask, online softmax
+    float sc[2][4];
+    float mx0 = NEG_INF, mx1 = NEG_INF, vmax = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int32_t pos = pos0 + 8 * nt + e;
+            const float v0 = a0 * (kn[nt][e] * s1[nt][e]) + b0 * (en[nt][e] * s2[nt][e]);
+            const float v1 = a1 * (kn[nt][e] * s1[nt][2 + e]) + b1 * (en[nt][e] * s2[nt][2 + e]);
+            sc[nt][e] = pos < lim0 ? v0 : NEG_INF;
+            sc[nt][2 + e] = pos < lim1 ? v1 : NEG_INF;
+            mx0 = fmaxf(mx0, sc[nt][e]);
+            mx1 = fmaxf(mx1, sc[nt][2 + e]);
+            vmax = fmaxf(vmax, vn[nt][e]);
+        }
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, m));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, m));
+        vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, m));
+    }
+    const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
+    const float u0s = n0 == NEG_INF ? 0.f : n0, u1s = n1 == NEG_INF ? 0.f : n1;
+    const float al0 = exp2f(st.m0 - u0s), al1 = exp2f(st.m1 - u1s);
+    st.m0 = n0;
+    st.m1 = n1;
+    const float vs_new = fmaxf(fmaxf(st.vs, vmax), 1e-30f);
+    const float rv_new = 1.f / vs_new;
+    const float g = st.vs * rv_new;
+    const float g0 = al0 * g, g1 = al1 * g;
+    st.vs = vs_new;
+    float ps0 = 0.f, ps1 = 0.f;
+    uint32_t pa[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            p[e] = exp2f(sc[nt][e] - u0s);
+            p[2 + e] = exp2f(sc[nt][2 + e] - u1s);
+            ps0 += p[e];
+            ps1 += p[2 + e];
+        }
+        const float w0 = vn[nt][0] * rv_new, w1 = vn[nt][1] * rv_new;
+        pa[2 * nt] = pack_half2(p[0] * w0, p[1] * w1);
+        pa[2 * nt + 1] = pack_half2(p[2] * w0, p[3] * w1);
+    }
+    st.l0 = st.l0 * al0 + ps0;
+    st.l1 = st.l1 * al1 + ps1;
+    if (!__all_sync(FULL, g0 == 1.f && g1 == 1.f)) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            st.o[n][0] *= g0;
+            st.o[n][1] *= g0;
+            st.o[n][2] *= g1;
+            st.o[n][3] *= g1;
+        }
+    }
+    // acc += P' U_v
+    {
+        const int mi = lane >> 3;
+        const int tokl = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t v0r, v1r, v2r, v3r;
+            ldsm_x4_t(vt + tq_swz(tokl, np * 16 + (mi >> 1) * 8), v0r, v1r, v2r, v3r);
+            mma16816_f16(st.o[2 * np], pa, v0r, v1r);
+            mma16816_f16(st.o[2 * np + 1], pa, v2r, v3r);
+        }
+    }
+}
+
+// Decodes rows 4 (pss % 4) + lane / 8 of the key (pss < 4) or value (pss >= 4)
+// records of one tile into the decoded tiles dk / dv (lane % 8: level-4 node).
+__device__ __forceinline__ void tq_decode_pass(int pss, const unsigned char* rk, const unsigned char* rv,
+                                               unsigned char* dk, unsigned char* dv, const float2* tab, int lane) {
+    const int j = lane & 7;
+    const int row = (pss & 3) * 4 + (lane >> 3);
+    const bool isv = pss >= 4;
+    const uint32_t* rec = reinterpret_cast<const uint32_t*>((isv ? rv : rk) + row * TQ_REC_ROW);
+    uint4 lo, hi;
+    tq_decode16(rec, j, tab, lo, hi);
+    unsigned char* d = isv ? dv : dk;
+    // lanes 4..7 of a row store their upper chunk first: each quarter-warp's
+    // eight 16-byte stores then fall in eight distinct bank groups
+    const bool up = j >= 4;
+    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + (up ? 8 : 0))) = up ? hi : lo;
+    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + (up ? 0 : 8))) = up ? lo : hi;
+}
+
+// Units of more than 16 rows (up to 64) share each tile's decode: the CTA's
+// four warps decode it together (two passes each; records double-buffered by
+// cp.async at CTA level), then warp w runs rows 16 w .. 16 w + 15 over it and
+// stores its rows' partials itself.  Shared memory of this mode (it reuses
+// the space of the per-warp mode between units):
+constexpr int TQB_Q_OFF = 0;                                   // 64 query rows x 512 bytes
+constexpr int TQB_STAGE_OFF = 64 * 512;                        // 2 record stages
+constexpr int TQB_DEC_OFF = TQB_STAGE_OFF + 2 * TQ_STAGE;      // decoded K then V tile
+constexpr int TQB_QSC_OFF = TQB_DEC_OFF + 2 * TQ_DEC_TILE;     // 64 (qmax, zmax)
+static_assert(TQB_QSC_OFF + 64 * 8 <= TQ_TAB_OFF, "the wide mode stays clear of the bin tables");
+
 __global__ void __launch_bounds__(128, 3) k_attn_partial_turbo(const AttnArgs a, const float* __restrict__ qs) {
     extern __shared__ __align__(16) unsigned char tq_smem[];
     __shared__ int st0;
@@ -482,20 +640,19 @@ __global__ void __launch_bounds__(128, 3) k_attn_partial_turbo(const AttnArgs a,
     const unsigned char* VP = reinterpret_cast<const unsigned char*>(a.pool_v);
     const float qjl_c = 0.0097916591f;   // sqrt(pi / 2) / 128
     const uint32_t sbase = smem_u32(tq_smem);
-    const uint32_t wbase = sbase + warp * TQ_WARP_BYTES;
-    const uint32_t qbase = sbase + TQ_Q_OFF;
-    unsigned char* wptr = tq_smem + warp * TQ_WARP_BYTES;
-    const float2* qsc = reinterpret_cast<const float2*>(tq_smem + TQ_QSC_OFF);
-    float2* sml = reinterpret_cast<float2*>(tq_smem + TQ_ML_OFF);
     const float NEG_INF = -INFINITY;
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
         const int32_t uend = U.tile_off + U.n_blk;
         if (t >= uend) { ++u; continue; }
         const int32_t cend = min(t_end, uend);
+        const bool wide = U.n_rows > 16;
+        const int qoff = wide ? TQB_Q_OFF : TQ_Q_OFF;
+        float2* qsc = reinterpret_cast<float2*>(tq_smem + (wide ? TQB_QSC_OFF : TQ_QSC_OFF));
+        const int q_rows = wide ? 64 : 16;
         // ---- the unit's query rows: fp16 tile (swizzled) and scales
-        {
-            const int r = tid >> 3, cc = tid & 7;
+        for (int e = tid; e < q_rows * 8; e += 128) {
+            const int r = e >> 3, cc = e & 7;
             const bool v = r < U.n_rows;
             const AttnRow R = v ? unit_row(pl, U, r) : AttnRow{0, 0};
             const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(qs) +
@@ -504,255 +661,183 @@ __global__ void __launch_bounds__(128, 3) k_attn_partial_turbo(const AttnArgs a,
             for (int k = 0; k < 4; ++k) {
                 const int ch = cc + 8 * k;
                 const uint4 val = v ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(tq_smem + TQ_Q_OFF + r * 512 + ((ch ^ (r & 7)) << 4)) = val;
+                *reinterpret_cast<uint4*>(tq_smem + qoff + r * 512 + ((ch ^ (r & 7)) << 4)) = val;
             }
             if (cc == 0)
-                reinterpret_cast<float2*>(tq_smem + TQ_QSC_OFF)[r] =
-                    v ? *reinterpret_cast<const float2*>(reinterpret_cast<const unsigned char*>(src) + 512)
-                      : make_float2(0.f, 0.f);
+                qsc[r] = v ? *reinterpret_cast<const float2*>(reinterpret_cast<const unsigned char*>(src) + 512)
+                           : make_float2(0.f, 0.f);
         }
         __syncthreads();
-        const int r0 = lane >> 2, r1 = r0 + 8;
+        // this warp's rows: 0..15 of a narrow unit, 16 w .. 16 w + 15 of a wide one
+        const int rbase = wide ? 16 * warp : 0;
+        const bool has_rows = rbase < U.n_rows;
+        const int r0 = rbase + (lane >> 2), r1 = r0 + 8;
         int32_t lim0 = 0, lim1 = 0;
         if (r0 < U.n_rows) lim0 = unit_row(pl, U, r0).limit;
         if (r1 < U.n_rows) lim1 = unit_row(pl, U, r1).limit;
-        const float2 sc0 = qsc[r0], sc1 = qsc[r1];
+        const float2 sc0 = qsc[r0 < q_rows ? r0 : 0], sc1 = qsc[r1 < q_rows ? r1 : 0];
         const float a0 = sc0.x * a.scale_log2, a1 = sc1.x * a.scale_log2;
         const float b0 = qjl_c * sc0.y * a.scale_log2, b1 = qjl_c * sc1.y * a.scale_log2;
-        float o[16][4];
+        TqRows st;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f, vs = 0.f;
-        // ---- this warp's tiles
-        auto issue = [&](int32_t tt, int stage) {
+        for (int n = 0; n < 16; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+        st.m0 = st.m1 = NEG_INF;
+        st.l0 = st.l1 = st.vs = 0.f;
+        // the records of tile tt into the stage at dst: key rows then value rows
+        // (96-byte smem rows), chunks k0, k0 + kstep, ... of the 160
+        auto issue = [&](int32_t tt, uint32_t dst, int k0, int kstep) {
             const int32_t lb = U.blk_start + (tt - U.tile_off);
             int32_t blk = a.table[(int64_t)U.table_row * a.bpb + lb];
             if ((uint32_t)blk >= (uint32_t)a.n_blocks) {
-                if (lane == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
+                if (k0 == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                 blk = 0;   // read a valid block; the pool is poisoned anyway
             }
             const unsigned char* kg = KP + ((int64_t)blk * a.n_kv + U.kv_head) * BS * KREC;
             const unsigned char* vg = VP + ((int64_t)blk * a.n_kv + U.kv_head) * BS * VREC;
-            const uint32_t dst = wbase + stage * TQ_STAGE;
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {   // key records: 96 chunks of 16 bytes
-                const int ch = lane + 32 * i, row = ch / 6, col = ch - 6 * row;
-                cp_async16(dst + row * TQ_REC_ROW + col * 16, kg + ch * 16);
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {   // value records: 64 chunks
-                const int ch = lane + 32 * i, row = ch >> 2, col = ch & 3;
-                cp_async16(dst + BS * TQ_REC_ROW + row * TQ_REC_ROW + col * 16, vg + ch * 16);
+            for (int ch = k0; ch < 160; ch += kstep) {
+                if (ch < 96) {
+                    const int row = ch / 6, col = ch - 6 * row;
+                    cp_async16(dst + row * TQ_REC_ROW + col * 16, kg + ch * 16);
+                } else {
+                    const int v = ch - 96, row = v >> 2, col = v & 3;
+                    cp_async16(dst + BS * TQ_REC_ROW + row * TQ_REC_ROW + col * 16, vg + v * 16);
+                }
             }
         };
-        int32_t tt = t + warp;
-        if (tt < cend) issue(tt, 0);
-        cp_async_commit();
-        for (int it = 0; tt < cend; tt += TQ_WARPS, ++it) {
-            if (tt + TQ_WARPS < cend) issue(tt + TQ_WARPS, (it + 1) & 1);
+        const int32_t lpos = U.blk_start - U.tile_off;   // logical block of tile tt: lpos + tt
+        if (!wide) {
+            // ---- per-warp tiles (warp w: tiles w, w + 4, ...)
+            const uint32_t wbase = sbase + warp * TQ_WARP_BYTES;
+            unsigned char* wptr = tq_smem + warp * TQ_WARP_BYTES;
+            int32_t tt = t + warp;
+            if (tt < cend) issue(tt, wbase, lane, 32);
             cp_async_commit();
-            cp_async_wait1();
-            __syncwarp();
-            const unsigned char* rk = wptr + (it & 1) * TQ_STAGE;   // key records
-            const unsigned char* rv = rk + BS * TQ_REC_ROW;          // value records
-            unsigned char* dk = wptr + 2 * TQ_STAGE;                 // decoded K
-            unsigned char* dv = dk + TQ_DEC_TILE;                    // decoded V
-            // decode: pass p takes rows 4 p + lane / 8, level-4 node lane % 8
-            {
-                const int j = lane & 7;
+            for (int it = 0; tt < cend; tt += TQ_WARPS, ++it) {
+                if (tt + TQ_WARPS < cend) issue(tt + TQ_WARPS, wbase + ((it + 1) & 1) * TQ_STAGE, lane, 32);
+                cp_async_commit();
+                cp_async_wait1();
+                __syncwarp();
+                const unsigned char* rk = wptr + (it & 1) * TQ_STAGE;
+                const unsigned char* rv = rk + BS * TQ_REC_ROW;
+                unsigned char* dk = wptr + 2 * TQ_STAGE;
+                unsigned char* dv = dk + TQ_DEC_TILE;
 #pragma unroll 2
-                for (int pss = 0; pss < 8; ++pss) {
-                    const int row = (pss & 3) * 4 + (lane >> 3);
-                    const bool isv = pss >= 4;
-                    const uint32_t* rec = reinterpret_cast<const uint32_t*>((isv ? rv : rk) + row * TQ_REC_ROW);
-                    uint4 lo, hi;
-                    tq_decode16(rec, j, tab, lo, hi);
-                    unsigned char* d = isv ? dv : dk;
-                    // lanes 4..7 of a row store their upper chunk first: each
-                    // quarter-warp's eight 16-byte stores then fall in eight
-                    // distinct bank groups
-                    const bool up = j >= 4;
-                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + (up ? 8 : 0))) = up ? hi : lo;
-                    *reinterpret_cast<uint4*>(d + tq_swz(row, 16 * j + (up ? 0 : 8))) = up ? lo : hi;
-                }
+                for (int pss = 0; pss < 8; ++pss) tq_decode_pass(pss, rk, rv, dk, dv, tab, lane);
+                __syncwarp();
+                tq_tile(st, sbase + TQ_Q_OFF, rk, rv, wbase + 2 * TQ_STAGE, wbase + 2 * TQ_STAGE + TQ_DEC_TILE,
+                        (lpos + tt) * BS + 2 * (lane & 3), lim0, lim1, a0, a1, b0, b1, lane);
+                __syncwarp();   // records and decoded tiles are reused by the next tile
             }
-            // per-token scalars of this lane's columns: tokens 2 (lane % 4) + e + 8 nt
-            float kn[2][2], en[2][2], vn[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = 2 * (lane & 3) + e + 8 * nt;
-                    const uint32_t* kr = reinterpret_cast<const uint32_t*>(rk + tok * TQ_REC_ROW);
-                    kn[nt][e] = __uint_as_float(kr[0]);
-                    en[nt][e] = __uint_as_float(kr[20]);
-                    vn[nt][e] = __uint_as_float(reinterpret_cast<const uint32_t*>(rv + tok * TQ_REC_ROW)[0]);
-                }
+            cp_async_wait0();
+            // ---- merge the four warps' states and write the partial rows
+            float2* sml = reinterpret_cast<float2*>(tq_smem + TQ_ML_OFF);
+            float l0 = st.l0, l1 = st.l1;
+            l0 += __shfl_xor_sync(FULL, l0, 1);
+            l0 += __shfl_xor_sync(FULL, l0, 2);
+            l1 += __shfl_xor_sync(FULL, l1, 1);
+            l1 += __shfl_xor_sync(FULL, l1, 2);
+            if ((lane & 3) == 0) {
+                sml[warp * 16 + r0] = make_float2(st.m0, l0);
+                sml[warp * 16 + r1] = make_float2(st.m1, l1);
             }
-            // the QJL bits of tokens lane / 4 and 8 + lane / 4
-            uint32_t qb[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t* kr = reinterpret_cast<const uint32_t*>(rk + ((lane >> 2) + 8 * nt) * TQ_REC_ROW);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) qb[nt][w] = kr[16 + w] >> (2 * (lane & 3));
-            }
-            __syncwarp();
-            // S1 = Q' U_k^T, S2 = Z sign^T (16 rows x 16 tokens each)
-            float s1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            __syncthreads();
             {
-                const uint32_t kt = wbase + 2 * TQ_STAGE;
-                const int mi = lane >> 3;
-                const int tokl = (mi >> 1) * 8 + (lane & 7);
-                const int qr = lane & 15, qh = lane >> 4;
+                float M0 = NEG_INF, M1 = NEG_INF;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    uint32_t qa[4], za[4], kb0, kb1, kb2, kb3;
-                    ldsm_x4(qbase + qr * 512 + (((2 * ks + qh) ^ (qr & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
-                    ldsm_x4(qbase + qr * 512 + (((16 + 2 * ks + qh) ^ (qr & 7)) << 4), za[0], za[1], za[2], za[3]);
-                    ldsm_x4(kt + tq_swz(tokl, ks * 16 + (mi & 1) * 8), kb0, kb1, kb2, kb3);
-                    mma16816_f16(s1[0], qa, kb0, kb1);
-                    mma16816_f16(s1[1], qa, kb2, kb3);
-                    const int sh = (ks & 1) * 16;
-                    mma16816_f16(s2[0], za, sign_pair(qb[0][ks >> 1] >> sh), sign_pair(qb[0][ks >> 1] >> (sh + 8)));
-                    mma16816_f16(s2[1], za, sign_pair(qb[1][ks >> 1] >> sh), sign_pair(qb[1][ks >> 1] >> (sh + 8)));
+                for (int w = 0; w < TQ_WARPS; ++w) {
+                    M0 = fmaxf(M0, sml[w * 16 + r0].x);
+                    M1 = fmaxf(M1, sml[w * 16 + r1].x);
                 }
-            }
-            // scores, mask, online softmax
-            const int32_t pos0 = (U.blk_start + (tt - U.tile_off)) * BS + 2 * (lane & 3);
-            float sc[2][4];
-            float mx0 = NEG_INF, mx1 = NEG_INF, vmax = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int32_t pos = pos0 + 8 * nt + e;
-                    const float v0 = a0 * (kn[nt][e] * s1[nt][e]) + b0 * (en[nt][e] * s2[nt][e]);
-                    const float v1 = a1 * (kn[nt][e] * s1[nt][2 + e]) + b1 * (en[nt][e] * s2[nt][2 + e]);
-                    sc[nt][e] = pos < lim0 ? v0 : NEG_INF;
-                    sc[nt][2 + e] = pos < lim1 ? v1 : NEG_INF;
-                    mx0 = fmaxf(mx0, sc[nt][e]);
-                    mx1 = fmaxf(mx1, sc[nt][2 + e]);
-                    vmax = fmaxf(vmax, vn[nt][e]);
-                }
-            }
-#pragma unroll
-            for (int m = 1; m <= 2; m <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, m));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, m));
-                vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, m));
-            }
-            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            const float u0s = n0 == NEG_INF ? 0.f : n0, u1s = n1 == NEG_INF ? 0.f : n1;
-            const float al0 = exp2f(m0 - u0s), al1 = exp2f(m1 - u1s);
-            m0 = n0;
-            m1 = n1;
-            const float vs_new = fmaxf(fmaxf(vs, vmax), 1e-30f);
-            const float rv_new = 1.f / vs_new;
-            const float g = vs * rv_new;
-            const float g0 = al0 * g, g1 = al1 * g;
-            vs = vs_new;
-            float ps0 = 0.f, ps1 = 0.f;
-            uint32_t pa[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float p[4];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    p[e] = exp2f(sc[nt][e] - u0s);
-                    p[2 + e] = exp2f(sc[nt][2 + e] - u1s);
-                    ps0 += p[e];
-                    ps1 += p[2 + e];
-                }
-                const float w0 = vn[nt][0] * rv_new, w1 = vn[nt][1] * rv_new;
-                pa[2 * nt] = pack_half2(p[0] * w0, p[1] * w1);
-                pa[2 * nt + 1] = pack_half2(p[2] * w0, p[3] * w1);
-            }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
-            if (!__all_sync(FULL, g0 == 1.f && g1 == 1.f)) {
+                const float f0 = st.m0 == NEG_INF ? 0.f : exp2f(st.m0 - M0) * st.vs;
+                const float f1 = st.m1 == NEG_INF ? 0.f : exp2f(st.m1 - M1) * st.vs;
+                float* scr = reinterpret_cast<float*>(wptr + 2 * TQ_STAGE);
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= g0;
-                    o[n][1] *= g0;
-                    o[n][2] *= g1;
-                    o[n][3] *= g1;
+                    const int col = 8 * n + 2 * (lane & 3);
+                    *reinterpret_cast<float2*>(scr + r0 * TQ_SCR_ROW + col) =
+                        make_float2(st.o[n][0] * f0, st.o[n][1] * f0);
+                    *reinterpret_cast<float2*>(scr + r1 * TQ_SCR_ROW + col) =
+                        make_float2(st.o[n][2] * f1, st.o[n][3] * f1);
                 }
             }
-            // acc += P' U_v
+            __syncthreads();
             {
-                const uint32_t vt = wbase + 2 * TQ_STAGE + TQ_DEC_TILE;
-                const int mi = lane >> 3;
-                const int tokl = (mi & 1) * 8 + (lane & 7);
+                const int r = tid >> 3, cc = tid & 7;
+                const int32_t prow = U.prow_base + (c - U.cfirst) * U.n_rows + r;
+                if (r < U.n_rows) {
 #pragma unroll
-                for (int np = 0; np < 8; ++np) {
-                    uint32_t v0r, v1r, v2r, v3r;
-                    ldsm_x4_t(vt + tq_swz(tokl, np * 16 + (mi >> 1) * 8), v0r, v1r, v2r, v3r);
-                    mma16816_f16(o[2 * np], pa, v0r, v1r);
-                    mma16816_f16(o[2 * np + 1], pa, v2r, v3r);
+                    for (int k = 0; k < 4; ++k) {
+                        const int col = 4 * cc + 32 * k;
+                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int w = 0; w < TQ_WARPS; ++w) {
+                            const float4 v = *reinterpret_cast<const float4*>(
+                                tq_smem + w * TQ_WARP_BYTES + 2 * TQ_STAGE + (r * TQ_SCR_ROW + col) * 4);
+                            sum.x += v.x;
+                            sum.y += v.y;
+                            sum.z += v.z;
+                            sum.w += v.w;
+                        }
+                        *reinterpret_cast<float4*>(a.part_acc + (int64_t)prow * D + col) = sum;
+                    }
+                    if (cc == 0) {
+                        float M = NEG_INF, L = 0.f;
+#pragma unroll
+                        for (int w = 0; w < TQ_WARPS; ++w) M = fmaxf(M, sml[w * 16 + r].x);
+#pragma unroll
+                        for (int w = 0; w < TQ_WARPS; ++w) {
+                            const float2 ml = sml[w * 16 + r];
+                            L += ml.x == NEG_INF ? 0.f : ml.y * exp2f(ml.x - M);
+                        }
+                        a.part_ml[prow] = make_float2(M, L);
+                    }
                 }
             }
-            __syncwarp();   // records and decoded tiles are reused by the next tile
-        }
-        cp_async_wait0();
-        // ---- merge the four warps' states and write the partial rows
-        l0 += __shfl_xor_sync(FULL, l0, 1);
-        l0 += __shfl_xor_sync(FULL, l0, 2);
-        l1 += __shfl_xor_sync(FULL, l1, 1);
-        l1 += __shfl_xor_sync(FULL, l1, 2);
-        if ((lane & 3) == 0) {
-            sml[warp * 16 + r0] = make_float2(m0, l0);
-            sml[warp * 16 + r1] = make_float2(m1, l1);
-        }
-        __syncthreads();
-        {
-            float M0 = NEG_INF, M1 = NEG_INF;
-#pragma unroll
-            for (int w = 0; w < TQ_WARPS; ++w) {
-                M0 = fmaxf(M0, sml[w * 16 + r0].x);
-                M1 = fmaxf(M1, sml[w * 16 + r1].x);
+        } else {
+            // ---- shared tiles: the CTA decodes, warp w runs its 16 rows
+            const uint32_t stage0 = sbase + TQB_STAGE_OFF;
+            unsigned char* sptr = tq_smem + TQB_STAGE_OFF;
+            unsigned char* dk = tq_smem + TQB_DEC_OFF;
+            unsigned char* dv = dk + TQ_DEC_TILE;
+            issue(t, stage0, tid, 128);
+            cp_async_commit();
+            for (int32_t tt = t, it = 0; tt < cend; ++tt, ++it) {
+                if (tt + 1 < cend) issue(tt + 1, stage0 + ((it + 1) & 1) * TQ_STAGE, tid, 128);
+                cp_async_commit();
+                cp_async_wait1();
+                __syncthreads();   // the tile's records, from every thread's copies
+                const unsigned char* rk = sptr + (it & 1) * TQ_STAGE;
+                const unsigned char* rv = rk + BS * TQ_REC_ROW;
+                tq_decode_pass(2 * warp, rk, rv, dk, dv, tab, lane);
+                tq_decode_pass(2 * warp + 1, rk, rv, dk, dv, tab, lane);
+                __syncthreads();   // the decoded tile
+                if (has_rows)
+                    tq_tile(st, sbase + TQB_Q_OFF + rbase * 512, rk, rv, sbase + TQB_DEC_OFF,
+                            sbase + TQB_DEC_OFF + TQ_DEC_TILE, (lpos + tt) * BS + 2 * (lane & 3), lim0, lim1, a0,
+                            a1, b0, b1, lane);
+                __syncthreads();   // records and decoded tile are reused by the next tile
             }
-            const float f0 = m0 == NEG_INF ? 0.f : exp2f(m0 - M0) * vs;
-            const float f1 = m1 == NEG_INF ? 0.f : exp2f(m1 - M1) * vs;
-            float* scr = reinterpret_cast<float*>(wptr + 2 * TQ_STAGE);
+            cp_async_wait0();
+            if (has_rows) {
+                float l0 = st.l0, l1 = st.l1;
+                l0 += __shfl_xor_sync(FULL, l0, 1);
+                l0 += __shfl_xor_sync(FULL, l0, 2);
+                l1 += __shfl_xor_sync(FULL, l1, 1);
+                l1 += __shfl_xor_sync(FULL, l1, 2);
+                const int32_t pbase = U.prow_base + (c - U.cfirst) * U.n_rows;
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const int col = 8 * n + 2 * (lane & 3);
-                *reinterpret_cast<float2*>(scr + r0 * TQ_SCR_ROW + col) = make_float2(o[n][0] * f0, o[n][1] * f0);
-                *reinterpret_cast<float2*>(scr + r1 * TQ_SCR_ROW + col) = make_float2(o[n][2] * f1, o[n][3] * f1);
-            }
-        }
-        __syncthreads();
-        {
-            const int r = tid >> 3, cc = tid & 7;
-            const int32_t prow = U.prow_base + (c - U.cfirst) * U.n_rows + r;
-            if (r < U.n_rows) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int col = 4 * cc + 32 * k;
-                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int w = 0; w < TQ_WARPS; ++w) {
-                        const float4 v = *reinterpret_cast<const float4*>(tq_smem + w * TQ_WARP_BYTES + 2 * TQ_STAGE +
-                                                                          (r * TQ_SCR_ROW + col) * 4);
-                        sum.x += v.x;
-                        sum.y += v.y;
-                        sum.z += v.z;
-                        sum.w += v.w;
-                    }
-                    *reinterpret_cast<float4*>(a.part_acc + (int64_t)prow * D + col) = sum;
+                for (int n = 0; n < 16; ++n) {
+                    const int col = 8 * n + 2 * (lane & 3);
+                    if (r0 < U.n_rows)
+                        *reinterpret_cast<float2*>(a.part_acc + (int64_t)(pbase + r0) * D + col) =
+                            make_float2(st.o[n][0] * st.vs, st.o[n][1] * st.vs);
+                    if (r1 < U.n_rows)
+                        *reinterpret_cast<float2*>(a.part_acc + (int64_t)(pbase + r1) * D + col) =
+                            make_float2(st.o[n][2] * st.vs, st.o[n][3] * st.vs);
                 }
-                if (cc == 0) {
-                    float M = NEG_INF, L = 0.f;
-#pragma unroll
-                    for (int w = 0; w < TQ_WARPS; ++w) M = fmaxf(M, sml[w * 16 + r].x);
-#pragma unroll
-                    for (int w = 0; w < TQ_WARPS; ++w) {
-                        const float2 ml = sml[w * 16 + r];
-                        L += ml.x == NEG_INF ? 0.f : ml.y * exp2f(ml.x - M);
-                    }
-                    a.part_ml[prow] = make_float2(M, L);
+                if ((lane & 3) == 0) {
+                    if (r0 < U.n_rows) a.part_ml[pbase + r0] = make_float2(st.m0, l0);
+                    if (r1 < U.n_rows) a.part_ml[pbase + r1] = make_float2(st.m1, l1);
                 }
             }
         }

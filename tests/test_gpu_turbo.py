@@ -143,6 +143,24 @@ def test_long_shared_prefix_over_compressed_rows(prefix, divergent):
     pool.close()
 
 
+@pytest.mark.parametrize("width,q_len", [(16, 1), (6, 2), (3, 3)])
+def test_wide_units_share_each_tiles_decode(width, q_len):
+    """More than 16 query rows per KV head on a shared prefix (16 x G 4 = 64,
+    6 x 2 x 4 = 48 and 3 x 3 x 4 = 36 rows): units of up to 64 rows whose
+    tiles the CTA decodes once for all its warps, each warp running 16 of the
+    rows (a warp past the unit's rows only decodes); causal queries for
+    q_len > 1."""
+    if q_len == 1:
+        w = W.beam(requests=2, prefix=700, width=width, divergent=20)
+    else:
+        w = W.spec_verify(requests=2, prefix=500, paths=width, draft=q_len)
+    ts, tS, signs, S = _codec(13 + width)
+    pool = pool_for(w, turbo=(ts, tS))
+    h = run_script(pool, w)
+    _check_attention(pool, h, w, signs, S, sample=[0, len(w.query) // 2, len(w.query) - 1])
+    pool.close()
+
+
 def test_multilayer_split_append_encodes_every_layer():
     w = W.beam(requests=1, prefix=40, width=2, divergent=9, n_kv=2, n_q=4)
     ts, tS, signs, S = _codec(3)
