@@ -242,6 +242,13 @@ int dendrite_append_layer(dendrite_pool* pool, int32_t layer, const void* K, con
  * DENDRITE_ELIMIT if a shared range would be read by 2^24 or more query rows
  * per KV head, or the plan outgrows 32-bit indices.
  * Reads layer 0 of a multi-layer pool.
+ * Stream order: the call's work is ordered on `stream`.  When a bf16 call
+ * has segments on both partial kernels (the tcgen05 one for segments read by
+ * more than 64 rows per KV head, the mma.sync one for the rest), the
+ * mma.sync kernel runs on a stream the pool owns, forked from `stream` and
+ * joined back into it with events before the merge, so it overlaps the
+ * tcgen05 kernel; work queued on `stream` after the call still sees the
+ * output, and a capture of `stream` takes both in.
  */
 int dendrite_tree_attn_decode(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,
                               const int32_t* branches, int32_t n_branches, void* out, void* stream);
