@@ -358,7 +358,8 @@ __global__ void __launch_bounds__(128, 16) k_append_copy(const __grid_constant__
                               int32_t row_vec, int32_t n_blocks, const int32_t* __restrict__ table,
                               const int32_t* __restrict__ call, const uint4* __restrict__ Kin0,
                               const uint4* __restrict__ Vin0, uint4* __restrict__ Kp0, uint4* __restrict__ Vp0,
-                              int64_t in_layer, int64_t pool_layer, const DevMeta* meta, int64_t n_tiles) {
+                              int64_t in_layer, int64_t pool_layer, const DevMeta* meta, int64_t n_tiles,
+                              int32_t uniform) {
     pdl_wait();
     // a grid of at most 16 CTAs per SM strides over the tiles
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -370,15 +371,23 @@ __global__ void __launch_bounds__(128, 16) k_append_copy(const __grid_constant__
     const int32_t* cow_src = call + n;
     const int32_t h = (int32_t)(tile % n_kv);
     const int32_t t = (int32_t)(tile / n_kv);   // touched-block index over the call
-    // branch i with tile_pre[i] <= t < tile_pre[i+1]
-    int32_t lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (args[2 * n + mid] <= t) lo = mid; else hi = mid - 1;
+    // branch i with tile_pre[i] <= t < tile_pre[i+1]: a division when every
+    // branch touches `uniform` blocks (decode steps: one each), else a search
+    int32_t i, t0;
+    if (uniform > 0) {
+        i = t / uniform;
+        t0 = i * uniform;
+    } else {
+        int32_t lo = 0, hi = n - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (args[2 * n + mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        i = lo;
+        t0 = args[2 * n + i];
     }
-    const int32_t i = lo;
     const int32_t L = args[n + i];
-    const int32_t lblk = L / bs + (t - args[2 * n + i]);
+    const int32_t lblk = L / bs + (t - t0);
     const int32_t s0 = lblk == L / bs ? L % bs : 0;
     const int32_t s1 = min(bs, L + n_new - lblk * bs);
     const int64_t tile_vec = (int64_t)bs * row_vec;
@@ -942,6 +951,13 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
     const int64_t n_tiles = touched * p->n_kv;
     const unsigned grid = (unsigned)std::min<int64_t>(n_tiles, (int64_t)p->sm_count * 16);
     const int64_t pool_layer = (int64_t)(p->layer_bytes / 16);
+    // blocks each branch touches, when the same for all (else 0)
+    int32_t uniform = -1;
+    for (int32_t i = 0; i < n && uniform != 0; ++i) {
+        const int32_t k = (lens[i] + n_new - 1) / bs - lens[i] / bs + 1;
+        uniform = uniform < 0 ? k : (uniform == k ? k : 0);
+    }
+    uniform = std::max(uniform, 0);
     auto fill = [&](int32_t* a) {
         int32_t acc = 0;
         for (int32_t i = 0; i < n; ++i) {
@@ -994,7 +1010,8 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
             DENDRITE_CUDA(launch_pdl(k_append_copy<decltype(args)>, dim3(grid, (unsigned)n_layers_in), dim3(128), 0,
                                      s, args, n, n_new, bs, p->bpb, p->n_kv, row_vec, (int32_t)p->num_blocks,
                                      (const int32_t*)p->d_table, (const int32_t*)p->d_call_i32, (const uint4*)K,
-                                     (const uint4*)V, kp, vp, in_layer, pool_layer, (const DevMeta*)p->d_meta, n_tiles));
+                                     (const uint4*)V, kp, vp, in_layer, pool_layer, (const DevMeta*)p->d_meta, n_tiles,
+                                     uniform));
             prof_end(p, T_APPEND_COPY, s);
         }
         return DENDRITE_OK;
