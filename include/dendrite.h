@@ -248,7 +248,7 @@ int dendrite_append_layer(dendrite_pool* pool, int32_t layer, const void* K, con
  * mma.sync kernel runs on a stream the pool owns, forked from `stream` and
  * joined back into it with events before the merge, so it overlaps the
  * tcgen05 kernel; work queued on `stream` after the call still sees the
- * output, and a capture of `stream` takes both in.
+ * output.
  */
 int dendrite_tree_attn_decode(dendrite_pool* pool, const void* Q, int32_t n_q_heads, int32_t q_len,
                               const int32_t* branches, int32_t n_branches, void* out, void* stream);
