@@ -269,7 +269,8 @@ def run_ours(args):
     from copy_write_forked_gb300 import workloads as W
     pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R + 2 * nl + 16,
                 max_blocks_per_branch=(P + Dv + grow) // bs + 8,
-                turbo=W.turbo_codec(rank) if args.turbo else None, device_planning=args.device_planning)
+                turbo=W.turbo_codec(rank) if args.turbo else None, device_planning=args.device_planning,
+                tc_sms=args.tc_sms)
     # prefill (untimed): the prefixes, resident in HBM
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
@@ -730,7 +731,7 @@ def run_attention_only(args):
     g.build()
     from copy_write_forked_gb300.runner import pool_for, run_script
     w, desc = other_workload(args.workload)
-    pool = pool_for(w, extra_blocks=len(w.query) + 16, tc_min_rows=args.tc_min_rows,
+    pool = pool_for(w, extra_blocks=len(w.query) + 16, tc_min_rows=args.tc_min_rows, tc_sms=args.tc_sms,
                     fold_segments=args.fold_segments,   # room for one more token per queried branch
                     device_planning=args.device_planning)
     h = run_script(pool, w, device=dev)
@@ -1214,6 +1215,9 @@ def main():
                     help="full-path workloads: fewer requests than the configuration (a smaller case for ncu)")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
+    ap.add_argument("--tc-sms", type=int, default=0,
+                    help="SMs given to the tcgen05 kernel when both partial kernels have work (0: library "
+                         "default, an estimate picks the split or none; -1: never split)")
     ap.add_argument("--device-planning", type=int, default=0, choices=[-1, 0, 1],
                     help="bf16 attention plans: expand units and the CTA split on the device (1), on the host (-1), "
                          "or by the library's default rule (0)")

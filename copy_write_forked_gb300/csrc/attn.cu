@@ -1569,6 +1569,45 @@ constexpr int32_t kDevicePlanMaxTilesPerUnit = 32;
 // device_planning setting, a bf16 plan leaves the units and CTA split to
 // k_plan_expand (hp.device): the host then fills the segment list (SegPlan)
 // that kernel reads, and space for what it writes.
+// SMs for the tcgen05 kernel when both partial classes have work (0: all SMs,
+// the mma.sync kernel's CTAs taking each SM as its tcgen05 CTA finishes).
+// The two kernels' CTAs never share an SM (shared memory), so without a split
+// their times add up, although the tcgen05 class is bound by its tensor and
+// softmax work once its units hold 256 rows, below the HBM rate, and the
+// mma.sync class by HBM on leaves of a few rows.  Given n SMs the tcgen05
+// kernel takes about A / n (A: its SM time) and reads its bytes at B_tc n / A,
+// and the mma.sync kernel, on the other SMs, streams its bytes through the
+// bandwidth left over, at most a per-SM rate; both end at the HBM floor when
+// n = A * bandwidth / (B_tc + B_s).  The split is taken when its estimate
+// beats the kernels one after the other by 7 %.  Weights are the partition's
+// (tile_weight per tile plus the unit starts); the ns per weight are fitted
+// to the kernels on GB300 (tcgen05: 255 ns per 16-token tile of a 256-row
+// unit per SM; mma.sync: 60 ns per 4-row tile per CTA, two CTAs per SM).
+int split_tc_sms(const dendrite_pool* p, int64_t w_tc, int64_t w_small, int64_t tiles_tc, int64_t tiles_small) {
+    const int sms = p->sm_count;
+    if (p->tc_sms < 0 || sms < 2) return 0;
+    if (p->tc_sms > 0) return p->tc_sms < sms ? p->tc_sms : 0;
+    constexpr double kTcNsPerWeight = 85.0, kSmallNsPerWeight = 30.0;   // SM ns
+    constexpr double kHbmBytesPerNs = 6700.0;                           // measured copy bandwidth
+    constexpr double kSmallBytesPerNsPerSm = 70.0;                      // one SM's two mma.sync CTAs
+    const double tile_bytes = 2.0 * p->block_size * p->head_dim * 2;   // K and V of one kv head, bf16
+    const double A = (double)w_tc * kTcNsPerWeight, S = (double)w_small * kSmallNsPerWeight;
+    const double Bt = (double)tiles_tc * tile_bytes, Bs = (double)tiles_small * tile_bytes;
+    const double serial = std::max(A / sms, Bt / kHbmBytesPerNs) + std::max(S / sms, Bs / kHbmBytesPerNs);
+    const double floor_ns = (Bt + Bs) / kHbmBytesPerNs;
+    double best = serial;
+    int best_n = 0;
+    for (int n = 1; n < sms; ++n) {
+        const int m = sms - n;
+        const double t = std::max(std::max(A / n, S / m), std::max(floor_ns, Bs / (m * kSmallBytesPerNsPerSm)));
+        if (t < best) {
+            best = t;
+            best_n = n;
+        }
+    }
+    return best < 0.93 * serial ? best_n : 0;
+}
+
 int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_len, int32_t nq, int max_ctas,
                 int max_tc_ctas, HostPlan& hp, bool allow_device) {
     const int32_t G = nq / p->n_kv, nkv = p->n_kv;
@@ -1664,9 +1703,20 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
         pc.s_hi = (int32_t)hp.segplan.size();
         pc.tiles = (int32_t)tile_off;
         pc.weight = weight;
-        const int maxc = pass == 0 ? max_tc_ctas : max_ctas;
-        pc.c0 = pc.u_hi > pc.u_lo ? class_ctas(weight, maxc, cwt) : 0;
         if (pass == 0) hp.n_tc_units = n_unit;
+    }
+    {
+        PlanClass& ct = hp.hdr.cls[0];
+        PlanClass& cs = hp.hdr.cls[1];
+        if (ct.u_hi > ct.u_lo && cs.u_hi > cs.u_lo) {
+            const int n = split_tc_sms(p, ct.weight, cs.weight, ct.tiles, cs.tiles);
+            if (n > 0) {
+                max_tc_ctas = std::min(max_tc_ctas, n);
+                max_ctas = std::min(max_ctas, (p->sm_count - n) * p->attn_ctas_per_sm);
+            }
+        }
+        ct.c0 = ct.u_hi > ct.u_lo ? class_ctas(ct.weight, max_tc_ctas, kTcWeights) : 0;
+        cs.c0 = cs.u_hi > cs.u_lo ? class_ctas(cs.weight, max_ctas, kSmallWeights) : 0;
     }
     if (n_rows >= INT32_MAX / 2) return DENDRITE_ELIMIT;
     hp.hdr.n_units = n_unit;

@@ -228,6 +228,7 @@ struct dendrite_pool {
     int sm_count = 0;
     int attn_ctas_per_sm = 1;
     int32_t tc_min_rows = dendrite::kTcMinRowsDefault;   // < 0: tensor-core attention kernel off
+    int32_t tc_sms = 0;   // SMs of the tcgen05 kernel beside the mma.sync one (0: estimated, -1: no split)
     int32_t fold_pct = dendrite::kFoldPctDefault;        // < 0: segments are never folded
     int32_t device_planning = 0;                         // 0 auto, 1 always, -1 never (bf16 plans)
 

@@ -44,7 +44,7 @@ class DendriteError(RuntimeError):
 
 class _Opts(ctypes.Structure):
     _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("tc_min_rows", _i32),
-                ("n_layers", _i32), ("fold_segments", _i32), ("device_planning", _i32), ("reserved", _i32 * 2)]
+                ("n_layers", _i32), ("fold_segments", _i32), ("device_planning", _i32), ("tc_sms", _i32), ("reserved", _i32 * 1)]
 
 
 class _PlanStats(ctypes.Structure):
@@ -151,7 +151,7 @@ class Pool:
     def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
                  dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
                  max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0, n_layers: int = 1,
-                 fold_segments: int = 0, turbo=None, device_planning: int = 0):
+                 fold_segments: int = 0, turbo=None, device_planning: int = 0, tc_sms: int = 0):
         """``turbo``: (rotation signs [128], QJL matrix [128][128]) to store
         compressed blocks (dendrite_pool_create_turbo); the calls then take
         bf16 tensors."""
@@ -162,7 +162,7 @@ class Pool:
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
         opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows), int(n_layers),
-                     int(fold_segments), int(device_planning))
+                     int(fold_segments), int(device_planning), int(tc_sms))
         self.n_layers = int(n_layers)
         self.turbo = turbo is not None
         h = ctypes.c_void_p()

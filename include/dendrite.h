@@ -96,7 +96,15 @@ typedef struct dendrite_pool_opts {
                                     * 32 tiles per unit, whose host expansion rivals the  *
                                     * kernels' work), 1 = always, -1 = never.  The result *
                                     * is the same plan either way.                        */
-    int32_t reserved[2];           /* must be zero                                         */
+    int32_t tc_sms;                /* bf16 attention calls with work for both partial     *
+                                    * kernels: SMs given to the tcgen05 kernel (one CTA   *
+                                    * each) while the mma.sync kernel's CTAs take the     *
+                                    * others, so the two run side by side.  0 = default   *
+                                    * (an estimate of both kernels' time picks the split, *
+                                    * or none: then each SM goes to the mma.sync kernel   *
+                                    * when its tcgen05 CTA finishes); k > 0 = k SMs (no   *
+                                    * split from the SM count up); -1 = never split.      */
+    int32_t reserved[1];           /* must be zero                                         */
 } dendrite_pool_opts;
 
 /*

@@ -65,3 +65,19 @@ def test_pool_calls_reject_null_pool_without_gpu():
     assert L.dendrite_sync(None, None) == -1
     assert L.dendrite_pool_destroy(None) == -1
     assert L.dendrite_free(None, None, 0, None) == -1
+
+
+def test_pool_options_are_checked_before_any_device_call():
+    """Out-of-range pool options fail with EINVAL before the pool touches a
+    device (so this runs without a GPU)."""
+    import ctypes
+    from copy_write_forked_gb300 import dendrite
+    L = dendrite.lib()
+    h = ctypes.c_void_p()
+    for field, bad in (("tc_sms", -2), ("device_planning", 2), ("fold_segments", -2), ("tc_min_rows", -2)):
+        o = dendrite._Opts()
+        setattr(o, field, bad)
+        assert L.dendrite_pool_create(64, 16, 8, 128, 1, ctypes.byref(o), ctypes.byref(h)) == -1, field
+    o = dendrite._Opts()
+    o.reserved[0] = 1
+    assert L.dendrite_pool_create(64, 16, 8, 128, 1, ctypes.byref(o), ctypes.byref(h)) == -1

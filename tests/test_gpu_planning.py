@@ -259,3 +259,35 @@ def test_decode_loop_forking_every_leaf_keeps_the_tree_flat():
         leaves = br
     assert len(set(segs)) == 1 and segs[0] <= R + R * Wd, segs
     pool.close()
+
+
+@pytest.mark.parametrize("tc_sms", [-1, 0, 40, 100])
+def test_sm_split_between_the_partial_kernels(tc_sms):
+    """A tree with work for both partial kernels (a 64-way fork: 256 rows per
+    KV head on the shared prefix, 4-row leaves) with the tcgen05 kernel given
+    tc_sms SMs and the mma.sync kernel the others' CTA slots: the class CTA
+    counts stay within the split, device and host expansion agree bit for
+    bit, and the output matches the oracle."""
+    from _harness import check_attention
+    from copy_write_forked_gb300.runner import run_script
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    w = W.fork_stress_attention(requests=2, prefix=2048, width=64, divergent=120)
+    outs, stats = [], []
+    for dev in (1, -1):
+        pool = pool_for(w, device_planning=dev, tc_sms=tc_sms)
+        h = run_script(pool, w)
+        out = pool.tree_attn_decode(w.q("cuda"), [h[b] for b in w.query])
+        pool.sync()
+        outs.append(out.clone())
+        stats.append(pool.last_plan_stats())
+        pool.close()
+    assert torch.equal(outs[0], outs[1])
+    for key in STAT_KEYS:
+        assert stats[0][key] == stats[1][key], (key, stats[0][key], stats[1][key])
+    st = stats[0]
+    assert st["n_tc_units"] == 2 * 8 and st["n_ctas"] > 0
+    if tc_sms > 0:
+        assert st["n_tc_ctas"] <= tc_sms and st["n_ctas"] <= 2 * (sms - tc_sms)
+    elif tc_sms < 0:
+        assert st["n_tc_ctas"] > tc_sms and st["n_tc_ctas"] + st["n_ctas"] > sms
+    check_attention(w, outs[0], list(range(0, len(w.query), 7)), TOL)
