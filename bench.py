@@ -270,7 +270,7 @@ def run_ours(args):
     pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R + 2 * nl + 16,
                 max_blocks_per_branch=(P + Dv + grow) // bs + 8,
                 turbo=W.turbo_codec(rank) if args.turbo else None, device_planning=args.device_planning,
-                tc_sms=args.tc_sms)
+                tc_sms=args.tc_sms, pack_segments=args.pack_segments)
     # prefill (untimed): the prefixes, resident in HBM
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
@@ -628,7 +628,8 @@ def run_decode_layers(args):
     nq, nkv, d, bs = w.n_q_heads, w.n_kv_heads, w.head_dim, w.block_size
     nblocks = R * (P // bs + 1) + R * Wd * (Dv // bs + 2) + 64
     pool = Pool(nblocks, bs, nkv, d, torch.bfloat16, max_branches=R * (Wd + 1) + 8,
-                max_blocks_per_branch=(P + Dv) // bs + 8, n_layers=NL, device_planning=args.device_planning)
+                max_blocks_per_branch=(P + Dv) // bs + 8, n_layers=NL, device_planning=args.device_planning,
+                pack_segments=args.pack_segments)
     roots = [pool.new_branch() for _ in range(R)]
     prefill_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == P)
     div_idx = next(i for i, op in enumerate(w.ops) if op.kind == "append" and op.n_new == Dv)
@@ -732,6 +733,7 @@ def run_attention_only(args):
     from copy_write_forked_gb300.runner import pool_for, run_script
     w, desc = other_workload(args.workload)
     pool = pool_for(w, extra_blocks=len(w.query) + 16, tc_min_rows=args.tc_min_rows, tc_sms=args.tc_sms,
+                    pack_segments=args.pack_segments,
                     fold_segments=args.fold_segments,   # room for one more token per queried branch
                     device_planning=args.device_planning)
     h = run_script(pool, w, device=dev)
@@ -833,7 +835,8 @@ def run_mcts_loop(args):
     from copy_write_forked_gb300 import workloads as W
     from copy_write_forked_gb300.runner import pool_for
     w = W.mcts(iters=args.mcts_iters)
-    pool = pool_for(w, fold_segments=args.fold_segments, device_planning=args.device_planning)
+    pool = pool_for(w, fold_segments=args.fold_segments, device_planning=args.device_planning,
+                    pack_segments=args.pack_segments)
     gen = torch.Generator(device=dev).manual_seed(77)
     maxq = len(w.query)
     Qall = torch.randn((maxq, 1, w.n_q_heads, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
@@ -1215,6 +1218,9 @@ def main():
                     help="full-path workloads: fewer requests than the configuration (a smaller case for ncu)")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="segments with more query rows per KV head use the tcgen05 kernel (0: default 64, -1: off)")
+    ap.add_argument("--pack-segments", type=int, default=0,
+                    help="pack a segment's leaf followers into it as masked tiles (0: default, k: below k percent "
+                         "of the estimate, -1: off)")
     ap.add_argument("--tc-sms", type=int, default=0,
                     help="SMs given to the tcgen05 kernel when both partial kernels have work (0: library "
                          "default, an estimate picks the split or none; -1: never split)")

@@ -37,6 +37,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <climits>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -54,7 +55,11 @@ constexpr int STAGE_BYTES = 4 * SLOT_BYTES;
 constexpr int NCONS = 4;
 constexpr int THREADS = (NCONS + 1) * 32;
 constexpr int ML_BYTES = NCONS * 16 * 2 * 4;
+constexpr int INFO_BYTES = NSTAGE * 4 * 16;  // per stage and tile: logical block, 64-bit row mask
+// plans with packed units also hold the tile info (INFO_BYTES more): kept
+// out of the others, which stay within the smaller shared-memory carveout
 constexpr size_t SMEM_BF16 = 1024 + (size_t)NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8 + ML_BYTES;
+constexpr size_t SMEM_BF16_PACKED = SMEM_BF16 + INFO_BYTES;
 
 
 // ------------------------------------------------ log-sum-exp merge of one row
@@ -211,10 +216,11 @@ struct ConsumerCtx {
     const AttnArgs* a;
     uint32_t base, bar_full, bar_empty;
     volatile int* abortp;
+    const int4* info;   // [NSTAGE][4]: each tile's logical block and row mask, written by the producer
     int warp, lane, c;
 };
 
-template <int P>
+template <int P, bool PACKED>
 __device__ __forceinline__ void consume_chunk(const ConsumerCtx& x, const AttnUnit& U, int32_t t, int32_t cend,
                                               int32_t& stage) {
     constexpr int NCOL = D / P, NT = NCOL / 8;   // columns and 8-column n-tiles of this warp
@@ -280,16 +286,27 @@ __device__ __forceinline__ void consume_chunk(const ConsumerCtx& x, const AttnUn
                     mma16816(sc[1], qa[ks], b2, b3);
                 }
             }
-            // scale, mask by per-row visibility, online softmax
-            const int32_t pos0 = (U.blk_start + (st - U.tile_off) + ti) * BS + (lane & 3) * 2;
+            // scale, mask by per-row visibility (the row's limit; in a
+            // packed unit also the tile's rows), online softmax
+            int32_t pos0, vl0 = lim0, vl1 = lim1;
+            if (PACKED) {
+                const int4 inf = x.info[slot * 4 + ti];
+                pos0 = inf.x * BS + (lane & 3) * 2;
+                const uint64_t rmask = (uint64_t)(uint32_t)inf.y | (uint64_t)(uint32_t)inf.z << 32;
+                const int row0 = r * 16 + (lane >> 2);
+                vl0 = (rmask >> row0) & 1u ? lim0 : INT_MIN;
+                vl1 = (rmask >> (row0 + 8)) & 1u ? lim1 : INT_MIN;
+            } else {
+                pos0 = (U.blk_start + (st - U.tile_off) + ti) * BS + (lane & 3) * 2;
+            }
             float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int32_t pos = pos0 + nt * 8 + e;
-                    sc[nt][e] = pos < lim0 ? sc[nt][e] * a.scale_log2 : NEG_INF;
-                    sc[nt][2 + e] = pos < lim1 ? sc[nt][2 + e] * a.scale_log2 : NEG_INF;
+                    sc[nt][e] = pos < vl0 ? sc[nt][e] * a.scale_log2 : NEG_INF;
+                    sc[nt][2 + e] = pos < vl1 ? sc[nt][2 + e] * a.scale_log2 : NEG_INF;
                     mx0 = fmaxf(mx0, sc[nt][e]);
                     mx1 = fmaxf(mx1, sc[nt][2 + e]);
                 }
@@ -372,6 +389,10 @@ __device__ __forceinline__ void consume_chunk(const ConsumerCtx& x, const AttnUn
 }
 
 // ============================================================ bf16 kernel
+// PACKED: the plan has packed units; the producer then writes every tile's
+// logical block and row mask into shared memory and the consumers mask by
+// them (plans without packed units run without that step or its memory).
+template <bool PACKED>
 __global__ void __launch_bounds__(THREADS, 2)
 k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const AttnArgs a) {
@@ -383,6 +404,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const uint32_t bar_full = base + NSTAGE * STAGE_BYTES;
     const uint32_t bar_empty = bar_full + NSTAGE * 8;
     float* ml = reinterpret_cast<float*>(sm + NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8);
+    int4* info = reinterpret_cast<int4*>(sm + NSTAGE * STAGE_BYTES + 2 * NSTAGE * 8 + ML_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -410,8 +432,12 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     if (warp == NCONS) {
         // ------------------------------------------------------ producer
         // Each stage is up to 4 consecutive tiles (blocks x one kv head) of
-        // one unit; lane i reads tile i's block id and issues its four TMA
-        // boxes (K and V, two 64-column halves each).
+        // one unit; lane i reads tile i's block id (for a packed unit's extra
+        // tile through its entry in the plan, which also gives the tile's
+        // logical block and member mask), writes the tile's logical block
+        // and the mask of the unit's rows that see it for the consumers, and
+        // after the stage's arrival issues its four TMA boxes (K and V, two
+        // 64-column halves each).
         uint32_t issued = 0, parity_bits = 0;
         int32_t stage = 0;
         int32_t t = t_begin, u = u0;
@@ -421,6 +447,14 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             if (t >= uend) { ++u; continue; }
             const int32_t cend = min(t_end, uend);
             const int32_t* trow = a.table + (int64_t)U.table_row * a.bpb + U.blk_start - U.tile_off;
+            // packed: the entry of this lane's extra tile in the next stage,
+            // loaded one stage ahead (the block id load still depends on it)
+            AttnXTile pre{0, 0u, 0, 0};
+            auto prefetch = [&](int32_t tt) {
+                const int32_t ti = tt - U.tile_off;
+                if (PACKED && lane < 4 && tt < cend && ti >= U.n_shared) pre = pl.xtiles[U.x_off + ti - U.n_shared];
+            };
+            prefetch(t + lane);
             for (int32_t st = t; st < cend; st += 4, ++stage) {
                 const int slot = stage % NSTAGE;
                 const uint32_t ph = (uint32_t)(stage / NSTAGE) & 1u;
@@ -435,10 +469,38 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && !*abortp;
                 if (!ok) continue;
-                if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
-                __syncwarp();
+                int32_t blk = 0;
+                if (!PACKED) {
+                    if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
+                    __syncwarp();
+                    if (lane < ntiles) blk = trow[st + lane];
+                } else if (lane < ntiles) {
+                    const int32_t ti = st + lane - U.tile_off;
+                    int4 inf;
+                    if (ti < U.n_shared) {
+                        blk = trow[st + lane];
+                        inf = make_int4(U.blk_start + ti, -1, -1, 0);
+                    } else {
+                        // packed units hold one row group: row k belongs to member k / (q_len G)
+                        const AttnXTile e = pre;
+                        blk = a.table[(int64_t)e.table_row * a.bpb + e.blk];
+                        const int32_t RM = pl.q_len * pl.group;
+                        const uint64_t one = RM >= 64 ? ~0ull : (1ull << RM) - 1ull;
+                        uint64_t rm = 0;
+                        for (uint32_t mm = e.mask; mm; mm &= mm - 1u) {
+                            const int32_t m = __ffs(mm) - 1;
+                            if (m * RM < 64) rm |= one << (m * RM);
+                        }
+                        inf = make_int4(e.blk, (int32_t)(uint32_t)rm, (int32_t)(uint32_t)(rm >> 32), 0);
+                    }
+                    info[slot * 4 + lane] = inf;
+                }
+                if (PACKED) {
+                    __syncwarp();   // the tile info is written before the stage's arrival releases it
+                    if (lane == 0) mbar_expect_tx(bar_full + 8 * slot, (uint32_t)(ntiles * SLOT_BYTES));
+                    __syncwarp();
+                }
                 if (lane < ntiles) {
-                    int32_t blk = trow[st + lane];
                     if ((uint32_t)blk >= (uint32_t)a.n_blocks) {   // broken table: poison, read zeros
                         atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                         blk = -1;
@@ -453,6 +515,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 }
                 issued |= 1u << slot;
                 parity_bits = (parity_bits & ~(1u << slot)) | (ph << slot);
+                prefetch(st + 4 + lane);
             }
             t = cend;
             ++u;
@@ -481,7 +544,7 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
     int32_t stage = 0;
     int32_t t = t_begin, u = u0;
-    const ConsumerCtx ctx{&a, base, bar_full, bar_empty, abortp, warp, lane, c};
+    const ConsumerCtx ctx{&a, base, bar_full, bar_empty, abortp, info, warp, lane, c};
     while (t < t_end) {
         const AttnUnit U = pl.units[u];
         const int32_t uend = U.tile_off + U.n_blk;
@@ -489,8 +552,8 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int32_t cend = min(t_end, uend);
         if (U.rt != 1) {
             // 32 or 64 rows: the warps of a row tile split head_dim (no exchange)
-            if (U.rt == 2) consume_chunk<2>(ctx, U, t, cend, stage);
-            else consume_chunk<1>(ctx, U, t, cend, stage);
+            if (U.rt == 2) consume_chunk<2, PACKED>(ctx, U, t, cend, stage);
+            else consume_chunk<1, PACKED>(ctx, U, t, cend, stage);
             t = cend;
             ++u;
             continue;
@@ -556,16 +619,25 @@ k_attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                         mma16816(s[1], qa[ks], b2, b3);
                     }
                 }
-                // scale, mask by per-row visibility, online softmax
-                const int32_t pos0 = (U.blk_start + (st - U.tile_off) + ti) * BS + (lane & 3) * 2;
+                // scale, mask by per-row visibility (the row's limit; in a
+                // packed unit also the tile's rows), online softmax
+                int32_t pos0, vl0 = lim0, vl1 = lim1;
+                if (PACKED) {
+                    const int4 inf = info[slot * 4 + ti];
+                    pos0 = inf.x * BS + (lane & 3) * 2;
+                    vl0 = ((uint32_t)inf.y >> (lane >> 2)) & 1u ? lim0 : INT_MIN;
+                    vl1 = ((uint32_t)inf.y >> ((lane >> 2) + 8)) & 1u ? lim1 : INT_MIN;
+                } else {
+                    pos0 = (U.blk_start + (st - U.tile_off) + ti) * BS + (lane & 3) * 2;
+                }
                 float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int32_t pos = pos0 + nt * 8 + e;
-                        s[nt][e] = pos < lim0 ? s[nt][e] * a.scale_log2 : NEG_INF;
-                        s[nt][2 + e] = pos < lim1 ? s[nt][2 + e] * a.scale_log2 : NEG_INF;
+                        s[nt][e] = pos < vl0 ? s[nt][e] * a.scale_log2 : NEG_INF;
+                        s[nt][2 + e] = pos < vl1 ? s[nt][2 + e] * a.scale_log2 : NEG_INF;
                         mx0 = fmaxf(mx0, s[nt][e]);
                         mx1 = fmaxf(mx1, s[nt][2 + e]);
                     }
@@ -1105,8 +1177,10 @@ struct SegPlan {
     int32_t mem_off;
     int32_t row_base;         // rows of all units before this segment's (tensor-core class first)
     int32_t w_full, w_last;   // weight of one unit of a full row group / of the last one
+    int32_t n_shared, x_off;  // packed segments: tiles of the table row, first extra tile
+    int32_t pad[2];
 };
-static_assert(sizeof(SegPlan) == 64, "SegPlan layout");
+static_assert(sizeof(SegPlan) == 80, "SegPlan layout");
 
 // A class of units (0: tcgen05, 1: mma.sync / fp32) for the CTA split.
 struct PlanClass {
@@ -1369,7 +1443,9 @@ __global__ void __launch_bounds__(kExpandThreads) k_plan_expand(const ExpandArgs
         U.blk_start = g.blk_start;
         U.n_blk = g.n_blk;
         U.mem_off = g.mem_off;
-        U.pad[0] = U.pad[1] = U.pad[2] = 0;
+        U.n_shared = g.n_shared;
+        U.x_off = g.x_off;
+        U.pad = 0;
         x.units[u] = U;
     }
 }
@@ -1409,12 +1485,16 @@ struct HostPlan {
     size_t partial_rows = 0;
     std::vector<int32_t> parent, fork_len, len, queried, seg_members, cursor;
     std::vector<Segment> psegs;
+    std::vector<ExtraTile> pxt;      // the planner's extra tiles of packed segments
+    std::vector<AttnXTile> xtiles;   // the same for the kernels (branch handles)
     std::vector<SegPlan> segplan;
     PlanHeader hdr{};
     bool device = false;       // units and CTA split left to the device
+    bool small_packed = false; // a packed segment in the mma.sync class
     void clear() {   // keeps capacity: plans are rebuilt whenever the tree changes; the unit and
                      // member arrays keep their size too (build_plan resizes and fills them in place)
-        segs.clear(); cta_begin.clear(); cta_unit.clear(); segplan.clear(); device = false;
+        segs.clear(); cta_begin.clear(); cta_unit.clear(); segplan.clear(); device = false; small_packed = false;
+        pxt.clear(); xtiles.clear();
         tc_cta_begin.clear(); tc_cta_unit.clear(); path_off.clear(); path.clear(); cuts.clear();
         tiles = unique_tiles = 0;
         n_tc_units = 0;
@@ -1537,6 +1617,9 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     // distinct tiles: the sharing segments before folding read each (block,
     // kv head) pair once
     for (const Segment& sg : hp.psegs) hp.unique_tiles += (int64_t)sg.block_count * nkv;
+    if (bf16 && p->pack_pct >= 0)
+        pack_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, p->pack_pct, n_nodes,
+                      hp.parent.data(), hp.fork_len.data(), p->block_size, hp.psegs, hp.seg_members, hp.pxt);
     if (p->fold_pct >= 0)
         fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, n_nodes,
                       hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
@@ -1624,8 +1707,9 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
         const int32_t rows_per_head = sg.n_members * RM;
         const int32_t group_rows = (tc_on && rows_per_head > p->tc_min_rows) ? kMaxUnitRowsTc : small_rows;
         const size_t units = (size_t)nkv * ((rows_per_head + group_rows - 1) / group_rows);
+        if (sg.n_x && units != (size_t)nkv) return DENDRITE_EINVAL;   // packed: one row group per kv head
         n_units_total += units;
-        n_tiles_total += units * (size_t)sg.block_count;
+        n_tiles_total += units * (size_t)(sg.block_count + sg.n_x);
         n_members_total += sg.n_members;
     }
     if (n_units_total >= (size_t)INT32_MAX / 2) return DENDRITE_ELIMIT;
@@ -1663,7 +1747,7 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
             AttnSeg S;
             S.table_row = p->nodes[sg.rep_node].handle;
             S.blk_start = sg.block_start;
-            S.n_blk = sg.block_count;
+            S.n_blk = sg.block_count + sg.n_x;
             S.mem_off = n_mem;
             S.n_mem = sg.n_members;
             S.unit_base = n_unit;
@@ -1686,6 +1770,14 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
             sp.table_row = S.table_row;
             sp.blk_start = S.blk_start;
             sp.mem_off = S.mem_off;
+            sp.n_shared = sg.block_count;
+            sp.x_off = (int32_t)hp.xtiles.size();
+            sp.pad[0] = sp.pad[1] = 0;
+            if (pass == 1 && sg.n_x) hp.small_packed = true;
+            for (int32_t k = 0; k < sg.n_x; ++k) {
+                const ExtraTile& e = hp.pxt[sg.x_off + k];
+                hp.xtiles.push_back(AttnXTile{e.blk, e.mask, p->nodes[e.rep_node].handle, 0});
+            }
             sp.row_base = (int32_t)n_rows;
             sp.wbase = weight;
             sp.w_full = (int32_t)(start_weight(cwt, group_rows) + (int64_t)S.n_blk * tile_weight(sp.rt_full));
@@ -1751,7 +1843,9 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
                     U.blk_start = sp.blk_start;
                     U.n_blk = sp.n_blk;
                     U.mem_off = sp.mem_off;
-                    U.pad[0] = U.pad[1] = U.pad[2] = 0;
+                    U.n_shared = sp.n_shared;
+                    U.x_off = sp.x_off;
+                    U.pad = 0;
                 }
             }
         }
@@ -1829,14 +1923,18 @@ int encode_pool_map(dendrite_pool* p, void* base, unsigned char* out) {
 // device expansion); from kPlanDeviceSection on, the units, CTA splits and
 // counts, which k_plan_expand writes when the plan is expanded on the device
 // (only the prefix before them is then uploaded).
-constexpr int kPlanSections = 12;
-constexpr int kPlanDeviceSection = 6;
+enum PlanSection {
+    SEC_SEGS, SEC_MEMBERS, SEC_PATH_OFF, SEC_PATH, SEC_SEGPLAN, SEC_HEADER, SEC_XTILES,
+    SEC_UNITS, SEC_CTA_BEGIN, SEC_CTA_UNIT, SEC_TC_BEGIN, SEC_TC_UNIT, SEC_COUNTS, kPlanSections
+};
+constexpr int kPlanDeviceSection = SEC_UNITS;
 size_t plan_layout(const HostPlan& hp, size_t (&off)[kPlanSections + 1]) {
     const size_t sz[kPlanSections] = {
         hp.segs.size() * sizeof(AttnSeg),     hp.members.size() * sizeof(AttnMember),
         hp.path_off.size() * 4,               hp.path.size() * 4,
         hp.device ? hp.segplan.size() * sizeof(SegPlan) : 0,
         hp.device ? sizeof(PlanHeader) : 0,
+        hp.xtiles.size() * sizeof(AttnXTile),
         hp.units.size() * sizeof(AttnUnit),   hp.cta_begin.size() * 4,
         hp.cta_unit.size() * 4,               hp.tc_cta_begin.size() * 4,
         hp.tc_cta_unit.size() * 4,            hp.device ? 4 * sizeof(int32_t) : 0};
@@ -1858,35 +1956,38 @@ void plan_pack(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], char*
     auto put = [&](int k, const void* src, size_t bytes) {
         if (bytes) std::memcpy(h + off[k], src, bytes);
     };
-    put(0, hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
-    put(1, hp.members.data(), hp.members.size() * sizeof(AttnMember));
-    put(2, hp.path_off.data(), hp.path_off.size() * 4);
-    put(3, hp.path.data(), hp.path.size() * 4);
+    put(SEC_SEGS, hp.segs.data(), hp.segs.size() * sizeof(AttnSeg));
+    put(SEC_MEMBERS, hp.members.data(), hp.members.size() * sizeof(AttnMember));
+    put(SEC_PATH_OFF, hp.path_off.data(), hp.path_off.size() * 4);
+    put(SEC_PATH, hp.path.data(), hp.path.size() * 4);
+    put(SEC_XTILES, hp.xtiles.data(), hp.xtiles.size() * sizeof(AttnXTile));
     if (hp.device) {
-        put(4, hp.segplan.data(), hp.segplan.size() * sizeof(SegPlan));
-        put(5, &hp.hdr, sizeof(PlanHeader));
+        put(SEC_SEGPLAN, hp.segplan.data(), hp.segplan.size() * sizeof(SegPlan));
+        put(SEC_HEADER, &hp.hdr, sizeof(PlanHeader));
         return;
     }
-    put(6, hp.units.data(), hp.units.size() * sizeof(AttnUnit));
-    put(7, hp.cta_begin.data(), hp.cta_begin.size() * 4);
-    put(8, hp.cta_unit.data(), hp.cta_unit.size() * 4);
-    put(9, hp.tc_cta_begin.data(), hp.tc_cta_begin.size() * 4);
-    put(10, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
+    put(SEC_UNITS, hp.units.data(), hp.units.size() * sizeof(AttnUnit));
+    put(SEC_CTA_BEGIN, hp.cta_begin.data(), hp.cta_begin.size() * 4);
+    put(SEC_CTA_UNIT, hp.cta_unit.data(), hp.cta_unit.size() * 4);
+    put(SEC_TC_BEGIN, hp.tc_cta_begin.data(), hp.tc_cta_begin.size() * 4);
+    put(SEC_TC_UNIT, hp.tc_cta_unit.data(), hp.tc_cta_unit.size() * 4);
 }
 
 AttnPlanDev plan_view(const HostPlan& hp, const size_t (&off)[kPlanSections + 1], const char* d, int32_t n,
                       int32_t q_len, int32_t nq, int32_t group) {
     AttnPlanDev v{};
-    v.segs = reinterpret_cast<const AttnSeg*>(d + off[0]);
-    v.members = reinterpret_cast<const AttnMember*>(d + off[1]);
-    v.path_off = reinterpret_cast<const int32_t*>(d + off[2]);
-    v.path = reinterpret_cast<const int32_t*>(d + off[3]);
-    v.units = reinterpret_cast<const AttnUnit*>(d + off[6]);
-    v.cta_begin = reinterpret_cast<const int32_t*>(d + off[7]);
-    v.cta_unit = reinterpret_cast<const int32_t*>(d + off[8]);
-    v.tc_cta_begin = reinterpret_cast<const int32_t*>(d + off[9]);
-    v.tc_cta_unit = reinterpret_cast<const int32_t*>(d + off[10]);
-    v.counts = hp.device ? reinterpret_cast<const int32_t*>(d + off[11]) : nullptr;
+    v.segs = reinterpret_cast<const AttnSeg*>(d + off[SEC_SEGS]);
+    v.members = reinterpret_cast<const AttnMember*>(d + off[SEC_MEMBERS]);
+    v.path_off = reinterpret_cast<const int32_t*>(d + off[SEC_PATH_OFF]);
+    v.path = reinterpret_cast<const int32_t*>(d + off[SEC_PATH]);
+    v.xtiles = reinterpret_cast<const AttnXTile*>(d + off[SEC_XTILES]);
+    v.units = reinterpret_cast<const AttnUnit*>(d + off[SEC_UNITS]);
+    v.cta_begin = reinterpret_cast<const int32_t*>(d + off[SEC_CTA_BEGIN]);
+    v.cta_unit = reinterpret_cast<const int32_t*>(d + off[SEC_CTA_UNIT]);
+    v.tc_cta_begin = reinterpret_cast<const int32_t*>(d + off[SEC_TC_BEGIN]);
+    v.tc_cta_unit = reinterpret_cast<const int32_t*>(d + off[SEC_TC_UNIT]);
+    v.counts = hp.device ? reinterpret_cast<const int32_t*>(d + off[SEC_COUNTS]) : nullptr;
+    v.packed = hp.small_packed ? 1 : 0;
     v.n_units = (int32_t)hp.units.size();
     v.n_ctas = (int32_t)hp.cta_unit.size();
     v.n_tc_units = hp.n_tc_units;
@@ -1915,6 +2016,7 @@ AttnPlanDev plan_rebase(AttnPlanDev v, const char* from, const char* to) {
     mv(v.tc_cta_unit);
     mv(v.path_off);
     mv(v.path);
+    mv(v.xtiles);
     if (v.counts) mv(v.counts);
     return v;
 }
@@ -1924,14 +2026,14 @@ AttnPlanDev plan_rebase(AttnPlanDev v, const char* from, const char* to) {
 int launch_plan_expand(dendrite_pool* p, char* d, const size_t* off, int32_t n_units, int32_t n_segs,
                        cudaStream_t s) {
     ExpandArgs x{};
-    x.sp = reinterpret_cast<const SegPlan*>(d + off[4]);
-    x.hdr = reinterpret_cast<const PlanHeader*>(d + off[5]);
-    x.units = reinterpret_cast<AttnUnit*>(d + off[6]);
-    x.begin = reinterpret_cast<int32_t*>(d + off[7]);
-    x.cunit = reinterpret_cast<int32_t*>(d + off[8]);
-    x.tc_begin = reinterpret_cast<int32_t*>(d + off[9]);
-    x.tc_cunit = reinterpret_cast<int32_t*>(d + off[10]);
-    x.counts = reinterpret_cast<int32_t*>(d + off[11]);
+    x.sp = reinterpret_cast<const SegPlan*>(d + off[SEC_SEGPLAN]);
+    x.hdr = reinterpret_cast<const PlanHeader*>(d + off[SEC_HEADER]);
+    x.units = reinterpret_cast<AttnUnit*>(d + off[SEC_UNITS]);
+    x.begin = reinterpret_cast<int32_t*>(d + off[SEC_CTA_BEGIN]);
+    x.cunit = reinterpret_cast<int32_t*>(d + off[SEC_CTA_UNIT]);
+    x.tc_begin = reinterpret_cast<int32_t*>(d + off[SEC_TC_BEGIN]);
+    x.tc_cunit = reinterpret_cast<int32_t*>(d + off[SEC_TC_UNIT]);
+    x.counts = reinterpret_cast<int32_t*>(d + off[SEC_COUNTS]);
     x.nkv = p->n_kv;
     DENDRITE_CUDA(launch_pdl(k_plan_expand, dim3((unsigned)std::max(1, (n_units + kExpandUnits - 1) / kExpandUnits)),
                              dim3(kExpandThreads), (size_t)n_segs * 16, s, x));
@@ -1976,7 +2078,10 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     if (beside) {
         DENDRITE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
         prof_begin(p, T_ATTN_MMA_SIDE, p->side);
-        k_attn_partial_bf16<<<dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, p->side>>>(mk, mv, a);
+        if (a.plan.packed)
+            k_attn_partial_bf16<true><<<dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16_PACKED, p->side>>>(mk, mv, a);
+        else
+            k_attn_partial_bf16<false><<<dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, p->side>>>(mk, mv, a);
         DENDRITE_CUDA(cudaGetLastError());
         prof_end(p, T_ATTN_MMA_SIDE, p->side);
         DENDRITE_CUDA(cudaEventRecord(p->ev_join, p->side));
@@ -1991,7 +2096,12 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
         DENDRITE_TRY(launch_turbo_partials(a, a.Q, n_out_rows, p->d_tq_signs, p->d_tq_S, p->d_tq_qs, s));
     } else if (a.plan.n_ctas > 0) {
         if (bf16) {
-            DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16, s, mk, mv, a));
+            if (a.plan.packed)
+                DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16<true>, dim3(a.plan.n_ctas), dim3(THREADS),
+                                         SMEM_BF16_PACKED, s, mk, mv, a));
+            else
+                DENDRITE_CUDA(launch_pdl(k_attn_partial_bf16<false>, dim3(a.plan.n_ctas), dim3(THREADS), SMEM_BF16,
+                                         s, mk, mv, a));
         } else {
             DENDRITE_CUDA(launch_pdl(k_attn_partial_f32, dim3(a.plan.n_ctas), dim3(128),
                                      2 * BS * p->head_dim * sizeof(float), s, a));
@@ -2105,11 +2215,15 @@ int attn_setup(dendrite_pool* p) {
             DENDRITE_TRY(encode_pool_map(p, static_cast<char*>(p->d_v) + off, p->tmap_v[l].bytes));
         }
         p->tmaps_ok = true;
-        DENDRITE_CUDA(cudaFuncSetAttribute(k_attn_partial_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        DENDRITE_CUDA(cudaFuncSetAttribute(k_attn_partial_bf16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BF16));
-        int occ = 0;
-        DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_bf16, THREADS, SMEM_BF16));
-        p->attn_ctas_per_sm = std::max(1, occ);
+        DENDRITE_CUDA(cudaFuncSetAttribute(k_attn_partial_bf16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BF16_PACKED));
+        int occ = 0, occ_packed = 0;
+        DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_partial_bf16<false>, THREADS, SMEM_BF16));
+        DENDRITE_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_packed, k_attn_partial_bf16<true>, THREADS,
+                                                                    SMEM_BF16_PACKED));
+        p->attn_ctas_per_sm = std::max(1, std::min(occ, occ_packed));
         p->tc_ready = attn_tc_setup() == DENDRITE_OK;
         DENDRITE_CUDA(cudaFuncSetAttribute(k_plan_expand, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kMaxExpandSegs * 16));
@@ -2189,7 +2303,7 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         const int32_t nb = (p->br[branches[i]].len + p->block_size - 1) / p->block_size;
         if (nb == pc.n_blocks[i]) continue;
         refresh = false;
-        if (nb < pc.n_blocks[i] || pc.last_seg[i] < 0) grow = false;
+        if (nb < pc.n_blocks[i] || (pc.last_seg[i] < 0 && pc.last_xt[i] < 0)) grow = false;
     }
     grow = grow && !refresh;
     if (refresh) {
@@ -2226,11 +2340,41 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
             hp.psegs = pc.segs;
             hp.seg_members = pc.seg_members;
             hp.unique_tiles = pc.unique_tiles;
+            // extra tiles to add: d more blocks after tile last_xt[i], the
+            // insertions in increasing position
+            static thread_local std::vector<std::pair<int32_t, int32_t>> ins;
+            ins.clear();
             for (int32_t i = 0; i < n; ++i) {
                 const int32_t d = (p->br[branches[i]].len + p->block_size - 1) / p->block_size - pc.n_blocks[i];
                 if (!d) continue;
-                hp.psegs[pc.last_seg[i]].block_count += d;
+                if (pc.last_seg[i] >= 0) hp.psegs[pc.last_seg[i]].block_count += d;
+                else ins.emplace_back(pc.last_xt[i], d);
                 hp.unique_tiles += (int64_t)d * p->n_kv;
+            }
+            if (ins.empty()) {
+                hp.pxt = pc.seg_xt;
+            } else {
+                std::sort(ins.begin(), ins.end());
+                hp.pxt.clear();
+                size_t k = 0;
+                for (int32_t x = 0; x < (int32_t)pc.seg_xt.size(); ++x) {
+                    const ExtraTile e = pc.seg_xt[x];
+                    hp.pxt.push_back(e);
+                    for (; k < ins.size() && ins[k].first == x; ++k)
+                        for (int32_t j = 1; j <= ins[k].second; ++j) hp.pxt.push_back(ExtraTile{e.rep_node, e.blk + j, e.mask});
+                }
+                // each packed segment's extra range moves by the tiles added before and inside it
+                k = 0;
+                int32_t added = 0;
+                for (Segment& sg : hp.psegs) {   // extra ranges are in segment order
+                    if (!sg.n_x) continue;
+                    const int32_t end = sg.x_off + sg.n_x;
+                    int32_t inside = 0;
+                    for (; k < ins.size() && ins[k].first < end; ++k) inside += ins[k].second;
+                    sg.x_off += added;
+                    sg.n_x += inside;
+                    added += inside;
+                }
             }
             DENDRITE_TRY(build_units(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp, true));
         } else {
@@ -2268,20 +2412,30 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
         pc.shape_version = p->shape_version;
         pc.buf = ib;
         pc.bytes = off[kPlanSections];
-        pc.members_off = off[1];
+        pc.members_off = off[SEC_MEMBERS];
         pc.n_members = (int32_t)hp.members.size();
         pc.n_blocks.resize(n);
         for (int32_t i = 0; i < n; ++i) pc.n_blocks[i] = (p->br[branches[i]].len + p->block_size - 1) / p->block_size;
         pc.segs = hp.psegs;
         pc.seg_members = hp.seg_members;
+        pc.seg_xt = hp.pxt;
         pc.unique_tiles = hp.unique_tiles;
         if (!grow) {   // grown segments still end at their branch's last block
             pc.last_seg.assign(n, -1);
             for (int32_t si = 0; si < (int32_t)hp.psegs.size(); ++si) {
                 const Segment& sg = hp.psegs[si];
-                if (sg.n_members != 1) continue;
+                if (sg.n_members != 1 || sg.n_x) continue;
                 const int32_t m = hp.seg_members[sg.member_offset];
                 if (sg.block_start + sg.block_count == pc.n_blocks[m]) pc.last_seg[m] = si;
+            }
+        }
+        pc.last_xt.assign(n, -1);   // extra tiles move when a grow inserts some
+        for (const Segment& sg : hp.psegs) {
+            for (int32_t x = sg.x_off; x < sg.x_off + sg.n_x; ++x) {
+                const ExtraTile& e = hp.pxt[x];
+                if (e.mask & (e.mask - 1u)) continue;   // read by several members
+                const int32_t m = hp.seg_members[sg.member_offset + __builtin_ctz(e.mask)];
+                if (e.blk == pc.n_blocks[m] - 1) pc.last_xt[m] = x;
             }
         }
         pc.q_len = q_len;
@@ -2329,7 +2483,7 @@ extern "C" int dendrite_last_plan_stats(dendrite_pool* p, dendrite_plan_stats* o
         int32_t c[4];
         DENDRITE_CUDA(cudaSetDevice(p->device));
         DENDRITE_CUDA(cudaDeviceSynchronize());
-        DENDRITE_CUDA(cudaMemcpy(c, p->d_plan[pc.buf] + pc.sec_off[11], sizeof(c), cudaMemcpyDeviceToHost));
+        DENDRITE_CUDA(cudaMemcpy(c, p->d_plan[pc.buf] + pc.sec_off[SEC_COUNTS], sizeof(c), cudaMemcpyDeviceToHost));
         pc.stats.n_ctas = c[0];
         pc.stats.n_tc_ctas = c[1];
         pc.stats.n_partials = c[2];

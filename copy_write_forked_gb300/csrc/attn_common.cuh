@@ -40,7 +40,7 @@ __device__ __forceinline__ AttnRow unit_row(const AttnPlanDev& pl, const AttnUni
     const int32_t mi = div_rcp(sr, RM, pl.rcp_rows_per_member), rem = sr - mi * RM;
     const int32_t j = div_rcp(rem, G, pl.rcp_group), g = rem - j * G;
     const AttnMember M = pl.members[U.mem_off + mi];
-    return AttnRow{(M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * G + g, M.len - pl.q_len + j + 1};
+    return AttnRow{(M.qi * pl.q_len + j) * pl.n_q_heads + U.kv_head * G + g, M.len - pl.q_len + j + 1, mi};
 }
 
 struct AttnArgs {

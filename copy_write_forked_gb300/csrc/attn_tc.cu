@@ -86,7 +86,9 @@ enum {
     B_FINAL = B_Q_FULL + 2,   // one per issuer: S0, PV0, S1, PV1
     B_COUNT = B_FINAL + 4
 };
-constexpr int SMEM_TC = 1024 + OFF_BAR + B_COUNT * 8 + 16;
+// a packed unit's extra tiles (logical block, member mask), per row tile
+constexpr int OFF_XINFO = OFF_BAR + B_COUNT * 8 + 16;
+constexpr int SMEM_TC = 1024 + OFF_XINFO + TC_ROWTILES * kMaxTcExtraTiles * 8;
 static_assert(SMEM_TC <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.f;
@@ -279,16 +281,24 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (t >= uend) { ++u; continue; }
             const int32_t cend = min(t_end, uend);
             const int32_t* trow = a.table + (int64_t)U.table_row * a.bpb + U.blk_start - U.tile_off;
+            // block id of tile t: from the unit's table row, or for a packed
+            // unit's extra tile through its entry in the plan
+            auto blk_at = [&](int32_t tt) -> int32_t {
+                const int32_t ti = tt - U.tile_off;
+                if (ti < U.n_shared) return trow[tt];
+                const AttnXTile e = pl.xtiles[U.x_off + ti - U.n_shared];
+                return a.table[(int64_t)e.table_row * a.bpb + e.blk];
+            };
             // block ids, 32 tiles per batch, the next batch loaded one batch ahead
             int32_t cur_base = t, nxt_base = t + 32;
-            int32_t cur = t + lane < cend ? trow[t + lane] : 0;
-            int32_t nxt = nxt_base + lane < cend ? trow[nxt_base + lane] : 0;
+            int32_t cur = t + lane < cend ? blk_at(t + lane) : 0;
+            int32_t nxt = nxt_base + lane < cend ? blk_at(nxt_base + lane) : 0;
             for (int32_t st = t; st < cend; st += 4, ++g) {
                 if (st >= cur_base + 32) {
                     cur = nxt;
                     cur_base = nxt_base;
                     nxt_base += 32;
-                    nxt = nxt_base + lane < cend ? trow[nxt_base + lane] : 0;
+                    nxt = nxt_base + lane < cend ? blk_at(nxt_base + lane) : 0;
                 }
                 int32_t blk = __shfl_sync(0xffffffffu, cur, (st - cur_base) + (lane & 3));
                 const int slot = g % TC_NSTAGE;
@@ -418,6 +428,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         unsigned char* sQ = sm + OFF_Q + r * TC_QTILE;
         const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.Q);
         const int row = r * 128 + trow;
+        int2* xinfo = reinterpret_cast<int2*>(sm + OFF_XINFO) + r * kMaxTcExtraTiles;
         // This thread's row of a unit's Q into the K-major swizzled tile, and
         // the row's record.  A unit's Q is staged as soon as the previous
         // chunk's last S was read (no S MMA of it is pending then), before
@@ -453,6 +464,15 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             const bool valid = row < U.n_rows;
             const AttnRow R = staged_u == u ? staged_R : stage_q(U);
+            if (U.n_blk > U.n_shared) {
+                // a packed unit: its extra tiles' logical blocks and member
+                // masks into shared memory, once every warp of the row tile
+                // is done with the previous unit's
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + r) : "memory");
+                for (int32_t i = trow; i < U.n_blk - U.n_shared; i += 128)
+                    xinfo[i] = *reinterpret_cast<const int2*>(pl.xtiles + U.x_off + i);
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + r) : "memory");
+            }
             const int32_t nst = (cend - t + 3) >> 2;
             float m_ref = -INFINITY, l = 0.f;
             for (int32_t k = 0; k < nst && ok; ++k, ++js) {
@@ -477,11 +497,31 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
                 // mask stage columns past the chunk and positions the row does
                 // not see (only stages some row of the warp does not fully see)
-                const int32_t pos0 = (U.blk_start + (st - U.tile_off)) * BS;
-                const int32_t vis = min(ntiles * BS, R.limit - pos0);
-                if (!__all_sync(0xffffffffu, vis >= TC_TOK)) {
+                const int32_t ti0 = st - U.tile_off;
+                if (ti0 + ntiles <= U.n_shared) {
+                    const int32_t vis = min(ntiles * BS, R.limit - (U.blk_start + ti0) * BS);
+                    if (!__all_sync(0xffffffffu, vis >= TC_TOK)) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) s[i] = i < vis ? s[i] : -INFINITY;
+                        for (int i = 0; i < 64; ++i) s[i] = i < vis ? s[i] : -INFINITY;
+                    }
+                } else {
+                    // a stage with a packed unit's extra tiles: each tile counts
+                    // only for the rows of the members in its mask
+                    const int32_t mi = div_rcp(U.row_lo + row, pl.q_len * pl.group, pl.rcp_rows_per_member);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int32_t tj = ti0 + j;
+                        int32_t lb = U.blk_start + tj;
+                        bool seen = j < ntiles;
+                        if (seen && tj >= U.n_shared) {
+                            const int2 e = xinfo[tj - U.n_shared];
+                            lb = e.x;
+                            seen = ((uint32_t)e.y >> (mi & 31)) & 1u;
+                        }
+                        const int32_t v = seen ? min(BS, R.limit - lb * BS) : 0;
+#pragma unroll
+                        for (int c = 0; c < BS; ++c) s[BS * j + c] = c < v ? s[BS * j + c] : -INFINITY;
+                    }
                 }
                 // row max of the raw scores (eight independent chains), then
                 // in base-2 units (the scale is positive)

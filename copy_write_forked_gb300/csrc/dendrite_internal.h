@@ -23,6 +23,7 @@ constexpr int kMaxUnitRowsTurbo = 64;  // rows per compressed-pool unit (4 warps
 constexpr int kMaxUnitRowsTc = 256;   // rows per tcgen05 attention unit (2 row tiles of 128)
 constexpr int kTcMinRowsDefault = 64; // segments with more rows per kv head use the tcgen05 kernel
 constexpr int32_t kFoldPctDefault = 100;  // fold a segment when that is estimated cheaper
+constexpr int32_t kPackPctDefault = 100;  // pack a segment's followers into it when that is estimated cheaper
 constexpr int kAppendMetaThreads = 1024;
 constexpr int kFreeCollectThreads = 1024;
 
@@ -77,14 +78,27 @@ struct AttnUnit {
     int32_t blk_start;  // first logical block of the segment
     int32_t n_blk;      // blocks (tiles) of the segment
     int32_t mem_off;    // the segment's first entry in the member list
-    int32_t pad[3];
+    int32_t n_shared;   // tiles [0, n_shared) are blocks blk_start + i of table_row, read by all rows;
+    int32_t x_off;      // tiles from n_shared on are the plan's extra tiles x_off + (i - n_shared)
+    int32_t pad;
 };
 static_assert(sizeof(AttnUnit) == 64, "AttnUnit layout");
+
+// An extra tile of a packed unit: logical block `blk` of branch handle
+// `table_row`'s table, read by the unit's rows whose member (index within the
+// segment's member list) has its bit set in `mask`.
+struct AttnXTile {
+    int32_t blk;
+    uint32_t mask;
+    int32_t table_row;
+    int32_t pad;
+};
 
 // One query row of a unit (computed by unit_row).
 struct AttnRow {
     int32_t q_row;   // row of Q/out viewed as [rows][head_dim]
     int32_t limit;   // visible positions: the row sees positions < limit
+    int32_t member;  // index of the row's member within its segment's member list
 };
 
 // Device view of an uploaded attention plan.
@@ -100,6 +114,7 @@ struct AttnPlanDev {
     const int32_t* tc_cta_begin;   // [n_tc_ctas + 1], same for the tc class
     const int32_t* tc_cta_unit;    // [n_tc_ctas]
     const int32_t* path_off;       // [n_queried + 1] into path
+    const AttnXTile* xtiles;       // extra tiles of packed units
     const int32_t* path;           // per path entry: (first unit of the segment, row groups per kv head,
                                    //  first segment row of the member, rows per row group)
     const int32_t* counts;         // plans expanded on the device: [0] CTAs of the mma.sync class,
@@ -115,6 +130,7 @@ struct AttnPlanDev {
     int32_t group;                 // G = n_q_heads / n_kv
     float rcp_rows_per_member;     // 1 / (q_len G)
     float rcp_group;               // 1 / G
+    int32_t packed;                // some unit reads extra tiles (the mma.sync kernel then needs its tile info)
 };
 
 // ------------------------------------------------------- host bookkeeping
@@ -180,7 +196,10 @@ struct PendingAppend {
     int32_t n_done = 0;
 };
 
-// A sharing segment found by the planner (planner.cpp).
+// A sharing segment found by the planner (planner.cpp).  A packed segment
+// (pack_segments) also holds the tiles of the segments that followed it:
+// extra tiles [x_off, x_off + n_x) of the planner's extra-tile list, each
+// read by a subset of the members only.
 struct Segment {
     int32_t rep_node;
     int32_t block_start;
@@ -188,7 +207,20 @@ struct Segment {
     int32_t member_offset;
     int32_t n_members;
     int32_t owner;      // node whose blocks these are (a node's segments are consecutive, ascending)
+    int32_t x_off = 0;
+    int32_t n_x = 0;
 };
+
+// One extra tile of a packed segment: logical block `blk` of node `rep`'s
+// table row, read by the segment's members whose bit is set in `mask`
+// (bit k: the segment's k-th member).
+struct ExtraTile {
+    int32_t rep_node;
+    int32_t blk;
+    uint32_t mask;
+};
+constexpr int kMaxPackMembers = 32;
+constexpr int kMaxTcExtraTiles = 64;   // extra tiles of a packed segment on the tcgen05 kernel
 
 struct PlanCache {
     bool valid = false;
@@ -213,7 +245,12 @@ struct PlanCache {
     // into new blocks only lengthen those segments.
     std::vector<Segment> segs;
     std::vector<int32_t> seg_members;
+    std::vector<ExtraTile> seg_xt;
     std::vector<int32_t> last_seg;
+    // per queried branch: the extra tile (index in seg_xt) holding its last
+    // block when that tile is read by it alone, else -1; appends that take
+    // such branches into new blocks add extra tiles after it
+    std::vector<int32_t> last_xt;
     int64_t unique_tiles = 0;
 };
 
@@ -230,6 +267,7 @@ struct dendrite_pool {
     int32_t tc_min_rows = dendrite::kTcMinRowsDefault;   // < 0: tensor-core attention kernel off
     int32_t tc_sms = 0;   // SMs of the tcgen05 kernel beside the mma.sync one (0: estimated, -1: no split)
     int32_t fold_pct = dendrite::kFoldPctDefault;        // < 0: segments are never folded
+    int32_t pack_pct = dendrite::kPackPctDefault;        // < 0: segments are never packed
     int32_t device_planning = 0;                         // 0 auto, 1 always, -1 never (bf16 plans)
 
     // device state
@@ -339,6 +377,15 @@ struct FoldParams {
 void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
                    const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
                    std::vector<Segment>& segs, std::vector<int32_t>& members);
+// Packing: a segment whose following segments have none of their own takes
+// their tiles as extra tiles (each read by that follower's members only) when
+// the estimate of one unit per row group over all the tiles beats the
+// separate units by pack_pct percent (< 0: never); the followers disappear.
+// Runs before folding; only segments of at most kMaxPackMembers members and
+// one row group per kv head pack.
+void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, const int32_t* parent,
+                   const int32_t* fork_len, int32_t block_size, std::vector<Segment>& segs,
+                   std::vector<int32_t>& members, std::vector<ExtraTile>& xt);
 
 // Attention (attn.cu)
 int attn_setup(dendrite_pool* p);      // tensor maps, occupancy

@@ -172,6 +172,12 @@ int64_t group_block_ns(bool tc, int32_t rows) {
 }
 int64_t group_unit_ns(bool tc, int32_t rows) { return (tc ? 3000 : 1000) + 29 * (int64_t)rows; }
 
+// Estimated time of one block for a row group of R rows (one unit).
+int64_t tile_ns(const FoldParams& fp, int64_t R) {
+    const bool tc = fp.tc_rows >= 0 && R > fp.tc_rows;
+    return group_block_ns(tc, (int32_t)std::min<int64_t>(R, tc ? kMaxUnitRowsTc : fp.small_rows));
+}
+
 // Estimate for R rows over T blocks, split into row groups as the plan splits
 // them; with_units adds the per-unit part.
 int64_t estimate_ns(const FoldParams& fp, int64_t T, int64_t R, bool with_units) {
@@ -183,20 +189,15 @@ int64_t estimate_ns(const FoldParams& fp, int64_t T, int64_t R, bool with_units)
     return ns;
 }
 
-}  // namespace
-
-void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
-                   const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
-                   std::vector<Segment>& segs, std::vector<int32_t>& members) {
+// The segment before each segment in its members' block order (the same for
+// all of them): the previous segment of the same owner, or for an owner's
+// first segment, the segment ending at its first block in the group of the
+// nearest ancestor that owns the block before it (-1: none).  Needs each
+// owner node's segments consecutive in segs, in ascending blocks.
+void segment_prev(const std::vector<Segment>& segs, int32_t n_nodes, const int32_t* parent,
+                  const int32_t* fork_len, int32_t bs, std::vector<int32_t>& prev) {
+    static thread_local std::vector<int32_t> node_first, node_count;
     const int32_t S = (int32_t)segs.size();
-    if (fp.fold_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
-    static thread_local std::vector<int32_t> node_first, node_count, prev, koff, kseg, eoff, emem, order, ext, qblocks;
-    static thread_local std::vector<char> folded;
-    const int32_t bs = block_size;
-    // each queried branch's block count
-    qblocks.resize(n_queried);
-    for (int32_t q = 0; q < n_queried; ++q) qblocks[q] = (len[queried[q]] + bs - 1) / bs;
-    // each owner node's segments (consecutive in segs, in ascending blocks)
     node_first.assign(n_nodes, -1);
     node_count.assign(n_nodes, 0);
     for (int32_t si = 0; si < S; ++si) {
@@ -204,10 +205,6 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
         if (node_first[o] < 0) node_first[o] = si;
         node_count[o]++;
     }
-    // The segment before each segment in its members' block order (the same
-    // for all of them): the previous segment of the same owner, or for an
-    // owner's first segment, the segment ending at its first block in the
-    // group of the nearest ancestor that owns the block before it.
     prev.assign(S, -1);
     for (int32_t si = 0; si < S; ++si) {
         const Segment& sg = segs[si];
@@ -228,6 +225,22 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
         }
         if (segs[lo].block_start + segs[lo].block_count == b) prev[si] = lo;
     }
+}
+
+}  // namespace
+
+void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                   const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
+                   std::vector<Segment>& segs, std::vector<int32_t>& members) {
+    const int32_t S = (int32_t)segs.size();
+    if (fp.fold_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
+    static thread_local std::vector<int32_t> prev, koff, kseg, eoff, emem, order, ext, qblocks;
+    static thread_local std::vector<char> folded;
+    const int32_t bs = block_size;
+    // each queried branch's block count
+    qblocks.resize(n_queried);
+    for (int32_t q = 0; q < n_queried; ++q) qblocks[q] = (len[queried[q]] + bs - 1) / bs;
+    segment_prev(segs, n_nodes, parent, fork_len, bs, prev);
     // the segments after each segment, and the members whose blocks end there
     koff.assign(S + 1, 0);
     eoff.resize(S + 1);
@@ -306,6 +319,8 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
             o.owner = sg.owner;
             o.rep_node = sg.rep_node;
             o.n_members = sg.n_members;
+            o.x_off = sg.x_off;
+            o.n_x = sg.n_x;
             out_members.insert(out_members.end(), members.begin() + sg.member_offset,
                                members.begin() + sg.member_offset + sg.n_members);
         } else {
@@ -315,6 +330,129 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
             o.n_members = eoff[si + 1] - eoff[si];
             out_members.insert(out_members.end(), emem.begin() + eoff[si], emem.begin() + eoff[si + 1]);
         }
+        out.push_back(o);
+    }
+    segs.swap(out);
+    members.swap(out_members);
+}
+
+// Packing.  A segment s whose members continue into following segments that
+// have no followers of their own (leaves of the segment tree: the private
+// tails of speculative draft paths, of beam leaves, of MCTS leaves) costs
+// every follower a unit start, a query load and a partial row per member row,
+// for a few blocks each.  Packing gives s the followers' tiles as extra
+// tiles, each masked to the members of the follower it came from, so one unit
+// per kv head reads s's blocks with all its rows and then each follower's
+// blocks with that follower's rows; a row's partial then covers all of its
+// blocks, and the followers' units, partial rows and merge reads disappear.
+// The price is that every extra tile is multiplied with all of s's rows (the
+// row tiles of s's unit), so long private tails (the stress leaves) stay on
+// their own.  Decisions run in decreasing block order, so a follower has
+// absorbed its own followers before its turn comes and a packed follower's
+// extra tiles move up with its own.
+void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, const int32_t* parent,
+                   const int32_t* fork_len, int32_t block_size, std::vector<Segment>& segs,
+                   std::vector<int32_t>& members, std::vector<ExtraTile>& xt) {
+    xt.clear();
+    const int32_t S = (int32_t)segs.size();
+    if (pack_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
+    static thread_local std::vector<int32_t> prev, koff, kseg, order, open_followers, pos;
+    static thread_local std::vector<char> gone;
+    static thread_local std::vector<std::vector<ExtraTile>> ext;
+    segment_prev(segs, n_nodes, parent, fork_len, block_size, prev);
+    koff.assign(S + 1, 0);
+    for (int32_t si = 0; si < S; ++si)
+        if (prev[si] >= 0) koff[prev[si] + 1]++;
+    for (int32_t si = 0; si < S; ++si) koff[si + 1] += koff[si];
+    kseg.resize(koff[S]);
+    {
+        static thread_local std::vector<int32_t> kc;
+        kc.assign(koff.begin(), koff.end() - 1);
+        for (int32_t si = 0; si < S; ++si)
+            if (prev[si] >= 0) kseg[kc[prev[si]]++] = si;
+    }
+    open_followers.resize(S);
+    for (int32_t si = 0; si < S; ++si) open_followers[si] = koff[si + 1] - koff[si];
+    order.resize(S);
+    for (int32_t si = 0; si < S; ++si) order[si] = si;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int32_t a, int32_t b) { return segs[a].block_start > segs[b].block_start; });
+    if ((int32_t)ext.size() < S) ext.resize(S);
+    for (int32_t si = 0; si < S; ++si) ext[si].clear();
+    gone.assign(S, 0);
+    const int64_t rpm = fp.rows_per_member;
+    bool any = false;
+    for (const int32_t si : order) {
+        const int32_t k0 = koff[si], k1 = koff[si + 1];
+        if (k0 == k1) continue;
+        Segment& sg = segs[si];
+        const int64_t R = (int64_t)sg.n_members * rpm;
+        const bool tc = fp.tc_rows >= 0 && R > fp.tc_rows;
+        if (sg.n_members > kMaxPackMembers || R > (tc ? kMaxUnitRowsTc : fp.small_rows)) continue;
+        // every follower closed, and none read by all of sg's members (a
+        // chain, which folding joins without masks)
+        bool closed = true;
+        for (int32_t k = k0; k < k1 && closed; ++k)
+            closed = open_followers[kseg[k]] == 0 && segs[kseg[k]].n_members < sg.n_members;
+        if (!closed) continue;
+        int64_t T = sg.block_count + (int64_t)ext[si].size();
+        int64_t apart = estimate_ns(fp, T, R, true);
+        for (int32_t k = k0; k < k1; ++k) {
+            const Segment& f = segs[kseg[k]];
+            const int64_t Tf = f.block_count + (int64_t)ext[kseg[k]].size();
+            apart += estimate_ns(fp, Tf, (int64_t)f.n_members * rpm, true);
+            T += Tf;
+        }
+        // the tcgen05 kernel stages a unit's extra tiles in shared memory
+        const int64_t X = T - sg.block_count;
+        if (tc && X > kMaxTcExtraTiles) continue;
+        // on the mma.sync kernel an extra tile also costs the producer its
+        // entry's load: about twice a tile's time, measured on beam leaves
+        const int64_t packed_ns = estimate_ns(fp, T, R, true) + (tc ? 0 : X * tile_ns(fp, R));
+        if (packed_ns * 100 >= apart * pack_pct) continue;
+        // each follower's members are a subset of sg's (both ascending):
+        // their bit positions in sg's member list
+        const int32_t* sm = members.data() + sg.member_offset;
+        for (int32_t k = k0; k < k1; ++k) {
+            const int32_t fi = kseg[k];
+            const Segment& f = segs[fi];
+            const int32_t* fm = members.data() + f.member_offset;
+            pos.resize(f.n_members);
+            uint32_t fmask = 0;
+            for (int32_t a = 0, b = 0; a < f.n_members; ++a) {
+                while (sm[b] != fm[a]) ++b;
+                pos[a] = b;
+                fmask |= 1u << b;
+            }
+            for (int32_t i = 0; i < f.block_count; ++i)
+                ext[si].push_back(ExtraTile{f.rep_node, f.block_start + i, fmask});
+            for (const ExtraTile& e : ext[fi]) {
+                uint32_t m = 0;
+                for (int32_t a = 0; a < f.n_members; ++a)
+                    if (e.mask >> a & 1u) m |= 1u << pos[a];
+                ext[si].push_back(ExtraTile{e.rep_node, e.blk, m});
+            }
+            ext[fi].clear();
+            gone[fi] = 1;
+        }
+        open_followers[si] = 0;
+        any = true;
+    }
+    if (!any) return;
+    // rebuild in the original order without the absorbed segments
+    static thread_local std::vector<Segment> out;
+    static thread_local std::vector<int32_t> out_members;
+    out.clear();
+    out_members.clear();
+    for (int32_t si = 0; si < S; ++si) {
+        if (gone[si]) continue;
+        Segment o = segs[si];
+        o.member_offset = (int32_t)out_members.size();
+        out_members.insert(out_members.end(), members.begin() + segs[si].member_offset,
+                           members.begin() + segs[si].member_offset + segs[si].n_members);
+        o.x_off = (int32_t)xt.size();
+        o.n_x = (int32_t)ext[si].size();
+        xt.insert(xt.end(), ext[si].begin(), ext[si].end());
         out.push_back(o);
     }
     segs.swap(out);
@@ -395,4 +533,38 @@ extern "C" int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* par
                                   fold_pct == 0 ? dendrite::kFoldPctDefault : fold_pct};
     dendrite::fold_segments(fp, n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
     return export_segments(s, m, segs, seg_cap, n_segs, members, member_cap, n_members);
+}
+
+extern "C" int dendrite_plan_segments_packed(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                                             const int32_t* len, int32_t block_size,
+                                             const int32_t* queried, int32_t n_queried,
+                                             int32_t rows_per_member, int32_t tc_min_rows, int32_t fold_pct,
+                                             int32_t pack_pct, dendrite_segment* segs, int32_t seg_cap,
+                                             int32_t* n_segs, int32_t* members, int32_t member_cap,
+                                             int32_t* n_members, int32_t* extra_off, dendrite_extra_tile* extras,
+                                             int32_t extra_cap, int32_t* n_extras) {
+    if (!n_segs || !n_members || !n_extras || rows_per_member <= 0 || tc_min_rows < -1 || fold_pct < -1 ||
+        pack_pct < -1)
+        return DENDRITE_EINVAL;
+    DENDRITE_TRY(check_forest(n_nodes, parent, fork_len, len, block_size, queried, n_queried));
+    std::vector<dendrite::Segment> s;
+    std::vector<int32_t> m;
+    std::vector<dendrite::ExtraTile> xt;
+    dendrite::plan_segments(n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
+    const dendrite::FoldParams fp{rows_per_member, tc_min_rows == 0 ? dendrite::kTcMinRowsDefault : tc_min_rows,
+                                  dendrite::kMaxUnitRowsBf16,
+                                  fold_pct == 0 ? dendrite::kFoldPctDefault : fold_pct};
+    dendrite::pack_segments(fp, pack_pct == 0 ? dendrite::kPackPctDefault : pack_pct, n_nodes, parent, fork_len,
+                            block_size, s, m, xt);
+    dendrite::fold_segments(fp, n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
+    *n_extras = (int32_t)xt.size();
+    const int rc = export_segments(s, m, segs, seg_cap, n_segs, members, member_cap, n_members);
+    if (rc != DENDRITE_OK || (int32_t)xt.size() > extra_cap) return rc != DENDRITE_OK ? rc : DENDRITE_ELIMIT;
+    if (extra_off) {
+        for (size_t i = 0; i < s.size(); ++i) extra_off[i] = s[i].x_off;
+        extra_off[s.size()] = (int32_t)xt.size();
+    }
+    for (size_t i = 0; i < xt.size(); ++i)
+        extras[i] = dendrite_extra_tile{xt[i].rep_node, xt[i].blk, xt[i].mask, 0};
+    return DENDRITE_OK;
 }

@@ -1077,7 +1077,7 @@ int pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int3
         if (opts->tc_min_rows < -1 || opts->fold_segments < -1) return DENDRITE_EINVAL;
         if (opts->device_planning < -1 || opts->device_planning > 1) return DENDRITE_EINVAL;
         if (opts->n_layers < 0 || opts->n_layers > 1024) return DENDRITE_EINVAL;
-        if (opts->tc_sms < -1) return DENDRITE_EINVAL;
+        if (opts->tc_sms < -1 || opts->pack_segments < -1) return DENDRITE_EINVAL;
     }
     if (max_branches < 1 || bpb < 1 || (int64_t)max_branches * bpb > (int64_t)1 << 34) return DENDRITE_EINVAL;
 
@@ -1092,6 +1092,7 @@ int pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv_heads, int3
     p->bpb = bpb;
     if (opts && opts->tc_min_rows) p->tc_min_rows = opts->tc_min_rows;
     if (opts) p->tc_sms = opts->tc_sms;
+    if (opts && opts->pack_segments) p->pack_pct = opts->pack_segments;
     if (opts && opts->n_layers) p->n_layers = opts->n_layers;
     if (opts && opts->fold_segments) p->fold_pct = opts->fold_segments;
     if (opts) p->device_planning = opts->device_planning;

@@ -44,7 +44,8 @@ class DendriteError(RuntimeError):
 
 class _Opts(ctypes.Structure):
     _fields_ = [("max_branches", _i32), ("max_blocks_per_branch", _i32), ("tc_min_rows", _i32),
-                ("n_layers", _i32), ("fold_segments", _i32), ("device_planning", _i32), ("tc_sms", _i32), ("reserved", _i32 * 1)]
+                ("n_layers", _i32), ("fold_segments", _i32), ("device_planning", _i32), ("tc_sms", _i32), ("pack_segments", _i32),
+                ("reserved", _i32 * 1)]
 
 
 class _PlanStats(ctypes.Structure):
@@ -56,6 +57,10 @@ class _PlanStats(ctypes.Structure):
 class _Segment(ctypes.Structure):
     _fields_ = [("rep", _i32), ("block_start", _i32), ("block_count", _i32),
                 ("member_offset", _i32), ("n_members", _i32)]
+
+
+class _ExtraTile(ctypes.Structure):
+    _fields_ = [("rep", _i32), ("block", _i32), ("member_mask", ctypes.c_uint32), ("reserved", _i32)]
 
 
 _SIGS = {
@@ -90,6 +95,9 @@ _SIGS = {
                                _pi32, _pi32, _i32, _pi32],
     "dendrite_plan_segments_folded": [_i32, _pi32, _pi32, _pi32, _i32, _pi32, _i32, _i32, _i32, _i32,
                                       ctypes.POINTER(_Segment), _i32, _pi32, _pi32, _i32, _pi32],
+    "dendrite_plan_segments_packed": [_i32, _pi32, _pi32, _pi32, _i32, _pi32, _i32, _i32, _i32, _i32, _i32,
+                                      ctypes.POINTER(_Segment), _i32, _pi32, _pi32, _i32, _pi32, _pi32,
+                                      ctypes.POINTER(_ExtraTile), _i32, _pi32],
 }
 
 
@@ -151,7 +159,8 @@ class Pool:
     def __init__(self, num_blocks: int, block_size: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
                  dtype: torch.dtype = torch.bfloat16, max_branches: int = 4096,
                  max_blocks_per_branch: int = 4096, device=None, tc_min_rows: int = 0, n_layers: int = 1,
-                 fold_segments: int = 0, turbo=None, device_planning: int = 0, tc_sms: int = 0):
+                 fold_segments: int = 0, turbo=None, device_planning: int = 0, tc_sms: int = 0,
+                 pack_segments: int = 0):
         """``turbo``: (rotation signs [128], QJL matrix [128][128]) to store
         compressed blocks (dendrite_pool_create_turbo); the calls then take
         bf16 tensors."""
@@ -162,7 +171,7 @@ class Pool:
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.n_kv_heads, self.head_dim, self.dtype = int(n_kv_heads), int(head_dim), dtype
         opts = _Opts(int(max_branches), int(max_blocks_per_branch), int(tc_min_rows), int(n_layers),
-                     int(fold_segments), int(device_planning), int(tc_sms))
+                     int(fold_segments), int(device_planning), int(tc_sms), int(pack_segments))
         self.n_layers = int(n_layers)
         self.turbo = turbo is not None
         h = ctypes.c_void_p()
@@ -417,4 +426,35 @@ def plan_segments(parent: Sequence[int], fork_len: Sequence[int], length: Sequen
     out = []
     for s in segs[:ns.value]:
         out.append((s.rep, s.block_start, s.block_count, list(mem[s.member_offset:s.member_offset + s.n_members])))
+    return out
+
+
+def plan_segments_packed(parent: Sequence[int], fork_len: Sequence[int], length: Sequence[int], block_size: int,
+                         queried: Sequence[int], rows_per_member: int, tc_min_rows: int = 0, fold_pct: int = 0,
+                         pack_pct: int = 0):
+    """Host planner with packing, then folding (dendrite_plan_segments_packed):
+    a list of (rep, block_start, block_count, members, extras), extras being
+    (rep, block, member_mask) tuples."""
+    n = len(parent)
+    ns, nm, nx = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    L = lib()
+    pa, fa, la, qa = _arr(parent), _arr(fork_len), _arr(length), _arr(queried)
+    head = (n, _ptr(pa), _ptr(fa), _ptr(la), block_size, _ptr(qa), len(queried), int(rows_per_member),
+            int(tc_min_rows), int(fold_pct), int(pack_pct))
+    fn = L.dendrite_plan_segments_packed
+    rc = fn(*head, None, 0, ctypes.addressof(ns), None, 0, ctypes.addressof(nm), None, None, 0,
+            ctypes.addressof(nx))
+    if rc not in (0, -4):
+        _check(rc, "plan_segments_packed")
+    segs = (_Segment * max(1, ns.value))()
+    mem = (ctypes.c_int32 * max(1, nm.value))()
+    xo = (ctypes.c_int32 * (ns.value + 1))()
+    xt = (_ExtraTile * max(1, nx.value))()
+    _check(fn(*head, segs, ns.value, ctypes.addressof(ns), ctypes.addressof(mem), nm.value, ctypes.addressof(nm),
+              ctypes.addressof(xo), xt, nx.value, ctypes.addressof(nx)), "plan_segments_packed")
+    out = []
+    for k, s in enumerate(segs[:ns.value]):
+        ex = [(e.rep, e.block, e.member_mask) for e in xt[xo[k]:xo[k + 1]]]
+        out.append((s.rep, s.block_start, s.block_count, list(mem[s.member_offset:s.member_offset + s.n_members]),
+                    ex))
     return out

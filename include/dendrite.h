@@ -104,6 +104,13 @@ typedef struct dendrite_pool_opts {
                                     * or none: then each SM goes to the mma.sync kernel   *
                                     * when its tcgen05 CTA finishes); k > 0 = k SMs (no   *
                                     * split from the SM count up); -1 = never split.      */
+    int32_t pack_segments;         /* bf16 attention planning: a sharing segment takes    *
+                                    * the tiles of the segments that follow it, when none *
+                                    * of those has followers of its own, as extra tiles   *
+                                    * read by their own rows only (one unit instead of    *
+                                    * several; dendrite_plan_segments_packed), when an    *
+                                    * estimate of the kernels' time drops.  0 = default;  *
+                                    * k > 0 = when it drops below k percent; -1 = never.  */
     int32_t reserved[1];           /* must be zero                                         */
 } dendrite_pool_opts;
 
@@ -375,9 +382,10 @@ typedef struct dendrite_plan_stats {
                              * refreshed (only appends since it was built, and no   *
                              * queried branch reached a new block); 2: only appends *
                              * since it was built and the branches that reached new *
-                             * blocks each read their last segment alone, so the    *
-                             * cached segments were lengthened and only the units,  *
-                             * CTA partition and paths rebuilt; 0: built anew       */
+                             * blocks each read their last segment (or, packed,     *
+                             * their last extra tile) alone, so the cached segments *
+                             * were lengthened and only the units, CTA partition    *
+                             * and paths rebuilt; 0: built anew                     */
     int32_t reserved;
 } dendrite_plan_stats;
 int dendrite_last_plan_stats(dendrite_pool* pool, dendrite_plan_stats* out);
@@ -436,6 +444,45 @@ int dendrite_plan_segments_folded(int32_t n_nodes, const int32_t* parent, const 
                                   int32_t rows_per_member, int32_t tc_min_rows, int32_t fold_pct,
                                   dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
                                   int32_t* members, int32_t member_cap, int32_t* n_members);
+
+/*
+ * The segments of the bf16 attention call with packing (pool option
+ * pack_segments) before folding.  A segment whose following segments (those
+ * that continue its members' block order) have no followers of their own can
+ * take their tiles as extra tiles: extra tile {rep, block, member_mask} is
+ * logical block `block` of node `rep`'s table, read only by the segment's
+ * members whose bit is set (bit k: members[member_offset + k]); the followers
+ * then disappear.  It packs when an estimate of one unit over all the tiles
+ * (every tile multiplied with all the segment's rows) beats the separate
+ * units; only segments of at most 32 members and one row group per kv head
+ * (64 rows on the mma.sync kernel, 256 on the tcgen05 kernel) pack.  Folding
+ * then runs as in dendrite_plan_segments_folded: a packed segment is never
+ * folded, and a folded segment before it extends its shared range (the
+ * blocks all its members read) downwards.  Every queried branch still reads
+ * each of its logical blocks exactly once, through the shared range or
+ * through the extra tiles of exactly one segment.
+ *   pack_pct  0 = default (pack when the estimate drops), k > 0 = when it drops
+ *             below k percent, -1 = never.
+ *   extra_off [seg_cap + 1]: segment k's extra tiles are extras[extra_off[k] ..
+ *             extra_off[k + 1]) (may be NULL).
+ * Returns DENDRITE_ELIMIT if a capacity is too small (the needed counts are
+ * still written).
+ */
+typedef struct dendrite_extra_tile {
+    int32_t rep;
+    int32_t block;
+    uint32_t member_mask;
+    int32_t reserved;
+} dendrite_extra_tile;
+
+int dendrite_plan_segments_packed(int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
+                                  const int32_t* len, int32_t block_size,
+                                  const int32_t* queried, int32_t n_queried,
+                                  int32_t rows_per_member, int32_t tc_min_rows, int32_t fold_pct,
+                                  int32_t pack_pct, dendrite_segment* segs, int32_t seg_cap, int32_t* n_segs,
+                                  int32_t* members, int32_t member_cap, int32_t* n_members,
+                                  int32_t* extra_off, dendrite_extra_tile* extras, int32_t extra_cap,
+                                  int32_t* n_extras);
 
 /* ------------------------------------------------- allocation-free variant
  * No counterpart on the pages: this entry point exists for callers that must

@@ -23,8 +23,8 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def run_and_check(w, tol, sample=None):
-    pool = pool_for(w)
+def run_and_check(w, tol, sample=None, **opts):
+    pool = pool_for(w, **opts)
     h = run_script(pool, w)
     Q = w.q("cuda")
     out = pool.tree_attn_decode(Q, [h[b] for b in w.query])
@@ -60,8 +60,11 @@ def test_random_trees_bf16(seed):
 def test_beam_small_ragged():
     # ragged prefix and leaves: partial blocks at the fork point and at every tail
     w = W.beam(requests=3, prefix=211, width=4, divergent=37)
-    err, st = run_and_check(w, TOL_BF16)
+    err, st = run_and_check(w, TOL_BF16, pack_segments=-1)
     assert st["n_segments"] == 3 + 12
+    # packed (the default): each prefix takes its four leaves' tiles
+    err, st = run_and_check(w, TOL_BF16)
+    assert st["n_segments"] == 3
 
 
 def test_wide_fork_spans_row_groups():
@@ -202,3 +205,41 @@ def test_attention_after_free_of_shared_parent():
            W.Op("free", (0,)), W.Op("append", (1, 2), 30)]
     w = W.Workload("orphans", 2, 4, 128, 16, torch.bfloat16, ops, (1, 2))
     run_and_check(w, TOL_BF16)
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("tc_min_rows", [0, -1])
+def test_random_trees_packed_everywhere_bf16(seed, tc_min_rows):
+    """Packing forced wherever the planner allows it (pack_segments far above
+    100 percent): packed units read their followers' tiles with per-tile row
+    masks, on the mma.sync kernel and (with enough rows) on the tcgen05
+    kernel; q_len 1..3 puts a member's causal limits inside its own tiles."""
+    q_len = 1 + seed % 3
+    w = W.random_script(seed, n_ops=40, max_live=12, max_append=90, n_kv=2, n_q=8, d=128, bs=16,
+                        dtype=torch.bfloat16, q_len=q_len, seed=seed)
+    pool = pool_for(w, pack_segments=1_000_000, tc_min_rows=tc_min_rows if tc_min_rows else 8)
+    h = run_script(pool, w)
+    out = pool.tree_attn_decode(w.q("cuda"), [h[b] for b in w.query])
+    pool.sync()
+    check_attention(w, out, list(range(len(w.query))), TOL_BF16)
+    pool.close()
+
+
+@pytest.mark.parametrize("make", [lambda: W.spec_verify(requests=3, prefix=700, paths=3, draft=8),
+                                  lambda: W.beam(requests=3, prefix=500, width=4, divergent=40),
+                                  lambda: W.mcts(root=300, iters=60, width=4, per_node=24)],
+                         ids=["spec_verify", "beam", "mcts"])
+def test_packed_and_unpacked_plans_agree_with_the_oracle(make):
+    """A plan packed as far as the planner allows reads fewer units than the
+    plan with packing off, and both (and the default plan) match the oracle."""
+    w = make()
+    units = []
+    for pack in (1_000_000, -1, 0):
+        pool = pool_for(w, pack_segments=pack)
+        h = run_script(pool, w)
+        out = pool.tree_attn_decode(w.q("cuda"), [h[b] for b in w.query])
+        pool.sync()
+        units.append(pool.last_plan_stats()["n_units"])
+        check_attention(w, out, list(range(len(w.query))), TOL_BF16)
+        pool.close()
+    assert units[0] < units[1]

@@ -50,6 +50,7 @@ def test_beam_4096_fork4_256_all_outputs():
     err, st = run_full(w, n_sample=32)
     assert st["n_segments"] == 8 + 32
     assert st["unique_tiles"] == (8 * 256 + 32 * 16) * 8
+    assert st["tiles"] == st["unique_tiles"]
 
 
 def test_mcts_2048_500_iterations():

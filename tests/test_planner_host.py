@@ -174,3 +174,128 @@ def test_folded_rejects_bad_arguments():
         plan_segments([-1], [0], [4], 4, [0], rows_per_member=1, tc_min_rows=-2)
     with pytest.raises(DendriteError):
         plan_segments([-1], [0], [4], 4, [0], rows_per_member=1, fold_pct=-2)
+
+
+# ---------------------------------------------------------------- packing
+# A packed segment reads its shared range with all its members and its extra
+# tiles each with a subset of them; the attention result depends on the same
+# two facts as for folding: every (queried branch, logical block) pair is read
+# exactly once, and each tile is one physical block for every member that
+# reads it (one owner by the walk of the sharing definition).
+
+def check_packed(w, queried, rows_per_member, tc_min_rows=0, fold_pct=0, pack_pct=0):
+    from copy_write_forked_gb300.dendrite import plan_segments_packed
+    parent, fork_len, ln = tree_arrays(w)
+    bs = w.block_size
+    segs = plan_segments_packed(parent, fork_len, ln, bs, queried, rows_per_member, tc_min_rows=tc_min_rows,
+                                fold_pct=fold_pct, pack_pct=pack_pct)
+    cover = {}
+    for rep, start, count, members, extras in segs:
+        assert count > 0 and members and members == sorted(members)
+        assert queried[members[0]] == rep
+        for i in range(start, start + count):
+            assert len({owner(parent, fork_len, queried[m], i, bs) for m in members}) == 1
+            for m in members:
+                assert (m, i) not in cover
+                cover[(m, i)] = True
+        if extras:
+            assert len(members) <= 32
+            rows = len(members) * rows_per_member
+            assert rows <= (256 if tc_min_rows >= 0 and rows > (tc_min_rows or 64) else 64)
+        for xrep, blk, mask in extras:
+            readers = [members[k] for k in range(len(members)) if mask >> k & 1]
+            assert readers and mask < (1 << len(members))
+            assert xrep in [queried[m] for m in readers]
+            o = owner(parent, fork_len, xrep, blk, bs)
+            for m in readers:
+                assert blk < -(-ln[queried[m]] // bs)
+                assert owner(parent, fork_len, queried[m], blk, bs) == o
+                assert (m, blk) not in cover
+                cover[(m, blk)] = True
+    assert len(cover) == sum(-(-ln[b] // bs) for b in queried)
+    return segs
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_trees_pack_everything(seed):
+    # pack_pct far above 100 packs every segment whose followers allow it
+    w = W.random_script(seed, n_ops=40, max_live=10, max_append=40, bs=4)
+    live = sorted(w.lengths().keys())
+    rng = random.Random(seed)
+    q = rng.sample(live, rng.randint(1, len(live)))
+    for rpm in (1, 4, 24):
+        for fold in (-1, 0, 1_000_000):
+            check_packed(w, q, rpm, fold_pct=fold, pack_pct=1_000_000)
+        check_packed(w, q, rpm, tc_min_rows=-1, pack_pct=1_000_000)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_trees_default_pack(seed):
+    w = W.random_script(seed, n_ops=60, max_live=12, max_append=20, bs=4)
+    live = sorted(w.lengths().keys())
+    check_packed(w, live, 4)
+    check_packed(w, live, 32, tc_min_rows=-1)
+
+
+def test_pack_off_is_the_folded_plan():
+    w = W.mcts(root=64, iters=40, width=4, per_node=8, max_depth=5)
+    parent, fork_len, ln = tree_arrays(w)
+    q = list(w.query)
+    packed = check_packed(w, q, 4, pack_pct=-1)
+    assert [s[:4] for s in packed] == plan_segments(parent, fork_len, ln, 16, q, rows_per_member=4)
+    assert all(not s[4] for s in packed)
+
+
+def test_spec_verify_paths_pack_into_their_prefix():
+    # 3 draft paths of 8 tokens (q_len 8, 32 rows each) below an 8192-token
+    # prefix: the paths' one block each joins the prefix's 96-row unit
+    w = W.spec_verify(requests=4)
+    segs = check_packed(w, list(w.query), 32)
+    assert len(segs) == 4
+    for rep, start, count, members, extras in segs:
+        assert (start, count, len(members)) == (0, 512, 3)
+        assert sorted(m for _, _, m in extras) == [1, 2, 4]
+
+
+def test_beam_leaves_pack_into_their_prefix_only_when_forced():
+    # 16-block leaves of 4 rows under a 256-block prefix: packing saves their
+    # unit starts, but every extra tile also costs the producer a dependent
+    # load, so by default the leaves keep their own units
+    w = W.beam(requests=2, prefix=4096, width=4, divergent=256)
+    segs = check_packed(w, list(w.query), 4, pack_pct=1_000_000)
+    assert len(segs) == 2 and all(len(s[4]) == 4 * 16 for s in segs)
+    assert all(not s[4] for s in check_packed(w, list(w.query), 4))
+
+
+def test_chains_are_folded_not_packed():
+    # a branch's own range followed by its own tail segment (the same single
+    # member): folding joins them without masks
+    w = W.fork_stress_attention(requests=1, width=4, prefix=512, divergent=64)
+    q = list(w.query)
+    parent, fork_len, ln = tree_arrays(w)
+    # each queried leaf forks one child that takes over the query
+    n = len(parent)
+    kids = []
+    for i, b in enumerate(q):
+        parent.append(b)
+        fork_len.append(ln[b] - 3)
+        ln.append(ln[b] - 3 + 1)
+        kids.append(n + i)
+    from copy_write_forked_gb300.dendrite import plan_segments_packed
+    segs = plan_segments_packed(parent, fork_len, ln, w.block_size, kids, 4, pack_pct=1_000_000)
+    assert all(not s[4] for s in segs)
+
+
+def test_long_private_tails_do_not_pack():
+    # the stress leaves (1024 tokens, 4 rows each) would be multiplied with the
+    # prefix's 256 rows
+    w = W.fork_stress_attention(requests=1, width=64)
+    segs = check_packed(w, list(w.query), 4)
+    assert all(not s[4] for s in segs) and len(segs) == 65
+
+
+def test_mcts_packs_leaf_families():
+    w = W.mcts()
+    segs = check_packed(w, list(w.query), 4)
+    folded = plan_segments(*tree_arrays(w), 16, list(w.query), rows_per_member=4)
+    assert len(segs) * 2 < len(folded)
