@@ -1617,13 +1617,15 @@ int build_plan(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_l
     // distinct tiles: the sharing segments before folding read each (block,
     // kv head) pair once
     for (const Segment& sg : hp.psegs) hp.unique_tiles += (int64_t)sg.block_count * nkv;
+    static thread_local std::vector<int32_t> prev;
+    prev.clear();
     if (bf16 && p->pack_pct >= 0)
         pack_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, p->pack_pct, n_nodes,
-                      hp.parent.data(), hp.fork_len.data(), p->block_size, hp.psegs, hp.seg_members, hp.pxt);
+                      hp.parent.data(), hp.fork_len.data(), p->block_size, hp.psegs, hp.seg_members, hp.pxt, &prev);
     if (p->fold_pct >= 0)
         fold_segments(FoldParams{RM, tc_on ? p->tc_min_rows : -1, small_rows, p->fold_pct}, n_nodes,
                       hp.parent.data(), hp.fork_len.data(), hp.len.data(), p->block_size, hp.queried.data(), n,
-                      hp.psegs, hp.seg_members);
+                      hp.psegs, hp.seg_members, &prev);
     return build_units(p, branches, n, q_len, nq, max_ctas, max_tc_ctas, hp, allow_device);
 }
 

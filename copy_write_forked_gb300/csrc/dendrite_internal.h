@@ -376,16 +376,20 @@ struct FoldParams {
 };
 void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
                    const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
-                   std::vector<Segment>& segs, std::vector<int32_t>& members);
+                   std::vector<Segment>& segs, std::vector<int32_t>& members,
+                   const std::vector<int32_t>* prev_in = nullptr);
 // Packing: a segment whose following segments have none of their own takes
 // their tiles as extra tiles (each read by that follower's members only) when
 // the estimate of one unit per row group over all the tiles beats the
 // separate units by pack_pct percent (< 0: never); the followers disappear.
 // Runs before folding; only segments of at most kMaxPackMembers members and
-// one row group per kv head pack.
+// one row group per kv head pack.  prev_out (optional) receives each kept
+// segment's predecessor in its members' block order, which folding can take
+// as prev_in instead of finding it again.
 void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, const int32_t* parent,
                    const int32_t* fork_len, int32_t block_size, std::vector<Segment>& segs,
-                   std::vector<int32_t>& members, std::vector<ExtraTile>& xt);
+                   std::vector<int32_t>& members, std::vector<ExtraTile>& xt,
+                   std::vector<int32_t>* prev_out = nullptr);
 
 // Attention (attn.cu)
 int attn_setup(dendrite_pool* p);      // tensor maps, occupancy

@@ -231,7 +231,7 @@ void segment_prev(const std::vector<Segment>& segs, int32_t n_nodes, const int32
 
 void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent, const int32_t* fork_len,
                    const int32_t* len, int32_t block_size, const int32_t* queried, int32_t n_queried,
-                   std::vector<Segment>& segs, std::vector<int32_t>& members) {
+                   std::vector<Segment>& segs, std::vector<int32_t>& members, const std::vector<int32_t>* prev_in) {
     const int32_t S = (int32_t)segs.size();
     if (fp.fold_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
     static thread_local std::vector<int32_t> prev, koff, kseg, eoff, emem, order, ext, qblocks;
@@ -240,7 +240,8 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
     // each queried branch's block count
     qblocks.resize(n_queried);
     for (int32_t q = 0; q < n_queried; ++q) qblocks[q] = (len[queried[q]] + bs - 1) / bs;
-    segment_prev(segs, n_nodes, parent, fork_len, bs, prev);
+    if (prev_in && (int32_t)prev_in->size() == S) prev = *prev_in;
+    else segment_prev(segs, n_nodes, parent, fork_len, bs, prev);
     // the segments after each segment, and the members whose blocks end there
     koff.assign(S + 1, 0);
     eoff.resize(S + 1);
@@ -352,13 +353,15 @@ void fold_segments(const FoldParams& fp, int32_t n_nodes, const int32_t* parent,
 // extra tiles move up with its own.
 void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, const int32_t* parent,
                    const int32_t* fork_len, int32_t block_size, std::vector<Segment>& segs,
-                   std::vector<int32_t>& members, std::vector<ExtraTile>& xt) {
+                   std::vector<int32_t>& members, std::vector<ExtraTile>& xt, std::vector<int32_t>* prev_out) {
     xt.clear();
+    if (prev_out) prev_out->clear();
     const int32_t S = (int32_t)segs.size();
     if (pack_pct < 0 || S < 2 || fp.rows_per_member <= 0) return;
-    static thread_local std::vector<int32_t> prev, koff, kseg, order, open_followers, pos;
+    static thread_local std::vector<int32_t> prev, koff, kseg, order, open_followers, cnt;
+    // absorbed followers of each segment (a list in absorption order) and its extra tiles so far
+    static thread_local std::vector<int32_t> nx, first_abs, next_abs, last_abs;
     static thread_local std::vector<char> gone;
-    static thread_local std::vector<std::vector<ExtraTile>> ext;
     segment_prev(segs, n_nodes, parent, fork_len, block_size, prev);
     koff.assign(S + 1, 0);
     for (int32_t si = 0; si < S; ++si)
@@ -373,19 +376,27 @@ void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, cons
     }
     open_followers.resize(S);
     for (int32_t si = 0; si < S; ++si) open_followers[si] = koff[si + 1] - koff[si];
-    order.resize(S);
-    for (int32_t si = 0; si < S; ++si) order[si] = si;
-    std::stable_sort(order.begin(), order.end(),
-                     [&](int32_t a, int32_t b) { return segs[a].block_start > segs[b].block_start; });
-    if ((int32_t)ext.size() < S) ext.resize(S);
-    for (int32_t si = 0; si < S; ++si) ext[si].clear();
+    // decreasing first block (a counting sort): followers come before the segment they follow
+    {
+        int32_t max_start = 0;
+        for (const Segment& sg : segs) max_start = std::max(max_start, sg.block_start);
+        cnt.assign((size_t)max_start + 2, 0);
+        for (const Segment& sg : segs) cnt[max_start - sg.block_start + 1]++;
+        for (int32_t k = 0; k <= max_start; ++k) cnt[k + 1] += cnt[k];
+        order.resize(S);
+        for (int32_t si = 0; si < S; ++si) order[cnt[max_start - segs[si].block_start]++] = si;
+    }
+    nx.assign(S, 0);
+    first_abs.assign(S, -1);
+    next_abs.assign(S, -1);
+    last_abs.assign(S, -1);
     gone.assign(S, 0);
     const int64_t rpm = fp.rows_per_member;
     bool any = false;
     for (const int32_t si : order) {
         const int32_t k0 = koff[si], k1 = koff[si + 1];
         if (k0 == k1) continue;
-        Segment& sg = segs[si];
+        const Segment& sg = segs[si];
         const int64_t R = (int64_t)sg.n_members * rpm;
         const bool tc = fp.tc_rows >= 0 && R > fp.tc_rows;
         if (sg.n_members > kMaxPackMembers || R > (tc ? kMaxUnitRowsTc : fp.small_rows)) continue;
@@ -395,11 +406,11 @@ void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, cons
         for (int32_t k = k0; k < k1 && closed; ++k)
             closed = open_followers[kseg[k]] == 0 && segs[kseg[k]].n_members < sg.n_members;
         if (!closed) continue;
-        int64_t T = sg.block_count + (int64_t)ext[si].size();
+        int64_t T = sg.block_count + (int64_t)nx[si];
         int64_t apart = estimate_ns(fp, T, R, true);
         for (int32_t k = k0; k < k1; ++k) {
             const Segment& f = segs[kseg[k]];
-            const int64_t Tf = f.block_count + (int64_t)ext[kseg[k]].size();
+            const int64_t Tf = f.block_count + (int64_t)nx[kseg[k]];
             apart += estimate_ns(fp, Tf, (int64_t)f.n_members * rpm, true);
             T += Tf;
         }
@@ -410,53 +421,63 @@ void pack_segments(const FoldParams& fp, int32_t pack_pct, int32_t n_nodes, cons
         // entry's load: about twice a tile's time, measured on beam leaves
         const int64_t packed_ns = estimate_ns(fp, T, R, true) + (tc ? 0 : X * tile_ns(fp, R));
         if (packed_ns * 100 >= apart * pack_pct) continue;
-        // each follower's members are a subset of sg's (both ascending):
-        // their bit positions in sg's member list
-        const int32_t* sm = members.data() + sg.member_offset;
         for (int32_t k = k0; k < k1; ++k) {
             const int32_t fi = kseg[k];
-            const Segment& f = segs[fi];
-            const int32_t* fm = members.data() + f.member_offset;
-            pos.resize(f.n_members);
-            uint32_t fmask = 0;
-            for (int32_t a = 0, b = 0; a < f.n_members; ++a) {
-                while (sm[b] != fm[a]) ++b;
-                pos[a] = b;
-                fmask |= 1u << b;
-            }
-            for (int32_t i = 0; i < f.block_count; ++i)
-                ext[si].push_back(ExtraTile{f.rep_node, f.block_start + i, fmask});
-            for (const ExtraTile& e : ext[fi]) {
-                uint32_t m = 0;
-                for (int32_t a = 0; a < f.n_members; ++a)
-                    if (e.mask >> a & 1u) m |= 1u << pos[a];
-                ext[si].push_back(ExtraTile{e.rep_node, e.blk, m});
-            }
-            ext[fi].clear();
+            if (first_abs[si] < 0) first_abs[si] = fi; else next_abs[last_abs[si]] = fi;
+            last_abs[si] = fi;
             gone[fi] = 1;
         }
+        nx[si] = (int32_t)X;
         open_followers[si] = 0;
         any = true;
     }
-    if (!any) return;
-    // rebuild in the original order without the absorbed segments
+    if (!any) {
+        if (prev_out) *prev_out = prev;
+        return;
+    }
+    // Rebuild in the original order without the absorbed segments.  A kept
+    // segment's extra tiles are its absorbed followers' blocks in absorption
+    // order, each follower's own blocks before those of the followers it had
+    // absorbed, masked to that follower's members (their bit positions in the
+    // kept segment's member list; both lists ascending).
+    // (The member list is left as it is: the kept segments keep their
+    // ranges in it, and the absorbed segments' ranges are no longer read.)
     static thread_local std::vector<Segment> out;
-    static thread_local std::vector<int32_t> out_members;
     out.clear();
-    out_members.clear();
     for (int32_t si = 0; si < S; ++si) {
         if (gone[si]) continue;
-        Segment o = segs[si];
-        o.member_offset = (int32_t)out_members.size();
-        out_members.insert(out_members.end(), members.begin() + segs[si].member_offset,
-                           members.begin() + segs[si].member_offset + segs[si].n_members);
+        const Segment& sg = segs[si];
+        Segment o = sg;
         o.x_off = (int32_t)xt.size();
-        o.n_x = (int32_t)ext[si].size();
-        xt.insert(xt.end(), ext[si].begin(), ext[si].end());
+        const int32_t* sm = members.data() + sg.member_offset;
+        auto emit = [&](auto&& self, int32_t fi) -> void {
+            const Segment& f = segs[fi];
+            const int32_t* fm = members.data() + f.member_offset;
+            uint32_t fmask = 0;
+            for (int32_t a = 0, b = 0; a < f.n_members; ++a) {
+                while (sm[b] != fm[a]) ++b;
+                fmask |= 1u << b;
+            }
+            for (int32_t i = 0; i < f.block_count; ++i) xt.push_back(ExtraTile{f.rep_node, f.block_start + i, fmask});
+            for (int32_t g = first_abs[fi]; g >= 0; g = next_abs[g]) self(self, g);
+        };
+        for (int32_t g = first_abs[si]; g >= 0; g = next_abs[g]) emit(emit, g);
+        o.n_x = (int32_t)xt.size() - o.x_off;
         out.push_back(o);
     }
+    // the kept segments' predecessors (an absorbed segment had no followers,
+    // so it is nobody's predecessor): their new indices
+    if (prev_out) {
+        static thread_local std::vector<int32_t> idx;
+        idx.assign(S, -1);
+        int32_t k = 0;
+        for (int32_t si = 0; si < S; ++si)
+            if (!gone[si]) idx[si] = k++;
+        prev_out->resize(k);
+        for (int32_t si = 0; si < S; ++si)
+            if (!gone[si]) (*prev_out)[idx[si]] = prev[si] >= 0 ? idx[prev[si]] : -1;
+    }
     segs.swap(out);
-    members.swap(out_members);
 }
 
 }  // namespace dendrite
@@ -554,9 +575,10 @@ extern "C" int dendrite_plan_segments_packed(int32_t n_nodes, const int32_t* par
     const dendrite::FoldParams fp{rows_per_member, tc_min_rows == 0 ? dendrite::kTcMinRowsDefault : tc_min_rows,
                                   dendrite::kMaxUnitRowsBf16,
                                   fold_pct == 0 ? dendrite::kFoldPctDefault : fold_pct};
+    std::vector<int32_t> prev;
     dendrite::pack_segments(fp, pack_pct == 0 ? dendrite::kPackPctDefault : pack_pct, n_nodes, parent, fork_len,
-                            block_size, s, m, xt);
-    dendrite::fold_segments(fp, n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m);
+                            block_size, s, m, xt, &prev);
+    dendrite::fold_segments(fp, n_nodes, parent, fork_len, len, block_size, queried, n_queried, s, m, &prev);
     *n_extras = (int32_t)xt.size();
     const int rc = export_segments(s, m, segs, seg_cap, n_segs, members, member_cap, n_members);
     if (rc != DENDRITE_OK || (int32_t)xt.size() > extra_cap) return rc != DENDRITE_OK ? rc : DENDRITE_ELIMIT;
