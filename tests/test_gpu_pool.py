@@ -154,11 +154,11 @@ def test_batched_forks_and_frees_of_siblings_match_oracle():
     prefixes: every step forks each of 300 leaves once (one call of 300
     pairs), appends one token to every child (a copy of each leaf's partial
     tail) and frees the 300 old leaves in one call; finally everything is
-    freed in one call.  Calls of this size take the tiled fork and free
-    kernels, whose lanes drop or take the references of a block shared
-    within a tile with one atomic; tables, refcounts, the free stack and
-    every valid slot match O2 after each step, and the last free returns
-    every block to the stack."""
+    freed in one call.  Calls of this size take the device-argument fork
+    kernel and the tiled free kernel, whose lanes drop the references of a
+    block shared within a tile with one atomic; tables, refcounts, the free
+    stack and every valid slot match O2 after each step, and the last free
+    returns every block to the stack."""
     ops = [W.Op("new", (0,)), W.Op("new", (1,)), W.Op("append", (0, 1), 100),
            W.Op("fork", (0, 1), children=(tuple(range(2, 152)), tuple(range(152, 302)))),
            W.Op("append", tuple(range(2, 302)), 5)]
