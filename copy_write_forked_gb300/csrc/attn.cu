@@ -1710,6 +1710,7 @@ int build_units(dendrite_pool* p, const int32_t* branches, int32_t n, int32_t q_
         const int32_t group_rows = (tc_on && rows_per_head > p->tc_min_rows) ? kMaxUnitRowsTc : small_rows;
         const size_t units = (size_t)nkv * ((rows_per_head + group_rows - 1) / group_rows);
         if (sg.n_x && units != (size_t)nkv) return DENDRITE_EINVAL;   // packed: one row group per kv head
+        if (sg.n_x > kMaxTcExtraTiles && group_rows == kMaxUnitRowsTc) return DENDRITE_ELIMIT;
         n_units_total += units;
         n_tiles_total += units * (size_t)(sg.block_count + sg.n_x);
         n_members_total += sg.n_members;
@@ -2378,6 +2379,16 @@ extern "C" int dendrite_tree_attn_decode_layer(dendrite_pool* p, int32_t layer, 
                     added += inside;
                 }
             }
+            // a packed segment of the tcgen05 class holds at most
+            // kMaxTcExtraTiles extra tiles (the kernel stages them in shared
+            // memory): one grown past that is planned anew
+            const int32_t rpm = q_len * (n_q_heads / p->n_kv);
+            const bool tc_on = p->dtype == DENDRITE_BF16 && tc_ctas(p) > 0;
+            for (const Segment& sg : hp.psegs)
+                if (tc_on && sg.n_x > kMaxTcExtraTiles && (int64_t)sg.n_members * rpm > p->tc_min_rows) grow = false;
+            if (!grow) hp.clear();
+        }
+        if (grow) {
             DENDRITE_TRY(build_units(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp, true));
         } else {
             DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, max_ctas, tc_ctas(p), hp, true));

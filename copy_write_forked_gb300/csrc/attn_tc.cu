@@ -467,9 +467,12 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (U.n_blk > U.n_shared) {
                 // a packed unit: its extra tiles' logical blocks and member
                 // masks into shared memory, once every warp of the row tile
-                // is done with the previous unit's
+                // is done with the previous unit's (the plan keeps them to
+                // kMaxTcExtraTiles; a unit past that reads none and is flagged)
+                const int32_t nx = U.n_blk - U.n_shared;
+                if (nx > kMaxTcExtraTiles && trow == 0) atomicCAS(&a.meta->status, 0, DENDRITE_ECORRUPT);
                 asm volatile("bar.sync %0, 128;" ::"r"(1 + r) : "memory");
-                for (int32_t i = trow; i < U.n_blk - U.n_shared; i += 128)
+                for (int32_t i = trow; i < min(nx, kMaxTcExtraTiles); i += 128)
                     xinfo[i] = *reinterpret_cast<const int2*>(pl.xtiles + U.x_off + i);
                 asm volatile("bar.sync %0, 128;" ::"r"(1 + r) : "memory");
             }
@@ -514,7 +517,7 @@ k_attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                         int32_t lb = U.blk_start + tj;
                         bool seen = j < ntiles;
                         if (seen && tj >= U.n_shared) {
-                            const int2 e = xinfo[tj - U.n_shared];
+                            const int2 e = xinfo[min(tj - U.n_shared, kMaxTcExtraTiles - 1)];
                             lb = e.x;
                             seen = ((uint32_t)e.y >> (mi & 31)) & 1u;
                         }

@@ -301,3 +301,39 @@ def test_sm_split_between_the_partial_kernels(tc_sms):
     elif tc_sms < 0:
         assert st["n_tc_ctas"] > tc_sms and st["n_tc_ctas"] + st["n_ctas"] > sms
     check_attention(w, outs[0], list(range(0, len(w.query), 7)), TOL)
+
+
+def test_packed_draft_paths_growing_past_the_extra_tile_limit():
+    """Draft paths packed into their prefix's tcgen05 unit (96 rows) keep
+    growing by a block per step: the cached plan adds their extra tiles while
+    the unit stays within the tcgen05 kernel's limit of 64, then the plan is
+    built anew (no longer packing the long paths); every checked step matches
+    the oracle and the pool reports no error."""
+    from _harness import check_attention
+    from copy_write_forked_gb300.runner import run_script
+    base = W.spec_verify(requests=1, prefix=600, paths=3, draft=8)
+    steps = [W.Op("append", tuple(base.query), 16) for _ in range(24)]
+    w_full = _extend(base, steps)
+    pool = pool_for(w_full)
+    h = run_script(pool, base)
+    br = [h[b] for b in base.query]
+    Q = base.q("cuda")
+    out = pool.tree_attn_decode(Q, br)
+    pool.sync()
+    assert pool.last_plan_stats()["n_tc_units"] == 8
+    seen = set()
+    for k in range(len(steps)):
+        idx = len(base.ops) + k
+        K, V = w_full.kv(idx, "cuda")
+        pool.append_kv(br, K, V)
+        out = pool.tree_attn_decode(Q, br)
+        pool.sync()
+        st = pool.last_plan_stats()
+        seen.add(st["refreshed"])
+        if k in (0, 9, 19, 20, len(steps) - 1):
+            w_k = W.Workload(w_full.name, w_full.n_kv_heads, w_full.n_q_heads, w_full.head_dim,
+                             w_full.block_size, w_full.dtype, w_full.ops[:idx + 1], w_full.query, w_full.q_len,
+                             w_full.seed)
+            check_attention(w_k, out, list(range(len(base.query))), TOL)
+    assert 2 in seen and 0 in seen, seen
+    pool.close()
