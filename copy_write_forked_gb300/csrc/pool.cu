@@ -95,13 +95,15 @@ struct ForkParams {
 
 __device__ __forceinline__ void fork_pair(int32_t* __restrict__ table, int32_t* __restrict__ refcount,
                                           int32_t bpb, int32_t child, int32_t parent, int32_t nb,
-                                          int32_t add, int lane, int32_t n_blocks, DevMeta* meta) {
+                                          int32_t add, int lane, int32_t n_blocks, DevMeta* meta,
+                                          int32_t first = 0) {
     // the parent's row is not written by this launch (children are new handles),
-    // so its entries are read through the read-only path, 8 per lane at once
+    // so its entries are read through the read-only path, 8 per lane at once;
+    // entries [first, nb)
     const int32_t* src = table + (int64_t)parent * bpb;
     int32_t* dst = table + (int64_t)child * bpb;
     constexpr int U = 8;
-    for (int32_t base = 0; base < nb; base += 32 * U) {
+    for (int32_t base = first; base < nb; base += 32 * U) {
         int32_t v[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
@@ -135,14 +137,20 @@ __global__ void k_fork_param(const __grid_constant__ ForkParams<CAP> a, int32_t*
 
 // Same for batches too large for kernel parameters: the four arrays
 // (child, parent, nb, add) are read from device memory.
+// blockIdx.y: a chunk of kForkChunk entries, so a large batch of long rows
+// keeps enough warps in flight (one warp per pair and chunk).
+constexpr int32_t kForkChunk = 256;
 __global__ void k_fork_global(const int32_t* __restrict__ args, int32_t n_pairs, int32_t* table,
                               int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
     pdl_wait();
     if (meta->status) return;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= n_pairs) return;
-    fork_pair(table, refcount, bpb, args[warp], args[n_pairs + warp], args[2 * n_pairs + warp],
-              args[3 * n_pairs + warp], threadIdx.x & 31, n_blocks, meta);
+    const int32_t first = (int32_t)blockIdx.y * kForkChunk;
+    const int32_t nb = min(args[2 * n_pairs + warp], first + kForkChunk);
+    if (first >= nb) return;
+    fork_pair(table, refcount, bpb, args[warp], args[n_pairs + warp], nb, args[3 * n_pairs + warp],
+              threadIdx.x & 31, n_blocks, meta, first);
 }
 
 // ------------------------------------------------------------ block scan
@@ -1273,7 +1281,9 @@ int dendrite_fork_batch(dendrite_pool* p, const int32_t* parents, const int32_t*
         DENDRITE_TRY(p->staging.upload(s, h, n * 16));
         const int threads = 128;
         const int blocks = (int)((n * 32 + threads - 1) / threads);
-        rc = launch_pdl(k_fork_global, dim3(blocks), dim3(threads), 0, s, (const int32_t*)d, (int32_t)n,
+        const int32_t max_nb = *std::max_element(nb.begin(), nb.end());
+        const unsigned chunks = (unsigned)std::max<int32_t>(1, (max_nb + kForkChunk - 1) / kForkChunk);
+        rc = launch_pdl(k_fork_global, dim3(blocks, chunks), dim3(threads), 0, s, (const int32_t*)d, (int32_t)n,
                         p->d_table, p->d_refcount, p->bpb, (int32_t)p->num_blocks, p->d_meta) == cudaSuccess
                  ? DENDRITE_OK : DENDRITE_ECUDA;
         DENDRITE_TRY(p->staging.release(s));
