@@ -279,7 +279,7 @@ struct dendrite_pool {
     dendrite::DevMeta* d_meta = nullptr;
     int32_t* d_holders = nullptr;    // [num_blocks] holders of a shared tail within one append
     int32_t* d_last = nullptr;       // [num_blocks] last holder index within one append
-    int32_t* d_released = nullptr;   // [num_blocks] flags set by free phase A
+    int32_t* d_released = nullptr;   // bitmap of the blocks a free released (word k: ids 32 k ..)
     int32_t* d_call_i32 = nullptr;   // [4 * max_branches] per-call scratch (offsets, cow sources)
 
     // layers: layer l's K pool starts at d_k + l * layer_bytes, its V pool at

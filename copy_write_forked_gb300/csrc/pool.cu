@@ -509,36 +509,23 @@ __device__ __forceinline__ void free_finish(int32_t* released, int32_t* stack, D
     __syncthreads();
     if (!is_last) return;
     if (!st && cnt > 0) {
-        // the flags of [lo, hi] in 32-flag groups aligned to 32, from the top
-        // group down: thread t of a pass takes one group (eight 16-byte
-        // loads), and a block scan of the groups' counts places its released
-        // ids, highest first.  Flags outside [lo, hi] are zero.
+        // the released bits of [lo, hi] (word g holds ids 32 g .. 32 g + 31),
+        // from the top word down: thread t of a pass takes one word, and a
+        // block scan of the words' counts places its released ids, highest
+        // first.  Bits outside [lo, hi] are zero.
+        uint32_t* bits = reinterpret_cast<uint32_t*>(released);
         int32_t carry = 0;
         const int32_t g_hi = hi >> 5, g_lo = lo >> 5;
         for (int32_t g0 = g_hi; g0 >= g_lo; g0 -= (int32_t)blockDim.x) {
             const int32_t g = g0 - (int32_t)threadIdx.x;
-            uint32_t mask = 0;   // bit k: flag of id 32 g + k
-            if (g >= g_lo) {
-                const int32_t b0 = g << 5;
-                if (b0 + 32 <= n_blocks) {
-                    const int4* f4 = reinterpret_cast<const int4*>(released + b0);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int4 f = __ldcg(f4 + q);
-                        mask |= ((uint32_t)(f.x != 0) | ((uint32_t)(f.y != 0) << 1) | ((uint32_t)(f.z != 0) << 2) |
-                                 ((uint32_t)(f.w != 0) << 3)) << (4 * q);
-                    }
-                } else {
-                    for (int k = 0; b0 + k < n_blocks && k < 32; ++k) mask |= (uint32_t)(__ldcg(released + b0 + k) != 0) << k;
-                }
-            }
+            const uint32_t mask = g >= g_lo ? __ldcg(bits + g) : 0u;   // bit k: id 32 g + k
             const int32_t ex = block_exclusive_scan<kFreeCollectThreads>(__popc(mask), warp_sums, &chunk_total);
             int32_t o = top0 + carry + ex;
             for (uint32_t m = mask; m; m &= ~(1u << (31 - __clz(m)))) {   // highest id first
                 const int32_t j = (g << 5) + (31 - __clz(m));
                 stack[o++] = j;
-                released[j] = 0;
             }
+            if (mask) bits[g] = 0;
             carry += chunk_total;
             __syncthreads();
         }
@@ -587,7 +574,7 @@ k_free(const __grid_constant__ A args, int32_t n, int32_t total, int32_t bpb, in
         } else {
             const int32_t old = atomicSub(refcount + blk, 1);
             if (old == 1) {
-                released[blk] = 1;
+                atomicOr(reinterpret_cast<uint32_t*>(released) + (blk >> 5), 1u << (blk & 31));
                 rel = true;
             } else if (old < 1) {
                 set_status(meta, DENDRITE_ECORRUPT);
@@ -649,7 +636,7 @@ k_free_tiles(const __grid_constant__ A args, int32_t n, int32_t total, int32_t b
             const int32_t c = __popc(grp);
             const int32_t old = atomicSub(refcount + b, c);
             if (old == c) {
-                released[b] = 1;
+                atomicOr(reinterpret_cast<uint32_t*>(released) + (b >> 5), 1u << (b & 31));
                 rel = true;
             } else if (old < c) {
                 set_status(meta, DENDRITE_ECORRUPT);
