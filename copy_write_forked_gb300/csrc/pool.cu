@@ -627,22 +627,27 @@ k_free_tiles(const __grid_constant__ A args, int32_t n, int32_t total, int32_t b
         tile[w][lane + 32 * k] = blk[k];
     }
     __syncthreads();
+    // all PER reference drops are issued before any result is looked at
+    int32_t bb[PER], cc[PER], old[PER];
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-        const int32_t b = tile[lane][w + 32 * k];
-        const unsigned grp = __match_any_sync(0xffffffffu, b);
+        bb[k] = tile[lane][w + 32 * k];
+        const unsigned grp = __match_any_sync(0xffffffffu, bb[k]);
+        cc[k] = (bb[k] >= 0 && lane == __ffs(grp) - 1) ? __popc(grp) : 0;
+        old[k] = cc[k] ? atomicSub(refcount + bb[k], cc[k]) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
         bool rel = false;
-        if (b >= 0 && lane == __ffs(grp) - 1) {
-            const int32_t c = __popc(grp);
-            const int32_t old = atomicSub(refcount + b, c);
-            if (old == c) {
-                atomicOr(reinterpret_cast<uint32_t*>(released) + (b >> 5), 1u << (b & 31));
+        if (cc[k]) {
+            if (old[k] == cc[k]) {
+                atomicOr(reinterpret_cast<uint32_t*>(released) + (bb[k] >> 5), 1u << (bb[k] & 31));
                 rel = true;
-            } else if (old < c) {
+            } else if (old[k] < cc[k]) {
                 set_status(meta, DENDRITE_ECORRUPT);
             }
         }
-        free_fold(rel, b, meta);
+        free_fold(rel, bb[k], meta);
     }
     free_finish(released, stack, meta, n_blocks);
 }
