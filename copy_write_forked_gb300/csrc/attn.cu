@@ -2064,9 +2064,11 @@ int launch_attention(dendrite_pool* p, int32_t layer, const AttnArgs& a, cudaStr
     // Both partial classes: the tcgen05 and the mma.sync kernel write
     // disjoint partial rows and read only the plan and the pool, so the
     // mma.sync kernel runs on the pool's side stream (lowest priority) beside
-    // the tcgen05 one: its CTAs take the SMs that the tcgen05 kernel's first
-    // CTAs to finish leave, and the caller's stream waits for it before the
-    // merge.
+    // the tcgen05 one, and the caller's stream waits for it before the merge.
+    // Their CTAs never share an SM: with an SM split in the plan each
+    // kernel's CTAs fit on their own SMs at once and the two run side by
+    // side; without one the mma.sync CTAs take the SMs the tcgen05 CTAs
+    // leave as they finish.
     const bool beside = bf16 && a.plan.n_tc_ctas > 0 && a.plan.n_ctas > 0 && p->side;
     if (beside) DENDRITE_CUDA(cudaEventRecord(p->ev_fork, s));
     // the tcgen05 kernel is submitted first, so that its CTAs are placed
