@@ -124,6 +124,9 @@ __device__ __forceinline__ void fork_pair(int32_t* __restrict__ table, int32_t* 
     }
 }
 
+// One warp per (pair, kForkChunk entries of its row): a fork of a long row
+// takes as long as one of a short row.
+constexpr int32_t kForkChunk = 256;
 template <int CAP>
 __global__ void k_fork_param(const __grid_constant__ ForkParams<CAP> a, int32_t* table,
                              int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
@@ -131,15 +134,17 @@ __global__ void k_fork_param(const __grid_constant__ ForkParams<CAP> a, int32_t*
     if (meta->status) return;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp >= a.n_pairs) return;
-    fork_pair(table, refcount, bpb, a.child[warp], a.parent[warp], a.nb[warp], a.add[warp],
-              threadIdx.x & 31, n_blocks, meta);
+    const int32_t first = (int32_t)blockIdx.y * kForkChunk;
+    const int32_t nb = min(a.nb[warp], first + kForkChunk);
+    if (first >= nb) return;
+    fork_pair(table, refcount, bpb, a.child[warp], a.parent[warp], nb, a.add[warp], threadIdx.x & 31, n_blocks, meta,
+              first);
 }
 
 // Same for batches too large for kernel parameters: the four arrays
 // (child, parent, nb, add) are read from device memory.
 // blockIdx.y: a chunk of kForkChunk entries, so a large batch of long rows
 // keeps enough warps in flight (one warp per pair and chunk).
-constexpr int32_t kForkChunk = 256;
 __global__ void k_fork_global(const int32_t* __restrict__ args, int32_t n_pairs, int32_t* table,
                               int32_t* refcount, int32_t bpb, int32_t n_blocks, DevMeta* meta) {
     pdl_wait();
@@ -911,8 +916,10 @@ int launch_fork_param(dendrite_pool* p, const std::vector<int32_t>& child, const
     }
     const int threads = 128;
     const int blocks = (int)((child.size() * 32 + threads - 1) / threads);
-    DENDRITE_CUDA(launch_pdl(k_fork_param<CAP>, dim3(blocks), dim3(threads), 0, s, a, p->d_table, p->d_refcount,
-                             p->bpb, (int32_t)p->num_blocks, p->d_meta));
+    const int32_t max_nb = child.empty() ? 0 : *std::max_element(nb.begin(), nb.end());
+    const unsigned chunks = (unsigned)std::max<int32_t>(1, (max_nb + kForkChunk - 1) / kForkChunk);
+    DENDRITE_CUDA(launch_pdl(k_fork_param<CAP>, dim3(blocks, chunks), dim3(threads), 0, s, a, p->d_table,
+                             p->d_refcount, p->bpb, (int32_t)p->num_blocks, p->d_meta));
     return DENDRITE_OK;
 }
 
