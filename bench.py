@@ -332,6 +332,19 @@ def run_ours(args):
             pool.free(br)
         return br
 
+    def rewind(s_to):
+        # Untimed: roll every branch back to its length after decode step
+        # s_to (truncate).  Each decode step adds one token to every branch,
+        # so the passes after the timed one (per-kernel events, end to end)
+        # would otherwise read a larger tree per step than the timed steps
+        # did; rewound, they repeat the timed steps' tree sizes.
+        if kind != "decode" or state["s"] == s_to:
+            return
+        if pool.branch_len(state["leaves"][0]) != P + Dv + state["s"]:
+            raise RuntimeError("unexpected branch length")
+        pool.truncate(state["leaves"], [P + Dv + s_to] * len(state["leaves"]))
+        state["s"] = s_to
+
     def unique_tokens():
         # tokens the next step's queries see, each shared one once
         extra = state["s"] + 1 if kind == "decode" else 0
@@ -349,6 +362,7 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
+    s_timed0 = state["s"]
     # ---- timed region: K steps enqueued back to back, one event pair per step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     tok_timed = []
@@ -390,6 +404,7 @@ def run_ours(args):
         return orig_attn(*a, **k)
 
     pool.tree_attn_decode = attn_after_flush
+    rewind(s_timed0)
     for i in range(n_prof):
         flush_l2()
         tok_prof.append(unique_tokens())
@@ -403,6 +418,7 @@ def run_ours(args):
     # call's kernels then overlap one another as they do unprofiled
     pool.set_profiling(2)
     call_light, tok_light = [], []
+    rewind(s_timed0)
     for i in range(n_prof):
         flush_l2()
         tok_light.append(unique_tokens())
@@ -517,10 +533,14 @@ def run_ours(args):
             br = e2e_step(i % 2, check=check if i == n - 1 else None)
         return br
 
+    # the e2e warm-up steps end where the timed steps began (a branch keeps
+    # at least one divergent token)
+    rewind(max(s_timed0 - 2 * args.warmup, 1 - Dv))
     for _ in range(args.warmup):
         flush_l2()
         e2e_run(2)
     torch.cuda.synchronize()
+    tok_e2e = [unique_tokens() + (nl * i if kind == "decode" else 0) for i in range(e2e_steps)]
     flush_l2()
     torch.cuda.synchronize()
     e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -590,6 +610,7 @@ def run_ours(args):
         "roofline_attention": attn_roof,
         "cpu_baseline": cpu,
         "e2e": {"value": world * nl / (e2e / 1e3), "unit": "branch-queries/s", "ms_per_step": e2e,
+                "unique_kv_bytes_mean": statistics.mean(tok_e2e) * kv_tok,
                 "steps": e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": per_step * args.steps,
         "clocks": clocks,
