@@ -2572,9 +2572,14 @@ extern "C" int dendrite_tree_attn_decode_noalloc(dendrite_pool* p, const void* Q
         if (seen[branches[i]]) return DENDRITE_EINVAL;
         seen[branches[i]] = 1;
     }
+    cudaStream_t s = (cudaStream_t)stream;
+    // a captured copy from the pageable host buffer would read it only when
+    // the graph is replayed, after later calls have rewritten it
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capturing) != cudaSuccess || capturing != cudaStreamCaptureStatusNone)
+        return DENDRITE_EINVAL;
     unsigned char* scratch = nullptr;
     DENDRITE_TRY(noalloc_scratch(p->device, &scratch));
-    cudaStream_t s = (cudaStream_t)stream;
     static thread_local HostPlan hp;
     hp.clear();
     DENDRITE_TRY(build_plan(p, branches, n, q_len, n_q_heads, p->sm_count * p->attn_ctas_per_sm, tc_ctas(p), hp,

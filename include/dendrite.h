@@ -510,6 +510,9 @@ int dendrite_plan_segments_packed(int32_t n_nodes, const int32_t* parent, const 
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) once for that device; make that first call before
  *     any stream capture.
+ *   - The call cannot be captured into a CUDA graph (a captured copy from
+ *     the pageable buffer would read it only when the graph runs): while
+ *     `stream` is capturing it returns DENDRITE_EINVAL and enqueues nothing.
  *   - A call whose plan plus partial rows exceed the array returns
  *     DENDRITE_ELIMIT and launches nothing (roughly: more than ~30,000 partial
  *     rows of head_dim 128).

@@ -136,3 +136,32 @@ def test_noalloc_calls_allocate_no_device_memory():
         assert (o.float() - ref.float()).abs().max().item() <= TOL
     pool.sync()
     pool.close()
+
+
+def test_noalloc_refuses_stream_capture():
+    """Under an active stream capture the allocation-free call returns
+    DENDRITE_EINVAL and enqueues nothing (its plan copy from a pageable host
+    buffer cannot be replayed); after the capture it runs as before."""
+    w = W.beam(requests=2, prefix=200, width=3, divergent=21)
+    pool = pool_for(w)
+    h = run_script(pool, w)
+    br = [h[b] for b in w.query]
+    Q = w.q("cuda")
+    out = torch.full_like(Q, float("nan"))
+    assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, out) == 0   # first call: address lookup
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        g.capture_begin()
+        try:
+            rc = _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, out)
+        finally:
+            g.capture_end()
+    assert rc == -1
+    again = torch.full_like(Q, float("nan"))
+    assert _call(lib().dendrite_tree_attn_decode_noalloc, pool, Q, br, again) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(again, out)
+    pool.sync()
+    pool.close()
