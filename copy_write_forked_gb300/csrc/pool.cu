@@ -45,7 +45,12 @@ __device__ __forceinline__ void pdl_wait() {
 }
 
 // Per-call argument arrays: small ones travel as kernel parameters (no copy
-// on the stream), large ones are staged in device memory.
+// on the stream), large ones are staged in device memory.  Kernel parameters
+// may fill up to 32,764 bytes; the largest tier keeps the argument words at
+// 16 KiB (a fork batch of 1,024 pairs, the tiled free of 1,024 branches),
+// for kernels whose lanes read the same argument word (a lane reading its
+// own word of kernel parameters is served one lane at a time).
+constexpr int kParamCapLarge = 4096;
 template <int CAP>
 struct ParamArgs {
     int32_t v[CAP];
@@ -1024,6 +1029,9 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
         return DENDRITE_OK;
     };
     // compressed pools encode from device-resident arguments
+    // (k_append_meta reads the arguments of a different branch in every
+    // lane: from kernel parameters such reads are serialised, so larger
+    // calls keep them in device memory)
     if (3 * n <= CAP && !(copy && p->dtype == DENDRITE_TURBO)) {
         ParamArgs<CAP> a;
         fill(a.v);
@@ -1269,6 +1277,7 @@ int dendrite_fork_batch(dendrite_pool* p, const int32_t* parents, const int32_t*
     if (n <= 4) rc = launch_fork_param<4>(p, child, par, nb, add, s);
     else if (n <= 32) rc = launch_fork_param<32>(p, child, par, nb, add, s);
     else if (n <= 256) rc = launch_fork_param<256>(p, child, par, nb, add, s);
+    else if (n <= kParamCapLarge / 4) rc = launch_fork_param<kParamCapLarge / 4>(p, child, par, nb, add, s);
     else {
         char *h, *d;
         DENDRITE_TRY(p->staging.reserve(n * 16, &h, &d));
@@ -1401,6 +1410,11 @@ int release_entries(dendrite_pool* p, const int32_t* branches, const int32_t* st
     constexpr int CAP = 1536;
     if (3 * n <= CAP) {
         ParamArgs<CAP> a;
+        fill(a.v);
+        return launch(a);
+    }
+    if (tiles && 3 * n <= kParamCapLarge) {   // the tiled kernel reads one branch's arguments per warp
+        ParamArgs<kParamCapLarge> a;
         fill(a.v);
         return launch(a);
     }

@@ -135,13 +135,18 @@ def test_three_holders_of_one_tail_follow_argument_order():
     pool.close()
 
 
-def test_large_fork_batch_uses_device_argument_path():
+@pytest.mark.parametrize("sizes,every", [((200, 150, 10), 3), ((800, 590, 10), 1)])
+def test_large_fork_batches_match_oracle(sizes, every):
+    """One fork call of 360 pairs (its arguments in kernel parameters) or of
+    1,400 pairs (staged in device memory), then an append to every third
+    child or to all 1,400: tables and refcounts match O2."""
+    n = sum(sizes)
+    bounds = [2, 2 + sizes[0], 2 + sizes[0] + sizes[1], 2 + n]
     w = W.Workload("wide", 1, 1, 128, 16, torch.bfloat16,
                    [W.Op("new", (0,)), W.Op("new", (1,)), W.Op("append", (0, 1), 77),
-                    W.Op("fork", (0, 1, 0), children=(tuple(range(2, 202)), tuple(range(202, 352)),
-                                                      tuple(range(352, 362)))),
-                    W.Op("append", tuple(range(2, 362, 3)), 9)], tuple(range(2, 362)))
-    pool = pool_for(w, max_branches=400)
+                    W.Op("fork", (0, 1, 0), children=tuple(tuple(range(bounds[k], bounds[k + 1])) for k in range(3))),
+                    W.Op("append", tuple(range(2, 2 + n, every)), 9)], tuple(range(2, 2 + n)))
+    pool = pool_for(w, max_branches=n + 40)
     h = run_script(pool, w)
     ref = run_script_pool(w, pool.num_blocks, kv_source=_gpu_kv(w))
     pool.sync()
@@ -149,21 +154,24 @@ def test_large_fork_batch_uses_device_argument_path():
     pool.close()
 
 
-def test_batched_forks_and_frees_of_siblings_match_oracle():
+@pytest.mark.parametrize("n_leaves", [300, 600, 1400])
+def test_batched_forks_and_frees_of_siblings_match_oracle(n_leaves):
     """The shape of a decode step over many leaves that share two prompts'
-    prefixes: every step forks each of 300 leaves once (one call of 300
-    pairs), appends one token to every child (a copy of each leaf's partial
-    tail) and frees the 300 old leaves in one call; finally everything is
-    freed in one call.  Calls of this size take the device-argument fork
-    kernel and the tiled free kernel, whose lanes drop the references of a
-    block shared within a tile with one atomic; tables, refcounts, the free
-    stack and every valid slot match O2 after each step, and the last free
-    returns every block to the stack."""
+    prefixes: every step forks each leaf once (one call of n_leaves pairs),
+    appends one token to every child (a copy of each leaf's partial tail) and
+    frees the old leaves in one call; finally everything is freed in one
+    call.  Calls of this size take the tiled free kernel, whose lanes drop
+    the references of a block shared within a tile with one atomic; their
+    arguments travel as kernel parameters (300, 600 leaves) or are staged in
+    device memory (1,400).  Tables, refcounts, the free stack and every valid
+    slot match O2 after each step, and the last free returns every block to
+    the stack."""
+    half = n_leaves // 2
     ops = [W.Op("new", (0,)), W.Op("new", (1,)), W.Op("append", (0, 1), 100),
-           W.Op("fork", (0, 1), children=(tuple(range(2, 152)), tuple(range(152, 302)))),
-           W.Op("append", tuple(range(2, 302)), 5)]
-    leaves = list(range(2, 302))
-    nxt = 302
+           W.Op("fork", (0, 1), children=(tuple(range(2, 2 + half)), tuple(range(2 + half, 2 + n_leaves)))),
+           W.Op("append", tuple(range(2, 2 + n_leaves)), 5)]
+    leaves = list(range(2, 2 + n_leaves))
+    nxt = 2 + n_leaves
     checkpoints = []
     for step in range(3):
         kids = tuple(range(nxt, nxt + len(leaves)))
