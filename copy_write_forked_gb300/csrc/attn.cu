@@ -1507,10 +1507,13 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 // Partition weights, fitted to per-CTA timelines on GB300.  mma.sync class: a
 // tile of a unit with rt row tiles of 16 costs about (1 + rt) units (HBM time
 // plus mma time: 0.25 us for rt = 1 vs 0.61 us for rt = 4 per CTA), and every
-// chunk boundary (partial store, combine, next unit's Q) about as much as 8
-// one-row-tile tiles plus a quarter tile per row (its query load, combine
-// and partial store grow with the rows: MCTS, whose units hold 4 to 64 rows,
-// 292 -> 283 us with the row term).  tcgen05 class (one CTA per SM): a tile
+// chunk boundary (partial store, combine, next unit's Q) about as much as 5
+// one-row-tile tiles plus an eighth of a tile per row (its query load,
+// combine and partial store grow with the rows).  Per-CTA end times of the
+// beam call put a 4-row unit's start at about 1.8 us against 0.32 us per
+// tile; on the packed MCTS plan these weights take the call from 237 to
+// 215 us against (8, 4 rows per tile) before, with beam, spec-verify and
+// stress unchanged.  tcgen05 class (one CTA per SM): a tile
 // costs about (1 + rt) with rt row tiles of 128; a chunk boundary drains the
 // MMA pipeline and stores up to 256 partial rows of 520 bytes.
 struct ClassWeights {
@@ -1518,7 +1521,7 @@ struct ClassWeights {
     int32_t row_shift;         // a unit start also weighs n_rows >> row_shift (-1: no row term)
     int64_t min_per_cta;       // smallest total weight worth a CTA of its own
 };
-constexpr ClassWeights kSmallWeights{16, 1, 8};
+constexpr ClassWeights kSmallWeights{10, 2, 8};
 constexpr ClassWeights kTcWeights{24, -1, 32};
 inline int64_t tile_weight(int rt) { return 1 + rt; }
 inline int64_t start_weight(const ClassWeights& cw, int32_t n_rows) {
