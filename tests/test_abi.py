@@ -17,7 +17,7 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(dendrite_[a-z_]+)\s*\(", src)))
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_pool_fork_append_attend_free_calls():
     names = declared_functions()
     for n in ("dendrite_pool_create", "dendrite_fork", "dendrite_append_kv",
               "dendrite_tree_attn_decode", "dendrite_free"):
