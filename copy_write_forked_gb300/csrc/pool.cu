@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(128, 16) k_append_copy(const __grid_constant__
                               int64_t in_layer, int64_t pool_layer, const DevMeta* meta, int64_t n_tiles,
                               int32_t uniform) {
     pdl_wait();
-    // a grid of at most 16 CTAs per SM strides over the tiles
+    // one tile per CTA up to 64 CTAs per SM (the scheduler starts the next
+    // tile's CTA as one finishes), beyond that the grid strides over the tiles
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     const uint4* __restrict__ Kin = Kin0 + blockIdx.y * in_layer;
     const uint4* __restrict__ Vin = Vin0 + blockIdx.y * in_layer;
@@ -961,7 +962,7 @@ int append_launch(dendrite_pool* p, const int32_t* branches, const int32_t* lens
     constexpr int CAP = 768;
     const int32_t row_vec = p->head_dim * p->elt / 16;
     const int64_t n_tiles = touched * p->n_kv;
-    const unsigned grid = (unsigned)std::min<int64_t>(n_tiles, (int64_t)p->sm_count * 16);
+    const unsigned grid = (unsigned)std::min<int64_t>(n_tiles, (int64_t)p->sm_count * 64);
     const int64_t pool_layer = (int64_t)(p->layer_bytes / 16);
     // blocks each branch touches, when the same for all (else 0)
     int32_t uniform = -1;
